@@ -1,0 +1,196 @@
+"""Pins for the oracle's NVFP4 / INT4 encoders and pool layout.
+
+Checked against the byte counts the pages print (tests/golden), exact round
+trips of representable values, brute-force nearest-value search, Python's
+own round-half-even, and the block locality the pages describe.
+"""
+import os
+
+import numpy as np
+import pytest
+
+from oracle import formats as F
+from oracle import pool as P
+from oracle import quant as Q
+from workloads import f32_to_bf16_bits, global_scale_from_amax
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "page_numbers.txt")
+
+
+def golden():
+    out = {}
+    for line in open(GOLDEN):
+        if line.strip() and not line.startswith("#"):
+            key, val = line.split()[:2]
+            out[key] = float(val)
+    return out
+
+
+def test_byte_accounting_matches_the_pages():
+    g = golden()
+    D, Pg = int(g["qwen27b_head_dim"]), 64
+    spec = P.PoolSpec("nvfp4", 1, Pg, 1, D)
+    bytes_per_value = spec.chunk_bytes / (Pg * 2 * D)
+    assert bytes_per_value == g["nvfp4_fraction_of_fp8"]            # FP8 stores 1 byte/value
+    assert round(1 / bytes_per_value, 4) == g["nvfp4_capacity_ratio"]
+    # block size from (4 + 8/B)/8 = 0.5625
+    assert (8 * g["nvfp4_fraction_of_fp8"] - 4) ** -1 * 8 == g["nvfp4_block_size"] == Q.NVFP4_BLOCK
+    layers, heads = int(g["qwen27b_full_attn_layers"]), int(g["qwen27b_kv_heads"])
+    elems = layers * heads * D * 2
+    assert elems == g["qwen27b_elems_per_token"] == g["qwen27b_fp8_bytes_per_token"]
+    per_token = layers * P.PoolSpec("nvfp4", 1, Pg, heads, D).pool_bytes // Pg
+    assert per_token == g["qwen27b_nvfp4_bytes_per_token"]
+    # INT4 per token and head, and the two page sizes
+    i4 = P.PoolSpec("int4", 1, 800, 1, 256)
+    assert i4.chunk_bytes / 800 == g["int4_bytes_per_head_token"]
+    assert i4.chunk_bytes == g["int4_page_bytes_800"]
+    assert P.PoolSpec("int4", 1, 1600, 1, 256).chunk_bytes == g["int4_page_bytes_1600"]
+    # the Mamba state does not fit an 800-token page but fits a 1600-token one
+    assert g["int4_page_bytes_800"] < g["mamba_state_bytes"] <= g["int4_page_bytes_1600"]
+
+
+def test_regions_are_16_byte_aligned():
+    for fmt in ("nvfp4", "int4"):
+        for D in (64, 128, 256):
+            for Pg in (16, 64, 256, 1600):
+                s = P.PoolSpec(fmt, 2, Pg, 3, D)
+                for r in ("kc", "vc", "ks", "vs"):
+                    assert s.region(r) % 16 == 0
+                assert s.chunk_bytes % 16 == 0
+
+
+def _representable_block(rng, S_code, g, with_max=True):
+    codes = rng.integers(0, 16, 16)
+    if with_max:
+        codes[rng.integers(16)] = 7 | (rng.integers(2) << 3)
+    vals = F.e2m1_decode(codes) * F.e4m3_decode(S_code) * float(g)
+    return vals, codes
+
+
+def test_nvfp4_exact_round_trip_of_representable_values():
+    rng = np.random.default_rng(0)
+    for _ in range(400):
+        g = np.float32(2.0 ** rng.integers(-8, 4))
+        S = int(rng.integers(8, 0x7F))               # normal E4M3 scales
+        vals, codes = _representable_block(rng, S, g)
+        x = f32_to_bf16_bits(vals.astype(np.float32))
+        assert np.array_equal(F.bf16_to_f32(x).astype(np.float64), vals)   # exact in bf16
+        c, s = Q.nvfp4_quantize(x[None], g)
+        assert s[0, 0] == S
+        # every code comes back, including the sign of zero (0x8 stays 0x8)
+        assert np.array_equal(Q._unpack_nibbles(c)[0], codes.astype(np.uint8))
+        assert np.array_equal(Q.nvfp4_dequantize(c, s, g)[0], vals)
+
+
+def test_nvfp4_codes_are_nearest_values_bruteforce():
+    rng = np.random.default_rng(1)
+    x = f32_to_bf16_bits(rng.standard_normal((64, 256)).astype(np.float32) * 3)
+    g = np.float32(0.01)
+    c, s = Q.nvfp4_quantize(x, g)
+    xf = F.bf16_to_f32(x).astype(np.float64).reshape(64, 16, 16)
+    grid2 = F.e2m1_decode(np.arange(8))
+    grid4 = F.e4m3_decode(np.arange(0x7F))
+    n = Q._unpack_nibbles(c).reshape(64, 16, 16)
+    for r in range(64):
+        for b in range(16):
+            amax = np.abs(xf[r, b]).max()
+            sf = float(np.float32(np.float32(amax) / (np.float32(6.0) * g)))
+            chosen = F.e4m3_decode(s[r, b])
+            assert abs(chosen - sf) <= np.abs(grid4 - sf).min()
+            denom = float(np.float32(np.float32(chosen) * g))
+            for i in range(16):
+                t = float(np.float32(np.float32(xf[r, b, i]) / np.float32(denom)))
+                v = abs(F.e2m1_decode(n[r, b, i]))
+                assert abs(v - abs(t)) <= np.abs(grid2 - abs(t)).min()
+                assert (n[r, b, i] >> 3) == (1 if np.signbit(np.float32(xf[r, b, i])) else 0)
+
+
+def test_nvfp4_layer_amax_block_uses_full_scale():
+    """With g = amax / (6 * 448) the block holding the layer maximum gets
+    the largest E4M3 scale and its maximum element the code for 6."""
+    rng = np.random.default_rng(2)
+    x = f32_to_bf16_bits(rng.standard_normal((8, 64)).astype(np.float32))
+    xf = F.bf16_to_f32(x)
+    g = global_scale_from_amax(np.abs(xf).max())
+    c, s = Q.nvfp4_quantize(x, g)
+    r, i = np.unravel_index(np.argmax(np.abs(xf)), xf.shape)
+    assert s[r, i // 16] == 0x7E
+    assert Q._unpack_nibbles(c)[r, i] & 7 == 7
+
+
+def test_nvfp4_zero_block_and_tiny_block():
+    x = np.zeros((1, 32), np.uint16)
+    x[0, 16:] = f32_to_bf16_bits(np.full(16, -1e-30, np.float32))   # rounds to S == 0
+    c, s = Q.nvfp4_quantize(x, np.float32(1.0))
+    assert s.tolist() == [[0, 0]] and np.all(c == 0)
+
+
+def test_nvfp4_block_locality():
+    """A per-16 scale confines an outlier to its own block ("SGLang's 4-bit
+    KV cache", section "Against what this site already established")."""
+    rng = np.random.default_rng(3)
+    xf = rng.standard_normal((4, 256)).astype(np.float32)
+    g = np.float32(0.005)
+    c0, s0 = Q.nvfp4_quantize(f32_to_bf16_bits(xf), g)
+    xf2 = xf.copy()
+    xf2[1, 37] *= 10.0
+    c1, s1 = Q.nvfp4_quantize(f32_to_bf16_bits(xf2), g)
+    blk = 37 // 16
+    diff_s = np.argwhere(s0 != s1)
+    assert all((r, b) == (1, blk) for r, b in diff_s)
+    n0, n1 = Q._unpack_nibbles(c0), Q._unpack_nibbles(c1)
+    diff_c = np.argwhere(n0 != n1)
+    assert len(diff_c) > 0 and all(r == 1 and i // 16 == blk for r, i in diff_c)
+
+
+def test_int4_round_trip_and_ties():
+    rng = np.random.default_rng(4)
+    for _ in range(200):
+        s = 2.0 ** int(rng.integers(-6, 4))
+        codes = rng.integers(-7, 8, 256)
+        codes[rng.integers(256)] = 7 * (1 if rng.integers(2) else -1)
+        x = f32_to_bf16_bits((codes * s).astype(np.float32))
+        c, sc = Q.int4_quantize(x[None])
+        assert sc[0] == np.float32(s)
+        assert np.array_equal(Q.int4_dequantize(c, sc)[0], codes * s)
+    # ties go to even, as Python's round() does
+    s = 1.0
+    vals = np.array([7.0, 0.5, 1.5, 2.5, -0.5, -1.5, -2.5, 3.49, -6.5, 4.5], np.float32)
+    c, sc = Q.int4_quantize(f32_to_bf16_bits(vals)[None])
+    got = Q.int4_dequantize(c, sc)[0] / sc[0]
+    assert got.tolist() == [float(round(float(v))) for v in vals]
+    z, sz = Q.int4_quantize(np.zeros((1, 256), np.uint16))
+    assert sz[0] == 0 and np.all(z == 0)
+
+
+def test_pool_write_places_rows_by_slot():
+    rng = np.random.default_rng(5)
+    for fmt in ("nvfp4", "int4"):
+        spec = P.PoolSpec(fmt, 5, 16, 2, 64)
+        T = 20
+        k = f32_to_bf16_bits(rng.standard_normal((T, 2, 64)).astype(np.float32))
+        v = f32_to_bf16_bits(rng.standard_normal((T, 2, 64)).astype(np.float32))
+        slots = rng.permutation(5 * 16)[:T].astype(np.int64)
+        slots[3] = -1
+        pool = P.new_pool(spec, fill=0xAB)
+        P.write(pool, spec, k, v, slots, np.array([0.01, 0.02], np.float32))
+        written = np.zeros(spec.pool_bytes, bool)
+        for t in range(T):
+            if slots[t] < 0:
+                continue
+            page, off = divmod(int(slots[t]), 16)
+            for h in range(2):
+                for kind, x, gg in (("k", k, 0.01), ("v", v, 0.02)):
+                    idx_c = P._row_index(spec, np.array([page]), np.array([off]), h, kind + "c")[0]
+                    idx_s = P._row_index(spec, np.array([page]), np.array([off]), h, kind + "s")[0]
+                    if fmt == "nvfp4":
+                        cc, ss = Q.nvfp4_quantize(x[t, h][None], np.float32(gg))
+                        ss = ss[0]
+                    else:
+                        cc, sc = Q.int4_quantize(x[t, h][None])
+                        ss = sc.astype(np.float32).view(np.uint8)
+                    assert np.array_equal(pool[idx_c], cc[0])
+                    assert np.array_equal(pool[idx_s], ss)
+                    written[idx_c] = True
+                    written[idx_s] = True
+        assert np.all(pool[~written] == 0xAB)       # nothing else touched
