@@ -1,0 +1,564 @@
+#!/usr/bin/env python
+"""Decode-step benchmark of the 4-bit paged KV cache on GB300.
+
+One step is the whole decode hot path for one batch: kv4_write of each
+request's new token into the NVFP4 pool, then kv4_decode_attention (split-KV
+kernel + log-sum-exp combine) over every request's full context.  The
+headline workload is a Qwen3.8-27B-shaped full-attention layer at 32K
+context (4 KV heads, 24 query heads, head dim 256, batch 16, lengths uniform
+in [24576, 32768], 64-token pages); the pool (about 0.53 GB) is far larger
+than L2, so every step streams it from HBM.
+
+Printed: one JSON line on rank 0 with the metric (achieved HBM GB/s of the
+step's algorithmic bytes), the roofline of the decode kernel, an end-to-end
+figure through the public API with host buffers, the oracle timed on the
+host cores, clock samples, and per-workload lines for 160K, 1M, the INT4
+lane and the prefix dequant under "workloads".
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kv4|reference]
+Multi-GPU runs (torchrun) are independent replicas (weak scaling): each rank
+decodes its own batch; only the timing is reduced (max over ranks).
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "NVFP4 decode-attn achieved HBM GB/s (% of peak) at 32K/160K/1M ctx"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ----------------------------------------------------------------------------- helpers
+def algorithmic_decode_bytes(w, lens, fmt=None):
+    """Bytes a decode call must move: every cached token's K and V codes and
+    scales for every kv head, plus q in and out (fp32) out."""
+    fmt = fmt or w.fmt
+    D = w.head_dim
+    per_token_head = 2 * (D // 2 + (D // 16 if fmt == "nvfp4" else 4))
+    kv = int(np.sum(lens, dtype=np.int64)) * w.num_kv_heads * per_token_head
+    return kv + len(lens) * w.num_q_heads * D * (2 + 4)
+
+
+def algorithmic_write_bytes(w, T):
+    D = w.head_dim
+    per_row = 2 * (D // 2 + (D // 16 if w.fmt == "nvfp4" else 4))
+    return T * w.num_kv_heads * (2 * D * 2 + per_row) + T * 8
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_source_hash():
+    h = hashlib.sha256()
+    for f in ("kv4_decode.cu", "kv4_device.cuh"):
+        with open(os.path.join(ROOT, "bit_paged_kv_kv4_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """ncu DRAM bytes per decode launch recorded in profiles/, if it was taken
+    on the current decode source; else None."""
+    p = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d.get(workload)
+        if e and e.get("source_hash") == decode_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"kv4_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            for line in open(self.path):
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        except OSError:
+            return None
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- device setup
+class Setup:
+    """A workload's pool filled through kv4_write, plus one decode step's inputs.
+    keep_kv=True keeps every request's bf16 K/V on the device (for tests)."""
+
+    def __init__(self, w, device, seed_offset=0, num_splits=None, keep_kv=False, fill=None):
+        import torch
+        import bit_paged_kv_kv4_gb300 as K
+        self.w, self.K, self.torch = w, K, torch
+        self.device = device
+        self.lens = w.seq_lens()
+        self.num_pages, self.table = w.block_table(self.lens)
+        B, Hkv, Hq, D, P = w.batch, w.num_kv_heads, w.num_q_heads, w.head_dim, w.page_size
+        self.pool = K.Pool(w.fmt, self.num_pages, P, Hkv, D, device=device)
+        if fill is not None:
+            self.pool.buffer.fill_(fill)
+        kvs = []
+        amax = torch.zeros(2, device=device)
+        for b in range(B):
+            kv = W.device_kv(w, b, int(self.lens[b]), device)
+            amax = torch.maximum(amax, kv.abs().amax(dim=(1, 2, 3)).float())
+            kvs.append(kv)
+        am = amax.cpu().numpy()
+        self.g_host = np.array([W.global_scale_from_amax(am[0]), W.global_scale_from_amax(am[1])],
+                               np.float32)
+        self.g = torch.from_numpy(self.g_host).to(device)
+        for b in range(B):
+            L = int(self.lens[b])
+            slots = torch.from_numpy(W.slots_for(self.table[b], P, np.arange(L))).to(device)
+            K.kv4_write(kvs[b][0], kvs[b][1], slots, self.pool, self.g)
+        self.kv = kvs if keep_kv else None
+        del kvs
+        # the step's inputs: q, and each request's newest token (position L-1)
+        self.q, self.k_new, self.v_new = W.device_q(w, device, salt=seed_offset)
+        self.slot_new = torch.from_numpy(np.array(
+            [W.slots_for(self.table[b], P, [int(self.lens[b]) - 1])[0] for b in range(B)],
+            np.int64)).to(device)
+        self.d_table = torch.from_numpy(self.table).to(device)
+        self.d_lens = torch.from_numpy(self.lens).to(device)
+        self.splits = num_splits if num_splits is not None else (
+            w.num_splits or K.kv4_decode_default_splits(B, Hkv, self.table.shape[1], P))
+        self.ws = K.alloc_workspace(B, Hq, D, self.splits, device=device)
+        self.out = torch.empty((B, Hq, D), dtype=torch.float32, device=device)
+        self.sm = float(w.sm_scale())
+        torch.cuda.synchronize()
+        assert K.kv4_device_error() == 0
+
+    def write(self):
+        self.K.kv4_write(self.k_new, self.v_new, self.slot_new, self.pool, self.g)
+
+    def decode(self):
+        self.K.kv4_decode_attention(self.q, self.pool, self.g, self.d_table, self.d_lens, self.sm,
+                                    self.out, num_splits=self.splits, workspace=self.ws)
+
+    def launches_per_step(self):
+        return 1 + 1 + (1 if self.splits > 1 else 0)
+
+
+def time_decode_only(s, iters):
+    torch = s.torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    for _ in range(3):
+        s.decode()
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record()
+        s.decode()
+        b.record()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) * 1e-3 for a, b in ev]
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def cpu_oracle_sample(name, seconds, max_steps=None):
+    """Time the oracle's FP64 decode attention on one request and kv head of
+    the workload (its whole context), repeated for about `seconds`.
+    Returns dict(value GB/s, steps, seconds_per_step, tokens)."""
+    import oracle
+    from oracle import pool as OP
+    w = W.ALL[name]
+    lens = w.seq_lens()
+    b, h = 0, 0
+    L = int(lens[b])
+    k, v = w.kv_request(b, h, L)
+    g = np.array([W.global_scale_from_amax(np.abs(W.bf16_bits_to_f32(k)).max()),
+                  W.global_scale_from_amax(np.abs(W.bf16_bits_to_f32(v)).max())], np.float32)
+    P = w.page_size
+    npg = (L + P - 1) // P
+    spec = OP.PoolSpec(w.fmt, npg, P, 1, w.head_dim)
+    pool = OP.new_pool(spec)
+    table = np.arange(npg, dtype=np.int32)[None]
+    OP.write(pool, spec, k[:, None], v[:, None], W.slots_for(table[0], P, np.arange(L)), g)
+    q = w.q()[b:b + 1, h * w.group:(h + 1) * w.group]
+    one = W.Workload(w.name, w.fmt, 1, w.group, w.head_dim, 1, P, L, L)
+    bytes_per = algorithmic_decode_bytes(one, [L])
+    times = []
+    t_end = time.perf_counter() + seconds
+    while (max_steps is None and (time.perf_counter() < t_end or len(times) < 2)) or \
+            (max_steps is not None and len(times) < max_steps):
+        t0 = time.perf_counter()
+        oracle.attention.decode_attention(q, pool, spec, g, table, np.array([L], np.int32), w.sm_scale())
+        times.append(time.perf_counter() - t0)
+    per = statistics.median(times)
+    return {"value": bytes_per / per / 1e9, "steps": len(times), "seconds_per_step": per,
+            "tokens": L, "bytes_per_step": bytes_per, "times": times}
+
+
+def run_cpu_oracle_subprocess(name, seconds, max_steps=None):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    code = ("import json,sys; sys.path.insert(0, %r); import bench; "
+            "r = bench.cpu_oracle_sample(%r, %r, %r); r.pop('times'); print(json.dumps(r))"
+            % (ROOT, name, seconds, max_steps))
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                         timeout=max(600, 20 * seconds))
+    if out.returncode != 0:
+        raise RuntimeError(out.stderr[-2000:])
+    return json.loads(out.stdout.strip().splitlines()[-1])
+
+
+# ----------------------------------------------------------------------------- arms
+def dist_setup(args):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return rank, world, local, pg
+
+
+def barrier(pg, device=None):
+    if pg is not None:
+        import torch
+        if device is not None and pg.get_backend() == "nccl":
+            pg.barrier(device_ids=[device.index])
+        else:
+            pg.barrier()
+
+
+def max_over_ranks(pg, x, device=None):
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device if pg.get_backend() == "nccl" else "cpu")
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reference_arm(args):
+    rank, world, local, pg = dist_setup(args)
+    if rank != 0:
+        return 0
+    w = W.ALL[args.workload]
+    r = cpu_oracle_sample(w.name, 0, max_steps=args.warmup + args.steps)
+    times = r["times"][args.warmup:]
+    per = statistics.mean(times)
+    value = r["bytes_per_step"] / per / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": per * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "sample": f"request 0, kv head 0 ({w.group} query heads), "
+                   f"{r['tokens']} tokens per step"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"one request x one kv head of {w.name}, {r['tokens']} tokens, "
+                                   f"{args.steps} timed steps"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def kv4_arm(args):
+    import torch
+    import bit_paged_kv_kv4_gb300 as K
+    rank, world, local, pg = dist_setup(args)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    K.load(build_if_missing=True)
+
+    w = W.ALL[args.workload]
+    s = Setup(w, device, seed_offset=rank)
+    B, Hkv, Hq, D = w.batch, w.num_kv_heads, w.num_q_heads, w.head_dim
+    dec_bytes = algorithmic_decode_bytes(w, s.lens)
+    step_bytes = dec_bytes + algorithmic_write_bytes(w, B)
+
+    # ---- device-resident timed region -----------------------------------
+    for _ in range(args.warmup):
+        s.write()
+        s.decode()
+    torch.cuda.synchronize()
+    ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+    ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    with clocks:
+        barrier(pg, device)
+        torch.cuda.synchronize()
+        t_start.record()
+        for i in range(args.steps):
+            ev_step[i][0].record()
+            s.write()
+            ev_dec[i][0].record()
+            s.decode()
+            ev_dec[i][1].record()
+            ev_step[i][1].record()
+        t_end.record()
+        torch.cuda.synchronize()
+        barrier(pg, device)
+    total = t_start.elapsed_time(t_end) * 1e-3
+    total = max_over_ranks(pg, total, device)
+    dec_times = [a.elapsed_time(b) * 1e-3 for a, b in ev_dec]
+    err = K.kv4_device_error()
+    if err != 0:
+        raise SystemExit(f"device error {err} during the timed region")
+    per_step = total / args.steps
+    value = step_bytes * world / per_step / 1e9
+
+    peak, peak_src = read_peaks()
+    dec_avg = statistics.mean(dec_times)
+    achieved = dec_bytes / dec_avg / 1e9
+
+    # ---- end to end through the public API, host buffers ----------------
+    h_q = torch.empty_like(s.q, device="cpu").pin_memory()
+    h_q.copy_(s.q.cpu())
+    h_k = s.k_new.cpu().pin_memory()
+    h_v = s.v_new.cpu().pin_memory()
+    h_slot = s.slot_new.cpu().pin_memory()
+    h_lens = s.d_lens.cpu().pin_memory()
+    h_out = torch.empty((B, Hq, D), dtype=torch.float32).pin_memory()
+    d_q, d_k, d_v = torch.empty_like(s.q), torch.empty_like(s.k_new), torch.empty_like(s.v_new)
+    d_slot, d_lens = torch.empty_like(s.slot_new), torch.empty_like(s.d_lens)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_slot, h_lens))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        d_q.copy_(h_q, non_blocking=True)
+        d_k.copy_(h_k, non_blocking=True)
+        d_v.copy_(h_v, non_blocking=True)
+        d_slot.copy_(h_slot, non_blocking=True)
+        d_lens.copy_(h_lens, non_blocking=True)
+        K.kv4_write(d_k, d_v, d_slot, s.pool, s.g)
+        K.kv4_decode_attention(d_q, s.pool, s.g, s.d_table, d_lens, s.sm, s.out,
+                               num_splits=s.splits, workspace=s.ws)
+        h_out.copy_(s.out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(pg, device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_total = max_over_ranks(pg, e0.elapsed_time(e1) * 1e-3, device)
+    e2e_value = step_bytes * world / (e2e_total / args.steps) / 1e9
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16*f16+f32 (nvfp4 cache)",
+        "data": "synthetic",
+        "config": {"workload": f"{w.name}: " + w.notes, "kv_heads": Hkv, "q_heads": Hq,
+                   "head_dim": D, "batch": B, "page_size": w.page_size,
+                   "seq_lens": [int(x) for x in s.lens], "num_splits": s.splits,
+                   "kv_bytes_per_step": dec_bytes, "step_bytes": step_bytes,
+                   "l2": "inputs larger than L2: the pool is %.0f MB vs 129 MB L2" % (s.pool.nbytes / 1e6),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": recorded_traffic(w.name),
+                     "kernel": "kv4_decode_attention (split kernel + combine)",
+                     "peak_source": f"{peak_src} hbm_gbs", "decode_us": dec_avg * 1e6,
+                     "decode_us_median": statistics.median(dec_times) * 1e6},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_total / args.steps * 1e3},
+        "gpu_launches": args.steps * s.launches_per_step(),
+        "clocks": clocks.summary(),
+    }
+    del s
+    torch.cuda.empty_cache()
+
+    # ---- the other workloads of the metric (one GPU, rank 0) -------------
+    if rank == 0 and not args.no_extra:
+        extra = {}
+        for name in ("nvfp4_160k", "nvfp4_1m", "int4_220k"):
+            wx = W.ALL[name]
+            sx = Setup(wx, device)
+            ts = time_decode_only(sx, max(5, min(args.steps, 20)))
+            bx = algorithmic_decode_bytes(wx, sx.lens)
+            med = statistics.median(ts)
+            extra[name] = {"decode_us": med * 1e6, "gbs": bx / med / 1e9, "frac": bx / med / 1e9 / peak,
+                           "num_splits": sx.splits, "kv_bytes": bx,
+                           "tokens_per_s_16_layers": wx.batch / (16 * med)}
+            if name == "nvfp4_160k":
+                extra["dequant_prefix_160k"] = time_prefix(sx, wx, peak)
+                extra["write_prefill_8k"] = time_write_prefill(sx, wx, peak)
+            del sx
+            torch.cuda.empty_cache()
+        line["workloads"] = extra
+
+    if rank == 0 and not args.no_cpu:
+        try:
+            r = run_cpu_oracle_subprocess(w.name, args.cpu_seconds)
+            line["cpu_baseline"] = {"value": r["value"], "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                    "sample": f"request 0 x kv head 0 of {w.name} ({r['tokens']} tokens, "
+                                              f"{w.group} query heads), {r['steps']} repeats, FP64 numpy, "
+                                              "one thread"}
+        except Exception as e:  # the baseline is reported, never required
+            line["cpu_baseline"] = {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                    "sample": f"failed: {str(e)[-200:]}"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+def time_prefix(s, w, peak):
+    import torch
+    K = s.K
+    prefix = np.array([max(int(s.lens[0]) - w.prefix_chunk, 0)], np.int32)
+    cu = np.array([0, prefix[0]], np.int64)
+    n = int(prefix[0])
+    wk = torch.empty((n, w.num_kv_heads, w.head_dim), dtype=torch.uint8, device=s.device)
+    wv = torch.empty_like(wk)
+    s8 = (6 * s.g).contiguous()
+    d_prefix = torch.from_numpy(prefix).to(s.device)
+    d_cu = torch.from_numpy(cu).to(s.device)
+    table0 = s.d_table[:1].contiguous()
+
+    def run():
+        K.kv4_dequant_prefix(s.pool, s.g, table0, d_prefix, d_cu, n, s8, wk, wv)
+
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(10):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        run()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b) * 1e-3)
+    med = statistics.median(ts)
+    D = w.head_dim
+    byts = n * w.num_kv_heads * (2 * (D // 2 + D // 16) + 2 * D)
+    return {"prefix_tokens": n, "us": med * 1e6, "gbs": byts / med / 1e9, "frac": byts / med / 1e9 / peak}
+
+
+def time_write_prefill(s, w, peak):
+    import torch
+    K = s.K
+    T = w.prefix_chunk
+    gen = torch.Generator(device=s.device).manual_seed(7)
+    k = torch.randn((T, w.num_kv_heads, w.head_dim), generator=gen, device=s.device).to(torch.bfloat16)
+    v = torch.randn((T, w.num_kv_heads, w.head_dim), generator=gen, device=s.device).to(torch.bfloat16)
+    # scratch pool of the same geometry, so the measured pool stays intact
+    pool = K.Pool(w.fmt, (T + w.page_size - 1) // w.page_size, w.page_size, w.num_kv_heads, w.head_dim,
+                  device=s.device)
+    slots = torch.arange(T, dtype=torch.int64, device=s.device)
+    for _ in range(3):
+        K.kv4_write(k, v, slots, pool, s.g)
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(10):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        K.kv4_write(k, v, slots, pool, s.g)
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b) * 1e-3)
+    med = statistics.median(ts)
+    byts = algorithmic_write_bytes(w, T)
+    return {"tokens": T, "us": med * 1e6, "gbs": byts / med / 1e9, "frac": byts / med / 1e9 / peak,
+            "note": "16 MB in, 9.4 MB out: smaller than L2, so this is an L2-warm figure"}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("kv4", "reference"), default="kv4")
+    ap.add_argument("--workload", default="nvfp4_32k", choices=sorted(W.ALL))
+    ap.add_argument("--no-extra", action="store_true", help="skip the 160K / 1M / INT4 lines")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return reference_arm(args)
+    return kv4_arm(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,370 @@
+// The C ABI of libkv4 (declared in include/kv4.h): host-side validation,
+// workspace sizing, TMA descriptor set-up and dispatch to the kernels.
+//
+// Every entry point validates its arguments before touching the CUDA
+// runtime, so argument errors are reported (and testable) on machines without
+// a GPU.  Nothing here allocates device memory or synchronises the host,
+// except kv4_device_error(), which reads the per-device error word.
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/kv4.h"
+#include "kv4_internal.h"
+
+namespace {
+
+thread_local std::string g_msg;
+
+kv4_status fail(kv4_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_msg = buf;
+  return s;
+}
+
+kv4_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(KV4_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int64_t chunk_bytes_of(const kv4_pool& p) {
+  const int64_t P = p.page_size, D = p.head_dim;
+  return p.fmt == KV4_NVFP4 ? P * (D + D / 8) : P * (D + 8);
+}
+
+kv4_status check_pool(const kv4_pool* p) {
+  if (p == nullptr) return fail(KV4_EINVAL, "pool descriptor is NULL");
+  if (p->fmt != KV4_NVFP4 && p->fmt != KV4_INT4_PTH) return fail(KV4_EINVAL, "bad fmt %d", p->fmt);
+  if (p->reserved != 0) return fail(KV4_EINVAL, "pool.reserved must be 0");
+  if (p->num_pages < 1) return fail(KV4_EINVAL, "num_pages must be >= 1");
+  if (p->num_kv_heads < 1) return fail(KV4_EINVAL, "num_kv_heads must be >= 1");
+  if (p->page_size < 16 || p->page_size % 16 != 0)
+    return fail(KV4_EINVAL, "page_size %d is not a positive multiple of 16", p->page_size);
+  if (p->head_dim != 64 && p->head_dim != 128 && p->head_dim != 256)
+    return fail(KV4_EUNSUPPORTED, "head_dim %d not built (64, 128, 256)", p->head_dim);
+  const int64_t bytes = static_cast<int64_t>(p->num_pages) * p->num_kv_heads * chunk_bytes_of(*p);
+  if (bytes / (p->head_dim / 2) >= (int64_t{1} << 31))
+    return fail(KV4_EUNSUPPORTED, "pool of %lld bytes exceeds the 2^31 code rows a TMA "
+                "coordinate addresses", static_cast<long long>(bytes));
+  return KV4_OK;
+}
+
+kv4_status check_pool_base(const kv4_pool* p) {
+  if (p->base == nullptr) return fail(KV4_EINVAL, "pool.base is NULL");
+  if (!aligned(p->base, 256)) return fail(KV4_EINVAL, "pool.base must be 256-byte aligned");
+  return KV4_OK;
+}
+
+// ---------------------------------------------------------------- device state
+__device__ int g_kv4_error_word;
+
+int* error_word() {
+  static int* cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (cache[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_kv4_error_word) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<int*>(p);
+  }
+  return cache[dev];
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 152;
+  return n;
+}
+
+// ---------------------------------------------------------------- TMA maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// The pool as a 2-D byte tensor of code rows: [pool_bytes / RB][RB], loaded in
+// boxes of RB bytes x `box_rows` rows with the swizzle whose span is RB.
+kv4_status code_row_map(const kv4_pool& p, CUtensorMap* map) {
+  struct Entry { const void* base; int64_t rows; int rb; CUtensorMap map; bool used; };
+  static Entry cache[8];
+  static int next = 0;
+  static std::mutex mu;
+  const int rb = p.head_dim / 2;
+  const int64_t rows = static_cast<int64_t>(p.num_pages) * p.num_kv_heads * chunk_bytes_of(p) / rb;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (auto& e : cache)
+      if (e.used && e.base == p.base && e.rows == rows && e.rb == rb) {
+        *map = e.map;
+        return KV4_OK;
+      }
+  }
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return fail(KV4_ECUDA, "cuTensorMapEncodeTiled is not available");
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(rb), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(rb)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(rb), static_cast<cuuint32_t>(kv4::decode_box_rows())};
+  cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapSwizzle sw = rb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : rb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                           : CU_TENSOR_MAP_SWIZZLE_32B;
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, p.base, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(KV4_ECUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  std::lock_guard<std::mutex> lock(mu);
+  cache[next] = Entry{p.base, rows, rb, *map, true};
+  next = (next + 1) % 8;
+  return KV4_OK;
+}
+
+int64_t align256(int64_t x) { return (x + 255) / 256 * 256; }
+
+}  // namespace
+
+extern "C" {
+
+int64_t kv4_pool_chunk_bytes(const kv4_pool* pool) {
+  if (check_pool(pool) != KV4_OK) return 0;
+  return chunk_bytes_of(*pool);
+}
+
+int64_t kv4_pool_bytes(const kv4_pool* pool) {
+  if (check_pool(pool) != KV4_OK) return 0;
+  return static_cast<int64_t>(pool->num_pages) * pool->num_kv_heads * chunk_bytes_of(*pool);
+}
+
+kv4_status kv4_write(const void* k, const void* v, const int64_t* slot_mapping,
+                     int64_t num_tokens, const kv4_pool* pool,
+                     const float* layer_global_scale, int32_t fmt, void* stream) {
+  g_msg.clear();
+  kv4_status s = check_pool(pool);
+  if (s != KV4_OK) return s;
+  if ((s = check_pool_base(pool)) != KV4_OK) return s;
+  if (fmt != pool->fmt) return fail(KV4_EINVAL, "fmt %d does not match pool.fmt %d", fmt, pool->fmt);
+  if (num_tokens < 0) return fail(KV4_EINVAL, "num_tokens < 0");
+  if (num_tokens == 0) return KV4_OK;
+  if (k == nullptr || v == nullptr || slot_mapping == nullptr)
+    return fail(KV4_EINVAL, "k, v and slot_mapping must be non-NULL");
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(slot_mapping, 8))
+    return fail(KV4_EINVAL, "k and v must be 16-byte aligned, slot_mapping 8-byte aligned");
+  if (fmt == KV4_NVFP4 && layer_global_scale == nullptr)
+    return fail(KV4_EINVAL, "NVFP4 needs layer_global_scale");
+  const int64_t threads = num_tokens * pool->num_kv_heads * (pool->head_dim / 8);
+  if ((threads + 255) / 256 >= (int64_t{1} << 31)) return fail(KV4_EINVAL, "num_tokens too large");
+
+  kv4::WriteArgs a{};
+  a.k = static_cast<const __nv_bfloat16*>(k);
+  a.v = static_cast<const __nv_bfloat16*>(v);
+  a.slot_mapping = slot_mapping;
+  a.T = num_tokens;
+  a.pool = static_cast<uint8_t*>(pool->base);
+  a.chunk_bytes = chunk_bytes_of(*pool);
+  a.P = pool->page_size;
+  a.Hkv = pool->num_kv_heads;
+  a.num_pages = pool->num_pages;
+  a.D = pool->head_dim;
+  a.fmt = fmt;
+  a.gscale = layer_global_scale;
+  a.err = error_word();
+  if (a.err == nullptr) return fail(KV4_ECUDA, "no CUDA device / error word unavailable");
+  cudaError_t e = kv4::launch_write(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KV4_OK : cuda_fail(e, "kv4_write launch");
+}
+
+int32_t kv4_decode_default_splits(int32_t batch, int32_t num_kv_heads, int32_t max_pages,
+                                  int32_t page_size) {
+  if (batch < 1 || num_kv_heads < 1 || max_pages < 1 || page_size < 1) return 1;
+  const int64_t units = static_cast<int64_t>(batch) * num_kv_heads;
+  const int64_t target = 4LL * sm_count();               // about four waves of CTAs
+  int64_t s = (target + units - 1) / units;
+  const int64_t max_tokens = static_cast<int64_t>(max_pages) * page_size;
+  const int64_t cap = (max_tokens + 4 * 64 - 1) / (4 * 64);   // >= one tile per warp
+  if (s > cap) s = cap;
+  if (s > 1024) s = 1024;
+  return static_cast<int32_t>(s < 1 ? 1 : s);
+}
+
+int64_t kv4_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t head_dim,
+                                   int32_t num_splits) {
+  if (batch < 0 || num_q_heads < 0 || head_dim < 0 || num_splits < 0) return 0;
+  if (num_splits <= 1) return 0;
+  const int64_t rows = static_cast<int64_t>(batch) * num_q_heads * num_splits;
+  return align256(rows * 4 * 4) + rows * head_dim * 4;
+}
+
+kv4_status kv4_decode_attention(const void* q, const kv4_pool* pool,
+                                const float* layer_global_scale, const int32_t* block_table,
+                                int32_t max_pages, const int32_t* seq_lens, int32_t batch,
+                                int32_t num_q_heads, float sm_scale, int32_t num_splits,
+                                void* workspace, int64_t workspace_bytes, void* out,
+                                int32_t out_is_fp32, void* stream) {
+  g_msg.clear();
+  kv4_status s = check_pool(pool);
+  if (s != KV4_OK) return s;
+  if ((s = check_pool_base(pool)) != KV4_OK) return s;
+  if (batch < 0) return fail(KV4_EINVAL, "batch < 0");
+  if (num_q_heads < 1 || num_q_heads % pool->num_kv_heads != 0)
+    return fail(KV4_EINVAL, "num_q_heads %d is not a positive multiple of num_kv_heads %d",
+                num_q_heads, pool->num_kv_heads);
+  if (max_pages < 1) return fail(KV4_EINVAL, "max_pages must be >= 1");
+  if (static_cast<int64_t>(max_pages) * pool->page_size >= (int64_t{1} << 31))
+    return fail(KV4_EINVAL, "max_pages * page_size must be < 2^31");
+  if (num_splits < 0 || num_splits > 1024) return fail(KV4_EINVAL, "num_splits must be in [0, 1024]");
+  if (!(sm_scale == sm_scale) || sm_scale > 3.0e38f || sm_scale < -3.0e38f)
+    return fail(KV4_EINVAL, "sm_scale must be finite");
+  if (batch == 0) return KV4_OK;
+  if (q == nullptr || out == nullptr || block_table == nullptr || seq_lens == nullptr)
+    return fail(KV4_EINVAL, "q, out, block_table and seq_lens must be non-NULL");
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
+    return fail(KV4_EINVAL, "q and out must be 16-byte aligned");
+  if (pool->fmt == KV4_NVFP4 && layer_global_scale == nullptr)
+    return fail(KV4_EINVAL, "NVFP4 needs layer_global_scale");
+  const int G = num_q_heads / pool->num_kv_heads;
+  if (batch > 65535 || static_cast<int64_t>(pool->num_kv_heads) * ((G + 7) / 8) > 65535)
+    return fail(KV4_EINVAL, "batch or heads exceed the launch grid");
+  const int S = num_splits == 0 ? kv4_decode_default_splits(batch, pool->num_kv_heads, max_pages,
+                                                             pool->page_size)
+                                : num_splits;
+  const int64_t need = kv4_decode_workspace_bytes(batch, num_q_heads, pool->head_dim, S);
+  if (need > 0) {
+    if (workspace == nullptr || workspace_bytes < need)
+      return fail(KV4_EINVAL, "workspace of %lld bytes needed for %d splits",
+                  static_cast<long long>(need), S);
+    if (!aligned(workspace, 256)) return fail(KV4_EINVAL, "workspace must be 256-byte aligned");
+  }
+
+  kv4::DecodeArgs a{};
+  a.pool = static_cast<const uint8_t*>(pool->base);
+  a.chunk_bytes = chunk_bytes_of(*pool);
+  a.P = pool->page_size;
+  a.Hkv = pool->num_kv_heads;
+  a.num_pages = pool->num_pages;
+  a.D = pool->head_dim;
+  a.fmt = pool->fmt;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.gscale = layer_global_scale;
+  a.block_table = block_table;
+  a.max_pages = max_pages;
+  a.seq_lens = seq_lens;
+  a.B = batch;
+  a.Hq = num_q_heads;
+  a.G = G;
+  a.sm_scale = sm_scale;
+  a.num_splits = S;
+  if (S > 1) {
+    const int64_t rows = static_cast<int64_t>(batch) * num_q_heads * S;
+    a.part_ml = static_cast<float*>(workspace);
+    a.part_o = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align256(rows * 4 * 4));
+  }
+  a.out = out;
+  a.out_f32 = out_is_fp32 ? 1 : 0;
+  a.err = error_word();
+  if (a.err == nullptr) return fail(KV4_ECUDA, "no CUDA device / error word unavailable");
+  CUtensorMap map;
+  if ((s = code_row_map(*pool, &map)) != KV4_OK) return s;
+  cudaError_t e = kv4::launch_decode(a, map, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KV4_OK : cuda_fail(e, "kv4_decode_attention launch");
+}
+
+kv4_status kv4_dequant_prefix(const kv4_pool* pool, const float* layer_global_scale,
+                              const int32_t* block_table, int32_t max_pages,
+                              const int32_t* prefix_lens, const int64_t* cu_prefix,
+                              int32_t batch, int32_t max_prefix_len, const float* fp8_scale,
+                              void* fp8_k, void* fp8_v, void* stream) {
+  g_msg.clear();
+  kv4_status s = check_pool(pool);
+  if (s != KV4_OK) return s;
+  if ((s = check_pool_base(pool)) != KV4_OK) return s;
+  if (batch < 0 || max_prefix_len < 0) return fail(KV4_EINVAL, "batch and max_prefix_len must be >= 0");
+  if (max_pages < 1) return fail(KV4_EINVAL, "max_pages must be >= 1");
+  if (static_cast<int64_t>(max_pages) * pool->page_size >= (int64_t{1} << 31))
+    return fail(KV4_EINVAL, "max_pages * page_size must be < 2^31");
+  if (max_prefix_len > max_pages * pool->page_size)
+    return fail(KV4_EINVAL, "max_prefix_len exceeds max_pages * page_size");
+  if (batch > 65535) return fail(KV4_EINVAL, "batch exceeds the launch grid");
+  if (batch == 0 || max_prefix_len == 0) return KV4_OK;
+  if (block_table == nullptr || prefix_lens == nullptr || cu_prefix == nullptr ||
+      fp8_scale == nullptr || fp8_k == nullptr || fp8_v == nullptr)
+    return fail(KV4_EINVAL, "block_table, prefix_lens, cu_prefix, fp8_scale and outputs must be non-NULL");
+  if (!aligned(fp8_k, 16) || !aligned(fp8_v, 16) || !aligned(cu_prefix, 8))
+    return fail(KV4_EINVAL, "fp8_k and fp8_v must be 16-byte aligned");
+  if (pool->fmt == KV4_NVFP4 && layer_global_scale == nullptr)
+    return fail(KV4_EINVAL, "NVFP4 needs layer_global_scale");
+  const int64_t threads = static_cast<int64_t>(max_prefix_len) * pool->num_kv_heads * (pool->head_dim / 8);
+  if ((threads + 255) / 256 >= (int64_t{1} << 31)) return fail(KV4_EINVAL, "prefix too large");
+
+  kv4::PrefixArgs a{};
+  a.pool = static_cast<const uint8_t*>(pool->base);
+  a.chunk_bytes = chunk_bytes_of(*pool);
+  a.P = pool->page_size;
+  a.Hkv = pool->num_kv_heads;
+  a.num_pages = pool->num_pages;
+  a.D = pool->head_dim;
+  a.fmt = pool->fmt;
+  a.gscale = layer_global_scale;
+  a.block_table = block_table;
+  a.max_pages = max_pages;
+  a.prefix_lens = prefix_lens;
+  a.cu_prefix = cu_prefix;
+  a.B = batch;
+  a.max_prefix_len = max_prefix_len;
+  a.fp8_scale = fp8_scale;
+  a.out_k = static_cast<uint8_t*>(fp8_k);
+  a.out_v = static_cast<uint8_t*>(fp8_v);
+  a.err = error_word();
+  if (a.err == nullptr) return fail(KV4_ECUDA, "no CUDA device / error word unavailable");
+  cudaError_t e = kv4::launch_prefix(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KV4_OK : cuda_fail(e, "kv4_dequant_prefix launch");
+}
+
+int32_t kv4_device_error(void) {
+  int* p = error_word();
+  if (p == nullptr) return KV4_ECUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return KV4_ECUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return KV4_ECUDA;
+  const int zero = 0;
+  if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return KV4_ECUDA;
+  return v;
+}
+
+const char* kv4_status_str(int32_t status) {
+  switch (status) {
+    case KV4_OK: return "KV4_OK";
+    case KV4_EINVAL: return "KV4_EINVAL: invalid argument";
+    case KV4_EUNSUPPORTED: return "KV4_EUNSUPPORTED: shape not supported";
+    case KV4_ECUDA: return "KV4_ECUDA: CUDA runtime error";
+    case KV4_EBOUNDS: return "KV4_EBOUNDS: index outside the pool or table";
+    case KV4_ETIMEOUT: return "KV4_ETIMEOUT: a bounded wait ran out";
+    default: return "KV4: unknown status";
+  }
+}
+
+const char* kv4_last_error_message(void) { return g_msg.c_str(); }
+
+}  // extern "C"

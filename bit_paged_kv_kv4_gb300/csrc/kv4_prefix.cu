@@ -1,0 +1,90 @@
+// Dequantise a cached 4-bit prefix into FP8 E4M3 workspaces: the chunked
+// prefill / extend path of "SGLang's 4-bit KV cache", Figure 2, which "reads
+// NVFP4 and dequantizes the cached prefix into a reused FP8 workspace" before
+// attending over prefix plus the current chunk.
+//
+// One thread turns 8 consecutive head-dim elements of one (token, head, K|V)
+// row into 8 E4M3 bytes: x_hat = (e2m1 * e4m3) * g in FP32 (NVFP4) or
+// code * s (INT4), then E4M3(x_hat / s_fp8) with RNE and saturation.  Pure
+// streaming: 4-byte code loads, one scale, one 8-byte store.
+#include <cstdint>
+
+#include "kv4_device.cuh"
+#include "kv4_internal.h"
+
+namespace kv4 {
+
+__global__ void __launch_bounds__(256)
+prefix_kernel(const PrefixArgs a) {
+  const int D = a.D;
+  const int tpr = D / 8;
+  const int b = blockIdx.z;
+  const int kind = blockIdx.y;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t row = tid / tpr;                         // (t, h)
+  const int part = static_cast<int>(tid % tpr);
+  const int t = static_cast<int>(row / a.Hkv);
+  const int h = static_cast<int>(row % a.Hkv);
+  int n = a.prefix_lens[b];
+  const int cap = min(a.max_prefix_len, a.max_pages * a.P);
+  if (n < 0 || n > cap) {
+    if (tid == 0) set_error(a.err, KV4_EBOUNDS);
+    n = n < 0 ? 0 : cap;
+  }
+  if (t >= n) return;
+
+  int page = __ldg(a.block_table + static_cast<int64_t>(b) * a.max_pages + t / a.P);
+  if (page < 0 || page >= a.num_pages) {
+    if (part == 0) set_error(a.err, KV4_EBOUNDS);
+    return;
+  }
+  const int off = t % a.P;
+  const uint8_t* chunk = a.pool + (static_cast<int64_t>(page) * a.Hkv + h) * a.chunk_bytes;
+  const int RB = D / 2;
+  const uint32_t codes = *reinterpret_cast<const uint32_t*>(
+      chunk + static_cast<int64_t>(kind) * a.P * RB + static_cast<int64_t>(off) * RB + part * 4);
+  const float s8 = __ldg(a.fp8_scale + kind);
+
+  float xh[8];
+  if (a.fmt == KV4_NVFP4) {
+    const int SB = D / 16;
+    const uint8_t* sc = chunk + static_cast<int64_t>(a.P) * D + static_cast<int64_t>(kind) * a.P * SB +
+                        static_cast<int64_t>(off) * SB;
+    const float s = e4m3_to_f32(sc[part >> 1]);
+    const float g = __ldg(a.gscale + kind);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t h2 = e2m1x2_to_f16x2(codes >> (8 * j));
+      const float2 e = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+      xh[2 * j] = __fmul_rn(__fmul_rn(e.x, s), g);
+      xh[2 * j + 1] = __fmul_rn(__fmul_rn(e.y, s), g);
+    }
+  } else {
+    const float s = *reinterpret_cast<const float*>(chunk + static_cast<int64_t>(a.P) * D +
+                                                     (static_cast<int64_t>(kind) * a.P + off) * 4);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int c = static_cast<int>((codes >> (4 * j)) & 0xFu);
+      xh[j] = __fmul_rn(static_cast<float>(c >= 8 ? c - 16 : c), s);
+    }
+  }
+  uint2 outw;
+  outw.x = f32x2_to_e4m3x2(__fdiv_rn(xh[0], s8), __fdiv_rn(xh[1], s8)) |
+           (f32x2_to_e4m3x2(__fdiv_rn(xh[2], s8), __fdiv_rn(xh[3], s8)) << 16);
+  outw.y = f32x2_to_e4m3x2(__fdiv_rn(xh[4], s8), __fdiv_rn(xh[5], s8)) |
+           (f32x2_to_e4m3x2(__fdiv_rn(xh[6], s8), __fdiv_rn(xh[7], s8)) << 16);
+  const int64_t orow = a.cu_prefix[b] + t;
+  uint8_t* dst = (kind == 0 ? a.out_k : a.out_v) + (orow * a.Hkv + h) * D + part * 8;
+  *reinterpret_cast<uint2*>(dst) = outw;
+}
+
+cudaError_t launch_prefix(const PrefixArgs& a, cudaStream_t st) {
+  const int64_t threads = static_cast<int64_t>(a.max_prefix_len) * a.Hkv * (a.D / 8);
+  if (threads == 0 || a.B == 0) return cudaSuccess;
+  const int bs = 256;
+  const int64_t blocks = (threads + bs - 1) / bs;
+  prefix_kernel<<<dim3(static_cast<unsigned>(blocks), 2, a.B), bs, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace kv4

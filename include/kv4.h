@@ -1,0 +1,202 @@
+/*
+ * kv4.h -- C ABI of libkv4: a 4-bit paged KV cache for LLM decode on GB300
+ * (sm_103a).
+ *
+ * Three operations, after the three attention paths over one pool in
+ * "SGLang's 4-bit KV cache: the 56% is exact, the 1.78x is untested",
+ * Figure 2 caption:
+ *
+ *   kv4_write             quantise new K/V tokens into the paged pool
+ *                         (the write into "a GPU KV pool of packed E2M1 K and
+ *                         V, block scales at one E4M3 per sixteen elements,
+ *                         and per-layer FP32 global scales");
+ *   kv4_decode_attention  decode attention that reads the 4-bit pool and
+ *                         dequantises inside the kernel ("Only decode reads
+ *                         NVFP4 and dequantizes inside the kernel"), split
+ *                         over the sequence with a log-sum-exp combine;
+ *   kv4_dequant_prefix    the chunked-prefill path: dequantise the cached
+ *                         prefix into a reused FP8 workspace.
+ *
+ * Two formats share the pool layout:
+ *   KV4_NVFP4     E2M1 elements, one E4M3 scale per 16 elements, one FP32
+ *                 global scale per layer for K and one for V; 9 bytes per 16
+ *                 values, 0.5625 of FP8 (same page, "The 56% survives its own
+ *                 scale").
+ *   KV4_INT4_PTH  INT4 per token and head: 4-bit codes plus per-token-head
+ *                 scales, 264 bytes per head and token at head_dim 256
+ *                 ("KV cache in 4 bits", section "What we changed").
+ *
+ * Encoding (the pages name the formats, not the encoder; this is the
+ * library's definition, identical to the test oracle's):
+ *   NVFP4, per 16-element block of a bf16 row x with global scale g (FP32):
+ *     amax = max|x_i|; sf = amax / (6*g) [6*g rounded first]; S = E4M3(sf)
+ *     with round-to-nearest-even, saturating at 448; denom = float(S) * g;
+ *     if S == 0 or denom == 0 every code is +0, else
+ *     code_i = E2M1(x_i / denom), RNE, saturating at 6, sign kept.
+ *     All arithmetic is IEEE FP32.  Decode: e2m1(code) * e4m3(S) * g.
+ *   INT4_PTH, per (token, head) row, separately for K and V:
+ *     s = amax / 7 (FP32); code = clamp(rne(x / s), -8, 7); s == 0 gives
+ *     all-zero codes.  Decode: code * s.
+ *   Two 4-bit codes per byte: element 2j in the low nibble of byte j.
+ *
+ * Pool layout (one pool per layer, caller-owned device memory):
+ *   base -> [num_pages][num_kv_heads][chunk_bytes]; each (page, head) chunk
+ *   holds four regions, row `off` of each belonging to token `off` of the
+ *   page (P = page_size, D = head_dim):
+ *     NVFP4: [K codes P*D/2][V codes P*D/2][K scales P*D/16][V scales P*D/16]
+ *     INT4 : [K codes P*D/2][V codes P*D/2][K scale f32 * P][V scale f32 * P]
+ *   chunk_bytes = P*(D + D/8) (NVFP4) or P*(D + 8) (INT4).  A slot is
+ *   page * P + off.  The FP32 global scales are not in the pool: callers pass
+ *   them as a device float[2] = {g_K, g_V} per layer.
+ *
+ * Conventions for every entry point:
+ *   - All device pointers are caller-owned; the library allocates nothing.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) and never synchronises the host.
+ *   - Arguments are validated on the host first.  A failure returns a status
+ *     (and a message, kv4_last_error_message) and launches nothing.
+ *   - Device-side range checks (a block_table entry outside [0, num_pages),
+ *     a slot beyond the pool, seq_len beyond max_pages*P, a wait that ran
+ *     out of time) never trap: the kernel skips the bad access, records a
+ *     kv4_status in a per-device error word and returns normally.  Read and
+ *     clear it with kv4_device_error().
+ *   - Supported shapes: head_dim in {64, 128, 256}; page_size a positive
+ *     multiple of 16; base 256-byte aligned; q, out and k/v 16-byte aligned.
+ *   - Sizes are element counts unless named *_bytes.
+ */
+#ifndef KV4_H_
+#define KV4_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { KV4_NVFP4 = 0, KV4_INT4_PTH = 1 } kv4_fmt;
+
+typedef enum {
+  KV4_OK = 0,
+  KV4_EINVAL = 1,        /* bad argument (null pointer, size, alignment)    */
+  KV4_EUNSUPPORTED = 2,  /* valid but not built (e.g. head_dim 96)          */
+  KV4_ECUDA = 3,         /* a CUDA runtime call or launch failed            */
+  KV4_EBOUNDS = 4,       /* device: an index fell outside the pool/table    */
+  KV4_ETIMEOUT = 5       /* device: a bounded wait on a copy ran out        */
+} kv4_status;
+
+/* One layer's paged pool.  Host-side descriptor; `base` is device memory of
+ * kv4_pool_bytes() bytes. */
+typedef struct {
+  int32_t fmt;           /* kv4_fmt                                          */
+  int32_t num_pages;
+  int32_t page_size;     /* tokens per page (P)                              */
+  int32_t num_kv_heads;  /* Hkv                                              */
+  int32_t head_dim;      /* D                                                */
+  int32_t reserved;      /* must be 0                                        */
+  void*   base;
+} kv4_pool;
+
+/* Bytes of one (page, kv head) chunk and of the whole pool; 0 if the
+ * descriptor is invalid.  Pure host functions. */
+int64_t kv4_pool_chunk_bytes(const kv4_pool* pool);
+int64_t kv4_pool_bytes(const kv4_pool* pool);
+
+/*
+ * kv4_write -- quantise T tokens of K and V into the pool (Figure 2: the
+ * decode step stores the new token's K/V; prefill stores the prompt).
+ *   k, v          device bf16 [T][Hkv][D], contiguous, 16-byte aligned.
+ *   slot_mapping  device int64 [T]: destination slot of token t, or < 0 to
+ *                 skip it.  A slot >= num_pages*P is skipped and flagged
+ *                 KV4_EBOUNDS in the device error word.
+ *   layer_global_scale  device float[2] {g_K, g_V}, each > 0 (NVFP4 only;
+ *                 may be NULL for INT4).
+ *   fmt           must equal pool->fmt.
+ * Writes only the rows of the slots it stores; nothing else in the pool.
+ * Two tokens mapped to one slot race (last writer unspecified).
+ */
+kv4_status kv4_write(const void* k, const void* v, const int64_t* slot_mapping,
+                     int64_t num_tokens, const kv4_pool* pool,
+                     const float* layer_global_scale, int32_t fmt, void* stream);
+
+/* Number of KV splits kv4_decode_attention uses when passed num_splits = 0,
+ * for a batch of `batch` requests whose block tables have max_pages
+ * entries.  Host-only; depends on the current device's SM count. */
+int32_t kv4_decode_default_splits(int32_t batch, int32_t num_kv_heads,
+                                  int32_t max_pages, int32_t page_size);
+
+/* Workspace bytes kv4_decode_attention needs for these sizes (0 when
+ * num_splits == 1: one split writes `out` directly). */
+int64_t kv4_decode_workspace_bytes(int32_t batch, int32_t num_q_heads,
+                                   int32_t head_dim, int32_t num_splits);
+
+/*
+ * kv4_decode_attention -- one decode step of paged attention over the 4-bit
+ * pool (Figure 2, "Decode ... reads NVFP4 directly for native FP4 decode
+ * with scales").  For request b and query head j (kv head
+ * h = j / (Hq/Hkv): GQA groups are contiguous), over tokens t < seq_lens[b]
+ * stored at slot block_table[b*max_pages + t/P]*P + t%P:
+ *     out[b][j] = sum_t softmax_t(sm_scale * <q[b][j], K_hat_t>) V_hat_t
+ * with K_hat/V_hat the decoded cache values.  The sequence is cut into
+ * num_splits contiguous ranges whose partial softmax states (m, l, o) are
+ * merged by a log-sum-exp combine.  seq_lens[b] == 0 gives a zero row.
+ *   q            device bf16 [B][Hq][D]
+ *   layer_global_scale  device float[2] {g_K, g_V} (NVFP4; NULL for INT4)
+ *   block_table  device int32 [B][max_pages]; entries past a request's last
+ *                page are never read.
+ *   seq_lens     device int32 [B]; the decode step's own token (written by
+ *                kv4_write beforehand) is included.
+ *   num_splits   1..1024, or 0 for kv4_decode_default_splits().
+ *   workspace    device scratch of >= kv4_decode_workspace_bytes() bytes
+ *                (may be NULL when that is 0); contents on entry ignored.
+ *   out          device [B][Hq][D], float32 if out_is_fp32 else bf16.
+ * Deterministic: the same inputs give bitwise the same output.
+ */
+kv4_status kv4_decode_attention(const void* q, const kv4_pool* pool,
+                                const float* layer_global_scale,
+                                const int32_t* block_table, int32_t max_pages,
+                                const int32_t* seq_lens, int32_t batch,
+                                int32_t num_q_heads, float sm_scale,
+                                int32_t num_splits, void* workspace,
+                                int64_t workspace_bytes, void* out,
+                                int32_t out_is_fp32, void* stream);
+
+/*
+ * kv4_dequant_prefix -- the chunked-prefill path of Figure 2: "reads NVFP4
+ * and dequantizes the cached prefix into a reused FP8 workspace".  For each
+ * request b, prefix token t < prefix_lens[b] and kv head h:
+ *     ws[cu_prefix[b] + t][h][d] = E4M3(x_hat / s)
+ * x_hat the FP32 decoded value ((e2m1*e4m3)*g for NVFP4, code*s for INT4),
+ * s = fp8_scale[0] for K and fp8_scale[1] for V (per-tensor FP8 scales, the
+ * consumer multiplies by s), FP32 division, E4M3 RNE saturating at 448.
+ *   prefix_lens  device int32 [B]; cu_prefix device int64 [B+1] (exclusive
+ *                prefix sums; rows of request b start at cu_prefix[b]).
+ *   max_prefix_len  host upper bound of every prefix_lens[b] (sizes the
+ *                grid); larger device values are clipped and flagged.
+ *   fp8_scale    device float[2] {s_K, s_V}, each > 0.
+ *   fp8_k, fp8_v device uint8 E4M3 [sum prefix_lens][Hkv][D].
+ */
+kv4_status kv4_dequant_prefix(const kv4_pool* pool,
+                              const float* layer_global_scale,
+                              const int32_t* block_table, int32_t max_pages,
+                              const int32_t* prefix_lens,
+                              const int64_t* cu_prefix, int32_t batch,
+                              int32_t max_prefix_len, const float* fp8_scale,
+                              void* fp8_k, void* fp8_v, void* stream);
+
+/* Read and clear the current device's error word (the first kv4_status a
+ * kernel recorded since the last call, KV4_OK if none).  Synchronises the
+ * device.  Returns KV4_ECUDA if the read itself fails. */
+int32_t kv4_device_error(void);
+
+/* Static text for a status code. */
+const char* kv4_status_str(int32_t status);
+
+/* Detail of the last host-side failure on the calling thread ("" if none). */
+const char* kv4_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KV4_H_ */

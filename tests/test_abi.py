@@ -1,0 +1,111 @@
+"""The C ABI without a GPU: the library builds and loads, exports every
+function include/kv4.h declares, and rejects bad arguments on the host
+before any CUDA call (the validation contract of the header)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import bit_paged_kv_kv4_gb300 as K
+from bit_paged_kv_kv4_gb300 import _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "kv4.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return K.load(build_if_missing=True)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kv4_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_three_operations():
+    names = declared_functions()
+    for n in ("kv4_write", "kv4_decode_attention", "kv4_dequant_prefix"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def desc(fmt=0, pages=4, P=64, H=2, D=256, base=None):
+    return K._PoolDesc(fmt, pages, P, H, D, 0, base)
+
+
+def test_pool_sizes(lib):
+    d = desc()
+    assert lib.kv4_pool_chunk_bytes(ctypes.byref(d)) == 64 * 288
+    assert lib.kv4_pool_bytes(ctypes.byref(d)) == 4 * 2 * 64 * 288
+    assert lib.kv4_pool_chunk_bytes(ctypes.byref(desc(fmt=1, P=1600))) == 422400
+    for bad in (desc(P=8), desc(P=40), desc(D=96), desc(H=0), desc(pages=0), desc(fmt=7)):
+        assert lib.kv4_pool_bytes(ctypes.byref(bad)) == 0
+
+
+def test_workspace_and_splits(lib):
+    assert lib.kv4_decode_workspace_bytes(2, 8, 256, 1) == 0
+    rows = 2 * 8 * 5
+    assert lib.kv4_decode_workspace_bytes(2, 8, 256, 5) == ((rows * 16 + 255) // 256) * 256 + rows * 256 * 4
+    s = lib.kv4_decode_default_splits(1, 4, 4096, 256)
+    assert 1 <= s <= 1024
+    assert lib.kv4_decode_default_splits(64, 8, 1, 64) == 1      # one tile: one split
+
+
+def _status(lib, st):
+    return st, lib.kv4_last_error_message().decode()
+
+
+def test_host_validation_rejects_without_gpu(lib):
+    d = desc(base=1 << 20)
+    p = ctypes.byref(d)
+    fake = ctypes.c_void_p(1 << 20)
+    # fmt mismatch
+    st, msg = _status(lib, lib.kv4_write(fake, fake, fake, 4, p, fake, 1, None))
+    assert st == 1 and "fmt" in msg
+    # unaligned k
+    st, _ = _status(lib, lib.kv4_write(ctypes.c_void_p((1 << 20) + 2), fake, fake, 4, p, fake, 0, None))
+    assert st == 1
+    # NVFP4 without global scale
+    st, msg = _status(lib, lib.kv4_write(fake, fake, fake, 4, p, None, 0, None))
+    assert st == 1 and "global" in msg
+    # zero tokens is a no-op
+    assert lib.kv4_write(None, None, None, 0, p, None, 0, None) == 0
+    # unsupported head_dim
+    d96 = desc(D=96, base=1 << 20)
+    assert lib.kv4_write(fake, fake, fake, 4, ctypes.byref(d96), fake, 0, None) == 2
+    # unaligned pool base
+    dmis = desc(base=(1 << 20) + 128)
+    assert lib.kv4_write(fake, fake, fake, 4, ctypes.byref(dmis), fake, 0, None) == 1
+    # decode: bad splits, bad head ratio, missing workspace
+    args = lambda **kw: dict(dict(q=fake, pool=p, g=fake, bt=fake, mp=8, sl=fake, B=2, Hq=12,
+                                  sm=0.0625, S=4, ws=None, wsb=0, out=fake, f32=1), **kw)
+
+    def dec(a):
+        return lib.kv4_decode_attention(a["q"], a["pool"], a["g"], a["bt"], a["mp"], a["sl"], a["B"],
+                                        a["Hq"], a["sm"], a["S"], a["ws"], a["wsb"], a["out"],
+                                        a["f32"], None)
+    assert dec(args(S=-1)) == 1
+    assert dec(args(S=2000)) == 1
+    assert dec(args(Hq=7)) == 1
+    assert dec(args(sm=float("nan"))) == 1
+    st, msg = _status(lib, dec(args()))
+    assert st == 1 and "workspace" in msg
+    assert dec(args(B=0)) == 0
+    # prefix: max_prefix_len beyond the table
+    assert lib.kv4_dequant_prefix(p, fake, fake, 2, fake, fake, 1, 1000, fake, fake, fake, None) == 1
+    assert lib.kv4_dequant_prefix(p, fake, fake, 2, fake, fake, 1, 0, fake, fake, fake, None) == 0
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert lib.kv4_status_str(s).decode().startswith("KV4_")
+
+
+def test_build_is_in_tree():
+    assert os.path.dirname(_build.LIB) == os.path.dirname(K.__file__)

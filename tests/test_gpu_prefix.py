@@ -1,0 +1,32 @@
+"""kv4_dequant_prefix on the GPU against the oracle: FP8 workspace bytes must
+match exactly (NVFP4 and INT4, ragged prefixes, zero-length prefixes)."""
+import numpy as np
+import pytest
+import torch
+
+import bit_paged_kv_kv4_gb300 as K
+import oracle
+from kv4_testlib import Case
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "int4"])
+@pytest.mark.parametrize("D", [64, 256])
+def test_prefix_bit_exact(fmt, D):
+    c = Case(fmt, 2, 4, D, [300, 17, 0, 129], 16 if D == 64 else 64, seed=11 + D)
+    prefix = np.array([250, 17, 0, 1], np.int32)
+    cu = np.concatenate([[0], np.cumsum(prefix)]).astype(np.int64)
+    s8 = (6 * c.g).astype(np.float32) if fmt == "nvfp4" else np.array([0.01, 0.02], np.float32)
+    spec, ref_pool = c.oracle_pool()
+    wk, wv = oracle.attention.dequant_prefix(ref_pool, spec, c.g, c.table, prefix, s8)
+    pool = c.gpu_pool()
+    total = int(prefix.sum())
+    gk = torch.full((total, c.Hkv, D), 0xEE, dtype=torch.uint8, device="cuda")
+    gv = torch.full_like(gk, 0xEE)
+    K.kv4_dequant_prefix(pool, c.d_g, torch.from_numpy(c.table).cuda(), torch.from_numpy(prefix).cuda(),
+                         torch.from_numpy(cu).cuda(), int(prefix.max()), torch.from_numpy(s8).cuda(), gk, gv)
+    torch.cuda.synchronize()
+    assert K.kv4_device_error() == 0
+    assert np.array_equal(gk.cpu().numpy(), wk)
+    assert np.array_equal(gv.cpu().numpy(), wv)

@@ -1,0 +1,111 @@
+"""kv4_write on the GPU against the oracle's encoder: packed codes and scales
+must match byte for byte (NVFP4 and INT4), including crafted rounding ties,
+zero blocks, saturating blocks and skipped / out-of-range slots."""
+import numpy as np
+import pytest
+import torch
+
+import bit_paged_kv_kv4_gb300 as K
+from kv4_testlib import Case, dev_bf16
+from oracle import formats as F
+from oracle import pool as OP
+from workloads import TINY, f32_to_bf16_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "int4"])
+@pytest.mark.parametrize("D,P", [(64, 16), (128, 32), (256, 64), (256, 1600)])
+def test_write_bit_exact(fmt, D, P):
+    c = Case(fmt, 2, 4, D, [37, 300, 1], P, seed=D + P, outlier_ch=(3, 77 % D))
+    pool = c.gpu_pool(fill=0xA5)
+    _, ref = c.oracle_pool(fill=0xA5)
+    got = pool.buffer.cpu().numpy()
+    assert K.kv4_device_error() == 0
+    diff = np.nonzero(got != ref)[0]
+    assert diff.size == 0, f"{diff.size} bytes differ, first at {diff[:8]}"
+
+
+def test_write_tiny_workload_exact():
+    w = TINY
+    L = int(w.seq_lens()[0])
+    num_pages, table = w.block_table(w.seq_lens())
+    k, v = w.kv_request(0, 0, L)
+    k, v = k[:, None], v[:, None]
+    from workloads import global_scale_from_amax, slots_for
+    g = np.array([global_scale_from_amax(np.abs(F.bf16_to_f32(k)).max()),
+                  global_scale_from_amax(np.abs(F.bf16_to_f32(v)).max())], np.float32)
+    slots = slots_for(table[0], w.page_size, np.arange(L))
+    spec = OP.PoolSpec("nvfp4", num_pages, w.page_size, 1, w.head_dim)
+    ref = OP.new_pool(spec, 0)
+    OP.write(ref, spec, k, v, slots, g)
+    pool = K.Pool("nvfp4", num_pages, w.page_size, 1, w.head_dim)
+    pool.buffer.zero_()
+    K.kv4_write(dev_bf16(k), dev_bf16(v), torch.from_numpy(slots).cuda(), pool, torch.from_numpy(g).cuda())
+    assert np.array_equal(pool.buffer.cpu().numpy(), ref)
+
+
+def _tie_rows(D=256):
+    """Rows whose blocks hit E4M3 and E2M1 rounding ties with g = 1."""
+    rows = []
+    # E4M3 ties: block amax = 6 * (midpoint of two E4M3 neighbours), exact in bf16
+    grid = F.e4m3_decode(np.arange(0x7F))
+    mids = (grid[:-1] + grid[1:]) / 2
+    for m in mids:
+        amax = np.float32(6.0 * m)
+        if F.bf16_to_f32(f32_to_bf16_bits(np.array([amax], np.float32)))[0] != amax:
+            continue
+        rows.append(np.full(16, amax / 3, np.float32))
+        rows[-1][0] = amax
+    # E2M1 ties: scale exactly 1 (amax 6), elements on every tie and neighbour
+    ties = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.25, -0.75, -5.0, 6.0, -6.0,
+                     1e-30, -1e-30, 0.0, -0.0], np.float32)
+    for sc in (1.0, 2.0 ** -6, 2.0 ** -9, 448.0 / 64):
+        rows.append(ties * np.float32(sc))
+    # all-zero block, tiny block (scale rounds to 0), huge block (saturating scale)
+    rows.append(np.zeros(16, np.float32))
+    rows.append(np.full(16, 1e-20, np.float32))
+    rows.append(np.linspace(-3e4, 3e4, 16).astype(np.float32))
+    blocks = np.stack(rows)
+    n = (len(blocks) + D // 16 - 1) // (D // 16) * (D // 16)
+    blocks = np.concatenate([blocks, np.zeros((n - len(blocks), 16), np.float32)])
+    return blocks.reshape(-1, D)
+
+
+@pytest.mark.parametrize("g", [1.0, 0.01, 3.0])
+def test_write_rounding_ties_exact(g):
+    x = f32_to_bf16_bits(_tie_rows())
+    T = x.shape[0]
+    k = x[:, None]
+    v = x[::-1].copy()[:, None]
+    spec = OP.PoolSpec("nvfp4", (T + 15) // 16, 16, 1, 256)
+    slots = np.arange(T, dtype=np.int64)
+    gs = np.array([g, g], np.float32)
+    ref = OP.new_pool(spec, 0)
+    OP.write(ref, spec, k, v, slots, gs)
+    pool = K.Pool("nvfp4", spec.num_pages, 16, 1, 256)
+    pool.buffer.zero_()
+    K.kv4_write(dev_bf16(k), dev_bf16(v), torch.from_numpy(slots).cuda(), pool, torch.from_numpy(gs).cuda())
+    got = pool.buffer.cpu().numpy()
+    diff = np.nonzero(got != ref)[0]
+    assert diff.size == 0, f"{diff.size} bytes differ, first at {diff[:8]}"
+
+
+def test_write_skips_negative_and_flags_out_of_range_slots():
+    c = Case("nvfp4", 1, 1, 64, [20], 16, seed=5)
+    slots = c.slots.copy()
+    slots[3] = -1
+    slots[5] = c.num_pages * 16 + 7          # beyond the pool: skipped, flagged
+    pool = K.Pool("nvfp4", c.num_pages, 16, 1, 64)
+    pool.buffer.fill_(0x5A)
+    g = torch.from_numpy(c.g).cuda()
+    K.kv4_device_error()
+    K.kv4_write(dev_bf16(c.k), dev_bf16(c.v), torch.from_numpy(slots).cuda(), pool, g)
+    assert K.kv4_device_error() == 4          # KV4_EBOUNDS
+    assert K.kv4_device_error() == 0          # cleared by the read
+    spec = OP.PoolSpec("nvfp4", c.num_pages, 16, 1, 64)
+    ref = OP.new_pool(spec, 0x5A)
+    keep = slots.copy()
+    keep[5] = -1
+    OP.write(ref, spec, c.k, c.v, keep, c.g)
+    assert np.array_equal(pool.buffer.cpu().numpy(), ref)

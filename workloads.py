@@ -25,9 +25,10 @@ E2M1_MAX, E4M3_MAX = 6.0, 448.0
 
 
 def f32_to_bf16_bits(x):
-    """float32 -> bf16 bit patterns (uint16), round to nearest even."""
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    """float32 -> bf16 bit patterns (uint16), round to nearest even (finite
+    inputs; uint32 arithmetic cannot overflow below the NaN range)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    u = (u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
     return u.astype(np.uint16)
 
 
@@ -122,6 +123,41 @@ class Workload:
 
     def sm_scale(self):
         return np.float32(1.0 / np.sqrt(self.head_dim))
+
+
+# --- device-side draws (large workloads) -----------------------------------------
+# At the 32K..1M sizes the host generator above is too slow (billions of
+# values), so the same distributions are drawn on the GPU by torch's seeded
+# Philox generator, one generator per (workload seed, request).  These are
+# inputs only; a test hands the oracle the slices it checks, copied to the host.
+def device_kv(w, b, L, device):
+    """bf16 [2, L, Hkv, D] (K then V) of request b, drawn on `device`."""
+    import torch
+    gen = torch.Generator(device=device).manual_seed(1_000_003 * (w.seed + 1) + b)
+    shape = (2, L, w.num_kv_heads, w.head_dim)
+    x = torch.randn(shape, generator=gen, device=device)
+    if w.dist == "student_t4":
+        chi = torch.zeros(shape, device=device)
+        for _ in range(4):
+            chi += torch.randn(shape, generator=gen, device=device) ** 2
+        x = x / torch.sqrt(chi / 4.0)
+    for h in range(w.num_kv_heads):
+        ch = w.outlier_channels(h)
+        if ch.size:
+            idx = torch.from_numpy(ch).to(device)
+            x[0, :, h, idx] *= w.outlier_scale
+            if w.outlier_kv == "kv":
+                x[1, :, h, idx] *= w.outlier_scale
+    return x.to(torch.bfloat16)
+
+
+def device_q(w, device, salt=0):
+    """bf16 [B, Hq, D] queries, plus bf16 [B, Hkv, D] K and V of one new token."""
+    import torch
+    gen = torch.Generator(device=device).manual_seed(7_000_003 * (w.seed + 1) + salt)
+    q = torch.randn((w.batch, w.num_q_heads, w.head_dim), generator=gen, device=device)
+    kv = torch.randn((2, w.batch, w.num_kv_heads, w.head_dim), generator=gen, device=device)
+    return q.to(torch.bfloat16), kv[0].to(torch.bfloat16), kv[1].to(torch.bfloat16)
 
 
 def global_scale_from_amax(amax):
