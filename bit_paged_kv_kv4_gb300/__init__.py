@@ -62,6 +62,8 @@ def _load(build_if_missing=False):
         "kv4_decode_attention": (i32, [vp, P, vp, vp, i32, vp, i32, i32, f32, i32, vp, i64, vp,
                                        i32, vp]),
         "kv4_dequant_prefix": (i32, [P, vp, vp, i32, vp, vp, i32, i32, vp, vp, vp, vp]),
+        "kv4_decode_attention_static_ws": (i32, [vp, P, vp, vp, i32, vp, i32, i32, f32, i32, vp,
+                                                 i32, vp]),
         "kv4_device_error": (i32, []),
         "kv4_status_str": (ctypes.c_char_p, [i32]),
         "kv4_last_error_message": (ctypes.c_char_p, []),
@@ -157,6 +159,19 @@ def kv4_decode_attention(q, pool, layer_global_scale, block_table, seq_lens, sm_
         _ptr(seq_lens), B, Hq, float(sm_scale), int(num_splits), _ptr(workspace), ws_bytes,
         _ptr(out), 1 if out.dtype == torch.float32 else 0, _stream(stream))
     _check(st, "kv4_decode_attention")
+
+
+def kv4_decode_attention_static_ws(q, pool, layer_global_scale, block_table, seq_lens, sm_scale,
+                                   out, num_splits=0, stream=None):
+    """kv4_decode_attention without a caller workspace, for callers that cannot
+    allocate device memory: the split scratch is the library's fixed 8 MiB
+    device array, shared by every call (serialise calls on the GPU)."""
+    B, Hq, D = q.shape
+    st = _load().kv4_decode_attention_static_ws(
+        _ptr(q), pool.ref, _ptr(layer_global_scale), _ptr(block_table), block_table.shape[1],
+        _ptr(seq_lens), B, Hq, float(sm_scale), int(num_splits), _ptr(out),
+        1 if out.dtype == torch.float32 else 0, _stream(stream))
+    _check(st, "kv4_decode_attention_static_ws")
 
 
 def kv4_dequant_prefix(pool, layer_global_scale, block_table, prefix_lens, cu_prefix,

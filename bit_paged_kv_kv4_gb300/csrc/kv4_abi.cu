@@ -146,6 +146,8 @@ int64_t align256(int64_t x) { return (x + 255) / 256 * 256; }
 
 }  // namespace
 
+void kv4::set_error_message(const char* msg) { g_msg = msg; }
+
 extern "C" {
 
 int64_t kv4_pool_chunk_bytes(const kv4_pool* pool) {

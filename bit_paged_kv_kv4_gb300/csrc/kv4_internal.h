@@ -59,6 +59,8 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& map, cudaStrea
 cudaError_t launch_write(const WriteArgs& a, cudaStream_t st);
 cudaError_t launch_prefix(const PrefixArgs& a, cudaStream_t st);
 int decode_tile_tokens();
+// Sets the message kv4_last_error_message() returns on this thread.
+void set_error_message(const char* msg);
 int decode_box_rows();
 
 }  // namespace kv4

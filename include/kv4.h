@@ -184,6 +184,41 @@ kv4_status kv4_dequant_prefix(const kv4_pool* pool,
                               int32_t max_prefix_len, const float* fp8_scale,
                               void* fp8_k, void* fp8_v, void* stream);
 
+/*
+ * kv4_decode_attention_static_ws -- kv4_decode_attention for callers that
+ * cannot allocate device memory.  The pages have no counterpart of this call;
+ * it exists for library users, not for the method.
+ *
+ * Some callers cannot call cudaMalloc: code hosted by a framework that owns
+ * every device allocation (for example an inference-server plugin held to a
+ * fixed memory budget), or a decode loop that cannot take the device-wide
+ * synchronisation an allocation may cause.  They pass the same inputs and
+ * output as to kv4_decode_attention, without a workspace: the split partials
+ * go to a scratch array inside the library instead.
+ *   - The scratch is a fixed 8 MiB (8,388,608-byte) device array that every GPU
+ *     loading the library holds until the process exits.  A call whose
+ *     kv4_decode_workspace_bytes(batch, num_q_heads, head_dim, splits) exceeds
+ *     it returns KV4_EINVAL (kv4_last_error_message gives both sizes) and
+ *     launches nothing; num_splits = 0 picks kv4_decode_default_splits() as
+ *     usual.  One split needs no scratch at all.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and keeps it; make that
+ *     first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents.
+ *     Nothing in it needs to start at zero (each call writes every partial
+ *     before reading it), but calls whose kernels overlap on the GPU -- on two
+ *     streams, or from two host threads -- race on it: serialise them.
+ *   - It allocates and frees nothing.  Results are bitwise those of
+ *     kv4_decode_attention with the same num_splits.
+ */
+kv4_status kv4_decode_attention_static_ws(const void* q, const kv4_pool* pool,
+                                          const float* layer_global_scale,
+                                          const int32_t* block_table, int32_t max_pages,
+                                          const int32_t* seq_lens, int32_t batch,
+                                          int32_t num_q_heads, float sm_scale,
+                                          int32_t num_splits, void* out,
+                                          int32_t out_is_fp32, void* stream);
+
 /* Read and clear the current device's error word (the first kv4_status a
  * kernel recorded since the last call, KV4_OK if none).  Synchronises the
  * device.  Returns KV4_ECUDA if the read itself fails. */
