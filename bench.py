@@ -182,6 +182,7 @@ class Setup:
             K.kv4_write(kvs[b][0], kvs[b][1], slots, self.pool, self.g)
         self.kv = kvs if keep_kv else None
         del kvs
+        torch.cuda.empty_cache()
         # the step's inputs: q, and each request's newest token (position L-1)
         self.q, self.k_new, self.v_new = W.device_q(w, device, salt=seed_offset)
         self.slot_new = torch.from_numpy(np.array(

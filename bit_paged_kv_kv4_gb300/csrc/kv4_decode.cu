@@ -37,10 +37,20 @@ namespace kv4 {
 
 namespace {
 
-constexpr int kTT = 64;        // tokens per tile
-constexpr int kSub = 16;       // rows per TMA box (sub-tile; never crosses a page)
-constexpr int kNW = 4;         // warps per CTA
-constexpr int kNS = 2;         // stages per warp
+#ifndef KV4_DECODE_TT
+#define KV4_DECODE_TT 32
+#endif
+#ifndef KV4_DECODE_NS
+#define KV4_DECODE_NS 3
+#endif
+#ifndef KV4_DECODE_MINB
+#define KV4_DECODE_MINB 2
+#endif
+constexpr int kTT = KV4_DECODE_TT;     // tokens per tile (per warp and stage)
+constexpr int kSub = 16;               // rows per TMA box (sub-tile; never crosses a page)
+constexpr int kNW = 4;                 // warps per CTA
+constexpr int kNS = KV4_DECODE_NS;     // stages per warp
+constexpr int kMinBlocks = KV4_DECODE_MINB;   // CTAs resident per SM (register budget)
 constexpr uint32_t kFull = 0xffffffffu;
 
 template <int D, int FMT>
@@ -49,7 +59,6 @@ struct Geo {
   static constexpr int SB = (FMT == KV4_NVFP4) ? D / 16 : 4;   // scale bytes per row
   static constexpr int KB = D / 8;                             // K code bytes per thread per token
   static constexpr int VB = D / 16;                            // V code bytes per thread per token
-  static constexpr int KS = D / 16;                            // k-steps of QK^T
   static constexpr int MT = D / 16;                            // m-tiles of PV
   static constexpr int STAGE_USED = kTT * (2 * RB + 2 * SB);
   static constexpr int STAGE = (STAGE_USED + 1023) / 1024 * 1024;
@@ -89,10 +98,6 @@ __device__ __forceinline__ uint32_t load_scale_bytes(uint32_t addr) {
   else return lds8(addr);
 }
 
-__device__ __forceinline__ uint32_t bcast_e4m3_f16x2(uint32_t code) {
-  return e4m3x2_to_f16x2((code & 0xFFu) * 0x0101u);
-}
-
 // INT4 two's-complement nibbles at bits 0-3 and 16-19 of `x` -> f16x2 codes.
 __device__ __forceinline__ uint32_t int4_lo_pair(uint32_t x) {
   const uint32_t h = (x & 0x000F000Fu) ^ 0x64086408u;    // 1024 + (n ^ 8)
@@ -119,10 +124,11 @@ __device__ __forceinline__ void store_out4(void* out, int out_f32, int64_t idx, 
 }  // namespace
 
 template <int D, int FMT>
-__global__ void __launch_bounds__(kNW * 32, 1)
+__global__ void __launch_bounds__(kNW * 32, kMinBlocks)
 decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap) {
   using Gm = Geo<D, FMT>;
-  constexpr int RB = Gm::RB, SB = Gm::SB, KB = Gm::KB, VB = Gm::VB, KS = Gm::KS, MT = Gm::MT;
+  constexpr int RB = Gm::RB, SB = Gm::SB, KB = Gm::KB, VB = Gm::VB, MT = Gm::MT;
+  constexpr int NM = kTT / 16;            // 16-token groups per tile (QK m-tiles = PV k-groups)
   extern __shared__ uint8_t smem_raw[];
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -198,26 +204,29 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
       const uint32_t st = ring + (i % kNS) * Gm::STAGE;
       const uint32_t bar = bars + 8 * (i % kNS);
       mbar_arrive_expect_tx(bar, nsub * kSub * (2 * RB + 2 * SB));
-      for (int u = 0; u < nsub; ++u) {
-        int page = pages[u];
-        if (page < 0 || page >= a.num_pages) {
-          set_error(a.err, KV4_EBOUNDS);
-          page = 0;
+#pragma unroll
+      for (int u = 0; u < kTT / kSub; ++u) {
+        if (u < nsub) {
+          int page = pages[u];
+          if (page < 0 || page >= a.num_pages) {
+            set_error(a.err, KV4_EBOUNDS);
+            page = 0;
+          }
+          const int off = (t0 + u * kSub) % a.P;
+          const int64_t chunk = (static_cast<int64_t>(page) * a.Hkv + h) * a.chunk_bytes;
+          const int row = static_cast<int>(chunk / RB) + off;
+          tma_load_2d(st + u * kSub * RB, &tmap, 0, row, bar, pol);
+          tma_load_2d(st + Gm::OFF_VC + u * kSub * RB, &tmap, 0, row + a.P, bar, pol);
+          const uint8_t* sc = pool + chunk + static_cast<int64_t>(a.P) * 2 * RB;
+          bulk_load(st + Gm::OFF_KS + u * kSub * SB, sc + off * SB, kSub * SB, bar, pol);
+          bulk_load(st + Gm::OFF_VS + u * kSub * SB, sc + static_cast<int64_t>(a.P) * SB + off * SB,
+                    kSub * SB, bar, pol);
         }
-        const int off = (t0 + u * kSub) % a.P;
-        const int64_t chunk = (static_cast<int64_t>(page) * a.Hkv + h) * a.chunk_bytes;
-        const int row = static_cast<int>(chunk / RB) + off;
-        tma_load_2d(st + u * kSub * RB, &tmap, 0, row, bar, pol);
-        tma_load_2d(st + Gm::OFF_VC + u * kSub * RB, &tmap, 0, row + a.P, bar, pol);
-        const uint8_t* sc = pool + chunk + static_cast<int64_t>(a.P) * 2 * RB;
-        bulk_load(st + Gm::OFF_KS + u * kSub * SB, sc + off * SB, kSub * SB, bar, pol);
-        bulk_load(st + Gm::OFF_VS + u * kSub * SB, sc + static_cast<int64_t>(a.P) * SB + off * SB,
-                  kSub * SB, bar, pol);
       }
     }
   };
 
-  // ---- query fragments (A operand of QK^T), f16, power-of-two prescaled ----
+  // ---- query fragments (B operand of S^T = K q^T), f16, power-of-two prescaled
   // Thread (grp, tig) holds query row g0+grp, head-dim range [2*KB*tig, 2*KB*(tig+1)).
   constexpr int QN = 2 * KB;                 // query elements per thread
   float qf[QN];
@@ -248,20 +257,20 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
     frexpf(qmax / 16384.f, &e);
     qpre = ldexpf(1.f, -e);
   }
-  uint32_t qa[QN / 2];
+  uint32_t qb[QN / 2];
   if constexpr (FMT == KV4_NVFP4) {
-    // k-step kk: pair (2tig, 2tig+1) <-> d = base + 4kk + {0,1}; (2tig+8, +9) <-> + {2,3}
+    // k-step kk: k (2tig, 2tig+1) <-> d = base + 4kk + {0,1}; (2tig+8, +9) <-> + {2,3}
 #pragma unroll
-    for (int i = 0; i < QN / 2; ++i) qa[i] = pack_f16x2(qf[2 * i] * qpre, qf[2 * i + 1] * qpre);
+    for (int i = 0; i < QN / 2; ++i) qb[i] = pack_f16x2(qf[2 * i] * qpre, qf[2 * i + 1] * qpre);
   } else {
     // per 8 elements e: kk even: (e0,e4), (e1,e5); kk odd: (e2,e6), (e3,e7)
 #pragma unroll
     for (int j = 0; j < QN / 8; ++j) {
       const float* e = qf + 8 * j;
-      qa[4 * j + 0] = pack_f16x2(e[0] * qpre, e[4] * qpre);
-      qa[4 * j + 1] = pack_f16x2(e[1] * qpre, e[5] * qpre);
-      qa[4 * j + 2] = pack_f16x2(e[2] * qpre, e[6] * qpre);
-      qa[4 * j + 3] = pack_f16x2(e[3] * qpre, e[7] * qpre);
+      qb[4 * j + 0] = pack_f16x2(e[0] * qpre, e[4] * qpre);
+      qb[4 * j + 1] = pack_f16x2(e[1] * qpre, e[5] * qpre);
+      qb[4 * j + 2] = pack_f16x2(e[2] * qpre, e[6] * qpre);
+      qb[4 * j + 3] = pack_f16x2(e[3] * qpre, e[7] * qpre);
     }
   }
 
@@ -269,14 +278,14 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
   const float gv = (FMT == KV4_NVFP4) ? __ldg(a.gscale + 1) : 1.f;
   const float qk_scale = a.sm_scale * gk * 1.4426950408889634f / qpre;   // base-2 logits
 
-  // ---- running softmax state (base 2), for head g0 + grp --------------------
+  // ---- running softmax state (base 2), for heads g0 + 2tig + c, c = 0, 1 ----
   // m_x: running max of the logits x_t, l_run = sum 2^(x_t - m_x) (partial
   // over this thread's tokens).  The PV weights are w_t = 2^(y_t - m_y) with
   // y_t = x_t (NVFP4) or x_t + log2 s_V(t) (INT4: the per-token V scale rides
   // in the exponent, so every f16 operand stays in [0, 1]);
   // out = 2^(m_y - m_x) * sum_t w_t code_t / l.
-  float m_x = -INFINITY, m_y = -INFINITY;
-  float l_run = 0.f;
+  float m_x[2] = {-INFINITY, -INFINITY}, m_y[2] = {-INFINITY, -INFINITY};
+  float l_run[2] = {0.f, 0.f};
   float o[MT][4];
 #pragma unroll
   for (int mi = 0; mi < MT; ++mi) o[mi][0] = o[mi][1] = o[mi][2] = o[mi][3] = 0.f;
@@ -297,104 +306,148 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
     const int valid = min(kTT, L - t0);
     const uint32_t sK = st, sV = st + Gm::OFF_VC, sKs = st + Gm::OFF_KS, sVs = st + Gm::OFF_VS;
 
-    // -------- scores S[g][t] for the 64 tokens: 8 n-tiles of 8 tokens -----
-    float sacc[kTT / 8][4];
+    // -------- S^T[t][g] = K q^T: NM m-tiles of 16 tokens ----------------------
+    // A = dequantised K (rows: tokens 16m+grp and 16m+grp+8), B = q^T.
+    // sacc[m]: c0 = (16m+grp, head 2tig), c1 = (16m+grp, 2tig+1),
+    //          c2 = (16m+grp+8, 2tig),    c3 = (16m+grp+8, 2tig+1)
+    float sacc[NM][4];
+    uint32_t kw[NM][2][KB / 4];
 #pragma unroll
-    for (int nt = 0; nt < kTT / 8; ++nt) {
-      sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
-      const int r = nt * 8 + grp;               // this thread's K token (B column)
-      uint32_t kw[KB / 4];
-      load_row_bytes<RB, KB>(sK, r, KB * tig, kw);
-      if constexpr (FMT == KV4_NVFP4) {
-        constexpr int NB = D / 64;              // block scales this thread needs
-        const uint32_t sc = load_scale_bytes<NB>(sKs + r * SB + NB * tig);
-        uint32_t hs[NB];
+    for (int m = 0; m < NM; ++m) {
+      sacc[m][0] = sacc[m][1] = sacc[m][2] = sacc[m][3] = 0.f;
+      load_row_bytes<RB, KB>(sK, 16 * m + grp, KB * tig, kw[m][0]);
+      load_row_bytes<RB, KB>(sK, 16 * m + grp + 8, KB * tig, kw[m][1]);
+    }
+    if constexpr (FMT == KV4_NVFP4) {
+      constexpr int NB = D / 64;              // block scales per token this thread needs
+      // hs[m][r][j]: f16x2 broadcast of block scale j of token 16m+grp+8r
+      uint32_t hs[NM][2][NB < 2 ? 2 : NB];
 #pragma unroll
-        for (int j = 0; j < NB; ++j) hs[j] = bcast_e4m3_f16x2(sc >> (8 * j));
+      for (int m = 0; m < NM; ++m) {
 #pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
-          const uint32_t two = kw[kk >> 1] >> (16 * (kk & 1));
-          const uint32_t b0 = hmul2(e2m1x2_to_f16x2(two), hs[kk >> 2]);
-          const uint32_t b1 = hmul2(e2m1x2_to_f16x2(two >> 8), hs[kk >> 2]);
-          mma_f16_16816(sacc[nt], qa[2 * kk], 0u, qa[2 * kk + 1], 0u, b0, b1);
+        for (int r = 0; r < 2; ++r) {
+          const uint32_t sc = load_scale_bytes<NB>(sKs + (16 * m + grp + 8 * r) * SB + NB * tig);
+#pragma unroll
+          for (int j = 0; j < NB; j += 2)   // bytes [s_j s_j s_j+1 s_j+1] -> two broadcasts
+            e4m3x4_to_f16x2x2(prmt(sc, 0u, (j == 0) ? 0x1100u : 0x3322u), hs[m][r][j], hs[m][r][j + 1]);
         }
-      } else {
+      }
 #pragma unroll
-        for (int j = 0; j < KB / 4; ++j) {
-          const uint32_t w = kw[j], w8 = kw[j] >> 8;
-          mma_f16_16816(sacc[nt], qa[4 * j + 0], 0u, qa[4 * j + 1], 0u, int4_lo_pair(w),
-                        int4_hi_pair(w));
-          mma_f16_16816(sacc[nt], qa[4 * j + 2], 0u, qa[4 * j + 3], 0u, int4_lo_pair(w8),
-                        int4_hi_pair(w8));
+      for (int j = 0; j < KB / 4; ++j) {      // word j: k-steps 2j (bytes 0, 1) and 2j+1 (bytes 2, 3)
+#pragma unroll
+        for (int m = 0; m < NM; ++m) {
+          uint32_t c0[4], c1[4];
+          e2m1x8_to_f16x2x4(kw[m][0][j], c0);
+          e2m1x8_to_f16x2x4(kw[m][1][j], c1);
+          const uint32_t s0 = hs[m][0][j >> 1], s1 = hs[m][1][j >> 1];
+          mma_f16_16816(sacc[m], hmul2(c0[0], s0), hmul2(c1[0], s1), hmul2(c0[1], s0),
+                        hmul2(c1[1], s1), qb[4 * j], qb[4 * j + 1]);
+          mma_f16_16816(sacc[m], hmul2(c0[2], s0), hmul2(c1[2], s1), hmul2(c0[3], s0),
+                        hmul2(c1[3], s1), qb[4 * j + 2], qb[4 * j + 3]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < KB / 4; ++j) {
+#pragma unroll
+        for (int m = 0; m < NM; ++m) {
+          const uint32_t w0 = kw[m][0][j], w1 = kw[m][1][j];
+          mma_f16_16816(sacc[m], int4_lo_pair(w0), int4_lo_pair(w1), int4_hi_pair(w0),
+                        int4_hi_pair(w1), qb[4 * j + 0], qb[4 * j + 1]);
+        }
+#pragma unroll
+        for (int m = 0; m < NM; ++m) {
+          const uint32_t w0 = kw[m][0][j] >> 8, w1 = kw[m][1][j] >> 8;
+          mma_f16_16816(sacc[m], int4_lo_pair(w0), int4_lo_pair(w1), int4_hi_pair(w0),
+                        int4_hi_pair(w1), qb[4 * j + 2], qb[4 * j + 3]);
         }
       }
     }
 
     // -------- online softmax (base 2) over this tile ----------------------
-    // sacc[nt][0..1]: head g0+grp, tokens nt*8 + 2*tig + {0,1}
-    float yv[kTT / 8][2];            // INT4: exponent of the PV weight
-    float tmx = -INFINITY, tmy = -INFINITY;
+    // token of sacc[m][2r + c]: 16m + grp + 8r; head 2tig + c
+    float yv[NM][4];                 // INT4: exponent of the PV weight
+    float tmx[2] = {-INFINITY, -INFINITY}, tmy[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-    for (int nt = 0; nt < kTT / 8; ++nt) {
+    for (int m = 0; m < NM; ++m) {
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int t = nt * 8 + 2 * tig + e;
-        float x = sacc[nt][e] * qk_scale;
+      for (int r = 0; r < 2; ++r) {
+        const int t = 16 * m + grp + 8 * r;
+        float sk = 1.f, lsv = 0.f;
+        bool vok = true;
         if constexpr (FMT == KV4_INT4_PTH) {
-          const float sk = __uint_as_float(lds32(sKs + 4 * t));
+          sk = __uint_as_float(lds32(sKs + 4 * t));
           const float sv = __uint_as_float(lds32(sVs + 4 * t));
-          x *= sk;
-          const float y = x + fast_log2(sv);          // sv == 0 -> -inf: no V weight
-          yv[nt][e] = (t < valid && sv > 0.f) ? y : -INFINITY;
-          tmy = fmaxf(tmy, yv[nt][e]);
+          lsv = fast_log2(sv);                // sv == 0: no V weight
+          vok = sv > 0.f;
         }
-        x = (t < valid) ? x : -INFINITY;
-        sacc[nt][e] = x;
-        tmx = fmaxf(tmx, x);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          float x = sacc[m][2 * r + c] * qk_scale * sk;
+          x = (t < valid) ? x : -INFINITY;
+          sacc[m][2 * r + c] = x;
+          tmx[c] = fmaxf(tmx[c], x);
+          if constexpr (FMT == KV4_INT4_PTH) {
+            yv[m][2 * r + c] = (t < valid && vok) ? x + lsv : -INFINITY;
+            tmy[c] = fmaxf(tmy[c], yv[m][2 * r + c]);
+          }
+        }
       }
     }
-    tmx = fmaxf(tmx, __shfl_xor_sync(kFull, tmx, 1));
-    tmx = fmaxf(tmx, __shfl_xor_sync(kFull, tmx, 2));
-    const float mx_new = fmaxf(m_x, tmx);            // finite: valid >= 1
-    const float corr_x = fast_exp2(m_x - mx_new);    // 0 when m_x == -inf
-    m_x = mx_new;
-    float corr_y = corr_x, my_new = mx_new;
-    if constexpr (FMT == KV4_INT4_PTH) {
-      tmy = fmaxf(tmy, __shfl_xor_sync(kFull, tmy, 1));
-      tmy = fmaxf(tmy, __shfl_xor_sync(kFull, tmy, 2));
-      my_new = fmaxf(m_y, tmy);
-      corr_y = (my_new == -INFINITY) ? 1.f : fast_exp2(m_y - my_new);
-    }
-    m_y = my_new;
-    float psum = 0.f;
-    uint32_t pb[kTT / 16][2], pl[kTT / 16][2];      // f16 hi and lo parts of the PV weights
+    float corr_x[2], corr_y[2], mx_new[2], my_new[2];
 #pragma unroll
-    for (int nt = 0; nt < kTT / 8; ++nt) {
-      const float p0 = fast_exp2(sacc[nt][0] - mx_new);
-      const float p1 = fast_exp2(sacc[nt][1] - mx_new);
-      psum += p0 + p1;
-      float w0 = p0, w1 = p1;
+    for (int c = 0; c < 2; ++c) {
+#pragma unroll
+      for (int o2 = 4; o2 < 32; o2 <<= 1) tmx[c] = fmaxf(tmx[c], __shfl_xor_sync(kFull, tmx[c], o2));
+      mx_new[c] = fmaxf(m_x[c], tmx[c]);            // finite: valid >= 1
+      corr_x[c] = fast_exp2(m_x[c] - mx_new[c]);     // 0 when m_x == -inf
+      m_x[c] = mx_new[c];
+      corr_y[c] = corr_x[c];
+      my_new[c] = mx_new[c];
       if constexpr (FMT == KV4_INT4_PTH) {
-        w0 = (my_new == -INFINITY) ? 0.f : fast_exp2(yv[nt][0] - my_new);
-        w1 = (my_new == -INFINITY) ? 0.f : fast_exp2(yv[nt][1] - my_new);
-      }
-      const uint32_t hi = pack_f16x2(w0, w1);
-      const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi));
-      pb[nt >> 1][nt & 1] = hi;
-      pl[nt >> 1][nt & 1] = pack_f16x2(w0 - hf.x, w1 - hf.y);
-    }
-    l_run = l_run * corr_x + psum;
-    // O^T columns are heads 2*tig, 2*tig+1: fetch their correction factors.
-    const float ca = __shfl_sync(kFull, corr_y, (2 * tig) * 4);
-    const float cb = __shfl_sync(kFull, corr_y, (2 * tig + 1) * 4);
 #pragma unroll
-    for (int mi = 0; mi < MT; ++mi) {
-      o[mi][0] *= ca; o[mi][1] *= cb; o[mi][2] *= ca; o[mi][3] *= cb;
+        for (int o2 = 4; o2 < 32; o2 <<= 1) tmy[c] = fmaxf(tmy[c], __shfl_xor_sync(kFull, tmy[c], o2));
+        my_new[c] = fmaxf(m_y[c], tmy[c]);
+        corr_y[c] = (my_new[c] == -INFINITY) ? 1.f : fast_exp2(m_y[c] - my_new[c]);
+      }
+      m_y[c] = my_new[c];
+    }
+    // P^T operand of PV per 16-token group m: b0 <- tokens (2tig, 2tig+1) of head grp,
+    // b1 <- tokens (8+2tig, 8+2tig+1); transposed from the score layout with movmatrix.
+    uint32_t pb[NM][2], pl[NM][2];
+    float psum[2] = {0.f, 0.f};
+#pragma unroll
+    for (int m = 0; m < NM; ++m) {
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        float w[2];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const float p = fast_exp2(sacc[m][2 * r + c] - mx_new[c]);
+          psum[c] += p;
+          w[c] = p;
+          if constexpr (FMT == KV4_INT4_PTH)
+            w[c] = (my_new[c] == -INFINITY) ? 0.f : fast_exp2(yv[m][2 * r + c] - my_new[c]);
+        }
+        const uint32_t hi = pack_f16x2(w[0], w[1]);
+        const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+        const uint32_t lo = pack_f16x2(w[0] - hf.x, w[1] - hf.y);
+        pb[m][r] = movmatrix_trans(hi);
+        pl[m][r] = movmatrix_trans(lo);
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < 2; ++c) l_run[c] = l_run[c] * corr_x[c] + psum[c];
+    if (__any_sync(kFull, corr_y[0] != 1.f || corr_y[1] != 1.f)) {
+#pragma unroll
+      for (int mi = 0; mi < MT; ++mi) {
+        o[mi][0] *= corr_y[0]; o[mi][1] *= corr_y[1]; o[mi][2] *= corr_y[0]; o[mi][3] *= corr_y[1];
+      }
     }
 
-    // -------- O^T += V^T P^T: 4 k-groups of 16 tokens ----------------------
+    // -------- O^T += V^T P^T: NM k-groups of 16 tokens -------------------------
 #pragma unroll
-    for (int kg = 0; kg < kTT / 16; ++kg) {
+    for (int kg = 0; kg < NM; ++kg) {
       const int ta = kg * 16 + 2 * tig;       // tokens ta, ta+1 (k 2tig..) and ta+8, ta+9
       uint32_t wa[VB / 4], wb[VB / 4], wc[VB / 4], wd[VB / 4];
       load_row_bytes<RB, VB>(sV, ta, VB * grp, wa);
@@ -405,23 +458,23 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
         // block scales of the thread's head-dim range, per token
         constexpr int NVB = (VB >= 8) ? VB / 8 : 1;
         const int blk0 = (VB * grp) / 8;
-        const uint32_t so = blk0;
-        const uint32_t xa = load_scale_bytes<NVB>(sVs + ta * SB + so);
-        const uint32_t xb = load_scale_bytes<NVB>(sVs + (ta + 1) * SB + so);
-        const uint32_t xc = load_scale_bytes<NVB>(sVs + (ta + 8) * SB + so);
-        const uint32_t xd = load_scale_bytes<NVB>(sVs + (ta + 9) * SB + so);
+        const uint32_t xa = load_scale_bytes<NVB>(sVs + ta * SB + blk0);
+        const uint32_t xb = load_scale_bytes<NVB>(sVs + (ta + 1) * SB + blk0);
+        const uint32_t xc = load_scale_bytes<NVB>(sVs + (ta + 8) * SB + blk0);
+        const uint32_t xd = load_scale_bytes<NVB>(sVs + (ta + 9) * SB + blk0);
         // mask tokens past the end: a zero scale zeroes the (finite) codes
         const uint32_t ma = (ta < valid) ? 0xFFFFu : 0u, mb = (ta + 1 < valid) ? 0xFFFF0000u : 0u;
         const uint32_t mc = (ta + 8 < valid) ? 0xFFFFu : 0u, md = (ta + 9 < valid) ? 0xFFFF0000u : 0u;
-        uint32_t sab[NVB], scd[NVB];
-#pragma unroll
-        for (int j = 0; j < NVB; ++j) {
-          const uint32_t fa = e4m3x2_to_f16x2((xa >> (8 * j)) & 0xFFu);
-          const uint32_t fb = e4m3x2_to_f16x2((xb >> (8 * j)) & 0xFFu);
-          const uint32_t fc = e4m3x2_to_f16x2((xc >> (8 * j)) & 0xFFu);
-          const uint32_t fd = e4m3x2_to_f16x2((xd >> (8 * j)) & 0xFFu);
-          sab[j] = (prmt(fa, fb, 0x5410u) & (ma | mb));
-          scd[j] = (prmt(fc, fd, 0x5410u) & (mc | md));
+        uint32_t sab[2], scd[2];
+        {
+          // each token's NVB scale bytes -> f16 (one conversion per token pair of bytes)
+          uint32_t fa, fb, fc, fd;
+          e4m3x4_to_f16x2x2(xa | (xb << 16), fa, fb);
+          e4m3x4_to_f16x2x2(xc | (xd << 16), fc, fd);
+          sab[0] = prmt(fa, fb, 0x5410u) & (ma | mb);   // block 0: (s(ta), s(tb))
+          scd[0] = prmt(fc, fd, 0x5410u) & (mc | md);
+          sab[1] = prmt(fa, fb, 0x7632u) & (ma | mb);   // block 1 (NVB == 2)
+          scd[1] = prmt(fc, fd, 0x7632u) & (mc | md);
         }
 #pragma unroll
         for (int j = 0; j < VB / 4; ++j) {
@@ -429,14 +482,19 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
           const uint32_t hab = ((wa[j] >> 4) & 0x0F0F0F0Fu) | (wb[j] & 0xF0F0F0F0u);
           const uint32_t lcd = (wc[j] & 0x0F0F0F0Fu) | ((wd[j] << 4) & 0xF0F0F0F0u);
           const uint32_t hcd = ((wc[j] >> 4) & 0x0F0F0F0Fu) | (wd[j] & 0xF0F0F0F0u);
+          uint32_t vl[4], vh[4], ul[4], uh[4];
+          e2m1x8_to_f16x2x4(lab, vl);
+          e2m1x8_to_f16x2x4(hab, vh);
+          e2m1x8_to_f16x2x4(lcd, ul);
+          e2m1x8_to_f16x2x4(hcd, uh);
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            const int mi = 4 * j + m;
+          for (int mm = 0; mm < 4; ++mm) {
+            const int mi = 4 * j + mm;
             const int bj = (VB * grp + mi) / 8 - blk0;
-            const uint32_t a0 = hmul2(e2m1x2_to_f16x2(lab >> (8 * m)), sab[bj]);
-            const uint32_t a1 = hmul2(e2m1x2_to_f16x2(hab >> (8 * m)), sab[bj]);
-            const uint32_t a2 = hmul2(e2m1x2_to_f16x2(lcd >> (8 * m)), scd[bj]);
-            const uint32_t a3 = hmul2(e2m1x2_to_f16x2(hcd >> (8 * m)), scd[bj]);
+            const uint32_t a0 = hmul2(vl[mm], sab[bj]);
+            const uint32_t a1 = hmul2(vh[mm], sab[bj]);
+            const uint32_t a2 = hmul2(ul[mm], scd[bj]);
+            const uint32_t a3 = hmul2(uh[mm], scd[bj]);
             mma_f16_16816(o[mi], a0, a1, a2, a3, pb[kg][0], pb[kg][1]);
             mma_f16_16816(o[mi], a0, a1, a2, a3, pl[kg][0], pl[kg][1]);
           }
@@ -445,9 +503,9 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
 #pragma unroll
         for (int j = 0; j < VB / 4; ++j) {
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            const int mi = 4 * j + m;
-            const uint32_t sel = m | (m << 4) | ((4 + m) << 8) | ((4 + m) << 12);
+          for (int mm = 0; mm < 4; ++mm) {
+            const int mi = 4 * j + mm;
+            const uint32_t sel = mm | (mm << 4) | ((4 + mm) << 8) | ((4 + mm) << 12);
             const uint32_t xab = prmt(wa[j], wb[j], sel);
             const uint32_t xcd = prmt(wc[j], wd[j], sel);
             const uint32_t a0 = int4_lo_pair(xab), a1 = int4_hi_pair(xab);
@@ -464,17 +522,23 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
   if (timed_out && lane == 0) set_error(a.err, KV4_ETIMEOUT);
 
   // ---- merge the warps' states in shared memory, fixed order --------------
-  l_run += __shfl_xor_sync(kFull, l_run, 1);
-  l_run += __shfl_xor_sync(kFull, l_run, 2);
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+#pragma unroll
+    for (int o2 = 4; o2 < 32; o2 <<= 1) l_run[c] += __shfl_xor_sync(kFull, l_run[c], o2);
+  }
   __syncthreads();   // every warp finished reading its ring
   float* sO = reinterpret_cast<float*>(smem_raw + (base - smem_u32(smem_raw)));
   float* sMx = sO + kNW * 8 * D;
   float* sMy = sMx + kNW * 8;
   float* sL = sMy + kNW * 8;
-  if (tig == 0) {
-    sMx[warp * 8 + grp] = m_x;
-    sMy[warp * 8 + grp] = m_y;
-    sL[warp * 8 + grp] = l_run;
+  if (grp == 0) {
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      sMx[warp * 8 + 2 * tig + c] = m_x[c];
+      sMy[warp * 8 + 2 * tig + c] = m_y[c];
+      sL[warp * 8 + 2 * tig + c] = l_run[c];
+    }
   }
   __syncthreads();
   {

@@ -76,6 +76,29 @@ __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
   return r;
 }
 
+// Four bytes of E2M1 code pairs -> four f16x2 (byte i -> r[i], low nibble ->
+// low half), exact.  Unpacking the word into byte registers in one PTX block
+// lets each conversion read its byte directly (no separate extraction).
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&r)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(w));
+}
+
+// Two pairs of E4M3 codes (16-bit halves of `w`) -> two f16x2, exact:
+// r0 = (w.byte0, w.byte1), r1 = (w.byte2, w.byte3).
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& r0, uint32_t& r1) {
+  asm("{\n\t.reg .b16 h0, h1;\n\t"
+      "mov.b32 {h0, h1}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, h0;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h1;\n\t}"
+      : "=r"(r0), "=r"(r1) : "r"(w));
+}
+
 // E2M1 code (low nibble) -> FP32, exact.
 __device__ __forceinline__ float e2m1_to_f32(uint32_t code) {
   uint32_t h2 = e2m1x2_to_f16x2(code & 0xFu);
@@ -121,6 +144,15 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
       "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Transpose of an 8x8 matrix of 16-bit elements held one row pair per thread
+// (thread t: row t/4, columns 2(t%4), 2(t%4)+1) -> the same layout of the
+// transposed matrix.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+  return r;
 }
 
 // ------------------------------------------------------------ shared memory
