@@ -190,8 +190,7 @@ class Setup:
             np.int64)).to(device)
         self.d_table = torch.from_numpy(self.table).to(device)
         self.d_lens = torch.from_numpy(self.lens).to(device)
-        self.splits = num_splits if num_splits is not None else (
-            w.num_splits or K.kv4_decode_default_splits(B, Hkv, self.table.shape[1], P))
+        self.splits = num_splits if num_splits is not None else w.num_splits
         self.ws = K.alloc_workspace(B, Hq, D, self.splits, device=device)
         self.out = torch.empty((B, Hq, D), dtype=torch.float32, device=device)
         self.sm = float(w.sm_scale())
@@ -206,7 +205,7 @@ class Setup:
                                     self.out, num_splits=self.splits, workspace=self.ws)
 
     def launches_per_step(self):
-        return 1 + 1 + (1 if self.splits > 1 else 0)
+        return 1 + 1 + (0 if self.splits == 1 else 1)
 
 
 def time_decode_only(s, iters):

@@ -108,8 +108,8 @@ EncodeTiledFn encode_fn() {
 
 // The pool as a 2-D byte tensor of code rows: [pool_bytes / RB][RB], loaded in
 // boxes of RB bytes x `box_rows` rows with the swizzle whose span is RB.
-kv4_status code_row_map(const kv4_pool& p, CUtensorMap* map) {
-  struct Entry { const void* base; int64_t rows; int rb; CUtensorMap map; bool used; };
+kv4_status code_row_map(const kv4_pool& p, int box_rows, CUtensorMap* map) {
+  struct Entry { const void* base; int64_t rows; int rb; int box; CUtensorMap map; bool used; };
   static Entry cache[8];
   static int next = 0;
   static std::mutex mu;
@@ -118,7 +118,7 @@ kv4_status code_row_map(const kv4_pool& p, CUtensorMap* map) {
   {
     std::lock_guard<std::mutex> lock(mu);
     for (auto& e : cache)
-      if (e.used && e.base == p.base && e.rows == rows && e.rb == rb) {
+      if (e.used && e.base == p.base && e.rows == rows && e.rb == rb && e.box == box_rows) {
         *map = e.map;
         return KV4_OK;
       }
@@ -127,7 +127,7 @@ kv4_status code_row_map(const kv4_pool& p, CUtensorMap* map) {
   if (fn == nullptr) return fail(KV4_ECUDA, "cuTensorMapEncodeTiled is not available");
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(rb), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(rb)};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(rb), static_cast<cuuint32_t>(kv4::decode_box_rows())};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(rb), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   const CUtensorMapSwizzle sw = rb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                                 : rb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
@@ -137,7 +137,7 @@ kv4_status code_row_map(const kv4_pool& p, CUtensorMap* map) {
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(KV4_ECUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
   std::lock_guard<std::mutex> lock(mu);
-  cache[next] = Entry{p.base, rows, rb, *map, true};
+  cache[next] = Entry{p.base, rows, rb, box_rows, *map, true};
   next = (next + 1) % 8;
   return KV4_OK;
 }
@@ -198,25 +198,15 @@ kv4_status kv4_write(const void* k, const void* v, const int64_t* slot_mapping,
   return e == cudaSuccess ? KV4_OK : cuda_fail(e, "kv4_write launch");
 }
 
-int32_t kv4_decode_default_splits(int32_t batch, int32_t num_kv_heads, int32_t max_pages,
-                                  int32_t page_size) {
-  if (batch < 1 || num_kv_heads < 1 || max_pages < 1 || page_size < 1) return 1;
-  const int64_t units = static_cast<int64_t>(batch) * num_kv_heads;
-  const int64_t target = 4LL * sm_count();               // about four waves of CTAs
-  int64_t s = (target + units - 1) / units;
-  const int64_t max_tokens = static_cast<int64_t>(max_pages) * page_size;
-  const int64_t cap = (max_tokens + 4 * 64 - 1) / (4 * 64);   // >= one tile per warp
-  if (s > cap) s = cap;
-  if (s > 1024) s = 1024;
-  return static_cast<int32_t>(s < 1 ? 1 : s);
-}
-
 int64_t kv4_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t head_dim,
                                    int32_t num_splits) {
   if (batch < 0 || num_q_heads < 0 || head_dim < 0 || num_splits < 0) return 0;
-  if (num_splits <= 1) return 0;
-  const int64_t rows = static_cast<int64_t>(batch) * num_q_heads * num_splits;
-  return align256(rows * 4 * 4) + rows * head_dim * 4;
+  if (num_splits == 1 || batch == 0) return 0;        // one CTA per unit writes `out` directly
+  const int64_t S = num_splits == 0 ? 1 : num_splits;
+  // units (request, kv head, slice of <= 8 query heads) number at most batch * num_q_heads
+  const int64_t slots = static_cast<int64_t>(sm_count()) * kv4::decode_ctas_per_sm() +
+                        static_cast<int64_t>(batch) * num_q_heads * S;
+  return align256((batch + 1) * 8) + align256(slots * 8 * 16) + slots * 8 * head_dim * 4;
 }
 
 kv4_status kv4_decode_attention(const void* q, const kv4_pool* pool,
@@ -249,16 +239,15 @@ kv4_status kv4_decode_attention(const void* q, const kv4_pool* pool,
   const int G = num_q_heads / pool->num_kv_heads;
   if (batch > 65535 || static_cast<int64_t>(pool->num_kv_heads) * ((G + 7) / 8) > 65535)
     return fail(KV4_EINVAL, "batch or heads exceed the launch grid");
-  const int S = num_splits == 0 ? kv4_decode_default_splits(batch, pool->num_kv_heads, max_pages,
-                                                             pool->page_size)
-                                : num_splits;
-  const int64_t need = kv4_decode_workspace_bytes(batch, num_q_heads, pool->head_dim, S);
+  const int64_t need = kv4_decode_workspace_bytes(batch, num_q_heads, pool->head_dim, num_splits);
   if (need > 0) {
     if (workspace == nullptr || workspace_bytes < need)
-      return fail(KV4_EINVAL, "workspace of %lld bytes needed for %d splits",
-                  static_cast<long long>(need), S);
+      return fail(KV4_EINVAL, "workspace of %lld bytes needed for num_splits %d",
+                  static_cast<long long>(need), num_splits);
     if (!aligned(workspace, 256)) return fail(KV4_EINVAL, "workspace must be 256-byte aligned");
   }
+  const int64_t units = static_cast<int64_t>(batch) * pool->num_kv_heads * ((G + 7) / 8);
+  if (units >= (int64_t{1} << 31)) return fail(KV4_EINVAL, "too many (request, head) units");
 
   kv4::DecodeArgs a{};
   a.pool = static_cast<const uint8_t*>(pool->base);
@@ -277,18 +266,33 @@ kv4_status kv4_decode_attention(const void* q, const kv4_pool* pool,
   a.Hq = num_q_heads;
   a.G = G;
   a.sm_scale = sm_scale;
-  a.num_splits = S;
-  if (S > 1) {
-    const int64_t rows = static_cast<int64_t>(batch) * num_q_heads * S;
-    a.part_ml = static_cast<float*>(workspace);
-    a.part_o = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align256(rows * 4 * 4));
+  if (num_splits == 1) {
+    a.num_splits = 1;
+    a.unit_ctas = 1;
+    a.n_cta = static_cast<int>(units);
+  } else {
+    // one wave of persistent CTAs, each given an equal share of all tiles
+    const int64_t tiles_max = units * ((static_cast<int64_t>(max_pages) * pool->page_size +
+                                        kv4::decode_tile_tokens() - 1) / kv4::decode_tile_tokens());
+    const int64_t resident = static_cast<int64_t>(sm_count()) * kv4::decode_ctas_per_sm();
+    int64_t n = (tiles_max + 3) / 4;
+    n = n < 1 ? 1 : (n > resident ? resident : n);
+    a.num_splits = num_splits == 0 ? 1 : num_splits;
+    a.unit_ctas = 0;
+    a.n_cta = static_cast<int>(n);
+    const int64_t slots = resident + static_cast<int64_t>(batch) * num_q_heads * a.num_splits;
+    uint8_t* w = static_cast<uint8_t*>(workspace);
+    a.cum = reinterpret_cast<int64_t*>(w);
+    a.part_ml = reinterpret_cast<float*>(w + align256((batch + 1) * 8));
+    a.part_o = reinterpret_cast<float*>(w + align256((batch + 1) * 8) + align256(slots * 8 * 16));
   }
   a.out = out;
   a.out_f32 = out_is_fp32 ? 1 : 0;
   a.err = error_word();
   if (a.err == nullptr) return fail(KV4_ECUDA, "no CUDA device / error word unavailable");
+  a.box_rows = (pool->page_size % 32 == 0) ? 32 : 16;
   CUtensorMap map;
-  if ((s = code_row_map(*pool, &map)) != KV4_OK) return s;
+  if ((s = code_row_map(*pool, a.box_rows, &map)) != KV4_OK) return s;
   cudaError_t e = kv4::launch_decode(a, map, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KV4_OK : cuda_fail(e, "kv4_decode_attention launch");
 }
@@ -317,7 +321,7 @@ kv4_status kv4_dequant_prefix(const kv4_pool* pool, const float* layer_global_sc
     return fail(KV4_EINVAL, "fp8_k and fp8_v must be 16-byte aligned");
   if (pool->fmt == KV4_NVFP4 && layer_global_scale == nullptr)
     return fail(KV4_EINVAL, "NVFP4 needs layer_global_scale");
-  const int64_t threads = static_cast<int64_t>(max_prefix_len) * pool->num_kv_heads * (pool->head_dim / 8);
+  const int64_t threads = static_cast<int64_t>(max_prefix_len) * pool->num_kv_heads * (pool->head_dim / 16);
   if ((threads + 255) / 256 >= (int64_t{1} << 31)) return fail(KV4_EINVAL, "prefix too large");
 
   kv4::PrefixArgs a{};

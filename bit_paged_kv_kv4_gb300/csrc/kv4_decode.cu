@@ -1,5 +1,5 @@
 // Paged decode attention over the 4-bit pool, split over the sequence, and
-// the log-sum-exp combine of the splits.
+// the log-sum-exp combine of the pieces.
 //
 // "SGLang's 4-bit KV cache", Figure 2: decode "reads NVFP4 directly for native
 // FP4 decode with scales"; the page's kernel section describes loading packed
@@ -7,27 +7,39 @@
 // applying the scales.  INT4 per-token-head follows "KV cache in 4 bits"
 // (section "What we changed"): one scale per token and head for K and for V.
 //
-// Design (GB300, sm_103a):
-//  * One CTA = (request b, kv head h, group of <= 8 query heads, split s);
-//    4 warps, each streaming its own contiguous run of 64-token tiles.
-//  * Each warp keeps a private NS-stage ring in shared memory filled by TMA:
-//    the packed code rows of K and V arrive through 2-D tiled loads (16-row
-//    boxes, 32/64/128-byte swizzle so the fragment reads are bank-conflict
-//    free), the scale rows through 1-D bulk copies; completion is tracked with
-//    one mbarrier per stage.  Only lane 0 issues copies; no warp waits on
-//    another warp, and every wait is bounded.
-//  * Dequantisation happens in registers straight into tensor-core fragments:
+// Work decomposition (GB300: 152 SMs, two CTAs of 4 warps resident on each):
+//  * A unit is (request b, kv head h, slice of <= 8 query heads of h's group);
+//    its work is ceil(seq_len / 32) tiles of 32 tokens.  All units' tiles are
+//    laid end to end in (b, h, slice, tile) order.
+//  * Balanced mode (num_splits != 1): one wave of persistent CTAs; CTA c takes
+//    the tiles [c*T/n, (c+1)*T/n) of the whole list, so every CTA streams the
+//    same number of bytes whatever the length mix.  Independently, each unit
+//    is cut into S equal split ranges (S = num_splits, or 1 when 0 is passed).
+//    A piece is the intersection of a CTA range with a split range; it gets
+//    workspace slot `c + (u*S + s)`, which is unique because both are ordered
+//    partitions of the same line.  combine_kernel merges each unit's pieces.
+//    A unit that lies inside one CTA range with S = 1 is written directly.
+//  * Unit mode (num_splits == 1): one CTA per unit, output written directly,
+//    no workspace.
+//  * Inside a CTA, each segment (one piece) is divided among the 4 warps in
+//    contiguous runs of tiles; the warps' (m_x, l, m_y, o) states merge in
+//    shared memory in warp order (deterministic) at the end of the segment.
+//
+// Per warp (GB300 data path):
+//  * A private 2-stage ring in shared memory filled by TMA: the packed code
+//    rows of K and V arrive through 2-D tiled loads (16-row boxes, 32/64/128-
+//    byte swizzle, so the fragment reads are bank-conflict free), the scale
+//    rows through 1-D bulk copies; one mbarrier per stage, bounded waits.
+//    Block-table entries are prefetched one per lane, 32 pages ahead.
+//  * Dequantisation in registers straight into tensor-core fragments:
 //    E2M1 bytes -> f16x2 by the hardware conversion, times the E4M3 block
 //    scale (e2m1 * e4m3 is exact in f16); INT4 nibbles -> f16x2 by exponent
-//    bias arithmetic, the per-token scale applied to the FP32 scores (K) and
-//    to the probabilities (V).
-//  * QK^T: A = the query group (16 rows, <= 8 used), B = dequantised K^T,
-//    so the score accumulator has exactly the layout PV needs for P^T.
-//    PV: A = dequantised V^T (16 head-dim rows), B = P^T.  m16n8k16 f16 MMA,
-//    FP32 accumulate.  Online softmax in the base-2 domain.
-//  * The 4 warps' partial states merge in shared memory in a fixed order
-//    (deterministic).  One split writes `out` directly; more splits write
-//    (m_x, l, m_y, o) partials that combine_kernel merges.
+//    bias arithmetic, with the per-token scales applied to the FP32 scores (K)
+//    and carried in the exponent of the PV weights (V).
+//  * S^T = K q^T with A = dequantised K (16 tokens per MMA) and B = the query
+//    slice; movmatrix turns the score tile into the P^T operand of
+//    O^T += V^T P^T (A = dequantised V^T, 16 head-dim rows per MMA).
+//    m16n8k16 f16 MMA, FP32 accumulate; PV weights as f16 hi + lo pairs.
 #include <cstdint>
 
 #include "kv4_device.cuh"
@@ -37,20 +49,14 @@ namespace kv4 {
 
 namespace {
 
-#ifndef KV4_DECODE_TT
-#define KV4_DECODE_TT 32
-#endif
 #ifndef KV4_DECODE_NS
-#define KV4_DECODE_NS 3
+#define KV4_DECODE_NS 2
 #endif
-#ifndef KV4_DECODE_MINB
-#define KV4_DECODE_MINB 2
-#endif
-constexpr int kTT = KV4_DECODE_TT;     // tokens per tile (per warp and stage)
-constexpr int kSub = 16;               // rows per TMA box (sub-tile; never crosses a page)
+constexpr int kTT = 32;                // tokens per tile (per warp and stage)
 constexpr int kNW = 4;                 // warps per CTA
 constexpr int kNS = KV4_DECODE_NS;     // stages per warp
-constexpr int kMinBlocks = KV4_DECODE_MINB;   // CTAs resident per SM (register budget)
+constexpr int kCtasPerSm = 2;          // resident CTAs per SM (register and smem budget)
+constexpr int kMaxSeg = 64;            // segments held in shared memory per pass
 constexpr uint32_t kFull = 0xffffffffu;
 
 template <int D, int FMT>
@@ -65,32 +71,41 @@ struct Geo {
   static constexpr int OFF_VC = kTT * RB;
   static constexpr int OFF_KS = 2 * kTT * RB;
   static constexpr int OFF_VS = 2 * kTT * RB + kTT * SB;
-  static constexpr int EPI = kNW * 8 * D * 4 + 3 * kNW * 8 * 4;   // epilogue scratch
   static constexpr int RING = kNW * kNS * STAGE;
-  static constexpr int SMEM = (RING > EPI ? RING : EPI) + kNW * kNS * 8 + 1024;
+  static constexpr int ACC = 8 * D * 4;                        // merged O of one segment
+  static constexpr int META = kNW * 8 * 3 * 4;                 // (m_x, m_y, l) per warp and head
+  static constexpr int SEG = kMaxSeg * 20 + 16;        // keeps the int64 scratch 8-byte aligned
+  static constexpr int SMEM = RING + ACC + META + SEG + 64 + kNW * kNS * 8 + 1024;
 };
 
-// Load `N` bytes (N in {4, 8, 16, 32}) of logical row `row`, starting at
-// logical column `col` (a multiple of N), of a swizzled code tile.
-template <int RB, int N>
-__device__ __forceinline__ void load_row_bytes(uint32_t tile, int row, int col, uint32_t* w) {
+struct Seg {          // one piece: tiles [t0, t0 + n) of unit u, inside split `split`
+  int u, t0, n, split, len;   // len: the request's (clamped) sequence length
+};
+
+// Load `N` bytes (N in {4, 8, 16, 32}) of a swizzled code row; `a0` is the
+// shared address of the first 16-byte unit (or of the N bytes when N < 16),
+// `a1` that of the second unit when N == 32.  A TMA swizzle pattern repeats
+// every 8 rows, so a thread's addresses are one per-thread constant plus a
+// compile-time offset for every row it reads.
+template <int N>
+__device__ __forceinline__ void load_bytes(uint32_t a0, uint32_t a1, uint32_t* w) {
   if constexpr (N == 32) {
-    uint4 a = lds128(tile + swz<RB>(row, col));
-    uint4 b = lds128(tile + swz<RB>(row, col + 16));
-    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
-    w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+    uint4 x = lds128(a0);
+    uint4 y = lds128(a1);
+    w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
+    w[4] = y.x; w[5] = y.y; w[6] = y.z; w[7] = y.w;
   } else if constexpr (N == 16) {
-    uint4 a = lds128(tile + swz<RB>(row, col));
-    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+    uint4 x = lds128(a0);
+    w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
   } else if constexpr (N == 8) {
-    uint2 a = lds64(tile + swz<RB>(row, col));
-    w[0] = a.x; w[1] = a.y;
+    uint2 x = lds64(a0);
+    w[0] = x.x; w[1] = x.y;
   } else {
-    w[0] = lds32(tile + swz<RB>(row, col));
+    w[0] = lds32(a0);
   }
 }
 
-// Load `N` scale bytes (N in {1, 2, 4}) at byte `off` of a scale tile.
+// Load `N` scale bytes (N in {1, 2, 4}) at shared address `addr`.
 template <int N>
 __device__ __forceinline__ uint32_t load_scale_bytes(uint32_t addr) {
   if constexpr (N == 4) return lds32(addr);
@@ -121,545 +136,808 @@ __device__ __forceinline__ void store_out4(void* out, int out_f32, int64_t idx, 
   }
 }
 
+// seq_lens[b] clamped to [0, max_pages * P]; a value outside is recorded.
+__device__ __forceinline__ int clamp_len(const DecodeArgs& a, int b, bool flag) {
+  int L = a.seq_lens[b];
+  const int Lmax = a.max_pages * a.P;
+  if (L < 0 || L > Lmax) {
+    if (flag) set_error(a.err, KV4_EBOUNDS);
+    L = L < 0 ? 0 : Lmax;
+  }
+  return L;
+}
+
+// Exclusive prefix of `v` over the CTA's threads; `total` gets the sum.
+// `red` is kNW int64 of shared scratch.  Every thread must call it.
+__device__ __forceinline__ int64_t block_scan(int64_t v, int64_t* red, int64_t& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int64_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) red[warp] = x;
+  __syncthreads();
+  int64_t before = 0;
+  total = 0;
+#pragma unroll
+  for (int w = 0; w < kNW; ++w) {
+    const int64_t t = red[w];
+    if (w < warp) before += t;
+    total += t;
+  }
+  __syncthreads();
+  return before + x - v;
+}
+
 }  // namespace
 
+// Partition of [0, total) into `parts` ranges [i*total/parts, (i+1)*total/parts):
+// the start of range i, and the range holding x (total > 0, 0 <= x < total).
+__host__ __device__ inline int64_t part_begin(int64_t i, int64_t total, int64_t parts) {
+  return i * total / parts;
+}
+__host__ __device__ inline int64_t part_of(int64_t x, int64_t total, int64_t parts) {
+  return ((x + 1) * parts - 1) / total;
+}
+
 template <int D, int FMT>
-__global__ void __launch_bounds__(kNW * 32, kMinBlocks)
+__global__ void __launch_bounds__(kNW * 32, kCtasPerSm)
 decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap) {
   using Gm = Geo<D, FMT>;
   constexpr int RB = Gm::RB, SB = Gm::SB, KB = Gm::KB, VB = Gm::VB, MT = Gm::MT;
   constexpr int NM = kTT / 16;            // 16-token groups per tile (QK m-tiles = PV k-groups)
   extern __shared__ uint8_t smem_raw[];
 
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
   const int grp = lane >> 2, tig = lane & 3;
-  const int split = blockIdx.x, b = blockIdx.z;
   const int ngrp = (a.G + 7) >> 3;
-  const int h = blockIdx.y / ngrp;
-  const int g0 = (blockIdx.y % ngrp) * 8;
-  const int ng = min(8, a.G - g0);
-  const int hq0 = h * a.G + g0;
+  const int UPB = a.Hkv * ngrp;            // units per request
   const int S = a.num_splits;
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - smem_u32(smem_raw));
   const uint32_t ring = base + warp * kNS * Gm::STAGE;
-  const uint32_t bars = base + (Gm::RING > Gm::EPI ? Gm::RING : Gm::EPI) + warp * kNS * 8;
-
-  // ---- sequence range of this CTA and of this warp ------------------------
-  int L = a.seq_lens[b];
-  const int Lmax = a.max_pages * a.P;
-  if (L < 0 || L > Lmax) {
-    if (threadIdx.x == 0) set_error(a.err, KV4_EBOUNDS);
-    L = L < 0 ? 0 : Lmax;
-  }
-  const int n_tiles = (L + kTT - 1) / kTT;
-  const int per_split = (n_tiles + S - 1) / S;
-  const int c_begin = min(n_tiles, split * per_split);
-  const int c_end = min(n_tiles, c_begin + per_split);
-  const int per_warp = (c_end - c_begin + kNW - 1) / kNW;
-  const int w_begin = min(c_end, c_begin + warp * per_warp);
-  const int w_end = min(c_end, w_begin + per_warp);
-  const int n_my = w_end - w_begin;
+  float* sAcc = reinterpret_cast<float*>(gbase + Gm::RING);
+  float* sMeta = reinterpret_cast<float*>(gbase + Gm::RING + Gm::ACC);
+  Seg* sSeg = reinterpret_cast<Seg*>(gbase + Gm::RING + Gm::ACC + Gm::META);
+  int64_t* sRed = reinterpret_cast<int64_t*>(gbase + Gm::RING + Gm::ACC + Gm::META + Gm::SEG);
+  const uint32_t bars = base + Gm::RING + Gm::ACC + Gm::META + Gm::SEG + 64 + warp * kNS * 8;
+  __shared__ int s_nseg;
+  __shared__ long long s_cursor, s_cum, s_b;
 
   if (lane == 0) {
-    for (int s = 0; s < kNS; ++s) mbar_init(bars + 8 * s, 1);
+    for (int s2 = 0; s2 < kNS; ++s2) mbar_init(bars + 8 * s2, 1);
     fence_mbar_init();
   }
-  if (threadIdx.x == 0) prefetch_tensormap(&tmap);
-  __syncwarp();
+  if (tid == 0) prefetch_tensormap(&tmap);
 
-  // ---- block-table entries, cached one page index per lane ----------------
-  const int32_t* bt = a.block_table + static_cast<int64_t>(b) * a.max_pages;
-  const int p_first = (w_begin * kTT) / a.P;
-  const int p_last = n_my > 0 ? (min(L, w_end * kTT) - 1) / a.P : p_first - 1;
-  auto load_page = [&](int rel) -> int {
-    const int pi = p_first + rel;
-    return pi <= p_last ? __ldg(bt + pi) : 0;
-  };
-  int win = 0;
-  int pg_cur = load_page(lane);
-  int pg_nxt = load_page(32 + lane);
-  const uint64_t pol = policy_evict_first();
-  const uint8_t* pool = a.pool;
-
-  // Issue the copies of warp-local tile i into stage i % kNS.  Warp-uniform.
-  auto issue = [&](int i) {
-    const int t0 = (w_begin + i) * kTT;
-    const int nsub = min(kTT, L - t0 + kSub - 1) / kSub;     // sub-tiles holding tokens
-    const int rel0 = t0 / a.P - p_first;
-    while ((rel0 >> 5) > win) {
-      ++win;
-      pg_cur = pg_nxt;
-      pg_nxt = load_page((win + 1) * 32 + lane);
+  // ---- this CTA's tile range [c0, c1) in the global (b, unit, tile) order ------
+  int64_t T = 0, c1 = 0;
+  if (a.unit_ctas) {
+    // one CTA per unit: the range is that unit's tiles
+    const int u = blockIdx.x, b = u / UPB;
+    const int n_u = (clamp_len(a, b, tid == 0) + kTT - 1) / kTT;
+    if (tid == 0) {
+      sSeg[0] = Seg{u, 0, n_u, 0, clamp_len(a, b, false)};
+      s_nseg = 1;
     }
-    int pages[kTT / kSub];
-#pragma unroll
-    for (int u = 0; u < kTT / kSub; ++u) {
-      const int rel = (t0 + u * kSub) / a.P - p_first;
-      const int pc = __shfl_sync(kFull, pg_cur, rel & 31);
-      const int pn = __shfl_sync(kFull, pg_nxt, rel & 31);
-      pages[u] = ((rel >> 5) == win) ? pc : pn;
-    }
-    if (lane == 0) {
-      const uint32_t st = ring + (i % kNS) * Gm::STAGE;
-      const uint32_t bar = bars + 8 * (i % kNS);
-      mbar_arrive_expect_tx(bar, nsub * kSub * (2 * RB + 2 * SB));
-#pragma unroll
-      for (int u = 0; u < kTT / kSub; ++u) {
-        if (u < nsub) {
-          int page = pages[u];
-          if (page < 0 || page >= a.num_pages) {
-            set_error(a.err, KV4_EBOUNDS);
-            page = 0;
-          }
-          const int off = (t0 + u * kSub) % a.P;
-          const int64_t chunk = (static_cast<int64_t>(page) * a.Hkv + h) * a.chunk_bytes;
-          const int row = static_cast<int>(chunk / RB) + off;
-          tma_load_2d(st + u * kSub * RB, &tmap, 0, row, bar, pol);
-          tma_load_2d(st + Gm::OFF_VC + u * kSub * RB, &tmap, 0, row + a.P, bar, pol);
-          const uint8_t* sc = pool + chunk + static_cast<int64_t>(a.P) * 2 * RB;
-          bulk_load(st + Gm::OFF_KS + u * kSub * SB, sc + off * SB, kSub * SB, bar, pol);
-          bulk_load(st + Gm::OFF_VS + u * kSub * SB, sc + static_cast<int64_t>(a.P) * SB + off * SB,
-                    kSub * SB, bar, pol);
-        }
-      }
-    }
-  };
-
-  // ---- query fragments (B operand of S^T = K q^T), f16, power-of-two prescaled
-  // Thread (grp, tig) holds query row g0+grp, head-dim range [2*KB*tig, 2*KB*(tig+1)).
-  constexpr int QN = 2 * KB;                 // query elements per thread
-  float qf[QN];
-  {
-    const bool row_ok = grp < ng;
-    const __nv_bfloat16* qrow = a.q + (static_cast<int64_t>(b) * a.Hq + hq0 + grp) * D + QN * tig;
-#pragma unroll
-    for (int i = 0; i < QN; i += 8) {
-      uint4 v = row_ok ? __ldg(reinterpret_cast<const uint4*>(qrow + i)) : make_uint4(0, 0, 0, 0);
-      const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&v);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float2 f = __bfloat1622float2(p2[j]);
-        qf[i + 2 * j] = f.x;
-        qf[i + 2 * j + 1] = f.y;
-      }
-    }
-  }
-  float qmax = 0.f;
-#pragma unroll
-  for (int i = 0; i < QN; ++i) qmax = fmaxf(qmax, fabsf(qf[i]));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(kFull, qmax, o));
-  // Keep |q| <= 2^14 in f16 by an exact power of two, undone on the scores.
-  float qpre = 1.f;
-  if (qmax > 16384.f) {
-    int e;
-    frexpf(qmax / 16384.f, &e);
-    qpre = ldexpf(1.f, -e);
-  }
-  uint32_t qb[QN / 2];
-  if constexpr (FMT == KV4_NVFP4) {
-    // k-step kk: k (2tig, 2tig+1) <-> d = base + 4kk + {0,1}; (2tig+8, +9) <-> + {2,3}
-#pragma unroll
-    for (int i = 0; i < QN / 2; ++i) qb[i] = pack_f16x2(qf[2 * i] * qpre, qf[2 * i + 1] * qpre);
   } else {
-    // per 8 elements e: kk even: (e0,e4), (e1,e5); kk odd: (e2,e6), (e3,e7)
-#pragma unroll
-    for (int j = 0; j < QN / 8; ++j) {
-      const float* e = qf + 8 * j;
-      qb[4 * j + 0] = pack_f16x2(e[0] * qpre, e[4] * qpre);
-      qb[4 * j + 1] = pack_f16x2(e[1] * qpre, e[5] * qpre);
-      qb[4 * j + 2] = pack_f16x2(e[2] * qpre, e[6] * qpre);
-      qb[4 * j + 3] = pack_f16x2(e[3] * qpre, e[7] * qpre);
+    for (int b0 = 0; b0 < a.B; b0 += kNW * 32) {
+      const int b = b0 + tid;
+      const int64_t v = (b < a.B) ? static_cast<int64_t>((clamp_len(a, b, blockIdx.x == 0) + kTT - 1) / kTT) * UPB : 0;
+      int64_t tot;
+      const int64_t ex = block_scan(v, sRed, tot);
+      if (blockIdx.x == 0 && b < a.B) a.cum[b] = T + ex;        // for combine_kernel
+      T += tot;
     }
+    if (blockIdx.x == 0 && tid == 0) a.cum[a.B] = T;
+    c1 = part_begin(blockIdx.x + 1, T, a.n_cta);
+    if (tid == 0) s_cursor = part_begin(blockIdx.x, T, a.n_cta);
   }
+  __syncthreads();
 
-  const float gk = (FMT == KV4_NVFP4) ? __ldg(a.gscale) : 1.f;
-  const float gv = (FMT == KV4_NVFP4) ? __ldg(a.gscale + 1) : 1.f;
-  const float qk_scale = a.sm_scale * gk * 1.4426950408889634f / qpre;   // base-2 logits
+  // ---- per-thread shared-memory offsets inside a stage ----------------------
+  // K rows 16m + grp (+8): swizzled units of row grp; V rows 16kg + 2tig (+1, +8,
+  // +9): units of rows 2tig and 2tig+1; shifting by 8 rows keeps the pattern.
+  const uint32_t k_off0 = swz<RB>(grp, KB * tig);
+  const uint32_t k_off1 = swz<RB>(grp, KB * tig + 16);
+  const uint32_t v_offa = Gm::OFF_VC + swz<RB>(2 * tig, VB * grp);
+  const uint32_t v_offb = Gm::OFF_VC + swz<RB>(2 * tig + 1, VB * grp);
+  const uint32_t ks_off = Gm::OFF_KS + grp * SB + (D / 64) * tig;
+  const uint32_t vs_off = Gm::OFF_VS + 2 * tig * SB + (VB * grp) / 8;
 
-  // ---- running softmax state (base 2), for heads g0 + 2tig + c, c = 0, 1 ----
-  // m_x: running max of the logits x_t, l_run = sum 2^(x_t - m_x) (partial
-  // over this thread's tokens).  The PV weights are w_t = 2^(y_t - m_y) with
-  // y_t = x_t (NVFP4) or x_t + log2 s_V(t) (INT4: the per-token V scale rides
-  // in the exponent, so every f16 operand stays in [0, 1]);
-  // out = 2^(m_y - m_x) * sum_t w_t code_t / l.
-  float m_x[2] = {-INFINITY, -INFINITY}, m_y[2] = {-INFINITY, -INFINITY};
-  float l_run[2] = {0.f, 0.f};
+  // ---- per-warp running state ----------------------------------------------
+  const uint64_t pol = policy_evict_first();
+  uint32_t qb[KB];                  // query fragments of the current unit
+  float qk_scale = 0.f, gv = 1.f;
+  float m_x[2], m_y[2], l_run[2];
   float o[MT][4];
-#pragma unroll
-  for (int mi = 0; mi < MT; ++mi) o[mi][0] = o[mi][1] = o[mi][2] = o[mi][3] = 0.f;
-
-  int issued = 0;
-  for (; issued < kNS && issued < n_my; ++issued) issue(issued);
-
+  int issued = 0, consumed = 0;     // warp-local tile counters (stage = counter % kNS)
   bool timed_out = false;
-  for (int i = 0; i < n_my; ++i) {
-    const uint32_t st = ring + (i % kNS) * Gm::STAGE;
-    if (!mbar_wait_bounded(bars + 8 * (i % kNS), (i / kNS) & 1)) {
-      // give the copies still in flight a bounded chance to land, then stop
-      for (int j = i + 1; j < issued; ++j) mbar_wait_bounded(bars + 8 * (j % kNS), (j / kNS) & 1);
-      timed_out = true;
-      break;
-    }
-    const int t0 = (w_begin + i) * kTT;
-    const int valid = min(kTT, L - t0);
-    const uint32_t sK = st, sV = st + Gm::OFF_VC, sKs = st + Gm::OFF_KS, sVs = st + Gm::OFF_VS;
 
-    // -------- S^T[t][g] = K q^T: NM m-tiles of 16 tokens ----------------------
-    // A = dequantised K (rows: tokens 16m+grp and 16m+grp+8), B = q^T.
-    // sacc[m]: c0 = (16m+grp, head 2tig), c1 = (16m+grp, 2tig+1),
-    //          c2 = (16m+grp+8, 2tig),    c3 = (16m+grp+8, 2tig+1)
-    float sacc[NM][4];
-    uint32_t kw[NM][2][KB / 4];
-#pragma unroll
-    for (int m = 0; m < NM; ++m) {
-      sacc[m][0] = sacc[m][1] = sacc[m][2] = sacc[m][3] = 0.f;
-      load_row_bytes<RB, KB>(sK, 16 * m + grp, KB * tig, kw[m][0]);
-      load_row_bytes<RB, KB>(sK, 16 * m + grp + 8, KB * tig, kw[m][1]);
+  // passes over the CTA range, kMaxSeg segments at a time
+  while (true) {
+    if (!a.unit_ctas) {
+      // thread 0 lists the next segments of [cursor, c1)
+      const int64_t cur = s_cursor;
+      __syncthreads();
+      if (cur >= c1) break;
+      // the request b holding tile `cur` (block scan over b)
+      if (tid == 0) s_b = -1;
+      __syncthreads();
+      int64_t acc = 0;
+      for (int b0 = 0; b0 < a.B; b0 += kNW * 32) {
+        const int b = b0 + tid;
+        const int64_t v = (b < a.B) ? static_cast<int64_t>((clamp_len(a, b, false) + kTT - 1) / kTT) * UPB : 0;
+        int64_t tot;
+        const int64_t ex = acc + block_scan(v, sRed, tot);
+        if (b < a.B && v > 0 && ex <= cur && cur < ex + v) {
+          s_b = b;
+          s_cum = ex;
+        }
+        acc += tot;
+        __syncthreads();
+        if (s_b >= 0) break;
+      }
+      if (tid == 0) {
+        int64_t x = cur;
+        int b = static_cast<int>(s_b);
+        int64_t cum = s_cum;
+        int ns = 0;
+        while (x < c1 && ns < kMaxSeg && b >= 0 && b < a.B) {
+          const int n_u = (clamp_len(a, b, false) + kTT - 1) / kTT;
+          if (n_u == 0 || x >= cum + static_cast<int64_t>(n_u) * UPB) {
+            cum += static_cast<int64_t>(n_u) * UPB;
+            ++b;
+            continue;
+          }
+          const int64_t rem = x - cum;
+          const int j = static_cast<int>(rem / n_u);
+          const int t = static_cast<int>(rem % n_u);
+          const int split = static_cast<int>(part_of(t, n_u, S));
+          const int64_t send = part_begin(split + 1, n_u, S);
+          const int n = static_cast<int>(send - t < c1 - x ? send - t : c1 - x);
+          sSeg[ns++] = Seg{b * UPB + j, t, n, split, clamp_len(a, b, false)};
+          x += n;
+        }
+        s_nseg = ns;
+        s_cursor = (ns == 0) ? c1 : x;     // no segment found: the range is done
+      }
+      __syncthreads();
     }
-    if constexpr (FMT == KV4_NVFP4) {
-      constexpr int NB = D / 64;              // block scales per token this thread needs
-      // hs[m][r][j]: f16x2 broadcast of block scale j of token 16m+grp+8r
-      uint32_t hs[NM][2][NB < 2 ? 2 : NB];
-#pragma unroll
-      for (int m = 0; m < NM; ++m) {
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const uint32_t sc = load_scale_bytes<NB>(sKs + (16 * m + grp + 8 * r) * SB + NB * tig);
-#pragma unroll
-          for (int j = 0; j < NB; j += 2)   // bytes [s_j s_j s_j+1 s_j+1] -> two broadcasts
-            e4m3x4_to_f16x2x2(prmt(sc, 0u, (j == 0) ? 0x1100u : 0x3322u), hs[m][r][j], hs[m][r][j + 1]);
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < KB / 4; ++j) {      // word j: k-steps 2j (bytes 0, 1) and 2j+1 (bytes 2, 3)
-#pragma unroll
-        for (int m = 0; m < NM; ++m) {
-          uint32_t c0[4], c1[4];
-          e2m1x8_to_f16x2x4(kw[m][0][j], c0);
-          e2m1x8_to_f16x2x4(kw[m][1][j], c1);
-          const uint32_t s0 = hs[m][0][j >> 1], s1 = hs[m][1][j >> 1];
-          mma_f16_16816(sacc[m], hmul2(c0[0], s0), hmul2(c1[0], s1), hmul2(c0[1], s0),
-                        hmul2(c1[1], s1), qb[4 * j], qb[4 * j + 1]);
-          mma_f16_16816(sacc[m], hmul2(c0[2], s0), hmul2(c1[2], s1), hmul2(c0[3], s0),
-                        hmul2(c1[3], s1), qb[4 * j + 2], qb[4 * j + 3]);
-        }
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < KB / 4; ++j) {
-#pragma unroll
-        for (int m = 0; m < NM; ++m) {
-          const uint32_t w0 = kw[m][0][j], w1 = kw[m][1][j];
-          mma_f16_16816(sacc[m], int4_lo_pair(w0), int4_lo_pair(w1), int4_hi_pair(w0),
-                        int4_hi_pair(w1), qb[4 * j + 0], qb[4 * j + 1]);
-        }
-#pragma unroll
-        for (int m = 0; m < NM; ++m) {
-          const uint32_t w0 = kw[m][0][j] >> 8, w1 = kw[m][1][j] >> 8;
-          mma_f16_16816(sacc[m], int4_lo_pair(w0), int4_lo_pair(w1), int4_hi_pair(w0),
-                        int4_hi_pair(w1), qb[4 * j + 2], qb[4 * j + 3]);
-        }
-      }
-    }
+    const int nseg = s_nseg;
 
-    // -------- online softmax (base 2) over this tile ----------------------
-    // token of sacc[m][2r + c]: 16m + grp + 8r; head 2tig + c
-    float yv[NM][4];                 // INT4: exponent of the PV weight
-    float tmx[2] = {-INFINITY, -INFINITY}, tmy[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int m = 0; m < NM; ++m) {
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int t = 16 * m + grp + 8 * r;
-        float sk = 1.f, lsv = 0.f;
-        bool vok = true;
-        if constexpr (FMT == KV4_INT4_PTH) {
-          sk = __uint_as_float(lds32(sKs + 4 * t));
-          const float sv = __uint_as_float(lds32(sVs + 4 * t));
-          lsv = fast_log2(sv);                // sv == 0: no V weight
-          vok = sv > 0.f;
+    // ---- this warp's run of tiles inside segment k ------------------------
+    auto my_run = [&](int k, int& beg, int& cnt) {
+      const int n = sSeg[k].n;
+      const int q = (n + kNW - 1) / kNW;
+      beg = min(n, warp * q);
+      cnt = min(n, beg + q) - beg;
+    };
+
+    // issue cursor and its block-table cache (one page index per lane)
+    int ks = -1, io = 0, is_cn = 0, is_bg = 0, is_t0 = 0, is_L = 0, is_h = 0;
+    int i_pass = 0, i_total = 0;   // tiles of this pass issued / in total for this warp
+    for (int k = 0; k < nseg; ++k) {
+      int bg, cn;
+      my_run(k, bg, cn);
+      i_total += cn;
+    }
+    int p_first = 0, p_last = -1, win = 0, pg_cur = 0, pg_nxt = 0;
+    int pi = 0, po = 0;              // page index and offset of the next tile's first token
+    const int32_t* bt = a.block_table;
+    const int box = a.box_rows;      // rows per TMA box: 32 when 32 divides P, else 16
+
+    auto issue = [&]() {      // warp-uniform; issues the next tile of this pass
+      while (io >= is_cn) {   // enter the next segment with tiles for this warp
+        ++ks;
+        io = 0;
+        my_run(ks, is_bg, is_cn);
+        const Seg sg = sSeg[ks];
+        const int b = sg.u / UPB;
+        is_h = (sg.u % UPB) / ngrp;
+        is_t0 = sg.t0;
+        is_L = sg.len;
+        if (is_cn > 0) {        // reload the page cache for this run
+          const int tf = (sg.t0 + is_bg) * kTT;
+          pi = tf / a.P;
+          po = tf - pi * a.P;
+          p_first = pi;
+          p_last = (min(is_L, (sg.t0 + is_bg + is_cn) * kTT) - 1) / a.P;
+          win = 0;
+          bt = a.block_table + static_cast<int64_t>(b) * a.max_pages;
+          const int r0 = p_first + lane, r1 = p_first + 32 + lane;
+          pg_cur = r0 <= p_last ? __ldg(bt + r0) : 0;
+          pg_nxt = r1 <= p_last ? __ldg(bt + r1) : 0;
         }
+      }
+      const int h = is_h, L = is_L;
+      const int t0 = (is_t0 + is_bg + io) * kTT;
+      const int nsub = (min(kTT, L - t0) + box - 1) / box;
+      while (((pi - p_first) >> 5) > win) {
+        ++win;
+        pg_cur = pg_nxt;
+        const int r = p_first + (win + 1) * 32 + lane;
+        pg_nxt = r <= p_last ? __ldg(bt + r) : 0;
+      }
+      int pages[kTT / 16], offs[kTT / 16];
+#pragma unroll
+      for (int u = 0; u < kTT / 16; ++u) {
+        int pu = pi, ou = po + u * box;         // a box never straddles a page
+        if (ou >= a.P) { ou -= a.P; ++pu; }
+        const int rel = pu - p_first;
+        const int pcv = __shfl_sync(kFull, pg_cur, rel & 31);
+        const int pnv = __shfl_sync(kFull, pg_nxt, rel & 31);
+        pages[u] = ((rel >> 5) == win) ? pcv : pnv;
+        offs[u] = ou;
+      }
+      if (lane == 0) {
+        const uint32_t st = ring + (issued % kNS) * Gm::STAGE;
+        const uint32_t bar = bars + 8 * (issued % kNS);
+        mbar_arrive_expect_tx(bar, nsub * box * (2 * RB + 2 * SB));
+#pragma unroll
+        for (int u = 0; u < kTT / 16; ++u) {
+          if (u < nsub) {
+            int page = pages[u];
+            if (page < 0 || page >= a.num_pages) {
+              set_error(a.err, KV4_EBOUNDS);
+              page = 0;
+            }
+            const int off = offs[u];
+            const int64_t chunk = (static_cast<int64_t>(page) * a.Hkv + h) * a.chunk_bytes;
+            const int row = static_cast<int>(chunk / RB) + off;
+            tma_load_2d(st + u * box * RB, &tmap, 0, row, bar, pol);
+            tma_load_2d(st + Gm::OFF_VC + u * box * RB, &tmap, 0, row + a.P, bar, pol);
+            const uint8_t* sc = a.pool + chunk + static_cast<int64_t>(a.P) * 2 * RB;
+            bulk_load(st + Gm::OFF_KS + u * box * SB, sc + off * SB, box * SB, bar, pol);
+            bulk_load(st + Gm::OFF_VS + u * box * SB, sc + static_cast<int64_t>(a.P) * SB + off * SB,
+                      box * SB, bar, pol);
+          }
+        }
+      }
+      po += kTT;                       // advance to the next tile's first token
+      while (po >= a.P) { po -= a.P; ++pi; }
+      ++io;
+      ++issued;
+      ++i_pass;
+    };
+
+    for (int k0 = 0; k0 < kNS && i_pass < i_total && !timed_out; ++k0) issue();
+
+    for (int k = 0; k < nseg; ++k) {
+      const Seg sg = sSeg[k];
+      const int b = sg.u / UPB;
+      const int h = (sg.u % UPB) / ngrp;
+      const int g0 = (sg.u % ngrp) * 8;
+      const int ng = min(8, a.G - g0);
+      const int hq0 = h * a.G + g0;
+      const int L = sg.len;
+      int bg, cn;
+      my_run(k, bg, cn);
+
+      // ---- query fragments of this unit (B operand of S^T = K q^T) ----------
+      // Thread (grp, tig) holds query row g0+grp, head-dim range [2*KB*tig, 2*KB*(tig+1)).
+      {
+        constexpr int QN = 2 * KB;
+        float qf[QN];
+        const bool row_ok = grp < ng;
+        const __nv_bfloat16* qrow = a.q + (static_cast<int64_t>(b) * a.Hq + hq0 + grp) * D + QN * tig;
+#pragma unroll
+        for (int i = 0; i < QN; i += 8) {
+          uint4 v = row_ok ? __ldg(reinterpret_cast<const uint4*>(qrow + i)) : make_uint4(0, 0, 0, 0);
+          const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float2 f = __bfloat1622float2(p2[j]);
+            qf[i + 2 * j] = f.x;
+            qf[i + 2 * j + 1] = f.y;
+          }
+        }
+        float qmax = 0.f;
+#pragma unroll
+        for (int i = 0; i < QN; ++i) qmax = fmaxf(qmax, fabsf(qf[i]));
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(kFull, qmax, o2));
+        // Keep |q| <= 2^14 in f16 by an exact power of two, undone on the scores.
+        float qpre = 1.f;
+        if (qmax > 16384.f) {
+          int e;
+          frexpf(qmax / 16384.f, &e);
+          qpre = ldexpf(1.f, -e);
+        }
+        if constexpr (FMT == KV4_NVFP4) {
+          // k-step kk: k (2tig, 2tig+1) <-> d = base + 4kk + {0,1}; (2tig+8, +9) <-> + {2,3}
+#pragma unroll
+          for (int i = 0; i < QN / 2; ++i) qb[i] = pack_f16x2(qf[2 * i] * qpre, qf[2 * i + 1] * qpre);
+        } else {
+          // per 8 elements e: kk even: (e0,e4), (e1,e5); kk odd: (e2,e6), (e3,e7)
+#pragma unroll
+          for (int j = 0; j < QN / 8; ++j) {
+            const float* e = qf + 8 * j;
+            qb[4 * j + 0] = pack_f16x2(e[0] * qpre, e[4] * qpre);
+            qb[4 * j + 1] = pack_f16x2(e[1] * qpre, e[5] * qpre);
+            qb[4 * j + 2] = pack_f16x2(e[2] * qpre, e[6] * qpre);
+            qb[4 * j + 3] = pack_f16x2(e[3] * qpre, e[7] * qpre);
+          }
+        }
+        const float gk = (FMT == KV4_NVFP4) ? __ldg(a.gscale) : 1.f;
+        gv = (FMT == KV4_NVFP4) ? __ldg(a.gscale + 1) : 1.f;
+        qk_scale = a.sm_scale * gk * 1.4426950408889634f / qpre;   // base-2 logits
+      }
+
+      // ---- running softmax state (base 2), heads g0 + 2tig + c, c = 0, 1 ------
+      // m_x: running max of the logits x_t, l_run = sum 2^(x_t - m_x) (partial
+      // over this thread's tokens).  The PV weights are w_t = 2^(y_t - m_y) with
+      // y_t = x_t (NVFP4) or x_t + log2 s_V(t) (INT4: the per-token V scale rides
+      // in the exponent, so every f16 operand stays in [0, 1]);
+      // out = 2^(m_y - m_x) * sum_t w_t code_t / l.
+      m_x[0] = m_x[1] = m_y[0] = m_y[1] = -INFINITY;
+      l_run[0] = l_run[1] = 0.f;
+#pragma unroll
+      for (int mi = 0; mi < MT; ++mi) o[mi][0] = o[mi][1] = o[mi][2] = o[mi][3] = 0.f;
+
+      for (int jt = 0; jt < cn && !timed_out; ++jt) {
+        const uint32_t st = ring + (consumed % kNS) * Gm::STAGE;
+        if (!mbar_wait_bounded(bars + 8 * (consumed % kNS), (consumed / kNS) & 1)) {
+          // give the copies still in flight a bounded chance to land, then stop
+          for (int j = consumed + 1; j < issued; ++j)
+            mbar_wait_bounded(bars + 8 * (j % kNS), (j / kNS) & 1);
+          timed_out = true;
+          break;
+        }
+        const int t0 = (sg.t0 + bg + jt) * kTT;
+        const int valid = min(kTT, L - t0);
+
+        // -------- S^T[t][g] = K q^T: NM m-tiles of 16 tokens ------------------
+        // A = dequantised K (rows: tokens 16m+grp and 16m+grp+8), B = q^T.
+        // sacc[m]: c0 = (16m+grp, head 2tig), c1 = (16m+grp, 2tig+1),
+        //          c2 = (16m+grp+8, 2tig),    c3 = (16m+grp+8, 2tig+1)
+        float sacc[NM][4];
+        uint32_t kw[NM][2][KB / 4];
+#pragma unroll
+        for (int m = 0; m < NM; ++m) {
+          sacc[m][0] = sacc[m][1] = sacc[m][2] = sacc[m][3] = 0.f;
+          load_bytes<KB>(st + k_off0 + 16 * m * RB, st + k_off1 + 16 * m * RB, kw[m][0]);
+          load_bytes<KB>(st + k_off0 + (16 * m + 8) * RB, st + k_off1 + (16 * m + 8) * RB, kw[m][1]);
+        }
+        if constexpr (FMT == KV4_NVFP4) {
+          constexpr int NB = D / 64;              // block scales per token this thread needs
+          // hs[m][r][j]: f16x2 broadcast of block scale j of token 16m+grp+8r
+          uint32_t hs[NM][2][NB < 2 ? 2 : NB];
+#pragma unroll
+          for (int m = 0; m < NM; ++m) {
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const uint32_t sc = load_scale_bytes<NB>(st + ks_off + (16 * m + 8 * r) * SB);
+#pragma unroll
+              for (int j = 0; j < NB; j += 2)   // bytes [s_j s_j s_j+1 s_j+1] -> two broadcasts
+                e4m3x4_to_f16x2x2(prmt(sc, 0u, (j == 0) ? 0x1100u : 0x3322u), hs[m][r][j],
+                                  hs[m][r][j + 1]);
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < KB / 4; ++j) {      // word j: k-steps 2j (bytes 0, 1), 2j+1 (bytes 2, 3)
+#pragma unroll
+            for (int m = 0; m < NM; ++m) {
+              uint32_t c0[4], c1[4];
+              e2m1x8_to_f16x2x4(kw[m][0][j], c0);
+              e2m1x8_to_f16x2x4(kw[m][1][j], c1);
+              const uint32_t s0 = hs[m][0][j >> 1], s1 = hs[m][1][j >> 1];
+              mma_f16_16816(sacc[m], hmul2(c0[0], s0), hmul2(c1[0], s1), hmul2(c0[1], s0),
+                            hmul2(c1[1], s1), qb[4 * j], qb[4 * j + 1]);
+              mma_f16_16816(sacc[m], hmul2(c0[2], s0), hmul2(c1[2], s1), hmul2(c0[3], s0),
+                            hmul2(c1[3], s1), qb[4 * j + 2], qb[4 * j + 3]);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < KB / 4; ++j) {
+#pragma unroll
+            for (int m = 0; m < NM; ++m) {
+              const uint32_t w0 = kw[m][0][j], w1 = kw[m][1][j];
+              mma_f16_16816(sacc[m], int4_lo_pair(w0), int4_lo_pair(w1), int4_hi_pair(w0),
+                            int4_hi_pair(w1), qb[4 * j + 0], qb[4 * j + 1]);
+            }
+#pragma unroll
+            for (int m = 0; m < NM; ++m) {
+              const uint32_t w0 = kw[m][0][j] >> 8, w1 = kw[m][1][j] >> 8;
+              mma_f16_16816(sacc[m], int4_lo_pair(w0), int4_lo_pair(w1), int4_hi_pair(w0),
+                            int4_hi_pair(w1), qb[4 * j + 2], qb[4 * j + 3]);
+            }
+          }
+        }
+
+        // -------- online softmax (base 2) over this tile ----------------------
+        // token of sacc[m][2r + c]: 16m + grp + 8r; head 2tig + c
+        float yv[NM][4];                 // INT4: exponent of the PV weight
+        float tmx[2] = {-INFINITY, -INFINITY}, tmy[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int m = 0; m < NM; ++m) {
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const int t = 16 * m + grp + 8 * r;
+            float sk = 1.f, lsv = 0.f;
+            bool vok = true;
+            if constexpr (FMT == KV4_INT4_PTH) {
+              sk = __uint_as_float(lds32(st + Gm::OFF_KS + 4 * grp + 4 * (16 * m + 8 * r)));
+              const float sv = __uint_as_float(lds32(st + Gm::OFF_VS + 4 * grp + 4 * (16 * m + 8 * r)));
+              lsv = fast_log2(sv);                // sv == 0: no V weight
+              vok = sv > 0.f;
+            }
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              float x = sacc[m][2 * r + c] * qk_scale * sk;
+              x = (t < valid) ? x : -INFINITY;
+              sacc[m][2 * r + c] = x;
+              tmx[c] = fmaxf(tmx[c], x);
+              if constexpr (FMT == KV4_INT4_PTH) {
+                yv[m][2 * r + c] = (t < valid && vok) ? x + lsv : -INFINITY;
+                tmy[c] = fmaxf(tmy[c], yv[m][2 * r + c]);
+              }
+            }
+          }
+        }
+        float corr_x[2], corr_y[2], mx_new[2], my_new[2];
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          float x = sacc[m][2 * r + c] * qk_scale * sk;
-          x = (t < valid) ? x : -INFINITY;
-          sacc[m][2 * r + c] = x;
-          tmx[c] = fmaxf(tmx[c], x);
+#pragma unroll
+          for (int o2 = 4; o2 < 32; o2 <<= 1) tmx[c] = fmaxf(tmx[c], __shfl_xor_sync(kFull, tmx[c], o2));
+          mx_new[c] = fmaxf(m_x[c], tmx[c]);            // finite: valid >= 1
+          corr_x[c] = fast_exp2(m_x[c] - mx_new[c]);     // 0 when m_x == -inf
+          m_x[c] = mx_new[c];
+          corr_y[c] = corr_x[c];
+          my_new[c] = mx_new[c];
           if constexpr (FMT == KV4_INT4_PTH) {
-            yv[m][2 * r + c] = (t < valid && vok) ? x + lsv : -INFINITY;
-            tmy[c] = fmaxf(tmy[c], yv[m][2 * r + c]);
+#pragma unroll
+            for (int o2 = 4; o2 < 32; o2 <<= 1) tmy[c] = fmaxf(tmy[c], __shfl_xor_sync(kFull, tmy[c], o2));
+            my_new[c] = fmaxf(m_y[c], tmy[c]);
+            corr_y[c] = (my_new[c] == -INFINITY) ? 1.f : fast_exp2(m_y[c] - my_new[c]);
+          }
+          m_y[c] = my_new[c];
+        }
+        // P^T operand of PV per 16-token group m: b0 <- tokens (2tig, 2tig+1) of head grp,
+        // b1 <- tokens (8+2tig, 8+2tig+1); transposed from the score layout with movmatrix.
+        uint32_t pb[NM][2], pl[NM][2];
+        float psum[2] = {0.f, 0.f};
+#pragma unroll
+        for (int m = 0; m < NM; ++m) {
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            float w[2];
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              const float p = fast_exp2(sacc[m][2 * r + c] - mx_new[c]);
+              psum[c] += p;
+              w[c] = p;
+              if constexpr (FMT == KV4_INT4_PTH)
+                w[c] = (my_new[c] == -INFINITY) ? 0.f : fast_exp2(yv[m][2 * r + c] - my_new[c]);
+            }
+            const uint32_t hi = pack_f16x2(w[0], w[1]);
+            const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+            const uint32_t lo = pack_f16x2(w[0] - hf.x, w[1] - hf.y);
+            pb[m][r] = movmatrix_trans(hi);
+            pl[m][r] = movmatrix_trans(lo);
           }
         }
+#pragma unroll
+        for (int c = 0; c < 2; ++c) l_run[c] = l_run[c] * corr_x[c] + psum[c];
+        if (__any_sync(kFull, corr_y[0] != 1.f || corr_y[1] != 1.f)) {
+#pragma unroll
+          for (int mi = 0; mi < MT; ++mi) {
+            o[mi][0] *= corr_y[0]; o[mi][1] *= corr_y[1]; o[mi][2] *= corr_y[0]; o[mi][3] *= corr_y[1];
+          }
+        }
+
+        // -------- O^T += V^T P^T: NM k-groups of 16 tokens ---------------------
+#pragma unroll
+        for (int kg = 0; kg < NM; ++kg) {
+          const int ta = kg * 16 + 2 * tig;       // tokens ta, ta+1 (k 2tig..) and ta+8, ta+9
+          uint32_t wa[VB / 4], wb[VB / 4], wc[VB / 4], wd[VB / 4];
+          load_bytes<VB>(st + v_offa + 16 * kg * RB, 0, wa);
+          load_bytes<VB>(st + v_offb + 16 * kg * RB, 0, wb);
+          load_bytes<VB>(st + v_offa + (16 * kg + 8) * RB, 0, wc);
+          load_bytes<VB>(st + v_offb + (16 * kg + 8) * RB, 0, wd);
+          if constexpr (FMT == KV4_NVFP4) {
+            // block scales of the thread's head-dim range, per token
+            constexpr int NVB = (VB >= 8) ? VB / 8 : 1;
+            const int blk0 = (VB * grp) / 8;
+            const uint32_t xa = load_scale_bytes<NVB>(st + vs_off + 16 * kg * SB);
+            const uint32_t xb = load_scale_bytes<NVB>(st + vs_off + (16 * kg + 1) * SB);
+            const uint32_t xc = load_scale_bytes<NVB>(st + vs_off + (16 * kg + 8) * SB);
+            const uint32_t xd = load_scale_bytes<NVB>(st + vs_off + (16 * kg + 9) * SB);
+            // mask tokens past the end: a zero scale zeroes the (finite) codes
+            const uint32_t ma = (ta < valid) ? 0xFFFFu : 0u, mb = (ta + 1 < valid) ? 0xFFFF0000u : 0u;
+            const uint32_t mc = (ta + 8 < valid) ? 0xFFFFu : 0u, md = (ta + 9 < valid) ? 0xFFFF0000u : 0u;
+            uint32_t sab[2], scd[2];
+            {
+              // each token's scale bytes -> f16 (one conversion per token's byte pair)
+              uint32_t fa, fb, fc, fd;
+              e4m3x4_to_f16x2x2(xa | (xb << 16), fa, fb);
+              e4m3x4_to_f16x2x2(xc | (xd << 16), fc, fd);
+              sab[0] = prmt(fa, fb, 0x5410u) & (ma | mb);   // first block: (s(ta), s(tb))
+              scd[0] = prmt(fc, fd, 0x5410u) & (mc | md);
+              sab[1] = prmt(fa, fb, 0x7632u) & (ma | mb);   // second block (NVB == 2)
+              scd[1] = prmt(fc, fd, 0x7632u) & (mc | md);
+            }
+#pragma unroll
+            for (int j = 0; j < VB / 4; ++j) {
+              const uint32_t lab = (wa[j] & 0x0F0F0F0Fu) | ((wb[j] << 4) & 0xF0F0F0F0u);
+              const uint32_t hab = ((wa[j] >> 4) & 0x0F0F0F0Fu) | (wb[j] & 0xF0F0F0F0u);
+              const uint32_t lcd = (wc[j] & 0x0F0F0F0Fu) | ((wd[j] << 4) & 0xF0F0F0F0u);
+              const uint32_t hcd = ((wc[j] >> 4) & 0x0F0F0F0Fu) | (wd[j] & 0xF0F0F0F0u);
+              uint32_t vl[4], vh[4], ul[4], uh[4];
+              e2m1x8_to_f16x2x4(lab, vl);
+              e2m1x8_to_f16x2x4(hab, vh);
+              e2m1x8_to_f16x2x4(lcd, ul);
+              e2m1x8_to_f16x2x4(hcd, uh);
+#pragma unroll
+              for (int mm = 0; mm < 4; ++mm) {
+                const int mi = 4 * j + mm;
+                const int bj = (VB * grp + mi) / 8 - blk0;
+                const uint32_t a0 = hmul2(vl[mm], sab[bj]);
+                const uint32_t a1 = hmul2(vh[mm], sab[bj]);
+                const uint32_t a2 = hmul2(ul[mm], scd[bj]);
+                const uint32_t a3 = hmul2(uh[mm], scd[bj]);
+                mma_f16_16816(o[mi], a0, a1, a2, a3, pb[kg][0], pb[kg][1]);
+                mma_f16_16816(o[mi], a0, a1, a2, a3, pl[kg][0], pl[kg][1]);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < VB / 4; ++j) {
+#pragma unroll
+              for (int mm = 0; mm < 4; ++mm) {
+                const int mi = 4 * j + mm;
+                const uint32_t sel = mm | (mm << 4) | ((4 + mm) << 8) | ((4 + mm) << 12);
+                const uint32_t xab = prmt(wa[j], wb[j], sel);
+                const uint32_t xcd = prmt(wc[j], wd[j], sel);
+                const uint32_t a0 = int4_lo_pair(xab), a1 = int4_hi_pair(xab);
+                const uint32_t a2 = int4_lo_pair(xcd), a3 = int4_hi_pair(xcd);
+                mma_f16_16816(o[mi], a0, a1, a2, a3, pb[kg][0], pb[kg][1]);
+                mma_f16_16816(o[mi], a0, a1, a2, a3, pl[kg][0], pl[kg][1]);
+              }
+            }
+          }
+        }
+        __syncwarp();
+        ++consumed;
+        if (i_pass < i_total) issue();
       }
-    }
-    float corr_x[2], corr_y[2], mx_new[2], my_new[2];
+      // A warp that timed out stops streaming but still joins every merge below,
+      // so the CTA's barriers stay matched; its partial state is empty.
+
+
+      if (timed_out) {
+        m_x[0] = m_x[1] = m_y[0] = m_y[1] = -INFINITY;
+        l_run[0] = l_run[1] = 0.f;
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-#pragma unroll
-      for (int o2 = 4; o2 < 32; o2 <<= 1) tmx[c] = fmaxf(tmx[c], __shfl_xor_sync(kFull, tmx[c], o2));
-      mx_new[c] = fmaxf(m_x[c], tmx[c]);            // finite: valid >= 1
-      corr_x[c] = fast_exp2(m_x[c] - mx_new[c]);     // 0 when m_x == -inf
-      m_x[c] = mx_new[c];
-      corr_y[c] = corr_x[c];
-      my_new[c] = mx_new[c];
-      if constexpr (FMT == KV4_INT4_PTH) {
-#pragma unroll
-        for (int o2 = 4; o2 < 32; o2 <<= 1) tmy[c] = fmaxf(tmy[c], __shfl_xor_sync(kFull, tmy[c], o2));
-        my_new[c] = fmaxf(m_y[c], tmy[c]);
-        corr_y[c] = (my_new[c] == -INFINITY) ? 1.f : fast_exp2(m_y[c] - my_new[c]);
+        for (int mi = 0; mi < MT; ++mi) o[mi][0] = o[mi][1] = o[mi][2] = o[mi][3] = 0.f;
       }
-      m_y[c] = my_new[c];
-    }
-    // P^T operand of PV per 16-token group m: b0 <- tokens (2tig, 2tig+1) of head grp,
-    // b1 <- tokens (8+2tig, 8+2tig+1); transposed from the score layout with movmatrix.
-    uint32_t pb[NM][2], pl[NM][2];
-    float psum[2] = {0.f, 0.f};
+      // ---- merge the warps' states for this segment, in warp order ------------
 #pragma unroll
-    for (int m = 0; m < NM; ++m) {
+      for (int c = 0; c < 2; ++c) {
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        float w[2];
+        for (int o2 = 4; o2 < 32; o2 <<= 1) l_run[c] += __shfl_xor_sync(kFull, l_run[c], o2);
+      }
+      if (grp == 0) {
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          const float p = fast_exp2(sacc[m][2 * r + c] - mx_new[c]);
-          psum[c] += p;
-          w[c] = p;
-          if constexpr (FMT == KV4_INT4_PTH)
-            w[c] = (my_new[c] == -INFINITY) ? 0.f : fast_exp2(yv[m][2 * r + c] - my_new[c]);
+          float* mt = sMeta + (warp * 8 + 2 * tig + c) * 3;
+          mt[0] = m_x[c];
+          mt[1] = m_y[c];
+          mt[2] = l_run[c];
         }
-        const uint32_t hi = pack_f16x2(w[0], w[1]);
-        const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi));
-        const uint32_t lo = pack_f16x2(w[0] - hf.x, w[1] - hf.y);
-        pb[m][r] = movmatrix_trans(hi);
-        pl[m][r] = movmatrix_trans(lo);
       }
-    }
+      __syncthreads();
+      float wgt[2];
 #pragma unroll
-    for (int c = 0; c < 2; ++c) l_run[c] = l_run[c] * corr_x[c] + psum[c];
-    if (__any_sync(kFull, corr_y[0] != 1.f || corr_y[1] != 1.f)) {
-#pragma unroll
-      for (int mi = 0; mi < MT; ++mi) {
-        o[mi][0] *= corr_y[0]; o[mi][1] *= corr_y[1]; o[mi][2] *= corr_y[0]; o[mi][3] *= corr_y[1];
+      for (int c = 0; c < 2; ++c) {
+        const int g = 2 * tig + c;
+        float My = -INFINITY;
+        for (int w = 0; w < kNW; ++w) My = fmaxf(My, sMeta[(w * 8 + g) * 3 + 1]);
+        const float mw = sMeta[(warp * 8 + g) * 3 + 1];
+        wgt[c] = (mw == -INFINITY) ? 0.f : fast_exp2(mw - My);
       }
-    }
-
-    // -------- O^T += V^T P^T: NM k-groups of 16 tokens -------------------------
+      for (int w = 0; w < kNW; ++w) {
+        if (warp == w) {
 #pragma unroll
-    for (int kg = 0; kg < NM; ++kg) {
-      const int ta = kg * 16 + 2 * tig;       // tokens ta, ta+1 (k 2tig..) and ta+8, ta+9
-      uint32_t wa[VB / 4], wb[VB / 4], wc[VB / 4], wd[VB / 4];
-      load_row_bytes<RB, VB>(sV, ta, VB * grp, wa);
-      load_row_bytes<RB, VB>(sV, ta + 1, VB * grp, wb);
-      load_row_bytes<RB, VB>(sV, ta + 8, VB * grp, wc);
-      load_row_bytes<RB, VB>(sV, ta + 9, VB * grp, wd);
-      if constexpr (FMT == KV4_NVFP4) {
-        // block scales of the thread's head-dim range, per token
-        constexpr int NVB = (VB >= 8) ? VB / 8 : 1;
-        const int blk0 = (VB * grp) / 8;
-        const uint32_t xa = load_scale_bytes<NVB>(sVs + ta * SB + blk0);
-        const uint32_t xb = load_scale_bytes<NVB>(sVs + (ta + 1) * SB + blk0);
-        const uint32_t xc = load_scale_bytes<NVB>(sVs + (ta + 8) * SB + blk0);
-        const uint32_t xd = load_scale_bytes<NVB>(sVs + (ta + 9) * SB + blk0);
-        // mask tokens past the end: a zero scale zeroes the (finite) codes
-        const uint32_t ma = (ta < valid) ? 0xFFFFu : 0u, mb = (ta + 1 < valid) ? 0xFFFF0000u : 0u;
-        const uint32_t mc = (ta + 8 < valid) ? 0xFFFFu : 0u, md = (ta + 9 < valid) ? 0xFFFF0000u : 0u;
-        uint32_t sab[2], scd[2];
-        {
-          // each token's NVB scale bytes -> f16 (one conversion per token pair of bytes)
-          uint32_t fa, fb, fc, fd;
-          e4m3x4_to_f16x2x2(xa | (xb << 16), fa, fb);
-          e4m3x4_to_f16x2x2(xc | (xd << 16), fc, fd);
-          sab[0] = prmt(fa, fb, 0x5410u) & (ma | mb);   // block 0: (s(ta), s(tb))
-          scd[0] = prmt(fc, fd, 0x5410u) & (mc | md);
-          sab[1] = prmt(fa, fb, 0x7632u) & (ma | mb);   // block 1 (NVB == 2)
-          scd[1] = prmt(fc, fd, 0x7632u) & (mc | md);
-        }
-#pragma unroll
-        for (int j = 0; j < VB / 4; ++j) {
-          const uint32_t lab = (wa[j] & 0x0F0F0F0Fu) | ((wb[j] << 4) & 0xF0F0F0F0u);
-          const uint32_t hab = ((wa[j] >> 4) & 0x0F0F0F0Fu) | (wb[j] & 0xF0F0F0F0u);
-          const uint32_t lcd = (wc[j] & 0x0F0F0F0Fu) | ((wd[j] << 4) & 0xF0F0F0F0u);
-          const uint32_t hcd = ((wc[j] >> 4) & 0x0F0F0F0Fu) | (wd[j] & 0xF0F0F0F0u);
-          uint32_t vl[4], vh[4], ul[4], uh[4];
-          e2m1x8_to_f16x2x4(lab, vl);
-          e2m1x8_to_f16x2x4(hab, vh);
-          e2m1x8_to_f16x2x4(lcd, ul);
-          e2m1x8_to_f16x2x4(hcd, uh);
-#pragma unroll
-          for (int mm = 0; mm < 4; ++mm) {
-            const int mi = 4 * j + mm;
-            const int bj = (VB * grp + mi) / 8 - blk0;
-            const uint32_t a0 = hmul2(vl[mm], sab[bj]);
-            const uint32_t a1 = hmul2(vh[mm], sab[bj]);
-            const uint32_t a2 = hmul2(ul[mm], scd[bj]);
-            const uint32_t a3 = hmul2(uh[mm], scd[bj]);
-            mma_f16_16816(o[mi], a0, a1, a2, a3, pb[kg][0], pb[kg][1]);
-            mma_f16_16816(o[mi], a0, a1, a2, a3, pl[kg][0], pl[kg][1]);
+          for (int mi = 0; mi < MT; ++mi) {
+            const int d = 2 * (VB * grp + mi);
+            float* r0 = sAcc + (2 * tig) * D + d;
+            float* r1 = sAcc + (2 * tig + 1) * D + d;
+            if (w == 0) {
+              r0[0] = o[mi][0] * wgt[0]; r1[0] = o[mi][1] * wgt[1];
+              r0[1] = o[mi][2] * wgt[0]; r1[1] = o[mi][3] * wgt[1];
+            } else {
+              r0[0] += o[mi][0] * wgt[0]; r1[0] += o[mi][1] * wgt[1];
+              r0[1] += o[mi][2] * wgt[0]; r1[1] += o[mi][3] * wgt[1];
+            }
           }
         }
-      } else {
-#pragma unroll
-        for (int j = 0; j < VB / 4; ++j) {
-#pragma unroll
-          for (int mm = 0; mm < 4; ++mm) {
-            const int mi = 4 * j + mm;
-            const uint32_t sel = mm | (mm << 4) | ((4 + mm) << 8) | ((4 + mm) << 12);
-            const uint32_t xab = prmt(wa[j], wb[j], sel);
-            const uint32_t xcd = prmt(wc[j], wd[j], sel);
-            const uint32_t a0 = int4_lo_pair(xab), a1 = int4_hi_pair(xab);
-            const uint32_t a2 = int4_lo_pair(xcd), a3 = int4_hi_pair(xcd);
-            mma_f16_16816(o[mi], a0, a1, a2, a3, pb[kg][0], pb[kg][1]);
-            mma_f16_16816(o[mi], a0, a1, a2, a3, pl[kg][0], pl[kg][1]);
-          }
+        __syncthreads();
+      }
+      const bool direct = a.unit_ctas || (S == 1 && sg.t0 == 0 && sg.n == (L + kTT - 1) / kTT);
+      const int64_t slot = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(sg.u) * S + sg.split;
+      for (int e = tid * 4; e < ng * D; e += kNW * 32 * 4) {
+        const int g = e / D, d = e % D;
+        float Mx = -INFINITY, My = -INFINITY;
+        for (int w = 0; w < kNW; ++w) {
+          Mx = fmaxf(Mx, sMeta[(w * 8 + g) * 3 + 0]);
+          My = fmaxf(My, sMeta[(w * 8 + g) * 3 + 1]);
+        }
+        float l = 0.f;
+        for (int w = 0; w < kNW; ++w) {
+          const float mw = sMeta[(w * 8 + g) * 3 + 0];
+          l += (mw == -INFINITY) ? 0.f : sMeta[(w * 8 + g) * 3 + 2] * fast_exp2(mw - Mx);
+        }
+        const float4 acc = *reinterpret_cast<const float4*>(sAcc + g * D + d);
+        if (direct) {
+          const float inv = (l > 0.f && My != -INFINITY) ? gv * fast_exp2(My - Mx) / l : 0.f;
+          const int64_t row = static_cast<int64_t>(b) * a.Hq + hq0 + g;
+          store_out4(a.out, a.out_f32, row * D + d,
+                     make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+        } else {
+          *reinterpret_cast<float4*>(a.part_o + (slot * 8 + g) * D + d) = acc;
+          if (d == 0)
+            *reinterpret_cast<float4*>(a.part_ml + (slot * 8 + g) * 4) = make_float4(Mx, l, My, 0.f);
         }
       }
+      __syncthreads();
     }
-    __syncwarp();
-    if (issued < n_my) issue(issued++);
+    if (a.unit_ctas) break;     // every thread takes the same exit
   }
   if (timed_out && lane == 0) set_error(a.err, KV4_ETIMEOUT);
-
-  // ---- merge the warps' states in shared memory, fixed order --------------
-#pragma unroll
-  for (int c = 0; c < 2; ++c) {
-#pragma unroll
-    for (int o2 = 4; o2 < 32; o2 <<= 1) l_run[c] += __shfl_xor_sync(kFull, l_run[c], o2);
-  }
-  __syncthreads();   // every warp finished reading its ring
-  float* sO = reinterpret_cast<float*>(smem_raw + (base - smem_u32(smem_raw)));
-  float* sMx = sO + kNW * 8 * D;
-  float* sMy = sMx + kNW * 8;
-  float* sL = sMy + kNW * 8;
-  if (grp == 0) {
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      sMx[warp * 8 + 2 * tig + c] = m_x[c];
-      sMy[warp * 8 + 2 * tig + c] = m_y[c];
-      sL[warp * 8 + 2 * tig + c] = l_run[c];
-    }
-  }
-  __syncthreads();
-  {
-    // this thread's O^T columns: heads 2tig, 2tig+1
-    float wgt[2];
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const int g = 2 * tig + c;
-      float My = -INFINITY;
-      for (int w = 0; w < kNW; ++w) My = fmaxf(My, sMy[w * 8 + g]);
-      const float mw = sMy[warp * 8 + g];
-      wgt[c] = (mw == -INFINITY) ? 0.f : fast_exp2(mw - My);
-    }
-    float* dst = sO + warp * 8 * D;
-#pragma unroll
-    for (int mi = 0; mi < MT; ++mi) {
-      const int d = 2 * (VB * grp + mi);
-      dst[(2 * tig) * D + d] = o[mi][0] * wgt[0];
-      dst[(2 * tig + 1) * D + d] = o[mi][1] * wgt[1];
-      dst[(2 * tig) * D + d + 1] = o[mi][2] * wgt[0];
-      dst[(2 * tig + 1) * D + d + 1] = o[mi][3] * wgt[1];
-    }
-  }
-  __syncthreads();
-  for (int e = threadIdx.x * 4; e < ng * D; e += kNW * 32 * 4) {
-    const int g = e / D, d = e % D;
-    float Mx = -INFINITY, My = -INFINITY;
-    for (int w = 0; w < kNW; ++w) {
-      Mx = fmaxf(Mx, sMx[w * 8 + g]);
-      My = fmaxf(My, sMy[w * 8 + g]);
-    }
-    float l = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int w = 0; w < kNW; ++w) {
-      const float mw = sMx[w * 8 + g];
-      l += (mw == -INFINITY) ? 0.f : sL[w * 8 + g] * fast_exp2(mw - Mx);
-      const float4 v = *reinterpret_cast<const float4*>(sO + (w * 8 + g) * D + d);
-      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-    }
-    const int64_t row = static_cast<int64_t>(b) * a.Hq + hq0 + g;
-    if (S == 1) {
-      const float inv = (l > 0.f && My != -INFINITY) ? gv * fast_exp2(My - Mx) / l : 0.f;
-      float4 r = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-      store_out4(a.out, a.out_f32, row * D + d, r);
-    } else {
-      const int64_t prow = row * S + split;
-      *reinterpret_cast<float4*>(a.part_o + prow * D + d) = acc;
-      if (d == 0) *reinterpret_cast<float4*>(a.part_ml + 4 * prow) = make_float4(Mx, l, My, 0.f);
-    }
-  }
 }
 
-// Merge the S split partials (m_x, l, m_y, o) of each (request, query head):
-//   Mx = max m_x, My = max m_y, l = sum_s l_s 2^(m_x,s - Mx),
-//   out = g_V * 2^(My - Mx) * sum_s o_s 2^(m_y,s - My) / l
-// Weights are summed in split order, so the result is deterministic.
-__global__ void __launch_bounds__(128)
-combine_kernel(const float* __restrict__ part_ml, const float* __restrict__ part_o, int S,
-               int D, int Hq, const float* __restrict__ gscale, int use_g, void* out,
-               int out_f32) {
-  extern __shared__ float sw[];          // [S] weights of o_s
-  __shared__ float red[2][4];
-  __shared__ float bcast[3];
-  const int j = blockIdx.x, b = blockIdx.y;
-  const int64_t row = static_cast<int64_t>(b) * Hq + j;
-  const float4* ml = reinterpret_cast<const float4*>(part_ml) + row * S;
-  const float* po = part_o + row * S * D;
-  const int tid = threadIdx.x, nt = blockDim.x;
+// Merge the pieces of each (request, query head):
+//   Mx = max m_x, My = max m_y, l = sum_p l_p 2^(m_x,p - Mx),
+//   out = g_V * 2^(My - Mx) * sum_p o_p 2^(m_y,p - My) / l
+// The unit's pieces are listed in line order (split by split, CTA by CTA)
+// with one thread per split; sums run over fixed thread groups and are
+// reduced in a fixed order, so the result is deterministic.
+constexpr int kCombineThreads = 256;
+constexpr int kMaxPieces = 2048;
 
-  float Mx = -INFINITY, My = -INFINITY;
-  for (int s = tid; s < S; s += nt) {
-    const float4 m = ml[s];
-    Mx = fmaxf(Mx, m.x);
-    My = fmaxf(My, m.z);
+__global__ void __launch_bounds__(kCombineThreads)
+combine_kernel(const DecodeArgs a) {
+  __shared__ int64_t s_slot[kMaxPieces];
+  __shared__ int64_t s_red[kCombineThreads / 32];
+  __shared__ float s_f[kCombineThreads];
+  __shared__ float4 s_o[kCombineThreads];
+  const int j = blockIdx.x, b = blockIdx.y;
+  const int D = a.D, S = a.num_splits;
+  const int ngrp = (a.G + 7) >> 3, UPB = a.Hkv * ngrp;
+  const int h = j / a.G, gi = j % a.G;
+  const int u = b * UPB + h * ngrp + gi / 8;
+  const int g = gi % 8;
+  const int64_t row = static_cast<int64_t>(b) * a.Hq + j;
+  int L = a.seq_lens[b];
+  const int Lmax = a.max_pages * a.P;
+  L = L < 0 ? 0 : (L > Lmax ? Lmax : L);
+  const int n_u = (L + kTT - 1) / kTT;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  if (n_u == 0) {
+    for (int d = tid * 4; d < D; d += kCombineThreads * 4)
+      store_out4(a.out, a.out_f32, row * D + d, make_float4(0.f, 0.f, 0.f, 0.f));
+    return;
   }
-  for (int o = 16; o > 0; o >>= 1) {
-    Mx = fmaxf(Mx, __shfl_xor_sync(kFull, Mx, o));
-    My = fmaxf(My, __shfl_xor_sync(kFull, My, o));
+  const int64_t T = a.cum[a.B];
+  const int64_t start = a.cum[b] + static_cast<int64_t>(u - b * UPB) * n_u;
+  if (S == 1 && part_of(start, T, a.n_cta) == part_of(start + n_u - 1, T, a.n_cta)) return;  // written directly
+  const bool may_be_empty = T < a.n_cta;   // only then can a CTA range hold no tile
+
+  // ---- list the pieces: split s holds CTAs part_of(x0)..part_of(x1-1) ----------
+  int64_t npieces = 0;
+  for (int s0 = 0; s0 < S; s0 += kCombineThreads) {
+    const int s = s0 + tid;
+    int64_t cf = 0, cl = -1;
+    if (s < S) {
+      const int64_t x0 = start + part_begin(s, n_u, S), x1 = start + part_begin(s + 1, n_u, S);
+      if (x1 > x0) {
+        cf = part_of(x0, T, a.n_cta);
+        cl = part_of(x1 - 1, T, a.n_cta);
+      }
+    }
+    int64_t cnt = 0;
+    for (int64_t c = cf; c <= cl; ++c)
+      if (!may_be_empty || part_begin(c, T, a.n_cta) != part_begin(c + 1, T, a.n_cta)) ++cnt;
+    // exclusive scan of the counts over the block
+    int64_t x = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) s_red[warp] = x;
+    __syncthreads();
+    int64_t before = 0, tot = 0;
+    for (int w = 0; w < kCombineThreads / 32; ++w) {
+      if (w < warp) before += s_red[w];
+      tot += s_red[w];
+    }
+    int64_t at = npieces + before + x - cnt;
+    for (int64_t c = cf; c <= cl; ++c) {
+      if (may_be_empty && part_begin(c, T, a.n_cta) == part_begin(c + 1, T, a.n_cta)) continue;
+      if (at < kMaxPieces) s_slot[at] = c + static_cast<int64_t>(u) * S + s;
+      ++at;
+    }
+    npieces += tot;
+    __syncthreads();
   }
-  if ((tid & 31) == 0) {
-    red[0][tid >> 5] = Mx;
-    red[1][tid >> 5] = My;
+  const int P = static_cast<int>(npieces < kMaxPieces ? npieces : kMaxPieces);
+  if (npieces > kMaxPieces && tid == 0) set_error(a.err, KV4_EUNSUPPORTED);
+
+  // ---- maxima of the piece states --------------------------------------------
+  float mx = -INFINITY, my = -INFINITY;
+  for (int p = tid; p < P; p += kCombineThreads) {
+    const float4 m = *reinterpret_cast<const float4*>(a.part_ml + (s_slot[p] * 8 + g) * 4);
+    mx = fmaxf(mx, m.x);
+    my = fmaxf(my, m.z);
   }
+  s_f[tid] = mx;
   __syncthreads();
   if (tid == 0) {
-    float mx = -INFINITY, my = -INFINITY;
-    for (int w = 0; w < (nt + 31) / 32; ++w) {
-      mx = fmaxf(mx, red[0][w]);
-      my = fmaxf(my, red[1][w]);
-    }
-    bcast[0] = mx;
-    bcast[1] = my;
+    float v = -INFINITY;
+    for (int t = 0; t < kCombineThreads; ++t) v = fmaxf(v, s_f[t]);
+    s_red[0] = __float_as_int(v);
   }
   __syncthreads();
-  Mx = bcast[0];
-  My = bcast[1];
-  for (int s = tid; s < S; s += nt) {
-    const float m = ml[s].z;
-    sw[s] = (m == -INFINITY) ? 0.f : fast_exp2(m - My);
-  }
+  const float Mx = __int_as_float(static_cast<int>(s_red[0]));
+  __syncthreads();
+  s_f[tid] = my;
   __syncthreads();
   if (tid == 0) {
-    float l = 0.f;
-    for (int s = 0; s < S; ++s) {
-      const float4 m = ml[s];
-      l += (m.x == -INFINITY) ? 0.f : m.y * fast_exp2(m.x - Mx);
-    }
-    bcast[2] = l;
+    float v = -INFINITY;
+    for (int t = 0; t < kCombineThreads; ++t) v = fmaxf(v, s_f[t]);
+    s_red[0] = __float_as_int(v);
   }
   __syncthreads();
-  const float l = bcast[2];
-  const float g = use_g ? __ldg(gscale + 1) : 1.f;
-  const float inv = (l > 0.f && My != -INFINITY) ? g * fast_exp2(My - Mx) / l : 0.f;
-  for (int d = tid * 4; d < D; d += nt * 4) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < S; ++s) {
-      const float w = sw[s];
-      const float4 v = __ldg(reinterpret_cast<const float4*>(po + static_cast<int64_t>(s) * D + d));
-      acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+  const float My = __int_as_float(static_cast<int>(s_red[0]));
+  __syncthreads();
+
+  // ---- normaliser l, summed per thread then in thread order ---------------------
+  float lp = 0.f;
+  for (int p = tid; p < P; p += kCombineThreads) {
+    const float4 m = *reinterpret_cast<const float4*>(a.part_ml + (s_slot[p] * 8 + g) * 4);
+    lp += (m.x == -INFINITY) ? 0.f : m.y * fast_exp2(m.x - Mx);
+  }
+  s_f[tid] = lp;
+  __syncthreads();
+  if (tid == 0) {
+    float v = 0.f;
+    for (int t = 0; t < kCombineThreads; ++t) v += s_f[t];
+    s_f[0] = v;
+  }
+  __syncthreads();
+  const float l = s_f[0];
+
+  // ---- weighted sum of the pieces' o: thread = (piece group, 4 columns) --------
+  const int cols = D / 4;                        // float4 columns
+  const int groups = kCombineThreads / cols;     // pieces handled side by side
+  const int col = tid % cols, grp = tid / cols;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int p = grp; p < P; p += groups) {
+    const int64_t slot = s_slot[p];
+    const float mz = a.part_ml[(slot * 8 + g) * 4 + 2];
+    const float w = (mz == -INFINITY) ? 0.f : fast_exp2(mz - My);
+    const float4 v = __ldg(reinterpret_cast<const float4*>(a.part_o + (slot * 8 + g) * D) + col);
+    acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+  }
+  s_o[tid] = acc;
+  __syncthreads();
+  if (grp == 0) {
+    for (int r = 1; r < groups; ++r) {
+      const float4 v = s_o[r * cols + col];
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
     }
-    store_out4(out, out_f32, row * D + d, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+    const float gv = (a.fmt == KV4_NVFP4) ? __ldg(a.gscale + 1) : 1.f;
+    const float inv = (l > 0.f && My != -INFINITY) ? gv * fast_exp2(My - Mx) / l : 0.f;
+    store_out4(a.out, a.out_f32, row * D + 4 * col,
+               make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
   }
 }
 
@@ -676,14 +954,13 @@ static cudaError_t launch_split(const DecodeArgs& a, const CUtensorMap& map, cud
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  const int ngrp = (a.G + 7) / 8;
-  dim3 grid(a.num_splits, a.Hkv * ngrp, a.B);
-  k<<<grid, kNW * 32, Gm::SMEM, st>>>(a, map);
+  k<<<a.n_cta, kNW * 32, Gm::SMEM, st>>>(a, map);
   return cudaGetLastError();
 }
 
 int decode_tile_tokens() { return kTT; }
-int decode_box_rows() { return kSub; }
+
+int decode_ctas_per_sm() { return kCtasPerSm; }
 
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& map, cudaStream_t st) {
   cudaError_t e;
@@ -700,10 +977,8 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& map, cudaStrea
       default: e = launch_split<256, KV4_INT4_PTH>(a, map, st); break;
     }
   }
-  if (e != cudaSuccess || a.num_splits == 1) return e;
-  const int S = a.num_splits;
-  combine_kernel<<<dim3(a.Hq, a.B), 64, S * sizeof(float), st>>>(
-      a.part_ml, a.part_o, S, a.D, a.Hq, a.gscale, a.fmt == KV4_NVFP4 ? 1 : 0, a.out, a.out_f32);
+  if (e != cudaSuccess || a.unit_ctas) return e;
+  combine_kernel<<<dim3(a.Hq, a.B), kCombineThreads, 0, st>>>(a);
   return cudaGetLastError();
 }
 

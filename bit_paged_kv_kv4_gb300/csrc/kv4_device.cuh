@@ -264,6 +264,23 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ------------------------------------------------------------ division
+// a / b rounded to nearest even, given yb = __frcp_rn(b) (1/b correctly
+// rounded).  Markstein's theorem (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1),
+// 1990): q0 = RN(a * yb) is within one ulp of a/b, the residual a - b*q0 is
+// exact under a fused multiply-add, and RN(q0 + residual * yb) equals
+// RN(a/b) whenever no intermediate overflows or underflows.  Outside that
+// range (a reciprocal or first quotient that is not finite) it falls back to
+// the IEEE division.  The sign of a zero quotient follows a (as a/b with
+// b > 0 does).  Callers only pass b > 0.
+__device__ __forceinline__ float div_rn(float a, float b, float yb) {
+  const float q0 = __fmul_rn(a, yb);
+  if (!(fabsf(q0) < 1.0e30f) || !(yb < 1.0e30f)) return __fdiv_rn(a, b);
+  const float r = __fmaf_rn(-b, q0, a);
+  return copysignf(__fmaf_rn(r, yb, q0), a);
+}
+
 // ------------------------------------------------------------ misc
 __device__ __forceinline__ float fast_log2(float x) {
   float r;

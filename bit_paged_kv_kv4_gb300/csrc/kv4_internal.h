@@ -19,9 +19,13 @@ struct DecodeArgs {
   const int32_t* seq_lens;      // [B]
   int B, Hq, G;
   float sm_scale;
-  int num_splits;
-  float* part_ml;               // [B][Hq][S][4]: m_x, l, m_y, 0
-  float* part_o;                // [B][Hq][S][D]
+  int num_splits;               // split ranges per unit (>= 1)
+  int n_cta;                    // CTAs launched
+  int unit_ctas;                // 1: one CTA per unit, output written directly
+  int box_rows;                 // rows per TMA box of the code-row map (16 or 32)
+  int64_t* cum;                 // [B+1] tile offsets of each request (balanced mode)
+  float* part_ml;               // [slots][8][4]: m_x, l, m_y, 0
+  float* part_o;                // [slots][8][D]
   void* out;
   int out_f32;
   int* err;
@@ -61,6 +65,6 @@ cudaError_t launch_prefix(const PrefixArgs& a, cudaStream_t st);
 int decode_tile_tokens();
 // Sets the message kv4_last_error_message() returns on this thread.
 void set_error_message(const char* msg);
-int decode_box_rows();
+int decode_ctas_per_sm();
 
 }  // namespace kv4

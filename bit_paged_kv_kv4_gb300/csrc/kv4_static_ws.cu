@@ -80,17 +80,13 @@ kv4_status kv4_decode_attention_static_ws(const void* q, const kv4_pool* pool,
     return kv4_decode_attention(q, pool, layer_global_scale, block_table, max_pages, seq_lens,
                                 batch, num_q_heads, sm_scale, num_splits, nullptr, 0, out,
                                 out_is_fp32, stream);
-  const int32_t S = num_splits == 0
-                        ? kv4_decode_default_splits(batch, pool->num_kv_heads, max_pages,
-                                                    pool->page_size)
-                        : num_splits;
-  const int64_t need = kv4_decode_workspace_bytes(batch, num_q_heads, pool->head_dim, S);
+  const int64_t need = kv4_decode_workspace_bytes(batch, num_q_heads, pool->head_dim, num_splits);
   if (need > kKv4StaticWorkspaceBytes) {
     char buf[256];
     snprintf(buf, sizeof(buf),
-             "kv4_decode_attention_static_ws: %d requests x %d query heads x %d splits need "
-             "%lld bytes of scratch; the static workspace holds %lld",
-             batch, num_q_heads, S, static_cast<long long>(need),
+             "kv4_decode_attention_static_ws: %d requests x %d query heads with num_splits %d "
+             "need %lld bytes of scratch; the static workspace holds %lld",
+             batch, num_q_heads, num_splits, static_cast<long long>(need),
              static_cast<long long>(kKv4StaticWorkspaceBytes));
     kv4::set_error_message(buf);
     return KV4_EINVAL;
@@ -101,7 +97,7 @@ kv4_status kv4_decode_attention_static_ws(const void* q, const kv4_pool* pool,
     if (s != KV4_OK) return s;
   }
   return kv4_decode_attention(q, pool, layer_global_scale, block_table, max_pages, seq_lens,
-                              batch, num_q_heads, sm_scale, S, ws, need > 0 ? need : 0, out,
+                              batch, num_q_heads, sm_scale, num_splits, ws, need > 0 ? need : 0, out,
                               out_is_fp32, stream);
 }
 

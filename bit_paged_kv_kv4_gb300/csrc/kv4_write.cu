@@ -9,7 +9,10 @@
 // One thread owns 8 consecutive elements (one 16-byte load of bf16); two
 // neighbouring threads form an NVFP4 block, D/8 neighbouring threads a row.
 // All encoder arithmetic is IEEE FP32 with round-to-nearest (no fast-math),
-// in the order the header states, so the bytes match the oracle exactly.
+// in the order the header states, so the bytes match the oracle exactly; the
+// per-element divisions by the block's (or row's) scale use a correctly
+// rounded reciprocal-and-correction division (div_rn), which returns the same
+// value as the IEEE quotient.
 #include <cstdint>
 
 #include "kv4_device.cuh"
@@ -68,10 +71,11 @@ write_kernel(const WriteArgs a) {
     const float denom = __fmul_rn(e4m3_to_f32(S), g);
     uint32_t word = 0;
     if (S != 0u && denom != 0.f) {
+      const float rd = __frcp_rn(denom);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const uint32_t byte = f32x2_to_e2m1x2(__fdiv_rn(x[2 * j], denom),
-                                              __fdiv_rn(x[2 * j + 1], denom));
+        const uint32_t byte = f32x2_to_e2m1x2(div_rn(x[2 * j], denom, rd),
+                                              div_rn(x[2 * j + 1], denom, rd));
         word |= byte << (8 * j);
       }
     }
@@ -91,9 +95,10 @@ write_kernel(const WriteArgs a) {
     const float s = __fdiv_rn(amax, 7.0f);
     uint32_t word = 0;
     if (s != 0.f) {
+      const float rs = __frcp_rn(s);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        int c = __float2int_rn(__fdiv_rn(x[j], s));
+        int c = __float2int_rn(div_rn(x[j], s, rs));
         c = c < -8 ? -8 : (c > 7 ? 7 : c);
         word |= (static_cast<uint32_t>(c) & 0xFu) << (4 * j);
       }

@@ -119,14 +119,9 @@ kv4_status kv4_write(const void* k, const void* v, const int64_t* slot_mapping,
                      int64_t num_tokens, const kv4_pool* pool,
                      const float* layer_global_scale, int32_t fmt, void* stream);
 
-/* Number of KV splits kv4_decode_attention uses when passed num_splits = 0,
- * for a batch of `batch` requests whose block tables have max_pages
- * entries.  Host-only; depends on the current device's SM count. */
-int32_t kv4_decode_default_splits(int32_t batch, int32_t num_kv_heads,
-                                  int32_t max_pages, int32_t page_size);
-
-/* Workspace bytes kv4_decode_attention needs for these sizes (0 when
- * num_splits == 1: one split writes `out` directly). */
+/* Workspace bytes kv4_decode_attention needs for these sizes and this
+ * num_splits (0 when num_splits == 1, which writes `out` directly).  Depends
+ * on the current device's SM count. */
 int64_t kv4_decode_workspace_bytes(int32_t batch, int32_t num_q_heads,
                                    int32_t head_dim, int32_t num_splits);
 
@@ -137,16 +132,22 @@ int64_t kv4_decode_workspace_bytes(int32_t batch, int32_t num_q_heads,
  * h = j / (Hq/Hkv): GQA groups are contiguous), over tokens t < seq_lens[b]
  * stored at slot block_table[b*max_pages + t/P]*P + t%P:
  *     out[b][j] = sum_t softmax_t(sm_scale * <q[b][j], K_hat_t>) V_hat_t
- * with K_hat/V_hat the decoded cache values.  The sequence is cut into
- * num_splits contiguous ranges whose partial softmax states (m, l, o) are
- * merged by a log-sum-exp combine.  seq_lens[b] == 0 gives a zero row.
+ * with K_hat/V_hat the decoded cache values.  seq_lens[b] == 0 gives a zero
+ * row.  Work is cut along the sequence and the partial softmax states
+ * (max, sum, weighted V) of the pieces are merged by a log-sum-exp combine:
+ *   num_splits == 0  one wave of CTAs, each streaming an equal share of all
+ *                    requests' tiles (balanced whatever the length mix);
+ *   num_splits == 1  one CTA per (request, kv head, <= 8 query heads), which
+ *                    writes `out` directly (no workspace, no combine);
+ *   num_splits == S  as 0, and every request's range is also cut into S equal
+ *                    splits, so each head's output merges at least S pieces.
  *   q            device bf16 [B][Hq][D]
  *   layer_global_scale  device float[2] {g_K, g_V} (NVFP4; NULL for INT4)
  *   block_table  device int32 [B][max_pages]; entries past a request's last
  *                page are never read.
  *   seq_lens     device int32 [B]; the decode step's own token (written by
  *                kv4_write beforehand) is included.
- *   num_splits   1..1024, or 0 for kv4_decode_default_splits().
+ *   num_splits   0..1024, see above.
  *   workspace    device scratch of >= kv4_decode_workspace_bytes() bytes
  *                (may be NULL when that is 0); contents on entry ignored.
  *   out          device [B][Hq][D], float32 if out_is_fp32 else bf16.
@@ -199,8 +200,7 @@ kv4_status kv4_dequant_prefix(const kv4_pool* pool,
  *     loading the library holds until the process exits.  A call whose
  *     kv4_decode_workspace_bytes(batch, num_q_heads, head_dim, splits) exceeds
  *     it returns KV4_EINVAL (kv4_last_error_message gives both sizes) and
- *     launches nothing; num_splits = 0 picks kv4_decode_default_splits() as
- *     usual.  One split needs no scratch at all.
+ *     launches nothing.  num_splits == 1 needs no scratch at all.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and keeps it; make that
  *     first call before any stream capture.

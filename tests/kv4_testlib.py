@@ -96,7 +96,7 @@ class Case:
 
     def gpu_out(self, pool, num_splits=0, out_dtype=torch.float32):
         B = len(self.lens)
-        S = num_splits or K.kv4_decode_default_splits(B, self.Hkv, self.table.shape[1], self.P)
+        S = num_splits
         ws = K.alloc_workspace(B, self.Hq, self.D, S)
         out = torch.full((B, self.Hq, self.D), float("nan"), dtype=out_dtype, device="cuda")
         K.kv4_decode_attention(dev_bf16(self.q), pool, self.d_g, torch.from_numpy(self.table).cuda(),

@@ -48,13 +48,14 @@ def test_pool_sizes(lib):
         assert lib.kv4_pool_bytes(ctypes.byref(bad)) == 0
 
 
-def test_workspace_and_splits(lib):
-    assert lib.kv4_decode_workspace_bytes(2, 8, 256, 1) == 0
-    rows = 2 * 8 * 5
-    assert lib.kv4_decode_workspace_bytes(2, 8, 256, 5) == ((rows * 16 + 255) // 256) * 256 + rows * 256 * 4
-    s = lib.kv4_decode_default_splits(1, 4, 4096, 256)
-    assert 1 <= s <= 1024
-    assert lib.kv4_decode_default_splits(64, 8, 1, 64) == 1      # one tile: one split
+def test_workspace_sizes(lib):
+    assert lib.kv4_decode_workspace_bytes(2, 8, 256, 1) == 0          # direct output
+    a0 = lib.kv4_decode_workspace_bytes(2, 8, 256, 0)
+    a5 = lib.kv4_decode_workspace_bytes(2, 8, 256, 5)
+    assert 0 < a0 < a5
+    # slots grow by one per (request, head, split): 16 heads x 4 more splits
+    assert a5 - a0 == 2 * 8 * 4 * 8 * (16 + 256 * 4)
+    assert lib.kv4_decode_workspace_bytes(0, 8, 256, 0) == 0
 
 
 def _status(lib, st):
