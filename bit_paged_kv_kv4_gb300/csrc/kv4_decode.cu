@@ -72,7 +72,8 @@ struct Geo {
   static constexpr int OFF_KS = 2 * kTT * RB;
   static constexpr int OFF_VS = 2 * kTT * RB + kTT * SB;
   static constexpr int RING = kNW * kNS * STAGE;
-  static constexpr int ACC = 8 * D * 4;                        // merged O of one segment
+  static constexpr int AS = MT * 4 + 4;                        // merge row per lane (floats)
+  static constexpr int ACC = 32 * AS * 4;                      // merged O of one segment
   static constexpr int META = kNW * 8 * 3 * 4;                 // (m_x, m_y, l) per warp and head
   static constexpr int SEG = kMaxSeg * 20 + 16;        // keeps the int64 scratch 8-byte aligned
   static constexpr int SMEM = RING + ACC + META + SEG + 64 + kNW * kNS * 8 + 1024;
@@ -363,30 +364,27 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
         const int r = p_first + (win + 1) * 32 + lane;
         pg_nxt = r <= p_last ? __ldg(bt + r) : 0;
       }
-      int pages[kTT / 16], offs[kTT / 16];
-#pragma unroll
-      for (int u = 0; u < kTT / 16; ++u) {
-        int pu = pi, ou = po + u * box;         // a box never straddles a page
-        if (ou >= a.P) { ou -= a.P; ++pu; }
-        const int rel = pu - p_first;
-        const int pcv = __shfl_sync(kFull, pg_cur, rel & 31);
-        const int pnv = __shfl_sync(kFull, pg_nxt, rel & 31);
-        pages[u] = ((rel >> 5) == win) ? pcv : pnv;
-        offs[u] = ou;
-      }
+      // the tile's one or two boxes (32 tokens; a box never straddles a page)
+      int pu1 = pi, ou1 = po + box;
+      if (ou1 >= a.P) { ou1 -= a.P; ++pu1; }
+      const int rel0 = pi - p_first, rel1 = pu1 - p_first;
+      const int pc0 = __shfl_sync(kFull, pg_cur, rel0 & 31), pn0 = __shfl_sync(kFull, pg_nxt, rel0 & 31);
+      const int pc1 = __shfl_sync(kFull, pg_cur, rel1 & 31), pn1 = __shfl_sync(kFull, pg_nxt, rel1 & 31);
+      const int page0 = ((rel0 >> 5) == win) ? pc0 : pn0;
+      const int page1 = ((rel1 >> 5) == win) ? pc1 : pn1;
       if (lane == 0) {
         const uint32_t st = ring + (issued % kNS) * Gm::STAGE;
         const uint32_t bar = bars + 8 * (issued % kNS);
         mbar_arrive_expect_tx(bar, nsub * box * (2 * RB + 2 * SB));
 #pragma unroll
-        for (int u = 0; u < kTT / 16; ++u) {
+        for (int u = 0; u < 2; ++u) {
           if (u < nsub) {
-            int page = pages[u];
+            int page = u ? page1 : page0;
             if (page < 0 || page >= a.num_pages) {
               set_error(a.err, KV4_EBOUNDS);
               page = 0;
             }
-            const int off = offs[u];
+            const int off = u ? ou1 : po;
             const int64_t chunk = (static_cast<int64_t>(page) * a.Hkv + h) * a.chunk_bytes;
             const int row = static_cast<int>(chunk / RB) + off;
             tma_load_2d(st + u * box * RB, &tmap, 0, row, bar, pol);
@@ -643,7 +641,6 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
           if constexpr (FMT == KV4_NVFP4) {
             // block scales of the thread's head-dim range, per token
             constexpr int NVB = (VB >= 8) ? VB / 8 : 1;
-            const int blk0 = (VB * grp) / 8;
             const uint32_t xa = load_scale_bytes<NVB>(st + vs_off + 16 * kg * SB);
             const uint32_t xb = load_scale_bytes<NVB>(st + vs_off + (16 * kg + 1) * SB);
             const uint32_t xc = load_scale_bytes<NVB>(st + vs_off + (16 * kg + 8) * SB);
@@ -676,7 +673,7 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
 #pragma unroll
               for (int mm = 0; mm < 4; ++mm) {
                 const int mi = 4 * j + mm;
-                const int bj = (VB * grp + mi) / 8 - blk0;
+                const int bj = (VB >= 8) ? mi / 8 : 0;   // block of this m-tile among the thread's two
                 const uint32_t a0 = hmul2(vl[mm], sab[bj]);
                 const uint32_t a1 = hmul2(vh[mm], sab[bj]);
                 const uint32_t a2 = hmul2(ul[mm], scd[bj]);
@@ -741,20 +738,20 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
         const float mw = sMeta[(warp * 8 + g) * 3 + 1];
         wgt[c] = (mw == -INFINITY) ? 0.f : fast_exp2(mw - My);
       }
+      // The merge buffer keeps the MMA fragment layout: lane L's o[mi][0..3] at
+      // sAcc[L * AS + 4 mi]; the padded row makes every float4 access
+      // conflict-free.  Warps add their scaled states in warp order.
       for (int w = 0; w < kNW; ++w) {
         if (warp == w) {
+          float* row = sAcc + lane * Gm::AS;
 #pragma unroll
           for (int mi = 0; mi < MT; ++mi) {
-            const int d = 2 * (VB * grp + mi);
-            float* r0 = sAcc + (2 * tig) * D + d;
-            float* r1 = sAcc + (2 * tig + 1) * D + d;
-            if (w == 0) {
-              r0[0] = o[mi][0] * wgt[0]; r1[0] = o[mi][1] * wgt[1];
-              r0[1] = o[mi][2] * wgt[0]; r1[1] = o[mi][3] * wgt[1];
-            } else {
-              r0[0] += o[mi][0] * wgt[0]; r1[0] += o[mi][1] * wgt[1];
-              r0[1] += o[mi][2] * wgt[0]; r1[1] += o[mi][3] * wgt[1];
+            float4 v = make_float4(o[mi][0] * wgt[0], o[mi][1] * wgt[1], o[mi][2] * wgt[0], o[mi][3] * wgt[1]);
+            if (w != 0) {
+              const float4 p = *reinterpret_cast<const float4*>(row + 4 * mi);
+              v.x += p.x; v.y += p.y; v.z += p.z; v.w += p.w;
             }
+            *reinterpret_cast<float4*>(row + 4 * mi) = v;
           }
         }
         __syncthreads();
@@ -773,7 +770,11 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
           const float mw = sMeta[(w * 8 + g) * 3 + 0];
           l += (mw == -INFINITY) ? 0.f : sMeta[(w * 8 + g) * 3 + 2] * fast_exp2(mw - Mx);
         }
-        const float4 acc = *reinterpret_cast<const float4*>(sAcc + g * D + d);
+        // (d, g) lives in lane (grp, tig) = ((d/2) / VB, g/2), o[mi][g%2] with
+        // mi = (d/2) % VB; d+1 in o[mi][g%2 + 2]; d+2, d+3 in o[mi+1][...].
+        const int hd = d >> 1, mi = hd % VB, c = g & 1;
+        const float* row = sAcc + ((hd / VB) * 4 + (g >> 1)) * Gm::AS + 4 * mi + c;
+        const float4 acc = make_float4(row[0], row[2], row[4], row[6]);
         if (direct) {
           const float inv = (l > 0.f && My != -INFINITY) ? gv * fast_exp2(My - Mx) / l : 0.f;
           const int64_t row = static_cast<int64_t>(b) * a.Hq + hq0 + g;
@@ -801,11 +802,37 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
 constexpr int kCombineThreads = 256;
 constexpr int kMaxPieces = 2048;
 
+// Block-wide max / sum over kCombineThreads threads: a butterfly inside each
+// warp, then the warp results in warp order.  The tree is fixed, so a sum is
+// the same bits on every run.  `red` holds kCombineThreads / 32 floats.
+__device__ __forceinline__ float block_max(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float r = red[0];
+#pragma unroll
+  for (int w = 1; w < kCombineThreads / 32; ++w) r = fmaxf(r, red[w]);
+  return r;
+}
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float r = red[0];
+#pragma unroll
+  for (int w = 1; w < kCombineThreads / 32; ++w) r += red[w];
+  return r;
+}
+
 __global__ void __launch_bounds__(kCombineThreads)
 combine_kernel(const DecodeArgs a) {
   __shared__ int64_t s_slot[kMaxPieces];
   __shared__ int64_t s_red[kCombineThreads / 32];
-  __shared__ float s_f[kCombineThreads];
+  __shared__ float s_f[kCombineThreads / 32];
   __shared__ float4 s_o[kCombineThreads];
   const int j = blockIdx.x, b = blockIdx.y;
   const int D = a.D, S = a.num_splits;
@@ -871,49 +898,22 @@ combine_kernel(const DecodeArgs a) {
   const int P = static_cast<int>(npieces < kMaxPieces ? npieces : kMaxPieces);
   if (npieces > kMaxPieces && tid == 0) set_error(a.err, KV4_EUNSUPPORTED);
 
-  // ---- maxima of the piece states --------------------------------------------
+  // ---- maxima of the piece states, normaliser l ------------------------------
   float mx = -INFINITY, my = -INFINITY;
   for (int p = tid; p < P; p += kCombineThreads) {
     const float4 m = *reinterpret_cast<const float4*>(a.part_ml + (s_slot[p] * 8 + g) * 4);
     mx = fmaxf(mx, m.x);
     my = fmaxf(my, m.z);
   }
-  s_f[tid] = mx;
-  __syncthreads();
-  if (tid == 0) {
-    float v = -INFINITY;
-    for (int t = 0; t < kCombineThreads; ++t) v = fmaxf(v, s_f[t]);
-    s_red[0] = __float_as_int(v);
-  }
-  __syncthreads();
-  const float Mx = __int_as_float(static_cast<int>(s_red[0]));
-  __syncthreads();
-  s_f[tid] = my;
-  __syncthreads();
-  if (tid == 0) {
-    float v = -INFINITY;
-    for (int t = 0; t < kCombineThreads; ++t) v = fmaxf(v, s_f[t]);
-    s_red[0] = __float_as_int(v);
-  }
-  __syncthreads();
-  const float My = __int_as_float(static_cast<int>(s_red[0]));
-  __syncthreads();
-
-  // ---- normaliser l, summed per thread then in thread order ---------------------
+  const float Mx = block_max(mx, s_f);
+  const float My = block_max(my, s_f);
+  // per-thread partial sums, then a fixed reduction tree: deterministic
   float lp = 0.f;
   for (int p = tid; p < P; p += kCombineThreads) {
     const float4 m = *reinterpret_cast<const float4*>(a.part_ml + (s_slot[p] * 8 + g) * 4);
     lp += (m.x == -INFINITY) ? 0.f : m.y * fast_exp2(m.x - Mx);
   }
-  s_f[tid] = lp;
-  __syncthreads();
-  if (tid == 0) {
-    float v = 0.f;
-    for (int t = 0; t < kCombineThreads; ++t) v += s_f[t];
-    s_f[0] = v;
-  }
-  __syncthreads();
-  const float l = s_f[0];
+  const float l = block_sum(lp, s_f);
 
   // ---- weighted sum of the pieces' o: thread = (piece group, 4 columns) --------
   const int cols = D / 4;                        // float4 columns
