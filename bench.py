@@ -349,8 +349,6 @@ def kv4_arm(args):
         s.write()
         s.decode()
     torch.cuda.synchronize()
-    ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
     ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
@@ -361,12 +359,10 @@ def kv4_arm(args):
         torch.cuda.synchronize()
         t_start.record()
         for i in range(args.steps):
-            ev_step[i][0].record()
             s.write()
             ev_dec[i][0].record()
             s.decode()
             ev_dec[i][1].record()
-            ev_step[i][1].record()
         t_end.record()
         torch.cuda.synchronize()
         barrier(pg, device)

@@ -41,6 +41,7 @@
 //    O^T += V^T P^T (A = dequantised V^T, 16 head-dim rows per MMA).
 //    m16n8k16 f16 MMA, FP32 accumulate; PV weights as f16 hi + lo pairs.
 #include <cstdint>
+#include <utility>
 
 #include "kv4_device.cuh"
 #include "kv4_internal.h"
@@ -188,6 +189,8 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm)
 decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap) {
   using Gm = Geo<D, FMT>;
   constexpr int RB = Gm::RB, SB = Gm::SB, KB = Gm::KB, VB = Gm::VB, MT = Gm::MT;
+  grid_dep_launch();   // the combine may be scheduled now; it waits for this grid
+  grid_dep_wait();     // inputs written by the previous kernel are visible
   constexpr int NM = kTT / 16;            // 16-token groups per tile (QK m-tiles = PV k-groups)
   extern __shared__ uint8_t smem_raw[];
 
@@ -830,6 +833,7 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 
 __global__ void __launch_bounds__(kCombineThreads)
 combine_kernel(const DecodeArgs a) {
+  grid_dep_wait();     // the pieces of the split kernel are complete
   __shared__ int64_t s_slot[kMaxPieces];
   __shared__ int64_t s_red[kCombineThreads / 32];
   __shared__ float s_f[kCombineThreads / 32];
@@ -942,6 +946,25 @@ combine_kernel(const DecodeArgs a) {
 }
 
 // ------------------------------------------------------------------ launch
+// Launch with programmatic stream serialisation: the kernel may be scheduled
+// while the previous kernel on the stream drains (its launch latency hides
+// behind that kernel's tail); it reads nothing before grid_dep_wait().
+template <typename... P, typename... A>
+static cudaError_t launch_pdl(void (*k)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              A&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, std::forward<A>(args)...);
+}
+
 template <int D, int FMT>
 static cudaError_t launch_split(const DecodeArgs& a, const CUtensorMap& map, cudaStream_t st) {
   using Gm = Geo<D, FMT>;
@@ -954,8 +977,7 @@ static cudaError_t launch_split(const DecodeArgs& a, const CUtensorMap& map, cud
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  k<<<a.n_cta, kNW * 32, Gm::SMEM, st>>>(a, map);
-  return cudaGetLastError();
+  return launch_pdl(k, dim3(a.n_cta), dim3(kNW * 32), Gm::SMEM, st, a, map);
 }
 
 int decode_tile_tokens() { return kTT; }
@@ -978,8 +1000,7 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& map, cudaStrea
     }
   }
   if (e != cudaSuccess || a.unit_ctas) return e;
-  combine_kernel<<<dim3(a.Hq, a.B), kCombineThreads, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3(a.Hq, a.B), dim3(kCombineThreads), 0, st, a);
 }
 
 }  // namespace kv4

@@ -25,6 +25,19 @@ __device__ __forceinline__ void set_error(int* err, int code) {
   if (err != nullptr) atomicCAS(err, 0, code);
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation may start before the previous kernel on the stream has
+// finished; grid_dep_wait() blocks until that kernel has completed and its
+// memory is visible (a no-op for a normally launched kernel).
+// grid_dep_launch() lets the next such kernel be scheduled early; it still
+// waits in its own grid_dep_wait() for this grid to complete.
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------ conversions
 // Two FP32 values -> one byte of two E2M1 codes, round to nearest even,
 // saturating at 6, sign kept: `lo` goes to the low nibble.

@@ -22,6 +22,7 @@ namespace kv4 {
 
 __global__ void __launch_bounds__(256)
 write_kernel(const WriteArgs a) {
+  grid_dep_launch();   // a following decode launch may be scheduled early
   const int D = a.D;
   const int tpr = D / 8;                          // threads per row
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
