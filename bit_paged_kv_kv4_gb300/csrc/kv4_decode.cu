@@ -819,6 +819,28 @@ __device__ __forceinline__ float block_max(float v, float* red) {
   for (int w = 1; w < kCombineThreads / 32; ++w) r = fmaxf(r, red[w]);
   return r;
 }
+// Two block-wide maxima with one pair of barriers; `red` holds
+// 2 * kCombineThreads / 32 floats.
+__device__ __forceinline__ void block_max2(float v, float w, float* red, float& rv, float& rw) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    w = fmaxf(w, __shfl_xor_sync(0xffffffffu, w, o));
+  }
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) {
+    red[threadIdx.x >> 5] = v;
+    red[kCombineThreads / 32 + (threadIdx.x >> 5)] = w;
+  }
+  __syncthreads();
+  rv = red[0];
+  rw = red[kCombineThreads / 32];
+#pragma unroll
+  for (int k = 1; k < kCombineThreads / 32; ++k) {
+    rv = fmaxf(rv, red[k]);
+    rw = fmaxf(rw, red[kCombineThreads / 32 + k]);
+  }
+}
 __device__ __forceinline__ float block_sum(float v, float* red) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -836,7 +858,7 @@ combine_kernel(const DecodeArgs a) {
   grid_dep_wait();     // the pieces of the split kernel are complete
   __shared__ int64_t s_slot[kMaxPieces];
   __shared__ int64_t s_red[kCombineThreads / 32];
-  __shared__ float s_f[kCombineThreads / 32];
+  __shared__ float s_f[2 * kCombineThreads / 32];
   __shared__ float4 s_o[kCombineThreads];
   const int j = blockIdx.x, b = blockIdx.y;
   const int D = a.D, S = a.num_splits;
@@ -862,8 +884,12 @@ combine_kernel(const DecodeArgs a) {
   const bool may_be_empty = T < a.n_cta;   // only then can a CTA range hold no tile
 
   // ---- list the pieces: split s holds CTAs part_of(x0)..part_of(x1-1) ----------
-  int64_t npieces = 0;
-  for (int s0 = 0; s0 < S; s0 += kCombineThreads) {
+  // One split and no empty CTA range (the usual case): the pieces are the
+  // CTAs c0 .. c1 in order, slot c + u.  Otherwise list them in shared memory.
+  const int64_t c0 = part_of(start, T, a.n_cta);
+  const bool contiguous = (S == 1 && !may_be_empty);
+  int64_t npieces = contiguous ? part_of(start + n_u - 1, T, a.n_cta) - c0 + 1 : 0;
+  for (int s0 = 0; !contiguous && s0 < S; s0 += kCombineThreads) {
     const int s = s0 + tid;
     int64_t cf = 0, cl = -1;
     if (s < S) {
@@ -899,22 +925,23 @@ combine_kernel(const DecodeArgs a) {
     npieces += tot;
     __syncthreads();
   }
-  const int P = static_cast<int>(npieces < kMaxPieces ? npieces : kMaxPieces);
-  if (npieces > kMaxPieces && tid == 0) set_error(a.err, KV4_EUNSUPPORTED);
+  const int P = static_cast<int>((contiguous || npieces < kMaxPieces) ? npieces : kMaxPieces);
+  if (!contiguous && npieces > kMaxPieces && tid == 0) set_error(a.err, KV4_EUNSUPPORTED);
+  auto slot_of = [&](int p) -> int64_t { return contiguous ? c0 + p + u : s_slot[p]; };
 
   // ---- maxima of the piece states, normaliser l ------------------------------
   float mx = -INFINITY, my = -INFINITY;
   for (int p = tid; p < P; p += kCombineThreads) {
-    const float4 m = *reinterpret_cast<const float4*>(a.part_ml + (s_slot[p] * 8 + g) * 4);
+    const float4 m = *reinterpret_cast<const float4*>(a.part_ml + (slot_of(p) * 8 + g) * 4);
     mx = fmaxf(mx, m.x);
     my = fmaxf(my, m.z);
   }
-  const float Mx = block_max(mx, s_f);
-  const float My = block_max(my, s_f);
+  float Mx, My;
+  block_max2(mx, my, s_f, Mx, My);
   // per-thread partial sums, then a fixed reduction tree: deterministic
   float lp = 0.f;
   for (int p = tid; p < P; p += kCombineThreads) {
-    const float4 m = *reinterpret_cast<const float4*>(a.part_ml + (s_slot[p] * 8 + g) * 4);
+    const float4 m = *reinterpret_cast<const float4*>(a.part_ml + (slot_of(p) * 8 + g) * 4);
     lp += (m.x == -INFINITY) ? 0.f : m.y * fast_exp2(m.x - Mx);
   }
   const float l = block_sum(lp, s_f);
@@ -925,7 +952,7 @@ combine_kernel(const DecodeArgs a) {
   const int col = tid % cols, grp = tid / cols;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int p = grp; p < P; p += groups) {
-    const int64_t slot = s_slot[p];
+    const int64_t slot = slot_of(p);
     const float mz = a.part_ml[(slot * 8 + g) * 4 + 2];
     const float w = (mz == -INFINITY) ? 0.f : fast_exp2(mz - My);
     const float4 v = __ldg(reinterpret_cast<const float4*>(a.part_o + (slot * 8 + g) * D) + col);
