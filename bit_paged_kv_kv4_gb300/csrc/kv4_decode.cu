@@ -252,6 +252,14 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
   const uint32_t v_offb = Gm::OFF_VC + swz<RB>(2 * tig + 1, VB * grp);
   const uint32_t ks_off = Gm::OFF_KS + grp * SB + (D / 64) * tig;
   const uint32_t vs_off = Gm::OFF_VS + 2 * tig * SB + (VB * grp) / 8;
+  // NVFP4 V in token-pair rows (2 code rows of RB bytes per pair, D/8 scale
+  // bytes per pair): thread (grp, tig) reads head dims [D0, D0 + D/8) of the
+  // pairs holding tokens (16kg + 2tig, +1) and (16kg + 2tig + 8, +9).
+  constexpr int D0S = D / 8;                          // dims (= bytes) per thread
+  const int D0 = D0S * grp;
+  const uint32_t vp_off0 = Gm::OFF_VC + swz<RB>(2 * tig + D0 / RB, D0 % RB);
+  const uint32_t vp_off1 = Gm::OFF_VC + swz<RB>(2 * tig + D0 / RB, D0 % RB + 16);
+  const uint32_t vps_off = Gm::OFF_VS + tig * (D / 8) + 2 * (D0 / 16);
 
   // ---- per-warp running state ----------------------------------------------
   const uint64_t pol = policy_evict_first();
@@ -636,56 +644,47 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
 #pragma unroll
         for (int kg = 0; kg < NM; ++kg) {
           const int ta = kg * 16 + 2 * tig;       // tokens ta, ta+1 (k 2tig..) and ta+8, ta+9
-          uint32_t wa[VB / 4], wb[VB / 4], wc[VB / 4], wd[VB / 4];
-          load_bytes<VB>(st + v_offa + 16 * kg * RB, 0, wa);
-          load_bytes<VB>(st + v_offb + 16 * kg * RB, 0, wb);
-          load_bytes<VB>(st + v_offa + (16 * kg + 8) * RB, 0, wc);
-          load_bytes<VB>(st + v_offb + (16 * kg + 8) * RB, 0, wd);
           if constexpr (FMT == KV4_NVFP4) {
-            // block scales of the thread's head-dim range, per token
-            constexpr int NVB = (VB >= 8) ? VB / 8 : 1;
-            const uint32_t xa = load_scale_bytes<NVB>(st + vs_off + 16 * kg * SB);
-            const uint32_t xb = load_scale_bytes<NVB>(st + vs_off + (16 * kg + 1) * SB);
-            const uint32_t xc = load_scale_bytes<NVB>(st + vs_off + (16 * kg + 8) * SB);
-            const uint32_t xd = load_scale_bytes<NVB>(st + vs_off + (16 * kg + 9) * SB);
+            // byte d of a pair row -> f16x2 (element d of the even token, of the
+            // odd token): exactly an A-fragment register of V^T, no regrouping
+            uint32_t wab[D0S / 4], wcd[D0S / 4];
+            load_bytes<D0S>(st + vp_off0 + 16 * kg * RB, st + vp_off1 + 16 * kg * RB, wab);
+            load_bytes<D0S>(st + vp_off0 + (16 * kg + 8) * RB, st + vp_off1 + (16 * kg + 8) * RB, wcd);
+            // the pairs' block scales: bytes (s_even, s_odd) per block
+            constexpr int NSB = (D0S >= 32) ? 4 : 2;
+            const uint32_t xab = load_scale_bytes<NSB>(st + vps_off + kg * D);
+            const uint32_t xcd = load_scale_bytes<NSB>(st + vps_off + kg * D + D / 2);
             // mask tokens past the end: a zero scale zeroes the (finite) codes
-            const uint32_t ma = (ta < valid) ? 0xFFFFu : 0u, mb = (ta + 1 < valid) ? 0xFFFF0000u : 0u;
-            const uint32_t mc = (ta + 8 < valid) ? 0xFFFFu : 0u, md = (ta + 9 < valid) ? 0xFFFF0000u : 0u;
+            const uint32_t mab = ((ta < valid) ? 0xFFFFu : 0u) | ((ta + 1 < valid) ? 0xFFFF0000u : 0u);
+            const uint32_t mcd = ((ta + 8 < valid) ? 0xFFFFu : 0u) | ((ta + 9 < valid) ? 0xFFFF0000u : 0u);
             uint32_t sab[2], scd[2];
-            {
-              // each token's scale bytes -> f16 (one conversion per token's byte pair)
-              uint32_t fa, fb, fc, fd;
-              e4m3x4_to_f16x2x2(xa | (xb << 16), fa, fb);
-              e4m3x4_to_f16x2x2(xc | (xd << 16), fc, fd);
-              sab[0] = prmt(fa, fb, 0x5410u) & (ma | mb);   // first block: (s(ta), s(tb))
-              scd[0] = prmt(fc, fd, 0x5410u) & (mc | md);
-              sab[1] = prmt(fa, fb, 0x7632u) & (ma | mb);   // second block (NVB == 2)
-              scd[1] = prmt(fc, fd, 0x7632u) & (mc | md);
-            }
+            e4m3x4_to_f16x2x2(xab, sab[0], sab[1]);
+            e4m3x4_to_f16x2x2(xcd, scd[0], scd[1]);
+            sab[0] &= mab; sab[1] &= mab;
+            scd[0] &= mcd; scd[1] &= mcd;
 #pragma unroll
-            for (int j = 0; j < VB / 4; ++j) {
-              const uint32_t lab = (wa[j] & 0x0F0F0F0Fu) | ((wb[j] << 4) & 0xF0F0F0F0u);
-              const uint32_t hab = ((wa[j] >> 4) & 0x0F0F0F0Fu) | (wb[j] & 0xF0F0F0F0u);
-              const uint32_t lcd = (wc[j] & 0x0F0F0F0Fu) | ((wd[j] << 4) & 0xF0F0F0F0u);
-              const uint32_t hcd = ((wc[j] >> 4) & 0x0F0F0F0Fu) | (wd[j] & 0xF0F0F0F0u);
-              uint32_t vl[4], vh[4], ul[4], uh[4];
-              e2m1x8_to_f16x2x4(lab, vl);
-              e2m1x8_to_f16x2x4(hab, vh);
-              e2m1x8_to_f16x2x4(lcd, ul);
-              e2m1x8_to_f16x2x4(hcd, uh);
+            for (int j = 0; j < D0S / 4; ++j) {
+              uint32_t f[4], h[4];
+              e2m1x8_to_f16x2x4(wab[j], f);
+              e2m1x8_to_f16x2x4(wcd[j], h);
 #pragma unroll
-              for (int mm = 0; mm < 4; ++mm) {
-                const int mi = 4 * j + mm;
-                const int bj = (VB >= 8) ? mi / 8 : 0;   // block of this m-tile among the thread's two
-                const uint32_t a0 = hmul2(vl[mm], sab[bj]);
-                const uint32_t a1 = hmul2(vh[mm], sab[bj]);
-                const uint32_t a2 = hmul2(ul[mm], scd[bj]);
-                const uint32_t a3 = hmul2(uh[mm], scd[bj]);
+              for (int hh = 0; hh < 2; ++hh) {
+                const int mi = 2 * j + hh;                 // dims D0 + 2mi, D0 + 2mi + 1
+                const int bj = (VB >= 8) ? mi / 8 : 0;     // block of this m-tile among the thread's
+                const uint32_t a0 = hmul2(f[2 * hh], sab[bj]);
+                const uint32_t a1 = hmul2(f[2 * hh + 1], sab[bj]);
+                const uint32_t a2 = hmul2(h[2 * hh], scd[bj]);
+                const uint32_t a3 = hmul2(h[2 * hh + 1], scd[bj]);
                 mma_f16_16816(o[mi], a0, a1, a2, a3, pb[kg][0], pb[kg][1]);
                 mma_f16_16816(o[mi], a0, a1, a2, a3, pl[kg][0], pl[kg][1]);
               }
             }
           } else {
+            uint32_t wa[VB / 4], wb[VB / 4], wc[VB / 4], wd[VB / 4];
+            load_bytes<VB>(st + v_offa + 16 * kg * RB, 0, wa);
+            load_bytes<VB>(st + v_offb + 16 * kg * RB, 0, wb);
+            load_bytes<VB>(st + v_offa + (16 * kg + 8) * RB, 0, wc);
+            load_bytes<VB>(st + v_offb + (16 * kg + 8) * RB, 0, wd);
 #pragma unroll
             for (int j = 0; j < VB / 4; ++j) {
 #pragma unroll

@@ -7,7 +7,8 @@
 // (token, head, K|V) row into 16 E4M3 bytes: x_hat = (e2m1 * e4m3) * g in
 // FP32 (NVFP4) or code * s (INT4), then E4M3(x_hat / s_fp8) with RNE and
 // saturation; the division is the correctly rounded div_rn.  Pure streaming:
-// one 8-byte code load, one scale, one 16-byte store.
+// one code load (8 bytes; 16 for the token-pair rows of NVFP4 V, of which
+// this token's nibbles are kept), one scale, one 16-byte store.
 #include <cstdint>
 
 #include "kv4_device.cuh"
@@ -42,17 +43,35 @@ prefix_kernel(const PrefixArgs a) {
   const int off = t % a.P;
   const uint8_t* chunk = a.pool + (static_cast<int64_t>(page) * a.Hkv + h) * a.chunk_bytes;
   const int RB = D / 2;
-  const uint2 codes = *reinterpret_cast<const uint2*>(
-      chunk + static_cast<int64_t>(kind) * a.P * RB + static_cast<int64_t>(off) * RB + part * 8);
+  uint2 codes;
+  if (a.fmt == KV4_NVFP4 && kind == 1) {
+    // V is stored in token pairs: byte d of pair row off/2 holds element d of
+    // this token in nibble off%2.  Gather the block's 16 nibbles back into
+    // the packed order (element 2j in the low nibble of byte j).
+    const uint4 w = *reinterpret_cast<const uint4*>(
+        chunk + static_cast<int64_t>(a.P) * RB + static_cast<int64_t>(off >> 1) * D + part * 16);
+    const int sh = 4 * (off & 1);
+    const uint32_t x0 = (w.x >> sh) & 0x0F0F0F0Fu, x1 = (w.y >> sh) & 0x0F0F0F0Fu;
+    const uint32_t x2 = (w.z >> sh) & 0x0F0F0F0Fu, x3 = (w.w >> sh) & 0x0F0F0F0Fu;
+    // byte pairs (n_2j, n_2j+1) -> one byte each, then keep bytes 0 and 2
+    codes.x = prmt(x0 | (x0 >> 4), x1 | (x1 >> 4), 0x6420u);
+    codes.y = prmt(x2 | (x2 >> 4), x3 | (x3 >> 4), 0x6420u);
+  } else {
+    codes = *reinterpret_cast<const uint2*>(
+        chunk + static_cast<int64_t>(kind) * a.P * RB + static_cast<int64_t>(off) * RB + part * 8);
+  }
   const float s8 = __ldg(a.fp8_scale + kind);
   const float r8 = __frcp_rn(s8);
 
   float xh[16];
   if (a.fmt == KV4_NVFP4) {
     const int SB = D / 16;
-    const uint8_t* sc = chunk + static_cast<int64_t>(a.P) * D + static_cast<int64_t>(kind) * a.P * SB +
-                        static_cast<int64_t>(off) * SB;
-    const float s = e4m3_to_f32(sc[part]);    // one block of 16 per thread
+    // K: one scale row per token; V: pair rows, byte 2*blk + off%2
+    const uint8_t* sc = (kind == 0)
+        ? chunk + static_cast<int64_t>(a.P) * D + static_cast<int64_t>(off) * SB + part
+        : chunk + static_cast<int64_t>(a.P) * D + static_cast<int64_t>(a.P) * SB +
+              static_cast<int64_t>(off >> 1) * 2 * SB + 2 * part + (off & 1);
+    const float s = e4m3_to_f32(*sc);          // one block of 16 per thread
     const float g = __ldg(a.gscale + kind);
     uint32_t h2[8];
     e2m1x8_to_f16x2x4(codes.x, *reinterpret_cast<uint32_t(*)[4]>(h2));

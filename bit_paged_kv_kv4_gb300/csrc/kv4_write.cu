@@ -8,6 +8,8 @@
 //
 // One thread owns 8 consecutive elements (one 16-byte load of bf16); two
 // neighbouring threads form an NVFP4 block, D/8 neighbouring threads a row.
+// NVFP4 V goes to the token-pair rows the decode kernel reads (element d of
+// tokens 2p and 2p+1 share a byte); K and INT4 rows are one per token.
 // All encoder arithmetic is IEEE FP32 with round-to-nearest (no fast-math),
 // in the order the header states, so the bytes match the oracle exactly; the
 // per-element divisions by the block's (or row's) scale use a correctly
@@ -80,14 +82,32 @@ write_kernel(const WriteArgs a) {
         word |= byte << (8 * j);
       }
     }
-    if (store) {
-      uint8_t* codes = chunk + static_cast<int64_t>(kind) * a.P * RB + static_cast<int64_t>(off) * RB;
+    if (store && kind == 0) {
+      uint8_t* codes = chunk + static_cast<int64_t>(off) * RB;
       *reinterpret_cast<uint32_t*>(codes + part * 4) = word;
       if ((part & 1) == 0) {
         const int SB = D / 16;
-        uint8_t* sc = chunk + static_cast<int64_t>(a.P) * D + static_cast<int64_t>(kind) * a.P * SB +
-                      static_cast<int64_t>(off) * SB;
+        uint8_t* sc = chunk + static_cast<int64_t>(a.P) * D + static_cast<int64_t>(off) * SB;
         sc[part >> 1] = static_cast<uint8_t>(S);
+      }
+    } else if (store) {
+      // V rows are stored in token pairs: byte d of pair row off/2 holds element
+      // d of the even token (low nibble) and of the odd token (high nibble).
+      // This token's 8 elements go to 8 consecutive bytes, in its own nibbles;
+      // the partner token may be written concurrently, so the update is an
+      // atomic clear and set of those nibbles only.
+      const uint32_t lo4 = word & 0x0F0F0F0Fu, hi4 = (word >> 4) & 0x0F0F0F0Fu;
+      const uint64_t spread = (static_cast<uint64_t>(prmt(lo4, hi4, 0x7362u)) << 32) | prmt(lo4, hi4, 0x5140u);
+      const int sh = 4 * (off & 1);
+      unsigned long long* dst = reinterpret_cast<unsigned long long*>(
+          chunk + static_cast<int64_t>(a.P) * RB + static_cast<int64_t>(off >> 1) * D + part * 8);
+      atomicAnd(dst, ~(0x0F0F0F0F0F0F0F0Full << sh));
+      atomicOr(dst, static_cast<unsigned long long>(spread << sh));
+      if ((part & 1) == 0) {
+        const int SB = D / 16;
+        uint8_t* sc = chunk + static_cast<int64_t>(a.P) * D + static_cast<int64_t>(a.P) * SB +
+                      static_cast<int64_t>(off >> 1) * 2 * SB;
+        sc[2 * (part >> 1) + (off & 1)] = static_cast<uint8_t>(S);
       }
     }
   } else {

@@ -108,8 +108,8 @@ def lse_combine(m, l, o):
 def _dequant_f32(pool, spec, gscale, page, off, h, kind):
     """Decoded rows in float32 as the prefix path computes them:
     NVFP4 (e2m1 * e4m3) * g, INT4 code * s -- each product rounded to float32."""
-    codes = pool[pool_mod._row_index(spec, page, off, h, kind + "c")]
-    sb = pool[pool_mod._row_index(spec, page, off, h, kind + "s")]
+    codes = pool_mod.get_codes(pool, spec, page, off, h, kind)
+    sb = pool_mod.get_scales(pool, spec, page, off, h, kind)
     n = _unpack_nibbles(codes)
     if spec.fmt == pool_mod.NVFP4:
         g = np.float32(gscale[0] if kind == "k" else gscale[1])

@@ -15,9 +15,21 @@ chunk holds four regions, each a whole number of 16-byte units:
     NVFP4: [K codes P*D/2][V codes P*D/2][K scales P*D/16][V scales P*D/16]
     INT4 : [K codes P*D/2][V codes P*D/2][K scale f32 * P][V scale f32 * P]
 
-so chunk_bytes = P*(D + D/8) for NVFP4 and P*(D + 8) for INT4.  Token
-``off`` of a page owns row ``off`` of every region.  A slot is
-``page * P + off``; a negative slot means "do not store".
+so chunk_bytes = P*(D + D/8) for NVFP4 and P*(D + 8) for INT4.
+
+Row order inside a region:
+
+* K codes and scales, and every INT4 region: token ``off`` of the page owns
+  row ``off`` (D/2 code bytes, element 2j in the low nibble of byte j; D/16
+  scale bytes, or one FP32 scale).
+* NVFP4 V: tokens are stored in pairs (2p, 2p+1).  Code byte d of pair row p
+  (D bytes) holds element d of token 2p in its low nibble and element d of
+  token 2p+1 in its high nibble; scale byte 2*blk + i of pair row p (D/8
+  bytes) is block blk of token 2p+i.  A decode kernel contracts V over
+  tokens, so its tensor-core operands pair two tokens of one element: this
+  order hands it those pairs as they are stored.  Sizes are unchanged.
+
+A slot is ``page * P + off``; a negative slot means "do not store".
 
 The FP32 global scales are not in the pool array: they are passed beside it
 as a float32 pair (K, V), as the caller owns them per layer.
@@ -72,10 +84,68 @@ def new_pool(spec, fill=0):
 
 
 def _row_index(spec, page, off, head, which):
-    """[N, row_bytes] byte indices of the rows (page, off) of one region."""
+    """[N, row_bytes] byte indices of token rows (page, off) of a region stored
+    one row per token (K codes and scales; every INT4 region)."""
     width = spec.code_bytes if which in ("kc", "vc") else spec.scale_bytes
     base = spec.chunk_offset(page, head) + spec.region(which) + np.asarray(off, np.int64) * width
     return base[:, None] + np.arange(width, dtype=np.int64)[None, :]
+
+
+def _pair_v(spec):
+    return spec.fmt == NVFP4
+
+
+def _v_pair_codes_index(spec, page, off, head):
+    """NVFP4 V codes: [N, D] byte indices of the pair rows of tokens (page,
+    off) and [N] nibble shifts (0 for even tokens, 4 for odd)."""
+    off = np.asarray(off, np.int64)
+    D = spec.head_dim
+    base = spec.chunk_offset(page, head) + spec.region("vc") + (off // 2) * D
+    return base[:, None] + np.arange(D, dtype=np.int64)[None, :], (off & 1) * 4
+
+
+def _v_pair_scales_index(spec, page, off, head):
+    """NVFP4 V scales: [N, D/16] byte indices of the scales of tokens (page, off)."""
+    off = np.asarray(off, np.int64)
+    W = spec.scale_bytes
+    base = spec.chunk_offset(page, head) + spec.region("vs") + (off // 2) * (2 * W) + (off & 1)
+    return base[:, None] + 2 * np.arange(W, dtype=np.int64)[None, :]
+
+
+def get_codes(pool, spec, page, off, head, kind):
+    """Packed codes [N, D/2] (element 2j in the low nibble of byte j) of tokens
+    (page, off), whatever the region's row order."""
+    if kind == "v" and _pair_v(spec):
+        idx, sh = _v_pair_codes_index(spec, page, off, head)
+        nib = (pool[idx] >> sh[:, None].astype(np.uint8)) & 0xF
+        return (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8)
+    return pool[_row_index(spec, page, off, head, kind + "c")]
+
+
+def get_scales(pool, spec, page, off, head, kind):
+    """Scale bytes [N, row_scale_bytes] of tokens (page, off)."""
+    if kind == "v" and _pair_v(spec):
+        return pool[_v_pair_scales_index(spec, page, off, head)]
+    return pool[_row_index(spec, page, off, head, kind + "s")]
+
+
+def put_rows(pool, spec, page, off, head, kind, codes, scales):
+    """Store packed codes [N, D/2] and scale bytes [N, W] of tokens (page, off),
+    touching nothing else (for paired V rows, only the token's own nibbles)."""
+    if kind == "v" and _pair_v(spec):
+        idx, sh = _v_pair_codes_index(spec, page, off, head)
+        c = np.asarray(codes, np.uint8)
+        nib = np.empty((c.shape[0], 2 * c.shape[1]), np.uint8)
+        nib[:, 0::2] = c & 0xF
+        nib[:, 1::2] = c >> 4
+        for r in range(idx.shape[0]):               # one token at a time: pairs may repeat
+            s = int(sh[r])
+            old = pool[idx[r]]
+            pool[idx[r]] = (old & np.uint8(0xF0 >> s)) | (nib[r] << np.uint8(s))
+        pool[_v_pair_scales_index(spec, page, off, head)] = scales
+        return
+    pool[_row_index(spec, page, off, head, kind + "c")] = codes
+    pool[_row_index(spec, page, off, head, kind + "s")] = scales
 
 
 def quantize_rows(spec, x_bf16, g):
@@ -102,8 +172,7 @@ def write(pool, spec, k, v, slot_mapping, gscale):
     for name, x, g in (("k", k, gk), ("v", v, gv)):
         codes, scales = quantize_rows(spec, np.asarray(x)[keep], g)
         for h in range(spec.num_kv_heads):
-            pool[_row_index(spec, page, off, h, name + "c")] = codes[:, h]
-            pool[_row_index(spec, page, off, h, name + "s")] = scales[:, h].reshape(len(keep), -1)
+            put_rows(pool, spec, page, off, h, name, codes[:, h], scales[:, h].reshape(len(keep), -1))
     return pool
 
 
@@ -115,8 +184,8 @@ def token_pages(block_table_row, positions, page_size):
 
 def read_rows(pool, spec, page, off, head, gscale, kind):
     """Dequantised float64 rows [N, D] of K (kind='k') or V (kind='v')."""
-    codes = pool[_row_index(spec, page, off, head, kind + "c")]
-    sbytes = pool[_row_index(spec, page, off, head, kind + "s")]
+    codes = get_codes(pool, spec, page, off, head, kind)
+    sbytes = get_scales(pool, spec, page, off, head, kind)
     if spec.fmt == NVFP4:
         g = gscale[0] if kind == "k" else gscale[1]
         return quant.nvfp4_dequantize(codes, sbytes, g)

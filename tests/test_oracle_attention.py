@@ -64,13 +64,23 @@ def test_bruteforce_tiny_by_hand():
     base = (page * 1 + 0) * spec.chunk_bytes
 
     def row(kind, t):
-        cbase = base + spec.region(kind + "c") + t * 8
-        s = F.e4m3_decode(pool[base + spec.region(kind + "s") + t])
         gg = float(g[0] if kind == "k" else g[1])
         vals = []
-        for j in range(8):
-            byte = int(pool[cbase + j])
-            for nib in (byte & 0xF, byte >> 4):
+        if kind == "k":
+            # one row per token: 8 bytes, element 2j low nibble of byte j; 1 scale byte
+            cbase = base + spec.region("kc") + t * 8
+            s = F.e4m3_decode(pool[base + spec.region("ks") + t])
+            for j in range(8):
+                byte = int(pool[cbase + j])
+                for nib in (byte & 0xF, byte >> 4):
+                    vals.append(float(F.e2m1_decode(nib)) * float(s) * gg)
+        else:
+            # token pairs: byte d of pair row t//2 (16 bytes) holds element d of
+            # token t in nibble t%2; the pair's scale row is (s_even, s_odd)
+            cbase = base + spec.region("vc") + (t // 2) * 16
+            s = F.e4m3_decode(pool[base + spec.region("vs") + (t // 2) * 2 + (t % 2)])
+            for d in range(16):
+                nib = (int(pool[cbase + d]) >> (4 * (t % 2))) & 0xF
                 vals.append(float(F.e2m1_decode(nib)) * float(s) * gg)
         return vals
 

@@ -164,33 +164,57 @@ def test_int4_round_trip_and_ties():
 
 
 def test_pool_write_places_rows_by_slot():
+    """Every code nibble and scale byte lands where the layout says (computed
+    here by hand from the documented order) and nothing else changes."""
     rng = np.random.default_rng(5)
     for fmt in ("nvfp4", "int4"):
-        spec = P.PoolSpec(fmt, 5, 16, 2, 64)
+        D, Pg = 64, 16
+        spec = P.PoolSpec(fmt, 5, Pg, 2, D)
         T = 20
-        k = f32_to_bf16_bits(rng.standard_normal((T, 2, 64)).astype(np.float32))
-        v = f32_to_bf16_bits(rng.standard_normal((T, 2, 64)).astype(np.float32))
-        slots = rng.permutation(5 * 16)[:T].astype(np.int64)
+        k = f32_to_bf16_bits(rng.standard_normal((T, 2, D)).astype(np.float32))
+        v = f32_to_bf16_bits(rng.standard_normal((T, 2, D)).astype(np.float32))
+        slots = rng.permutation(5 * Pg)[:T].astype(np.int64)
         slots[3] = -1
         pool = P.new_pool(spec, fill=0xAB)
         P.write(pool, spec, k, v, slots, np.array([0.01, 0.02], np.float32))
-        written = np.zeros(spec.pool_bytes, bool)
+        W = D // 16 if fmt == "nvfp4" else 4              # scale bytes per token
+        chunk = Pg * (D + 2 * W)
+        reg = {"kc": 0, "vc": Pg * D // 2, "ks": Pg * D, "vs": Pg * D + Pg * W}
+        written = np.zeros((spec.pool_bytes, 2), bool)    # per nibble
         for t in range(T):
             if slots[t] < 0:
                 continue
-            page, off = divmod(int(slots[t]), 16)
+            page, off = divmod(int(slots[t]), Pg)
             for h in range(2):
+                base = (page * 2 + h) * chunk
                 for kind, x, gg in (("k", k, 0.01), ("v", v, 0.02)):
-                    idx_c = P._row_index(spec, np.array([page]), np.array([off]), h, kind + "c")[0]
-                    idx_s = P._row_index(spec, np.array([page]), np.array([off]), h, kind + "s")[0]
                     if fmt == "nvfp4":
                         cc, ss = Q.nvfp4_quantize(x[t, h][None], np.float32(gg))
                         ss = ss[0]
                     else:
                         cc, sc = Q.int4_quantize(x[t, h][None])
                         ss = sc.astype(np.float32).view(np.uint8)
-                    assert np.array_equal(pool[idx_c], cc[0])
-                    assert np.array_equal(pool[idx_s], ss)
-                    written[idx_c] = True
-                    written[idx_s] = True
-        assert np.all(pool[~written] == 0xAB)       # nothing else touched
+                    nib = np.empty(D, np.uint8)
+                    nib[0::2], nib[1::2] = cc[0] & 0xF, cc[0] >> 4
+                    if kind == "v" and fmt == "nvfp4":
+                        # pair row off//2 of D bytes; element d in nibble off%2 of byte d
+                        for d in range(D):
+                            at = base + reg["vc"] + (off // 2) * D + d
+                            assert (pool[at] >> (4 * (off % 2))) & 0xF == nib[d]
+                            written[at, off % 2] = True
+                        for blk in range(W):
+                            at = base + reg["vs"] + (off // 2) * 2 * W + 2 * blk + off % 2
+                            assert pool[at] == ss[blk]
+                            written[at, :] = True
+                    else:
+                        for d in range(D):
+                            at = base + reg[kind + "c"] + off * (D // 2) + d // 2
+                            assert (pool[at] >> (4 * (d % 2))) & 0xF == nib[d]
+                            written[at, d % 2] = True
+                        for i in range(W):
+                            at = base + reg[kind + "s"] + off * W + i
+                            assert pool[at] == ss[i]
+                            written[at, :] = True
+        lo_ok = (pool & 0xF) == 0xB
+        hi_ok = (pool >> 4) == 0xA
+        assert np.all(lo_ok | written[:, 0]) and np.all(hi_ok | written[:, 1])   # nothing else touched
