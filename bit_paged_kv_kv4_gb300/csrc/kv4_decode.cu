@@ -255,8 +255,11 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
   // NVFP4 V in token-pair rows (2 code rows of RB bytes per pair, D/8 scale
   // bytes per pair): thread (grp, tig) reads head dims [D0, D0 + D/8) of the
   // pairs holding tokens (16kg + 2tig, +1) and (16kg + 2tig + 8, +9).
+  // Threads take the D/8-dim chunks in the order pi(grp) = 4 (grp & 1) + grp / 2,
+  // so the two groups sharing a quarter-warp read pair-row halves of opposite
+  // parity: their swizzled 16-byte units then fall in distinct banks.
   constexpr int D0S = D / 8;                          // dims (= bytes) per thread
-  const int D0 = D0S * grp;
+  const int D0 = D0S * (4 * (grp & 1) + (grp >> 1));
   const uint32_t vp_off0 = Gm::OFF_VC + swz<RB>(2 * tig + D0 / RB, D0 % RB);
   const uint32_t vp_off1 = Gm::OFF_VC + swz<RB>(2 * tig + D0 / RB, D0 % RB + 16);
   const uint32_t vps_off = Gm::OFF_VS + tig * (D / 8) + 2 * (D0 / 16);
@@ -772,10 +775,13 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
           const float mw = sMeta[(w * 8 + g) * 3 + 0];
           l += (mw == -INFINITY) ? 0.f : sMeta[(w * 8 + g) * 3 + 2] * fast_exp2(mw - Mx);
         }
-        // (d, g) lives in lane (grp, tig) = ((d/2) / VB, g/2), o[mi][g%2] with
-        // mi = (d/2) % VB; d+1 in o[mi][g%2 + 2]; d+2, d+3 in o[mi+1][...].
+        // (d, g) lives in lane (grp, tig) with tig = g/2 and grp the group that
+        // holds dim chunk q = (d/2) / VB (q itself for INT4, pi^-1(q) for
+        // NVFP4), in o[mi][g%2] with mi = (d/2) % VB; d+1 in o[mi][g%2 + 2];
+        // d+2, d+3 in o[mi+1][...].
         const int hd = d >> 1, mi = hd % VB, c = g & 1;
-        const float* row = sAcc + ((hd / VB) * 4 + (g >> 1)) * Gm::AS + 4 * mi + c;
+        const int q = hd / VB, gq = (FMT == KV4_NVFP4) ? 2 * (q & 3) + (q >> 2) : q;
+        const float* row = sAcc + (gq * 4 + (g >> 1)) * Gm::AS + 4 * mi + c;
         const float4 acc = make_float4(row[0], row[2], row[4], row[6]);
         if (direct) {
           const float inv = (l > 0.f && My != -INFINITY) ? gv * fast_exp2(My - Mx) / l : 0.f;
