@@ -177,7 +177,8 @@ kv4_status kv4_write(const void* k, const void* v, const int64_t* slot_mapping,
   if (fmt == KV4_NVFP4 && layer_global_scale == nullptr)
     return fail(KV4_EINVAL, "NVFP4 needs layer_global_scale");
   const int64_t threads = num_tokens * pool->num_kv_heads * (pool->head_dim / 8);
-  if ((threads + 255) / 256 >= (int64_t{1} << 31)) return fail(KV4_EINVAL, "num_tokens too large");
+  if (threads >= (int64_t{1} << 31))           // thread indices are 32-bit
+    return fail(KV4_EINVAL, "num_tokens too large");
 
   kv4::WriteArgs a{};
   a.k = static_cast<const __nv_bfloat16*>(k);
@@ -322,7 +323,7 @@ kv4_status kv4_dequant_prefix(const kv4_pool* pool, const float* layer_global_sc
   if (pool->fmt == KV4_NVFP4 && layer_global_scale == nullptr)
     return fail(KV4_EINVAL, "NVFP4 needs layer_global_scale");
   const int64_t threads = static_cast<int64_t>(max_prefix_len) * pool->num_kv_heads * (pool->head_dim / 16);
-  if ((threads + 255) / 256 >= (int64_t{1} << 31)) return fail(KV4_EINVAL, "prefix too large");
+  if (threads >= (int64_t{1} << 31)) return fail(KV4_EINVAL, "prefix too large");  // 32-bit thread indices
 
   kv4::PrefixArgs a{};
   a.pool = static_cast<const uint8_t*>(pool->base);

@@ -9,6 +9,7 @@
 #include <cuda_bf16.h>
 
 #include "../../include/kv4.h"
+#include "kv4_internal.h"
 
 namespace kv4 {
 
@@ -277,6 +278,11 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// n / f.d for n < 2^31 (see FastDiv).
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f) {
+  return (__umulhi(n, f.m) + n) >> f.s;
+}
+
 // ------------------------------------------------------------ division
 // a / b rounded to nearest even, given yb = __frcp_rn(b) (1/b correctly
 // rounded).  Markstein's theorem (P. Markstein, "Computation of elementary
@@ -290,6 +296,14 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
 __device__ __forceinline__ float div_rn(float a, float b, float yb) {
   const float q0 = __fmul_rn(a, yb);
   if (!(fabsf(q0) < 1.0e30f) || !(yb < 1.0e30f)) return __fdiv_rn(a, b);
+  const float r = __fmaf_rn(-b, q0, a);
+  return copysignf(__fmaf_rn(r, yb, q0), a);
+}
+
+// div_rn without the range check, for callers that have checked once that
+// yb < 1e30 and |a * yb| < 1e30 for every a they pass.
+__device__ __forceinline__ float div_rn_inrange(float a, float b, float yb) {
+  const float q0 = __fmul_rn(a, yb);
   const float r = __fmaf_rn(-b, q0, a);
   return copysignf(__fmaf_rn(r, yb, q0), a);
 }

@@ -8,6 +8,21 @@
 
 namespace kv4 {
 
+// Division of n < 2^31 by a fixed d in [1, 2^31) with one multiply-high, an
+// add and a shift (T. Granlund, P. Montgomery, "Division by invariant integers
+// using multiplication", PLDI 1994, section 4): s = ceil(log2 d),
+// m = floor(2^32 (2^s - d) / d) + 1, n / d = (mulhi(n, m) + n) >> s.
+struct FastDiv {
+  uint32_t d, m, s;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+  uint32_t s = 0;
+  while ((uint64_t{1} << s) < d) ++s;
+  const uint64_t m = ((uint64_t{1} << 32) * ((uint64_t{1} << s) - d)) / d + 1;
+  return FastDiv{d, static_cast<uint32_t>(m), s};
+}
+
+
 struct DecodeArgs {
   const uint8_t* pool;
   int64_t chunk_bytes;
@@ -41,6 +56,8 @@ struct WriteArgs {
   int P, Hkv, num_pages, D, fmt;
   const float* gscale;
   int* err;
+  int rows;                     // T * Hkv (< 2^31)
+  FastDiv hkv_div, p_div;       // by Hkv, by P
 };
 
 struct PrefixArgs {
@@ -57,6 +74,7 @@ struct PrefixArgs {
   uint8_t* out_k;
   uint8_t* out_v;
   int* err;
+  FastDiv hkv_div, p_div;       // by Hkv, by P
 };
 
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& map, cudaStream_t st);

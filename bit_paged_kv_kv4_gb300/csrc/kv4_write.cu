@@ -22,50 +22,18 @@
 
 namespace kv4 {
 
-__global__ void __launch_bounds__(256)
-write_kernel(const WriteArgs a) {
-  grid_dep_launch();   // a following decode launch may be scheduled early
-  const int D = a.D;
-  const int tpr = D / 8;                          // threads per row
-  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int kind = blockIdx.y;                    // 0: K, 1: V
-  const int64_t rows = a.T * a.Hkv;
-  const int64_t row = tid / tpr;
-  const int part = static_cast<int>(tid % tpr);
-  const bool in_range = row < rows;
-  const int64_t t = in_range ? row / a.Hkv : 0;
-  const int h = in_range ? static_cast<int>(row % a.Hkv) : 0;
-
-  // load 8 bf16 -> fp32 (rows past the end read row 0 and store nothing)
-  const __nv_bfloat16* src = (kind == 0 ? a.k : a.v) + (in_range ? row : 0) * D + part * 8;
-  uint4 raw = __ldg(reinterpret_cast<const uint4*>(src));
-  float x[8];
-  {
-    const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      float2 f = __bfloat1622float2(p2[j]);
-      x[2 * j] = f.x;
-      x[2 * j + 1] = f.y;
-    }
-  }
+// Quantise this thread's 8 elements x of row (token, head) and store them at
+// (chunk, off).  NVFP4: the two threads of a 16-element block exchange their
+// maxima; INT4: the D/8 threads of the row do.
+template <int D, int FMT>
+__device__ __forceinline__ void write_row_part(const WriteArgs& a, int kind, int part, const float (&x)[8],
+                                               bool store, uint8_t* chunk, int off) {
+  constexpr int TPR = D / 8;
+  constexpr int RB = D / 2;
   float amax = 0.f;
 #pragma unroll
   for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(x[j]));
-
-  const int64_t slot = in_range ? a.slot_mapping[t] : -1;
-  const int64_t cap = static_cast<int64_t>(a.num_pages) * a.P;
-  bool store = slot >= 0;
-  if (slot >= cap) {
-    if (part == 0) set_error(a.err, KV4_EBOUNDS);
-    store = false;
-  }
-  const int64_t page = store ? slot / a.P : 0;
-  const int off = store ? static_cast<int>(slot % a.P) : 0;
-  uint8_t* chunk = a.pool + (page * a.Hkv + h) * a.chunk_bytes;
-  const int RB = D / 2;
-
-  if (a.fmt == KV4_NVFP4) {
+  if constexpr (FMT == KV4_NVFP4) {
     // block amax over the thread pair
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     const float g = __ldg(a.gscale + kind);
@@ -75,21 +43,23 @@ write_kernel(const WriteArgs a) {
     uint32_t word = 0;
     if (S != 0u && denom != 0.f) {
       const float rd = __frcp_rn(denom);
+      float q[8];
+      if (rd < 1.0e30f && amax * rd < 1.0e30f) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t byte = f32x2_to_e2m1x2(div_rn(x[2 * j], denom, rd),
-                                              div_rn(x[2 * j + 1], denom, rd));
-        word |= byte << (8 * j);
+        for (int j = 0; j < 8; ++j) q[j] = div_rn_inrange(x[j], denom, rd);
+      } else {                                  // operands near the FP32 range limits
+#pragma unroll
+        for (int j = 0; j < 8; ++j) q[j] = __fdiv_rn(x[j], denom);
       }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) word |= f32x2_to_e2m1x2(q[2 * j], q[2 * j + 1]) << (8 * j);
     }
+    constexpr int SB = D / 16;
     if (store && kind == 0) {
-      uint8_t* codes = chunk + static_cast<int64_t>(off) * RB;
-      *reinterpret_cast<uint32_t*>(codes + part * 4) = word;
-      if ((part & 1) == 0) {
-        const int SB = D / 16;
-        uint8_t* sc = chunk + static_cast<int64_t>(a.P) * D + static_cast<int64_t>(off) * SB;
-        sc[part >> 1] = static_cast<uint8_t>(S);
-      }
+      *reinterpret_cast<uint32_t*>(chunk + static_cast<int64_t>(off) * RB + part * 4) = word;
+      if ((part & 1) == 0)
+        chunk[static_cast<int64_t>(a.P) * D + static_cast<int64_t>(off) * SB + (part >> 1)] =
+            static_cast<uint8_t>(S);
     } else if (store) {
       // V rows are stored in token pairs: byte d of pair row off/2 holds element
       // d of the even token (low nibble) and of the odd token (high nibble).
@@ -103,23 +73,29 @@ write_kernel(const WriteArgs a) {
           chunk + static_cast<int64_t>(a.P) * RB + static_cast<int64_t>(off >> 1) * D + part * 8);
       atomicAnd(dst, ~(0x0F0F0F0F0F0F0F0Full << sh));
       atomicOr(dst, static_cast<unsigned long long>(spread << sh));
-      if ((part & 1) == 0) {
-        const int SB = D / 16;
-        uint8_t* sc = chunk + static_cast<int64_t>(a.P) * D + static_cast<int64_t>(a.P) * SB +
-                      static_cast<int64_t>(off >> 1) * 2 * SB;
-        sc[2 * (part >> 1) + (off & 1)] = static_cast<uint8_t>(S);
-      }
+      if ((part & 1) == 0)
+        chunk[static_cast<int64_t>(a.P) * D + static_cast<int64_t>(a.P) * SB +
+              static_cast<int64_t>(off >> 1) * 2 * SB + 2 * (part >> 1) + (off & 1)] = static_cast<uint8_t>(S);
     }
   } else {
     // row amax over the D/8 threads of the row (aligned groups of a warp)
-    for (int o = 1; o < tpr; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+#pragma unroll
+    for (int o = 1; o < TPR; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const float s = __fdiv_rn(amax, 7.0f);
     uint32_t word = 0;
     if (s != 0.f) {
       const float rs = __frcp_rn(s);
+      float q[8];
+      if (rs < 1.0e30f && amax * rs < 1.0e30f) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) q[j] = div_rn_inrange(x[j], s, rs);
+      } else {                                  // operands near the FP32 range limits
+#pragma unroll
+        for (int j = 0; j < 8; ++j) q[j] = __fdiv_rn(x[j], s);
+      }
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        int c = __float2int_rn(div_rn(x[j], s, rs));
+        int c = __float2int_rn(q[j]);
         c = c < -8 ? -8 : (c > 7 ? 7 : c);
         word |= (static_cast<uint32_t>(c) & 0xFu) << (4 * j);
       }
@@ -136,13 +112,74 @@ write_kernel(const WriteArgs a) {
   }
 }
 
-cudaError_t launch_write(const WriteArgs& a, cudaStream_t st) {
-  const int64_t threads = a.T * a.Hkv * (a.D / 8);
-  if (threads == 0) return cudaSuccess;
-  const int bs = 256;
-  const int64_t blocks = (threads + bs - 1) / bs;
-  write_kernel<<<dim3(static_cast<unsigned>(blocks), 2), bs, 0, st>>>(a);
+// Thread (row (t, h), 8-element part, K|V = blockIdx.y).
+template <int D, int FMT>
+__global__ void __launch_bounds__(256)
+write_kernel(const WriteArgs a) {
+  grid_dep_launch();   // a following decode launch may be scheduled early
+  constexpr int TPR = D / 8;                      // threads per row
+  const uint32_t gtid = blockIdx.x * 256u + threadIdx.x;
+  const int kind = blockIdx.y;                    // 0: K, 1: V
+  const uint32_t row = gtid / TPR;
+  const int part = static_cast<int>(gtid % TPR);
+  const bool in_range = row < static_cast<uint32_t>(a.rows);
+  const uint32_t t = in_range ? fdiv(row, a.hkv_div) : 0u;
+  const int h = in_range ? static_cast<int>(row - t * static_cast<uint32_t>(a.Hkv)) : 0;
+
+  // load 8 bf16 -> fp32 (rows past the end read row 0 and store nothing)
+  const __nv_bfloat16* src = (kind == 0 ? a.k : a.v) + static_cast<int64_t>(in_range ? row : 0u) * D + part * 8;
+  const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src));
+  float x[8];
+  {
+    const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float2 f = __bfloat1622float2(p2[j]);
+      x[2 * j] = f.x;
+      x[2 * j + 1] = f.y;
+    }
+  }
+  // slots are below num_pages * P < 2^31 (the pool check), so 32-bit math
+  const int64_t slot = in_range ? a.slot_mapping[t] : -1;
+  const int64_t cap = static_cast<int64_t>(a.num_pages) * a.P;
+  bool store = slot >= 0;
+  if (slot >= cap) {
+    if (part == 0) set_error(a.err, KV4_EBOUNDS);
+    store = false;
+  }
+  const uint32_t su = store ? static_cast<uint32_t>(slot) : 0u;
+  const uint32_t page = fdiv(su, a.p_div);
+  const int off = static_cast<int>(su - page * static_cast<uint32_t>(a.P));
+  uint8_t* chunk = a.pool + (static_cast<int64_t>(page) * a.Hkv + h) * a.chunk_bytes;
+  write_row_part<D, FMT>(a, kind, part, x, store, chunk, off);
+}
+
+template <int D, int FMT>
+static cudaError_t launch_write_t(const WriteArgs& a, cudaStream_t st) {
+  const int64_t threads = static_cast<int64_t>(a.rows) * (D / 8);
+  const int64_t blocks = (threads + 255) / 256;
+  write_kernel<D, FMT><<<dim3(static_cast<unsigned>(blocks), 2), 256, 0, st>>>(a);
   return cudaGetLastError();
+}
+
+cudaError_t launch_write(const WriteArgs& a_in, cudaStream_t st) {
+  if (a_in.T == 0) return cudaSuccess;
+  WriteArgs a = a_in;
+  a.rows = static_cast<int>(a.T * a.Hkv);
+  a.hkv_div = make_fastdiv(static_cast<uint32_t>(a.Hkv));
+  a.p_div = make_fastdiv(static_cast<uint32_t>(a.P));
+  if (a.fmt == KV4_NVFP4) {
+    switch (a.D) {
+      case 64: return launch_write_t<64, KV4_NVFP4>(a, st);
+      case 128: return launch_write_t<128, KV4_NVFP4>(a, st);
+      default: return launch_write_t<256, KV4_NVFP4>(a, st);
+    }
+  }
+  switch (a.D) {
+    case 64: return launch_write_t<64, KV4_INT4_PTH>(a, st);
+    case 128: return launch_write_t<128, KV4_INT4_PTH>(a, st);
+    default: return launch_write_t<256, KV4_INT4_PTH>(a, st);
+  }
 }
 
 }  // namespace kv4
