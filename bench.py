@@ -558,12 +558,39 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the 160K / 1M / INT4 lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--only", choices=("prefix", "write"),
+                    help="time just the 160K prefix dequant or the 8K prefill write and print "
+                         "its line (for profiling one kernel)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return reference_arm(args)
+    if args.only:
+        return only_arm(args)
     return kv4_arm(args)
+
+
+def only_arm(args):
+    import torch
+    import bit_paged_kv_kv4_gb300 as K
+    K.load(build_if_missing=True)
+    device = torch.device("cuda", 0)
+    w = W.ALL["nvfp4_160k"]
+    peak, _ = read_peaks()
+    if args.only == "prefix":
+        r = time_prefix(Setup(w, device), w, peak)
+    else:
+        # the prefill write needs no filled pool: a device, a pair of global scales
+        # of the workload's magnitude and the library
+        import types
+        lite = types.SimpleNamespace(device=device, K=K,
+                                     g=torch.tensor([1.0 / (6 * 448)] * 2, dtype=torch.float32, device=device))
+        r = time_write_prefill(lite, w, peak)
+    if K.kv4_device_error() != 0:
+        raise SystemExit(f"device error {K.kv4_device_error()}")
+    print(json.dumps({"only": args.only, "workload": w.name, **r}))
+    return 0
 
 
 if __name__ == "__main__":
