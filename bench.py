@@ -258,8 +258,16 @@ def cpu_oracle_sample(name, seconds, max_steps=None):
             "tokens": L, "bytes_per_step": bytes_per, "times": times}
 
 
-def run_cpu_oracle_subprocess(name, seconds, max_steps=None):
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_cpu_oracle_subprocess(name, seconds, max_steps=None, threads=1):
+    n = str(threads)
+    env = dict(os.environ, OMP_NUM_THREADS=n, OPENBLAS_NUM_THREADS=n, MKL_NUM_THREADS=n,
                CUDA_VISIBLE_DEVICES="")
     code = ("import json,sys; sys.path.insert(0, %r); import bench; "
             "r = bench.cpu_oracle_sample(%r, %r, %r); r.pop('times'); print(json.dumps(r))"
@@ -442,7 +450,8 @@ def kv4_arm(args):
                      "kernel": "kv4_decode_attention (split kernel + combine)",
                      "peak_source": f"{peak_src} hbm_gbs", "decode_us": dec_avg * 1e6,
                      "decode_us_median": statistics.median(dec_times) * 1e6,
-                     "decode_samples": f"{len(dec_times)} of {args.steps} timed steps (every {EVENT_EVERY}th)"},
+                     "decode_samples": f"{len(dec_times)} of {args.steps} timed steps (every {EVENT_EVERY}th)",
+                     "tokens_per_s_16_layers": B / (16 * statistics.median(dec_times))},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_total / args.steps * 1e3},
         "gpu_launches": args.steps * s.launches_per_step(),
@@ -480,6 +489,14 @@ def kv4_arm(args):
         except Exception as e:  # the baseline is reported, never required
             line["cpu_baseline"] = {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle",
                                     "sample": f"failed: {str(e)[-200:]}"}
+        try:
+            # the same sample with numpy's BLAS threads on every host core
+            nc = host_cores()
+            r = run_cpu_oracle_subprocess(w.name, args.cpu_seconds, threads=nc)
+            line["cpu_baseline"]["all_cores"] = {"value": r["value"], "unit": "GB/s", "cores": nc,
+                                                 "repeats": r["steps"]}
+        except Exception as e:
+            line["cpu_baseline"]["all_cores"] = {"value": None, "failed": str(e)[-200:]}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if pg is not None:
