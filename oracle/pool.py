@@ -14,14 +14,16 @@ chunk holds four regions, each a whole number of 16-byte units:
 
     NVFP4: [K codes P*D/2][V codes P*D/2][K scales P*D/16][V scales P*D/16]
     INT4 : [K codes P*D/2][V codes P*D/2][K scale f32 * P][V scale f32 * P]
+    FP8  : [K codes P*D]  [V codes P*D]   (per-tensor scales beside the pool)
 
-so chunk_bytes = P*(D + D/8) for NVFP4 and P*(D + 8) for INT4.
+so chunk_bytes = P*(D + D/8) for NVFP4, P*(D + 8) for INT4, P*2*D for FP8.
 
 Row order inside a region:
 
-* K codes and scales, and every INT4 region: token ``off`` of the page owns
-  row ``off`` (D/2 code bytes, element 2j in the low nibble of byte j; D/16
-  scale bytes, or one FP32 scale).
+* K codes and scales, and every INT4 and FP8 region: token ``off`` of the
+  page owns row ``off`` (D/2 code bytes, element 2j in the low nibble of
+  byte j; D/16 scale bytes, or one FP32 scale; FP8: D code bytes, element d
+  in byte d).
 * NVFP4 V: tokens are stored in pairs (2p, 2p+1).  Code byte d of pair row p
   (D bytes) holds element d of token 2p in its low nibble and element d of
   token 2p+1 in its high nibble; scale byte 2*blk + i of pair row p (D/8
@@ -42,6 +44,7 @@ from . import quant
 
 NVFP4 = "nvfp4"
 INT4 = "int4"
+FP8 = "fp8"
 
 
 @dataclass(frozen=True)
@@ -53,12 +56,12 @@ class PoolSpec:
     head_dim: int
 
     @property
-    def code_bytes(self):            # packed 4-bit codes of one row
-        return self.head_dim // 2
+    def code_bytes(self):            # codes of one row: packed 4-bit, or one byte each (FP8)
+        return self.head_dim if self.fmt == FP8 else self.head_dim // 2
 
     @property
     def scale_bytes(self):           # scale bytes of one row (K or V)
-        return self.head_dim // 16 if self.fmt == NVFP4 else 4
+        return {NVFP4: self.head_dim // 16, INT4: 4, FP8: 0}[self.fmt]
 
     @property
     def chunk_bytes(self):           # one (page, kv head) chunk, K and V
@@ -152,6 +155,9 @@ def quantize_rows(spec, x_bf16, g):
     """Rows [..., D] of bf16 bits -> (codes bytes, scale bytes) in pool form."""
     if spec.fmt == NVFP4:
         return quant.nvfp4_quantize(x_bf16, g)
+    if spec.fmt == FP8:
+        codes = quant.fp8_quantize(x_bf16, g)
+        return codes, np.zeros(codes.shape[:-1] + (0,), np.uint8)
     codes, s = quant.int4_quantize(x_bf16)
     return codes, s.astype(np.float32).view(np.uint8).reshape(s.shape + (4,))
 
@@ -160,7 +166,8 @@ def write(pool, spec, k, v, slot_mapping, gscale):
     """Store tokens into the pool (the write path of Figure 2).
 
     k, v: uint16 bf16 bits [T, Hkv, D]; slot_mapping: int64 [T]; gscale:
-    float32 [2] = (g_K, g_V), used by NVFP4 only.  Slots < 0 are skipped.
+    float32 [2] = (g_K, g_V): NVFP4 global scales or FP8 per-tensor scales
+    (unused for INT4).  Slots < 0 are skipped.
     """
     slot = np.asarray(slot_mapping, dtype=np.int64)
     keep = np.nonzero(slot >= 0)[0]
@@ -189,5 +196,7 @@ def read_rows(pool, spec, page, off, head, gscale, kind):
     if spec.fmt == NVFP4:
         g = gscale[0] if kind == "k" else gscale[1]
         return quant.nvfp4_dequantize(codes, sbytes, g)
+    if spec.fmt == FP8:
+        return quant.fp8_dequantize(codes, gscale[0] if kind == "k" else gscale[1])
     s = np.ascontiguousarray(sbytes).view(np.float32).reshape(-1)
     return quant.int4_dequantize(codes, s)

@@ -29,6 +29,12 @@ amax == 0 (or s == 0) gives s = 0 and all-zero codes.  Decode: code * s.
 The split of the eight scale bytes into two FP32 scales is a reading that
 fits the byte count but that nothing on the pages confirms: parity unpinned
 beyond the byte count.
+
+FP8 E4M3 per tensor, the format the 4-bit cache is compared against ("SGLang's
+4-bit KV cache", "The 56% survives its own scale": FP8 is per-tensor scaled,
+sixteen bytes per sixteen values).  Reading: one FP32 decode scale s per
+layer for K and one for V; code = E4M3(float32(x) / s), RNE, saturating at
+448, sign kept.  Decode: e4m3(code) * s.
 """
 import numpy as np
 
@@ -101,3 +107,15 @@ def int4_dequantize(codes, scale):
     n = _unpack_nibbles(codes).astype(np.int64)
     c = np.where(n >= 8, n - 16, n)
     return c * np.asarray(scale, dtype=np.float64)[..., None]
+
+
+def fp8_quantize(x_bf16, s):
+    """bf16 bits [..., D] -> E4M3 codes uint8 [..., D]: E4M3(x / s), the FP32
+    quotient rounded to nearest, then RNE onto the E4M3 grid with saturation."""
+    x = bf16_to_f32(x_bf16)
+    return e4m3_encode((x / np.float32(s)).astype(np.float32))
+
+
+def fp8_dequantize(codes, s):
+    """E4M3 codes -> float64 values e4m3(code) * s."""
+    return e4m3_decode(codes) * np.float64(np.float32(s))

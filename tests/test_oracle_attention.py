@@ -242,3 +242,27 @@ def test_nvfp4_error_within_half_step_when_unsaturated():
     ok = t <= 6
     assert np.all(err[ok] <= 0.5 * step[ok] * (1 + 1e-6))
     assert np.all(err[~ok] <= (t[~ok] - 6) * (1 + 1e-6))
+
+
+def test_fp8_bruteforce_tiny_by_hand():
+    """FP8 pool, D = 16, 3 tokens: read every code byte at the position the
+    layout gives (token rows of D bytes), decode it with torch's float8 view
+    and expand the attention with Python loops."""
+    spec, pool, table, lens, g, q, Ks, Vs = build("fp8", 1, 16, [3], 16, seed=4, Hq=2)
+    sm = np.float32(0.25)
+    got = A.decode_attention(q, pool, spec, g, table, lens, sm)
+    page = int(table[0, 0])
+    base = page * spec.chunk_bytes
+
+    def row(kind, t):
+        start = base + (0 if kind == "k" else 16 * 16) + t * 16
+        vals = torch.from_numpy(pool[start:start + 16].copy()).view(torch.float8_e4m3fn).double().numpy()
+        return list(vals * float(g[0] if kind == "k" else g[1]))
+
+    for j in range(2):
+        qq = [float(x) for x in F.bf16_to_f32(q[0, j])]
+        sc = [float(sm) * sum(a * b for a, b in zip(qq, row("k", t))) for t in range(3)]
+        mx = max(sc)
+        w = [math.exp(s - mx) for s in sc]
+        out = [sum(w[t] * row("v", t)[d] for t in range(3)) / sum(w) for d in range(16)]
+        assert np.allclose(got[0, j], out, rtol=1e-13, atol=1e-15)

@@ -167,7 +167,7 @@ def test_pool_write_places_rows_by_slot():
     """Every code nibble and scale byte lands where the layout says (computed
     here by hand from the documented order) and nothing else changes."""
     rng = np.random.default_rng(5)
-    for fmt in ("nvfp4", "int4"):
+    for fmt in ("nvfp4", "int4", "fp8"):
         D, Pg = 64, 16
         spec = P.PoolSpec(fmt, 5, Pg, 2, D)
         T = 20
@@ -177,9 +177,10 @@ def test_pool_write_places_rows_by_slot():
         slots[3] = -1
         pool = P.new_pool(spec, fill=0xAB)
         P.write(pool, spec, k, v, slots, np.array([0.01, 0.02], np.float32))
-        W = D // 16 if fmt == "nvfp4" else 4              # scale bytes per token
-        chunk = Pg * (D + 2 * W)
-        reg = {"kc": 0, "vc": Pg * D // 2, "ks": Pg * D, "vs": Pg * D + Pg * W}
+        W = {"nvfp4": D // 16, "int4": 4, "fp8": 0}[fmt]     # scale bytes per token
+        CB = D if fmt == "fp8" else D // 2                   # code bytes per token
+        chunk = Pg * 2 * (CB + W)
+        reg = {"kc": 0, "vc": Pg * CB, "ks": 2 * Pg * CB, "vs": 2 * Pg * CB + Pg * W}
         written = np.zeros((spec.pool_bytes, 2), bool)    # per nibble
         for t in range(T):
             if slots[t] < 0:
@@ -188,6 +189,14 @@ def test_pool_write_places_rows_by_slot():
             for h in range(2):
                 base = (page * 2 + h) * chunk
                 for kind, x, gg in (("k", k, 0.01), ("v", v, 0.02)):
+                    if fmt == "fp8":
+                        # one byte per element, token rows of D bytes, no scale rows
+                        cc = Q.fp8_quantize(x[t, h][None], np.float32(gg))[0]
+                        for d in range(D):
+                            at = base + reg[kind + "c"] + off * D + d
+                            assert pool[at] == cc[d]
+                            written[at, :] = True
+                        continue
                     if fmt == "nvfp4":
                         cc, ss = Q.nvfp4_quantize(x[t, h][None], np.float32(gg))
                         ss = ss[0]
@@ -218,3 +227,31 @@ def test_pool_write_places_rows_by_slot():
         lo_ok = (pool & 0xF) == 0xB
         hi_ok = (pool >> 4) == 0xA
         assert np.all(lo_ok | written[:, 0]) and np.all(hi_ok | written[:, 1])   # nothing else touched
+
+
+def test_fp8_quantize_matches_torch_cast():
+    """FP8 per tensor: E4M3(float32(x) / s), checked against torch's float32 ->
+    float8_e4m3fn cast of the same FP32 quotient (in range), the saturation at
+    448 and the sign of zero."""
+    import torch
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((64, 128)).astype(np.float32) * 3
+    xb = f32_to_bf16_bits(x)
+    for s in (np.float32(0.01), np.float32(1 / 448), np.float32(0.37)):
+        q = (F.bf16_to_f32(xb) / s).astype(np.float32)
+        keep = np.abs(q) <= 448
+        got = Q.fp8_quantize(xb, s)
+        want = torch.from_numpy(np.where(keep, q, 0).astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert np.array_equal(got[keep], want[keep])
+        # beyond 448 the code saturates to +-448 (0x7E / 0xFE), never NaN
+        over = ~keep
+        assert np.all((got[over] & 0x7F) == 0x7E)
+        assert np.array_equal(got[over] >> 7, (q[over] < 0).astype(np.uint8))
+    # a tiny negative element keeps its sign as -0
+    tiny = f32_to_bf16_bits(np.array([[-1e-30, 1e-30, 0.0]], np.float32))
+    assert Q.fp8_quantize(tiny, np.float32(1.0)).tolist() == [[0x80, 0x00, 0x00]]
+    # decode is code value times s
+    c = np.arange(256, dtype=np.uint8)
+    finite = (c & 0x7F) != 0x7F
+    v = Q.fp8_dequantize(c[finite], np.float32(0.5))
+    assert np.allclose(v, torch.from_numpy(c[finite]).view(torch.float8_e4m3fn).float().numpy() * 0.5)
