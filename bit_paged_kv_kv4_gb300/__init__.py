@@ -18,7 +18,8 @@ from . import _build
 
 KV4_NVFP4 = 0
 KV4_INT4_PTH = 1
-FMT = {"nvfp4": KV4_NVFP4, "int4": KV4_INT4_PTH}
+KV4_FP8 = 2
+FMT = {"nvfp4": KV4_NVFP4, "int4": KV4_INT4_PTH, "fp8": KV4_FP8}
 
 _lib = None
 

@@ -37,12 +37,13 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int64_t chunk_bytes_of(const kv4_pool& p) {
   const int64_t P = p.page_size, D = p.head_dim;
-  return p.fmt == KV4_NVFP4 ? P * (D + D / 8) : P * (D + 8);
+  return p.fmt == KV4_NVFP4 ? P * (D + D / 8) : p.fmt == KV4_FP8 ? P * 2 * D : P * (D + 8);
 }
 
 kv4_status check_pool(const kv4_pool* p) {
   if (p == nullptr) return fail(KV4_EINVAL, "pool descriptor is NULL");
-  if (p->fmt != KV4_NVFP4 && p->fmt != KV4_INT4_PTH) return fail(KV4_EINVAL, "bad fmt %d", p->fmt);
+  if (p->fmt != KV4_NVFP4 && p->fmt != KV4_INT4_PTH && p->fmt != KV4_FP8)
+    return fail(KV4_EINVAL, "bad fmt %d", p->fmt);
   if (p->reserved != 0) return fail(KV4_EINVAL, "pool.reserved must be 0");
   if (p->num_pages < 1) return fail(KV4_EINVAL, "num_pages must be >= 1");
   if (p->num_kv_heads < 1) return fail(KV4_EINVAL, "num_kv_heads must be >= 1");
@@ -174,8 +175,8 @@ kv4_status kv4_write(const void* k, const void* v, const int64_t* slot_mapping,
     return fail(KV4_EINVAL, "k, v and slot_mapping must be non-NULL");
   if (!aligned(k, 16) || !aligned(v, 16) || !aligned(slot_mapping, 8))
     return fail(KV4_EINVAL, "k and v must be 16-byte aligned, slot_mapping 8-byte aligned");
-  if (fmt == KV4_NVFP4 && layer_global_scale == nullptr)
-    return fail(KV4_EINVAL, "NVFP4 needs layer_global_scale");
+  if (fmt != KV4_INT4_PTH && layer_global_scale == nullptr)
+    return fail(KV4_EINVAL, "NVFP4 and FP8 need layer_global_scale");
   const int64_t threads = num_tokens * pool->num_kv_heads * (pool->head_dim / 8);
   if (threads >= (int64_t{1} << 31))           // thread indices are 32-bit
     return fail(KV4_EINVAL, "num_tokens too large");
@@ -235,8 +236,8 @@ kv4_status kv4_decode_attention(const void* q, const kv4_pool* pool,
     return fail(KV4_EINVAL, "q, out, block_table and seq_lens must be non-NULL");
   if (!aligned(q, 16) || !aligned(out, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
     return fail(KV4_EINVAL, "q and out must be 16-byte aligned");
-  if (pool->fmt == KV4_NVFP4 && layer_global_scale == nullptr)
-    return fail(KV4_EINVAL, "NVFP4 needs layer_global_scale");
+  if (pool->fmt != KV4_INT4_PTH && layer_global_scale == nullptr)
+    return fail(KV4_EINVAL, "NVFP4 and FP8 need layer_global_scale");
   const int G = num_q_heads / pool->num_kv_heads;
   if (batch > 65535 || static_cast<int64_t>(pool->num_kv_heads) * ((G + 7) / 8) > 65535)
     return fail(KV4_EINVAL, "batch or heads exceed the launch grid");
@@ -274,7 +275,8 @@ kv4_status kv4_decode_attention(const void* q, const kv4_pool* pool,
   } else {
     // one wave of persistent CTAs, each given an equal share of all tiles
     const int64_t tiles_max = units * ((static_cast<int64_t>(max_pages) * pool->page_size +
-                                        kv4::decode_tile_tokens() - 1) / kv4::decode_tile_tokens());
+                                        kv4::decode_tile_tokens(pool->fmt) - 1) /
+                                       kv4::decode_tile_tokens(pool->fmt));
     const int64_t resident = static_cast<int64_t>(sm_count()) * kv4::decode_ctas_per_sm();
     int64_t n = (tiles_max + 3) / 4;
     n = n < 1 ? 1 : (n > resident ? resident : n);
@@ -291,7 +293,10 @@ kv4_status kv4_decode_attention(const void* q, const kv4_pool* pool,
   a.out_f32 = out_is_fp32 ? 1 : 0;
   a.err = error_word();
   if (a.err == nullptr) return fail(KV4_ECUDA, "no CUDA device / error word unavailable");
-  a.box_rows = (pool->page_size % 32 == 0) ? 32 : 16;
+  a.tile = kv4::decode_tile_tokens(pool->fmt);
+  // a tile is one box, or two when 32 does not divide P; an FP8 tile of 16
+  // tokens is 32 code rows
+  a.box_rows = (pool->fmt == KV4_FP8 || pool->page_size % 32 == 0) ? 32 : 16;
   CUtensorMap map;
   if ((s = code_row_map(*pool, a.box_rows, &map)) != KV4_OK) return s;
   cudaError_t e = kv4::launch_decode(a, map, static_cast<cudaStream_t>(stream));
@@ -307,6 +312,8 @@ kv4_status kv4_dequant_prefix(const kv4_pool* pool, const float* layer_global_sc
   kv4_status s = check_pool(pool);
   if (s != KV4_OK) return s;
   if ((s = check_pool_base(pool)) != KV4_OK) return s;
+  if (pool->fmt == KV4_FP8)
+    return fail(KV4_EUNSUPPORTED, "an FP8 pool is already FP8: no prefix dequant");
   if (batch < 0 || max_prefix_len < 0) return fail(KV4_EINVAL, "batch and max_prefix_len must be >= 0");
   if (max_pages < 1) return fail(KV4_EINVAL, "max_pages must be >= 1");
   if (static_cast<int64_t>(max_pages) * pool->page_size >= (int64_t{1} << 31))

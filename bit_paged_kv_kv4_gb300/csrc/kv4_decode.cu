@@ -53,7 +53,6 @@ namespace {
 #ifndef KV4_DECODE_NS
 #define KV4_DECODE_NS 2
 #endif
-constexpr int kTT = 32;                // tokens per tile (per warp and stage)
 constexpr int kNW = 4;                 // warps per CTA
 constexpr int kNS = KV4_DECODE_NS;     // stages per warp
 constexpr int kCtasPerSm = 2;          // resident CTAs per SM (register and smem budget)
@@ -62,16 +61,18 @@ constexpr uint32_t kFull = 0xffffffffu;
 
 template <int D, int FMT>
 struct Geo {
-  static constexpr int RB = D / 2;                             // code bytes per row
-  static constexpr int SB = (FMT == KV4_NVFP4) ? D / 16 : 4;   // scale bytes per row
+  static constexpr int TT = (FMT == KV4_FP8) ? 16 : 32;        // tokens per tile
+  static constexpr int RPT = (FMT == KV4_FP8) ? 2 : 1;         // code rows per token
+  static constexpr int RB = D / 2;                             // code bytes per code row
+  static constexpr int SB = (FMT == KV4_NVFP4) ? D / 16 : (FMT == KV4_FP8) ? 0 : 4;  // scale bytes per token
   static constexpr int KB = D / 8;                             // K code bytes per thread per token
   static constexpr int VB = D / 16;                            // V code bytes per thread per token
   static constexpr int MT = D / 16;                            // m-tiles of PV
-  static constexpr int STAGE_USED = kTT * (2 * RB + 2 * SB);
+  static constexpr int STAGE_USED = TT * (2 * RPT * RB + 2 * SB);
   static constexpr int STAGE = (STAGE_USED + 1023) / 1024 * 1024;
-  static constexpr int OFF_VC = kTT * RB;
-  static constexpr int OFF_KS = 2 * kTT * RB;
-  static constexpr int OFF_VS = 2 * kTT * RB + kTT * SB;
+  static constexpr int OFF_VC = TT * RPT * RB;
+  static constexpr int OFF_KS = 2 * TT * RPT * RB;
+  static constexpr int OFF_VS = 2 * TT * RPT * RB + TT * SB;
   static constexpr int RING = kNW * kNS * STAGE;
   static constexpr int AS = MT * 4 + 4;                        // merge row per lane (floats)
   static constexpr int ACC = 32 * AS * 4;                      // merged O of one segment
@@ -189,6 +190,7 @@ __global__ void __launch_bounds__(kNW * 32, kCtasPerSm)
 decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap) {
   using Gm = Geo<D, FMT>;
   constexpr int RB = Gm::RB, SB = Gm::SB, KB = Gm::KB, VB = Gm::VB, MT = Gm::MT;
+  constexpr int kTT = Gm::TT, RPT = Gm::RPT;
   grid_dep_launch();   // the combine may be scheduled now; it waits for this grid
   grid_dep_wait();     // inputs written by the previous kernel are visible
   constexpr int NM = kTT / 16;            // 16-token groups per tile (QK m-tiles = PV k-groups)
@@ -263,6 +265,19 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
   const uint32_t vp_off0 = Gm::OFF_VC + swz<RB>(2 * tig + D0 / RB, D0 % RB);
   const uint32_t vp_off1 = Gm::OFF_VC + swz<RB>(2 * tig + D0 / RB, D0 % RB + 16);
   const uint32_t vps_off = Gm::OFF_VS + tig * (D / 8) + 2 * (D0 / 16);
+  // FP8: token rows of D bytes (two code rows).  K: thread reads its D/4 bytes
+  // of token rows grp (+8); V: its D/8 bytes (dims [D0f, D0f + D/8)) of token
+  // rows 2tig, 2tig+1 (+8, +9).  Shifts by multiples of 8 code rows keep the
+  // swizzle pattern, so one per-thread constant per row parity suffices.
+  const int D0f = D0S * grp;
+  const uint32_t k8_off = swz<RB>(2 * grp + (tig >> 1), (D / 4) * (tig & 1));
+  const uint32_t k8_off1 = swz<RB>(2 * grp + (tig >> 1), (D / 4) * (tig & 1) + 16);
+  const uint32_t k8_off2 = swz<RB>(2 * grp + (tig >> 1), (D / 4) * (tig & 1) + 32);
+  const uint32_t k8_off3 = swz<RB>(2 * grp + (tig >> 1), (D / 4) * (tig & 1) + 48);
+  const uint32_t v8a0 = Gm::OFF_VC + swz<RB>(4 * tig + D0f / RB, D0f % RB);
+  const uint32_t v8a1 = Gm::OFF_VC + swz<RB>(4 * tig + D0f / RB, D0f % RB + 16);
+  const uint32_t v8b0 = Gm::OFF_VC + swz<RB>(4 * tig + D0f / RB + 2, D0f % RB);
+  const uint32_t v8b1 = Gm::OFF_VC + swz<RB>(4 * tig + D0f / RB + 2, D0f % RB + 16);
 
   // ---- per-warp running state ----------------------------------------------
   const uint64_t pol = policy_evict_first();
@@ -371,15 +386,16 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
       }
       const int h = is_h, L = is_L;
       const int t0 = (is_t0 + is_bg + io) * kTT;
-      const int nsub = (min(kTT, L - t0) + box - 1) / box;
+      const int boxt = box / RPT;      // tokens per box
+      const int nsub = (min(kTT, L - t0) + boxt - 1) / boxt;
       while (((pi - p_first) >> 5) > win) {
         ++win;
         pg_cur = pg_nxt;
         const int r = p_first + (win + 1) * 32 + lane;
         pg_nxt = r <= p_last ? __ldg(bt + r) : 0;
       }
-      // the tile's one or two boxes (32 tokens; a box never straddles a page)
-      int pu1 = pi, ou1 = po + box;
+      // the tile's one or two boxes (a box never straddles a page)
+      int pu1 = pi, ou1 = po + boxt;
       if (ou1 >= a.P) { ou1 -= a.P; ++pu1; }
       const int rel0 = pi - p_first, rel1 = pu1 - p_first;
       const int pc0 = __shfl_sync(kFull, pg_cur, rel0 & 31), pn0 = __shfl_sync(kFull, pg_nxt, rel0 & 31);
@@ -389,7 +405,7 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
       if (lane == 0) {
         const uint32_t st = ring + (issued % kNS) * Gm::STAGE;
         const uint32_t bar = bars + 8 * (issued % kNS);
-        mbar_arrive_expect_tx(bar, nsub * box * (2 * RB + 2 * SB));
+        mbar_arrive_expect_tx(bar, nsub * boxt * (2 * RPT * RB + 2 * SB));
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           if (u < nsub) {
@@ -400,13 +416,15 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
             }
             const int off = u ? ou1 : po;
             const int64_t chunk = (static_cast<int64_t>(page) * a.Hkv + h) * a.chunk_bytes;
-            const int row = static_cast<int>(chunk / RB) + off;
+            const int row = static_cast<int>(chunk / RB) + off * RPT;
             tma_load_2d(st + u * box * RB, &tmap, 0, row, bar, pol);
-            tma_load_2d(st + Gm::OFF_VC + u * box * RB, &tmap, 0, row + a.P, bar, pol);
-            const uint8_t* sc = a.pool + chunk + static_cast<int64_t>(a.P) * 2 * RB;
-            bulk_load(st + Gm::OFF_KS + u * box * SB, sc + off * SB, box * SB, bar, pol);
-            bulk_load(st + Gm::OFF_VS + u * box * SB, sc + static_cast<int64_t>(a.P) * SB + off * SB,
-                      box * SB, bar, pol);
+            tma_load_2d(st + Gm::OFF_VC + u * box * RB, &tmap, 0, row + a.P * RPT, bar, pol);
+            if constexpr (SB > 0) {
+              const uint8_t* sc = a.pool + chunk + static_cast<int64_t>(a.P) * 2 * RB;
+              bulk_load(st + Gm::OFF_KS + u * boxt * SB, sc + off * SB, boxt * SB, bar, pol);
+              bulk_load(st + Gm::OFF_VS + u * boxt * SB, sc + static_cast<int64_t>(a.P) * SB + off * SB,
+                        boxt * SB, bar, pol);
+            }
           }
         }
       }
@@ -460,7 +478,7 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
           frexpf(qmax / 16384.f, &e);
           qpre = ldexpf(1.f, -e);
         }
-        if constexpr (FMT == KV4_NVFP4) {
+        if constexpr (FMT != KV4_INT4_PTH) {
           // k-step kk: k (2tig, 2tig+1) <-> d = base + 4kk + {0,1}; (2tig+8, +9) <-> + {2,3}
 #pragma unroll
           for (int i = 0; i < QN / 2; ++i) qb[i] = pack_f16x2(qf[2 * i] * qpre, qf[2 * i + 1] * qpre);
@@ -475,8 +493,8 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
             qb[4 * j + 3] = pack_f16x2(e[3] * qpre, e[7] * qpre);
           }
         }
-        const float gk = (FMT == KV4_NVFP4) ? __ldg(a.gscale) : 1.f;
-        gv = (FMT == KV4_NVFP4) ? __ldg(a.gscale + 1) : 1.f;
+        const float gk = (FMT != KV4_INT4_PTH) ? __ldg(a.gscale) : 1.f;
+        gv = (FMT != KV4_INT4_PTH) ? __ldg(a.gscale + 1) : 1.f;
         qk_scale = a.sm_scale * gk * 1.4426950408889634f / qpre;   // base-2 logits
       }
 
@@ -512,8 +530,10 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
 #pragma unroll
         for (int m = 0; m < NM; ++m) {
           sacc[m][0] = sacc[m][1] = sacc[m][2] = sacc[m][3] = 0.f;
-          load_bytes<KB>(st + k_off0 + 16 * m * RB, st + k_off1 + 16 * m * RB, kw[m][0]);
-          load_bytes<KB>(st + k_off0 + (16 * m + 8) * RB, st + k_off1 + (16 * m + 8) * RB, kw[m][1]);
+          if constexpr (FMT != KV4_FP8) {
+            load_bytes<KB>(st + k_off0 + 16 * m * RB, st + k_off1 + 16 * m * RB, kw[m][0]);
+            load_bytes<KB>(st + k_off0 + (16 * m + 8) * RB, st + k_off1 + (16 * m + 8) * RB, kw[m][1]);
+          }
         }
         if constexpr (FMT == KV4_NVFP4) {
           constexpr int NB = D / 64;              // block scales per token this thread needs
@@ -544,7 +564,7 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
                             hmul2(c1[3], s1), qb[4 * j + 2], qb[4 * j + 3]);
             }
           }
-        } else {
+        } else if constexpr (FMT == KV4_INT4_PTH) {
 #pragma unroll
           for (int j = 0; j < KB / 4; ++j) {
 #pragma unroll
@@ -560,7 +580,32 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
                             int4_hi_pair(w1), qb[4 * j + 2], qb[4 * j + 3]);
             }
           }
-        }
+                } else {
+          // FP8: one E4M3 byte per element; the per-tensor scale is in qk_scale.
+          // Word j of a row holds dims 4j..4j+3 of the thread's range = k-step j.
+          constexpr int KW8 = D / 16;             // words per row (D/4 bytes)
+#pragma unroll
+          for (int m = 0; m < NM; ++m) {
+            uint32_t k8[2][KW8];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const uint32_t rowoff = (32 * m + 16 * r) * RB;      // token rows 16m + 8r (+ grp)
+              const uint32_t offs[4] = {k8_off, k8_off1, k8_off2, k8_off3};
+#pragma unroll
+              for (int u = 0; u < KW8 / 4; ++u) {
+                const uint4 x = lds128(st + offs[u] + rowoff);
+                k8[r][4 * u] = x.x; k8[r][4 * u + 1] = x.y; k8[r][4 * u + 2] = x.z; k8[r][4 * u + 3] = x.w;
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < KW8; ++j) {
+              uint32_t a0, a1, a2, a3;
+              e4m3x4_to_f16x2x2(k8[0][j], a0, a2);
+              e4m3x4_to_f16x2x2(k8[1][j], a1, a3);
+              mma_f16_16816(sacc[m], a0, a1, a2, a3, qb[2 * j], qb[2 * j + 1]);
+            }
+          }
+}
 
         // -------- online softmax (base 2) over this tile ----------------------
         // token of sacc[m][2r + c]: 16m + grp + 8r; head 2tig + c
@@ -681,6 +726,38 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
                 mma_f16_16816(o[mi], a0, a1, a2, a3, pb[kg][0], pb[kg][1]);
                 mma_f16_16816(o[mi], a0, a1, a2, a3, pl[kg][0], pl[kg][1]);
               }
+            }
+          } else if constexpr (FMT == KV4_FP8) {
+            // token rows: word j of each row holds dims D0f + 4j .. +3 of one
+            // token; byte-interleave two tokens, then E4M3x2 -> f16x2 gives
+            // the (token a, token b) operand registers of two m-tiles
+            constexpr int VW8 = D0S / 4;
+            uint32_t wa[VW8], wb[VW8], wc[VW8], wd[VW8];
+            load_bytes<D0S>(st + v8a0 + 32 * kg * RB, st + v8a1 + 32 * kg * RB, wa);
+            load_bytes<D0S>(st + v8b0 + 32 * kg * RB, st + v8b1 + 32 * kg * RB, wb);
+            load_bytes<D0S>(st + v8a0 + (32 * kg + 16) * RB, st + v8a1 + (32 * kg + 16) * RB, wc);
+            load_bytes<D0S>(st + v8b0 + (32 * kg + 16) * RB, st + v8b1 + (32 * kg + 16) * RB, wd);
+            if (valid < kTT) {
+              // rows past the end may hold anything, NaN codes included: zero them
+#pragma unroll
+              for (int j = 0; j < VW8; ++j) {
+                wa[j] = (ta < valid) ? wa[j] : 0u;
+                wb[j] = (ta + 1 < valid) ? wb[j] : 0u;
+                wc[j] = (ta + 8 < valid) ? wc[j] : 0u;
+                wd[j] = (ta + 9 < valid) ? wd[j] : 0u;
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < VW8; ++j) {
+              uint32_t ab0, ab1, ab2, ab3, cd0, cd1, cd2, cd3;
+              e4m3x4_to_f16x2x2(prmt(wa[j], wb[j], 0x5140u), ab0, ab1);   // dims +0, +1
+              e4m3x4_to_f16x2x2(prmt(wa[j], wb[j], 0x7362u), ab2, ab3);   // dims +2, +3
+              e4m3x4_to_f16x2x2(prmt(wc[j], wd[j], 0x5140u), cd0, cd1);
+              e4m3x4_to_f16x2x2(prmt(wc[j], wd[j], 0x7362u), cd2, cd3);
+              mma_f16_16816(o[2 * j], ab0, ab1, cd0, cd1, pb[kg][0], pb[kg][1]);
+              mma_f16_16816(o[2 * j], ab0, ab1, cd0, cd1, pl[kg][0], pl[kg][1]);
+              mma_f16_16816(o[2 * j + 1], ab2, ab3, cd2, cd3, pb[kg][0], pb[kg][1]);
+              mma_f16_16816(o[2 * j + 1], ab2, ab3, cd2, cd3, pl[kg][0], pl[kg][1]);
             }
           } else {
             uint32_t wa[VB / 4], wb[VB / 4], wc[VB / 4], wd[VB / 4];
@@ -875,7 +952,7 @@ combine_kernel(const DecodeArgs a) {
   int L = a.seq_lens[b];
   const int Lmax = a.max_pages * a.P;
   L = L < 0 ? 0 : (L > Lmax ? Lmax : L);
-  const int n_u = (L + kTT - 1) / kTT;
+  const int n_u = (L + a.tile - 1) / a.tile;
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   if (n_u == 0) {
@@ -970,7 +1047,7 @@ combine_kernel(const DecodeArgs a) {
       const float4 v = s_o[r * cols + col];
       acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
     }
-    const float gv = (a.fmt == KV4_NVFP4) ? __ldg(a.gscale + 1) : 1.f;
+    const float gv = (a.fmt != KV4_INT4_PTH) ? __ldg(a.gscale + 1) : 1.f;
     const float inv = (l > 0.f && My != -INFINITY) ? gv * fast_exp2(My - Mx) / l : 0.f;
     store_out4(a.out, a.out_f32, row * D + 4 * col,
                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
@@ -1012,7 +1089,7 @@ static cudaError_t launch_split(const DecodeArgs& a, const CUtensorMap& map, cud
   return launch_pdl(k, dim3(a.n_cta), dim3(kNW * 32), Gm::SMEM, st, a, map);
 }
 
-int decode_tile_tokens() { return kTT; }
+int decode_tile_tokens(int fmt) { return fmt == KV4_FP8 ? Geo<256, KV4_FP8>::TT : Geo<256, KV4_NVFP4>::TT; }
 
 int decode_ctas_per_sm() { return kCtasPerSm; }
 
@@ -1023,6 +1100,12 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& map, cudaStrea
       case 64: e = launch_split<64, KV4_NVFP4>(a, map, st); break;
       case 128: e = launch_split<128, KV4_NVFP4>(a, map, st); break;
       default: e = launch_split<256, KV4_NVFP4>(a, map, st); break;
+    }
+  } else if (a.fmt == KV4_FP8) {
+    switch (a.D) {
+      case 64: e = launch_split<64, KV4_FP8>(a, map, st); break;
+      case 128: e = launch_split<128, KV4_FP8>(a, map, st); break;
+      default: e = launch_split<256, KV4_FP8>(a, map, st); break;
     }
   } else {
     switch (a.D) {

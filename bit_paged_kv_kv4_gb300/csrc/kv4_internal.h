@@ -38,6 +38,7 @@ struct DecodeArgs {
   int n_cta;                    // CTAs launched
   int unit_ctas;                // 1: one CTA per unit, output written directly
   int box_rows;                 // rows per TMA box of the code-row map (16 or 32)
+  int tile;                     // tokens per tile (decode_tile_tokens(fmt))
   int64_t* cum;                 // [B+1] tile offsets of each request (balanced mode)
   float* part_ml;               // [slots][8][4]: m_x, l, m_y, 0
   float* part_o;                // [slots][8][D]
@@ -80,7 +81,7 @@ struct PrefixArgs {
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& map, cudaStream_t st);
 cudaError_t launch_write(const WriteArgs& a, cudaStream_t st);
 cudaError_t launch_prefix(const PrefixArgs& a, cudaStream_t st);
-int decode_tile_tokens();
+int decode_tile_tokens(int fmt);
 // Sets the message kv4_last_error_message() returns on this thread.
 void set_error_message(const char* msg);
 int decode_ctas_per_sm();

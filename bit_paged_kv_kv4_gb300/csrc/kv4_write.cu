@@ -77,6 +77,24 @@ __device__ __forceinline__ void write_row_part(const WriteArgs& a, int kind, int
         chunk[static_cast<int64_t>(a.P) * D + static_cast<int64_t>(a.P) * SB +
               static_cast<int64_t>(off >> 1) * 2 * SB + 2 * (part >> 1) + (off & 1)] = static_cast<uint8_t>(S);
     }
+  } else if constexpr (FMT == KV4_FP8) {
+    // FP8 per tensor: E4M3(x / s) for each element, s the layer's scale
+    const float s = __ldg(a.gscale + kind);
+    const float rs = __frcp_rn(s);
+    float q[8];
+    if (rs < 1.0e30f && amax * rs < 1.0e30f) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) q[j] = div_rn_inrange(x[j], s, rs);
+    } else {                                    // operands near the FP32 range limits
+#pragma unroll
+      for (int j = 0; j < 8; ++j) q[j] = __fdiv_rn(x[j], s);
+    }
+    if (store) {
+      const uint32_t w0 = f32x2_to_e4m3x2(q[0], q[1]) | (f32x2_to_e4m3x2(q[2], q[3]) << 16);
+      const uint32_t w1 = f32x2_to_e4m3x2(q[4], q[5]) | (f32x2_to_e4m3x2(q[6], q[7]) << 16);
+      *reinterpret_cast<uint2*>(chunk + static_cast<int64_t>(kind) * a.P * D + static_cast<int64_t>(off) * D +
+                                part * 8) = make_uint2(w0, w1);
+    }
   } else {
     // row amax over the D/8 threads of the row (aligned groups of a warp)
 #pragma unroll
@@ -173,6 +191,13 @@ cudaError_t launch_write(const WriteArgs& a_in, cudaStream_t st) {
       case 64: return launch_write_t<64, KV4_NVFP4>(a, st);
       case 128: return launch_write_t<128, KV4_NVFP4>(a, st);
       default: return launch_write_t<256, KV4_NVFP4>(a, st);
+    }
+  }
+  if (a.fmt == KV4_FP8) {
+    switch (a.D) {
+      case 64: return launch_write_t<64, KV4_FP8>(a, st);
+      case 128: return launch_write_t<128, KV4_FP8>(a, st);
+      default: return launch_write_t<256, KV4_FP8>(a, st);
     }
   }
   switch (a.D) {

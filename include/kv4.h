@@ -17,7 +17,7 @@
  *   kv4_dequant_prefix    the chunked-prefill path: dequantise the cached
  *                         prefix into a reused FP8 workspace.
  *
- * Two formats share the pool layout:
+ * Three formats share the pool structure:
  *   KV4_NVFP4     E2M1 elements, one E4M3 scale per 16 elements, one FP32
  *                 global scale per layer for K and one for V; 9 bytes per 16
  *                 values, 0.5625 of FP8 (same page, "The 56% survives its own
@@ -25,6 +25,10 @@
  *   KV4_INT4_PTH  INT4 per token and head: 4-bit codes plus per-token-head
  *                 scales, 264 bytes per head and token at head_dim 256
  *                 ("KV cache in 4 bits", section "What we changed").
+ *   KV4_FP8       FP8 E4M3 with one FP32 scale per layer for K and one for V
+ *                 (per tensor), 16 bytes per 16 values: the format the 4-bit
+ *                 cache is compared against ("The 56% survives its own
+ *                 scale").  Write and decode only.
  *
  * Encoding (the pages name the formats, not the encoder; this is the
  * library's definition, identical to the test oracle's):
@@ -37,17 +41,23 @@
  *   INT4_PTH, per (token, head) row, separately for K and V:
  *     s = amax / 7 (FP32); code = clamp(rne(x / s), -8, 7); s == 0 gives
  *     all-zero codes.  Decode: code * s.
+ *   FP8, per element with the layer's scale s: code = E4M3(x / s) (FP32
+ *     quotient, RNE, saturating at 448, sign kept).  Decode: e4m3(code) * s.
  *   Two 4-bit codes per byte: element 2j in the low nibble of byte j.
  *
  * Pool layout (one pool per layer, caller-owned device memory):
  *   base -> [num_pages][num_kv_heads][chunk_bytes]; each (page, head) chunk
- *   holds four regions, row `off` of each belonging to token `off` of the
- *   page (P = page_size, D = head_dim):
+ *   holds these regions (P = page_size, D = head_dim):
  *     NVFP4: [K codes P*D/2][V codes P*D/2][K scales P*D/16][V scales P*D/16]
  *     INT4 : [K codes P*D/2][V codes P*D/2][K scale f32 * P][V scale f32 * P]
- *   chunk_bytes = P*(D + D/8) (NVFP4) or P*(D + 8) (INT4).  A slot is
- *   page * P + off.  The FP32 global scales are not in the pool: callers pass
- *   them as a device float[2] = {g_K, g_V} per layer.
+ *     FP8  : [K codes P*D]  [V codes P*D]
+ *   chunk_bytes = P*(D + D/8) (NVFP4), P*(D + 8) (INT4), P*2*D (FP8).
+ *   Row `off` of a region belongs to token `off` of the page, except NVFP4 V,
+ *   stored in token pairs: byte d of pair row p (D bytes) holds element d of
+ *   token 2p in its low nibble and of token 2p+1 in its high nibble, and the
+ *   pair's scale row (D/8 bytes) holds block b's scale of token 2p+i at byte
+ *   2b+i.  A slot is page * P + off.  The FP32 scales are not in the pool:
+ *   callers pass them as a device float[2] = {g_K, g_V} per layer.
  *
  * Conventions for every entry point:
  *   - All device pointers are caller-owned; the library allocates nothing.
@@ -74,7 +84,7 @@
 extern "C" {
 #endif
 
-typedef enum { KV4_NVFP4 = 0, KV4_INT4_PTH = 1 } kv4_fmt;
+typedef enum { KV4_NVFP4 = 0, KV4_INT4_PTH = 1, KV4_FP8 = 2 } kv4_fmt;
 
 typedef enum {
   KV4_OK = 0,
@@ -109,8 +119,9 @@ int64_t kv4_pool_bytes(const kv4_pool* pool);
  *   slot_mapping  device int64 [T]: destination slot of token t, or < 0 to
  *                 skip it.  A slot >= num_pages*P is skipped and flagged
  *                 KV4_EBOUNDS in the device error word.
- *   layer_global_scale  device float[2] {g_K, g_V}, each > 0 (NVFP4 only;
- *                 may be NULL for INT4).
+ *   layer_global_scale  device float[2] {g_K, g_V}, each > 0: the NVFP4
+ *                 global scales or the FP8 per-tensor scales (may be NULL for
+ *                 INT4).
  *   fmt           must equal pool->fmt.
  * Writes only the rows of the slots it stores; nothing else in the pool.
  * Two tokens mapped to one slot race (last writer unspecified).
@@ -142,7 +153,7 @@ int64_t kv4_decode_workspace_bytes(int32_t batch, int32_t num_q_heads,
  *   num_splits == S  as 0, and every request's range is also cut into S equal
  *                    splits, so each head's output merges at least S pieces.
  *   q            device bf16 [B][Hq][D]
- *   layer_global_scale  device float[2] {g_K, g_V} (NVFP4; NULL for INT4)
+ *   layer_global_scale  device float[2] {g_K, g_V} (NVFP4, FP8; NULL for INT4)
  *   block_table  device int32 [B][max_pages]; entries past a request's last
  *                page are never read.
  *   seq_lens     device int32 [B]; the decode step's own token (written by
@@ -176,6 +187,7 @@ kv4_status kv4_decode_attention(const void* q, const kv4_pool* pool,
  *                grid); larger device values are clipped and flagged.
  *   fp8_scale    device float[2] {s_K, s_V}, each > 0.
  *   fp8_k, fp8_v device uint8 E4M3 [sum prefix_lens][Hkv][D].
+ * A KV4_FP8 pool is already FP8: KV4_EUNSUPPORTED.
  */
 kv4_status kv4_dequant_prefix(const kv4_pool* pool,
                               const float* layer_global_scale,

@@ -68,7 +68,11 @@ class Case:
                                     + [np.zeros(0, np.int64)]).astype(np.int64)
         amk = np.abs(bf16_bits_to_f32(self.k)).max() if T else 1.0
         amv = np.abs(bf16_bits_to_f32(self.v)).max() if T else 1.0
-        self.g = np.array([global_scale_from_amax(amk), global_scale_from_amax(amv)], np.float32)
+        if fmt == "fp8":
+            from workloads import fp8_scale_from_amax
+            self.g = np.array([fp8_scale_from_amax(amk), fp8_scale_from_amax(amv)], np.float32)
+        else:
+            self.g = np.array([global_scale_from_amax(amk), global_scale_from_amax(amv)], np.float32)
         self.q = f32_to_bf16_bits(rng.standard_normal((B, Hq, D)).astype(np.float32))
         self.sm = np.float32(1.0 / np.sqrt(D))
 

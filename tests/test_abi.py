@@ -44,6 +44,7 @@ def test_pool_sizes(lib):
     assert lib.kv4_pool_chunk_bytes(ctypes.byref(d)) == 64 * 288
     assert lib.kv4_pool_bytes(ctypes.byref(d)) == 4 * 2 * 64 * 288
     assert lib.kv4_pool_chunk_bytes(ctypes.byref(desc(fmt=1, P=1600))) == 422400
+    assert lib.kv4_pool_chunk_bytes(ctypes.byref(desc(fmt=2))) == 64 * 2 * 256      # FP8: 16 B per 16 values
     for bad in (desc(P=8), desc(P=40), desc(D=96), desc(H=0), desc(pages=0), desc(fmt=7)):
         assert lib.kv4_pool_bytes(ctypes.byref(bad)) == 0
 
@@ -101,6 +102,13 @@ def test_host_validation_rejects_without_gpu(lib):
     # prefix: max_prefix_len beyond the table
     assert lib.kv4_dequant_prefix(p, fake, fake, 2, fake, fake, 1, 1000, fake, fake, fake, None) == 1
     assert lib.kv4_dequant_prefix(p, fake, fake, 2, fake, fake, 1, 0, fake, fake, fake, None) == 0
+    # FP8 pools: write and decode need the per-tensor scales; no prefix dequant
+    d8 = desc(fmt=2, base=1 << 20)
+    st, msg = _status(lib, lib.kv4_write(fake, fake, fake, 4, ctypes.byref(d8), None, 2, None))
+    assert st == 1 and "scale" in msg
+    st, msg = _status(lib, lib.kv4_dequant_prefix(ctypes.byref(d8), fake, fake, 2, fake, fake, 1, 1,
+                                                  fake, fake, fake, None))
+    assert st == 2 and "FP8" in msg
 
 
 def test_status_strings(lib):

@@ -31,7 +31,7 @@ def test_tiny_workload():
         check_close(got, want, what=f"tiny S={S}")
 
 
-@pytest.mark.parametrize("fmt", ["nvfp4", "int4"])
+@pytest.mark.parametrize("fmt", ["nvfp4", "int4", "fp8"])
 @pytest.mark.parametrize("D", [64, 128, 256])
 def test_ragged_batch(fmt, D):
     c = Case(fmt, 2, 12, D, [1, 63, 64, 65, 700, 0, 1333], 64 if fmt == "nvfp4" else 48 * 2,
@@ -98,3 +98,12 @@ def test_bad_block_table_entry_is_flagged_not_faulted():
     c.table[0, 2] = 0
     out = c.gpu_out(pool, 1)
     assert K.kv4_device_error() == 4
+
+
+@pytest.mark.parametrize("G", [1, 6, 8, 11])
+def test_fp8_gqa_groups_and_pages(G):
+    """FP8 comparison format: GQA groups, pages that 32 does not divide, splits."""
+    c = Case("fp8", 2, 2 * G, 256, [300, 129, 16], 48, seed=100 + G, outlier_ch=(7,))
+    want = c.oracle_out()
+    for S in (0, 1, 5):
+        check_close(run(c, S).cpu().numpy(), want, what=f"fp8 G={G} S={S}")

@@ -1,5 +1,5 @@
 """kv4_write on the GPU against the oracle's encoder: packed codes and scales
-must match byte for byte (NVFP4 and INT4), including crafted rounding ties,
+must match byte for byte (NVFP4, INT4 and FP8), including crafted rounding ties,
 zero blocks, saturating blocks and skipped / out-of-range slots."""
 import numpy as np
 import pytest
@@ -14,7 +14,7 @@ from workloads import TINY, f32_to_bf16_bits
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("fmt", ["nvfp4", "int4"])
+@pytest.mark.parametrize("fmt", ["nvfp4", "int4", "fp8"])
 @pytest.mark.parametrize("D,P", [(64, 16), (128, 32), (256, 64), (256, 1600)])
 def test_write_bit_exact(fmt, D, P):
     c = Case(fmt, 2, 4, D, [37, 300, 1], P, seed=D + P, outlier_ch=(3, 77 % D))

@@ -167,6 +167,12 @@ def global_scale_from_amax(amax):
     return np.float32(a / np.float32(E2M1_MAX * E4M3_MAX)) if a > 0 else np.float32(1.0)
 
 
+def fp8_scale_from_amax(amax):
+    """FP8 per-tensor decode scale that maps the layer amax to the E4M3 maximum:
+    amax / 448 in float32 (inputs recipe of the FP8 comparison workloads)."""
+    return np.float32(np.float32(amax) / np.float32(448.0))
+
+
 def slots_for(table_row, page_size, positions):
     pos = np.asarray(positions, dtype=np.int64)
     return np.asarray(table_row, np.int64)[pos // page_size] * page_size + pos % page_size
