@@ -48,14 +48,14 @@ def algorithmic_decode_bytes(w, lens, fmt=None):
     scales for every kv head, plus q in and out (fp32) out."""
     fmt = fmt or w.fmt
     D = w.head_dim
-    per_token_head = 2 * (D // 2 + (D // 16 if fmt == "nvfp4" else 4))
+    per_token_head = {"nvfp4": 2 * (D // 2 + D // 16), "int4": 2 * (D // 2 + 4), "fp8": 2 * D}[fmt]
     kv = int(np.sum(lens, dtype=np.int64)) * w.num_kv_heads * per_token_head
     return kv + len(lens) * w.num_q_heads * D * (2 + 4)
 
 
 def algorithmic_write_bytes(w, T):
     D = w.head_dim
-    per_row = 2 * (D // 2 + (D // 16 if w.fmt == "nvfp4" else 4))
+    per_row = {"nvfp4": 2 * (D // 2 + D // 16), "int4": 2 * (D // 2 + 4), "fp8": 2 * D}[w.fmt]
     return T * w.num_kv_heads * (2 * D * 2 + per_row) + T * 8
 
 
@@ -174,8 +174,8 @@ class Setup:
             amax = torch.maximum(amax, kv.abs().amax(dim=(1, 2, 3)).float())
             kvs.append(kv)
         am = amax.cpu().numpy()
-        self.g_host = np.array([W.global_scale_from_amax(am[0]), W.global_scale_from_amax(am[1])],
-                               np.float32)
+        scale_of = W.fp8_scale_from_amax if w.fmt == "fp8" else W.global_scale_from_amax
+        self.g_host = np.array([scale_of(am[0]), scale_of(am[1])], np.float32)
         self.g = torch.from_numpy(self.g_host).to(device)
         for b in range(B):
             L = int(self.lens[b])
@@ -457,13 +457,15 @@ def kv4_arm(args):
         "gpu_launches": args.steps * s.launches_per_step(),
         "clocks": clocks.summary(),
     }
+    # back-to-back decode calls of the same workload, for the FP8 comparison
+    dec_b2b = statistics.median(time_decode_only(s, 20)) if (rank == 0 and not args.no_extra) else None
     del s
     torch.cuda.empty_cache()
 
     # ---- the other workloads of the metric (one GPU, rank 0) -------------
     if rank == 0 and not args.no_extra:
         extra = {}
-        for name in ("nvfp4_160k", "nvfp4_1m", "int4_220k"):
+        for name in ("nvfp4_160k", "nvfp4_1m", "int4_220k", "fp8_32k"):
             wx = W.ALL[name]
             sx = Setup(wx, device)
             ts = time_decode_only(sx, max(5, min(args.steps, 20)))
@@ -472,6 +474,11 @@ def kv4_arm(args):
             extra[name] = {"decode_us": med * 1e6, "gbs": bx / med / 1e9, "frac": bx / med / 1e9 / peak,
                            "num_splits": sx.splits, "kv_bytes": bx,
                            "tokens_per_s_16_layers": wx.batch / (16 * med)}
+            if name == "fp8_32k":
+                # the comparison the pages draw: same shapes and lengths as the
+                # headline workload, FP8 E4M3 per tensor instead of NVFP4
+                extra[name]["nvfp4_32k_decode_us"] = dec_b2b * 1e6
+                extra[name]["nvfp4_32k_speedup"] = med / dec_b2b
             if name == "nvfp4_160k":
                 extra["dequant_prefix_160k"] = time_prefix(sx, wx, peak)
                 extra["write_prefill_8k"] = time_write_prefill(sx, wx, peak)

@@ -194,4 +194,9 @@ CTX1M = Workload("nvfp4_1m", "nvfp4", 4, 24, 256, 1, 256, 1 << 20, 1 << 20,
 INT4_220K = Workload("int4_220k", "int4", 2, 16, 256, 8, 1600, 220000, 220000, seed=5,
                      notes="INT4 per-token-head, 2 KV heads, 16 query heads, B8 at 220,000 tokens, 1600-token pages")
 
-ALL = {w.name: w for w in (TINY, CTX32K, CTX160K, CTX1M, INT4_220K)}
+FP8_32K = Workload("fp8_32k", "fp8", 4, 24, 256, 16, 64, 24576, 32768,
+                   outliers=4, outlier_scale=10.0, seed=2, num_splits=0,
+                   notes="the 32K workload in the FP8 E4M3 per-tensor format (the comparison "
+                         "the 4-bit cache is measured against)")
+
+ALL = {w.name: w for w in (TINY, CTX32K, CTX160K, CTX1M, INT4_220K, FP8_32K)}
