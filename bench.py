@@ -484,6 +484,7 @@ def kv4_arm(args):
                 extra["write_prefill_8k"] = time_write_prefill(sx, wx, peak)
             del sx
             torch.cuda.empty_cache()
+        extra["calibrate_64k"] = time_calibrate(device, peak)
         line["workloads"] = extra
 
     if rank == 0 and not args.no_cpu:
@@ -542,6 +543,31 @@ def time_prefix(s, w, peak):
     D = w.head_dim
     byts = n * w.num_kv_heads * (2 * (D // 2 + D // 16) + 2 * D)
     return {"prefix_tokens": n, "us": med * 1e6, "gbs": byts / med / 1e9, "frac": byts / med / 1e9 / peak}
+
+
+def time_calibrate(device, peak, T=65536, Hkv=4, D=256):
+    """Serving-time NVFP4 global-scale calibration over the K and V of T
+    tokens (bf16, 2 x 134 MB: larger than L2, so an HBM figure)."""
+    import torch
+    import bit_paged_kv_kv4_gb300 as K
+    gen = torch.Generator(device=device).manual_seed(11)
+    k = torch.randn((T, Hkv, D), generator=gen, device=device).to(torch.bfloat16)
+    v = torch.randn((T, Hkv, D), generator=gen, device=device).to(torch.bfloat16)
+    out = torch.empty(2, dtype=torch.float32, device=device)
+    for _ in range(3):
+        K.kv4_calibrate_global_scale(k, v, out)
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(10):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        K.kv4_calibrate_global_scale(k, v, out)
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b) * 1e-3)
+    med = statistics.median(ts)
+    byts = 2 * T * Hkv * D * 2 + 8
+    return {"tokens": T, "us": med * 1e6, "gbs": byts / med / 1e9, "frac": byts / med / 1e9 / peak}
 
 
 def time_write_prefill(s, w, peak):

@@ -62,6 +62,7 @@ def _load(build_if_missing=False):
         "kv4_decode_attention": (i32, [vp, P, vp, vp, i32, vp, i32, i32, f32, i32, vp, i64, vp,
                                        i32, vp]),
         "kv4_dequant_prefix": (i32, [P, vp, vp, i32, vp, vp, i32, i32, vp, vp, vp, vp]),
+        "kv4_calibrate_global_scale": (i32, [vp, vp, i64, i32, i32, vp, vp]),
         "kv4_decode_attention_static_ws": (i32, [vp, P, vp, vp, i32, vp, i32, i32, f32, i32, vp,
                                                  i32, vp]),
         "kv4_device_error": (i32, []),
@@ -168,6 +169,14 @@ def kv4_decode_attention_static_ws(q, pool, layer_global_scale, block_table, seq
         _ptr(seq_lens), B, Hq, float(sm_scale), int(num_splits), _ptr(out),
         1 if out.dtype == torch.float32 else 0, _stream(stream))
     _check(st, "kv4_decode_attention_static_ws")
+
+
+def kv4_calibrate_global_scale(k, v, out, stream=None):
+    """NVFP4 global scales {g_K, g_V} of bf16 k, v [T, Hkv, D] into ``out``
+    (float32 CUDA tensor of 2): amax / 2688 each, 1 for an all-zero tensor."""
+    T, H, D = k.shape
+    st = _load().kv4_calibrate_global_scale(_ptr(k), _ptr(v), T, H, D, _ptr(out), _stream(stream))
+    _check(st, "kv4_calibrate_global_scale")
 
 
 def kv4_dequant_prefix(pool, layer_global_scale, block_table, prefix_lens, cu_prefix,

@@ -303,6 +303,26 @@ kv4_status kv4_decode_attention(const void* q, const kv4_pool* pool,
   return e == cudaSuccess ? KV4_OK : cuda_fail(e, "kv4_decode_attention launch");
 }
 
+kv4_status kv4_calibrate_global_scale(const void* k, const void* v, int64_t num_tokens,
+                                      int32_t num_kv_heads, int32_t head_dim,
+                                      float* layer_global_scale, void* stream) {
+  g_msg.clear();
+  if (num_tokens < 0 || num_kv_heads < 1) return fail(KV4_EINVAL, "num_tokens < 0 or num_kv_heads < 1");
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256)
+    return fail(KV4_EUNSUPPORTED, "head_dim %d not built (64, 128, 256)", head_dim);
+  if (layer_global_scale == nullptr || !aligned(layer_global_scale, 8))
+    return fail(KV4_EINVAL, "layer_global_scale must be a non-NULL, 8-byte aligned float[2]");
+  if (num_tokens > 0 && (k == nullptr || v == nullptr || !aligned(k, 16) || !aligned(v, 16)))
+    return fail(KV4_EINVAL, "k and v must be non-NULL and 16-byte aligned");
+  kv4::CalibArgs a{};
+  a.k = static_cast<const __nv_bfloat16*>(k);
+  a.v = static_cast<const __nv_bfloat16*>(v);
+  a.n = num_tokens * num_kv_heads * head_dim;
+  a.out = layer_global_scale;
+  cudaError_t e = kv4::launch_calibrate(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KV4_OK : cuda_fail(e, "kv4_calibrate_global_scale launch");
+}
+
 kv4_status kv4_dequant_prefix(const kv4_pool* pool, const float* layer_global_scale,
                               const int32_t* block_table, int32_t max_pages,
                               const int32_t* prefix_lens, const int64_t* cu_prefix,

@@ -1,0 +1,72 @@
+// Serving-time calibration of the NVFP4 global scales ("SGLang's 4-bit KV
+// cache", Figure 2: per-layer FP32 global scales; the caveat above "The
+// agentic result": the measured runs dropped them and calibration is listed
+// as ongoing work).  g = float32(amax) / 2688 (E2M1 max x E4M3 max), one
+// FP32 rounding, and g = 1 when amax is not positive.
+//
+// amax_kernel: every thread takes 8 bf16 at a time (one 16-byte load) in a
+// grid-stride loop and keeps the largest |x| as bits (a non-negative float's
+// bit pattern orders like the float); warps and the block reduce it and one
+// atomicMax per block lands in the caller's output word, which the launch
+// cleared first.  finalize_kernel turns the two maxima into the scales.
+// The maximum is exact and order-free, so the result is deterministic.
+#include <cstdint>
+
+#include "kv4_device.cuh"
+#include "kv4_internal.h"
+
+namespace kv4 {
+
+__global__ void __launch_bounds__(256)
+amax_kernel(const CalibArgs a) {
+  const uint4* src = reinterpret_cast<const uint4*>(blockIdx.y == 0 ? a.k : a.v);
+  const int64_t n8 = a.n / 8;
+  uint32_t m = 0;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint4 w = __ldg(src + i);
+    const uint32_t x[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      m = max(m, x[j] & 0x7FFFu);                 // |bf16| of the low element
+      m = max(m, (x[j] >> 16) & 0x7FFFu);         // and of the high one
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __shared__ uint32_t red[8];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < 8; ++w) m = max(m, red[w]);
+    // bf16 bits << 16 are the FP32 bits of the same value
+    atomicMax(reinterpret_cast<unsigned int*>(a.out) + blockIdx.y, m << 16);
+  }
+}
+
+__global__ void finalize_kernel(float* out) {
+  const int i = threadIdx.x;
+  if (i < 2) {
+    const float amax = __uint_as_float(reinterpret_cast<const unsigned int*>(out)[i]);
+    out[i] = (amax > 0.f) ? __fdiv_rn(amax, 2688.0f) : 1.0f;
+  }
+}
+
+cudaError_t launch_calibrate(const CalibArgs& a, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(a.out, 0, 2 * sizeof(float), st);
+  if (e != cudaSuccess) return e;
+  if (a.n > 0) {
+    int dev = 0, sms = 152;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t want = (a.n / 8 + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(sms) * 8;             // enough blocks to fill the GPU
+    const unsigned blocks = static_cast<unsigned>(want < cap ? (want > 0 ? want : 1) : cap);
+    amax_kernel<<<dim3(blocks, 2), 256, 0, st>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  finalize_kernel<<<1, 32, 0, st>>>(a.out);
+  return cudaGetLastError();
+}
+
+}  // namespace kv4

@@ -81,6 +81,14 @@ struct PrefixArgs {
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& map, cudaStream_t st);
 cudaError_t launch_write(const WriteArgs& a, cudaStream_t st);
 cudaError_t launch_prefix(const PrefixArgs& a, cudaStream_t st);
+
+struct CalibArgs {
+  const __nv_bfloat16* k;       // [n] elements (T * Hkv * D)
+  const __nv_bfloat16* v;
+  int64_t n;
+  float* out;                   // [2]
+};
+cudaError_t launch_calibrate(const CalibArgs& a, cudaStream_t st);
 int decode_tile_tokens(int fmt);
 // Sets the message kv4_last_error_message() returns on this thread.
 void set_error_message(const char* msg);

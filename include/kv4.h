@@ -198,6 +198,23 @@ kv4_status kv4_dequant_prefix(const kv4_pool* pool,
                               void* fp8_k, void* fp8_v, void* stream);
 
 /*
+ * kv4_calibrate_global_scale -- the NVFP4 global scales of one layer from its
+ * K and V at serving time ("SGLang's 4-bit KV cache": Figure 2 keeps
+ * per-layer FP32 global scales; the measured runs dropped them, and the post
+ * lists calibration as ongoing work).  For each of K and V:
+ *     g = float32(amax) / 2688   (E2M1 max 6 x E4M3 max 448, FP32 rounding)
+ * with amax the largest |x| over the tensor, and g = 1 when amax is not
+ * positive.  The layer maximum then encodes to E4M3 scale 448 and code 6.
+ *   k, v          device bf16 [T][Hkv][D], 16-byte aligned (T may be 0).
+ *   layer_global_scale  device float[2], 8-byte aligned: receives {g_K, g_V}
+ *                 (used as scratch while the maxima are reduced).
+ * Inputs must be finite (a NaN gives g = 1).  Deterministic.
+ */
+kv4_status kv4_calibrate_global_scale(const void* k, const void* v, int64_t num_tokens,
+                                      int32_t num_kv_heads, int32_t head_dim,
+                                      float* layer_global_scale, void* stream);
+
+/*
  * kv4_decode_attention_static_ws -- kv4_decode_attention for callers that
  * cannot allocate device memory.  The pages have no counterpart of this call;
  * it exists for library users, not for the method.

@@ -119,3 +119,15 @@ def fp8_quantize(x_bf16, s):
 def fp8_dequantize(codes, s):
     """E4M3 codes -> float64 values e4m3(code) * s."""
     return e4m3_decode(codes) * np.float64(np.float32(s))
+
+
+def calibrate_global_scale(x_bf16):
+    """Serving-time calibration of one NVFP4 global scale ("SGLang's 4-bit KV
+    cache": Figure 2 keeps per-layer FP32 global scales; the measured runs
+    dropped them and the post lists calibration as ongoing work).  Reading:
+    the tensor's absolute maximum mapped onto E2M1 max x E4M3 max,
+    g = float32(amax) / 2688 (one FP32 rounding), and g = 1 when amax is not
+    positive (an all-zero tensor encodes to zeros whatever g is)."""
+    x = bf16_to_f32(np.asarray(x_bf16))
+    amax = np.float32(np.max(np.abs(x))) if x.size else np.float32(0.0)
+    return np.float32(amax / np.float32(2688.0)) if amax > 0 else np.float32(1.0)

@@ -109,6 +109,10 @@ def test_host_validation_rejects_without_gpu(lib):
     st, msg = _status(lib, lib.kv4_dequant_prefix(ctypes.byref(d8), fake, fake, 2, fake, fake, 1, 1,
                                                   fake, fake, fake, None))
     assert st == 2 and "FP8" in msg
+    # calibration: output pointer, head_dim, alignment
+    assert lib.kv4_calibrate_global_scale(fake, fake, 4, 2, 256, None, None) == 1
+    assert lib.kv4_calibrate_global_scale(fake, fake, 4, 2, 96, fake, None) == 2
+    assert lib.kv4_calibrate_global_scale(ctypes.c_void_p((1 << 20) + 2), fake, 4, 2, 256, fake, None) == 1
 
 
 def test_status_strings(lib):

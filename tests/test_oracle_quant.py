@@ -255,3 +255,22 @@ def test_fp8_quantize_matches_torch_cast():
     finite = (c & 0x7F) != 0x7F
     v = Q.fp8_dequantize(c[finite], np.float32(0.5))
     assert np.allclose(v, torch.from_numpy(c[finite]).view(torch.float8_e4m3fn).float().numpy() * 0.5)
+
+
+def test_calibrate_global_scale():
+    """g = amax / (6 * 448) in FP32, 1 for an all-zero tensor; the layer
+    amax then encodes to the largest E4M3 scale (0x7E) and E2M1 code 6."""
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal((300, 4, 64)).astype(np.float32) * 7
+    xb = f32_to_bf16_bits(x)
+    amax = np.abs(F.bf16_to_f32(xb)).max()
+    g = Q.calibrate_global_scale(xb)
+    assert g == np.float32(np.float32(amax) / np.float32(2688.0))
+    assert Q.calibrate_global_scale(np.zeros((3, 64), np.uint16)) == np.float32(1.0)
+    assert Q.calibrate_global_scale(f32_to_bf16_bits(np.array([[2688.0, -1.0]], np.float32))) == 1.0
+    # with the calibrated g the block holding the amax gets scale code 0x7E
+    flat = xb.reshape(-1, 64)
+    row = np.argmax(np.abs(F.bf16_to_f32(flat)).max(axis=1))
+    codes, scales = Q.nvfp4_quantize(flat[row][None], g)
+    blk = np.argmax(np.abs(F.bf16_to_f32(flat[row])).reshape(4, 16).max(axis=1))
+    assert scales[0, blk] == 0x7E
