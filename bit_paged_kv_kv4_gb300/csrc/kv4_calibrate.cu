@@ -4,11 +4,12 @@
 // as ongoing work).  g = float32(amax) / 2688 (E2M1 max x E4M3 max), one
 // FP32 rounding, and g = 1 when amax is not positive.
 //
-// amax_kernel: every thread takes 8 bf16 at a time (one 16-byte load) in a
-// grid-stride loop and keeps the largest |x| as bits (a non-negative float's
-// bit pattern orders like the float); warps and the block reduce it and one
-// atomicMax per block lands in the caller's output word, which the launch
-// cleared first.  finalize_kernel turns the two maxima into the scales.
+// amax_kernel: every thread takes 8 bf16 per 16-byte load, four loads in
+// flight, in a grid-stride loop, and keeps the largest |x| as bits (a
+// non-negative float's bit pattern orders like the float); warps and the
+// block reduce it and one atomicMax per block lands in the caller's output
+// word, which the launch cleared first.  finalize_kernel turns the two
+// maxima into the scales.
 // The maximum is exact and order-free, so the result is deterministic.
 #include <cstdint>
 
@@ -21,17 +22,26 @@ __global__ void __launch_bounds__(256)
 amax_kernel(const CalibArgs a) {
   const uint4* src = reinterpret_cast<const uint4*>(blockIdx.y == 0 ? a.k : a.v);
   const int64_t n8 = a.n / 8;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   uint32_t m = 0;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const uint4 w = __ldg(src + i);
+  auto fold = [&m](const uint4 w) {
     const uint32_t x[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       m = max(m, x[j] & 0x7FFFu);                 // |bf16| of the low element
       m = max(m, (x[j] >> 16) & 0x7FFFu);         // and of the high one
     }
+  };
+  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  // four independent 16-byte loads in flight per thread, then the tail
+  for (; i + 3 * stride < n8; i += 4 * stride) {
+    uint4 w[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) w[u] = __ldg(src + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) fold(w[u]);
   }
+  for (; i < n8; i += stride) fold(__ldg(src + i));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
   __shared__ uint32_t red[8];
@@ -60,7 +70,7 @@ cudaError_t launch_calibrate(const CalibArgs& a, cudaStream_t st) {
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int64_t want = (a.n / 8 + 255) / 256;
-    const int64_t cap = static_cast<int64_t>(sms) * 8;             // enough blocks to fill the GPU
+    const int64_t cap = static_cast<int64_t>(sms) * 4;  // x 2 tensors: one wave of 8 blocks per SM
     const unsigned blocks = static_cast<unsigned>(want < cap ? (want > 0 ? want : 1) : cap);
     amax_kernel<<<dim3(blocks, 2), 256, 0, st>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
