@@ -149,3 +149,63 @@ def dequant_prefix(pool, spec, gscale, block_table, prefix_lens, fp8_scale):
                     ws[kind][row + lo:row + hi, h] = e4m3_encode((xh / s).astype(np.float32))
         row += n
     return ws["k"], ws["v"]
+
+
+def extend_attention(q, chunk_k, chunk_v, prefix_k, prefix_v, fp8_scale, prefix_lens,
+                     chunk_lens, sm_scale, rows=None):
+    """FP64 chunked-prefill / extend attention over an FP8 prefix plus an FP8 chunk.
+
+    Figure 2 of "SGLang's 4-bit KV cache", right-hand column: the current
+    chunk arrives as FP8 K/V, the cached prefix has been dequantised into the
+    FP8 workspace (``dequant_prefix``), and the chunk's queries attend over
+    prefix plus chunk.  For request b with prefix length Lp = prefix_lens[b]
+    and chunk length C = chunk_lens[b], the key sequence is the Lp prefix rows
+    followed by the C chunk rows; chunk query i sits at position Lp + i and
+    sees keys 0 .. Lp + i (all of the prefix, and the chunk causally up to
+    itself).  Values are e4m3(code) * s with s = fp8_scale[0] for K and
+    fp8_scale[1] for V (one per-tensor scale pair for prefix and chunk), and
+
+        out[i, j] = sum_k softmax_k(sm_scale * <q_ij, K_k>) V_k
+
+    over the visible keys of kv head j // (Hq / Hkv), in float64.
+
+    q: uint16 bf16 bits [sum C, Hq, D]; chunk_k/v: uint8 E4M3 [sum C, Hkv, D];
+    prefix_k/v: uint8 E4M3 [sum Lp, Hkv, D]; rows of request b start at the
+    exclusive prefix sums of chunk_lens / prefix_lens.  rows: optional
+    iterable of (chunk row, query head) to compute; others stay zero.
+    Returns float64 [sum C, Hq, D].
+    """
+    T, Hq, D = q.shape
+    Hkv = chunk_k.shape[1]
+    G = Hq // Hkv
+    sk, sv = float(np.float32(fp8_scale[0])), float(np.float32(fp8_scale[1]))
+    out = np.zeros((T, Hq, D), np.float64)
+    cu_c = np.concatenate([[0], np.cumsum(np.asarray(chunk_lens, np.int64))])
+    cu_p = np.concatenate([[0], np.cumsum(np.asarray(prefix_lens, np.int64))])
+    want = None if rows is None else {}
+    if rows is not None:
+        for r, j in rows:
+            want.setdefault(int(r), set()).add(int(j))
+    for b in range(len(chunk_lens)):
+        C, Lp = int(chunk_lens[b]), int(prefix_lens[b])
+        if C == 0:
+            continue
+        r0, p0 = int(cu_c[b]), int(cu_p[b])
+        sel = range(C) if want is None else sorted(i - r0 for i in want if r0 <= i < r0 + C)
+        if not sel:
+            continue
+        for h in range(Hkv):
+            keys = np.concatenate([e4m3_decode(prefix_k[p0:p0 + Lp, h]),
+                                   e4m3_decode(chunk_k[r0:r0 + C, h])]) * sk
+            vals = np.concatenate([e4m3_decode(prefix_v[p0:p0 + Lp, h]),
+                                   e4m3_decode(chunk_v[r0:r0 + C, h])]) * sv
+            for j in range(h * G, (h + 1) * G):
+                for i in sel:
+                    if want is not None and j not in want[r0 + i]:
+                        continue
+                    n = Lp + i + 1                      # visible keys of query i
+                    qv = bf16_to_f32(q[r0 + i, j]).astype(np.float64)
+                    s = float(sm_scale) * (keys[:n] @ qv)
+                    p = np.exp(s - s.max())
+                    out[r0 + i, j] = (p @ vals[:n]) / p.sum()
+    return out
