@@ -1,13 +1,15 @@
 """Python binding of libkv4 (include/kv4.h): a 4-bit paged KV cache for GB300.
 
-Argument marshalling only.  Every step of the write, decode and prefix paths
-runs in the library's CUDA kernels; torch supplies device memory and streams.
+Argument marshalling only.  Every step of the write, decode, prefix, extend
+and calibration paths runs in the library's CUDA kernels; torch supplies
+device memory and streams.
 There is no fallback: if libkv4.so is missing or cannot load, importing the
 binding's functions raises.
 
 The functions carry the C names: ``kv4_write``, ``kv4_decode_attention``,
-``kv4_dequant_prefix``, plus the sizing helpers and ``Pool`` (the pool
-descriptor with its device buffer).
+``kv4_dequant_prefix``, ``kv4_extend_attention``,
+``kv4_calibrate_global_scale``, plus the sizing helpers and ``Pool`` (the
+pool descriptor with its device buffer).
 """
 import ctypes
 import os
@@ -63,6 +65,8 @@ def _load(build_if_missing=False):
                                        i32, vp]),
         "kv4_dequant_prefix": (i32, [P, vp, vp, i32, vp, vp, i32, i32, vp, vp, vp, vp]),
         "kv4_calibrate_global_scale": (i32, [vp, vp, i64, i32, i32, vp, vp]),
+        "kv4_extend_attention": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
+                                       i32, i32, f32, vp, i32, vp]),
         "kv4_decode_attention_static_ws": (i32, [vp, P, vp, vp, i32, vp, i32, i32, f32, i32, vp,
                                                  i32, vp]),
         "kv4_device_error": (i32, []),
@@ -188,6 +192,21 @@ def kv4_dequant_prefix(pool, layer_global_scale, block_table, prefix_lens, cu_pr
         _ptr(prefix_lens), _ptr(cu_prefix), prefix_lens.shape[0], int(max_prefix_len),
         _ptr(fp8_scale), _ptr(fp8_k), _ptr(fp8_v), _stream(stream))
     _check(st, "kv4_dequant_prefix")
+
+
+def kv4_extend_attention(q, chunk_k, chunk_v, prefix_k, prefix_v, fp8_scale, prefix_lens,
+                         cu_prefix, chunk_lens, cu_chunk, max_chunk_len, sm_scale, out,
+                         stream=None):
+    """Extend attention of the chunk's queries q (bf16 [sum C, Hq, D]) over
+    the FP8 prefix workspace plus the FP8 chunk K/V; out is bf16 or float32
+    [sum C, Hq, D]."""
+    Hq, D = q.shape[1], q.shape[2]
+    st = _load().kv4_extend_attention(
+        _ptr(q), _ptr(chunk_k), _ptr(chunk_v), _ptr(prefix_k), _ptr(prefix_v), _ptr(fp8_scale),
+        _ptr(prefix_lens), _ptr(cu_prefix), _ptr(chunk_lens), _ptr(cu_chunk),
+        chunk_lens.shape[0], int(max_chunk_len), Hq, chunk_k.shape[1], D, float(sm_scale),
+        _ptr(out), 1 if out.dtype == torch.float32 else 0, _stream(stream))
+    _check(st, "kv4_extend_attention")
 
 
 def kv4_device_error():

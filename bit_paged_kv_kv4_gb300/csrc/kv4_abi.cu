@@ -376,6 +376,59 @@ kv4_status kv4_dequant_prefix(const kv4_pool* pool, const float* layer_global_sc
   return e == cudaSuccess ? KV4_OK : cuda_fail(e, "kv4_dequant_prefix launch");
 }
 
+kv4_status kv4_extend_attention(const void* q, const void* chunk_k, const void* chunk_v,
+                                const void* prefix_k, const void* prefix_v,
+                                const float* fp8_scale, const int32_t* prefix_lens,
+                                const int64_t* cu_prefix, const int32_t* chunk_lens,
+                                const int64_t* cu_chunk, int32_t batch, int32_t max_chunk_len,
+                                int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                float sm_scale, void* out, int32_t out_is_fp32, void* stream) {
+  g_msg.clear();
+  if (batch < 0 || max_chunk_len < 0) return fail(KV4_EINVAL, "batch and max_chunk_len must be >= 0");
+  if (num_kv_heads < 1 || num_q_heads < 1 || num_q_heads % num_kv_heads != 0)
+    return fail(KV4_EINVAL, "num_q_heads must be a positive multiple of num_kv_heads");
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256)
+    return fail(KV4_EUNSUPPORTED, "head_dim %d not built (64, 128, 256)", head_dim);
+  if (!(sm_scale > 0.f) || !(sm_scale < 3.0e38f)) return fail(KV4_EINVAL, "sm_scale must be positive and finite");
+  if (batch > 65535) return fail(KV4_EINVAL, "batch exceeds the launch grid");
+  if ((static_cast<int64_t>(max_chunk_len) + 127) / 128 > 65535)
+    return fail(KV4_EINVAL, "max_chunk_len exceeds the launch grid");
+  if (batch == 0 || max_chunk_len == 0) return KV4_OK;
+  if (q == nullptr || chunk_k == nullptr || chunk_v == nullptr || prefix_k == nullptr ||
+      prefix_v == nullptr || fp8_scale == nullptr || prefix_lens == nullptr ||
+      cu_prefix == nullptr || chunk_lens == nullptr || cu_chunk == nullptr || out == nullptr)
+    return fail(KV4_EINVAL, "device pointers must be non-NULL");
+  if (!aligned(q, 16) || !aligned(chunk_k, 16) || !aligned(chunk_v, 16) || !aligned(prefix_k, 16) ||
+      !aligned(prefix_v, 16) || !aligned(out, 16) || !aligned(cu_prefix, 8) || !aligned(cu_chunk, 8) ||
+      !aligned(fp8_scale, 4) || !aligned(prefix_lens, 4) || !aligned(chunk_lens, 4))
+    return fail(KV4_EINVAL, "device buffers must be 16-byte aligned (int64 arrays 8-byte)");
+
+  kv4::ExtendArgs a{};
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.ck = static_cast<const uint8_t*>(chunk_k);
+  a.cv = static_cast<const uint8_t*>(chunk_v);
+  a.pk = static_cast<const uint8_t*>(prefix_k);
+  a.pv = static_cast<const uint8_t*>(prefix_v);
+  a.fp8_scale = fp8_scale;
+  a.prefix_lens = prefix_lens;
+  a.cu_prefix = cu_prefix;
+  a.chunk_lens = chunk_lens;
+  a.cu_chunk = cu_chunk;
+  a.B = batch;
+  a.max_chunk_len = max_chunk_len;
+  a.Hq = num_q_heads;
+  a.Hkv = num_kv_heads;
+  a.D = head_dim;
+  a.G = num_q_heads / num_kv_heads;
+  a.sm_scale = sm_scale;
+  a.out = out;
+  a.out_f32 = out_is_fp32 ? 1 : 0;
+  a.err = error_word();
+  if (a.err == nullptr) return fail(KV4_ECUDA, "no CUDA device / error word unavailable");
+  cudaError_t e = kv4::launch_extend(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KV4_OK : cuda_fail(e, "kv4_extend_attention launch");
+}
+
 int32_t kv4_device_error(void) {
   int* p = error_word();
   if (p == nullptr) return KV4_ECUDA;

@@ -89,6 +89,25 @@ struct CalibArgs {
   float* out;                   // [2]
 };
 cudaError_t launch_calibrate(const CalibArgs& a, cudaStream_t st);
+
+struct ExtendArgs {
+  const __nv_bfloat16* q;       // [sum C][Hq][D]
+  const uint8_t* ck;            // E4M3 [sum C][Hkv][D]
+  const uint8_t* cv;
+  const uint8_t* pk;            // E4M3 [sum Lp][Hkv][D]
+  const uint8_t* pv;
+  const float* fp8_scale;       // [2] {s_K, s_V}
+  const int32_t* prefix_lens;   // [B]
+  const int64_t* cu_prefix;     // [B+1]
+  const int32_t* chunk_lens;    // [B]
+  const int64_t* cu_chunk;      // [B+1]
+  int B, max_chunk_len, Hq, Hkv, D, G;
+  float sm_scale;
+  void* out;                    // [sum C][Hq][D] bf16 or f32
+  int out_f32;
+  int* err;
+};
+cudaError_t launch_extend(const ExtendArgs& a, cudaStream_t st);
 int decode_tile_tokens(int fmt);
 // Sets the message kv4_last_error_message() returns on this thread.
 void set_error_message(const char* msg);

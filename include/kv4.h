@@ -2,20 +2,25 @@
  * kv4.h -- C ABI of libkv4: a 4-bit paged KV cache for LLM decode on GB300
  * (sm_103a).
  *
- * Three operations, after the three attention paths over one pool in
- * "SGLang's 4-bit KV cache: the 56% is exact, the 1.78x is untested",
- * Figure 2 caption:
+ * The operations follow the three attention paths over one pool drawn in
+ * Figure 2 of "SGLang's 4-bit KV cache: the 56% is exact, the 1.78x is
+ * untested":
  *
- *   kv4_write             quantise new K/V tokens into the paged pool
- *                         (the write into "a GPU KV pool of packed E2M1 K and
- *                         V, block scales at one E4M3 per sixteen elements,
- *                         and per-layer FP32 global scales");
+ *   kv4_write             quantise new K/V tokens into the paged pool (the
+ *                         pool holds packed E2M1 K and V, one E4M3 block
+ *                         scale per 16 elements and FP32 global scales per
+ *                         layer);
  *   kv4_decode_attention  decode attention that reads the 4-bit pool and
- *                         dequantises inside the kernel ("Only decode reads
- *                         NVFP4 and dequantizes inside the kernel"), split
+ *                         dequantises inside the kernel (decode is the only
+ *                         path that reads the 4-bit cache directly), split
  *                         over the sequence with a log-sum-exp combine;
- *   kv4_dequant_prefix    the chunked-prefill path: dequantise the cached
- *                         prefix into a reused FP8 workspace.
+ *   kv4_dequant_prefix    the chunked-prefill path, first step: dequantise
+ *                         the cached prefix into a reused FP8 workspace;
+ *   kv4_extend_attention  the chunked-prefill path, second step: the chunk's
+ *                         queries attend over that FP8 prefix plus the FP8
+ *                         current chunk, on the tensor cores;
+ *   kv4_calibrate_global_scale  the per-layer FP32 global scales from the
+ *                         layer's K and V at serving time.
  *
  * Three formats share the pool structure:
  *   KV4_NVFP4     E2M1 elements, one E4M3 scale per 16 elements, one FP32
@@ -196,6 +201,44 @@ kv4_status kv4_dequant_prefix(const kv4_pool* pool,
                               const int64_t* cu_prefix, int32_t batch,
                               int32_t max_prefix_len, const float* fp8_scale,
                               void* fp8_k, void* fp8_v, void* stream);
+
+/*
+ * kv4_extend_attention -- the chunked-prefill / extend attention of Figure 2
+ * ("SGLang's 4-bit KV cache", right-hand column): the current chunk's
+ * queries attend over the cached prefix (the FP8 workspace that
+ * kv4_dequant_prefix wrote) plus the current chunk, which arrives as FP8
+ * K/V.  For request b with prefix length Lp = prefix_lens[b] and chunk
+ * length C = chunk_lens[b], chunk query i sits at position Lp + i and sees
+ * every prefix key and chunk keys 0..i:
+ *     out[i][j] = sum_k softmax_k(sm_scale * <q_ij, K_k>) V_k
+ * over those keys of kv head j / (Hq / Hkv), K_k = e4m3(code) * fp8_scale[0],
+ * V_k = e4m3(code) * fp8_scale[1] (one per-tensor scale pair for prefix and
+ * chunk).  Computed on the tensor cores with f16 operands (exact for the FP8
+ * values; q rounded to f16, |q| <= 65504 else KV4_EINVAL in the error word),
+ * softmax weights rounded to f16 and FP32 accumulation.
+ *   q            device bf16 [sum C][Hq][D]; row cu_chunk[b] + i is chunk
+ *                token i of request b.
+ *   chunk_k/v    device uint8 E4M3 [sum C][Hkv][D], same rows as q.
+ *   prefix_k/v   device uint8 E4M3 [sum Lp][Hkv][D]; rows of request b start
+ *                at cu_prefix[b] (the kv4_dequant_prefix layout).
+ *   fp8_scale    device float[2] {s_K, s_V}, each > 0.
+ *   prefix_lens, chunk_lens  device int32 [B] (>= 0, Lp + C < 2^31);
+ *   cu_prefix, cu_chunk      device int64 [B+1] exclusive prefix sums.
+ *   max_chunk_len  host upper bound of every chunk_lens[b] (sizes the grid);
+ *                larger device values leave rows uncomputed and are flagged
+ *                (KV4_EBOUNDS in the error word).
+ *   sm_scale     > 0.   out  device [sum C][Hq][D], bf16 or FP32.
+ * All device buffers 16-byte aligned (the int64 arrays 8-byte); Hq a
+ * multiple of Hkv; head_dim 64, 128 or 256.  Asynchronous on `stream`;
+ * allocates nothing.
+ */
+kv4_status kv4_extend_attention(const void* q, const void* chunk_k, const void* chunk_v,
+                                const void* prefix_k, const void* prefix_v,
+                                const float* fp8_scale, const int32_t* prefix_lens,
+                                const int64_t* cu_prefix, const int32_t* chunk_lens,
+                                const int64_t* cu_chunk, int32_t batch, int32_t max_chunk_len,
+                                int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                float sm_scale, void* out, int32_t out_is_fp32, void* stream);
 
 /*
  * kv4_calibrate_global_scale -- the NVFP4 global scales of one layer from its

@@ -26,7 +26,8 @@ def declared_functions():
 
 def test_header_declares_the_three_operations():
     names = declared_functions()
-    for n in ("kv4_write", "kv4_decode_attention", "kv4_dequant_prefix"):
+    for n in ("kv4_write", "kv4_decode_attention", "kv4_dequant_prefix", "kv4_extend_attention",
+              "kv4_calibrate_global_scale"):
         assert n in names
 
 
@@ -122,3 +123,24 @@ def test_status_strings(lib):
 
 def test_build_is_in_tree():
     assert os.path.dirname(_build.LIB) == os.path.dirname(K.__file__)
+
+
+def test_extend_validation_without_gpu(lib):
+    fake = ctypes.c_void_p(1 << 20)
+
+    def ext(**kw):
+        a = dict(q=fake, ck=fake, cv=fake, pk=fake, pv=fake, s=fake, pl=fake, cp=fake, cl=fake,
+                 cc=fake, B=2, mc=300, Hq=24, Hkv=4, D=256, sm=0.0625, out=fake, f32=0)
+        a.update(kw)
+        return lib.kv4_extend_attention(a["q"], a["ck"], a["cv"], a["pk"], a["pv"], a["s"], a["pl"],
+                                        a["cp"], a["cl"], a["cc"], a["B"], a["mc"], a["Hq"], a["Hkv"],
+                                        a["D"], a["sm"], a["out"], a["f32"], None)
+    assert ext(Hq=25) == 1                      # heads not a multiple of kv heads
+    assert ext(D=96) == 2                       # head_dim not built
+    assert ext(sm=0.0) == 1 and ext(sm=float("nan")) == 1
+    assert ext(B=-1) == 1 and ext(mc=-5) == 1
+    assert ext(B=70000) == 1
+    assert ext(pk=None) == 1                    # missing prefix workspace
+    st, msg = _status(lib, ext(q=ctypes.c_void_p((1 << 20) + 8)))
+    assert st == 1 and "aligned" in msg
+    assert ext(B=0) == 0 and ext(mc=0) == 0     # nothing to do

@@ -160,6 +160,35 @@ def device_q(w, device, salt=0):
     return q.to(torch.bfloat16), kv[0].to(torch.bfloat16), kv[1].to(torch.bfloat16)
 
 
+def fp8_kv_codes(seed, L, Hkv, D, device, outlier_channels=None, outlier_scale=1.0, scales=None):
+    """Seeded FP8 K/V input of the extend path: normal draws (outlier channels
+    of each kv head scaled up) mapped onto the E4M3 range by per-tensor scales
+    and encoded by torch's float8_e4m3fn cast.  Returns (uint8 codes
+    [2, L, Hkv, D], float32 scales [2]); `scales` fixes the scales instead of
+    deriving them from the draws' maxima (amax / 448)."""
+    import torch
+    gen = torch.Generator(device=device).manual_seed(9_000_011 * (seed + 1) + L)
+    x = torch.randn((2, L, Hkv, D), generator=gen, device=device)
+    if outlier_channels is not None:
+        for h, ch in enumerate(outlier_channels):
+            if len(ch):
+                x[:, :, h, torch.as_tensor(ch, device=device)] *= outlier_scale
+    if scales is None:
+        am = x.abs().amax(dim=(1, 2, 3)).cpu().numpy() if L else np.ones(2, np.float32)
+        scales = np.array([fp8_scale_from_amax(a) for a in am], np.float32)
+    s = torch.as_tensor(np.asarray(scales, np.float32), device=device)
+    # saturate like a satfinite encoder: fixed scales may not cover every draw
+    codes = (x / s.view(2, 1, 1, 1)).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes, np.asarray(scales, np.float32)
+
+
+def extend_q(seed, T, Hq, D, device):
+    """Seeded bf16 queries [T, Hq, D] of an extend chunk."""
+    import torch
+    gen = torch.Generator(device=device).manual_seed(5_000_011 * (seed + 1) + T)
+    return torch.randn((T, Hq, D), generator=gen, device=device).to(torch.bfloat16)
+
+
 def global_scale_from_amax(amax):
     """The per-layer FP32 global scale used by the workloads: the layer's
     absolute maximum mapped onto E2M1 max x E4M3 max, amax / (6 * 448)."""
