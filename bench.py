@@ -38,6 +38,7 @@ import workloads as W  # noqa: E402
 
 METRIC = "NVFP4 decode-attn achieved HBM GB/s (% of peak) at 32K/160K/1M ctx"
 EVENT_EVERY = 4       # timed-loop steps per sampled decode-event pair
+FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
 
@@ -67,6 +68,17 @@ def read_peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def read_tensor_peak():
+    """(dense f16/bf16 tensor TFLOP/s burst, source).  kind::f16 runs f16 and
+    bf16 operands at the same rate, so the measured bf16 GEMM peak serves."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured bf16_tflops (burst)"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def decode_source_hash():
@@ -480,7 +492,9 @@ def kv4_arm(args):
                 extra[name]["nvfp4_32k_decode_us"] = dec_b2b * 1e6
                 extra[name]["nvfp4_32k_speedup"] = med / dec_b2b
             if name == "nvfp4_160k":
-                extra["dequant_prefix_160k"] = time_prefix(sx, wx, peak)
+                extra["dequant_prefix_160k"], ws = time_prefix(sx, wx, peak, keep=True)
+                extra["extend_160k"] = time_extend(device, wx, ws, read_tensor_peak()[0])
+                del ws
                 extra["write_prefill_8k"] = time_write_prefill(sx, wx, peak)
             del sx
             torch.cuda.empty_cache()
@@ -512,7 +526,7 @@ def kv4_arm(args):
     return 0
 
 
-def time_prefix(s, w, peak):
+def time_prefix(s, w, peak, keep=False):
     import torch
     K = s.K
     prefix = np.array([max(int(s.lens[0]) - w.prefix_chunk, 0)], np.int32)
@@ -542,7 +556,52 @@ def time_prefix(s, w, peak):
     med = statistics.median(ts)
     D = w.head_dim
     byts = n * w.num_kv_heads * (2 * (D // 2 + D // 16) + 2 * D)
-    return {"prefix_tokens": n, "us": med * 1e6, "gbs": byts / med / 1e9, "frac": byts / med / 1e9 / peak}
+    r = {"prefix_tokens": n, "us": med * 1e6, "gbs": byts / med / 1e9, "frac": byts / med / 1e9 / peak}
+    return (r, (wk, wv, s8)) if keep else r
+
+
+def extend_flops(Lp, C, Hq, D):
+    """Algorithmic FLOPs of extend attention: per query row i and head,
+    2*D*(Lp+i+1) for Q.K and the same for P.V."""
+    return 4 * D * Hq * (C * Lp + C * (C + 1) // 2)
+
+
+def time_extend(device, w, ws, tpeak, reps=5):
+    """Chunked-prefill attention of an 8192-token chunk over the dequantised
+    prefix of request 0 (the kv4_dequant_prefix workspace) plus the chunk's own
+    FP8 K/V, on the tensor cores: TFLOP/s of algorithmic work."""
+    import torch
+    import bit_paged_kv_kv4_gb300 as K
+    wk, wv, s8 = ws
+    Lp, C = int(wk.shape[0]), w.prefix_chunk
+    Hq, Hkv, D = w.num_q_heads, w.num_kv_heads, w.head_dim
+    chunk, _ = W.fp8_kv_codes(w.seed, C, Hkv, D, device, scales=s8.cpu().numpy())
+    ck, cv = chunk[0].contiguous(), chunk[1].contiguous()
+    q = W.extend_q(w.seed, C, Hq, D, device)
+    out = torch.empty((C, Hq, D), dtype=torch.bfloat16, device=device)
+    i32 = lambda x: torch.tensor(x, dtype=torch.int32, device=device)
+    i64 = lambda x: torch.tensor(x, dtype=torch.int64, device=device)
+    pl, cp, cl, cc = i32([Lp]), i64([0, Lp]), i32([C]), i64([0, C])
+
+    def run():
+        K.kv4_extend_attention(q, ck, cv, wk, wv, s8, pl, cp, cl, cc, C, w.sm_scale(), out)
+
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        run()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b) * 1e-3)
+    med = statistics.median(ts)
+    fl = extend_flops(Lp, C, Hq, D)
+    return {"prefix_tokens": Lp, "chunk_tokens": C, "ms": med * 1e3, "tflops": fl / med / 1e12,
+            "frac": fl / med / 1e12 / tpeak, "unit": "TFLOP/s", "bound": "tensor",
+            "peak": tpeak, "flops": fl}
 
 
 def time_calibrate(device, peak, T=65536, Hkv=4, D=256):
@@ -608,7 +667,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the 160K / 1M / INT4 lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--only", choices=("prefix", "write"),
+    ap.add_argument("--only", choices=("prefix", "write", "extend"),
                     help="time just the 160K prefix dequant or the 8K prefill write and print "
                          "its line (for profiling one kernel)")
     args = ap.parse_args()
@@ -630,6 +689,9 @@ def only_arm(args):
     peak, _ = read_peaks()
     if args.only == "prefix":
         r = time_prefix(Setup(w, device), w, peak)
+    elif args.only == "extend":
+        r, ws = time_prefix(Setup(w, device), w, peak, keep=True)
+        r = time_extend(device, w, ws, read_tensor_peak()[0], reps=args.steps)
     else:
         # the prefill write needs no filled pool: a device, a pair of global scales
         # of the workload's magnitude and the library

@@ -6,37 +6,45 @@
 // keys 0..i.  One per-tensor FP8 scale pair {s_K, s_V} serves both.
 //
 // This is the dense part of the path, so it runs on the fifth-generation
-// tensor cores: tcgen05.mma kind::f16 with the accumulators in tensor memory.
+// tensor cores: tcgen05.mma kind::f16, accumulators in tensor memory (TMEM).
 // One CTA owns 128 query rows of one query head (the MMA's M) and streams the
 // request's keys in tiles of 64:
 //
-//   warps 0-3   softmax, one thread per query row: S from TMEM, mask, online
-//               softmax in the log2 domain, P (f16) into shared memory, the
-//               rare rescale of O in TMEM, and the epilogue.
-//   warps 4-7   converters: FP8 K and V rows from global memory (one tile in
-//               registers ahead, three tiles ahead into L2) to f16 tiles in
-//               the 128-byte-swizzled layout the MMA reads.
-//   warp 8      TMEM allocation and, on one lane, the MMA issue:
-//               S_j = Q K_j^T (M128 N64, K = head_dim), then O += P_{j-1} V_{j-1}
-//               (M128 N=head_dim K64), so S_j overlaps the softmax of tile j-1.
+//   warps 0-3   softmax, one thread per query row (= TMEM lane): Q into TMEM
+//               at the start; per tile S from TMEM, mask, online softmax in
+//               the log2 domain, P (f16) back into TMEM over its own S, the
+//               rare rescale of O in TMEM; the epilogue.
+//   warps 4-11  converters: FP8 K and V rows from global memory (one tile in
+//               registers ahead, a few tiles ahead into L2) to f16 tiles in
+//               the 128-byte-swizzled layout the MMA reads, three shared-
+//               memory stages each for K and V, freed by the MMA reading them.
+//   warp 12     TMEM allocation and, on one lane, the MMA issue:
+//               S_j = Q K_j^T (M128 N64, K = head_dim; A = Q in TMEM) and
+//               O += P_j V_j (M128 N=head_dim K64; A = P in TMEM), each issued
+//               as soon as its operands are ready.
 //
-// Operand layouts (all K-major rows of 128 bytes, 8-row swizzle atoms of 1024
-// bytes, 16-byte unit index XOR row % 8):
-//   Q  f16 [D/64][128 rows][64]        A of S   (stride between 8-row groups 1024)
-//   K  f16 [D/64][64 keys][64]         B of S   (K-major)
-//   P  f16 [128 rows][64 keys]         A of O
-//   V  f16 [D/64][64 keys][64]         B of O, MN-major: N = head_dim runs along
-//                                      the 128-byte rows; 64-column blocks are
-//                                      the leading-byte-offset stride (64*128),
-//                                      8-key groups the stride-byte-offset (1024)
+// Keeping Q and P in TMEM leaves the shared-memory data path to the K / V
+// tiles (the converters' stores and the MMAs' B reads), which is what bounds
+// this kernel once the tensor pipe is fed.
 //
-// Exact FP8 -> f16 by integer ops: with the E4M3 byte b placed in a 16-bit
-// lane, (b + (b & 0x80)) << 7 is the f16 whose value is e4m3(b) * 2^-8, for
-// normal and subnormal codes alike (f16 exponent bias 15 = 7 + 8).  The 2^8
-// is folded into the softmax scale for K and the output scale for V.  Q is
-// converted bf16 -> f16 once per CTA (exact for 2^-14 <= |q| <= 65504; larger
-// magnitudes are flagged).  P is rounded to f16 once (relative 2^-11); S and
-// O accumulate in FP32.
+// Operand layouts.  Shared memory, K-major rows of 128 bytes in 8-row swizzle
+// atoms of 1024 bytes (16-byte unit index XOR row % 8):
+//   K  f16 [D/64][64 keys][64]   B of S (K-major; 8-key groups 1024 bytes apart)
+//   V  f16 [D/64][64 keys][64]   B of O, MN-major: N = head_dim runs along the
+//                                rows; 64-column blocks are the leading-byte-
+//                                offset stride (64*128), 8-key groups the
+//                                stride-byte-offset (1024)
+// TMEM (lane = query row; 32-bit columns):
+//   S_j  FP32, 64 columns at (j % 2) * 64;  P_j f16 pairs over its first 32
+//   Q    f16 pairs (elements 2c, 2c+1 in column c), D/2 columns at 128
+//   O    FP32, D columns at 256 (192 for head_dim 64)
+// S_{j+2} reuses the columns of P_j; it is issued after O += P_j V_j, and
+// tcgen05.mma operations of one thread execute in issue order.
+//
+// FP8 -> f16 with the hardware conversion (exact: every E4M3 value is an f16
+// value).  Q is converted bf16 -> f16 once per CTA (exact for
+// 2^-14 <= |q| <= 65504; larger magnitudes are flagged).  P is rounded to f16
+// once (relative 2^-11); S and O accumulate in FP32.
 //
 // The maximum used for exponentiation is raised only when a tile's maximum
 // exceeds it by more than 8 (log2 units), so P stays below 2^8 and O is
@@ -54,25 +62,26 @@ namespace {
 
 constexpr int kQT = 128;          // query rows per CTA (MMA M)
 constexpr int kKT = 64;           // keys per tile
-constexpr int kThreads = 288;     // 4 softmax warps, 4 converter warps, 1 MMA warp
+constexpr int kNST = 3;           // shared-memory stages for K and for V
+constexpr int kThreads = 416;     // 4 softmax warps, 8 converter warps, 1 MMA warp
+constexpr int kConv = 256;        // converter threads
+constexpr int kMmaWarp = 12;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct ExtGeo {
-  static constexpr int Q_BYTES = kQT * D * 2;
   static constexpr int KV_BYTES = kKT * D * 2;
-  static constexpr int P_BYTES = kQT * kKT * 2;
-  static constexpr int OFF_K = Q_BYTES;          // two buffers
-  static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;
-  static constexpr int OFF_P = OFF_V + 2 * KV_BYTES;
-  static constexpr int SMEM = OFF_P + P_BYTES + 1024;   // + alignment slack
-  static constexpr int TM_COLS = (2 * kKT + D <= 256) ? 256 : 512;
-  static constexpr int O_COL = TM_COLS / 2;      // S buffers at columns 0 and 64
-  static constexpr int NI = kKT * (D / 16) / 128;  // 16-byte units per converter thread per tensor
+  static constexpr int OFF_V = kNST * KV_BYTES;
+  static constexpr int SMEM = 2 * kNST * KV_BYTES + 1024;     // + alignment slack
+  static constexpr int S_COL = 0;                             // two S / P buffers
+  static constexpr int Q_COL = 2 * kKT;
+  static constexpr int O_COL = (D == 64) ? 192 : 256;
+  static constexpr int TM_COLS = (O_COL + D <= 256) ? 256 : 512;
+  static constexpr int NI = kKT * (D / 16) / kConv;  // 16-byte units per converter thread per tensor
 };
 
-enum Bar { KV_FULL = 0, KV_EMPTY = 2, S_FULL = 4, S_EMPTY = 6, P_FULL = 8, PV_DONE = 9, FINAL = 10,
-           NBAR = 11 };
+enum Bar { K_FULL = 0, K_EMPTY = 3, V_FULL = 6, V_EMPTY = 9, S_FULL = 12, P_FULL = 14, PV_DONE = 16,
+           Q_FULL = 17, FINAL = 18, NBAR = 19 };
 
 // ------------------------------------------------------------ tcgen05 glue
 // Shared-memory matrix descriptor: start address, leading / stride byte
@@ -90,11 +99,6 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int b_mn) {
   return (1u << 4) | (static_cast<uint32_t>(b_mn) << 16) |
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
-__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
-  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-               :: "r"(d), "l"(a), "l"(b), "r"(id), "r"(acc) : "memory");
-}
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                :: "r"(bar) : "memory");
@@ -107,6 +111,16 @@ __device__ __forceinline__ void tc_fence_after() {
 }
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Non-blocking test of phase `parity` of a barrier (for polling several).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
 }
 // 32 lanes x 16 consecutive FP32 columns: thread t of the warp gets lane
 // (32 * (warp % 4) + t) of the address's lane base.
@@ -137,18 +151,31 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
 }
 
-// Two E4M3 bytes in the low bytes of 16-bit lanes -> f16x2 of value * 2^-8.
-__device__ __forceinline__ uint32_t e4m3_lanes_to_f16x2(uint32_t y) {
-  return (y + (y & 0x00800080u)) << 7;
-}
-// 16 E4M3 codes -> 8 f16x2 words (value * 2^-8), element order kept.
+// 16 E4M3 codes -> 8 f16x2 words, element order kept, exact.
 __device__ __forceinline__ void e4m3x16_to_f16(const uint4 w, uint32_t (&o)[8]) {
-  const uint32_t x[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    o[2 * i] = e4m3_lanes_to_f16x2(prmt(x[i], 0u, 0x4140u));
-    o[2 * i + 1] = e4m3_lanes_to_f16x2(prmt(x[i], 0u, 0x4342u));
-  }
+  e4m3x4_to_f16x2x2(w.x, o[0], o[1]);
+  e4m3x4_to_f16x2x2(w.y, o[2], o[3]);
+  e4m3x4_to_f16x2x2(w.z, o[4], o[5]);
+  e4m3x4_to_f16x2x2(w.w, o[6], o[7]);
+}
+
+// 32 lanes x 32 consecutive 32-bit columns (tcgen05.st).
+__device__ __forceinline__ void tmem_st32(uint32_t ta, const uint32_t (&r)[32]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+               "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+               "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+               :: "r"(ta), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+                  "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]),
+                  "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+                  "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+                  "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+               : "memory");
+}
+// O += A B with A in TMEM (f16 pairs, lane = row) and B from shared memory.
+__device__ __forceinline__ void tc_mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t id, uint32_t acc) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+               :: "r"(d), "r"(a_tmem), "l"(b), "r"(id), "r"(acc) : "memory");
 }
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -179,95 +206,84 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const ExtendArgs a)
   const int hk = h / a.G;
 
   uint8_t* sm = align1024(ext_raw);
-  const uint32_t sQ = smem_u32(sm), sK = sQ + Gm::OFF_K, sV = sQ + Gm::OFF_V, sP = sQ + Gm::OFF_P;
+  const uint32_t sK = smem_u32(sm), sV = sK + Gm::OFF_V;
   const uint32_t bar0 = smem_u32(&bars[0]);
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
 
   if (tid == 0) {
-    mbar_init(bar(KV_FULL), 128);
-    mbar_init(bar(KV_FULL + 1), 128);
-    mbar_init(bar(KV_EMPTY), 1);
-    mbar_init(bar(KV_EMPTY + 1), 1);
-    mbar_init(bar(S_FULL), 1);
-    mbar_init(bar(S_FULL + 1), 1);
-    mbar_init(bar(S_EMPTY), 128);
-    mbar_init(bar(S_EMPTY + 1), 128);
-    mbar_init(bar(P_FULL), 128);
+    for (int i = 0; i < kNST; ++i) {
+      mbar_init(bar(K_FULL + i), kConv);
+      mbar_init(bar(V_FULL + i), kConv);
+      mbar_init(bar(K_EMPTY + i), 1);
+      mbar_init(bar(V_EMPTY + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(S_FULL + i), 1);
+      mbar_init(bar(P_FULL + i), 128);
+    }
     mbar_init(bar(PV_DONE), 1);
+    mbar_init(bar(Q_FULL), 128);
     mbar_init(bar(FINAL), 1);
     fence_mbar_init();
   }
-  if (warp == 8) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                  :: "r"(smem_u32(&tmem_slot)), "r"(Gm::TM_COLS) : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-
-  // Q rows of this CTA: bf16 -> f16 into the swizzled A layout (rows past
-  // the chunk are zero).  Warps 0-7, one 16-byte unit per thread and step.
-  bool bad = false;
-  if (tid < 256) {
-    constexpr int U = D / 8;                          // 16-byte units per row
-    for (int it = tid; it < kQT * U; it += 256) {
-      const int r = it / U, u = it % U;
-      uint4 w = make_uint4(0u, 0u, 0u, 0u);
-      if (r < rows) {
-        const __nv_bfloat16* src = a.q + ((c0 + qt * kQT + r) * a.Hq + h) * static_cast<int64_t>(D) + u * 8;
-        w = __ldg(reinterpret_cast<const uint4*>(src));
-      }
-      uint32_t x[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float lo = __uint_as_float(x[i] << 16), hi = __uint_as_float(x[i] & 0xFFFF0000u);
-        bad |= !(fabsf(lo) <= 65504.f) || !(fabsf(hi) <= 65504.f);
-        x[i] = pack_f16x2(lo, hi);
-      }
-      const uint32_t addr = sQ + (u >> 3) * (kQT * 128) + r * 128 + (((u & 7) ^ (r & 7)) << 4);
-      sts128(addr, x[0], x[1], x[2], x[3]);
-    }
-    fence_async_smem();
-  }
   tc_fence_before();
-  const int any_bad = __syncthreads_or(bad);
+  __syncthreads();
   tc_fence_after();
-  if (any_bad && tid == 0) set_error(a.err, KV4_EINVAL);
   const uint32_t tmem = tmem_slot;
-  const uint32_t tO = tmem + Gm::O_COL;
+  const uint32_t tO = tmem + Gm::O_COL, tQ = tmem + Gm::Q_COL;
 
-  if (warp == 8) {
+  if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issue
+    // One lane polls the operand barriers and issues whichever MMA is ready:
+    // O += P_n V_n as soon as P_n and V_n are in; S_m = Q K_m^T as soon as
+    // K_m is in and O += P_{m-2} V_{m-2} (the last reader of S buffer m % 2)
+    // has been issued.
     if (lane == 0) {
-      bool ok = true;
+      bool ok = mbar_wait_bounded(bar(Q_FULL), 0);
+      tc_fence_after();
       constexpr uint32_t idS = idesc_f16(kQT, kKT, 0), idO = idesc_f16(kQT, D, 1);
-      const uint64_t dQ = sw128_desc(sQ, 16, 1024);
-      for (int j = 0; j <= nT && ok; ++j) {
-        if (j < nT) {
-          const int bb = j & 1;
-          ok = mbar_wait_bounded(bar(KV_FULL + bb), (j >> 1) & 1) &&
-               (j < 2 || mbar_wait_bounded(bar(S_EMPTY + bb), ((j - 2) >> 1) & 1));
-          if (!ok) break;
+      int nS = 0, nP = 0, kst = 0, kph = 0, vst = 0, vph = 0;
+      long long idle_since = clock64();
+      while (ok && nP < nT) {
+        bool progress = false;
+        if (nP < nS && mbar_test(bar(P_FULL + (nP & 1)), (nP >> 1) & 1) &&
+            mbar_test(bar(V_FULL + vst), vph)) {
           tc_fence_after();
-          const uint64_t dK = sw128_desc(sK + bb * Gm::KV_BYTES, 16, 1024);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t qo = (kk >> 2) * (kQT * 128) + (kk & 3) * 32;
-            const uint32_t ko = (kk >> 2) * (kKT * 128) + (kk & 3) * 32;
-            tc_mma(tmem + bb * kKT, dQ + (qo >> 4), dK + (ko >> 4), idS, kk > 0);
-          }
-          tc_commit(bar(S_FULL + bb));
-        }
-        if (j >= 1) {
-          const int jp = j - 1, pb = jp & 1;
-          ok = mbar_wait_bounded(bar(P_FULL), jp & 1);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t dP = sw128_desc(sP, 16, 1024);
-          const uint64_t dV = sw128_desc(sV + pb * Gm::KV_BYTES, kKT * 128, 1024);
+          const uint64_t dV = sw128_desc(sV + vst * Gm::KV_BYTES, kKT * 128, 1024);
+          const uint32_t tP = tmem + Gm::S_COL + (nP & 1) * kKT;
 #pragma unroll
           for (int kk = 0; kk < kKT / 16; ++kk)
-            tc_mma(tO, dP + ((kk * 32) >> 4), dV + ((kk * 2048) >> 4), idO, (jp > 0 || kk > 0));
+            tc_mma_ts(tO, tP + kk * 8, dV + ((kk * 2048) >> 4), idO, (nP > 0 || kk > 0));
           tc_commit(bar(PV_DONE));
-          tc_commit(bar(KV_EMPTY + pb));
+          tc_commit(bar(V_EMPTY + vst));
+          if (++vst == kNST) { vst = 0; vph ^= 1; }
+          ++nP;
+          progress = true;
+        }
+        if (nS < nT && (nS < 2 || nP >= nS - 1) && mbar_test(bar(K_FULL + kst), kph)) {
+          tc_fence_after();
+          const uint64_t dK = sw128_desc(sK + kst * Gm::KV_BYTES, 16, 1024);
+          const uint32_t tS = tmem + Gm::S_COL + (nS & 1) * kKT;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ko = (kk >> 2) * (kKT * 128) + (kk & 3) * 32;
+            tc_mma_ts(tS, tQ + kk * 8, dK + (ko >> 4), idS, kk > 0);
+          }
+          tc_commit(bar(S_FULL + (nS & 1)));
+          tc_commit(bar(K_EMPTY + kst));
+          if (++kst == kNST) { kst = 0; kph ^= 1; }
+          ++nS;
+          progress = true;
+        }
+        if (progress) {
+          idle_since = clock64();
+        } else if (clock64() - idle_since > kWaitCycles) {
+          ok = false;
         }
       }
       if (!ok) set_error(a.err, KV4_ETIMEOUT);
@@ -287,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const ExtendArgs a)
     auto load = [&](int j, uint4 (&kr)[NI], uint4 (&vr)[NI]) {
 #pragma unroll
       for (int m = 0; m < NI; ++m) {
-        const int it = m * 128 + t, r = it / U16, u = it % U16;
+        const int it = m * kConv + t, r = it / U16, u = it % U16;
         const int key = j * kKT + r;
         kr[m] = make_uint4(0u, 0u, 0u, 0u);
         vr[m] = kr[m];
@@ -300,17 +316,24 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const ExtendArgs a)
         }
       }
     };
+    // One bulk L2 prefetch per tensor and tile over the tile's contiguous
+    // rows (all kv heads: the CTAs of the other heads read them too).
     auto prefetch = [&](int j) {
-      if (j >= nT) return;
-      const int key = j * kKT + (t & 63);
-      const bool isv = t >= 64;
-      if (key < Lp) prefetch_l2((isv ? pv : pk) + key * rs, D);
-      else if (key < kend) prefetch_l2((isv ? cv : ck) + (key - Lp) * rs, D);
+      if (j >= nT || t >= 4) return;
+      const int k0 = j * kKT, k1 = min(k0 + kKT, kend);
+      const bool isv = t & 1;
+      if (t < 2) {
+        const int e = min(k1, Lp);
+        if (k0 < e) prefetch_l2((isv ? a.pv : a.pk) + (p0 + k0) * rs, static_cast<uint32_t>((e - k0) * rs));
+      } else {
+        const int s0 = max(k0, Lp);
+        if (s0 < k1) prefetch_l2((isv ? a.cv : a.ck) + (c0 + s0 - Lp) * rs, static_cast<uint32_t>((k1 - s0) * rs));
+      }
     };
     auto store = [&](uint32_t base, const uint4 (&w)[NI]) {
 #pragma unroll
       for (int m = 0; m < NI; ++m) {
-        const int it = m * 128 + t, r = it / U16, u = it % U16;
+        const int it = m * kConv + t, r = it / U16, u = it % U16;
         uint32_t o[8];
         e4m3x16_to_f16(w[m], o);
         const int blk = u >> 2, c0u = (u & 3) * 2;
@@ -327,36 +350,73 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const ExtendArgs a)
         }
       }
     };
-    uint4 kc[NI], vc[NI];
-    prefetch(1);
-    prefetch(2);
-    load(0, kc, vc);
-    bool ok = true;
-    for (int j = 0; j < nT; ++j) {
-      const int bb = j & 1;
-      uint4 kn[NI], vn[NI];
-      prefetch(j + 3);
-      if (j + 1 < nT) load(j + 1, kn, vn);
-      if (j >= 2 && !mbar_wait_bounded(bar(KV_EMPTY + bb), ((j - 2) >> 1) & 1)) { ok = false; break; }
-      store(sK + bb * Gm::KV_BYTES, kc);
-      store(sV + bb * Gm::KV_BYTES, vc);
+    int st = 0, ph = 0;
+    // Tile j's registers are converted while tile j+1's loads are in flight
+    // (two register sets, the loop unrolled by two so nothing is copied).
+    auto convert = [&](int j, const uint4 (&kr)[NI], const uint4 (&vr)[NI]) -> bool {
+      if (j >= kNST && !mbar_wait_bounded(bar(K_EMPTY + st), ph ^ 1)) return false;
+      store(sK + st * Gm::KV_BYTES, kr);
       fence_async_smem();
-      mbar_arrive(bar(KV_FULL + bb));
-#pragma unroll
-      for (int m = 0; m < NI; ++m) { kc[m] = kn[m]; vc[m] = vn[m]; }
+      mbar_arrive(bar(K_FULL + st));
+      if (j >= kNST && !mbar_wait_bounded(bar(V_EMPTY + st), ph ^ 1)) return false;
+      store(sV + st * Gm::KV_BYTES, vr);
+      fence_async_smem();
+      mbar_arrive(bar(V_FULL + st));
+      if (++st == kNST) { st = 0; ph ^= 1; }
+      return true;
+    };
+    uint4 ka[NI], va[NI], kb[NI], vb[NI];
+    for (int j = 1; j <= 4; ++j) prefetch(j);
+    load(0, ka, va);
+    bool ok = true;
+    for (int j = 0; j < nT; j += 2) {
+      if (j + 1 < nT) load(j + 1, kb, vb);
+      prefetch(j + 5);
+      if (!(ok = convert(j, ka, va)) || j + 1 >= nT) break;
+      if (j + 2 < nT) load(j + 2, ka, va);
+      prefetch(j + 6);
+      if (!(ok = convert(j + 1, kb, vb))) break;
     }
     if (!ok && lane == 0) set_error(a.err, KV4_ETIMEOUT);
   } else {
     // ------------------------------------------------------------ softmax
     const int r = tid;                                // TMEM lane = query row
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // Q row r: bf16 -> f16 pairs into TMEM (rows past the chunk are zero).
+    {
+      bool bad = false;
+      const bool valid = r < rows;
+      const uint4* src = reinterpret_cast<const uint4*>(
+          a.q + ((c0 + qt * kQT + (valid ? r : 0)) * a.Hq + h) * static_cast<int64_t>(D));
+#pragma unroll 1
+      for (int c = 0; c < D / 64; ++c) {              // 32 columns = 64 elements per store
+        uint32_t v[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 w = valid ? __ldg(src + c * 8 + i) : make_uint4(0u, 0u, 0u, 0u);
+          const uint32_t x[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float lo = __uint_as_float(x[k] << 16), hi = __uint_as_float(x[k] & 0xFFFF0000u);
+            bad |= !(fabsf(lo) <= 65504.f) || !(fabsf(hi) <= 65504.f);
+            v[4 * i + k] = pack_f16x2(lo, hi);
+          }
+        }
+        tmem_st32(tQ + lane_base + c * 32, v);
+      }
+      tmem_wait_st();
+      if (bad) set_error(a.err, KV4_EINVAL);
+      tc_fence_before();
+      mbar_arrive(bar(Q_FULL));
+    }
     const float sk = a.fp8_scale[0], sv = a.fp8_scale[1];
-    const float c2 = a.sm_scale * sk * 256.f * kLog2e;   // S from the 2^-8 operands -> log2 units
+    const float c2 = a.sm_scale * sk * kLog2e;           // S -> log2 units
     const int lim = min(Lp + qt * kQT + r, kend - 1);     // last key this row sees
     float m_use = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nT; ++j) {
       const int bb = j & 1;
+      const uint32_t tS = tmem + Gm::S_COL + bb * kKT + lane_base;
       if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(S_FULL + bb), (j >> 1) & 1))) {
         ok = false;
         break;
@@ -365,10 +425,8 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const ExtendArgs a)
       uint32_t sr[kKT];
 #pragma unroll
       for (int c = 0; c < kKT / 16; ++c)
-        tmem_ld16(tmem + lane_base + bb * kKT + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&sr[c * 16]));
+        tmem_ld16(tS + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&sr[c * 16]));
       tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(bar(S_EMPTY + bb));
       float s[kKT];
       const int kb = j * kKT;
 #pragma unroll
@@ -398,6 +456,8 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const ExtendArgs a)
       }
       l = l * alpha + rs;
       if (j >= 1) {
+        // O holds tiles < j once O += P_{j-1} V_{j-1} is done (waited every
+        // tile to keep the barrier's phases in step; usually long complete)
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(PV_DONE), (j - 1) & 1))) {
           ok = false;
           break;
@@ -415,15 +475,12 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const ExtendArgs a)
             for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
             tmem_st16(tO + lane_base + c * 16, o);
           }
-          tmem_wait_st();
         }
       }
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        sts128(sP + r * 128 + ((c ^ (r & 7)) << 4), ph[4 * c], ph[4 * c + 1], ph[4 * c + 2], ph[4 * c + 3]);
-      fence_async_smem();
+      tmem_st32(tS, ph);                              // P_j over S_j
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(P_FULL));
+      mbar_arrive(bar(P_FULL + bb));
     }
     if (ok && !__all_sync(0xffffffffu, mbar_wait_bounded(bar(PV_DONE), (nT - 1) & 1))) ok = false;
     if (!ok) {
@@ -431,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const ExtendArgs a)
     } else {
       tc_fence_after();
       const bool valid = r < rows;
-      const float inv = sv * 256.f / l;
+      const float inv = sv / l;
       const int64_t orow = ((c0 + qt * kQT + r) * a.Hq + h) * static_cast<int64_t>(D);
 #pragma unroll 1
       for (int c = 0; c < D / 16; ++c) {
@@ -465,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const ExtendArgs a)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 8)
+  if (warp == kMmaWarp)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
                  :: "r"(tmem), "r"(Gm::TM_COLS) : "memory");
 }
