@@ -14,10 +14,12 @@
 //               at the start; per tile S from TMEM, mask, online softmax in
 //               the log2 domain, P (f16) back into TMEM over its own S, the
 //               rare rescale of O in TMEM; the epilogue.
-//   warps 4-11  converters: FP8 K and V rows from global memory (one tile in
-//               registers ahead, a few tiles ahead into L2) to f16 tiles in
-//               the 128-byte-swizzled layout the MMA reads, three shared-
-//               memory stages each for K and V, freed by the MMA reading them.
+//   warps 4-11  converters: FP8 K and V rows from global memory (two
+//               register sets, one tile of loads in flight) to f16 tiles in the 128-byte-swizzled layout the MMA reads,
+//               three shared-memory stages each for K and V, freed by the
+//               MMA reading them.
+//   warp 13     one lane keeps an L2 bulk prefetch of the K / V rows a few
+//               tiles ahead of the converters.
 //   warp 12     TMEM allocation and, on one lane, the MMA issue:
 //               S_j = Q K_j^T (M128 N64, K = head_dim; A = Q in TMEM) and
 //               O += P_j V_j (M128 N=head_dim K64; A = P in TMEM), each issued
@@ -63,9 +65,11 @@ namespace {
 constexpr int kQT = 128;          // query rows per CTA (MMA M)
 constexpr int kKT = 64;           // keys per tile
 constexpr int kNST = 3;           // shared-memory stages for K and for V
-constexpr int kThreads = 416;     // 4 softmax warps, 8 converter warps, 1 MMA warp
+constexpr int kThreads = 448;     // 4 softmax, 8 converter, 1 MMA and 1 prefetch warp
 constexpr int kConv = 256;        // converter threads
 constexpr int kMmaWarp = 12;
+constexpr int kPrefetchWarp = 13;
+constexpr int kPrefetchAhead = 6;  // tiles the L2 prefetch runs ahead of the converters
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
@@ -188,6 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const ExtendArgs a)
   extern __shared__ uint8_t ext_raw[];
   __shared__ __align__(8) uint64_t bars[NBAR];
   __shared__ uint32_t tmem_slot;
+  __shared__ volatile int conv_tile;                 // tiles the converters have stored
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.x, qt = blockIdx.y, b = blockIdx.z;
@@ -224,6 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const ExtendArgs a)
     mbar_init(bar(PV_DONE), 1);
     mbar_init(bar(Q_FULL), 128);
     mbar_init(bar(FINAL), 1);
+    conv_tile = 0;
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -240,9 +246,9 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const ExtendArgs a)
   if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issue
     // One lane polls the operand barriers and issues whichever MMA is ready:
-    // O += P_n V_n as soon as P_n and V_n are in; S_m = Q K_m^T as soon as
-    // K_m is in and O += P_{m-2} V_{m-2} (the last reader of S buffer m % 2)
-    // has been issued.
+    // O += P_n V_n as soon as P_n and V_n are in; S_m = Q K_m^T (a whole
+    // tile: issuing it in parts starves the tensor pipe) once K_m is in and
+    // O += P_{m-2} V_{m-2}, the last reader of S buffer m % 2, has been issued.
     if (lane == 0) {
       bool ok = mbar_wait_bounded(bar(Q_FULL), 0);
       tc_fence_after();
@@ -291,6 +297,38 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const ExtendArgs a)
       tc_commit(bar(FINAL));
       if (!mbar_wait_bounded(bar(FINAL), 0)) set_error(a.err, KV4_ETIMEOUT);
     }
+  } else if (warp == kPrefetchWarp) {
+    // ------------------------------------------------------------ L2 prefetch
+    // One bulk prefetch per tensor and tile over the tile's contiguous rows
+    // (all kv heads: the CTAs of the other heads read them too), kept
+    // kPrefetchAhead tiles ahead of the converters.
+    if (lane == 0) {
+      const int64_t rs = static_cast<int64_t>(a.Hkv) * D;
+      auto prefetch = [&](int j) {
+        const int k0 = j * kKT, k1 = min(k0 + kKT, kend);
+        const int e = min(k1, Lp), s0 = max(k0, Lp);
+        if (k0 < e) {
+          prefetch_l2(a.pk + (p0 + k0) * rs, static_cast<uint32_t>((e - k0) * rs));
+          prefetch_l2(a.pv + (p0 + k0) * rs, static_cast<uint32_t>((e - k0) * rs));
+        }
+        if (s0 < k1) {
+          prefetch_l2(a.ck + (c0 + s0 - Lp) * rs, static_cast<uint32_t>((k1 - s0) * rs));
+          prefetch_l2(a.cv + (c0 + s0 - Lp) * rs, static_cast<uint32_t>((k1 - s0) * rs));
+        }
+      };
+      int next = 1;
+      long long idle_since = clock64();
+      while (next < nT) {
+        const int lim = min(nT, conv_tile + kPrefetchAhead);
+        if (next < lim) {
+          while (next < lim) prefetch(next++);
+          idle_since = clock64();
+        } else {
+          __nanosleep(200);
+          if (clock64() - idle_since > kWaitCycles) break;   // converters stopped: nothing to do
+        }
+      }
+    }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ converters
     constexpr int NI = Gm::NI, U16 = D / 16;
@@ -300,34 +338,15 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const ExtendArgs a)
     const uint8_t* pv = a.pv + (p0 * a.Hkv + hk) * static_cast<int64_t>(D);
     const uint8_t* ck = a.ck + (c0 * a.Hkv + hk) * static_cast<int64_t>(D);
     const uint8_t* cv = a.cv + (c0 * a.Hkv + hk) * static_cast<int64_t>(D);
-    auto load = [&](int j, uint4 (&kr)[NI], uint4 (&vr)[NI]) {
+    // Loads of one tensor's part of tile j into registers (zero past kend).
+    auto load = [&](int j, const uint8_t* pre, const uint8_t* chk, uint4 (&w)[NI]) {
 #pragma unroll
       for (int m = 0; m < NI; ++m) {
         const int it = m * kConv + t, r = it / U16, u = it % U16;
         const int key = j * kKT + r;
-        kr[m] = make_uint4(0u, 0u, 0u, 0u);
-        vr[m] = kr[m];
-        if (key < Lp) {
-          kr[m] = __ldg(reinterpret_cast<const uint4*>(pk + key * rs) + u);
-          vr[m] = __ldg(reinterpret_cast<const uint4*>(pv + key * rs) + u);
-        } else if (key < kend) {
-          kr[m] = __ldg(reinterpret_cast<const uint4*>(ck + (key - Lp) * rs) + u);
-          vr[m] = __ldg(reinterpret_cast<const uint4*>(cv + (key - Lp) * rs) + u);
-        }
-      }
-    };
-    // One bulk L2 prefetch per tensor and tile over the tile's contiguous
-    // rows (all kv heads: the CTAs of the other heads read them too).
-    auto prefetch = [&](int j) {
-      if (j >= nT || t >= 4) return;
-      const int k0 = j * kKT, k1 = min(k0 + kKT, kend);
-      const bool isv = t & 1;
-      if (t < 2) {
-        const int e = min(k1, Lp);
-        if (k0 < e) prefetch_l2((isv ? a.pv : a.pk) + (p0 + k0) * rs, static_cast<uint32_t>((e - k0) * rs));
-      } else {
-        const int s0 = max(k0, Lp);
-        if (s0 < k1) prefetch_l2((isv ? a.cv : a.ck) + (c0 + s0 - Lp) * rs, static_cast<uint32_t>((k1 - s0) * rs));
+        w[m] = make_uint4(0u, 0u, 0u, 0u);
+        if (key < Lp) w[m] = __ldg(reinterpret_cast<const uint4*>(pre + key * rs) + u);
+        else if (key < kend) w[m] = __ldg(reinterpret_cast<const uint4*>(chk + (key - Lp) * rs) + u);
       }
     };
     auto store = [&](uint32_t base, const uint4 (&w)[NI]) {
@@ -350,32 +369,43 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const ExtendArgs a)
         }
       }
     };
-    int st = 0, ph = 0;
-    // Tile j's registers are converted while tile j+1's loads are in flight
-    // (two register sets, the loop unrolled by two so nothing is copied).
-    auto convert = [&](int j, const uint4 (&kr)[NI], const uint4 (&vr)[NI]) -> bool {
-      if (j >= kNST && !mbar_wait_bounded(bar(K_EMPTY + st), ph ^ 1)) return false;
-      store(sK + st * Gm::KV_BYTES, kr);
+    // Stores of tile j's K (then V) into its stage, after the MMA that read
+    // the stage's previous tile has completed.
+    int kst = 0, kph = 0, vst = 0, vph = 0;
+    auto put_k = [&](int j, const uint4 (&w)[NI]) -> bool {
+      if (j >= kNST && !mbar_wait_bounded(bar(K_EMPTY + kst), kph ^ 1)) return false;
+      store(sK + kst * Gm::KV_BYTES, w);
       fence_async_smem();
-      mbar_arrive(bar(K_FULL + st));
-      if (j >= kNST && !mbar_wait_bounded(bar(V_EMPTY + st), ph ^ 1)) return false;
-      store(sV + st * Gm::KV_BYTES, vr);
-      fence_async_smem();
-      mbar_arrive(bar(V_FULL + st));
-      if (++st == kNST) { st = 0; ph ^= 1; }
+      mbar_arrive(bar(K_FULL + kst));
+      if (++kst == kNST) { kst = 0; kph ^= 1; }
       return true;
     };
-    uint4 ka[NI], va[NI], kb[NI], vb[NI];
-    for (int j = 1; j <= 4; ++j) prefetch(j);
-    load(0, ka, va);
+    auto put_v = [&](int j, const uint4 (&w)[NI]) -> bool {
+      if (j >= kNST && !mbar_wait_bounded(bar(V_EMPTY + vst), vph ^ 1)) return false;
+      store(sV + vst * Gm::KV_BYTES, w);
+      fence_async_smem();
+      mbar_arrive(bar(V_FULL + vst));
+      if (++vst == kNST) { vst = 0; vph ^= 1; }
+      if (t == 0) conv_tile = j + 1;
+      return true;
+    };
+    // Two register sets, the loop unrolled by two: tile j+1's loads are in
+    // flight while tile j is converted and stored.
+    uint4 ak[NI], av[NI], bk[NI], bv[NI];
+    load(0, pk, ck, ak);
+    load(0, pv, cv, av);
     bool ok = true;
     for (int j = 0; j < nT; j += 2) {
-      if (j + 1 < nT) load(j + 1, kb, vb);
-      prefetch(j + 5);
-      if (!(ok = convert(j, ka, va)) || j + 1 >= nT) break;
-      if (j + 2 < nT) load(j + 2, ka, va);
-      prefetch(j + 6);
-      if (!(ok = convert(j + 1, kb, vb))) break;
+      if (j + 1 < nT) {
+        load(j + 1, pk, ck, bk);
+        load(j + 1, pv, cv, bv);
+      }
+      if (!(ok = put_k(j, ak) && put_v(j, av)) || j + 1 >= nT) break;
+      if (j + 2 < nT) {
+        load(j + 2, pk, ck, ak);
+        load(j + 2, pv, cv, av);
+      }
+      if (!(ok = put_k(j + 1, bk) && put_v(j + 1, bv))) break;
     }
     if (!ok && lane == 0) set_error(a.err, KV4_ETIMEOUT);
   } else {
@@ -435,9 +465,13 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const ExtendArgs a)
 #pragma unroll
         for (int c = 0; c < kKT; ++c) s[c] = (kb + c <= lim) ? s[c] : -INFINITY;
       }
-      float mx = s[0];
+      float mx4[4] = {s[0], s[1], s[2], s[3]};        // four independent chains
 #pragma unroll
-      for (int c = 1; c < kKT; ++c) mx = fmaxf(mx, s[c]);
+      for (int c = 4; c < kKT; c += 4) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mx4[i] = fmaxf(mx4[i], s[c + i]);
+      }
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       const float mnew = mx * c2;
       const bool resc = mnew > m_use + 8.f;
       float alpha = 1.f;
@@ -445,15 +479,16 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const ExtendArgs a)
         alpha = fast_exp2(m_use - mnew);
         m_use = mnew;
       }
-      float rs = 0.f;
+      float rs4[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t ph[kKT / 2];
 #pragma unroll
       for (int c = 0; c < kKT; c += 2) {
         const float e0 = fast_exp2(fmaf(s[c], c2, -m_use));
         const float e1 = fast_exp2(fmaf(s[c + 1], c2, -m_use));
-        rs += e0 + e1;
+        rs4[(c >> 1) & 3] += e0 + e1;
         ph[c / 2] = pack_f16x2(e0, e1);
       }
+      const float rs = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
       l = l * alpha + rs;
       if (j >= 1) {
         // O holds tiles < j once O += P_{j-1} V_{j-1} is done (waited every
