@@ -21,6 +21,7 @@ decodes its own batch; only the timing is reduced (max over ranks).
 """
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -82,10 +83,16 @@ def read_tensor_peak():
 
 
 def decode_source_hash():
+    """Hash of the decode kernel's code with comments and blank space removed,
+    so a recorded ncu traffic figure survives comment edits but not code
+    changes."""
     h = hashlib.sha256()
     for f in ("kv4_decode.cu", "kv4_device.cuh"):
-        with open(os.path.join(ROOT, "bit_paged_kv_kv4_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "bit_paged_kv_kv4_gb300", "csrc", f)) as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        h.update("".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,7 +1,7 @@
 // Serving-time calibration of the NVFP4 global scales ("SGLang's 4-bit KV
 // cache", Figure 2: per-layer FP32 global scales; the caveat above "The
-// agentic result": the measured runs dropped them and calibration is listed
-// as ongoing work).  g = float32(amax) / 2688 (E2M1 max x E4M3 max), one
+// agentic result": the measured runs went without them, and calibrating them
+// is named as unfinished work).  g = float32(amax) / 2688 (E2M1 max x E4M3 max), one
 // FP32 rounding, and g = 1 when amax is not positive.
 //
 // amax_kernel: every thread takes 8 bf16 per 16-byte load, four loads in

@@ -1,10 +1,10 @@
 // Paged decode attention over the 4-bit pool, split over the sequence, and
 // the log-sum-exp combine of the pieces.
 //
-// "SGLang's 4-bit KV cache", Figure 2: decode "reads NVFP4 directly for native
-// FP4 decode with scales"; the page's kernel section describes loading packed
-// tiles and E4M3 block scales, unpacking E2M1 with a hardware conversion and
-// applying the scales.  INT4 per-token-head follows "KV cache in 4 bits"
+// "SGLang's 4-bit KV cache", Figure 2: decode consumes the 4-bit pool as it
+// is stored, block scales included; per the page's kernel section, its kernel
+// brings in the packed code tiles and their E4M3 scales, unpacks E2M1 with a
+// hardware conversion instruction and multiplies by the scales.  INT4 per-token-head follows "KV cache in 4 bits"
 // (section "What we changed"): one scale per token and head for K and for V.
 //
 // Work decomposition (GB300: 152 SMs, two CTAs of 4 warps resident on each):

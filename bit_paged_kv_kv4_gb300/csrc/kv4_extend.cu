@@ -1,7 +1,7 @@
 // Chunked-prefill / extend attention over the FP8 workspace plus the FP8
 // current chunk ("SGLang's 4-bit KV cache", Figure 2, right-hand column: the
-// cached prefix is dequantised into a reused FP8 workspace and the chunk's
-// queries attend over prefix plus current chunk).  Chunk query i of a
+// cached prefix has been turned into FP8 in a reused buffer, and the chunk's
+// queries attend over that prefix and the chunk itself).  Chunk query i of a
 // request sits at position Lp + i and sees all Lp prefix keys and the chunk
 // keys 0..i.  One per-tensor FP8 scale pair {s_K, s_V} serves both.
 //

@@ -1,7 +1,7 @@
-// Dequantise a cached 4-bit prefix into FP8 E4M3 workspaces: the chunked
-// prefill / extend path of "SGLang's 4-bit KV cache", Figure 2, which "reads
-// NVFP4 and dequantizes the cached prefix into a reused FP8 workspace" before
-// attending over prefix plus the current chunk.
+// Dequantise a cached 4-bit prefix into FP8 E4M3 workspaces: the first step
+// of the chunked prefill / extend path of "SGLang's 4-bit KV cache", Figure 2,
+// which turns the 4-bit prefix into FP8 in a buffer that is reused, then
+// attends over prefix plus the current chunk.
 //
 // One thread turns 16 consecutive head-dim elements (one NVFP4 block) of one
 // (token, head, K|V) row into 16 E4M3 bytes: x_hat = (e2m1 * e4m3) * g in

@@ -15,7 +15,7 @@
  *                         path that reads the 4-bit cache directly), split
  *                         over the sequence with a log-sum-exp combine;
  *   kv4_dequant_prefix    the chunked-prefill path, first step: dequantise
- *                         the cached prefix into a reused FP8 workspace;
+ *                         the 4-bit prefix into an FP8 buffer that is reused;
  *   kv4_extend_attention  the chunked-prefill path, second step: the chunk's
  *                         queries attend over that FP8 prefix plus the FP8
  *                         current chunk, on the tensor cores;
@@ -28,8 +28,8 @@
  *                 values, 0.5625 of FP8 (same page, "The 56% survives its own
  *                 scale").
  *   KV4_INT4_PTH  INT4 per token and head: 4-bit codes plus per-token-head
- *                 scales, 264 bytes per head and token at head_dim 256
- *                 ("KV cache in 4 bits", section "What we changed").
+ *                 scales; at head_dim 256 each head of each token takes 264
+ *                 bytes ("KV cache in 4 bits", section "What we changed").
  *   KV4_FP8       FP8 E4M3 with one FP32 scale per layer for K and one for V
  *                 (per tensor), 16 bytes per 16 values: the format the 4-bit
  *                 cache is compared against ("The 56% survives its own
@@ -143,8 +143,8 @@ int64_t kv4_decode_workspace_bytes(int32_t batch, int32_t num_q_heads,
 
 /*
  * kv4_decode_attention -- one decode step of paged attention over the 4-bit
- * pool (Figure 2, "Decode ... reads NVFP4 directly for native FP4 decode
- * with scales").  For request b and query head j (kv head
+ * pool (Figure 2: decode consumes the stored 4-bit codes and block scales
+ * directly).  For request b and query head j (kv head
  * h = j / (Hq/Hkv): GQA groups are contiguous), over tokens t < seq_lens[b]
  * stored at slot block_table[b*max_pages + t/P]*P + t%P:
  *     out[b][j] = sum_t softmax_t(sm_scale * <q[b][j], K_hat_t>) V_hat_t
@@ -179,8 +179,8 @@ kv4_status kv4_decode_attention(const void* q, const kv4_pool* pool,
                                 int32_t out_is_fp32, void* stream);
 
 /*
- * kv4_dequant_prefix -- the chunked-prefill path of Figure 2: "reads NVFP4
- * and dequantizes the cached prefix into a reused FP8 workspace".  For each
+ * kv4_dequant_prefix -- the chunked-prefill path of Figure 2: the 4-bit
+ * cached prefix is turned into FP8, in a buffer that is reused.  For each
  * request b, prefix token t < prefix_lens[b] and kv head h:
  *     ws[cu_prefix[b] + t][h][d] = E4M3(x_hat / s)
  * x_hat the FP32 decoded value ((e2m1*e4m3)*g for NVFP4, code*s for INT4),
@@ -243,8 +243,8 @@ kv4_status kv4_extend_attention(const void* q, const void* chunk_k, const void* 
 /*
  * kv4_calibrate_global_scale -- the NVFP4 global scales of one layer from its
  * K and V at serving time ("SGLang's 4-bit KV cache": Figure 2 keeps
- * per-layer FP32 global scales; the measured runs dropped them, and the post
- * lists calibration as ongoing work).  For each of K and V:
+ * per-layer FP32 global scales; the measured runs went without them, and
+ * calibrating them is named as unfinished work).  For each of K and V:
  *     g = float32(amax) / 2688   (E2M1 max 6 x E4M3 max 448, FP32 rounding)
  * with amax the largest |x| over the tensor, and g = 1 when amax is not
  * positive.  The layer maximum then encodes to E4M3 scale 448 and code 6.

@@ -13,10 +13,11 @@ The oracle restates, step by step and in plain numpy, what the pages define:
   FP32 global scale) and the INT4 per-token-head encoding ("KV cache in 4
   bits", section "What we changed").
 * ``pool``      -- the paged pool: request -> token -> slot -> page bytes
-  (Figure 2 caption: "maps request to token to slot").
+  (Figure 2 caption: the memory system that assigns tokens to slots).
 * ``attention`` -- exact FP64 softmax attention over the dequantised cache,
-  the split-KV log-sum-exp combine, and the dequantisation of a cached prefix
-  into an FP8 E4M3 workspace (Figure 2: "Chunked Prefill and Extend").
+  the split-KV log-sum-exp combine, the dequantisation of a cached prefix
+  into an FP8 E4M3 workspace, and the chunk's attention over that prefix
+  plus itself (Figure 2, the chunked prefill and extend column).
 
 Every function is pinned by ``tests/test_oracle_*.py`` against something
 other than itself (library casts, closed forms, brute force, the pages'

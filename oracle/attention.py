@@ -3,10 +3,10 @@ and the dequantisation of a cached prefix into an FP8 workspace.
 
 Test infrastructure only (see ``oracle/__init__.py``).
 
-Figure 2 of "SGLang's 4-bit KV cache" has three paths over one pool: only
-decode reads NVFP4 and dequantises inside the kernel; chunked prefill /
-extend dequantises the cached prefix into a reused FP8 workspace and attends
-over prefix plus chunk.  The decode reference here is the plain definition:
+Figure 2 of "SGLang's 4-bit KV cache" has three paths over one pool: decode
+alone reads the 4-bit codes, dequantising them in the kernel; chunked
+prefill / extend first turns the cached prefix into FP8, in a buffer that is
+reused, then attends over that prefix plus the chunk.  The decode reference here is the plain definition:
 for request b and query head j (GQA groups are contiguous, kv head
 h = j // (Hq / Hkv)), over the request's tokens t < seq_len[b] at slot
 block_table[b][t // P] * P + t % P,

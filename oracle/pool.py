@@ -3,8 +3,8 @@
 Test infrastructure only (see ``oracle/__init__.py``).
 
 Figure 2 of "SGLang's 4-bit KV cache" shows one GPU KV pool holding packed
-E2M1 K and V, the E4M3 block scales and per-layer FP32 global scales, with a
-memory system that "maps request to token to slot".  "KV cache in 4 bits"
+E2M1 K and V, the E4M3 block scales and per-layer FP32 global scales, and a
+memory system that takes each request's tokens to pool slots.  "KV cache in 4 bits"
 (section "What we changed") sizes an INT4 page as 211,200 bytes at 800 tokens
 and 422,400 bytes at 1600 tokens, i.e. page_size * 264 bytes per KV head.
 

@@ -31,8 +31,8 @@ fits the byte count but that nothing on the pages confirms: parity unpinned
 beyond the byte count.
 
 FP8 E4M3 per tensor, the format the 4-bit cache is compared against ("SGLang's
-4-bit KV cache", "The 56% survives its own scale": FP8 is per-tensor scaled,
-sixteen bytes per sixteen values).  Reading: one FP32 decode scale s per
+4-bit KV cache", "The 56% survives its own scale": one scale for the whole
+tensor and one byte per value, so 16 bytes per 16 values).  Reading: one FP32 decode scale s per
 layer for K and one for V; code = E4M3(float32(x) / s), RNE, saturating at
 448, sign kept.  Decode: e4m3(code) * s.
 """
@@ -124,7 +124,8 @@ def fp8_dequantize(codes, s):
 def calibrate_global_scale(x_bf16):
     """Serving-time calibration of one NVFP4 global scale ("SGLang's 4-bit KV
     cache": Figure 2 keeps per-layer FP32 global scales; the measured runs
-    dropped them and the post lists calibration as ongoing work).  Reading:
+    went without them, and calibrating them is named there as unfinished
+    work).  Reading:
     the tensor's absolute maximum mapped onto E2M1 max x E4M3 max,
     g = float32(amax) / 2688 (one FP32 rounding), and g = 1 when amax is not
     positive (an all-zero tensor encodes to zeros whatever g is)."""

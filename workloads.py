@@ -4,8 +4,9 @@ This module only draws inputs: shapes, value distributions, sequence
 lengths, page tables and slot mappings.  It holds none of the cache
 method's arithmetic, so both the CUDA path and the CPU oracle may use it.
 
-The workloads follow the pages' serving runs (Qwen3.8-27B full-attention
-layers: 4 KV heads, head dim 256, GQA 6, at 32K / 160K / 1M context, from
+The workloads follow the pages' serving runs (the full-attention layers of
+the 27B model, 24 query and 4 KV heads of dimension 256, at 32K / 160K / 1M
+context, from
 "SGLang's 4-bit KV cache", sections "The 56% survives its own scale" and
 "The decode gain, separated"; and the INT4 lane at 220,000 tokens with
 1600-token pages from "KV cache in 4 bits").  No dataset, trace or weight is
