@@ -152,7 +152,7 @@ def put_rows(pool, spec, page, off, head, kind, codes, scales):
 
 
 def quantize_rows(spec, x_bf16, g):
-    """Rows [..., D] of bf16 bits -> (codes bytes, scale bytes) in pool form."""
+    """Rows [..., D] of bf16 bits or float32 values -> (codes bytes, scale bytes) in pool form."""
     if spec.fmt == NVFP4:
         return quant.nvfp4_quantize(x_bf16, g)
     if spec.fmt == FP8:
@@ -165,7 +165,7 @@ def quantize_rows(spec, x_bf16, g):
 def write(pool, spec, k, v, slot_mapping, gscale):
     """Store tokens into the pool (the write path of Figure 2).
 
-    k, v: uint16 bf16 bits [T, Hkv, D]; slot_mapping: int64 [T]; gscale:
+    k, v: uint16 bf16 bits (or float32 values) [T, Hkv, D]; slot_mapping: int64 [T]; gscale:
     float32 [2] = (g_K, g_V): NVFP4 global scales or FP8 per-tensor scales
     (unused for INT4).  Slots < 0 are skipped.
     """
@@ -181,6 +181,17 @@ def write(pool, spec, k, v, slot_mapping, gscale):
         for h in range(spec.num_kv_heads):
             put_rows(pool, spec, page, off, h, name, codes[:, h], scales[:, h].reshape(len(keep), -1))
     return pool
+
+
+def write_fp8(pool, spec, k_codes, v_codes, in_scale, slot_mapping, gscale):
+    """The write fed with FP8 K/V, as the engine hands them to the cache
+    ("SGLang's 4-bit KV cache", Figure 2: prompt and new-token K/V arrive as
+    FP8): k_codes, v_codes uint8 E4M3 [T, Hkv, D] with per-tensor scales
+    in_scale = (s_K, s_V); each value is e4m3(code) * s as one float32
+    product, then encoded exactly as ``write`` encodes its bf16 values."""
+    k = quant.fp8_input_values(k_codes, np.float32(in_scale[0]))
+    v = quant.fp8_input_values(v_codes, np.float32(in_scale[1]))
+    return write(pool, spec, k, v, slot_mapping, gscale)
 
 
 def token_pages(block_table_row, positions, page_size):

@@ -58,13 +58,31 @@ def _unpack_nibbles(packed):
     return out
 
 
+def _values(x):
+    """Encoder input as float32: uint16 arrays are bf16 bit patterns, float32
+    arrays are taken as they are (the FP8-input write's decoded values)."""
+    x = np.asarray(x)
+    if x.dtype == np.float32:
+        return x
+    assert x.dtype == np.uint16, x.dtype
+    return bf16_to_f32(x)
+
+
+def fp8_input_values(codes, s_in):
+    """The FP8-input write's values: e4m3(code) * s_in as one IEEE float32
+    product (round to nearest), the engine's FP8 K/V with its per-tensor
+    scale ("SGLang's 4-bit KV cache", Figure 2: the K/V handed to the cache
+    are FP8)."""
+    return (e4m3_decode(np.asarray(codes)).astype(np.float32) * np.float32(s_in)).astype(np.float32)
+
+
 def nvfp4_quantize(x_bf16, g):
-    """Quantise rows of bf16 bit patterns to NVFP4.
+    """Quantise rows of bf16 bit patterns (or float32 values) to NVFP4.
 
     x_bf16: uint16 [..., D] (D a multiple of 16); g: float32 global scale > 0.
     Returns (codes uint8 [..., D/2], scales uint8 [..., D/16]).
     """
-    x = bf16_to_f32(x_bf16)
+    x = _values(x_bf16)
     D = x.shape[-1]
     assert D % NVFP4_BLOCK == 0
     g = np.float32(g)
@@ -91,8 +109,8 @@ def nvfp4_dequantize(codes, scales, g):
 
 
 def int4_quantize(x_bf16):
-    """INT4 per-token-head: rows of bf16 -> (codes uint8 [..., D/2], scale f32 [...])."""
-    x = bf16_to_f32(x_bf16)
+    """INT4 per-token-head: rows of bf16 (or float32) -> (codes uint8 [..., D/2], scale f32 [...])."""
+    x = _values(x_bf16)
     amax = np.max(np.abs(x), axis=-1)
     s = (amax / np.float32(7.0)).astype(np.float32)
     safe = np.where(s == 0, np.float32(1.0), s).astype(np.float32)
@@ -112,7 +130,7 @@ def int4_dequantize(codes, scale):
 def fp8_quantize(x_bf16, s):
     """bf16 bits [..., D] -> E4M3 codes uint8 [..., D]: E4M3(x / s), the FP32
     quotient rounded to nearest, then RNE onto the E4M3 grid with saturation."""
-    x = bf16_to_f32(x_bf16)
+    x = _values(x_bf16)
     return e4m3_encode((x / np.float32(s)).astype(np.float32))
 
 

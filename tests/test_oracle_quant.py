@@ -274,3 +274,39 @@ def test_calibrate_global_scale():
     codes, scales = Q.nvfp4_quantize(flat[row][None], g)
     blk = np.argmax(np.abs(F.bf16_to_f32(flat[row])).reshape(4, 16).max(axis=1))
     assert scales[0, blk] == 0x7E
+
+
+def test_fp8_input_values_match_torch_cast():
+    """The FP8-input write's values: torch's float8_e4m3fn -> float32 cast of
+    every code, times the scale in float32."""
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    codes = codes[(codes & 0x7F) != 0x7F]                      # no NaN codes
+    for s in (np.float32(1.0), np.float32(0.0123), np.float32(3.7)):
+        got = Q.fp8_input_values(codes, s)
+        want = (torch.from_numpy(codes).view(torch.float8_e4m3fn).float() * float(s)).numpy()
+        assert got.dtype == np.float32 and np.array_equal(got, want.astype(np.float32))
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "int4", "fp8"])
+def test_write_fp8_equals_write_of_the_same_bf16_values(fmt):
+    """With a power-of-two input scale every e4m3(code) * s is a bf16 value,
+    so the FP8-input write must store exactly what the bf16 write stores for
+    those values (ties the new path to the pinned one)."""
+    from oracle import pool as P
+    rng = np.random.default_rng(31)
+    T, H, D, Pg = 40, 2, 64, 16
+    kc = rng.integers(0, 256, (T, H, D), dtype=np.uint8)
+    vc = rng.integers(0, 256, (T, H, D), dtype=np.uint8)
+    kc = np.where((kc & 0x7F) == 0x7F, kc ^ 1, kc).astype(np.uint8)
+    vc = np.where((vc & 0x7F) == 0x7F, vc ^ 1, vc).astype(np.uint8)
+    s_in = np.array([0.25, 2.0], np.float32)
+    spec = P.PoolSpec(fmt, 4, Pg, H, D)
+    slots = rng.permutation(4 * Pg)[:T].astype(np.int64)
+    g = np.array([0.01, 0.02], np.float32)
+    a = P.write_fp8(P.new_pool(spec), spec, kc, vc, s_in, slots, g)
+    kb = f32_to_bf16_bits(Q.fp8_input_values(kc, s_in[0]))
+    vb = f32_to_bf16_bits(Q.fp8_input_values(vc, s_in[1]))
+    assert np.array_equal(F.bf16_to_f32(kb), Q.fp8_input_values(kc, s_in[0]))   # exact in bf16
+    b = P.write(P.new_pool(spec), spec, kb, vb, slots, g)
+    assert np.array_equal(a, b)
