@@ -60,6 +60,7 @@ def _load(build_if_missing=False):
         "kv4_pool_chunk_bytes": (i64, [P]),
         "kv4_pool_bytes": (i64, [P]),
         "kv4_write": (i32, [vp, vp, vp, i64, P, vp, i32, vp]),
+        "kv4_write_fp8": (i32, [vp, vp, vp, vp, i64, P, vp, i32, vp]),
         "kv4_decode_workspace_bytes": (i64, [i32, i32, i32, i32]),
         "kv4_decode_attention": (i32, [vp, P, vp, vp, i32, vp, i32, i32, f32, i32, vp, i64, vp,
                                        i32, vp]),
@@ -142,6 +143,15 @@ def kv4_write(k, v, slot_mapping, pool, layer_global_scale, fmt=None, stream=Non
     st = _load().kv4_write(_ptr(k), _ptr(v), _ptr(slot_mapping), k.shape[0], pool.ref,
                            _ptr(layer_global_scale), fmt, _stream(stream))
     _check(st, "kv4_write")
+
+
+def kv4_write_fp8(k, v, in_scale, slot_mapping, pool, layer_global_scale, fmt=None, stream=None):
+    """Quantise FP8 E4M3 k, v (uint8 [T, Hkv, D], per-tensor scales in_scale
+    float32 [2]) into ``pool`` at ``slot_mapping``."""
+    fmt = pool.fmt if fmt is None else (FMT[fmt] if isinstance(fmt, str) else fmt)
+    st = _load().kv4_write_fp8(_ptr(k), _ptr(v), _ptr(in_scale), _ptr(slot_mapping), k.shape[0],
+                               pool.ref, _ptr(layer_global_scale), fmt, _stream(stream))
+    _check(st, "kv4_write_fp8")
 
 
 def kv4_decode_workspace_bytes(batch, num_q_heads, head_dim, num_splits):

@@ -161,9 +161,9 @@ int64_t kv4_pool_bytes(const kv4_pool* pool) {
   return static_cast<int64_t>(pool->num_pages) * pool->num_kv_heads * chunk_bytes_of(*pool);
 }
 
-kv4_status kv4_write(const void* k, const void* v, const int64_t* slot_mapping,
-                     int64_t num_tokens, const kv4_pool* pool,
-                     const float* layer_global_scale, int32_t fmt, void* stream) {
+static kv4_status write_common(const void* k, const void* v, const float* in_scale, bool fp8_in,
+                               const int64_t* slot_mapping, int64_t num_tokens, const kv4_pool* pool,
+                               const float* layer_global_scale, int32_t fmt, void* stream) {
   g_msg.clear();
   kv4_status s = check_pool(pool);
   if (s != KV4_OK) return s;
@@ -175,6 +175,8 @@ kv4_status kv4_write(const void* k, const void* v, const int64_t* slot_mapping,
     return fail(KV4_EINVAL, "k, v and slot_mapping must be non-NULL");
   if (!aligned(k, 16) || !aligned(v, 16) || !aligned(slot_mapping, 8))
     return fail(KV4_EINVAL, "k and v must be 16-byte aligned, slot_mapping 8-byte aligned");
+  if (fp8_in && (in_scale == nullptr || !aligned(in_scale, 4)))
+    return fail(KV4_EINVAL, "the FP8 input needs its scales (in_scale, 4-byte aligned)");
   if (fmt != KV4_INT4_PTH && layer_global_scale == nullptr)
     return fail(KV4_EINVAL, "NVFP4 and FP8 need layer_global_scale");
   const int64_t threads = num_tokens * pool->num_kv_heads * (pool->head_dim / 8);
@@ -182,8 +184,14 @@ kv4_status kv4_write(const void* k, const void* v, const int64_t* slot_mapping,
     return fail(KV4_EINVAL, "num_tokens too large");
 
   kv4::WriteArgs a{};
-  a.k = static_cast<const __nv_bfloat16*>(k);
-  a.v = static_cast<const __nv_bfloat16*>(v);
+  if (fp8_in) {
+    a.k8 = static_cast<const uint8_t*>(k);
+    a.v8 = static_cast<const uint8_t*>(v);
+    a.in_scale = in_scale;
+  } else {
+    a.k = static_cast<const __nv_bfloat16*>(k);
+    a.v = static_cast<const __nv_bfloat16*>(v);
+  }
   a.slot_mapping = slot_mapping;
   a.T = num_tokens;
   a.pool = static_cast<uint8_t*>(pool->base);
@@ -197,7 +205,21 @@ kv4_status kv4_write(const void* k, const void* v, const int64_t* slot_mapping,
   a.err = error_word();
   if (a.err == nullptr) return fail(KV4_ECUDA, "no CUDA device / error word unavailable");
   cudaError_t e = kv4::launch_write(a, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? KV4_OK : cuda_fail(e, "kv4_write launch");
+  return e == cudaSuccess ? KV4_OK : cuda_fail(e, fp8_in ? "kv4_write_fp8 launch" : "kv4_write launch");
+}
+
+kv4_status kv4_write(const void* k, const void* v, const int64_t* slot_mapping,
+                     int64_t num_tokens, const kv4_pool* pool,
+                     const float* layer_global_scale, int32_t fmt, void* stream) {
+  return write_common(k, v, nullptr, false, slot_mapping, num_tokens, pool, layer_global_scale, fmt,
+                      stream);
+}
+
+kv4_status kv4_write_fp8(const void* k, const void* v, const float* in_scale,
+                         const int64_t* slot_mapping, int64_t num_tokens, const kv4_pool* pool,
+                         const float* layer_global_scale, int32_t fmt, void* stream) {
+  return write_common(k, v, in_scale, true, slot_mapping, num_tokens, pool, layer_global_scale, fmt,
+                      stream);
 }
 
 int64_t kv4_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t head_dim,

@@ -59,6 +59,9 @@ struct WriteArgs {
   int* err;
   int rows;                     // T * Hkv (< 2^31)
   FastDiv hkv_div, p_div;       // by Hkv, by P
+  const uint8_t* k8;            // FP8-input write: E4M3 [T][Hkv][D] (else null)
+  const uint8_t* v8;
+  const float* in_scale;        // [2] {s_K, s_V} of the FP8 input
 };
 
 struct PrefixArgs {

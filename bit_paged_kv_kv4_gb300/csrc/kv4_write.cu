@@ -6,6 +6,10 @@
 // codes.  INT4 per-token-head ("KV cache in 4 bits", "What we changed"): one
 // FP32 scale per (token, head) row of K and of V, 4-bit two's-complement codes.
 //
+// The input is bf16 K/V, or FP8 E4M3 K/V with per-tensor scales (the form the
+// engine hands to the cache in Figure 2): then each element is
+// e4m3(code) * s_in, one FP32 product, and is encoded the same way.
+//
 // One thread owns 8 consecutive elements (one 16-byte load of bf16); two
 // neighbouring threads form an NVFP4 block, D/8 neighbouring threads a row.
 // NVFP4 V goes to the token-pair rows the decode kernel reads (element d of
@@ -144,11 +148,24 @@ write_kernel(const WriteArgs a) {
   const uint32_t t = in_range ? fdiv(row, a.hkv_div) : 0u;
   const int h = in_range ? static_cast<int>(row - t * static_cast<uint32_t>(a.Hkv)) : 0;
 
-  // load 8 bf16 -> fp32 (rows past the end read row 0 and store nothing)
-  const __nv_bfloat16* src = (kind == 0 ? a.k : a.v) + static_cast<int64_t>(in_range ? row : 0u) * D + part * 8;
-  const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src));
+  // load 8 elements -> fp32 (rows past the end read row 0 and store nothing)
+  const int64_t base = static_cast<int64_t>(in_range ? row : 0u) * D + part * 8;
   float x[8];
-  {
+  if (a.k8 != nullptr) {
+    // FP8 input: e4m3 (exact through f16) times the tensor's input scale
+    const uint2 raw = __ldg(reinterpret_cast<const uint2*>((kind == 0 ? a.k8 : a.v8) + base));
+    const float s_in = __ldg(a.in_scale + kind);
+    uint32_t hh[4];
+    e4m3x4_to_f16x2x2(raw.x, hh[0], hh[1]);
+    e4m3x4_to_f16x2x2(raw.y, hh[2], hh[3]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hh[j]));
+      x[2 * j] = __fmul_rn(f.x, s_in);
+      x[2 * j + 1] = __fmul_rn(f.y, s_in);
+    }
+  } else {
+    const uint4 raw = __ldg(reinterpret_cast<const uint4*>((kind == 0 ? a.k : a.v) + base));
     const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {

@@ -135,6 +135,19 @@ kv4_status kv4_write(const void* k, const void* v, const int64_t* slot_mapping,
                      int64_t num_tokens, const kv4_pool* pool,
                      const float* layer_global_scale, int32_t fmt, void* stream);
 
+/*
+ * kv4_write_fp8 -- kv4_write fed with FP8 K/V, the form in which the engine
+ * of Figure 2 ("SGLang's 4-bit KV cache") hands prompt and new-token K/V to
+ * the cache.  k, v are device uint8 E4M3 codes [T][Hkv][D] (16-byte
+ * aligned) with per-tensor scales in_scale = device float[2] {s_K, s_V};
+ * each element is x = e4m3(code) * s as one IEEE FP32 product (round to
+ * nearest), then encoded exactly as kv4_write encodes its bf16 values.
+ * Other arguments, sizes and errors as kv4_write.
+ */
+kv4_status kv4_write_fp8(const void* k, const void* v, const float* in_scale,
+                         const int64_t* slot_mapping, int64_t num_tokens, const kv4_pool* pool,
+                         const float* layer_global_scale, int32_t fmt, void* stream);
+
 /* Workspace bytes kv4_decode_attention needs for these sizes and this
  * num_splits (0 when num_splits == 1, which writes `out` directly).  Depends
  * on the current device's SM count. */

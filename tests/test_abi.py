@@ -144,3 +144,13 @@ def test_extend_validation_without_gpu(lib):
     st, msg = _status(lib, ext(q=ctypes.c_void_p((1 << 20) + 8)))
     assert st == 1 and "aligned" in msg
     assert ext(B=0) == 0 and ext(mc=0) == 0     # nothing to do
+
+
+def test_write_fp8_validation_without_gpu(lib):
+    d = desc(base=1 << 20)
+    p = ctypes.byref(d)
+    fake = ctypes.c_void_p(1 << 20)
+    st, msg = _status(lib, lib.kv4_write_fp8(fake, fake, None, fake, 4, p, fake, 0, None))
+    assert st == 1 and "in_scale" in msg                    # FP8 input without its scales
+    assert lib.kv4_write_fp8(fake, fake, fake, fake, 4, p, fake, 1, None) == 1   # fmt mismatch
+    assert lib.kv4_write_fp8(None, None, None, None, 0, p, None, 0, None) == 0   # nothing to do

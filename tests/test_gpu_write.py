@@ -109,3 +109,30 @@ def test_write_skips_negative_and_flags_out_of_range_slots():
     keep[5] = -1
     OP.write(ref, spec, c.k, c.v, keep, c.g)
     assert np.array_equal(pool.buffer.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "int4", "fp8"])
+@pytest.mark.parametrize("D", [64, 256])
+def test_write_fp8_input_bit_exact(fmt, D):
+    """kv4_write_fp8 (FP8 E4M3 K/V with per-tensor input scales, non-power-of-
+    two so the products round) against the oracle's write_fp8, byte for byte."""
+    from workloads import fp8_kv_codes
+    T, H, P, pages = 300, 2, 16, 24
+    codes, s_in = fp8_kv_codes(D, T, H, D, "cuda", [[1, 5]] * H, 9.0)
+    s_in = (s_in * np.float32(1.37)).astype(np.float32)
+    rng = np.random.default_rng(D)
+    slots = rng.permutation(pages * P)[:T].astype(np.int64)
+    slots[::17] = -1                                    # skipped tokens
+    g = np.array([0.013, 0.021], np.float32)
+    pool = K.Pool(fmt, pages, P, H, D, device="cuda")
+    pool.buffer.fill_(0x5A)
+    K.kv4_write_fp8(codes[0].contiguous(), codes[1].contiguous(), torch.from_numpy(s_in).cuda(),
+                    torch.from_numpy(slots).cuda(), pool, torch.from_numpy(g).cuda())
+    torch.cuda.synchronize()
+    assert K.kv4_device_error() == 0
+    spec = OP.PoolSpec(fmt, pages, P, H, D)
+    ref = OP.write_fp8(OP.new_pool(spec, 0x5A), spec, codes[0].cpu().numpy(), codes[1].cpu().numpy(),
+                       s_in, slots, g)
+    got = pool.buffer.cpu().numpy()
+    diff = np.nonzero(got != ref)[0]
+    assert diff.size == 0, f"{diff.size} bytes differ, first at {diff[:8]}"
