@@ -508,6 +508,9 @@ def kv4_arm(args):
             del sx
             torch.cuda.empty_cache()
         extra["calibrate_64k"] = time_calibrate(device, peak)
+        # the k8v4 variant on the headline shapes: FP8 keys, 4-bit values, rotated
+        extra["k8v4_32k"] = time_k8v4(device, W.ALL["nvfp4_32k"], peak)
+        torch.cuda.empty_cache()
         line["workloads"] = extra
 
     if rank == 0 and not args.no_cpu:
@@ -613,6 +616,54 @@ def time_extend(device, w, ws, tpeak, reps=5):
             "peak": tpeak, "flops": fl}
 
 
+def time_k8v4(device, w, peak, reps=20):
+    """Decode over a k8v4 pool (FP8 keys, INT4 values, Hadamard-rotated) with
+    the shapes, lengths and values of workload w: HBM GB/s of pool bytes."""
+    import torch
+    import bit_paged_kv_kv4_gb300 as K
+    lens = w.seq_lens()
+    num_pages, table = w.block_table(lens)
+    B, Hkv, Hq, D, P = w.batch, w.num_kv_heads, w.num_q_heads, w.head_dim, w.page_size
+    pool = K.Pool("k8v4", num_pages, P, Hkv, D, device=device)
+    kvs, amax = [], torch.zeros((), device=device)
+    for b in range(B):
+        kv = W.device_kv(w, b, int(lens[b]), device)
+        amax = torch.maximum(amax, kv[0].abs().amax().float())
+        kvs.append(kv)
+    s_k = torch.tensor([W.fp8_scale_from_amax(float(amax))], dtype=torch.float32, device=device)
+    for b in range(B):
+        slots = torch.from_numpy(W.slots_for(table[b], P, np.arange(int(lens[b])))).to(device)
+        K.kv4_k8v4_write(kvs[b][0], kvs[b][1], slots, pool, s_k)
+    del kvs
+    torch.cuda.empty_cache()
+    q, _, _ = W.device_q(w, device)
+    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=device)
+    chunks = max(1, round(8 * torch.cuda.get_device_properties(device).multi_processor_count / (B * Hkv)))
+    ws = torch.empty(K.kv4_k8v4_workspace_bytes(B, Hkv, D, chunks), dtype=torch.uint8, device=device)
+    d_table, d_lens = torch.from_numpy(table).to(device), torch.from_numpy(lens).to(device)
+
+    def run():
+        K.kv4_k8v4_decode_attention(q, pool, s_k, d_table, d_lens, w.sm_scale(), out, chunks, ws)
+
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        run()
+        b2.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b2) * 1e-3)
+    if K.kv4_device_error() != 0:
+        raise RuntimeError("k8v4 decode flagged a device error")
+    med = statistics.median(ts)
+    byts = int(np.sum(lens)) * Hkv * (D + D // 2 + 4) + 2 * B * Hq * D * 2
+    return {"decode_us": med * 1e6, "gbs": byts / med / 1e9, "frac": byts / med / 1e9 / peak,
+            "num_chunks": chunks, "kv_bytes": byts, "tokens_per_s_16_layers": B / (16 * med)}
+
+
 def time_calibrate(device, peak, T=65536, Hkv=4, D=256):
     """Serving-time NVFP4 global-scale calibration over the K and V of T
     tokens (bf16, 2 x 134 MB: larger than L2, so an HBM figure)."""
@@ -695,7 +746,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the 160K / 1M / INT4 lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--only", choices=("prefix", "write", "extend"),
+    ap.add_argument("--only", choices=("prefix", "write", "extend", "k8v4"),
                     help="time just the 160K prefix dequant or the 8K prefill write and print "
                          "its line (for profiling one kernel)")
     args = ap.parse_args()
@@ -717,6 +768,8 @@ def only_arm(args):
     peak, _ = read_peaks()
     if args.only == "prefix":
         r = time_prefix(Setup(w, device), w, peak)
+    elif args.only == "k8v4":
+        r = time_k8v4(device, W.ALL["nvfp4_32k"], peak)
     elif args.only == "extend":
         r, ws = time_prefix(Setup(w, device), w, peak, keep=True)
         r = time_extend(device, w, ws, read_tensor_peak()[0], reps=args.steps)

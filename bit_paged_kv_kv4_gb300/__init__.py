@@ -21,7 +21,8 @@ from . import _build
 KV4_NVFP4 = 0
 KV4_INT4_PTH = 1
 KV4_FP8 = 2
-FMT = {"nvfp4": KV4_NVFP4, "int4": KV4_INT4_PTH, "fp8": KV4_FP8}
+KV4_K8V4 = 3
+FMT = {"nvfp4": KV4_NVFP4, "int4": KV4_INT4_PTH, "fp8": KV4_FP8, "k8v4": KV4_K8V4}
 
 _lib = None
 
@@ -70,6 +71,10 @@ def _load(build_if_missing=False):
                                        i32, i32, f32, vp, i32, vp]),
         "kv4_decode_attention_static_ws": (i32, [vp, P, vp, vp, i32, vp, i32, i32, f32, i32, vp,
                                                  i32, vp]),
+        "kv4_k8v4_write": (i32, [vp, vp, vp, i64, P, vp, vp]),
+        "kv4_k8v4_workspace_bytes": (i64, [i32, i32, i32, i32]),
+        "kv4_k8v4_decode_attention": (i32, [vp, P, vp, vp, i32, vp, i32, i32, f32, i32, vp, i64, vp,
+                                            i32, vp]),
         "kv4_device_error": (i32, []),
         "kv4_status_str": (ctypes.c_char_p, [i32]),
         "kv4_last_error_message": (ctypes.c_char_p, []),
@@ -217,6 +222,29 @@ def kv4_extend_attention(q, chunk_k, chunk_v, prefix_k, prefix_v, fp8_scale, pre
         chunk_lens.shape[0], int(max_chunk_len), Hq, chunk_k.shape[1], D, float(sm_scale),
         _ptr(out), 1 if out.dtype == torch.float32 else 0, _stream(stream))
     _check(st, "kv4_extend_attention")
+
+
+def kv4_k8v4_write(k, v, slot_mapping, pool, key_scale, stream=None):
+    """Rotate and quantise bf16 k, v [T, Hkv, D] into a k8v4 ``pool``."""
+    st = _load().kv4_k8v4_write(_ptr(k), _ptr(v), _ptr(slot_mapping), k.shape[0], pool.ref,
+                                _ptr(key_scale), _stream(stream))
+    _check(st, "kv4_k8v4_write")
+
+
+def kv4_k8v4_workspace_bytes(batch, num_kv_heads, head_dim, num_chunks):
+    return _load().kv4_k8v4_workspace_bytes(batch, num_kv_heads, head_dim, num_chunks)
+
+
+def kv4_k8v4_decode_attention(q, pool, key_scale, block_table, seq_lens, sm_scale, out,
+                              num_chunks, workspace, stream=None):
+    """Decode attention over a k8v4 pool; ``workspace`` a uint8 CUDA tensor of
+    at least kv4_k8v4_workspace_bytes(...) bytes."""
+    st = _load().kv4_k8v4_decode_attention(
+        _ptr(q), pool.ref, _ptr(key_scale), _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+        q.shape[0], q.shape[1], float(sm_scale), int(num_chunks), _ptr(workspace),
+        workspace.numel() if workspace is not None else 0, _ptr(out),
+        1 if out.dtype == torch.float32 else 0, _stream(stream))
+    _check(st, "kv4_k8v4_decode_attention")
 
 
 def kv4_device_error():

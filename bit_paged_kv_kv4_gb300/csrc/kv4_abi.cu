@@ -37,12 +37,15 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int64_t chunk_bytes_of(const kv4_pool& p) {
   const int64_t P = p.page_size, D = p.head_dim;
-  return p.fmt == KV4_NVFP4 ? P * (D + D / 8) : p.fmt == KV4_FP8 ? P * 2 * D : P * (D + 8);
+  return p.fmt == KV4_NVFP4 ? P * (D + D / 8)
+         : p.fmt == KV4_FP8   ? P * 2 * D
+         : p.fmt == KV4_K8V4  ? P * (D + D / 2 + 4)
+                              : P * (D + 8);
 }
 
 kv4_status check_pool(const kv4_pool* p) {
   if (p == nullptr) return fail(KV4_EINVAL, "pool descriptor is NULL");
-  if (p->fmt != KV4_NVFP4 && p->fmt != KV4_INT4_PTH && p->fmt != KV4_FP8)
+  if (p->fmt != KV4_NVFP4 && p->fmt != KV4_INT4_PTH && p->fmt != KV4_FP8 && p->fmt != KV4_K8V4)
     return fail(KV4_EINVAL, "bad fmt %d", p->fmt);
   if (p->reserved != 0) return fail(KV4_EINVAL, "pool.reserved must be 0");
   if (p->num_pages < 1) return fail(KV4_EINVAL, "num_pages must be >= 1");
@@ -169,6 +172,7 @@ static kv4_status write_common(const void* k, const void* v, const float* in_sca
   if (s != KV4_OK) return s;
   if ((s = check_pool_base(pool)) != KV4_OK) return s;
   if (fmt != pool->fmt) return fail(KV4_EINVAL, "fmt %d does not match pool.fmt %d", fmt, pool->fmt);
+  if (fmt == KV4_K8V4) return fail(KV4_EUNSUPPORTED, "a k8v4 pool is written by kv4_k8v4_write");
   if (num_tokens < 0) return fail(KV4_EINVAL, "num_tokens < 0");
   if (num_tokens == 0) return KV4_OK;
   if (k == nullptr || v == nullptr || slot_mapping == nullptr)
@@ -243,6 +247,8 @@ kv4_status kv4_decode_attention(const void* q, const kv4_pool* pool,
   kv4_status s = check_pool(pool);
   if (s != KV4_OK) return s;
   if ((s = check_pool_base(pool)) != KV4_OK) return s;
+  if (pool->fmt == KV4_K8V4)
+    return fail(KV4_EUNSUPPORTED, "a k8v4 pool is read by kv4_k8v4_decode_attention");
   if (batch < 0) return fail(KV4_EINVAL, "batch < 0");
   if (num_q_heads < 1 || num_q_heads % pool->num_kv_heads != 0)
     return fail(KV4_EINVAL, "num_q_heads %d is not a positive multiple of num_kv_heads %d",
@@ -356,6 +362,8 @@ kv4_status kv4_dequant_prefix(const kv4_pool* pool, const float* layer_global_sc
   if ((s = check_pool_base(pool)) != KV4_OK) return s;
   if (pool->fmt == KV4_FP8)
     return fail(KV4_EUNSUPPORTED, "an FP8 pool is already FP8: no prefix dequant");
+  if (pool->fmt == KV4_K8V4)
+    return fail(KV4_EUNSUPPORTED, "no prefix dequant for a k8v4 pool");
   if (batch < 0 || max_prefix_len < 0) return fail(KV4_EINVAL, "batch and max_prefix_len must be >= 0");
   if (max_pages < 1) return fail(KV4_EINVAL, "max_pages must be >= 1");
   if (static_cast<int64_t>(max_pages) * pool->page_size >= (int64_t{1} << 31))
@@ -449,6 +457,108 @@ kv4_status kv4_extend_attention(const void* q, const void* chunk_k, const void* 
   if (a.err == nullptr) return fail(KV4_ECUDA, "no CUDA device / error word unavailable");
   cudaError_t e = kv4::launch_extend(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KV4_OK : cuda_fail(e, "kv4_extend_attention launch");
+}
+
+kv4_status kv4_k8v4_write(const void* k, const void* v, const int64_t* slot_mapping,
+                          int64_t num_tokens, const kv4_pool* pool, const float* key_scale,
+                          void* stream) {
+  g_msg.clear();
+  kv4_status s = check_pool(pool);
+  if (s != KV4_OK) return s;
+  if ((s = check_pool_base(pool)) != KV4_OK) return s;
+  if (pool->fmt != KV4_K8V4) return fail(KV4_EINVAL, "pool.fmt must be KV4_K8V4");
+  if (num_tokens < 0) return fail(KV4_EINVAL, "num_tokens < 0");
+  if (num_tokens == 0) return KV4_OK;
+  if (k == nullptr || v == nullptr || slot_mapping == nullptr || key_scale == nullptr)
+    return fail(KV4_EINVAL, "k, v, slot_mapping and key_scale must be non-NULL");
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(slot_mapping, 8) || !aligned(key_scale, 4))
+    return fail(KV4_EINVAL, "k and v must be 16-byte aligned, slot_mapping 8-byte aligned");
+  if (num_tokens * pool->num_kv_heads >= (int64_t{1} << 34))
+    return fail(KV4_EINVAL, "num_tokens too large");
+  kv4::K8V4WriteArgs a{};
+  a.k = static_cast<const __nv_bfloat16*>(k);
+  a.v = static_cast<const __nv_bfloat16*>(v);
+  a.slot_mapping = slot_mapping;
+  a.rows = num_tokens * pool->num_kv_heads;
+  a.pool = static_cast<uint8_t*>(pool->base);
+  a.chunk_bytes = chunk_bytes_of(*pool);
+  a.P = pool->page_size;
+  a.Hkv = pool->num_kv_heads;
+  a.num_pages = pool->num_pages;
+  a.D = pool->head_dim;
+  a.s_k = key_scale;
+  a.err = error_word();
+  if (a.err == nullptr) return fail(KV4_ECUDA, "no CUDA device / error word unavailable");
+  cudaError_t e = kv4::launch_k8v4_write(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KV4_OK : cuda_fail(e, "kv4_k8v4_write launch");
+}
+
+int64_t kv4_k8v4_workspace_bytes(int32_t batch, int32_t num_kv_heads, int32_t head_dim,
+                                 int32_t num_chunks) {
+  if (batch < 0 || num_kv_heads < 0 || head_dim < 0 || num_chunks < 1) return 0;
+  const int64_t slots = static_cast<int64_t>(batch) * num_kv_heads * num_chunks;
+  const int64_t o_bytes = slots * 8 * head_dim * 4;
+  return ((o_bytes + 255) / 256) * 256 + slots * 8 * 2 * 4;
+}
+
+kv4_status kv4_k8v4_decode_attention(const void* q, const kv4_pool* pool, const float* key_scale,
+                                     const int32_t* block_table, int32_t max_pages,
+                                     const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                                     float sm_scale, int32_t num_chunks, void* workspace,
+                                     int64_t workspace_bytes, void* out, int32_t out_is_fp32,
+                                     void* stream) {
+  g_msg.clear();
+  kv4_status s = check_pool(pool);
+  if (s != KV4_OK) return s;
+  if ((s = check_pool_base(pool)) != KV4_OK) return s;
+  if (pool->fmt != KV4_K8V4) return fail(KV4_EINVAL, "pool.fmt must be KV4_K8V4");
+  if (batch < 0 || batch > 65535) return fail(KV4_EINVAL, "batch must be in [0, 65535]");
+  if (num_q_heads < 1 || num_q_heads % pool->num_kv_heads != 0)
+    return fail(KV4_EINVAL, "num_q_heads must be a positive multiple of num_kv_heads");
+  if (num_q_heads / pool->num_kv_heads > 8)
+    return fail(KV4_EUNSUPPORTED, "k8v4 decode supports at most 8 query heads per kv head");
+  if (num_chunks < 1 || num_chunks > 65535) return fail(KV4_EINVAL, "num_chunks must be in [1, 65535]");
+  if (max_pages < 1) return fail(KV4_EINVAL, "max_pages must be >= 1");
+  if (static_cast<int64_t>(max_pages) * pool->page_size >= (int64_t{1} << 31))
+    return fail(KV4_EINVAL, "max_pages * page_size must be < 2^31");
+  if (!(sm_scale > 0.f) || !(sm_scale < 3.0e38f)) return fail(KV4_EINVAL, "sm_scale must be positive and finite");
+  if (batch == 0) return KV4_OK;
+  if (q == nullptr || key_scale == nullptr || block_table == nullptr || seq_lens == nullptr ||
+      out == nullptr || workspace == nullptr)
+    return fail(KV4_EINVAL, "q, key_scale, block_table, seq_lens, workspace and out must be non-NULL");
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(workspace, 256))
+    return fail(KV4_EINVAL, "q and out must be 16-byte aligned, workspace 256-byte aligned");
+  const int64_t need = kv4_k8v4_workspace_bytes(batch, pool->num_kv_heads, pool->head_dim, num_chunks);
+  if (workspace_bytes < need)
+    return fail(KV4_EINVAL, "workspace of %lld bytes is smaller than the %lld needed",
+                static_cast<long long>(workspace_bytes), static_cast<long long>(need));
+  kv4::K8V4DecodeArgs a{};
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.pool = static_cast<const uint8_t*>(pool->base);
+  a.chunk_bytes = chunk_bytes_of(*pool);
+  a.P = pool->page_size;
+  a.Hkv = pool->num_kv_heads;
+  a.num_pages = pool->num_pages;
+  a.D = pool->head_dim;
+  a.s_k = key_scale;
+  a.block_table = block_table;
+  a.max_pages = max_pages;
+  a.seq_lens = seq_lens;
+  a.B = batch;
+  a.Hq = num_q_heads;
+  a.G = num_q_heads / pool->num_kv_heads;
+  a.nchunks = num_chunks;
+  a.sm_scale = sm_scale;
+  const int64_t slots = static_cast<int64_t>(batch) * pool->num_kv_heads * num_chunks;
+  a.part_o = static_cast<float*>(workspace);
+  a.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                       ((slots * 8 * pool->head_dim * 4 + 255) / 256) * 256);
+  a.out = out;
+  a.out_f32 = out_is_fp32 ? 1 : 0;
+  a.err = error_word();
+  if (a.err == nullptr) return fail(KV4_ECUDA, "no CUDA device / error word unavailable");
+  cudaError_t e = kv4::launch_k8v4_decode(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KV4_OK : cuda_fail(e, "kv4_k8v4_decode_attention launch");
 }
 
 int32_t kv4_device_error(void) {

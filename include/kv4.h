@@ -20,7 +20,10 @@
  *                         queries attend over that FP8 prefix plus the FP8
  *                         current chunk, on the tensor cores;
  *   kv4_calibrate_global_scale  the per-layer FP32 global scales from the
- *                         layer's K and V at serving time.
+ *                         layer's K and V at serving time;
+ *   kv4_k8v4_write / kv4_k8v4_decode_attention  the k8v4 variant the same
+ *                         page contrasts (FP8 keys, 4-bit values, both given
+ *                         one fixed Hadamard rotation), KV4_K8V4 pools only.
  *
  * Three formats share the pool structure:
  *   KV4_NVFP4     E2M1 elements, one E4M3 scale per 16 elements, one FP32
@@ -89,7 +92,7 @@
 extern "C" {
 #endif
 
-typedef enum { KV4_NVFP4 = 0, KV4_INT4_PTH = 1, KV4_FP8 = 2 } kv4_fmt;
+typedef enum { KV4_NVFP4 = 0, KV4_INT4_PTH = 1, KV4_FP8 = 2, KV4_K8V4 = 3 } kv4_fmt;
 
 typedef enum {
   KV4_OK = 0,
@@ -303,6 +306,47 @@ kv4_status kv4_decode_attention_static_ws(const void* q, const kv4_pool* pool,
                                           int32_t num_q_heads, float sm_scale,
                                           int32_t num_splits, void* out,
                                           int32_t out_is_fp32, void* stream);
+
+/*
+ * The k8v4 variant ("SGLang's 4-bit KV cache", section "Against what this
+ * site already established": the other 4-bit KV cache of the month stores
+ * keys in FP8 and values in 4 bits and rotates both by one fixed FP32
+ * Hadamard transform of size D).  KV4_K8V4 pools; chunk of P tokens =
+ * [K codes P*D][V codes P*D/2][V scales FP32 * P], rows per token.
+ * Rotation H = S_D / sqrt(D) (Sylvester; symmetric, H H = I), evaluated on
+ * the write path in FP32 as the fast Walsh-Hadamard transform (stages
+ * len = 1, 2, ..., D/2, pairs (x_i, x_{i+len}) with bit len of i clear ->
+ * (x_i + x_{i+len}, x_i - x_{i+len}), then times float32(1/sqrt(D))).
+ * Keys: E4M3(k_rot / s_K), s_K = *key_scale (one FP32 scale per layer);
+ * values: INT4 per (token, head), s = amax(v_rot) / 7,
+ * code = clamp(rne(v_rot / s), -8, 7).  (The page names no value encoder;
+ * this is the library's reading.)
+ *
+ * kv4_k8v4_write -- rotate and quantise T tokens of bf16 K/V
+ *   ([T][Hkv][D], 16-byte aligned) into the pool at slot_mapping (int64
+ *   [T], 8-byte aligned; < 0 skipped; beyond the pool flagged KV4_EBOUNDS).
+ *
+ * kv4_k8v4_decode_attention -- one decode step: q_rot = H q (bf16 q
+ *   [B][Hq][D]), softmax(sm_scale * q_rot . K_hat_rot) over the request's
+ *   tokens (block_table / seq_lens / max_pages as kv4_decode_attention),
+ *   o = H (sum_t p_t V_hat_rot_t), out [B][Hq][D] bf16 or FP32.  Each
+ *   request's tokens are cut into num_chunks ranges handled by separate CTAs
+ *   and merged by a second kernel; workspace (256-byte aligned) of at least
+ *   kv4_k8v4_workspace_bytes(B, Hkv, D, num_chunks) bytes.  At most 8 query
+ *   heads per kv head (else KV4_EUNSUPPORTED).  An empty request gives a zero
+ *   row.  Asynchronous on `stream`; allocates nothing.
+ */
+kv4_status kv4_k8v4_write(const void* k, const void* v, const int64_t* slot_mapping,
+                          int64_t num_tokens, const kv4_pool* pool, const float* key_scale,
+                          void* stream);
+int64_t kv4_k8v4_workspace_bytes(int32_t batch, int32_t num_kv_heads, int32_t head_dim,
+                                 int32_t num_chunks);
+kv4_status kv4_k8v4_decode_attention(const void* q, const kv4_pool* pool, const float* key_scale,
+                                     const int32_t* block_table, int32_t max_pages,
+                                     const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                                     float sm_scale, int32_t num_chunks, void* workspace,
+                                     int64_t workspace_bytes, void* out, int32_t out_is_fp32,
+                                     void* stream);
 
 /* Read and clear the current device's error word (the first kv4_status a
  * kernel recorded since the last call, KV4_OK if none).  Synchronises the

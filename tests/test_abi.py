@@ -154,3 +154,26 @@ def test_write_fp8_validation_without_gpu(lib):
     assert st == 1 and "in_scale" in msg                    # FP8 input without its scales
     assert lib.kv4_write_fp8(fake, fake, fake, fake, 4, p, fake, 1, None) == 1   # fmt mismatch
     assert lib.kv4_write_fp8(None, None, None, None, 0, p, None, 0, None) == 0   # nothing to do
+
+
+def test_k8v4_validation_without_gpu(lib):
+    fake = ctypes.c_void_p(1 << 20)
+    d = desc(fmt=3, base=1 << 20)
+    p = ctypes.byref(d)
+    assert lib.kv4_pool_chunk_bytes(p) == 64 * (256 + 128 + 4)
+    # the generic entry points refuse a k8v4 pool
+    assert lib.kv4_write(fake, fake, fake, 4, p, fake, 3, None) == 2
+    assert lib.kv4_dequant_prefix(p, fake, fake, 2, fake, fake, 1, 1, fake, fake, fake, None) == 2
+    assert lib.kv4_decode_attention(fake, p, fake, fake, 8, fake, 2, 8, 0.0625, 4, fake, 1 << 20,
+                                    fake, 1, None) == 2
+    # k8v4 entries: scale pointer, head ratio, group size, workspace size
+    assert lib.kv4_k8v4_write(fake, fake, fake, 4, p, None, None) == 1
+    assert lib.kv4_k8v4_write(fake, fake, fake, 0, p, None, None) == 0
+    dec = lambda **kw: lib.kv4_k8v4_decode_attention(
+        fake, p, fake, fake, 8, fake, kw.get("B", 2), kw.get("Hq", 8), 0.0625, kw.get("S", 4), fake,
+        kw.get("ws", 1 << 30), fake, 1, None)
+    assert dec(Hq=7) == 1 and dec(Hq=18) == 2 and dec(S=0) == 1
+    assert dec(ws=16) == 1
+    assert lib.kv4_k8v4_workspace_bytes(2, 2, 256, 4) > 2 * 2 * 4 * 8 * 256 * 4
+    nv = desc(fmt=0, base=1 << 20)
+    assert lib.kv4_k8v4_write(fake, fake, fake, 4, ctypes.byref(nv), fake, None) == 1
