@@ -20,9 +20,12 @@
 // keys, and the combined output is rotated back (H H = I).  A CTA owns one
 // contiguous range (chunk) of one request's tokens and one kv head with all
 // its G <= 8 query heads; per sub-block of 256 tokens each thread scores one
-// token against the G rotated queries, then each warp accumulates P V over a
-// stride of tokens with eight value dimensions per lane.  The combine merges
+// token against the G rotated queries (its whole key row loaded at once) while
+// an asynchronous copy brings that token's value row and scale into shared
+// memory; then each warp accumulates P V from shared memory over a stride of
+// tokens with eight value dimensions per lane.  The combine merges
 // the chunks' (max, sum, partial output) and applies the inverse rotation.
+#include <algorithm>
 #include <cstdint>
 
 #include "kv4_device.cuh"
@@ -162,14 +165,20 @@ __device__ void fwht_smem(float* v, int n_vec, float mul) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kTB) k8v4_partial_kernel(const K8V4DecodeArgs a) {
+__global__ void __launch_bounds__(kTB, 2) k8v4_partial_kernel(const K8V4DecodeArgs a) {
   constexpr int TPR = D / 8;                  // lanes per value row (8 dims each)
   constexpr int NTG = kTB / TPR;              // token groups in pass 2
   __shared__ float qs[kMaxG * D];             // rotated, pre-scaled queries
   __shared__ float ps[kTB * kMaxG];           // scores, then weights, of the sub-block
   __shared__ float red[kMaxG][kTB / 32];
   __shared__ float mrun[kMaxG], lrun[kMaxG], alpha_s[kMaxG];
-  extern __shared__ float oacc[];             // [NTG][G][D] partial outputs
+  // dynamic: the sub-block's value codes [kTB][D/2] and row scales [kTB]
+  // during the token loop; the token groups' partial outputs [NTG][G][D]
+  // after it (the same bytes)
+  extern __shared__ __align__(16) float dyn_smem[];
+  uint8_t* vrow = reinterpret_cast<uint8_t*>(dyn_smem);
+  float* vsc = reinterpret_cast<float*>(vrow + kTB * (D / 2));
+  float* oacc = dyn_smem;
 
   const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int G = a.G, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -201,7 +210,8 @@ __global__ void __launch_bounds__(kTB) k8v4_partial_kernel(const K8V4DecodeArgs 
   };
 
   for (int t0 = t_begin; t0 < t_end; t0 += kTB) {
-    // pass 1: thread tid scores token t0 + tid against the G queries
+    // pass 1: thread tid scores token t0 + tid against the G queries and
+    // starts the copy of its value row and scale into shared memory
     {
       const int t = t0 + tid;
       float s[kMaxG];
@@ -210,12 +220,27 @@ __global__ void __launch_bounds__(kTB) k8v4_partial_kernel(const K8V4DecodeArgs 
       bool ok = t < t_end;
       const uint8_t* ch = ok ? chunk_of(t) : nullptr;
       if (ok && ch == nullptr) { set_error(a.err, KV4_EBOUNDS); ok = false; }
+      uint8_t* vdst = vrow + tid * (D / 2);
       if (ok) {
-        const uint4* krow = reinterpret_cast<const uint4*>(ch + static_cast<int64_t>(t % a.P) * D);
-#pragma unroll 2
-        for (int u = 0; u < D / 16; ++u) {
-          const uint4 w = __ldg(krow + u);
-          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        const int off = t % a.P;
+        const uint8_t* vsrc = ch + static_cast<int64_t>(a.P) * D + static_cast<int64_t>(off) * (D / 2);
+#pragma unroll
+        for (int u = 0; u < D / 32; ++u)
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                       :: "r"(smem_u32(vdst + 16 * u)), "l"(vsrc + 16 * u) : "memory");
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;"
+                     :: "r"(smem_u32(vsc + tid)),
+                        "l"(ch + static_cast<int64_t>(a.P) * D + static_cast<int64_t>(a.P) * (D / 2) + 4 * off)
+                     : "memory");
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        const uint4* krow = reinterpret_cast<const uint4*>(ch + static_cast<int64_t>(off) * D);
+        constexpr int KU = D / 16;
+        uint4 kw[KU];
+#pragma unroll
+        for (int u = 0; u < KU; ++u) kw[u] = __ldg(krow + u);     // the whole key row in flight
+#pragma unroll
+        for (int u = 0; u < KU; ++u) {
+          const uint32_t ws[4] = {kw[u].x, kw[u].y, kw[u].z, kw[u].w};
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             uint32_t h0, h1;
@@ -226,12 +251,16 @@ __global__ void __launch_bounds__(kTB) k8v4_partial_kernel(const K8V4DecodeArgs 
 #pragma unroll
             for (int g = 0; g < kMaxG; ++g) {
               if (g < G) {
-                const float* qq = qs + g * D + d;
-                s[g] = fmaf(f0.x, qq[0], fmaf(f0.y, qq[1], fmaf(f1.x, qq[2], fmaf(f1.y, qq[3], s[g]))));
+                const float4 qq = *reinterpret_cast<const float4*>(qs + g * D + d);
+                s[g] = fmaf(f0.x, qq.x, fmaf(f0.y, qq.y, fmaf(f1.x, qq.z, fmaf(f1.y, qq.w, s[g]))));
               }
             }
           }
         }
+      } else {
+#pragma unroll
+        for (int u = 0; u < D / 32; ++u) *reinterpret_cast<uint4*>(vdst + 16 * u) = make_uint4(0u, 0u, 0u, 0u);
+        vsc[tid] = 0.f;
       }
 #pragma unroll
       for (int g = 0; g < kMaxG; ++g) ps[tid * kMaxG + g] = ok ? s[g] : -INFINITY;
@@ -273,6 +302,7 @@ __global__ void __launch_bounds__(kTB) k8v4_partial_kernel(const K8V4DecodeArgs 
 #pragma unroll
       for (int k = 0; k < 8; ++k) o[g][k] *= al;
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");      // this thread's value copies
     __syncthreads();
     if (tid < G) {
       float sum = 0.f;
@@ -282,14 +312,8 @@ __global__ void __launch_bounds__(kTB) k8v4_partial_kernel(const K8V4DecodeArgs 
     // pass 2: token group tg takes tokens t0 + tg, t0 + tg + NTG, ...; lane
     // dg accumulates value dims 8 dg .. 8 dg + 7
     for (int i = tg; i < kTB && t0 + i < t_end; i += NTG) {
-      const int t = t0 + i;
-      const uint8_t* ch = chunk_of(t);
-      if (ch == nullptr) continue;
-      const int off = t % a.P;
-      const uint32_t nib = __ldg(reinterpret_cast<const uint32_t*>(
-          ch + static_cast<int64_t>(a.P) * D + static_cast<int64_t>(off) * (D / 2)) + dg);
-      const float sv = __ldg(reinterpret_cast<const float*>(
-          ch + static_cast<int64_t>(a.P) * D + static_cast<int64_t>(a.P) * (D / 2) + 4 * off));
+      const uint32_t nib = *reinterpret_cast<const uint32_t*>(vrow + i * (D / 2) + 4 * dg);
+      const float sv = vsc[i];
       float v[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
@@ -359,11 +383,12 @@ __global__ void __launch_bounds__(D) k8v4_combine_kernel(const K8V4DecodeArgs a)
 template <int D>
 cudaError_t launch_decode_d(const K8V4DecodeArgs& a, cudaStream_t st) {
   constexpr int NTG = kTB / (D / 8);
-  const size_t dyn = static_cast<size_t>(NTG) * a.G * D * sizeof(float);
+  constexpr int kStage = kTB * (D / 2 + 4);
+  const size_t dyn = std::max(static_cast<size_t>(NTG) * a.G * D * sizeof(float), static_cast<size_t>(kStage));
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(k8v4_partial_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         NTG * kMaxG * D * static_cast<int>(sizeof(float)));
+                                         std::max(NTG * kMaxG * D * static_cast<int>(sizeof(float)), kStage));
     if (e != cudaSuccess) return e;
     attr = true;
   }
