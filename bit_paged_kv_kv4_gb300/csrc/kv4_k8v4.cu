@@ -19,13 +19,11 @@
 // way (q_rot . k_rot = q . k), the softmax runs over the dequantised rotated
 // keys, and the combined output is rotated back (H H = I).  A CTA owns one
 // contiguous range (chunk) of one request's tokens and one kv head with all
-// its G <= 8 query heads; per sub-block of 256 tokens each thread scores one
-// token against the G rotated queries (its whole key row loaded at once) while
-// an asynchronous copy brings that token's value row and scale into shared
-// memory; then each warp accumulates P V from shared memory over a stride of
-// tokens with eight value dimensions per lane.  The combine merges
+// its G <= 8 query heads; its 4 warps take 16-token tiles in turn and run
+// both products on the tensor cores (m16n8k16 f16 MMAs, FP32 accumulation;
+// keys exact in f16, values as exact INT4 codes with the per-token scale
+// carried by the softmax weight, split into f16 hi + lo).  The combine merges
 // the chunks' (max, sum, partial output) and applies the inverse rotation.
-#include <algorithm>
 #include <cstdint>
 
 #include "kv4_device.cuh"
@@ -35,7 +33,6 @@ namespace kv4 {
 namespace {
 
 constexpr int kMaxG = 8;          // query heads per kv head the decode supports
-constexpr int kTB = 256;          // tokens per sub-block (= threads per CTA)
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
@@ -164,193 +161,240 @@ __device__ void fwht_smem(float* v, int n_vec, float mul) {
   __syncthreads();
 }
 
+// INT4 nibbles at bits 0-3 and 16-19 (lo) or 4-7 and 20-23 (hi) of x ->
+// f16x2 of the signed codes: (n ^ 8) + 1024 as an f16 bit pattern, minus
+// 1032 (for hi, the nibble sits 16 times higher and is scaled down first).
+__device__ __forceinline__ uint32_t nib_lo_pair(uint32_t x) {
+  const uint32_t h = (x & 0x000F000Fu) ^ 0x64086408u;
+  return hfma2(h, 0x3C003C00u, 0xE408E408u);
+}
+__device__ __forceinline__ uint32_t nib_hi_pair(uint32_t x) {
+  const uint32_t h = ((x & 0x00F000F0u) ^ 0x00800080u) | 0x64006400u;
+  return hfma2(h, 0x2C002C00u, 0xD480D480u);
+}
+
+// Tensor-core partial decode over one token range (chunk) of one request and
+// kv head: 4 warps, each taking 16-token tiles in turn with its own online
+// softmax state, merged at the end.  m16n8k16 f16 MMAs, FP32 accumulation:
+//   S^T (16 tokens x 8 heads) = K (exact f16 from E4M3) q_rot^T (f16 hi + lo);
+//   O^T (16 dims x 8 heads)  += V^T (INT4 codes, exact) P'^T, where
+//   P' = p * s_v(token) is split into f16 hi + lo parts.
+// Lane (grp = lane / 4, tig = lane % 4).  K-step j of S covers dims
+// (D/4) tig + 4j .. +3 for lane tig (any fixed assignment of dims to k works
+// when q uses the same one), so a lane reads one contiguous D/4-byte segment
+// of each key row.  O row r of m-tile mi is dim (D/8) grp + 2 mi + (r >= 8),
+// so a lane reads one contiguous D/16-byte segment of each value row.
 template <int D>
-__global__ void __launch_bounds__(kTB, 2) k8v4_partial_kernel(const K8V4DecodeArgs a) {
-  constexpr int TPR = D / 8;                  // lanes per value row (8 dims each)
-  constexpr int NTG = kTB / TPR;              // token groups in pass 2
-  __shared__ float qs[kMaxG * D];             // rotated, pre-scaled queries
-  __shared__ float ps[kTB * kMaxG];           // scores, then weights, of the sub-block
-  __shared__ float red[kMaxG][kTB / 32];
-  __shared__ float mrun[kMaxG], lrun[kMaxG], alpha_s[kMaxG];
-  // dynamic: the sub-block's value codes [kTB][D/2] and row scales [kTB]
-  // during the token loop; the token groups' partial outputs [NTG][G][D]
-  // after it (the same bytes)
-  extern __shared__ __align__(16) float dyn_smem[];
-  uint8_t* vrow = reinterpret_cast<uint8_t*>(dyn_smem);
-  float* vsc = reinterpret_cast<float*>(vrow + kTB * (D / 2));
-  float* oacc = dyn_smem;
+__global__ void __launch_bounds__(128) k8v4_partial_kernel(const K8V4DecodeArgs a) {
+  constexpr int KS = D / 16;                  // k-steps of S, m-tiles of O
+  constexpr int KSEG = D / 4;                 // key bytes per lane and token
+  constexpr int VSEG = D / 16;                // value bytes per lane and token
+  __shared__ float qsh[kMaxG * D];
+  __shared__ float obuf[4 * kMaxG * D];
+  __shared__ float sm_m[4][kMaxG], sm_l[4][kMaxG];
 
   const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int G = a.G, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int grp = lane >> 2, tig = lane & 3;
   const int L = max(0, min(a.seq_lens[b], a.max_pages * a.P));
-  if (tid == 0 && a.seq_lens[b] > a.max_pages * a.P) set_error(a.err, KV4_EBOUNDS);
+  if (tid == 0 && c == 0 && a.seq_lens[b] > a.max_pages * a.P) set_error(a.err, KV4_EBOUNDS);
   const int per = (L + a.nchunks - 1) / a.nchunks;
   const int t_begin = min(L, c * per), t_end = min(L, t_begin + per);
 
-  // rotated queries, scaled so scores come out in log2 units
-  for (int p = tid; p < G * D; p += kTB) {
+  // rotated queries (FP32), then this lane's B fragments of S: head grp
+  for (int p = tid; p < G * D; p += blockDim.x) {
     const int g = p / D, d = p % D;
-    qs[p] = __bfloat162float(a.q[(static_cast<int64_t>(b) * a.Hq + h * G + g) * D + d]);
+    qsh[p] = __bfloat162float(a.q[(static_cast<int64_t>(b) * a.Hq + h * G + g) * D + d]);
   }
-  fwht_smem<D>(qs, G, a.sm_scale * __ldg(a.s_k) * kLog2e);
-  if (tid < kMaxG) { mrun[tid] = -INFINITY; lrun[tid] = 0.f; }
-
-  const int tg = tid / TPR, dg = tid % TPR;   // pass 2: token group, 8-dim group
-  float o[kMaxG][8];
+  fwht_smem<D>(qsh, G, 1.0f);
+  // The rotated q is an FP32 result: split it into f16 hi + lo parts (two
+  // MMAs per k-step), so the scores keep FP32-level accuracy.
+  uint32_t qb[2 * KS], ql[2 * KS];
 #pragma unroll
-  for (int g = 0; g < kMaxG; ++g)
+  for (int j = 0; j < KS; ++j) {
+    const int d = KSEG * tig + 4 * j;
+    const float* qq = qsh + grp * D + d;
+    const bool hv = grp < G;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) o[g][k] = 0.f;
+    for (int e = 0; e < 2; ++e) {
+      const uint32_t hi = hv ? pack_f16x2(qq[2 * e], qq[2 * e + 1]) : 0u;
+      const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+      qb[2 * j + e] = hi;
+      ql[2 * j + e] = hv ? pack_f16x2(qq[2 * e] - hf.x, qq[2 * e + 1] - hf.y) : 0u;
+    }
+  }
+  const float qk_scale = a.sm_scale * __ldg(a.s_k) * kLog2e;
 
   const int32_t* bt = a.block_table + static_cast<int64_t>(b) * a.max_pages;
   auto chunk_of = [&](int t) -> const uint8_t* {
+    if (t >= t_end) return nullptr;
     const int32_t page = bt[t / a.P];
-    if (page < 0 || page >= a.num_pages) return nullptr;
+    if (page < 0 || page >= a.num_pages) {
+      set_error(a.err, KV4_EBOUNDS);
+      return nullptr;
+    }
     return a.pool + (static_cast<int64_t>(page) * a.Hkv + h) * a.chunk_bytes;
   };
+  const int64_t vcode0 = static_cast<int64_t>(a.P) * D;           // value codes region
+  const int64_t vsc0 = vcode0 + static_cast<int64_t>(a.P) * (D / 2); // value scales region
 
-  for (int t0 = t_begin; t0 < t_end; t0 += kTB) {
-    // pass 1: thread tid scores token t0 + tid against the G queries and
-    // starts the copy of its value row and scale into shared memory
-    {
-      const int t = t0 + tid;
-      float s[kMaxG];
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+  float o[KS][4];
 #pragma unroll
-      for (int g = 0; g < kMaxG; ++g) s[g] = 0.f;
-      bool ok = t < t_end;
-      const uint8_t* ch = ok ? chunk_of(t) : nullptr;
-      if (ok && ch == nullptr) { set_error(a.err, KV4_EBOUNDS); ok = false; }
-      uint8_t* vdst = vrow + tid * (D / 2);
-      if (ok) {
+  for (int mi = 0; mi < KS; ++mi) o[mi][0] = o[mi][1] = o[mi][2] = o[mi][3] = 0.f;
+
+  for (int t0 = t_begin + 16 * warp; t0 < t_end; t0 += 64) {
+    // ---- loads: key segments of tokens grp, grp+8 (+ their value scales);
+    //      value segments of tokens 2tig, 2tig+1, 2tig+8, 2tig+9
+    uint32_t kw[2][KS];
+    float sv[2];
+    bool kval[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int t = t0 + grp + 8 * r;
+      const uint8_t* ch = chunk_of(t);
+      kval[r] = ch != nullptr;
+      sv[r] = 0.f;
+      if (kval[r]) {
         const int off = t % a.P;
-        const uint8_t* vsrc = ch + static_cast<int64_t>(a.P) * D + static_cast<int64_t>(off) * (D / 2);
+        const uint4* src = reinterpret_cast<const uint4*>(ch + static_cast<int64_t>(off) * D + KSEG * tig);
 #pragma unroll
-        for (int u = 0; u < D / 32; ++u)
-          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
-                       :: "r"(smem_u32(vdst + 16 * u)), "l"(vsrc + 16 * u) : "memory");
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;"
-                     :: "r"(smem_u32(vsc + tid)),
-                        "l"(ch + static_cast<int64_t>(a.P) * D + static_cast<int64_t>(a.P) * (D / 2) + 4 * off)
-                     : "memory");
-        asm volatile("cp.async.commit_group;" ::: "memory");
-        const uint4* krow = reinterpret_cast<const uint4*>(ch + static_cast<int64_t>(off) * D);
-        constexpr int KU = D / 16;
-        uint4 kw[KU];
-#pragma unroll
-        for (int u = 0; u < KU; ++u) kw[u] = __ldg(krow + u);     // the whole key row in flight
-#pragma unroll
-        for (int u = 0; u < KU; ++u) {
-          const uint32_t ws[4] = {kw[u].x, kw[u].y, kw[u].z, kw[u].w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            uint32_t h0, h1;
-            e4m3x4_to_f16x2x2(ws[k], h0, h1);
-            const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&h0));
-            const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&h1));
-            const int d = u * 16 + k * 4;
-#pragma unroll
-            for (int g = 0; g < kMaxG; ++g) {
-              if (g < G) {
-                const float4 qq = *reinterpret_cast<const float4*>(qs + g * D + d);
-                s[g] = fmaf(f0.x, qq.x, fmaf(f0.y, qq.y, fmaf(f1.x, qq.z, fmaf(f1.y, qq.w, s[g]))));
-              }
-            }
-          }
+        for (int u = 0; u < KS / 4; ++u) {
+          const uint4 w = __ldg(src + u);
+          kw[r][4 * u] = w.x; kw[r][4 * u + 1] = w.y; kw[r][4 * u + 2] = w.z; kw[r][4 * u + 3] = w.w;
         }
+        sv[r] = __ldg(reinterpret_cast<const float*>(ch + vsc0 + 4 * off));
       } else {
 #pragma unroll
-        for (int u = 0; u < D / 32; ++u) *reinterpret_cast<uint4*>(vdst + 16 * u) = make_uint4(0u, 0u, 0u, 0u);
-        vsc[tid] = 0.f;
-      }
-#pragma unroll
-      for (int g = 0; g < kMaxG; ++g) ps[tid * kMaxG + g] = ok ? s[g] : -INFINITY;
-      // sub-block maximum per head
-#pragma unroll
-      for (int g = 0; g < kMaxG; ++g) {
-        float m = ok ? s[g] : -INFINITY;
-#pragma unroll
-        for (int x = 16; x > 0; x >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, x));
-        if (lane == 0) red[g][warp] = m;
+        for (int j = 0; j < KS; ++j) kw[r][j] = 0u;
       }
     }
-    __syncthreads();
-    if (tid < G) {
-      float m = red[tid][0];
-      for (int w = 1; w < kTB / 32; ++w) m = fmaxf(m, red[tid][w]);
-      const float mn = fmaxf(mrun[tid], m);
-      alpha_s[tid] = (mn == -INFINITY) ? 1.f : fast_exp2(mrun[tid] - mn);
-      mrun[tid] = mn;
-    }
-    __syncthreads();
-    // weights of this thread's token, and their sum per head
+    uint32_t vw[4][(VSEG + 3) / 4];           // tokens 2tig, 2tig+1, 2tig+8, 2tig+9
 #pragma unroll
-    for (int g = 0; g < kMaxG; ++g) {
-      float p = 0.f;
-      if (g < G) {
-        const float sc = ps[tid * kMaxG + g];
-        p = (sc == -INFINITY) ? 0.f : fast_exp2(sc - mrun[g]);
-        ps[tid * kMaxG + g] = p;
-      }
-#pragma unroll
-      for (int x = 16; x > 0; x >>= 1) p += __shfl_xor_sync(0xffffffffu, p, x);
-      if (lane == 0) red[g][warp] = p;
-    }
-    // rescale the running outputs
-#pragma unroll
-    for (int g = 0; g < kMaxG; ++g) {
-      const float al = (g < G) ? alpha_s[g] : 1.f;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) o[g][k] *= al;
-    }
-    asm volatile("cp.async.wait_all;" ::: "memory");      // this thread's value copies
-    __syncthreads();
-    if (tid < G) {
-      float sum = 0.f;
-      for (int w = 0; w < kTB / 32; ++w) sum += red[tid][w];
-      lrun[tid] = lrun[tid] * alpha_s[tid] + sum;
-    }
-    // pass 2: token group tg takes tokens t0 + tg, t0 + tg + NTG, ...; lane
-    // dg accumulates value dims 8 dg .. 8 dg + 7
-    for (int i = tg; i < kTB && t0 + i < t_end; i += NTG) {
-      const uint32_t nib = *reinterpret_cast<const uint32_t*>(vrow + i * (D / 2) + 4 * dg);
-      const float sv = vsc[i];
-      float v[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int code = static_cast<int>((nib >> (4 * k)) & 0xFu);
-        v[k] = static_cast<float>(code >= 8 ? code - 16 : code) * sv;
-      }
-#pragma unroll
-      for (int g = 0; g < kMaxG; ++g) {
-        if (g < G) {
-          const float p = ps[i * kMaxG + g];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) o[g][k] = fmaf(p, v[k], o[g][k]);
-        }
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const int t = t0 + 2 * tig + (q4 & 1) + 8 * (q4 >> 1);
+      const uint8_t* ch = chunk_of(t);
+      const uint8_t* src = ch ? ch + vcode0 + static_cast<int64_t>(t % a.P) * (D / 2) + VSEG * grp : nullptr;
+      if constexpr (VSEG == 16) {
+        const uint4 w = src ? __ldg(reinterpret_cast<const uint4*>(src)) : make_uint4(0u, 0u, 0u, 0u);
+        vw[q4][0] = w.x; vw[q4][1] = w.y; vw[q4][2] = w.z; vw[q4][3] = w.w;
+      } else if constexpr (VSEG == 8) {
+        const uint2 w = src ? __ldg(reinterpret_cast<const uint2*>(src)) : make_uint2(0u, 0u);
+        vw[q4][0] = w.x; vw[q4][1] = w.y;
+      } else {
+        vw[q4][0] = src ? __ldg(reinterpret_cast<const uint32_t*>(src)) : 0u;
       }
     }
-    __syncthreads();
+
+    // ---- S^T = K q_rot^T; acc: (token grp, heads 2tig, 2tig+1), (token grp+8, ...)
+    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < KS; ++j) {
+      uint32_t a0, a1, a2, a3;
+      e4m3x4_to_f16x2x2(kw[0][j], a0, a2);
+      e4m3x4_to_f16x2x2(kw[1][j], a1, a3);
+      mma_f16_16816(sacc, a0, a1, a2, a3, qb[2 * j], qb[2 * j + 1]);
+      mma_f16_16816(sacc, a0, a1, a2, a3, ql[2 * j], ql[2 * j + 1]);
+    }
+
+    // ---- online softmax (base 2) for heads 2tig + cc
+    float x[4], tmx[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) x[2 * r + cc] = kval[r] ? sacc[2 * r + cc] * qk_scale : -INFINITY;
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      tmx[cc] = fmaxf(x[cc], x[2 + cc]);
+#pragma unroll
+      for (int o2 = 4; o2 < 32; o2 <<= 1) tmx[cc] = fmaxf(tmx[cc], __shfl_xor_sync(0xffffffffu, tmx[cc], o2));
+    }
+    float mnew[2], corr[2];
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      mnew[cc] = fmaxf(m_run[cc], tmx[cc]);
+      corr[cc] = (mnew[cc] == -INFINITY) ? 1.f : fast_exp2(m_run[cc] - mnew[cc]);
+      m_run[cc] = mnew[cc];
+    }
+    uint32_t pb[2], pl[2];
+    float psum[2] = {0.f, 0.f};
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      float w[2];
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const float p = (x[2 * r + cc] == -INFINITY) ? 0.f : fast_exp2(x[2 * r + cc] - mnew[cc]);
+        psum[cc] += p;
+        w[cc] = kval[r] ? p * sv[r] : 0.f;      // the token's value scale rides on its weight
+      }
+      const uint32_t hi = pack_f16x2(w[0], w[1]);
+      const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+      const uint32_t lo = pack_f16x2(w[0] - hf.x, w[1] - hf.y);
+      pb[r] = movmatrix_trans(hi);            // (tokens 2tig, 2tig+1 [+8r]) of head grp
+      pl[r] = movmatrix_trans(lo);
+    }
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) l_run[cc] = l_run[cc] * corr[cc] + psum[cc];
+#pragma unroll
+    for (int mi = 0; mi < KS; ++mi) {
+      o[mi][0] *= corr[0]; o[mi][1] *= corr[1]; o[mi][2] *= corr[0]; o[mi][3] *= corr[1];
+    }
+
+    // ---- O^T += V^T P'^T over m-tiles mi (byte mi of the value segments)
+#pragma unroll
+    for (int mi = 0; mi < KS; ++mi) {
+      const int wj = mi >> 2, mm = mi & 3;
+      const uint32_t sel = mm | (mm << 4) | ((4 + mm) << 8) | ((4 + mm) << 12);
+      const uint32_t xab = prmt(vw[0][wj], vw[1][wj], sel);
+      const uint32_t xcd = prmt(vw[2][wj], vw[3][wj], sel);
+      const uint32_t a0 = nib_lo_pair(xab), a1 = nib_hi_pair(xab);
+      const uint32_t a2 = nib_lo_pair(xcd), a3 = nib_hi_pair(xcd);
+      mma_f16_16816(o[mi], a0, a1, a2, a3, pb[0], pb[1]);
+      mma_f16_16816(o[mi], a0, a1, a2, a3, pl[0], pl[1]);
+    }
   }
 
-  // reduce the token groups' partial outputs and write this chunk's partial
+  // ---- merge the 4 warps: row sums over the grp lanes, then in shared memory
 #pragma unroll
-  for (int g = 0; g < kMaxG; ++g) {
-    if (g < G) {
+  for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
-      for (int k = 0; k < 8; ++k) oacc[(tg * G + g) * D + dg * 8 + k] = o[g][k];
+    for (int o2 = 4; o2 < 32; o2 <<= 1) l_run[cc] += __shfl_xor_sync(0xffffffffu, l_run[cc], o2);
+  if (grp == 0) {
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      sm_m[warp][2 * tig + cc] = m_run[cc];
+      sm_l[warp][2 * tig + cc] = l_run[cc];
     }
+  }
+  __syncthreads();
+  float f[2];
+#pragma unroll
+  for (int cc = 0; cc < 2; ++cc) {
+    const int hd = 2 * tig + cc;
+    const float M = fmaxf(fmaxf(sm_m[0][hd], sm_m[1][hd]), fmaxf(sm_m[2][hd], sm_m[3][hd]));
+    f[cc] = (m_run[cc] == -INFINITY) ? 0.f : fast_exp2(m_run[cc] - M);
+  }
+  float* ob = obuf + warp * kMaxG * D;
+#pragma unroll
+  for (int mi = 0; mi < KS; ++mi) {
+    const int d0 = (D / 8) * grp + 2 * mi;
+    ob[(2 * tig) * D + d0] = o[mi][0] * f[0];
+    ob[(2 * tig + 1) * D + d0] = o[mi][1] * f[1];
+    ob[(2 * tig) * D + d0 + 1] = o[mi][2] * f[0];
+    ob[(2 * tig + 1) * D + d0 + 1] = o[mi][3] * f[1];
   }
   __syncthreads();
   const int64_t slot = (static_cast<int64_t>(b) * a.Hkv + h) * a.nchunks + c;
   float* wo = a.part_o + slot * kMaxG * D;
-  for (int p = tid; p < G * D; p += kTB) {
-    float sum = 0.f;
-    for (int j = 0; j < NTG; ++j) sum += oacc[j * G * D + p];
-    wo[p] = sum;
-  }
+  for (int p = tid; p < G * D; p += blockDim.x)
+    wo[p] = obuf[p] + obuf[kMaxG * D + p] + obuf[2 * kMaxG * D + p] + obuf[3 * kMaxG * D + p];
   if (tid < G) {
-    a.part_ml[(slot * kMaxG + tid) * 2] = mrun[tid];
-    a.part_ml[(slot * kMaxG + tid) * 2 + 1] = lrun[tid];
+    const float M = fmaxf(fmaxf(sm_m[0][tid], sm_m[1][tid]), fmaxf(sm_m[2][tid], sm_m[3][tid]));
+    float Ls = 0.f;
+    for (int w = 0; w < 4; ++w)
+      if (sm_m[w][tid] != -INFINITY) Ls += sm_l[w][tid] * fast_exp2(sm_m[w][tid] - M);
+    a.part_ml[(slot * kMaxG + tid) * 2] = M;
+    a.part_ml[(slot * kMaxG + tid) * 2 + 1] = Ls;
   }
 }
 
@@ -382,17 +426,7 @@ __global__ void __launch_bounds__(D) k8v4_combine_kernel(const K8V4DecodeArgs a)
 
 template <int D>
 cudaError_t launch_decode_d(const K8V4DecodeArgs& a, cudaStream_t st) {
-  constexpr int NTG = kTB / (D / 8);
-  constexpr int kStage = kTB * (D / 2 + 4);
-  const size_t dyn = std::max(static_cast<size_t>(NTG) * a.G * D * sizeof(float), static_cast<size_t>(kStage));
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k8v4_partial_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         std::max(NTG * kMaxG * D * static_cast<int>(sizeof(float)), kStage));
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  k8v4_partial_kernel<D><<<dim3(a.nchunks, a.Hkv, a.B), kTB, dyn, st>>>(a);
+  k8v4_partial_kernel<D><<<dim3(a.nchunks, a.Hkv, a.B), 128, 0, st>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   k8v4_combine_kernel<D><<<dim3(a.Hq, a.B), D, 0, st>>>(a);
