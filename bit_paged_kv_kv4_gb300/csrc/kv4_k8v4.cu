@@ -190,8 +190,11 @@ __global__ void __launch_bounds__(128) k8v4_partial_kernel(const K8V4DecodeArgs 
   constexpr int KSEG = D / 4;                 // key bytes per lane and token
   constexpr int VSEG = D / 16;                // value bytes per lane and token
   __shared__ float qsh[kMaxG * D];
-  __shared__ float obuf[4 * kMaxG * D];
+  __shared__ __align__(16) float obuf[4 * kMaxG * D];
   __shared__ float sm_m[4][kMaxG], sm_l[4][kMaxG];
+  // per k-step and lane: q hi b0, b1, lo b0, b1 -- read only inside the token
+  // loop, so it shares bytes with obuf, written only after every warp's loop
+  uint4* qfrag = reinterpret_cast<uint4*>(obuf);
 
   const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int G = a.G, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -208,21 +211,26 @@ __global__ void __launch_bounds__(128) k8v4_partial_kernel(const K8V4DecodeArgs 
   }
   fwht_smem<D>(qsh, G, 1.0f);
   // The rotated q is an FP32 result: split it into f16 hi + lo parts (two
-  // MMAs per k-step), so the scores keep FP32-level accuracy.
-  uint32_t qb[2 * KS], ql[2 * KS];
+  // MMAs per k-step), so the scores keep FP32-level accuracy.  The B
+  // fragments go to shared memory (one 16-byte load per k-step later).
+  if (warp == 0) {
 #pragma unroll
-  for (int j = 0; j < KS; ++j) {
-    const int d = KSEG * tig + 4 * j;
-    const float* qq = qsh + grp * D + d;
-    const bool hv = grp < G;
+    for (int j = 0; j < KS; ++j) {
+      const int d = KSEG * tig + 4 * j;
+      const float* qq = qsh + grp * D + d;
+      const bool hv = grp < G;
+      uint32_t f[4];
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const uint32_t hi = hv ? pack_f16x2(qq[2 * e], qq[2 * e + 1]) : 0u;
-      const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi));
-      qb[2 * j + e] = hi;
-      ql[2 * j + e] = hv ? pack_f16x2(qq[2 * e] - hf.x, qq[2 * e + 1] - hf.y) : 0u;
+      for (int e = 0; e < 2; ++e) {
+        const uint32_t hi = hv ? pack_f16x2(qq[2 * e], qq[2 * e + 1]) : 0u;
+        const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+        f[e] = hi;
+        f[2 + e] = hv ? pack_f16x2(qq[2 * e] - hf.x, qq[2 * e + 1] - hf.y) : 0u;
+      }
+      qfrag[j * 32 + lane] = make_uint4(f[0], f[1], f[2], f[3]);
     }
   }
+  __syncthreads();
   const float qk_scale = a.sm_scale * __ldg(a.s_k) * kLog2e;
 
   const int32_t* bt = a.block_table + static_cast<int64_t>(b) * a.max_pages;
@@ -243,33 +251,35 @@ __global__ void __launch_bounds__(128) k8v4_partial_kernel(const K8V4DecodeArgs 
 #pragma unroll
   for (int mi = 0; mi < KS; ++mi) o[mi][0] = o[mi][1] = o[mi][2] = o[mi][3] = 0.f;
 
-  for (int t0 = t_begin + 16 * warp; t0 < t_end; t0 += 64) {
-    // ---- loads: key segments of tokens grp, grp+8 (+ their value scales);
-    //      value segments of tokens 2tig, 2tig+1, 2tig+8, 2tig+9
+  // ---- loads of one tile: key segments of tokens grp, grp+8 (+ their value
+  //      scales); value segments of tokens 2tig, 2tig+1, 2tig+8, 2tig+9
+  struct Tile {
     uint32_t kw[2][KS];
+    uint32_t vw[4][(VSEG + 3) / 4];
     float sv[2];
     bool kval[2];
+  };
+  auto load_tile = [&](int t0, Tile& T) {
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       const int t = t0 + grp + 8 * r;
       const uint8_t* ch = chunk_of(t);
-      kval[r] = ch != nullptr;
-      sv[r] = 0.f;
-      if (kval[r]) {
+      T.kval[r] = ch != nullptr;
+      T.sv[r] = 0.f;
+      if (T.kval[r]) {
         const int off = t % a.P;
         const uint4* src = reinterpret_cast<const uint4*>(ch + static_cast<int64_t>(off) * D + KSEG * tig);
 #pragma unroll
         for (int u = 0; u < KS / 4; ++u) {
           const uint4 w = __ldg(src + u);
-          kw[r][4 * u] = w.x; kw[r][4 * u + 1] = w.y; kw[r][4 * u + 2] = w.z; kw[r][4 * u + 3] = w.w;
+          T.kw[r][4 * u] = w.x; T.kw[r][4 * u + 1] = w.y; T.kw[r][4 * u + 2] = w.z; T.kw[r][4 * u + 3] = w.w;
         }
-        sv[r] = __ldg(reinterpret_cast<const float*>(ch + vsc0 + 4 * off));
+        T.sv[r] = __ldg(reinterpret_cast<const float*>(ch + vsc0 + 4 * off));
       } else {
 #pragma unroll
-        for (int j = 0; j < KS; ++j) kw[r][j] = 0u;
+        for (int j = 0; j < KS; ++j) T.kw[r][j] = 0u;
       }
     }
-    uint32_t vw[4][(VSEG + 3) / 4];           // tokens 2tig, 2tig+1, 2tig+8, 2tig+9
 #pragma unroll
     for (int q4 = 0; q4 < 4; ++q4) {
       const int t = t0 + 2 * tig + (q4 & 1) + 8 * (q4 >> 1);
@@ -277,15 +287,25 @@ __global__ void __launch_bounds__(128) k8v4_partial_kernel(const K8V4DecodeArgs 
       const uint8_t* src = ch ? ch + vcode0 + static_cast<int64_t>(t % a.P) * (D / 2) + VSEG * grp : nullptr;
       if constexpr (VSEG == 16) {
         const uint4 w = src ? __ldg(reinterpret_cast<const uint4*>(src)) : make_uint4(0u, 0u, 0u, 0u);
-        vw[q4][0] = w.x; vw[q4][1] = w.y; vw[q4][2] = w.z; vw[q4][3] = w.w;
+        T.vw[q4][0] = w.x; T.vw[q4][1] = w.y; T.vw[q4][2] = w.z; T.vw[q4][3] = w.w;
       } else if constexpr (VSEG == 8) {
         const uint2 w = src ? __ldg(reinterpret_cast<const uint2*>(src)) : make_uint2(0u, 0u);
-        vw[q4][0] = w.x; vw[q4][1] = w.y;
+        T.vw[q4][0] = w.x; T.vw[q4][1] = w.y;
       } else {
-        vw[q4][0] = src ? __ldg(reinterpret_cast<const uint32_t*>(src)) : 0u;
+        T.vw[q4][0] = src ? __ldg(reinterpret_cast<const uint32_t*>(src)) : 0u;
       }
     }
+  };
 
+  // Tile i+1's loads are issued before tile i's math.
+  Tile cur, nxt;
+  if (t_begin + 16 * warp < t_end) load_tile(t_begin + 16 * warp, cur);
+  for (int t0 = t_begin + 16 * warp; t0 < t_end; t0 += 64) {
+    if (t0 + 64 < t_end) load_tile(t0 + 64, nxt);
+    const auto& kw = cur.kw;
+    const auto& vw = cur.vw;
+    const auto& sv = cur.sv;
+    const auto& kval = cur.kval;
     // ---- S^T = K q_rot^T; acc: (token grp, heads 2tig, 2tig+1), (token grp+8, ...)
     float sacc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -293,8 +313,9 @@ __global__ void __launch_bounds__(128) k8v4_partial_kernel(const K8V4DecodeArgs 
       uint32_t a0, a1, a2, a3;
       e4m3x4_to_f16x2x2(kw[0][j], a0, a2);
       e4m3x4_to_f16x2x2(kw[1][j], a1, a3);
-      mma_f16_16816(sacc, a0, a1, a2, a3, qb[2 * j], qb[2 * j + 1]);
-      mma_f16_16816(sacc, a0, a1, a2, a3, ql[2 * j], ql[2 * j + 1]);
+      const uint4 qf = qfrag[j * 32 + lane];
+      mma_f16_16816(sacc, a0, a1, a2, a3, qf.x, qf.y);
+      mma_f16_16816(sacc, a0, a1, a2, a3, qf.z, qf.w);
     }
 
     // ---- online softmax (base 2) for heads 2tig + cc
@@ -352,6 +373,7 @@ __global__ void __launch_bounds__(128) k8v4_partial_kernel(const K8V4DecodeArgs 
       mma_f16_16816(o[mi], a0, a1, a2, a3, pb[0], pb[1]);
       mma_f16_16816(o[mi], a0, a1, a2, a3, pl[0], pl[1]);
     }
+    cur = nxt;
   }
 
   // ---- merge the 4 warps: row sums over the grp lanes, then in shared memory
