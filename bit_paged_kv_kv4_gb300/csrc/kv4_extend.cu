@@ -565,11 +565,15 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const ExtendArgs a)
 template <int D>
 cudaError_t launch_d(const ExtendArgs& a, cudaStream_t st) {
   using Gm = ExtGeo<D>;
-  static bool attr = false;
-  if (!attr) {
+  // the shared-memory opt-in is per device; set it once per device (always
+  // beyond the first 64 ids), racing threads set the same value
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(extend_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM);
     if (e != cudaSuccess) return e;
-    attr = true;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   const dim3 grid(a.Hq, (a.max_chunk_len + kQT - 1) / kQT, a.B);
   extend_kernel<D><<<grid, kThreads, Gm::SMEM, st>>>(a);
