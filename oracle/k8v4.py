@@ -25,6 +25,10 @@ layout and no value encoder; the readings here:
   [K codes P*D][V codes P*D/2][V scales FP32 * P], rows per token.
 * Decode: q is rotated too (q_rot = H q), so q_rot . k_rot = q . k before
   quantisation; the output is o = H (sum_t p_t v_hat_rot_t).  In float64.
+
+Parity unpinned for the value encoder and the chunk layout (readings the
+page does not fix); every function below is pinned against something other
+than itself in ``tests/test_oracle_k8v4.py``.
 """
 import numpy as np
 
