@@ -1,0 +1,43 @@
+"""Host-side logic with no GPU: the decode-source hash that keys recorded
+ncu traffic, the FP8 input generator, and the k8v4 workspace sizing."""
+import numpy as np
+import torch
+
+import bench
+import workloads as W
+
+
+def test_decode_hash_ignores_comments_and_blank_space(tmp_path, monkeypatch):
+    src = tmp_path / "bit_paged_kv_kv4_gb300" / "csrc"
+    src.mkdir(parents=True)
+    (src / "kv4_decode.cu").write_text("int f(int x) { return x + 1; }  // one\n/* block */\n")
+    (src / "kv4_device.cuh").write_text("#pragma once\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.decode_source_hash()
+    (src / "kv4_decode.cu").write_text("int f(int x) {\n  return x + 1;  // two\n}\n")
+    assert bench.decode_source_hash() == h0                 # comments and layout only
+    (src / "kv4_decode.cu").write_text("int f(int x) { return x + 2; }\n")
+    assert bench.decode_source_hash() != h0                 # code changed
+
+
+def test_fp8_kv_codes_saturate_and_repeat():
+    a, s = W.fp8_kv_codes(3, 50, 2, 64, "cpu", [[1], [7]], 30.0)
+    b, _ = W.fp8_kv_codes(3, 50, 2, 64, "cpu", [[1], [7]], 30.0)
+    assert torch.equal(a, b)                                 # seeded
+    assert a.dtype == torch.uint8 and a.shape == (2, 50, 2, 64)
+    codes = a.numpy()
+    assert not np.any((codes & 0x7F) == 0x7F)                # no NaN code
+    # scales from the draws' maxima: the largest magnitude encodes to 448
+    assert np.any((codes & 0x7F) == 0x7E)
+    # fixed scales smaller than the data saturate instead of producing NaN
+    c, _ = W.fp8_kv_codes(4, 50, 2, 64, "cpu", scales=np.array([1e-3, 1e-3], np.float32))
+    assert not np.any((c.numpy() & 0x7F) == 0x7F)
+
+
+def test_k8v4_workspace_sizing():
+    import bit_paged_kv_kv4_gb300 as K
+    n = K.kv4_k8v4_workspace_bytes(16, 4, 256, 19)
+    slots = 16 * 4 * 19
+    o_bytes = slots * 8 * 256 * 4
+    assert n == ((o_bytes + 255) // 256) * 256 + slots * 8 * 2 * 4
+    assert K.kv4_k8v4_workspace_bytes(2, 2, 64, 0) == 0     # no chunks: nothing to size
