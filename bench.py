@@ -508,6 +508,7 @@ def kv4_arm(args):
             del sx
             torch.cuda.empty_cache()
         extra["calibrate_64k"] = time_calibrate(device, peak)
+        extra["write_prefill_8k_int4"] = time_write_int4(device, peak)
         # the k8v4 variant on the headline shapes: FP8 keys, 4-bit values, rotated
         extra["k8v4_32k"] = time_k8v4(device, W.ALL["nvfp4_32k"], peak)
         torch.cuda.empty_cache()
@@ -664,6 +665,35 @@ def time_k8v4(device, w, peak, reps=20):
             "num_chunks": chunks, "kv_bytes": byts, "tokens_per_s_16_layers": B / (16 * med)}
 
 
+def time_write_int4(device, peak, T=8192):
+    """Prefill write of T bf16 tokens into an INT4 per-token-head pool with the
+    shapes of the 220K INT4 workload (Hkv 2, D 256, 1600-token pages)."""
+    import torch
+    import bit_paged_kv_kv4_gb300 as K
+    w = W.ALL["int4_220k"]
+    gen = torch.Generator(device=device).manual_seed(13)
+    k = torch.randn((T, w.num_kv_heads, w.head_dim), generator=gen, device=device).to(torch.bfloat16)
+    v = torch.randn((T, w.num_kv_heads, w.head_dim), generator=gen, device=device).to(torch.bfloat16)
+    pool = K.Pool("int4", (T + w.page_size - 1) // w.page_size, w.page_size, w.num_kv_heads, w.head_dim,
+                  device=device)
+    slots = torch.arange(T, dtype=torch.int64, device=device)
+    for _ in range(3):
+        K.kv4_write(k, v, slots, pool, None)
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(10):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        K.kv4_write(k, v, slots, pool, None)
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b) * 1e-3)
+    med = statistics.median(ts)
+    byts = algorithmic_write_bytes(w, T)
+    return {"tokens": T, "us": med * 1e6, "gbs": byts / med / 1e9, "frac": byts / med / 1e9 / peak,
+            "note": "8 MB in, 4.3 MB out: smaller than L2, so this is an L2-warm figure"}
+
+
 def time_calibrate(device, peak, T=65536, Hkv=4, D=256):
     """Serving-time NVFP4 global-scale calibration over the K and V of T
     tokens (bf16, 2 x 134 MB: larger than L2, so an HBM figure)."""
@@ -780,6 +810,7 @@ def only_arm(args):
         lite = types.SimpleNamespace(device=device, K=K,
                                      g=torch.tensor([1.0 / (6 * 448)] * 2, dtype=torch.float32, device=device))
         r = time_write_prefill(lite, w, peak)
+        r["int4"] = time_write_int4(device, peak)
     if K.kv4_device_error() != 0:
         raise SystemExit(f"device error {K.kv4_device_error()}")
     print(json.dumps({"only": args.only, "workload": w.name, **r}))
