@@ -177,3 +177,12 @@ def test_k8v4_validation_without_gpu(lib):
     assert lib.kv4_k8v4_workspace_bytes(2, 2, 256, 4) > 2 * 2 * 4 * 8 * 256 * 4
     nv = desc(fmt=0, base=1 << 20)
     assert lib.kv4_k8v4_write(fake, fake, fake, 4, ctypes.byref(nv), fake, None) == 1
+
+
+def test_every_declared_function_has_a_binding_signature():
+    """The binding declares argument and result types for every C entry point
+    of the header (an undeclared one would be called with ctypes' defaults)."""
+    import inspect
+    src = inspect.getsource(K._load)
+    for name in declared_functions():
+        assert f'"{name}"' in src, name
