@@ -152,6 +152,41 @@ int64_t align256(int64_t x) { return (x + 255) / 256 * 256; }
 
 void kv4::set_error_message(const char* msg) { g_msg = msg; }
 
+// Every argument check of kv4_decode_attention except the workspace's; shared
+// with the static-workspace entry point so both report the same errors.
+kv4_status kv4::check_decode_args(const void* q, const kv4_pool* pool,
+                                  const float* layer_global_scale, const int32_t* block_table,
+                                  int32_t max_pages, const int32_t* seq_lens, int32_t batch,
+                                  int32_t num_q_heads, float sm_scale, int32_t num_splits,
+                                  const void* out) {
+  kv4_status s = check_pool(pool);
+  if (s != KV4_OK) return s;
+  if ((s = check_pool_base(pool)) != KV4_OK) return s;
+  if (pool->fmt == KV4_K8V4)
+    return fail(KV4_EUNSUPPORTED, "a k8v4 pool is read by kv4_k8v4_decode_attention");
+  if (batch < 0) return fail(KV4_EINVAL, "batch < 0");
+  if (num_q_heads < 1 || num_q_heads % pool->num_kv_heads != 0)
+    return fail(KV4_EINVAL, "num_q_heads %d is not a positive multiple of num_kv_heads %d",
+                num_q_heads, pool->num_kv_heads);
+  if (max_pages < 1) return fail(KV4_EINVAL, "max_pages must be >= 1");
+  if (static_cast<int64_t>(max_pages) * pool->page_size >= (int64_t{1} << 31))
+    return fail(KV4_EINVAL, "max_pages * page_size must be < 2^31");
+  if (num_splits < 0 || num_splits > 1024) return fail(KV4_EINVAL, "num_splits must be in [0, 1024]");
+  if (!(sm_scale == sm_scale) || sm_scale > 3.0e38f || sm_scale < -3.0e38f)
+    return fail(KV4_EINVAL, "sm_scale must be finite");
+  if (batch == 0) return KV4_OK;
+  if (q == nullptr || out == nullptr || block_table == nullptr || seq_lens == nullptr)
+    return fail(KV4_EINVAL, "q, out, block_table and seq_lens must be non-NULL");
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
+    return fail(KV4_EINVAL, "q and out must be 16-byte aligned");
+  if (pool->fmt != KV4_INT4_PTH && layer_global_scale == nullptr)
+    return fail(KV4_EINVAL, "NVFP4 and FP8 need layer_global_scale");
+  const int G = num_q_heads / pool->num_kv_heads;
+  if (batch > 65535 || static_cast<int64_t>(pool->num_kv_heads) * ((G + 7) / 8) > 65535)
+    return fail(KV4_EINVAL, "batch or heads exceed the launch grid");
+  return KV4_OK;
+}
+
 extern "C" {
 
 int64_t kv4_pool_chunk_bytes(const kv4_pool* pool) {
@@ -244,31 +279,10 @@ kv4_status kv4_decode_attention(const void* q, const kv4_pool* pool,
                                 void* workspace, int64_t workspace_bytes, void* out,
                                 int32_t out_is_fp32, void* stream) {
   g_msg.clear();
-  kv4_status s = check_pool(pool);
-  if (s != KV4_OK) return s;
-  if ((s = check_pool_base(pool)) != KV4_OK) return s;
-  if (pool->fmt == KV4_K8V4)
-    return fail(KV4_EUNSUPPORTED, "a k8v4 pool is read by kv4_k8v4_decode_attention");
-  if (batch < 0) return fail(KV4_EINVAL, "batch < 0");
-  if (num_q_heads < 1 || num_q_heads % pool->num_kv_heads != 0)
-    return fail(KV4_EINVAL, "num_q_heads %d is not a positive multiple of num_kv_heads %d",
-                num_q_heads, pool->num_kv_heads);
-  if (max_pages < 1) return fail(KV4_EINVAL, "max_pages must be >= 1");
-  if (static_cast<int64_t>(max_pages) * pool->page_size >= (int64_t{1} << 31))
-    return fail(KV4_EINVAL, "max_pages * page_size must be < 2^31");
-  if (num_splits < 0 || num_splits > 1024) return fail(KV4_EINVAL, "num_splits must be in [0, 1024]");
-  if (!(sm_scale == sm_scale) || sm_scale > 3.0e38f || sm_scale < -3.0e38f)
-    return fail(KV4_EINVAL, "sm_scale must be finite");
-  if (batch == 0) return KV4_OK;
-  if (q == nullptr || out == nullptr || block_table == nullptr || seq_lens == nullptr)
-    return fail(KV4_EINVAL, "q, out, block_table and seq_lens must be non-NULL");
-  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
-    return fail(KV4_EINVAL, "q and out must be 16-byte aligned");
-  if (pool->fmt != KV4_INT4_PTH && layer_global_scale == nullptr)
-    return fail(KV4_EINVAL, "NVFP4 and FP8 need layer_global_scale");
+  kv4_status s = kv4::check_decode_args(q, pool, layer_global_scale, block_table, max_pages,
+                                        seq_lens, batch, num_q_heads, sm_scale, num_splits, out);
+  if (s != KV4_OK || batch == 0) return s;
   const int G = num_q_heads / pool->num_kv_heads;
-  if (batch > 65535 || static_cast<int64_t>(pool->num_kv_heads) * ((G + 7) / 8) > 65535)
-    return fail(KV4_EINVAL, "batch or heads exceed the launch grid");
   const int64_t need = kv4_decode_workspace_bytes(batch, num_q_heads, pool->head_dim, num_splits);
   if (need > 0) {
     if (workspace == nullptr || workspace_bytes < need)

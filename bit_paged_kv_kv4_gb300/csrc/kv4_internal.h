@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
+#include "../../include/kv4.h"
+
 namespace kv4 {
 
 // Division of n < 2^31 by a fixed d in [1, 2^31) with one multiply-high, an
@@ -146,5 +148,11 @@ int decode_tile_tokens(int fmt);
 // Sets the message kv4_last_error_message() returns on this thread.
 void set_error_message(const char* msg);
 int decode_ctas_per_sm();
+// Every argument check of kv4_decode_attention except those of the workspace
+// (the message goes to kv4_last_error_message); KV4_OK when all pass.
+kv4_status check_decode_args(const void* q, const kv4_pool* pool, const float* layer_global_scale,
+                             const int32_t* block_table, int32_t max_pages, const int32_t* seq_lens,
+                             int32_t batch, int32_t num_q_heads, float sm_scale, int32_t num_splits,
+                             const void* out);
 
 }  // namespace kv4

@@ -15,7 +15,10 @@
 //  * Host code cannot pass `kScratch` itself to a kernel (on the host it names
 //    a stand-in, not the device copy), so the first call on each device looks up
 //    the device address with cudaGetSymbolAddress while that device is current
-//    and caches it.  Make that first call before any stream capture.
+//    and caches it.  Make that first call before any stream capture.  The
+//    cached address belongs to the device's context of that moment:
+//    cudaDeviceReset discards it with the rest of the library's device state,
+//    so a process that resets a device must not call here on it again.
 //  * Every call shares the one array and it keeps the last call's contents.
 //    Nothing in it has to start at zero: each call writes every partial before
 //    the combine step reads it.  Calls whose kernels overlap on the GPU (two
@@ -74,12 +77,12 @@ kv4_status kv4_decode_attention_static_ws(const void* q, const kv4_pool* pool,
                                           int32_t num_q_heads, float sm_scale,
                                           int32_t num_splits, void* out, int32_t out_is_fp32,
                                           void* stream) {
-  if (pool == nullptr || kv4_pool_bytes(pool) == 0 || num_splits < 0 || num_splits > 1024 ||
-      batch < 0 || max_pages < 1 || num_q_heads < 1)
-    // the regular entry point reports the precise argument error
-    return kv4_decode_attention(q, pool, layer_global_scale, block_table, max_pages, seq_lens,
-                                batch, num_q_heads, sm_scale, num_splits, nullptr, 0, out,
-                                out_is_fp32, stream);
+  // the argument checks of kv4_decode_attention come first, so an invalid call
+  // gets the same precise message as there, not the scratch-size one below
+  kv4::set_error_message("");
+  kv4_status s = kv4::check_decode_args(q, pool, layer_global_scale, block_table, max_pages,
+                                        seq_lens, batch, num_q_heads, sm_scale, num_splits, out);
+  if (s != KV4_OK || batch == 0) return s;
   const int64_t need = kv4_decode_workspace_bytes(batch, num_q_heads, pool->head_dim, num_splits);
   if (need > kKv4StaticWorkspaceBytes) {
     char buf[256];
@@ -93,7 +96,7 @@ kv4_status kv4_decode_attention_static_ws(const void* q, const kv4_pool* pool,
   }
   void* ws = nullptr;
   if (need > 0) {
-    kv4_status s = scratch_address(&ws);
+    s = scratch_address(&ws);
     if (s != KV4_OK) return s;
   }
   return kv4_decode_attention(q, pool, layer_global_scale, block_table, max_pages, seq_lens,

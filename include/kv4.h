@@ -291,7 +291,12 @@ kv4_status kv4_calibrate_global_scale(const void* k, const void* v, int64_t num_
  *     launches nothing.  num_splits == 1 needs no scratch at all.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and keeps it; make that
- *     first call before any stream capture.
+ *     first call before any stream capture.  The kept address belongs to the
+ *     device's context of that moment: cudaDeviceReset discards it together
+ *     with the rest of the library's device state, so a process that resets a
+ *     device must not call into the library on that device again.
+ *   - Invalid arguments get the same status and message as from
+ *     kv4_decode_attention; the scratch size is checked after them.
  *   - All calls share the one array and it keeps the last call's contents.
  *     Nothing in it needs to start at zero (each call writes every partial
  *     before reading it), but calls whose kernels overlap on the GPU -- on two

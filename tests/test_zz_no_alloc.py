@@ -4,10 +4,12 @@ or a loop that cannot take an allocation's synchronisation).  Its split
 scratch is the library's fixed 8 MiB device array instead of a caller
 workspace.
 
-Checked through the C ABI on a GPU: two calls in a row match the regular
-entry point (same split count) within the parity tolerance of the other
-decode tests, and a request too large for the array is refused without a
-launch.  This file is collected last on purpose, and also passes on its own.
+Checked through the C ABI on a GPU: two calls in a row give bitwise the
+output of the regular entry point with the same split count, and both stay
+within the decode parity gate of the FP64 oracle; a request too large for
+the array is refused without a launch, and an invalid argument gets the
+regular entry point's own message.  This file is collected last on purpose,
+and also passes on its own.
 """
 import ctypes
 
@@ -36,6 +38,7 @@ def test_static_workspace_matches_regular_entry_point_twice(fmt):
     pool = c.gpu_pool()
     S = 9
     ref = c.gpu_out(pool, num_splits=S).cpu().numpy()
+    want = c.oracle_out()
     q = dev_bf16(c.q)
     table = torch.from_numpy(c.table).cuda()
     lens = torch.from_numpy(c.lens).cuda()
@@ -46,7 +49,8 @@ def test_static_workspace_matches_regular_entry_point_twice(fmt):
         torch.cuda.synchronize()
         assert K.kv4_device_error() == 0
         got = out.cpu().numpy()
-        check_close(got, ref, atol=ATOL, what=f"static workspace, call {call + 1}")
+        assert np.array_equal(got, ref), f"static workspace, call {call + 1}: not bitwise equal"
+        check_close(got, want, atol=ATOL, what=f"static workspace vs oracle, call {call + 1}")
 
 
 def test_static_workspace_refuses_oversized_requests():
@@ -63,3 +67,22 @@ def test_static_workspace_refuses_oversized_requests():
     assert "8388608" in msg and "static workspace" in msg
     torch.cuda.synchronize()
     assert float(out.abs().sum()) == 0.0                # nothing was launched
+
+
+def test_static_workspace_reports_argument_errors_first():
+    lib = K.load(build_if_missing=True)
+    c = Case("nvfp4", 2, 6, 256, [64] * 4, 64, seed=23)
+    pool = c.gpu_pool()
+    table = torch.from_numpy(c.table).cuda()
+    lens = torch.from_numpy(c.lens).cuda()
+    out = torch.zeros((4, 6, 256), device="cuda")
+    # 7 query heads over 2 kv heads, with a split count whose scratch would
+    # not fit either: the argument error is the one reported
+    st = lib.kv4_decode_attention_static_ws(
+        ctypes.c_void_p(dev_bf16(c.q).data_ptr()), pool.ref, ctypes.c_void_p(c.d_g.data_ptr()),
+        ctypes.c_void_p(table.data_ptr()), table.shape[1], ctypes.c_void_p(lens.data_ptr()),
+        4, 7, float(c.sm), 1024, ctypes.c_void_p(out.data_ptr()), 1,
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 1
+    msg = lib.kv4_last_error_message().decode()
+    assert "multiple of num_kv_heads" in msg and "static workspace" not in msg
