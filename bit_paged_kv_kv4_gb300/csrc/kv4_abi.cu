@@ -146,6 +146,67 @@ kv4_status code_row_map(const kv4_pool& p, int box_rows, CUtensorMap* map) {
   return KV4_OK;
 }
 
+// The two 3-D views the NVFP4 / INT4 decode kernel loads a 16-token tile
+// through, each with one TMA copy per tile:
+//  * codes: [2 (K, V: P code rows apart)][pool_bytes / RB rows][RB bytes],
+//    box 16 rows x RB bytes x 2 (the tile's K rows, then its V rows), with the
+//    swizzle whose span is RB;
+//  * scales: [2 (K, V: P * SB bytes apart)][pool_bytes / (16 SB) rows][16 SB
+//    bytes], box 1 row x 2 (the tile's 16 K scale rows, then its V rows).
+// A chunk's scale region starts on a multiple of 16 SB bytes and a tile's
+// first token is a multiple of 16, so every coordinate is whole.
+kv4_status decode4_maps(const kv4_pool& p, CUtensorMap* codes, CUtensorMap* scales) {
+  struct Entry { const void* base; int64_t bytes; int P, D, fmt; CUtensorMap c, s; bool used; };
+  static Entry cache[8];
+  static int next = 0;
+  static std::mutex mu;
+  const int64_t bytes = static_cast<int64_t>(p.num_pages) * p.num_kv_heads * chunk_bytes_of(p);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (auto& e : cache)
+      if (e.used && e.base == p.base && e.bytes == bytes && e.P == p.page_size && e.D == p.head_dim &&
+          e.fmt == p.fmt) {
+        *codes = e.c;
+        *scales = e.s;
+        return KV4_OK;
+      }
+  }
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return fail(KV4_ECUDA, "cuTensorMapEncodeTiled is not available");
+  const int rb = p.head_dim / 2;
+  const int sb = p.fmt == KV4_NVFP4 ? p.head_dim / 16 : 4;
+  const int srow = 16 * sb;
+  if ((bytes / srow) >= (int64_t{1} << 31))
+    return fail(KV4_EUNSUPPORTED, "pool of %lld bytes exceeds the 2^31 scale rows a TMA "
+                "coordinate addresses", static_cast<long long>(bytes));
+  const CUtensorMapSwizzle sw = rb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : rb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                           : CU_TENSOR_MAP_SWIZZLE_32B;
+  cuuint32_t estr[3] = {1, 1, 1};
+  {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(rb), static_cast<cuuint64_t>(bytes / rb), 2};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(rb), static_cast<cuuint64_t>(p.page_size) * rb};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(rb), 16, 2};
+    CUresult r = fn(codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, p.base, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(KV4_ECUDA, "cuTensorMapEncodeTiled (codes) failed (%d)", static_cast<int>(r));
+  }
+  {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(srow), static_cast<cuuint64_t>(bytes / srow), 2};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(srow), static_cast<cuuint64_t>(p.page_size) * sb};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(srow), 1, 2};
+    CUresult r = fn(scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, p.base, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(KV4_ECUDA, "cuTensorMapEncodeTiled (scales) failed (%d)", static_cast<int>(r));
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  cache[next] = Entry{p.base, bytes, p.page_size, p.head_dim, p.fmt, *codes, *scales, true};
+  next = (next + 1) % 8;
+  return KV4_OK;
+}
+
 int64_t align256(int64_t x) { return (x + 255) / 256 * 256; }
 
 }  // namespace
@@ -267,7 +328,7 @@ int64_t kv4_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t h
   if (num_splits == 1 || batch == 0) return 0;        // one CTA per unit writes `out` directly
   const int64_t S = num_splits == 0 ? 1 : num_splits;
   // units (request, kv head, slice of <= 8 query heads) number at most batch * num_q_heads
-  const int64_t slots = static_cast<int64_t>(sm_count()) * kv4::decode_ctas_per_sm() +
+  const int64_t slots = static_cast<int64_t>(sm_count()) * kv4::decode_max_ctas_per_sm() +
                         static_cast<int64_t>(batch) * num_q_heads * S;
   return align256((batch + 1) * 8) + align256(slots * 8 * 16) + slots * 8 * head_dim * 4;
 }
@@ -319,13 +380,16 @@ kv4_status kv4_decode_attention(const void* q, const kv4_pool* pool,
     const int64_t tiles_max = units * ((static_cast<int64_t>(max_pages) * pool->page_size +
                                         kv4::decode_tile_tokens(pool->fmt) - 1) /
                                        kv4::decode_tile_tokens(pool->fmt));
-    const int64_t resident = static_cast<int64_t>(sm_count()) * kv4::decode_ctas_per_sm();
-    int64_t n = (tiles_max + 3) / 4;
+    const int64_t resident = static_cast<int64_t>(sm_count()) * kv4::decode_ctas_per_sm(pool->fmt);
+    // at least a few tiles per compute warp
+    const int64_t min_tiles = pool->fmt == KV4_FP8 ? 4 : 12;
+    int64_t n = (tiles_max + min_tiles - 1) / min_tiles;
     n = n < 1 ? 1 : (n > resident ? resident : n);
     a.num_splits = num_splits == 0 ? 1 : num_splits;
     a.unit_ctas = 0;
     a.n_cta = static_cast<int>(n);
-    const int64_t slots = resident + static_cast<int64_t>(batch) * num_q_heads * a.num_splits;
+    const int64_t slots = static_cast<int64_t>(sm_count()) * kv4::decode_max_ctas_per_sm() +
+                          static_cast<int64_t>(batch) * num_q_heads * a.num_splits;
     uint8_t* w = static_cast<uint8_t*>(workspace);
     a.cum = reinterpret_cast<int64_t*>(w);
     a.part_ml = reinterpret_cast<float*>(w + align256((batch + 1) * 8));
@@ -336,12 +400,17 @@ kv4_status kv4_decode_attention(const void* q, const kv4_pool* pool,
   a.err = error_word();
   if (a.err == nullptr) return fail(KV4_ECUDA, "no CUDA device / error word unavailable");
   a.tile = kv4::decode_tile_tokens(pool->fmt);
-  // a tile is one box, or two when 32 does not divide P; an FP8 tile of 16
-  // tokens is 32 code rows
-  a.box_rows = (pool->fmt == KV4_FP8 || pool->page_size % 32 == 0) ? 32 : 16;
-  CUtensorMap map;
-  if ((s = code_row_map(*pool, a.box_rows, &map)) != KV4_OK) return s;
-  cudaError_t e = kv4::launch_decode(a, map, static_cast<cudaStream_t>(stream));
+  // a tile is 16 tokens: one box of 16 code rows (NVFP4, INT4) or 32 (FP8,
+  // two code rows a token)
+  a.box_rows = pool->fmt == KV4_FP8 ? 32 : 16;
+  CUtensorMap map, map2;
+  if (pool->fmt == KV4_FP8) {
+    if ((s = code_row_map(*pool, a.box_rows, &map)) != KV4_OK) return s;
+    map2 = map;
+  } else if ((s = decode4_maps(*pool, &map, &map2)) != KV4_OK) {
+    return s;
+  }
+  cudaError_t e = kv4::launch_decode(a, map, map2, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KV4_OK : cuda_fail(e, "kv4_decode_attention launch");
 }
 

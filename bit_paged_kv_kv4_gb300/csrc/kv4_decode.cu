@@ -1089,30 +1089,24 @@ static cudaError_t launch_split(const DecodeArgs& a, const CUtensorMap& map, cud
   return launch_pdl(k, dim3(a.n_cta), dim3(kNW * 32), Gm::SMEM, st, a, map);
 }
 
-int decode_tile_tokens(int fmt) { return fmt == KV4_FP8 ? Geo<256, KV4_FP8>::TT : Geo<256, KV4_NVFP4>::TT; }
+// NVFP4 and INT4 run decode4_kernel (kv4_decode4.cu): 16-token tiles as well.
+int decode_tile_tokens(int fmt) { return Geo<256, KV4_FP8>::TT; }
 
-int decode_ctas_per_sm() { return kCtasPerSm; }
+int decode_ctas_per_sm(int fmt) { return fmt == KV4_FP8 ? kCtasPerSm : decode4_ctas_per_sm(); }
 
-cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& map, cudaStream_t st) {
+int decode_max_ctas_per_sm() { return kCtasPerSm > decode4_ctas_per_sm() ? kCtasPerSm : decode4_ctas_per_sm(); }
+
+cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& map, const CUtensorMap& smap,
+                          cudaStream_t st) {
   cudaError_t e;
-  if (a.fmt == KV4_NVFP4) {
-    switch (a.D) {
-      case 64: e = launch_split<64, KV4_NVFP4>(a, map, st); break;
-      case 128: e = launch_split<128, KV4_NVFP4>(a, map, st); break;
-      default: e = launch_split<256, KV4_NVFP4>(a, map, st); break;
-    }
-  } else if (a.fmt == KV4_FP8) {
+  if (a.fmt == KV4_FP8) {
     switch (a.D) {
       case 64: e = launch_split<64, KV4_FP8>(a, map, st); break;
       case 128: e = launch_split<128, KV4_FP8>(a, map, st); break;
       default: e = launch_split<256, KV4_FP8>(a, map, st); break;
     }
   } else {
-    switch (a.D) {
-      case 64: e = launch_split<64, KV4_INT4_PTH>(a, map, st); break;
-      case 128: e = launch_split<128, KV4_INT4_PTH>(a, map, st); break;
-      default: e = launch_split<256, KV4_INT4_PTH>(a, map, st); break;
-    }
+    e = launch_decode4(a, map, smap, st);
   }
   if (e != cudaSuccess || a.unit_ctas) return e;
   return launch_pdl(combine_kernel, dim3(a.Hq, a.B), dim3(kCombineThreads), 0, st, a);

@@ -1,0 +1,824 @@
+// Paged decode attention over the NVFP4 and INT4 pools (the FP8 comparison
+// format runs the kernel in kv4_decode.cu).
+//
+// "SGLang's 4-bit KV cache", Figure 2: decode reads the 4-bit pool as it is
+// stored, block scales included, and dequantises inside the kernel; the
+// page's kernel section names the hardware E2M1 unpack and the multiply by
+// the E4M3 scales.  INT4 per-token-head follows "KV cache in 4 bits", section
+// "What we changed": one scale per token and head for K and for V.
+//
+// Work decomposition: the tile line, balanced CTA ranges, split ranges,
+// pieces and their workspace slots are those described in kv4_decode.cu, with
+// 16-token tiles (so a tile never straddles a page: P is a multiple of 16),
+// and three CTAs of four warps on each SM (at most 168 registers a thread).
+// Inside a CTA each segment (one piece) is cut into four runs of consecutive
+// tiles, one per warp; at the segment's end the warps' (m, l, O) merge in
+// shared memory in warp order (deterministic) and one piece, or the output,
+// is written.
+//
+// Per warp, per tile:
+//  * a private ring of kNS stages filled by two TMA copies a tile: one 3-D box
+//    of the tile's 16 K code rows and 16 V code rows (swizzled so the
+//    fragment reads are bank-conflict free) and one of its K and V scale rows,
+//    both completing on the stage's mbarrier.  The page of the next tile comes
+//    from a block-table cache of one page index per lane; the TMA row and
+//    the scale address of a page are computed once per page.
+//  * S^T = K q^T on the tensor cores: dequantised K is the A operand (16
+//    tokens by 16 dims per m16n8k16 MMA, two accumulation chains), the query
+//    slice the B operand, read from a per-CTA copy in shared memory.
+//  * an online softmax in base 2 whose base m rises only when a logit
+//    exceeds it by more than kLazy, so most tiles need neither a cross-lane
+//    maximum nor a rescale of O; the weights (below 2^kLazy) go to the PV MMAs
+//    as f16 hi + lo pairs (about 22 significant bits), transposed into the
+//    B-operand layout with movmatrix.  INT4's per-token V scale rides on the
+//    weight: w = p * s_V(t) / s_ref, s_ref the largest V scale seen so far
+//    (raised only when exceeded), and the piece's m_y = m_x + log2(s_ref)
+//    carries it to the merge and to the combine kernel.
+//  * O^T += V^T P^T with dequantised V^T as the A operand: NVFP4 V is stored
+//    in token pairs, so one hardware E2M1 conversion of a stored byte is one
+//    A-fragment register (two tokens of one dim), times the pair's scales.
+//
+// Every mbarrier wait is bounded (about a second); a warp that runs out
+// records KV4_ETIMEOUT, lets its copies in flight land (bounded), stops
+// streaming and keeps joining the CTA's barriers, so the CTA drains and exits.
+#include <cstdint>
+#include <utility>
+
+#include "kv4_device.cuh"
+#include "kv4_internal.h"
+
+namespace kv4 {
+
+namespace {
+
+constexpr int kNW = 4;                     // warps per CTA
+constexpr int kNS = 3;                     // ring stages per warp
+constexpr int kTT = 16;                    // tokens per tile
+constexpr int kCtas = 3;                   // resident CTAs per SM
+constexpr int kMaxSeg = 64;                // segments listed per pass
+constexpr float kLazy = 8.f;
+constexpr uint32_t kFull = 0xffffffffu;
+
+template <int D, int FMT>
+struct Geo4 {
+  static constexpr int RB = D / 2;                               // code bytes per code row
+  static constexpr int SB = (FMT == KV4_NVFP4) ? D / 16 : 4;     // scale bytes per token
+  static constexpr int KB = D / 8;                               // K code bytes per thread per token
+  static constexpr int VB = D / 16;
+  static constexpr int MT = D / 16;                              // m-tiles of PV
+  static constexpr int CS = kTT * RB;                            // K (or V) code bytes of a tile
+  static constexpr int STC = 2 * CS;                             // code stage: K box, then V box
+  static constexpr int STS = 2 * kTT * SB;                       // scale stage: K rows, then V rows
+  static constexpr int OFF_C = 0;
+  static constexpr int OFF_S = OFF_C + kNW * kNS * STC;
+  static constexpr int OFF_Q = (OFF_S + kNW * kNS * STS + 15) / 16 * 16;
+  static constexpr int QF = KB * 128;                            // query fragments (KB/4 x 32 lanes x 16 B)
+  static constexpr int AS = MT * 4 + 4;                          // merge row per lane (floats)
+  static constexpr int OFF_ACC = OFF_Q + QF;
+  static constexpr int OFF_META = OFF_ACC + 32 * AS * 4;
+  static constexpr int OFF_SEG = (OFF_META + kNW * 8 * 3 * 4 + 15) / 16 * 16;
+  static constexpr int OFF_RED = OFF_SEG + kMaxSeg * 24;
+  static constexpr int OFF_BAR = OFF_RED + kNW * 8;
+  static constexpr int SMEM = OFF_BAR + kNW * kNS * 8 + 1024;
+};
+
+struct Seg {          // one piece: tiles [t0, t0 + n) of unit u, inside split `split`
+  int u, t0, n, split, len;
+};
+
+template <int N>
+__device__ __forceinline__ void load_bytes(uint32_t a0, uint32_t* w) {
+  if constexpr (N == 16) {
+    uint4 x = lds128(a0);
+    w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
+  } else if constexpr (N == 8) {
+    uint2 x = lds64(a0);
+    w[0] = x.x; w[1] = x.y;
+  } else {
+    w[0] = lds32(a0);
+  }
+}
+
+template <int N>
+__device__ __forceinline__ uint32_t load_scale_bytes(uint32_t addr) {
+  if constexpr (N == 4) return lds32(addr);
+  else if constexpr (N == 2) return lds16(addr);
+  else return lds8(addr);
+}
+
+// INT4 two's-complement nibbles at bits 0-3 and 16-19 of `x` -> f16x2 codes.
+__device__ __forceinline__ uint32_t int4_lo_pair(uint32_t x) {
+  const uint32_t h = (x & 0x000F000Fu) ^ 0x64086408u;    // 1024 + (n ^ 8)
+  return hfma2(h, 0x3C003C00u, 0xE408E408u);              // * 1 - 1032
+}
+// INT4 nibbles at bits 4-7 and 20-23 of `x` -> f16x2 codes.
+__device__ __forceinline__ uint32_t int4_hi_pair(uint32_t x) {
+  const uint32_t h = ((x & 0x00F000F0u) ^ 0x00800080u) | 0x64006400u;  // 1024 + 16 (n ^ 8)
+  return hfma2(h, 0x2C002C00u, 0xD480D480u);              // / 16 - 72
+}
+
+__device__ __forceinline__ void store_out4(void* out, int out_f32, int64_t idx, float4 r) {
+  if (out_f32) {
+    *reinterpret_cast<float4*>(static_cast<float*>(out) + idx) = r;
+  } else {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(r.x, r.y), hi = __floats2bfloat162_rn(r.z, r.w);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + idx) = pk;
+  }
+}
+
+// seq_lens[b] clamped to [0, max_pages * P]; a value outside is recorded.
+__device__ __forceinline__ int clamp_len(const DecodeArgs& a, int b, bool flag) {
+  int L = a.seq_lens[b];
+  const int Lmax = a.max_pages * a.P;
+  if (L < 0 || L > Lmax) {
+    if (flag) set_error(a.err, KV4_EBOUNDS);
+    L = L < 0 ? 0 : Lmax;
+  }
+  return L;
+}
+
+// Exclusive prefix of `v` over the CTA's threads; `total` gets the sum.
+__device__ __forceinline__ int64_t block_scan(int64_t v, int64_t* red, int64_t& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int64_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) red[warp] = x;
+  __syncthreads();
+  int64_t before = 0;
+  total = 0;
+#pragma unroll
+  for (int w = 0; w < kNW; ++w) {
+    const int64_t t = red[w];
+    if (w < warp) before += t;
+    total += t;
+  }
+  __syncthreads();
+  return before + x - v;
+}
+
+__host__ __device__ inline int64_t part_begin4(int64_t i, int64_t total, int64_t parts) {
+  return i * total / parts;
+}
+__host__ __device__ inline int64_t part_of4(int64_t x, int64_t total, int64_t parts) {
+  return ((x + 1) * parts - 1) / total;
+}
+
+}  // namespace
+
+template <int D, int FMT>
+__global__ void __launch_bounds__(kNW * 32, kCtas)
+decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
+               const __grid_constant__ CUtensorMap smap) {
+  using Gm = Geo4<D, FMT>;
+  constexpr int RB = Gm::RB, SB = Gm::SB, KB = Gm::KB, VB = Gm::VB, MT = Gm::MT;
+  grid_dep_launch();   // the combine may be scheduled now; it waits for this grid
+  grid_dep_wait();     // inputs written by the previous kernel are visible
+  extern __shared__ uint8_t smem_raw[];
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int grp = lane >> 2, tig = lane & 3;
+  const int ngrp = (a.G + 7) >> 3;
+  const int UPB = a.Hkv * ngrp;            // units per request
+  const int S = a.num_splits;
+
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - smem_u32(smem_raw));
+  const uint32_t cring = base + Gm::OFF_C + warp * kNS * Gm::STC;      // this warp's code stages
+  const uint32_t sring = base + Gm::OFF_S + warp * kNS * Gm::STS;      // and scale stages
+  const uint32_t qsm = base + Gm::OFF_Q + lane * 16;                   // query fragment group j at + 512 j
+  float* sAcc = reinterpret_cast<float*>(gbase + Gm::OFF_ACC);
+  float* sMeta = reinterpret_cast<float*>(gbase + Gm::OFF_META);
+  Seg* sSeg = reinterpret_cast<Seg*>(gbase + Gm::OFF_SEG);
+  int64_t* sRed = reinterpret_cast<int64_t*>(gbase + Gm::OFF_RED);
+  const uint32_t bars = base + Gm::OFF_BAR + warp * kNS * 8;
+  __shared__ int s_nseg;
+  __shared__ float s_qpre;
+  __shared__ long long s_cursor, s_cum, s_b;
+
+  if (lane == 0) {
+    for (int s2 = 0; s2 < kNS; ++s2) mbar_init(bars + 8 * s2, 1);
+    fence_mbar_init();
+  }
+  if (tid == 0) {
+    prefetch_tensormap(&cmap);
+    prefetch_tensormap(&smap);
+  }
+
+  // ---- this CTA's tile range [cursor, c1) in the global (b, unit, tile) order ------
+  int64_t T = 0, c1 = 0;
+  if (a.unit_ctas) {
+    const int u = blockIdx.x, b = u / UPB;
+    const int n_u = (clamp_len(a, b, tid == 0) + kTT - 1) / kTT;
+    if (tid == 0) {
+      sSeg[0] = Seg{u, 0, n_u, 0, clamp_len(a, b, false)};
+      s_nseg = 1;
+    }
+  } else {
+    for (int b0 = 0; b0 < a.B; b0 += kNW * 32) {
+      const int b = b0 + tid;
+      const int64_t v = (b < a.B) ? static_cast<int64_t>((clamp_len(a, b, blockIdx.x == 0) + kTT - 1) / kTT) * UPB : 0;
+      int64_t tot;
+      const int64_t ex = block_scan(v, sRed, tot);
+      if (blockIdx.x == 0 && b < a.B) a.cum[b] = T + ex;        // for combine_kernel
+      T += tot;
+    }
+    if (blockIdx.x == 0 && tid == 0) a.cum[a.B] = T;
+    c1 = part_begin4(blockIdx.x + 1, T, a.n_cta);
+    if (tid == 0) s_cursor = part_begin4(blockIdx.x, T, a.n_cta);
+  }
+  __syncthreads();
+
+  // ---- per-thread shared-memory offsets inside a stage ----------------------
+  // K: bytes [KB tig, KB (tig + 1)) of token rows grp and grp + 8, in 16-byte
+  // units with their own swizzled offsets (a TMA swizzle pattern repeats every
+  // 8 rows, so row grp + 8 is the same offset plus 8 rows).
+  const uint32_t k_off0 = swz<RB>(grp, KB * tig);
+  const uint32_t k_off1 = swz<RB>(grp, KB * tig + 16);
+  const uint32_t ks_off = grp * SB + (D / 64) * tig;                 // K scale bytes of row grp
+  // NVFP4 V (token-pair rows: byte d of pair row p holds dim d of tokens 2p,
+  // 2p+1): head dims [D0, D0 + D/8) of pairs tig and tig + 4; the dim chunks
+  // go to groups in the order 4 (grp & 1) + grp/2 so the two groups of a
+  // quarter-warp read pair-row halves of opposite parity (distinct banks).
+  constexpr int D0S = D / 8;
+  const int D0 = D0S * (4 * (grp & 1) + (grp >> 1));
+  const uint32_t vp_off0 = Gm::CS + swz<RB>(2 * tig + D0 / RB, D0 % RB);
+  const uint32_t vp_off1 = Gm::CS + swz<RB>(2 * tig + D0 / RB, D0 % RB + 16);
+  const uint32_t vps_off = kTT * SB + tig * (D / 8) + 2 * (D0 / 16);
+  // INT4 V (token rows): VB bytes at VB grp of rows 2tig, 2tig+1 (+8).
+  const uint32_t v_offa = Gm::CS + swz<RB>(2 * tig, VB * grp);
+  const uint32_t v_offb = Gm::CS + swz<RB>(2 * tig + 1, VB * grp);
+
+  const uint64_t pol = policy_evict_first();
+  int issued = 0, consumed = 0;     // warp-local tile counters
+  int islot = 0, cslot = 0;         // ring slots of the next tile to issue / consume
+  uint32_t cphase = 0;              // phase parity of the consume slot's barrier
+  bool timed_out = false;
+
+  // passes over the CTA range, kMaxSeg segments at a time
+  while (true) {
+    if (!a.unit_ctas) {
+      const int64_t cur = s_cursor;
+      __syncthreads();
+      if (cur >= c1) break;
+      if (tid == 0) s_b = -1;
+      __syncthreads();
+      int64_t acc = 0;
+      for (int b0 = 0; b0 < a.B; b0 += kNW * 32) {
+        const int b = b0 + tid;
+        const int64_t v = (b < a.B) ? static_cast<int64_t>((clamp_len(a, b, false) + kTT - 1) / kTT) * UPB : 0;
+        int64_t tot;
+        const int64_t ex = acc + block_scan(v, sRed, tot);
+        if (b < a.B && v > 0 && ex <= cur && cur < ex + v) {
+          s_b = b;
+          s_cum = ex;
+        }
+        acc += tot;
+        __syncthreads();
+        if (s_b >= 0) break;
+      }
+      if (tid == 0) {
+        int64_t x = cur;
+        int b = static_cast<int>(s_b);
+        int64_t cum = s_cum;
+        int ns = 0;
+        while (x < c1 && ns < kMaxSeg && b >= 0 && b < a.B) {
+          const int n_u = (clamp_len(a, b, false) + kTT - 1) / kTT;
+          if (n_u == 0 || x >= cum + static_cast<int64_t>(n_u) * UPB) {
+            cum += static_cast<int64_t>(n_u) * UPB;
+            ++b;
+            continue;
+          }
+          const int64_t rem = x - cum;
+          const int j = static_cast<int>(rem / n_u);
+          const int t = static_cast<int>(rem % n_u);
+          const int split = static_cast<int>(part_of4(t, n_u, S));
+          const int64_t send = part_begin4(split + 1, n_u, S);
+          const int n = static_cast<int>(send - t < c1 - x ? send - t : c1 - x);
+          sSeg[ns++] = Seg{b * UPB + j, t, n, split, clamp_len(a, b, false)};
+          x += n;
+        }
+        s_nseg = ns;
+        s_cursor = (ns == 0) ? c1 : x;     // no segment found: the range is done
+      }
+      __syncthreads();
+    }
+    const int nseg = s_nseg;
+
+    // this warp's run of tiles inside segment k
+    auto my_run = [&](int k, int& beg, int& cnt) {
+      const int n = sSeg[k].n;
+      const int q = (n + kNW - 1) / kNW;
+      beg = min(n, warp * q);
+      cnt = min(n, beg + q) - beg;
+    };
+
+    // ---- issue cursor over this pass's segments, with its block-table cache ----
+    int ks = -1, io = 0, is_bg = 0, is_cn = 0, is_t0 = 0, is_h = 0;
+    int i_pass = 0, i_total = 0;
+    for (int k = 0; k < nseg; ++k) {
+      int bg, cn;
+      my_run(k, bg, cn);
+      i_total += cn;
+    }
+    int p_first = 0, p_last = -1, win = 0, pg_cur = 0, pg_nxt = 0;
+    int pi = 0, po = 0;               // page index and offset of the next tile's first token
+    int c_pi = -1;                    // page whose TMA bases are cached below
+    uint32_t c_row = 0;               // code-row index of that page-head chunk
+    uint32_t c_srow = 0;              // scale-row index (16 SB bytes a row) of its K scales
+    const int32_t* bt = a.block_table;
+
+    auto issue = [&]() {      // warp-uniform; issues the next tile of this pass
+      while (io >= is_cn) {   // enter the next segment with tiles for this warp
+        ++ks;
+        io = 0;
+        my_run(ks, is_bg, is_cn);
+        const Seg sg = sSeg[ks];
+        const int b = sg.u / UPB;
+        is_h = (sg.u % UPB) / ngrp;
+        is_t0 = sg.t0;
+        if (is_cn > 0) {        // reload the page cache for this run
+          const int tf = (sg.t0 + is_bg) * kTT;
+          pi = tf / a.P;
+          po = tf - pi * a.P;
+          p_first = pi;
+          p_last = (min(sg.len, (sg.t0 + is_bg + is_cn) * kTT) - 1) / a.P;
+          win = 0;
+          c_pi = -1;
+          bt = a.block_table + static_cast<int64_t>(b) * a.max_pages;
+          const int r0 = p_first + lane, r1 = p_first + 32 + lane;
+          pg_cur = r0 <= p_last ? __ldg(bt + r0) : 0;
+          pg_nxt = r1 <= p_last ? __ldg(bt + r1) : 0;
+        }
+      }
+      if (pi != c_pi) {       // a new page: its chunk's TMA row and scale address
+        while (((pi - p_first) >> 5) > win) {
+          ++win;
+          pg_cur = pg_nxt;
+          const int r = p_first + (win + 1) * 32 + lane;
+          pg_nxt = r <= p_last ? __ldg(bt + r) : 0;
+        }
+        const int rel = pi - p_first;
+        const int pc = __shfl_sync(kFull, pg_cur, rel & 31), pn = __shfl_sync(kFull, pg_nxt, rel & 31);
+        int page = ((rel >> 5) == win) ? pc : pn;
+        if (page < 0 || page >= a.num_pages) {
+          if (lane == 0) set_error(a.err, KV4_EBOUNDS);
+          page = 0;
+        }
+        const int64_t chunk = (static_cast<int64_t>(page) * a.Hkv + is_h) * a.chunk_bytes;
+        c_row = static_cast<uint32_t>(chunk / RB);
+        c_srow = static_cast<uint32_t>((chunk + static_cast<int64_t>(a.P) * 2 * RB) / (kTT * SB));
+        c_pi = pi;
+      }
+      if (lane == 0) {
+        const uint32_t cst = cring + islot * Gm::STC, sst = sring + islot * Gm::STS;
+        const uint32_t bar = bars + 8 * islot;
+        mbar_arrive_expect_tx(bar, kTT * (2 * RB + 2 * SB));
+        // the tile's K and V code rows (one 3-D box), then its K and V scale rows
+        tma_load_3d(cst, &cmap, 0, static_cast<int>(c_row) + po, 0, bar, pol);
+        tma_load_3d(sst, &smap, 0, static_cast<int>(c_srow) + po / kTT, 0, bar, pol);
+      }
+      islot = (islot + 1 == kNS) ? 0 : islot + 1;
+      po += kTT;                       // a tile never straddles a page: 16 divides P
+      if (po == a.P) { po = 0; ++pi; }
+      ++io;
+      ++issued;
+      ++i_pass;
+    };
+
+    for (int k0 = 0; k0 < kNS && i_pass < i_total && !timed_out; ++k0) issue();
+
+    for (int k = 0; k < nseg; ++k) {
+      const Seg sg = sSeg[k];
+      const int b = sg.u / UPB;
+      const int h = (sg.u % UPB) / ngrp;
+      const int g0 = (sg.u % ngrp) * 8;
+      const int ng = min(8, a.G - g0);
+      const int hq0 = h * a.G + g0;
+      const int L = sg.len;
+      int bg, cn;
+      my_run(k, bg, cn);
+
+      // ---- the unit's query fragments (B operand of S^T = K q^T), once per CTA ----
+      // Thread (grp, tig) of any warp uses query row g0 + grp, dims
+      // [2 KB tig, 2 KB (tig + 1)); warp 0 converts them (bf16 -> f16, |q|
+      // pre-scaled by an exact power of two into f16 range) into shared memory.
+      if (warp == 0) {
+        constexpr int NG = KB / 4;
+        uint4 raw[NG];
+        const bool row_ok = grp < ng;
+        const __nv_bfloat16* qrow = a.q + (static_cast<int64_t>(b) * a.Hq + hq0 + grp) * D + 2 * KB * tig;
+#pragma unroll
+        for (int i = 0; i < NG; ++i)
+          raw[i] = row_ok ? __ldg(reinterpret_cast<const uint4*>(qrow + 8 * i)) : make_uint4(0, 0, 0, 0);
+        float qmax = 0.f;
+#pragma unroll
+        for (int i = 0; i < NG; ++i) {
+          const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&raw[i]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 f = __bfloat1622float2(p2[j]);
+            qmax = fmaxf(qmax, fmaxf(fabsf(f.x), fabsf(f.y)));
+          }
+        }
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(kFull, qmax, o2));
+        float qpre = 1.f;
+        if (qmax > 16384.f) {
+          int e;
+          frexpf(qmax / 16384.f, &e);
+          qpre = ldexpf(1.f, -e);
+        }
+#pragma unroll
+        for (int i = 0; i < NG; ++i) {
+          float e[8];
+          const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&raw[i]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 f = __bfloat1622float2(p2[j]);
+            e[2 * j] = f.x * qpre;
+            e[2 * j + 1] = f.y * qpre;
+          }
+          uint32_t w0, w1, w2, w3;
+          if constexpr (FMT == KV4_NVFP4) {
+            // k-step: k (2tig, 2tig+1) <-> dims {0,1} of a 4-dim group, (2tig+8, +9) <-> {2,3}
+            w0 = pack_f16x2(e[0], e[1]); w1 = pack_f16x2(e[2], e[3]);
+            w2 = pack_f16x2(e[4], e[5]); w3 = pack_f16x2(e[6], e[7]);
+          } else {
+            // INT4 nibble order: (e0,e4), (e1,e5) for one k-step; (e2,e6), (e3,e7) for the next
+            w0 = pack_f16x2(e[0], e[4]); w1 = pack_f16x2(e[1], e[5]);
+            w2 = pack_f16x2(e[2], e[6]); w3 = pack_f16x2(e[3], e[7]);
+          }
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};"
+                       :: "r"(qsm + i * 512), "r"(w0), "r"(w1), "r"(w2), "r"(w3) : "memory");
+        }
+        if (lane == 0) s_qpre = qpre;
+      }
+      __syncthreads();
+      const float qk_scale = a.sm_scale * ((FMT == KV4_NVFP4) ? __ldg(a.gscale) : 1.f) * 1.4426950408889634f / s_qpre;
+
+      // ---- running softmax state, heads g0 + 2tig + c, c = 0, 1 -------------------
+      float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+      float sref = 0.f;       // INT4: largest V scale seen
+      float o[MT][4];
+#pragma unroll
+      for (int mi = 0; mi < MT; ++mi) o[mi][0] = o[mi][1] = o[mi][2] = o[mi][3] = 0.f;
+
+      for (int jt = 0; jt < cn && !timed_out; ++jt) {
+        const uint32_t st = cring + cslot * Gm::STC, sst = sring + cslot * Gm::STS;
+        if (!mbar_wait_bounded(bars + 8 * cslot, cphase)) {
+          // give the copies still in flight a bounded chance to land, then stop
+          for (int j = consumed + 1; j < issued; ++j) mbar_wait_bounded(bars + 8 * (j % kNS), (j / kNS) & 1);
+          timed_out = true;
+          break;
+        }
+        const int t0 = (sg.t0 + bg + jt) * kTT;
+        const int valid = min(kTT, L - t0);
+
+        // -------- S^T[t][g] = K q^T: 16 tokens x 8 heads, two accumulation chains --------
+        // sacc: c0 = (token grp, head 2tig), c1 = (grp, 2tig+1), c2 = (grp+8, 2tig), c3 = (grp+8, 2tig+1)
+        float sacc[2][4];
+        sacc[0][0] = sacc[0][1] = sacc[0][2] = sacc[0][3] = 0.f;
+        sacc[1][0] = sacc[1][1] = sacc[1][2] = sacc[1][3] = 0.f;
+        {
+          constexpr int W = KB / 4, CW = W < 4 ? W : 4;     // words per row, per chunk
+          uint32_t sraw[2];
+          if constexpr (FMT == KV4_NVFP4) {
+            sraw[0] = load_scale_bytes<D / 64>(sst + ks_off);
+            sraw[1] = load_scale_bytes<D / 64>(sst + ks_off + 8 * SB);
+          }
+#pragma unroll
+          for (int c0 = 0; c0 < W; c0 += CW) {
+            uint32_t kw0[CW], kw1[CW];
+            const uint32_t ko = st + (c0 ? k_off1 : k_off0);
+            load_bytes<4 * CW>(ko, kw0);
+            load_bytes<4 * CW>(ko + 8 * RB, kw1);
+            uint32_t hs[2][2];       // NVFP4: f16x2 broadcasts of blocks c0/2, c0/2 + 1 of each row
+            if constexpr (FMT == KV4_NVFP4) {
+#pragma unroll
+              for (int r = 0; r < 2; ++r)
+                e4m3x4_to_f16x2x2(prmt(sraw[r], 0u, (c0 == 0) ? 0x1100u : 0x3322u), hs[r][0], hs[r][1]);
+            }
+#pragma unroll
+            for (int jj = 0; jj < CW; ++jj) {
+              const uint4 qv = lds128(qsm + (c0 + jj) * 512);
+              if constexpr (FMT == KV4_NVFP4) {
+                uint32_t e0[4], e1[4];
+                e2m1x8_to_f16x2x4(kw0[jj], e0);
+                e2m1x8_to_f16x2x4(kw1[jj], e1);
+                const uint32_t s0 = hs[0][jj >> 1], s1 = hs[1][jj >> 1];
+                mma_f16_16816(sacc[0], hmul2(e0[0], s0), hmul2(e1[0], s1), hmul2(e0[1], s0), hmul2(e1[1], s1),
+                              qv.x, qv.y);
+                mma_f16_16816(sacc[1], hmul2(e0[2], s0), hmul2(e1[2], s1), hmul2(e0[3], s0), hmul2(e1[3], s1),
+                              qv.z, qv.w);
+              } else {
+                const uint32_t w0 = kw0[jj], w1 = kw1[jj];
+                mma_f16_16816(sacc[0], int4_lo_pair(w0), int4_lo_pair(w1), int4_hi_pair(w0), int4_hi_pair(w1),
+                              qv.x, qv.y);
+                const uint32_t y0 = w0 >> 8, y1 = w1 >> 8;
+                mma_f16_16816(sacc[1], int4_lo_pair(y0), int4_lo_pair(y1), int4_hi_pair(y0), int4_hi_pair(y1),
+                              qv.z, qv.w);
+              }
+            }
+          }
+        }
+        // x[2r + c]: token grp + 8r, head 2tig + c (base-2 logits)
+        float x[4];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          float sk = 1.f;
+          if constexpr (FMT == KV4_INT4_PTH) sk = __uint_as_float(lds32(sst + 4 * (grp + 8 * r)));
+#pragma unroll
+          for (int c = 0; c < 2; ++c) x[2 * r + c] = (sacc[0][2 * r + c] + sacc[1][2 * r + c]) * (qk_scale * sk);
+        }
+        if (valid < kTT) {
+          // tokens past the end get no weight (their rows may hold anything)
+#pragma unroll
+          for (int r = 0; r < 2; ++r)
+            if (grp + 8 * r >= valid) x[2 * r] = x[2 * r + 1] = -INFINITY;
+        }
+
+        // -------- online softmax with a lazily raised base --------
+        float corr_o[2] = {1.f, 1.f};
+        float sv[2];
+        if constexpr (FMT == KV4_INT4_PTH) {
+          float smax = 0.f;
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const int t = grp + 8 * r;
+            const float v = __uint_as_float(lds32(sst + kTT * SB + 4 * t));
+            sv[r] = (t < valid && v > 0.f) ? v : 0.f;     // NaN, <= 0 and past the end: no weight
+            smax = fmaxf(smax, sv[r]);
+          }
+          if (__any_sync(kFull, smax > sref)) {
+#pragma unroll
+            for (int o2 = 4; o2 < 32; o2 <<= 1) smax = fmaxf(smax, __shfl_xor_sync(kFull, smax, o2));
+            smax = fmaxf(smax, sref);
+            corr_o[0] = corr_o[1] = (sref > 0.f) ? sref / smax : 0.f;
+            sref = smax;
+          }
+        }
+        float tmx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
+        if (__any_sync(kFull, tmx[0] > m_run[0] + kLazy || tmx[1] > m_run[1] + kLazy)) {
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+#pragma unroll
+            for (int o2 = 4; o2 < 32; o2 <<= 1) tmx[c] = fmaxf(tmx[c], __shfl_xor_sync(kFull, tmx[c], o2));
+            const float mnew = fmaxf(m_run[c], tmx[c]);
+            if (mnew > m_run[c]) {
+              const float cr = fast_exp2(m_run[c] - mnew);     // 0 when m_run == -inf
+              l_run[c] *= cr;
+              corr_o[c] *= cr;
+              m_run[c] = mnew;
+            }
+          }
+        }
+        if (__any_sync(kFull, corr_o[0] != 1.f || corr_o[1] != 1.f)) {
+#pragma unroll
+          for (int mi = 0; mi < MT; ++mi) {
+            o[mi][0] *= corr_o[0]; o[mi][1] *= corr_o[1]; o[mi][2] *= corr_o[0]; o[mi][3] *= corr_o[1];
+          }
+        }
+        // weights and their f16 hi + lo split, transposed into the P^T B operand:
+        // b0 <- tokens (2tig, 2tig+1) of head grp, b1 <- tokens (8+2tig, 8+2tig+1)
+        uint32_t pb[2], pl[2];
+        const float inv_sref = (FMT == KV4_INT4_PTH && sref > 0.f) ? 1.f / sref : 1.f;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          float w[2];
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            // m_run is finite here: every tile has a valid first token, and the
+            // run's first tile raised it from -inf
+            const float p = fast_exp2(x[2 * r + c] - m_run[c]);
+            l_run[c] += p;
+            w[c] = p;
+            if constexpr (FMT == KV4_INT4_PTH) w[c] = p * (sv[r] * inv_sref);
+          }
+          const uint32_t hi = pack_f16x2(w[0], w[1]);
+          const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+          const uint32_t lo = pack_f16x2(w[0] - hf.x, w[1] - hf.y);
+          pb[r] = movmatrix_trans(hi);
+          pl[r] = movmatrix_trans(lo);
+        }
+
+        // -------- O^T += V^T P^T --------
+        const int ta = 2 * tig;                   // tokens ta, ta+1 (k 2tig..) and ta+8, ta+9
+        if constexpr (FMT == KV4_NVFP4) {
+          constexpr int NSB = (D0S >= 32) ? 4 : 2;
+          const uint32_t xab = load_scale_bytes<NSB>(sst + vps_off);
+          const uint32_t xcd = load_scale_bytes<NSB>(sst + vps_off + D / 2);
+          uint32_t sab[2], scd[2];
+          e4m3x4_to_f16x2x2(xab, sab[0], sab[1]);
+          e4m3x4_to_f16x2x2(xcd, scd[0], scd[1]);
+          if (valid < kTT) {
+            // a zero scale zeroes the (finite) codes of tokens past the end
+            const uint32_t mab = ((ta < valid) ? 0xFFFFu : 0u) | ((ta + 1 < valid) ? 0xFFFF0000u : 0u);
+            const uint32_t mcd = ((ta + 8 < valid) ? 0xFFFFu : 0u) | ((ta + 9 < valid) ? 0xFFFF0000u : 0u);
+            sab[0] &= mab; sab[1] &= mab;
+            scd[0] &= mcd; scd[1] &= mcd;
+          }
+          constexpr int W = D0S / 4, CW = W < 4 ? W : 4;
+#pragma unroll
+          for (int c0 = 0; c0 < W; c0 += CW) {
+            const uint32_t vo = st + (c0 ? vp_off1 : vp_off0);
+            uint32_t wab[CW], wcd[CW];
+            load_bytes<4 * CW>(vo, wab);
+            load_bytes<4 * CW>(vo + 8 * RB, wcd);
+#pragma unroll
+            for (int jj = 0; jj < CW; ++jj) {
+              const int j = c0 + jj;
+              uint32_t f[4], hh4[4];
+              e2m1x8_to_f16x2x4(wab[jj], f);
+              e2m1x8_to_f16x2x4(wcd[jj], hh4);
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                const int mi = 2 * j + hh;                 // dims D0 + 2mi, D0 + 2mi + 1
+                const int bj = (VB >= 8) ? mi / 8 : 0;     // block of this m-tile among the thread's
+                const uint32_t a0 = hmul2(f[2 * hh], sab[bj]);
+                const uint32_t a1 = hmul2(f[2 * hh + 1], sab[bj]);
+                const uint32_t a2 = hmul2(hh4[2 * hh], scd[bj]);
+                const uint32_t a3 = hmul2(hh4[2 * hh + 1], scd[bj]);
+                mma_f16_16816(o[mi], a0, a1, a2, a3, pb[0], pb[1]);
+                mma_f16_16816(o[mi], a0, a1, a2, a3, pl[0], pl[1]);
+              }
+            }
+          }
+        } else {
+          constexpr int W = VB / 4, CW = W < 2 ? W : 2;
+#pragma unroll
+          for (int c0 = 0; c0 < W; c0 += CW) {
+            uint32_t wa[CW], wb[CW], wc[CW], wd[CW];
+            load_bytes<4 * CW>(st + v_offa + 4 * c0, wa);
+            load_bytes<4 * CW>(st + v_offb + 4 * c0, wb);
+            load_bytes<4 * CW>(st + v_offa + 8 * RB + 4 * c0, wc);
+            load_bytes<4 * CW>(st + v_offb + 8 * RB + 4 * c0, wd);
+#pragma unroll
+            for (int jj = 0; jj < CW; ++jj) {
+#pragma unroll
+              for (int mm = 0; mm < 4; ++mm) {
+                const int mi = 4 * (c0 + jj) + mm;
+                const uint32_t sel = mm | (mm << 4) | ((4 + mm) << 8) | ((4 + mm) << 12);
+                const uint32_t xab = prmt(wa[jj], wb[jj], sel);
+                const uint32_t xcd = prmt(wc[jj], wd[jj], sel);
+                const uint32_t a0 = int4_lo_pair(xab), a1 = int4_hi_pair(xab);
+                const uint32_t a2 = int4_lo_pair(xcd), a3 = int4_hi_pair(xcd);
+                mma_f16_16816(o[mi], a0, a1, a2, a3, pb[0], pb[1]);
+                mma_f16_16816(o[mi], a0, a1, a2, a3, pl[0], pl[1]);
+              }
+            }
+          }
+        }
+        __syncwarp();
+        ++consumed;
+        cslot = (cslot + 1 == kNS) ? 0 : cslot + 1;
+        if (cslot == 0) cphase ^= 1u;
+        if (i_pass < i_total) issue();     // refill the stage just freed
+      }
+      // A warp that timed out stops streaming but still joins every merge below,
+      // so the CTA's barriers stay matched; its partial state is empty.
+      if (timed_out) {
+        m_run[0] = m_run[1] = -INFINITY;
+        l_run[0] = l_run[1] = 0.f;
+#pragma unroll
+        for (int mi = 0; mi < MT; ++mi) o[mi][0] = o[mi][1] = o[mi][2] = o[mi][3] = 0.f;
+      }
+
+      // ---- merge the warps' states for this segment, in warp order ------------
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+#pragma unroll
+        for (int o2 = 4; o2 < 32; o2 <<= 1) l_run[c] += __shfl_xor_sync(kFull, l_run[c], o2);
+      }
+      if (grp == 0) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          float* mt = sMeta + (warp * 8 + 2 * tig + c) * 3;
+          const bool some = l_run[c] > 0.f;
+          float my = m_run[c];
+          if constexpr (FMT == KV4_INT4_PTH) my = (sref > 0.f) ? m_run[c] + fast_log2(sref) : -INFINITY;
+          mt[0] = some ? m_run[c] : -INFINITY;
+          mt[1] = some ? my : -INFINITY;
+          mt[2] = l_run[c];
+        }
+      }
+      __syncthreads();
+      float wgt[2];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int g = 2 * tig + c;
+        float My = -INFINITY;
+        for (int w = 0; w < kNW; ++w) My = fmaxf(My, sMeta[(w * 8 + g) * 3 + 1]);
+        const float mw = sMeta[(warp * 8 + g) * 3 + 1];
+        wgt[c] = (mw == -INFINITY) ? 0.f : fast_exp2(mw - My);
+      }
+      // The merge buffer keeps the MMA fragment layout: lane L's o[mi][0..3] at
+      // sAcc[L * AS + 4 mi]; the padded row makes every float4 access
+      // conflict-free.  Warps add their scaled states in warp order.
+      for (int w = 0; w < kNW; ++w) {
+        if (warp == w) {
+          float* row = sAcc + lane * Gm::AS;
+#pragma unroll
+          for (int mi = 0; mi < MT; ++mi) {
+            float4 v = make_float4(o[mi][0] * wgt[0], o[mi][1] * wgt[1], o[mi][2] * wgt[0], o[mi][3] * wgt[1]);
+            if (w != 0) {
+              const float4 p = *reinterpret_cast<const float4*>(row + 4 * mi);
+              v.x += p.x; v.y += p.y; v.z += p.z; v.w += p.w;
+            }
+            *reinterpret_cast<float4*>(row + 4 * mi) = v;
+          }
+        }
+        __syncthreads();
+      }
+      const bool direct = a.unit_ctas || (S == 1 && sg.t0 == 0 && sg.n == (L + kTT - 1) / kTT);
+      const int64_t slot = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(sg.u) * S + sg.split;
+      for (int e = tid * 4; e < ng * D; e += kNW * 32 * 4) {
+        const int g = e / D, d = e % D;
+        float Mx = -INFINITY, My = -INFINITY;
+        for (int w = 0; w < kNW; ++w) {
+          Mx = fmaxf(Mx, sMeta[(w * 8 + g) * 3 + 0]);
+          My = fmaxf(My, sMeta[(w * 8 + g) * 3 + 1]);
+        }
+        float l = 0.f;
+        for (int w = 0; w < kNW; ++w) {
+          const float mw = sMeta[(w * 8 + g) * 3 + 0];
+          l += (mw == -INFINITY) ? 0.f : sMeta[(w * 8 + g) * 3 + 2] * fast_exp2(mw - Mx);
+        }
+        // (d, g) lives in lane (grp, tig) with tig = g/2 and grp the group that
+        // holds dim chunk q = (d/2) / VB (q for INT4, pi^-1(q) for NVFP4), in
+        // o[mi][g%2] with mi = (d/2) % VB; d+1 in o[mi][g%2 + 2]; d+2, d+3 in o[mi+1].
+        const int hd = d >> 1, mi = hd % VB, c = g & 1;
+        const int q = hd / VB, gq = (FMT == KV4_NVFP4) ? 2 * (q & 3) + (q >> 2) : q;
+        const float* row = sAcc + (gq * 4 + (g >> 1)) * Gm::AS + 4 * mi + c;
+        const float4 acc = make_float4(row[0], row[2], row[4], row[6]);
+        if (direct) {
+          const float gv = (FMT == KV4_NVFP4) ? __ldg(a.gscale + 1) : 1.f;
+          const float inv = (l > 0.f && My != -INFINITY) ? gv * fast_exp2(My - Mx) / l : 0.f;
+          const int64_t orow = static_cast<int64_t>(b) * a.Hq + hq0 + g;
+          store_out4(a.out, a.out_f32, orow * D + d, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+        } else {
+          *reinterpret_cast<float4*>(a.part_o + (slot * 8 + g) * D + d) = acc;
+          if (d == 0)
+            *reinterpret_cast<float4*>(a.part_ml + (slot * 8 + g) * 4) = make_float4(Mx, l, My, 0.f);
+        }
+      }
+      __syncthreads();
+    }
+    if (a.unit_ctas) break;     // every thread takes the same exit
+  }
+  if (timed_out && lane == 0) set_error(a.err, KV4_ETIMEOUT);
+}
+
+// ------------------------------------------------------------------ launch
+template <int D, int FMT>
+static cudaError_t launch4(const DecodeArgs& a, const CUtensorMap& cmap, const CUtensorMap& smap,
+                           cudaStream_t st) {
+  using Gm = Geo4<D, FMT>;
+  auto* k = decode4_kernel<D, FMT>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n_cta);
+  cfg.blockDim = dim3(kNW * 32);
+  cfg.dynamicSmemBytes = Gm::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, a, cmap, smap);
+}
+
+int decode4_ctas_per_sm() { return kCtas; }
+
+cudaError_t launch_decode4(const DecodeArgs& a, const CUtensorMap& cmap, const CUtensorMap& smap,
+                           cudaStream_t st) {
+  if (a.fmt == KV4_NVFP4) {
+    switch (a.D) {
+      case 64: return launch4<64, KV4_NVFP4>(a, cmap, smap, st);
+      case 128: return launch4<128, KV4_NVFP4>(a, cmap, smap, st);
+      default: return launch4<256, KV4_NVFP4>(a, cmap, smap, st);
+    }
+  }
+  switch (a.D) {
+    case 64: return launch4<64, KV4_INT4_PTH>(a, cmap, smap, st);
+    case 128: return launch4<128, KV4_INT4_PTH>(a, cmap, smap, st);
+    default: return launch4<256, KV4_INT4_PTH>(a, cmap, smap, st);
+  }
+}
+
+}  // namespace kv4

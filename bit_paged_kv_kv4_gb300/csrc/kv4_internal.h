@@ -83,7 +83,10 @@ struct PrefixArgs {
   FastDiv hkv_div, p_div;       // by Hkv, by P
 };
 
-cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& map, cudaStream_t st);
+// `map`: the code-row view (FP8) or the 3-D code view (NVFP4, INT4); `smap`:
+// the 3-D scale view (NVFP4, INT4; ignored for FP8).
+cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& map, const CUtensorMap& smap,
+                          cudaStream_t st);
 cudaError_t launch_write(const WriteArgs& a, cudaStream_t st);
 cudaError_t launch_prefix(const PrefixArgs& a, cudaStream_t st);
 
@@ -147,7 +150,14 @@ cudaError_t launch_k8v4_decode(const K8V4DecodeArgs& a, cudaStream_t st);
 int decode_tile_tokens(int fmt);
 // Sets the message kv4_last_error_message() returns on this thread.
 void set_error_message(const char* msg);
-int decode_ctas_per_sm();
+// Resident CTAs per SM of the decode kernel for `fmt`, and the largest over
+// formats (the workspace is sized for it).
+int decode_ctas_per_sm(int fmt);
+int decode_max_ctas_per_sm();
+// The NVFP4 / INT4 decode kernel (kv4_decode4.cu) and its resident CTAs per SM.
+cudaError_t launch_decode4(const DecodeArgs& a, const CUtensorMap& cmap, const CUtensorMap& smap,
+                           cudaStream_t st);
+int decode4_ctas_per_sm();
 // Every argument check of kv4_decode_attention except those of the workspace
 // (the message goes to kv4_last_error_message); KV4_OK when all pass.
 kv4_status check_decode_args(const void* q, const kv4_pool* pool, const float* layer_global_scale,
