@@ -38,7 +38,6 @@ if ROOT not in sys.path:
 import workloads as W  # noqa: E402
 
 METRIC = "NVFP4 decode-attn achieved HBM GB/s (% of peak) at 32K/160K/1M ctx"
-EVENT_EVERY = 4       # timed-loop steps per sampled decode-event pair
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
@@ -379,15 +378,14 @@ def kv4_arm(args):
         s.write()
         s.decode()
     torch.cuda.synchronize()
-    # The decode call's own duration is sampled with events on every
-    # EVENT_EVERY-th step of the timed loop: an event recorded between the
-    # write and the decode holds back the decode's early launch, so timing
-    # every step would add that gap to the whole loop.
-    sampled = [i for i in range(args.steps) if i % EVENT_EVERY == 0]
-    ev_dec = {i: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for i in sampled}
+    # The timed steps (write + decode); no event sits between a write and its
+    # decode, so each decode's early launch overlaps the write as in serving.
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    # The decode call's own average duration: the same decode call K times back
+    # to back between two events (the roofline's kernel time).
+    d_start = torch.cuda.Event(enable_timing=True)
+    d_end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     with clocks:
         barrier(pg, device)
@@ -395,18 +393,19 @@ def kv4_arm(args):
         t_start.record()
         for i in range(args.steps):
             s.write()
-            if i in ev_dec:
-                ev_dec[i][0].record()
-                s.decode()
-                ev_dec[i][1].record()
-            else:
-                s.decode()
+            s.decode()
         t_end.record()
+        torch.cuda.synchronize()
+        barrier(pg, device)
+        d_start.record()
+        for i in range(args.steps):
+            s.decode()
+        d_end.record()
         torch.cuda.synchronize()
         barrier(pg, device)
     total = t_start.elapsed_time(t_end) * 1e-3
     total = max_over_ranks(pg, total, device)
-    dec_times = [a.elapsed_time(b) * 1e-3 for a, b in ev_dec.values()]
+    dec_avg = max_over_ranks(pg, d_start.elapsed_time(d_end) * 1e-3 / args.steps, device)
     err = K.kv4_device_error()
     if err != 0:
         raise SystemExit(f"device error {err} during the timed region")
@@ -414,7 +413,6 @@ def kv4_arm(args):
     value = step_bytes * world / per_step / 1e9
 
     peak, peak_src = read_peaks()
-    dec_avg = statistics.mean(dec_times)
     achieved = dec_bytes / dec_avg / 1e9
 
     # ---- end to end through the public API, host buffers ----------------
@@ -470,9 +468,9 @@ def kv4_arm(args):
                      "frac": achieved / peak, "traffic": recorded_traffic(w.name),
                      "kernel": "kv4_decode_attention (split kernel + combine)",
                      "peak_source": f"{peak_src} hbm_gbs", "decode_us": dec_avg * 1e6,
-                     "decode_us_median": statistics.median(dec_times) * 1e6,
-                     "decode_samples": f"{len(dec_times)} of {args.steps} timed steps (every {EVENT_EVERY}th)",
-                     "tokens_per_s_16_layers": B / (16 * statistics.median(dec_times))},
+                     "decode_timing": f"mean of {args.steps} back-to-back decode calls between two CUDA "
+                                      "events on the launching stream, after the timed steps",
+                     "tokens_per_s_16_layers": B / (16 * dec_avg)},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_total / args.steps * 1e3},
         "gpu_launches": args.steps * s.launches_per_step(),

@@ -942,6 +942,7 @@ combine_kernel(const DecodeArgs a) {
   __shared__ int64_t s_red[kCombineThreads / 32];
   __shared__ float s_f[2 * kCombineThreads / 32];
   __shared__ float4 s_o[kCombineThreads];
+  __shared__ float s_w[kMaxPieces];
   const int j = blockIdx.x, b = blockIdx.y;
   const int D = a.D, S = a.num_splits;
   const int ngrp = (a.G + 7) >> 3, UPB = a.Hkv * ngrp;
@@ -1011,22 +1012,35 @@ combine_kernel(const DecodeArgs a) {
   if (!contiguous && npieces > kMaxPieces && tid == 0) set_error(a.err, KV4_EUNSUPPORTED);
   auto slot_of = [&](int p) -> int64_t { return contiguous ? c0 + p + u : s_slot[p]; };
 
-  // ---- maxima of the piece states, normaliser l ------------------------------
+  // ---- the piece states, read once: maxima, normaliser l, weights ------------
+  // Thread t holds pieces t, t + kCombineThreads, ... (at most kPPT of them);
+  // each piece's O weight 2^(m_y,p - My) goes to shared memory for the sum.
+  constexpr int kPPT = kMaxPieces / kCombineThreads;
+  float pmx[kPPT], pl[kPPT], pmy[kPPT];
   float mx = -INFINITY, my = -INFINITY;
-  for (int p = tid; p < P; p += kCombineThreads) {
-    const float4 m = *reinterpret_cast<const float4*>(a.part_ml + (slot_of(p) * 8 + g) * 4);
-    mx = fmaxf(mx, m.x);
-    my = fmaxf(my, m.z);
+#pragma unroll
+  for (int k = 0; k < kPPT; ++k) {
+    const int p = tid + k * kCombineThreads;
+    pmx[k] = pmy[k] = -INFINITY;
+    pl[k] = 0.f;
+    if (p < P) {
+      const float4 m = *reinterpret_cast<const float4*>(a.part_ml + (slot_of(p) * 8 + g) * 4);
+      pmx[k] = m.x; pl[k] = m.y; pmy[k] = m.z;
+      mx = fmaxf(mx, m.x);
+      my = fmaxf(my, m.z);
+    }
   }
   float Mx, My;
   block_max2(mx, my, s_f, Mx, My);
   // per-thread partial sums, then a fixed reduction tree: deterministic
   float lp = 0.f;
-  for (int p = tid; p < P; p += kCombineThreads) {
-    const float4 m = *reinterpret_cast<const float4*>(a.part_ml + (slot_of(p) * 8 + g) * 4);
-    lp += (m.x == -INFINITY) ? 0.f : m.y * fast_exp2(m.x - Mx);
+#pragma unroll
+  for (int k = 0; k < kPPT; ++k) {
+    const int p = tid + k * kCombineThreads;
+    lp += (pmx[k] == -INFINITY) ? 0.f : pl[k] * fast_exp2(pmx[k] - Mx);
+    if (p < P) s_w[p] = (pmy[k] == -INFINITY) ? 0.f : fast_exp2(pmy[k] - My);
   }
-  const float l = block_sum(lp, s_f);
+  const float l = block_sum(lp, s_f);      // its barriers also publish s_w
 
   // ---- weighted sum of the pieces' o: thread = (piece group, 4 columns) --------
   const int cols = D / 4;                        // float4 columns
@@ -1035,8 +1049,7 @@ combine_kernel(const DecodeArgs a) {
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int p = grp; p < P; p += groups) {
     const int64_t slot = slot_of(p);
-    const float mz = a.part_ml[(slot * 8 + g) * 4 + 2];
-    const float w = (mz == -INFINITY) ? 0.f : fast_exp2(mz - My);
+    const float w = s_w[p];
     const float4 v = __ldg(reinterpret_cast<const float4*>(a.part_o + (slot * 8 + g) * D) + col);
     acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
   }

@@ -546,10 +546,12 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
         }
 
         // -------- online softmax with a lazily raised base --------
-        float corr_o[2] = {1.f, 1.f};
+        // One vote a tile: only when a logit tops its head's base by more than
+        // kLazy (or, INT4, a V scale tops s_ref) are the bases raised and O,
+        // l rescaled.
         float sv[2];
+        float smax = 0.f;
         if constexpr (FMT == KV4_INT4_PTH) {
-          float smax = 0.f;
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
             const int t = grp + 8 * r;
@@ -557,16 +559,20 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
             sv[r] = (t < valid && v > 0.f) ? v : 0.f;     // NaN, <= 0 and past the end: no weight
             smax = fmaxf(smax, sv[r]);
           }
-          if (__any_sync(kFull, smax > sref)) {
-#pragma unroll
-            for (int o2 = 4; o2 < 32; o2 <<= 1) smax = fmaxf(smax, __shfl_xor_sync(kFull, smax, o2));
-            smax = fmaxf(smax, sref);
-            corr_o[0] = corr_o[1] = (sref > 0.f) ? sref / smax : 0.f;
-            sref = smax;
-          }
         }
         float tmx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
-        if (__any_sync(kFull, tmx[0] > m_run[0] + kLazy || tmx[1] > m_run[1] + kLazy)) {
+        bool raise = tmx[0] > m_run[0] + kLazy || tmx[1] > m_run[1] + kLazy;
+        if constexpr (FMT == KV4_INT4_PTH) raise = raise || smax > sref;
+        if (__any_sync(kFull, raise)) {
+          float corr_o[2] = {1.f, 1.f};
+          if constexpr (FMT == KV4_INT4_PTH) {
+#pragma unroll
+            for (int o2 = 4; o2 < 32; o2 <<= 1) smax = fmaxf(smax, __shfl_xor_sync(kFull, smax, o2));
+            if (smax > sref) {
+              corr_o[0] = corr_o[1] = (sref > 0.f) ? sref / smax : 0.f;
+              sref = smax;
+            }
+          }
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
 #pragma unroll
@@ -579,8 +585,6 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
               m_run[c] = mnew;
             }
           }
-        }
-        if (__any_sync(kFull, corr_o[0] != 1.f || corr_o[1] != 1.f)) {
 #pragma unroll
           for (int mi = 0; mi < MT; ++mi) {
             o[mi][0] *= corr_o[0]; o[mi][1] *= corr_o[1]; o[mi][2] *= corr_o[0]; o[mi][3] *= corr_o[1];
