@@ -12,7 +12,7 @@
 //
 //   warps 0-3   softmax, one thread per query row (= TMEM lane): Q into TMEM
 //               at the start; per tile S from TMEM, mask, online softmax in
-//               the log2 domain, P (f16) back into TMEM over its own S, the
+//               the log2 domain, P (f16 hi + lo) back into TMEM over its own S, the
 //               rare rescale of O in TMEM; the epilogue.
 //   warps 4-11  converters: FP8 K and V rows from global memory (two
 //               register sets, one tile of loads in flight) to f16 tiles in the 128-byte-swizzled layout the MMA reads,
@@ -22,7 +22,7 @@
 //               tiles ahead of the converters.
 //   warp 12     TMEM allocation and, on one lane, the MMA issue:
 //               S_j = Q K_j^T (M128 N64, K = head_dim; A = Q in TMEM) and
-//               O += P_j V_j (M128 N=head_dim K64; A = P in TMEM), each issued
+//               O += P_j V_j (M128 N=head_dim K64, hi then lo; A = P in TMEM), each issued
 //               as soon as its operands are ready.
 //
 // Keeping Q and P in TMEM leaves the shared-memory data path to the K / V
@@ -37,7 +37,8 @@
 //                                offset stride (64*128), 8-key groups the
 //                                stride-byte-offset (1024)
 // TMEM (lane = query row; 32-bit columns):
-//   S_j  FP32, 64 columns at (j % 2) * 64;  P_j f16 pairs over its first 32
+//   S_j  FP32, 64 columns at (j % 2) * 64;  P_j as f16 pairs over them: the
+//        hi part in the first 32 columns, the lo part (p - hi) in the last 32
 //   Q    f16 pairs (elements 2c, 2c+1 in column c), D/2 columns at 128
 //   O    FP32, D columns at 256 (192 for head_dim 64)
 // S_{j+2} reuses the columns of P_j; it is issued after O += P_j V_j, and
@@ -45,8 +46,9 @@
 //
 // FP8 -> f16 with the hardware conversion (exact: every E4M3 value is an f16
 // value).  Q is converted bf16 -> f16 once per CTA (exact for
-// 2^-14 <= |q| <= 65504; larger magnitudes are flagged).  P is rounded to f16
-// once (relative 2^-11); S and O accumulate in FP32.
+// 2^-14 <= |q| <= 65504; larger magnitudes are flagged).  P goes to the PV
+// product as an f16 hi + lo pair (the two roundings leave about 2^-22 of p);
+// S and O accumulate in FP32.
 //
 // The maximum used for exponentiation is raised only when a tile's maximum
 // exceeds it by more than 8 (log2 units), so P stays below 2^8 and O is
@@ -265,6 +267,9 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const ExtendArgs a)
 #pragma unroll
           for (int kk = 0; kk < kKT / 16; ++kk)
             tc_mma_ts(tO, tP + kk * 8, dV + ((kk * 2048) >> 4), idO, (nP > 0 || kk > 0));
+#pragma unroll
+          for (int kk = 0; kk < kKT / 16; ++kk)          // the lo part of P
+            tc_mma_ts(tO, tP + 32 + kk * 8, dV + ((kk * 2048) >> 4), idO, 1);
           tc_commit(bar(PV_DONE));
           tc_commit(bar(V_EMPTY + vst));
           if (++vst == kNST) { vst = 0; vph ^= 1; }
@@ -480,13 +485,18 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const ExtendArgs a)
         m_use = mnew;
       }
       float rs4[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t ph[kKT / 2];
+      // P as an f16 hi + lo pair (about 22 significant bits): hi over the
+      // first 32 columns of S_j, lo over the last 32
+      uint32_t ph[kKT / 2], pl[kKT / 2];
 #pragma unroll
       for (int c = 0; c < kKT; c += 2) {
         const float e0 = fast_exp2(fmaf(s[c], c2, -m_use));
         const float e1 = fast_exp2(fmaf(s[c + 1], c2, -m_use));
         rs4[(c >> 1) & 3] += e0 + e1;
-        ph[c / 2] = pack_f16x2(e0, e1);
+        const uint32_t hi = pack_f16x2(e0, e1);
+        const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+        ph[c / 2] = hi;
+        pl[c / 2] = pack_f16x2(e0 - hf.x, e1 - hf.y);
       }
       const float rs = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
       l = l * alpha + rs;
@@ -512,7 +522,8 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const ExtendArgs a)
           }
         }
       }
-      tmem_st32(tS, ph);                              // P_j over S_j
+      tmem_st32(tS, ph);                              // P_j over S_j: hi, then lo
+      tmem_st32(tS + 32, pl);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(P_FULL + bb));

@@ -1,17 +1,22 @@
 """GPU parity of kv4_extend_attention (chunked-prefill / extend attention
 over the FP8 prefix workspace plus the FP8 chunk) against the FP64 oracle.
 
-Tolerance, from the kernel's arithmetic: K, V and (in range) q are exact in
-the f16 operands and S, O accumulate in FP32; the one rounding that matters
-is the softmax weight p rounded to f16 before the P.V product (relative
-error <= 2^-11), so |out - exact| <= 2^-11 * max|V| over the visible values,
-plus FP32 accumulation noise.  bf16 outputs add one bf16 rounding.
+The gate is the attention gate of the decode tests: per output row max-abs
+error <= 2e-3 and cosine >= 0.9999 against the FP64 oracle, FP32 outputs.
+Why the kernel meets it on any data: K, V and (in range) q are exact in the
+f16 operands, S and O accumulate in FP32, and the softmax weight p enters
+the P.V product as an f16 hi + lo pair, so what is left of p's rounding is
+about 2^-22 * p (a single f16 rounding, 2^-11 * max|V|, is 0.02 on the
+outlier workloads, ten times the gate, when one key dominates a row: the
+peaked-attention test holds exactly that case).  bf16 outputs add one bf16
+rounding of the FP32 result.
 """
 import numpy as np
 import pytest
 import torch
 
 import bit_paged_kv_kv4_gb300 as K
+from kv4_testlib import ATOL, MIN_COS, check_close
 from oracle import attention as A
 from workloads import extend_q, fp8_kv_codes
 
@@ -57,16 +62,7 @@ def vmax(x):
 
 
 def check(got, want, x, what):
-    tol = 2.0 ** -11 * vmax(x) + 1e-5
-    got = np.asarray(got, np.float64)
-    assert np.all(np.isfinite(got)), what
-    err = np.abs(got - want).max()
-    assert err <= tol, f"{what}: max abs error {err:.3g} > {tol:.3g}"
-    g, w = got.reshape(-1, got.shape[-1]), want.reshape(-1, want.shape[-1])
-    keep = np.linalg.norm(w, axis=1) > 0
-    cos = (g[keep] * w[keep]).sum(1) / (np.linalg.norm(g[keep], axis=1) * np.linalg.norm(w[keep], axis=1))
-    assert cos.min() >= 0.99999, f"{what}: cosine {cos.min():.7f}"
-    return err
+    return check_close(np.asarray(got, np.float64), want, atol=ATOL, min_cos=MIN_COS, what=what)
 
 
 @pytest.mark.parametrize("D,Hq,Hkv,lp,lc", [
@@ -109,6 +105,34 @@ def test_large_prefix_many_tiles_and_rescales():
     check(got, oracle(x), x, "ramp prefix")
 
 
+def test_peaked_attention_on_large_values():
+    # Two prefix keys along the queries' own +-1 pattern (at the FP8 values 448
+    # and 416) take nearly all the weight of every row; the first sets the
+    # row's maximum (weight exactly 1), the second gets 2^(x2 - x1), about
+    # 0.3-0.7 as the query scale varies over the rows and heads.  Their values
+    # sit at the FP8 maximum (|V| = 448 s_V, tens) with different sign
+    # patterns.  A weight rounded once to f16 (half an ulp: 2^-12 of it) would
+    # move these outputs by up to ~5e-3, above the gate; hi + lo does not.
+    x = make([200], [40], 4, 1, 128, seed=7)
+    sv = float(x["s_host"][1])
+    d = torch.arange(128, device="cuda")
+    sign = torch.where(d % 3 == 0, -1.0, 1.0)
+    alt = torch.where(d % 2 == 0, 1.0, -1.0)
+    r = torch.arange(40, device="cuda").view(-1, 1, 1).float()
+    hq = torch.arange(4, device="cuda").view(1, -1, 1).float()
+    alpha = 0.02 * (1.0 + (r * 4 + hq) / 160.0)
+    x["q"][:] = (sign * alpha).to(torch.bfloat16)
+    x["pk"][123, 0] = (sign * 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+    x["pk"][124, 0] = (sign * 416.0).to(torch.float8_e4m3fn).view(torch.uint8)
+    x["pv"][123, 0] = (-sign * 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+    x["pv"][124, 0] = (alt * 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+    got = run(x).cpu().numpy()
+    assert K.kv4_device_error() == 0
+    want = oracle(x)
+    assert np.abs(want).max() > 0.3 * 448.0 * sv            # the two large values dominate
+    check(got, want, x, "peaked")
+
+
 def test_oversized_chunk_and_bad_query_are_flagged():
     x = make([10], [300], 2, 1, 64, seed=5)
     run(x, max_chunk_len=128)                  # rows past the grid are not computed
@@ -127,14 +151,11 @@ def test_full_size_chunk_of_160k_request_sampled():
     # Hkv 4, head_dim 256; sampled rows against the oracle
     lp, lc = [155426], [8192]
     x = make(lp, lc, 24, 4, 256, seed=3)
-    got = run(x, torch.bfloat16)
+    got = run(x)
     assert K.kv4_device_error() == 0
     rng = np.random.default_rng(0)
     rows = [(0, 0), (127, 23), (128, 5), (8191, 17), (4096, 12)] + \
         [(int(r), int(h)) for r, h in zip(rng.integers(0, 8192, 11), rng.integers(0, 24, 11))]
     want = oracle(x, rows=rows)
-    g = got.float().cpu().numpy()
-    for r, h in rows:
-        w = want[r, h]
-        tol = 2.0 ** -11 * vmax(x) + np.abs(w) * 2.0 ** -8 + 1e-5
-        assert np.all(np.abs(g[r, h] - w) <= tol), (r, h, np.abs(g[r, h] - w).max())
+    g = got.cpu().numpy()
+    check(np.stack([g[r, h] for r, h in rows]), np.stack([want[r, h] for r, h in rows]), x, "160K chunk")
