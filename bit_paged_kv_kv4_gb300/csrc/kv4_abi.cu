@@ -311,6 +311,7 @@ static kv4_status write_common(const void* k, const void* v, const float* in_sca
 kv4_status kv4_write(const void* k, const void* v, const int64_t* slot_mapping,
                      int64_t num_tokens, const kv4_pool* pool,
                      const float* layer_global_scale, int32_t fmt, void* stream) {
+  kv4::NvtxRange nvtx_range("kv4_write");
   return write_common(k, v, nullptr, false, slot_mapping, num_tokens, pool, layer_global_scale, fmt,
                       stream);
 }
@@ -318,6 +319,7 @@ kv4_status kv4_write(const void* k, const void* v, const int64_t* slot_mapping,
 kv4_status kv4_write_fp8(const void* k, const void* v, const float* in_scale,
                          const int64_t* slot_mapping, int64_t num_tokens, const kv4_pool* pool,
                          const float* layer_global_scale, int32_t fmt, void* stream) {
+  kv4::NvtxRange nvtx_range("kv4_write_fp8");
   return write_common(k, v, in_scale, true, slot_mapping, num_tokens, pool, layer_global_scale, fmt,
                       stream);
 }
@@ -339,6 +341,7 @@ kv4_status kv4_decode_attention(const void* q, const kv4_pool* pool,
                                 int32_t num_q_heads, float sm_scale, int32_t num_splits,
                                 void* workspace, int64_t workspace_bytes, void* out,
                                 int32_t out_is_fp32, void* stream) {
+  kv4::NvtxRange nvtx_range("kv4_decode_attention");
   g_msg.clear();
   kv4_status s = kv4::check_decode_args(q, pool, layer_global_scale, block_table, max_pages,
                                         seq_lens, batch, num_q_heads, sm_scale, num_splits, out);
@@ -417,6 +420,7 @@ kv4_status kv4_decode_attention(const void* q, const kv4_pool* pool,
 kv4_status kv4_calibrate_global_scale(const void* k, const void* v, int64_t num_tokens,
                                       int32_t num_kv_heads, int32_t head_dim,
                                       float* layer_global_scale, void* stream) {
+  kv4::NvtxRange nvtx_range("kv4_calibrate_global_scale");
   g_msg.clear();
   if (num_tokens < 0 || num_kv_heads < 1) return fail(KV4_EINVAL, "num_tokens < 0 or num_kv_heads < 1");
   if (head_dim != 64 && head_dim != 128 && head_dim != 256)
@@ -439,6 +443,7 @@ kv4_status kv4_dequant_prefix(const kv4_pool* pool, const float* layer_global_sc
                               const int32_t* prefix_lens, const int64_t* cu_prefix,
                               int32_t batch, int32_t max_prefix_len, const float* fp8_scale,
                               void* fp8_k, void* fp8_v, void* stream) {
+  kv4::NvtxRange nvtx_range("kv4_dequant_prefix");
   g_msg.clear();
   kv4_status s = check_pool(pool);
   if (s != KV4_OK) return s;
@@ -496,6 +501,7 @@ kv4_status kv4_extend_attention(const void* q, const void* chunk_k, const void* 
                                 const int64_t* cu_chunk, int32_t batch, int32_t max_chunk_len,
                                 int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                 float sm_scale, void* out, int32_t out_is_fp32, void* stream) {
+  kv4::NvtxRange nvtx_range("kv4_extend_attention");
   g_msg.clear();
   if (batch < 0 || max_chunk_len < 0) return fail(KV4_EINVAL, "batch and max_chunk_len must be >= 0");
   if (num_kv_heads < 1 || num_q_heads < 1 || num_q_heads % num_kv_heads != 0)
@@ -545,6 +551,7 @@ kv4_status kv4_extend_attention(const void* q, const void* chunk_k, const void* 
 kv4_status kv4_k8v4_write(const void* k, const void* v, const int64_t* slot_mapping,
                           int64_t num_tokens, const kv4_pool* pool, const float* key_scale,
                           void* stream) {
+  kv4::NvtxRange nvtx_range("kv4_k8v4_write");
   g_msg.clear();
   kv4_status s = check_pool(pool);
   if (s != KV4_OK) return s;
@@ -590,6 +597,7 @@ kv4_status kv4_k8v4_decode_attention(const void* q, const kv4_pool* pool, const 
                                      float sm_scale, int32_t num_chunks, void* workspace,
                                      int64_t workspace_bytes, void* out, int32_t out_is_fp32,
                                      void* stream) {
+  kv4::NvtxRange nvtx_range("kv4_k8v4_decode_attention");
   g_msg.clear();
   kv4_status s = check_pool(pool);
   if (s != KV4_OK) return s;

@@ -6,9 +6,20 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/kv4.h"
 
 namespace kv4 {
+
+// An NVTX range around one C-ABI call: named in Nsight timelines, and a
+// no-op (the header-only NVTX v3 API) when no tool is attached.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // Division of n < 2^31 by a fixed d in [1, 2^31) with one multiply-high, an
 // add and a shift (T. Granlund, P. Montgomery, "Division by invariant integers

@@ -77,6 +77,7 @@ kv4_status kv4_decode_attention_static_ws(const void* q, const kv4_pool* pool,
                                           int32_t num_q_heads, float sm_scale,
                                           int32_t num_splits, void* out, int32_t out_is_fp32,
                                           void* stream) {
+  kv4::NvtxRange nvtx_range("kv4_decode_attention_static_ws");
   // the argument checks of kv4_decode_attention come first, so an invalid call
   // gets the same precise message as there, not the scratch-size one below
   kv4::set_error_message("");

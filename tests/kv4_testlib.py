@@ -13,6 +13,38 @@ from workloads import CHUNK, bf16_bits_to_f32, global_scale_from_amax, slots_for
 ATOL = 2e-3
 MIN_COS = 0.9999
 
+# Guard bytes after a device buffer: a kernel writing past the buffer's end
+# changes them (the whole-buffer compares only see writes inside it).
+GUARD_BYTES = 4096
+GUARD = 0x5C
+
+
+def guarded_pool(fmt, num_pages, P, Hkv, D, fill=0):
+    """A pool whose device buffer is followed by GUARD_BYTES guard bytes;
+    ``pool.buffer`` is the pool itself, ``pool.guard`` the bytes after it."""
+    n = K.kv4_pool_bytes(fmt, num_pages, P, Hkv, D)
+    raw = torch.empty(n + GUARD_BYTES, dtype=torch.uint8, device="cuda")
+    raw[:n].fill_(fill)
+    raw[n:].fill_(GUARD)
+    pool = K.Pool(fmt, num_pages, P, Hkv, D, buffer=raw)
+    pool.buffer, pool.guard = raw[:n], raw[n:]
+    return pool
+
+
+def guarded_empty(shape, fill, dtype=torch.uint8):
+    """A uint8 device tensor of `shape` (filled with `fill`) followed by guard
+    bytes; returns (tensor, guard)."""
+    n = int(np.prod(shape))
+    raw = torch.empty(n + GUARD_BYTES, dtype=dtype, device="cuda")
+    raw[:n].fill_(fill)
+    raw[n:].fill_(GUARD)
+    return raw[:n].view(shape), raw[n:]
+
+
+def assert_guard_intact(guard, what="buffer"):
+    torch.cuda.synchronize()
+    assert bool((guard == GUARD).all()), f"bytes past the end of the {what} were written"
+
 
 def dev_bf16(u16):
     return torch.from_numpy(np.ascontiguousarray(u16).view(np.int16)).view(torch.bfloat16).cuda()
@@ -90,8 +122,7 @@ class Case:
 
     # device side
     def gpu_pool(self, fill=0):
-        pool = K.Pool(self.fmt, self.num_pages, self.P, self.Hkv, self.D)
-        pool.buffer.fill_(fill)
+        pool = guarded_pool(self.fmt, self.num_pages, self.P, self.Hkv, self.D, fill)
         self.d_g = torch.from_numpy(self.g).cuda()
         if len(self.slots):
             K.kv4_write(dev_bf16(self.k), dev_bf16(self.v), torch.from_numpy(self.slots).cuda(), pool,

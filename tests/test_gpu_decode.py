@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import bit_paged_kv_kv4_gb300 as K
-from kv4_testlib import Case, check_close, to_u16
+from kv4_testlib import Case, assert_guard_intact, check_close, to_u16
 from workloads import TINY
 
 pytestmark = pytest.mark.gpu
@@ -18,6 +18,7 @@ def run(c, splits=0, out_dtype=torch.float32):
     pool = c.gpu_pool()
     out = c.gpu_out(pool, num_splits=splits, out_dtype=out_dtype)
     assert K.kv4_device_error() == 0
+    assert_guard_intact(pool.guard, "pool")
     return out
 
 

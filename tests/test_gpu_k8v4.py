@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import bit_paged_kv_kv4_gb300 as K
-from kv4_testlib import check_close, dev_bf16
+from kv4_testlib import assert_guard_intact, check_close, dev_bf16, guarded_pool
 from oracle import k8v4 as KV
 from workloads import f32_to_bf16_bits
 
@@ -30,12 +30,12 @@ def test_k8v4_write_bit_exact(D):
     slots = rng.permutation(pages * P)[:T].astype(np.int64)
     slots[::13] = -1
     s_k = np.float32(0.05)
-    pool = K.Pool("k8v4", pages, P, H, D, device="cuda")
-    pool.buffer.fill_(0xA5)
+    pool = guarded_pool("k8v4", pages, P, H, D, fill=0xA5)
     K.kv4_k8v4_write(dev_bf16(k), dev_bf16(v), torch.from_numpy(slots).cuda(), pool,
                      torch.tensor([s_k], dtype=torch.float32, device="cuda"))
     torch.cuda.synchronize()
     assert K.kv4_device_error() == 0
+    assert_guard_intact(pool.guard, "pool")
     ref = KV.write(KV.new_pool(pages, P, H, D, fill=0xA5), P, H, k, v, slots, s_k)
     got = pool.buffer.cpu().numpy()
     diff = np.nonzero(got != ref)[0]

@@ -6,7 +6,7 @@ import torch
 
 import bit_paged_kv_kv4_gb300 as K
 import oracle
-from kv4_testlib import Case
+from kv4_testlib import Case, assert_guard_intact, guarded_empty
 
 pytestmark = pytest.mark.gpu
 
@@ -22,11 +22,14 @@ def test_prefix_bit_exact(fmt, D):
     wk, wv = oracle.attention.dequant_prefix(ref_pool, spec, c.g, c.table, prefix, s8)
     pool = c.gpu_pool()
     total = int(prefix.sum())
-    gk = torch.full((total, c.Hkv, D), 0xEE, dtype=torch.uint8, device="cuda")
-    gv = torch.full_like(gk, 0xEE)
+    gk, gk_guard = guarded_empty((total, c.Hkv, D), 0xEE)
+    gv, gv_guard = guarded_empty((total, c.Hkv, D), 0xEE)
     K.kv4_dequant_prefix(pool, c.d_g, torch.from_numpy(c.table).cuda(), torch.from_numpy(prefix).cuda(),
                          torch.from_numpy(cu).cuda(), int(prefix.max()), torch.from_numpy(s8).cuda(), gk, gv)
     torch.cuda.synchronize()
     assert K.kv4_device_error() == 0
     assert np.array_equal(gk.cpu().numpy(), wk)
     assert np.array_equal(gv.cpu().numpy(), wv)
+    assert_guard_intact(gk_guard, "K workspace")
+    assert_guard_intact(gv_guard, "V workspace")
+    assert_guard_intact(pool.guard, "pool")

@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import bit_paged_kv_kv4_gb300 as K
-from kv4_testlib import Case, dev_bf16
+from kv4_testlib import Case, assert_guard_intact, dev_bf16, guarded_pool
 from oracle import formats as F
 from oracle import pool as OP
 from workloads import TINY, f32_to_bf16_bits
@@ -22,6 +22,7 @@ def test_write_bit_exact(fmt, D, P):
     _, ref = c.oracle_pool(fill=0xA5)
     got = pool.buffer.cpu().numpy()
     assert K.kv4_device_error() == 0
+    assert_guard_intact(pool.guard, "pool")
     diff = np.nonzero(got != ref)[0]
     assert diff.size == 0, f"{diff.size} bytes differ, first at {diff[:8]}"
 
@@ -96,8 +97,7 @@ def test_write_skips_negative_and_flags_out_of_range_slots():
     slots = c.slots.copy()
     slots[3] = -1
     slots[5] = c.num_pages * 16 + 7          # beyond the pool: skipped, flagged
-    pool = K.Pool("nvfp4", c.num_pages, 16, 1, 64)
-    pool.buffer.fill_(0x5A)
+    pool = guarded_pool("nvfp4", c.num_pages, 16, 1, 64, fill=0x5A)
     g = torch.from_numpy(c.g).cuda()
     K.kv4_device_error()
     K.kv4_write(dev_bf16(c.k), dev_bf16(c.v), torch.from_numpy(slots).cuda(), pool, g)
@@ -109,6 +109,7 @@ def test_write_skips_negative_and_flags_out_of_range_slots():
     keep[5] = -1
     OP.write(ref, spec, c.k, c.v, keep, c.g)
     assert np.array_equal(pool.buffer.cpu().numpy(), ref)
+    assert_guard_intact(pool.guard, "pool")             # the slot past the end went nowhere
 
 
 @pytest.mark.parametrize("fmt", ["nvfp4", "int4", "fp8"])
@@ -124,8 +125,7 @@ def test_write_fp8_input_bit_exact(fmt, D):
     slots = rng.permutation(pages * P)[:T].astype(np.int64)
     slots[::17] = -1                                    # skipped tokens
     g = np.array([0.013, 0.021], np.float32)
-    pool = K.Pool(fmt, pages, P, H, D, device="cuda")
-    pool.buffer.fill_(0x5A)
+    pool = guarded_pool(fmt, pages, P, H, D, fill=0x5A)
     K.kv4_write_fp8(codes[0].contiguous(), codes[1].contiguous(), torch.from_numpy(s_in).cuda(),
                     torch.from_numpy(slots).cuda(), pool, torch.from_numpy(g).cuda())
     torch.cuda.synchronize()
@@ -136,3 +136,4 @@ def test_write_fp8_input_bit_exact(fmt, D):
     got = pool.buffer.cpu().numpy()
     diff = np.nonzero(got != ref)[0]
     assert diff.size == 0, f"{diff.size} bytes differ, first at {diff[:8]}"
+    assert_guard_intact(pool.guard, "pool")
