@@ -463,8 +463,10 @@ kv4_status kv4_dequant_prefix(const kv4_pool* pool, const float* layer_global_sc
   if (block_table == nullptr || prefix_lens == nullptr || cu_prefix == nullptr ||
       fp8_scale == nullptr || fp8_k == nullptr || fp8_v == nullptr)
     return fail(KV4_EINVAL, "block_table, prefix_lens, cu_prefix, fp8_scale and outputs must be non-NULL");
-  if (!aligned(fp8_k, 16) || !aligned(fp8_v, 16) || !aligned(cu_prefix, 8))
-    return fail(KV4_EINVAL, "fp8_k and fp8_v must be 16-byte aligned");
+  if (!aligned(fp8_k, 16) || !aligned(fp8_v, 16) || !aligned(cu_prefix, 8) || !aligned(fp8_scale, 4) ||
+      !aligned(block_table, 4) || !aligned(prefix_lens, 4) ||
+      (layer_global_scale != nullptr && !aligned(layer_global_scale, 4)))
+    return fail(KV4_EINVAL, "fp8_k and fp8_v must be 16-byte aligned (int64 arrays 8-byte, others 4-byte)");
   if (pool->fmt == KV4_NVFP4 && layer_global_scale == nullptr)
     return fail(KV4_EINVAL, "NVFP4 needs layer_global_scale");
   const int64_t threads = static_cast<int64_t>(max_prefix_len) * pool->num_kv_heads * (pool->head_dim / 16);
@@ -490,6 +492,7 @@ kv4_status kv4_dequant_prefix(const kv4_pool* pool, const float* layer_global_sc
   a.out_v = static_cast<uint8_t*>(fp8_v);
   a.err = error_word();
   if (a.err == nullptr) return fail(KV4_ECUDA, "no CUDA device / error word unavailable");
+  a.sms = sm_count();
   cudaError_t e = kv4::launch_prefix(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KV4_OK : cuda_fail(e, "kv4_dequant_prefix launch");
 }

@@ -302,18 +302,24 @@ __device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f) {
 // 1990): q0 = RN(a * yb) is within one ulp of a/b, the residual a - b*q0 is
 // exact under a fused multiply-add, and RN(q0 + residual * yb) equals
 // RN(a/b) whenever no intermediate overflows or underflows.  Outside that
-// range (a reciprocal or first quotient that is not finite) it falls back to
-// the IEEE division.  The sign of a zero quotient follows a (as a/b with
+// range (a reciprocal that is subnormal or not finite, a first quotient that
+// is not finite) it falls back to the IEEE division; a quotient that falls
+// below FP32's normal range may be off in its last subnormal bit, which no
+// caller sees (it converts to a zero of E4M3 or E2M1).  The sign of a zero quotient follows a (as a/b with
 // b > 0 does).  Callers only pass b > 0.
 __device__ __forceinline__ float div_rn(float a, float b, float yb) {
   const float q0 = __fmul_rn(a, yb);
-  if (!(fabsf(q0) < 1.0e30f) || !(yb < 1.0e30f)) return __fdiv_rn(a, b);
+  if (!(fabsf(q0) < 1.0e30f) || !(yb < 1.0e30f) || !(yb >= 1.17549435e-38f)) return __fdiv_rn(a, b);
   const float r = __fmaf_rn(-b, q0, a);
   return copysignf(__fmaf_rn(r, yb, q0), a);
 }
 
-// div_rn without the range check, for callers that have checked once that
-// yb < 1e30 and |a * yb| < 1e30 for every a they pass.
+// div_rn without the range check, for callers that have checked once, with
+// div_rn_in_range(yb, bound), that yb is a normal number below 1e30 and that
+// |a * yb| < 1e30 for every a they pass (|a| <= bound).
+__device__ __forceinline__ bool div_rn_in_range(float yb, float bound) {
+  return yb < 1.0e30f && yb >= 1.17549435e-38f && bound * yb < 1.0e30f;
+}
 __device__ __forceinline__ float div_rn_inrange(float a, float b, float yb) {
   const float q0 = __fmul_rn(a, yb);
   const float r = __fmaf_rn(-b, q0, a);

@@ -92,6 +92,7 @@ struct PrefixArgs {
   uint8_t* out_v;
   int* err;
   FastDiv hkv_div, p_div;       // by Hkv, by P
+  int sms;                      // SMs of the device (sizes the grid)
 };
 
 // `map`: the code-row view (FP8) or the 3-D code view (NVFP4, INT4); `smap`:

@@ -3,12 +3,29 @@
 // which turns the 4-bit prefix into FP8 in a buffer that is reused, then
 // attends over prefix plus the current chunk.
 //
-// One thread turns 16 consecutive head-dim elements (one NVFP4 block) of one
-// (token, head, K|V) row into 16 E4M3 bytes: x_hat = (e2m1 * e4m3) * g in
-// FP32 (NVFP4) or code * s (INT4), then E4M3(x_hat / s_fp8) with RNE and
-// saturation; the division is the correctly rounded div_rn.  Pure streaming:
-// one code load (8 bytes; 16 for the token-pair rows of NVFP4 V, of which
-// this token's nibbles are kept), one scale, one 16-byte store.
+// Every output byte is E4M3(RN(x_hat / s_fp8)) with RNE and saturation, where
+// x_hat = RN((e2m1 * e4m3) * g) in FP32 (NVFP4) or RN(code * s) (INT4).  A
+// 16-element block takes only a handful of distinct x_hat values (the eight
+// E2M1 magnitudes under the block's E4M3 scale; the sixteen INT4 codes under
+// the row's scale), so the kernel computes the output bytes of those values
+// once, exactly as the per-element definition does, and turns each element
+// into one byte selection from an 8-byte table (PRMT):
+//
+//  * NVFP4: the table depends only on the block-scale byte and the launch's
+//    (g, s_fp8) of K or V, so each CTA builds all 256 of them (2 KB of shared
+//    memory) once, with the IEEE division, and then streams.  E2M1 is
+//    sign-magnitude and every step is odd in x, so a negative code takes its
+//    magnitude's byte with the sign bit flipped.  (A NaN scale byte, which
+//    the write never stores, gives a NaN byte of the code's sign where the
+//    per-element computation would give 0x7F.)
+//  * INT4: one FP32 scale per (token, head) row; each thread builds the two
+//    tables of its row (codes 0..7 and 8..15 = -8..-1) with the correctly
+//    rounded division on packed FP32 pairs.
+//
+// One thread converts 64 consecutive elements of one (token, head, K|V) row:
+// 32 code bytes (64 for the token-pair rows of NVFP4 V, of which this token's
+// nibbles are kept), one scale word, 64 bytes stored.  One wave of resident
+// CTAs strides over the rows, so the tables are built once per CTA.
 #include <cstdint>
 
 #include "kv4_device.cuh"
@@ -16,147 +33,239 @@
 
 namespace kv4 {
 
-__device__ __forceinline__ uint32_t pack_f16x2_same(__half h) {
-  const uint32_t u = __half_as_ushort(h);
-  return u | (u << 16);
+constexpr int kPrefixThreads = 256;
+
+// Packed FP32 pairs: each lane of mul.rn / fma.rn .f32x2 is the IEEE
+// round-to-nearest result of the scalar operation, so pairs give the same
+// bits as two scalar instructions at half the issue cost.
+__device__ __forceinline__ uint64_t f2(float x, float y) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& x, float& y) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(v));
+}
+__device__ __forceinline__ uint64_t mul_f2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma_f2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
 }
 
-// One E4M3 block of 16 elements of row (t, h): x_hat -> E4M3(x_hat / s8).
-template <int D, int FMT>
-__device__ __forceinline__ uint4 prefix_block(uint2 codes, float s, float g, float s8, float r8) {
-  float xh[16];
-  float bound;                                  // >= |x_hat| of every element
-  if constexpr (FMT == KV4_NVFP4) {
-    uint32_t h2[8];
-    e2m1x8_to_f16x2x4(codes.x, *reinterpret_cast<uint32_t(*)[4]>(h2));
-    e2m1x8_to_f16x2x4(codes.y, *reinterpret_cast<uint32_t(*)[4]>(h2 + 4));
-    // e2m1 * e4m3 is exact in f16 (<= 6 significant bits, within [2^-10, 2688]),
-    // so it equals the FP32 product; then one FP32 rounding for the * g
-    const __half hs = __float2half_rn(s);     // s is an E4M3 value: exact
-    const uint32_t s2 = pack_f16x2_same(hs);
+// RN(a / b) for a pair (div_rn_inrange on each lane, Markstein's correction
+// step): q0 = a yb, r = a - b q0 (exact under fma), q = q0 + r yb; the sign of
+// a zero quotient follows a.  nb = (-b, -b), yb2 = (yb, yb) with yb = RN(1/b).
+__device__ __forceinline__ void div_rn_pair(float a0, float a1, uint64_t nb, uint64_t yb2, float& q0o,
+                                            float& q1o) {
+  const uint64_t a = f2(a0, a1);
+  const uint64_t q0 = mul_f2(a, yb2);
+  const uint64_t r = fma_f2(nb, q0, a);
+  f2_split(fma_f2(r, yb2, q0), q0o, q1o);
+  q0o = __uint_as_float((__float_as_uint(q0o) & 0x7FFFFFFFu) | (__float_as_uint(a0) & 0x80000000u));
+  q1o = __uint_as_float((__float_as_uint(q1o) & 0x7FFFFFFFu) | (__float_as_uint(a1) & 0x80000000u));
+}
+
+__device__ __forceinline__ uint2 pack_e4m3x8(const float (&q)[8]) {
+  return make_uint2(f32x2_to_e4m3x2(q[0], q[1]) | (f32x2_to_e4m3x2(q[2], q[3]) << 16),
+                    f32x2_to_e4m3x2(q[4], q[5]) | (f32x2_to_e4m3x2(q[6], q[7]) << 16));
+}
+
+// NVFP4 table of scale byte sb: E4M3(RN(RN(e_i s g) / s8)) for the E2M1
+// magnitudes e_i = 0, 0.5, 1, 1.5, 2, 3, 4, 6 (index = the code's low three
+// bits).  e_i * s is exact in FP32 (at most 6 significant bits, within
+// [2^-10, 2688]).
+__device__ __forceinline__ uint2 nvfp4_scale_table(uint32_t sb, float g, float s8) {
+  const float s = e4m3_to_f32(sb);
+  const float e[8] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f};
+  float q[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t es = hmul2(h2[j], s2);
-      const float2 e = __half22float2(*reinterpret_cast<const __half2*>(&es));
-      xh[2 * j] = __fmul_rn(e.x, g);
-      xh[2 * j + 1] = __fmul_rn(e.y, g);
-    }
-    bound = 6.f * s * g * 2.f;
+  for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(__fmul_rn(__fmul_rn(e[i], s), g), s8);
+  return pack_e4m3x8(q);
+}
+
+// The bytes of RN(x_i / s8) for 8 values x_i, as an 8-byte PRMT table.  Away
+// from the FP32 range limits the division is div_rn on pairs, else the IEEE
+// division.
+__device__ __forceinline__ uint2 e4m3_table(const float (&x)[8], float s8, float r8, bool in_range) {
+  float q[8];
+  if (in_range) {
+    const uint64_t nb = f2(-s8, -s8), yb2 = f2(r8, r8);
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) div_rn_pair(x[i], x[i + 1], nb, yb2, q[i], q[i + 1]);
   } else {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const uint32_t w = (j < 8) ? codes.x : codes.y;
-      const int c = static_cast<int>((w >> (4 * (j & 7))) & 0xFu);
-      xh[j] = __fmul_rn(static_cast<float>(c >= 8 ? c - 16 : c), s);
-    }
-    bound = 8.f * fabsf(s) * 2.f;
+    for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(x[i], s8);
   }
-  float q[16];
-  if (r8 < 1.0e30f && bound * r8 < 1.0e30f) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) q[i] = div_rn_inrange(xh[i], s8, r8);
-  } else {                                      // operands near the FP32 range limits
-#pragma unroll
-    for (int i = 0; i < 16; ++i) q[i] = __fdiv_rn(xh[i], s8);
-  }
-  uint32_t outw[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-    outw[j] = f32x2_to_e4m3x2(q[4 * j], q[4 * j + 1]) | (f32x2_to_e4m3x2(q[4 * j + 2], q[4 * j + 3]) << 16);
-  return make_uint4(outw[0], outw[1], outw[2], outw[3]);
+  return pack_e4m3x8(q);
 }
 
-// Thread (request b = blockIdx.z, K|V = blockIdx.y, row (t, h), blocks
-// 2 part and 2 part + 1): 32 elements, so the per-thread set-up (indices,
-// block-table lookup, reciprocal) is paid once per two blocks.
+// Bit 0 of byte i = bit 3 of nibble i of sel (the code's sign), for the four
+// low nibbles: PRMT from an all-0x80 table gives 0x80 for a selector below 8
+// and the replicated sign bit, 0xFF, for one of 8 or more.
+__device__ __forceinline__ uint32_t sign_bytes(uint32_t sel) { return prmt(0x80808080u, 0x80808080u, sel); }
+
+// Four NVFP4 elements: mag_sel holds their codes' magnitude bits in its four
+// low nibbles, signs has each element's sign in bit 7 of its byte (other bits
+// ignored).
+__device__ __forceinline__ uint32_t nvfp4_bytes(uint2 tab, uint32_t mag_sel, uint32_t signs) {
+  return prmt(tab.x, tab.y, mag_sel) ^ (signs & 0x80808080u);
+}
+
+// Eight packed NVFP4 codes (element i in nibble i) -> 8 E4M3 bytes.
+__device__ __forceinline__ uint2 nvfp4_word(uint2 tab, uint32_t w) {
+  const uint32_t m = w & 0x77777777u;
+  return make_uint2(nvfp4_bytes(tab, m, sign_bytes(w) << 7), nvfp4_bytes(tab, m >> 16, sign_bytes(w >> 16) << 7));
+}
+
+// Four NVFP4 elements of a token-pair row word x (element i in byte i, this
+// token's nibble at bit sh of it) -> 4 E4M3 bytes.
+__device__ __forceinline__ uint32_t nvfp4_pair_word(uint2 tab, uint32_t x, int sh) {
+  const uint32_t xs = x >> sh;
+  const uint32_t y = xs & 0x07070707u;
+  const uint32_t sel = prmt(y | (y >> 4), 0u, 0x0020u);     // nibbles e0 e1 e2 e3
+  return nvfp4_bytes(tab, sel, xs << 4);
+}
+
+// Eight INT4 codes (two's complement, element i in nibble i) -> 8 E4M3 bytes:
+// tp holds the bytes of codes 0..7, tn those of 8..15.
+__device__ __forceinline__ uint32_t int4_bytes(uint2 tp, uint2 tn, uint32_t mag_sel, uint32_t sel) {
+  const uint32_t neg = prmt(sign_bytes(sel) << 7, 0u, 0xBA98u);   // 0xFF per negative code
+  return (prmt(tp.x, tp.y, mag_sel) & ~neg) | (prmt(tn.x, tn.y, mag_sel) & neg);
+}
+__device__ __forceinline__ uint2 int4_word(uint2 tp, uint2 tn, uint32_t w) {
+  const uint32_t m = w & 0x77777777u;
+  return make_uint2(int4_bytes(tp, tn, m, w), int4_bytes(tp, tn, m >> 16, w >> 16));
+}
+
+// CTA (gx, kind = blockIdx.y, request b = blockIdx.z); item i of request b =
+// (row = (t, h), part): elements [64 part, 64 part + 64) of that row.
 template <int D, int FMT>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kPrefixThreads)
 prefix_kernel(const PrefixArgs a) {
-  constexpr int TPR = D / 32;                   // threads per row: 32 elements each
+  constexpr int TPR = D / 64;                   // threads per row
   constexpr int RB = D / 2, SB = D / 16;
+  __shared__ uint2 s_tab[FMT == KV4_NVFP4 ? 256 : 1];
   const int b = blockIdx.z;
   const int kind = blockIdx.y;
-  const uint32_t gtid = blockIdx.x * 256u + threadIdx.x;
-  const uint32_t row = gtid / TPR;              // (t, h), row < max_prefix_len * Hkv < 2^31
-  const int part = static_cast<int>(gtid % TPR);
-  const uint32_t t = fdiv(row, a.hkv_div);
-  const int h = static_cast<int>(row - t * static_cast<uint32_t>(a.Hkv));
+  const float s8 = __ldg(a.fp8_scale + kind);
+  if constexpr (FMT == KV4_NVFP4) {
+    s_tab[threadIdx.x] = nvfp4_scale_table(threadIdx.x, __ldg(a.gscale + kind), s8);
+    __syncthreads();
+  }
   int n = a.prefix_lens[b];
   const int cap = min(a.max_prefix_len, a.max_pages * a.P);
   if (n < 0 || n > cap) {
-    if (gtid == 0) set_error(a.err, KV4_EBOUNDS);
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_error(a.err, KV4_EBOUNDS);
     n = n < 0 ? 0 : cap;
   }
-  if (t >= static_cast<uint32_t>(n)) return;
-
-  const uint32_t pidx = fdiv(t, a.p_div);
-  const int page = __ldg(a.block_table + static_cast<int64_t>(b) * a.max_pages + pidx);
-  if (page < 0 || page >= a.num_pages) {
-    if (part == 0) set_error(a.err, KV4_EBOUNDS);
-    return;
-  }
-  const int off = static_cast<int>(t - pidx * static_cast<uint32_t>(a.P));
-  const uint8_t* chunk = a.pool + (static_cast<int64_t>(page) * a.Hkv + h) * a.chunk_bytes;
-  uint2 codes[2];
-  float sc[2];
-  if (FMT == KV4_NVFP4 && kind == 1) {
-    // V is stored in token pairs: byte d of pair row off/2 holds element d of
-    // this token in nibble off%2.  Gather the blocks' 32 nibbles back into
-    // the packed order (element 2j in the low nibble of byte j).
-    const uint4* src = reinterpret_cast<const uint4*>(
-        chunk + static_cast<int64_t>(a.P) * RB + static_cast<int64_t>(off >> 1) * D + part * 32);
-    const int sh = 4 * (off & 1);
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const uint4 w = src[k];
-      const uint32_t x0 = (w.x >> sh) & 0x0F0F0F0Fu, x1 = (w.y >> sh) & 0x0F0F0F0Fu;
-      const uint32_t x2 = (w.z >> sh) & 0x0F0F0F0Fu, x3 = (w.w >> sh) & 0x0F0F0F0Fu;
-      // byte pairs (n_2j, n_2j+1) -> one byte each, then keep bytes 0 and 2
-      codes[k].x = prmt(x0 | (x0 >> 4), x1 | (x1 >> 4), 0x6420u);
-      codes[k].y = prmt(x2 | (x2 >> 4), x3 | (x3 >> 4), 0x6420u);
-    }
-  } else {
-    const uint4 w = *reinterpret_cast<const uint4*>(
-        chunk + static_cast<int64_t>(kind) * a.P * RB + static_cast<int64_t>(off) * RB + part * 16);
-    codes[0] = make_uint2(w.x, w.y);
-    codes[1] = make_uint2(w.z, w.w);
-  }
-  if constexpr (FMT == KV4_NVFP4) {
-    // K: one scale row per token; V: pair rows, byte 2*blk + off%2
-    if (kind == 0) {
-      const uint8_t* sp = chunk + static_cast<int64_t>(a.P) * D + static_cast<int64_t>(off) * SB + 2 * part;
-      sc[0] = e4m3_to_f32(sp[0]);
-      sc[1] = e4m3_to_f32(sp[1]);
-    } else {
-      const uint8_t* sp = chunk + static_cast<int64_t>(a.P) * D + static_cast<int64_t>(a.P) * SB +
-                          static_cast<int64_t>(off >> 1) * 2 * SB + 4 * part + (off & 1);
-      sc[0] = e4m3_to_f32(sp[0]);
-      sc[1] = e4m3_to_f32(sp[2]);
-    }
-  } else {
-    sc[0] = sc[1] = *reinterpret_cast<const float*>(chunk + static_cast<int64_t>(a.P) * D +
-                                                    (static_cast<int64_t>(kind) * a.P + off) * 4);
-  }
-  const float s8 = __ldg(a.fp8_scale + kind);
+  const uint32_t items = static_cast<uint32_t>(n) * static_cast<uint32_t>(a.Hkv) * TPR;
+  const int64_t obase = a.cu_prefix[b];
+  const int32_t* table = a.block_table + static_cast<int64_t>(b) * a.max_pages;
+  uint8_t* out = kind == 0 ? a.out_k : a.out_v;
   const float r8 = __frcp_rn(s8);
-  const float g = (FMT == KV4_NVFP4) ? __ldg(a.gscale + kind) : 1.f;
-  const int64_t orow = a.cu_prefix[b] + t;
-  uint4* dst = reinterpret_cast<uint4*>((kind == 0 ? a.out_k : a.out_v) + (orow * a.Hkv + h) * D + part * 32);
-  dst[0] = prefix_block<D, FMT>(codes[0], sc[0], g, s8, r8);
-  dst[1] = prefix_block<D, FMT>(codes[1], sc[1], g, s8, r8);
+
+  for (uint32_t i = blockIdx.x * kPrefixThreads + threadIdx.x; i < items; i += gridDim.x * kPrefixThreads) {
+    const uint32_t row = i / TPR;
+    const int part = static_cast<int>(i % TPR);
+    const uint32_t t = fdiv(row, a.hkv_div);
+    const int h = static_cast<int>(row - t * static_cast<uint32_t>(a.Hkv));
+    const uint32_t pidx = fdiv(t, a.p_div);
+    const int page = __ldg(table + pidx);
+    if (page < 0 || page >= a.num_pages) {
+      if (part == 0) set_error(a.err, KV4_EBOUNDS);
+      continue;
+    }
+    const int off = static_cast<int>(t - pidx * static_cast<uint32_t>(a.P));
+    const uint8_t* chunk = a.pool + (static_cast<int64_t>(page) * a.Hkv + h) * a.chunk_bytes;
+    uint4* dst = reinterpret_cast<uint4*>(out + ((obase + t) * a.Hkv + h) * D + part * 64);
+    uint4 o[4];
+    if constexpr (FMT == KV4_NVFP4) {
+      if (kind == 0) {
+        const uint4* src = reinterpret_cast<const uint4*>(chunk + static_cast<int64_t>(off) * RB + part * 32);
+        const uint4 c0 = src[0], c1 = src[1];
+        // the four blocks' scale bytes, in order
+        const uint32_t sw = *reinterpret_cast<const uint32_t*>(chunk + static_cast<int64_t>(a.P) * D +
+                                                               static_cast<int64_t>(off) * SB + part * 4);
+        const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint2 tab = s_tab[(sw >> (8 * j)) & 0xFFu];
+          const uint2 lo = nvfp4_word(tab, cw[2 * j]), hi = nvfp4_word(tab, cw[2 * j + 1]);
+          o[j] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+        }
+      } else {
+        // V is stored in token pairs: byte d of pair row off/2 holds element d
+        // of this token in nibble off%2; scale byte 2 blk + off%2 of the pair
+        const uint4* src = reinterpret_cast<const uint4*>(
+            chunk + static_cast<int64_t>(a.P) * RB + static_cast<int64_t>(off >> 1) * D + part * 64);
+        const uint2 sw = *reinterpret_cast<const uint2*>(chunk + static_cast<int64_t>(a.P) * D +
+                                                         static_cast<int64_t>(a.P) * SB +
+                                                         static_cast<int64_t>(off >> 1) * 2 * SB + part * 8);
+        const int sh = 4 * (off & 1);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t sbw = j < 2 ? sw.x : sw.y;
+          const uint2 tab = s_tab[(sbw >> (16 * (j & 1) + 8 * (off & 1))) & 0xFFu];
+          const uint4 x = src[j];
+          o[j] = make_uint4(nvfp4_pair_word(tab, x.x, sh), nvfp4_pair_word(tab, x.y, sh),
+                            nvfp4_pair_word(tab, x.z, sh), nvfp4_pair_word(tab, x.w, sh));
+        }
+      }
+    } else {
+      const uint4* src = reinterpret_cast<const uint4*>(chunk + static_cast<int64_t>(kind) * a.P * RB +
+                                                        static_cast<int64_t>(off) * RB + part * 32);
+      const uint4 c0 = src[0], c1 = src[1];
+      const float s = *reinterpret_cast<const float*>(chunk + static_cast<int64_t>(a.P) * D +
+                                                      (static_cast<int64_t>(kind) * a.P + off) * 4);
+      // the row's tables: codes 0..7 and 8..15 (values -8..-1), x = RN(code * s)
+      const bool in_range = div_rn_in_range(r8, 16.f * fabsf(s));
+      const uint64_t ss = f2(s, s);
+      float xp[8], xn[8];
+#pragma unroll
+      for (int k = 0; k < 8; k += 2) {
+        f2_split(mul_f2(f2(static_cast<float>(k), static_cast<float>(k + 1)), ss), xp[k], xp[k + 1]);
+        f2_split(mul_f2(f2(static_cast<float>(k - 8), static_cast<float>(k - 7)), ss), xn[k], xn[k + 1]);
+      }
+      const uint2 tp = e4m3_table(xp, s8, r8, in_range), tn = e4m3_table(xn, s8, r8, in_range);
+      const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint2 lo = int4_word(tp, tn, cw[2 * j]), hi = int4_word(tp, tn, cw[2 * j + 1]);
+        o[j] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) dst[j] = o[j];
+  }
 }
 
 template <int D, int FMT>
 static cudaError_t launch_prefix_t(const PrefixArgs& a, cudaStream_t st) {
-  const int64_t threads = static_cast<int64_t>(a.max_prefix_len) * a.Hkv * (D / 32);
-  const int64_t blocks = (threads + 255) / 256;
-  prefix_kernel<D, FMT><<<dim3(static_cast<unsigned>(blocks), 2, a.B), 256, 0, st>>>(a);
+  const int64_t items = static_cast<int64_t>(a.max_prefix_len) * a.Hkv * (D / 64);
+  const int64_t need = (items + kPrefixThreads - 1) / kPrefixThreads;
+  // one wave of resident CTAs over all (kind, request) pairs; each strides
+  // over its request's rows
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, prefix_kernel<D, FMT>, kPrefixThreads, 0) !=
+            cudaSuccess || n < 1)
+      n = 4;
+    per_sm = n;
+  }
+  const int64_t target = (static_cast<int64_t>(a.sms) * per_sm + 2 * a.B - 1) / (2 * a.B);
+  const int64_t gx = need < target ? need : (target > 0 ? target : 1);
+  prefix_kernel<D, FMT><<<dim3(static_cast<unsigned>(gx), 2, a.B), kPrefixThreads, 0, st>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_prefix(const PrefixArgs& a_in, cudaStream_t st) {
-  const int64_t threads = static_cast<int64_t>(a_in.max_prefix_len) * a_in.Hkv * (a_in.D / 16);
-  if (threads == 0 || a_in.B == 0) return cudaSuccess;
+  if (a_in.max_prefix_len == 0 || a_in.B == 0) return cudaSuccess;
   PrefixArgs a = a_in;
   a.hkv_div = make_fastdiv(static_cast<uint32_t>(a.Hkv));
   a.p_div = make_fastdiv(static_cast<uint32_t>(a.P));

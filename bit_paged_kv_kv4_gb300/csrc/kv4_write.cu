@@ -48,7 +48,7 @@ __device__ __forceinline__ void write_row_part(const WriteArgs& a, int kind, int
     if (S != 0u && denom != 0.f) {
       const float rd = __frcp_rn(denom);
       float q[8];
-      if (rd < 1.0e30f && amax * rd < 1.0e30f) {
+      if (div_rn_in_range(rd, amax)) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) q[j] = div_rn_inrange(x[j], denom, rd);
       } else {                                  // operands near the FP32 range limits
@@ -86,7 +86,7 @@ __device__ __forceinline__ void write_row_part(const WriteArgs& a, int kind, int
     const float s = __ldg(a.gscale + kind);
     const float rs = __frcp_rn(s);
     float q[8];
-    if (rs < 1.0e30f && amax * rs < 1.0e30f) {
+    if (div_rn_in_range(rs, amax)) {
 #pragma unroll
       for (int j = 0; j < 8; ++j) q[j] = div_rn_inrange(x[j], s, rs);
     } else {                                    // operands near the FP32 range limits
@@ -108,7 +108,7 @@ __device__ __forceinline__ void write_row_part(const WriteArgs& a, int kind, int
     if (s != 0.f) {
       const float rs = __frcp_rn(s);
       float q[8];
-      if (rs < 1.0e30f && amax * rs < 1.0e30f) {
+      if (div_rn_in_range(rs, amax)) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) q[j] = div_rn_inrange(x[j], s, rs);
       } else {                                  // operands near the FP32 range limits
