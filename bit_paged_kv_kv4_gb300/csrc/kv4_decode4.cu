@@ -57,6 +57,10 @@ constexpr int kTT = 16;                    // tokens per tile
 constexpr int kCtas = 3;                   // resident CTAs per SM
 constexpr int kMaxSeg = 64;                // segments listed per pass
 constexpr float kLazy = 8.f;
+// Code words per row loaded at a time in the K and the NVFP4 V loops
+// (shorter live ranges against the 168-register budget of three CTAs).
+constexpr int KCW = 4;
+constexpr int VCW = 4;
 constexpr uint32_t kFull = 0xffffffffu;
 
 template <int D, int FMT>
@@ -467,6 +471,7 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
       // ---- running softmax state, heads g0 + 2tig + c, c = 0, 1 -------------------
       float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
       float sref = 0.f;       // INT4: largest V scale seen
+      float inv_sref = 1.f;   // and 1 / s_ref (1 until s_ref > 0)
       float o[MT][4];
 #pragma unroll
       for (int mi = 0; mi < MT; ++mi) o[mi][0] = o[mi][1] = o[mi][2] = o[mi][3] = 0.f;
@@ -488,24 +493,24 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
         sacc[0][0] = sacc[0][1] = sacc[0][2] = sacc[0][3] = 0.f;
         sacc[1][0] = sacc[1][1] = sacc[1][2] = sacc[1][3] = 0.f;
         {
-          constexpr int W = KB / 4, CW = W < 4 ? W : 4;     // words per row, per chunk
-          uint32_t sraw[2];
+          // KCW code words of each row at a time (word c of the thread's KB bytes
+          // sits at byte 4 (c % 4) of 16-byte unit c / 4)
+          constexpr int W = KB / 4, CW = KCW < W ? KCW : W;
+          uint32_t hs[2][4];         // NVFP4: f16x2 broadcasts of the row's blocks
           if constexpr (FMT == KV4_NVFP4) {
-            sraw[0] = load_scale_bytes<D / 64>(sst + ks_off);
-            sraw[1] = load_scale_bytes<D / 64>(sst + ks_off + 8 * SB);
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const uint32_t sraw = load_scale_bytes<D / 64>(sst + ks_off + 8 * SB * r);
+              e4m3x4_to_f16x2x2(prmt(sraw, 0u, 0x1100u), hs[r][0], hs[r][1]);
+              if constexpr (D / 64 > 2) e4m3x4_to_f16x2x2(prmt(sraw, 0u, 0x3322u), hs[r][2], hs[r][3]);
+            }
           }
 #pragma unroll
           for (int c0 = 0; c0 < W; c0 += CW) {
             uint32_t kw0[CW], kw1[CW];
-            const uint32_t ko = st + (c0 ? k_off1 : k_off0);
+            const uint32_t ko = st + ((c0 >> 2) ? k_off1 : k_off0) + 4 * (c0 & 3);
             load_bytes<4 * CW>(ko, kw0);
             load_bytes<4 * CW>(ko + 8 * RB, kw1);
-            uint32_t hs[2][2];       // NVFP4: f16x2 broadcasts of blocks c0/2, c0/2 + 1 of each row
-            if constexpr (FMT == KV4_NVFP4) {
-#pragma unroll
-              for (int r = 0; r < 2; ++r)
-                e4m3x4_to_f16x2x2(prmt(sraw[r], 0u, (c0 == 0) ? 0x1100u : 0x3322u), hs[r][0], hs[r][1]);
-            }
 #pragma unroll
             for (int jj = 0; jj < CW; ++jj) {
               const uint4 qv = lds128(qsm + (c0 + jj) * 512);
@@ -513,7 +518,7 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
                 uint32_t e0[4], e1[4];
                 e2m1x8_to_f16x2x4(kw0[jj], e0);
                 e2m1x8_to_f16x2x4(kw1[jj], e1);
-                const uint32_t s0 = hs[0][jj >> 1], s1 = hs[1][jj >> 1];
+                const uint32_t s0 = hs[0][(c0 + jj) >> 1], s1 = hs[1][(c0 + jj) >> 1];
                 mma_f16_16816(sacc[0], hmul2(e0[0], s0), hmul2(e1[0], s1), hmul2(e0[1], s0), hmul2(e1[1], s1),
                               qv.x, qv.y);
                 mma_f16_16816(sacc[1], hmul2(e0[2], s0), hmul2(e1[2], s1), hmul2(e0[3], s0), hmul2(e1[3], s1),
@@ -571,6 +576,7 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
             if (smax > sref) {
               corr_o[0] = corr_o[1] = (sref > 0.f) ? sref / smax : 0.f;
               sref = smax;
+              inv_sref = 1.f / sref;
             }
           }
 #pragma unroll
@@ -593,7 +599,6 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
         // weights and their f16 hi + lo split, transposed into the P^T B operand:
         // b0 <- tokens (2tig, 2tig+1) of head grp, b1 <- tokens (8+2tig, 8+2tig+1)
         uint32_t pb[2], pl[2];
-        const float inv_sref = (FMT == KV4_INT4_PTH && sref > 0.f) ? 1.f / sref : 1.f;
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           float w[2];
@@ -629,10 +634,10 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
             sab[0] &= mab; sab[1] &= mab;
             scd[0] &= mcd; scd[1] &= mcd;
           }
-          constexpr int W = D0S / 4, CW = W < 4 ? W : 4;
+          constexpr int W = D0S / 4, CW = VCW < W ? VCW : W;
 #pragma unroll
           for (int c0 = 0; c0 < W; c0 += CW) {
-            const uint32_t vo = st + (c0 ? vp_off1 : vp_off0);
+            const uint32_t vo = st + ((c0 >> 2) ? vp_off1 : vp_off0) + 4 * (c0 & 3);
             uint32_t wab[CW], wcd[CW];
             load_bytes<4 * CW>(vo, wab);
             load_bytes<4 * CW>(vo + 8 * RB, wcd);
