@@ -712,7 +712,7 @@ def time_k8v4(device, w, peak, reps=20):
     torch.cuda.empty_cache()
     q, _, _ = W.device_q(w, device)
     out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=device)
-    chunks = max(1, round(8 * torch.cuda.get_device_properties(device).multi_processor_count / (B * Hkv)))
+    chunks = 1           # one split range per unit: the persistent CTAs balance the tiles
     ws = torch.empty(K.kv4_k8v4_workspace_bytes(B, Hkv, D, chunks), dtype=torch.uint8, device=device)
     d_table, d_lens = torch.from_numpy(table).to(device), torch.from_numpy(lens).to(device)
 

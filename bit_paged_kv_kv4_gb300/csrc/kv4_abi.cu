@@ -174,6 +174,44 @@ kv4_status decode4_maps(const kv4_pool& p, CUtensorMap* codes, CUtensorMap* scal
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return fail(KV4_ECUDA, "cuTensorMapEncodeTiled is not available");
   const int rb = p.head_dim / 2;
+  auto swizzle_of = [](int row_bytes) {
+    return row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+         : row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+  };
+  if (p.fmt == KV4_K8V4) {
+    // K: [chunk][token][line][KHB] (FP8 rows of D bytes as lines of at most 128);
+    // V: [chunk][token][D/2] starting P*D bytes into each chunk.  The scales
+    // are read with plain bulk copies.
+    const int64_t nchunks = static_cast<int64_t>(p.num_pages) * p.num_kv_heads;
+    const int khb = p.head_dim < 128 ? p.head_dim : 128, kh = p.head_dim / khb;
+    const cuuint64_t cb = static_cast<cuuint64_t>(chunk_bytes_of(p));
+    cuuint32_t e4[4] = {1, 1, 1, 1};
+    {
+      cuuint64_t dims[4] = {static_cast<cuuint64_t>(khb), static_cast<cuuint64_t>(kh),
+                            static_cast<cuuint64_t>(p.page_size), static_cast<cuuint64_t>(nchunks)};
+      cuuint64_t strides[3] = {static_cast<cuuint64_t>(khb), static_cast<cuuint64_t>(p.head_dim), cb};
+      cuuint32_t box[4] = {static_cast<cuuint32_t>(khb), static_cast<cuuint32_t>(kh), 16, 1};
+      CUresult r = fn(codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, p.base, dims, strides, box, e4,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_of(khb), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS) return fail(KV4_ECUDA, "cuTensorMapEncodeTiled (k8v4 keys) failed (%d)", static_cast<int>(r));
+    }
+    {
+      cuuint64_t dims[3] = {static_cast<cuuint64_t>(rb), static_cast<cuuint64_t>(p.page_size),
+                            static_cast<cuuint64_t>(nchunks)};
+      cuuint64_t strides[2] = {static_cast<cuuint64_t>(rb), cb};
+      cuuint32_t box[3] = {static_cast<cuuint32_t>(rb), 16, 1};
+      void* vbase = static_cast<uint8_t*>(p.base) + static_cast<int64_t>(p.page_size) * p.head_dim;
+      CUresult r = fn(scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, vbase, dims, strides, box, e4,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_of(rb), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS) return fail(KV4_ECUDA, "cuTensorMapEncodeTiled (k8v4 values) failed (%d)", static_cast<int>(r));
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    cache[next] = Entry{p.base, bytes, p.page_size, p.head_dim, p.fmt, *codes, *scales, true};
+    next = (next + 1) % 8;
+    return KV4_OK;
+  }
   const int sb = p.fmt == KV4_NVFP4 ? p.head_dim / 16 : 4;
   const int srow = 16 * sb;
   if ((bytes / srow) >= (int64_t{1} << 31))
@@ -589,9 +627,11 @@ kv4_status kv4_k8v4_write(const void* k, const void* v, const int64_t* slot_mapp
 int64_t kv4_k8v4_workspace_bytes(int32_t batch, int32_t num_kv_heads, int32_t head_dim,
                                  int32_t num_chunks) {
   if (batch < 0 || num_kv_heads < 0 || head_dim < 0 || num_chunks < 1) return 0;
-  const int64_t slots = static_cast<int64_t>(batch) * num_kv_heads * num_chunks;
-  const int64_t o_bytes = slots * 8 * head_dim * 4;
-  return ((o_bytes + 255) / 256) * 256 + slots * 8 * 2 * 4;
+  // the layout of kv4_decode_attention's: tile offsets, piece states, piece
+  // outputs; a unit is one (request, kv head) with its <= 8 query heads
+  const int64_t slots = static_cast<int64_t>(sm_count()) * kv4::decode_max_ctas_per_sm() +
+                        static_cast<int64_t>(batch) * num_kv_heads * num_chunks;
+  return align256((static_cast<int64_t>(batch) + 1) * 8) + align256(slots * 8 * 16) + slots * 8 * head_dim * 4;
 }
 
 kv4_status kv4_k8v4_decode_attention(const void* q, const kv4_pool* pool, const float* key_scale,
@@ -620,38 +660,54 @@ kv4_status kv4_k8v4_decode_attention(const void* q, const kv4_pool* pool, const 
   if (q == nullptr || key_scale == nullptr || block_table == nullptr || seq_lens == nullptr ||
       out == nullptr || workspace == nullptr)
     return fail(KV4_EINVAL, "q, key_scale, block_table, seq_lens, workspace and out must be non-NULL");
-  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(workspace, 256))
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(workspace, 256) || !aligned(key_scale, 4) ||
+      !aligned(block_table, 4) || !aligned(seq_lens, 4))
     return fail(KV4_EINVAL, "q and out must be 16-byte aligned, workspace 256-byte aligned");
   const int64_t need = kv4_k8v4_workspace_bytes(batch, pool->num_kv_heads, pool->head_dim, num_chunks);
   if (workspace_bytes < need)
     return fail(KV4_EINVAL, "workspace of %lld bytes is smaller than the %lld needed",
                 static_cast<long long>(workspace_bytes), static_cast<long long>(need));
-  kv4::K8V4DecodeArgs a{};
-  a.q = static_cast<const __nv_bfloat16*>(q);
+  const int64_t units = static_cast<int64_t>(batch) * pool->num_kv_heads;
+
+  // the NVFP4 / INT4 decode kernel with FP8 keys and rotated queries, always
+  // through the combine (which rotates the output back)
+  kv4::DecodeArgs a{};
   a.pool = static_cast<const uint8_t*>(pool->base);
   a.chunk_bytes = chunk_bytes_of(*pool);
   a.P = pool->page_size;
   a.Hkv = pool->num_kv_heads;
   a.num_pages = pool->num_pages;
   a.D = pool->head_dim;
-  a.s_k = key_scale;
+  a.fmt = KV4_K8V4;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.gscale = key_scale;
   a.block_table = block_table;
   a.max_pages = max_pages;
   a.seq_lens = seq_lens;
   a.B = batch;
   a.Hq = num_q_heads;
   a.G = num_q_heads / pool->num_kv_heads;
-  a.nchunks = num_chunks;
   a.sm_scale = sm_scale;
-  const int64_t slots = static_cast<int64_t>(batch) * pool->num_kv_heads * num_chunks;
-  a.part_o = static_cast<float*>(workspace);
-  a.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                       ((slots * 8 * pool->head_dim * 4 + 255) / 256) * 256);
+  a.tile = kv4::decode_tile_tokens(KV4_K8V4);
+  const int64_t tiles_max = units * ((static_cast<int64_t>(max_pages) * pool->page_size + a.tile - 1) / a.tile);
+  const int64_t resident = static_cast<int64_t>(sm_count()) * kv4::decode_ctas_per_sm(KV4_K8V4);
+  int64_t n = (tiles_max + 11) / 12;       // at least a few tiles per compute warp
+  n = n < 1 ? 1 : (n > resident ? resident : n);
+  a.num_splits = num_chunks;
+  a.unit_ctas = 0;
+  a.n_cta = static_cast<int>(n);
+  const int64_t slots = static_cast<int64_t>(sm_count()) * kv4::decode_max_ctas_per_sm() + units * num_chunks;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  a.cum = reinterpret_cast<int64_t*>(w);
+  a.part_ml = reinterpret_cast<float*>(w + align256((static_cast<int64_t>(batch) + 1) * 8));
+  a.part_o = reinterpret_cast<float*>(w + align256((static_cast<int64_t>(batch) + 1) * 8) + align256(slots * 8 * 16));
   a.out = out;
   a.out_f32 = out_is_fp32 ? 1 : 0;
   a.err = error_word();
   if (a.err == nullptr) return fail(KV4_ECUDA, "no CUDA device / error word unavailable");
-  cudaError_t e = kv4::launch_k8v4_decode(a, static_cast<cudaStream_t>(stream));
+  CUtensorMap kmap, vmap;
+  if ((s = decode4_maps(*pool, &kmap, &vmap)) != KV4_OK) return s;
+  cudaError_t e = kv4::launch_decode(a, kmap, vmap, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KV4_OK : cuda_fail(e, "kv4_k8v4_decode_attention launch");
 }
 

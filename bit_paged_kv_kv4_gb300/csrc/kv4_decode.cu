@@ -963,7 +963,8 @@ combine_kernel(const DecodeArgs a) {
   }
   const int64_t T = a.cum[a.B];
   const int64_t start = a.cum[b] + static_cast<int64_t>(u - b * UPB) * n_u;
-  if (S == 1 && part_of(start, T, a.n_cta) == part_of(start + n_u - 1, T, a.n_cta)) return;  // written directly
+  if (a.fmt != KV4_K8V4 && S == 1 && part_of(start, T, a.n_cta) == part_of(start + n_u - 1, T, a.n_cta))
+    return;  // written directly
   const bool may_be_empty = T < a.n_cta;   // only then can a CTA range hold no tile
 
   // ---- list the pieces: split s holds CTAs part_of(x0)..part_of(x1-1) ----------
@@ -1055,15 +1056,40 @@ combine_kernel(const DecodeArgs a) {
   }
   s_o[tid] = acc;
   __syncthreads();
+  float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
   if (grp == 0) {
     for (int r = 1; r < groups; ++r) {
       const float4 v = s_o[r * cols + col];
       acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
     }
-    const float gv = (a.fmt != KV4_INT4_PTH) ? __ldg(a.gscale + 1) : 1.f;
+    // NVFP4 and FP8 carry the layer's V scale; INT4 and k8v4 put a scale per
+    // token into the weights
+    const float gv = (a.fmt == KV4_NVFP4 || a.fmt == KV4_FP8) ? __ldg(a.gscale + 1) : 1.f;
     const float inv = (l > 0.f && My != -INFINITY) ? gv * fast_exp2(My - Mx) / l : 0.f;
-    store_out4(a.out, a.out_f32, row * D + 4 * col,
-               make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+    res = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  }
+  if (a.fmt != KV4_K8V4) {
+    if (grp == 0) store_out4(a.out, a.out_f32, row * D + 4 * col, res);
+    return;
+  }
+  // k8v4: the pieces hold sum p V_rot; o = H o_rot with H = S_D / sqrt(D), the
+  // Walsh-Hadamard butterflies over the row in FP32
+  __shared__ float s_row[kCombineThreads * 4];
+  if (grp == 0) *reinterpret_cast<float4*>(s_row + 4 * col) = res;
+  for (int len = 1; len < D; len <<= 1) {
+    __syncthreads();
+    for (int p = tid; p < D / 2; p += kCombineThreads) {
+      float* v = s_row + (p / len) * 2 * len + (p % len);
+      const float x0 = v[0], x1 = v[len];
+      v[0] = __fadd_rn(x0, x1);
+      v[len] = __fsub_rn(x0, x1);
+    }
+  }
+  __syncthreads();
+  if (grp == 0) {
+    const float r = rsqrtf(static_cast<float>(D));
+    const float4 v = *reinterpret_cast<const float4*>(s_row + 4 * col);
+    store_out4(a.out, a.out_f32, row * D + 4 * col, make_float4(v.x * r, v.y * r, v.z * r, v.w * r));
   }
 }
 

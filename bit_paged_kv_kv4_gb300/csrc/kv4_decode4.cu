@@ -1,5 +1,5 @@
-// Paged decode attention over the NVFP4 and INT4 pools (the FP8 comparison
-// format runs the kernel in kv4_decode.cu).
+// Paged decode attention over the NVFP4 and INT4 pools and the k8v4 pool
+// (the FP8 comparison format runs the kernel in kv4_decode.cu).
 //
 // "SGLang's 4-bit KV cache", Figure 2: decode reads the 4-bit pool as it is
 // stored, block scales included, and dequantises inside the kernel; the
@@ -17,7 +17,7 @@
 // is written.
 //
 // Per warp, per tile:
-//  * a private ring of kNS stages filled by two TMA copies a tile: one 3-D box
+//  * a private ring of NS stages (3) filled by two TMA copies a tile: one 3-D box
 //    of the tile's 16 K code rows and 16 V code rows (swizzled so the
 //    fragment reads are bank-conflict free) and one of its K and V scale rows,
 //    both completing on the stage's mbarrier.  The page of the next tile comes
@@ -37,6 +37,17 @@
 //  * O^T += V^T P^T with dequantised V^T as the A operand: NVFP4 V is stored
 //    in token pairs, so one hardware E2M1 conversion of a stored byte is one
 //    A-fragment register (two tokens of one dim), times the pair's scales.
+//
+// k8v4 (keys FP8 E4M3 of D bytes a token under one FP32 scale, values INT4
+// with a scale per token, both rotated by H = S_D / sqrt(D)) runs the same
+// loop: its K box is a 4-D copy of the tile's key rows as lines of at most
+// 128 bytes, its V box a 3-D copy of the value rows and its 16 V scales one
+// 64-byte bulk copy, in two ring stages per warp (a stage is half as large
+// again).  The unit's queries are rotated at the segment's start (FP32
+// butterflies; the 1/sqrt(D) joins qk_scale) and kept as f16 hi + lo
+// fragments, so S^T takes two MMAs per k-step against the exact f16 keys;
+// the V scale rides on the weight as for INT4; the output always goes out as
+// pieces, and the combine rotates the merged row back.
 //
 // Every mbarrier wait is bounded (about a second); a warp that runs out
 // records KV4_ETIMEOUT, lets its copies in flight land (bounded), stops
@@ -65,25 +76,39 @@ constexpr uint32_t kFull = 0xffffffffu;
 
 template <int D, int FMT>
 struct Geo4 {
-  static constexpr int RB = D / 2;                               // code bytes per code row
+  static constexpr bool K8 = FMT == KV4_K8V4;                    // FP8 keys, INT4 values, rotated
+  static constexpr bool PTV = FMT != KV4_NVFP4;                  // a V scale per token (INT4, k8v4)
+  static constexpr int NS = K8 ? 2 : kNS;                        // ring stages per warp
+  static constexpr int RB = D / 2;                               // 4-bit code row bytes
+  static constexpr int KRB = K8 ? D : RB;                        // K row bytes
+  static constexpr int KHB = KRB < 128 ? KRB : 128;              // K line bytes (one swizzle span)
+  static constexpr int KH = KRB / KHB;                           // K lines per token
   static constexpr int SB = (FMT == KV4_NVFP4) ? D / 16 : 4;     // scale bytes per token
-  static constexpr int KB = D / 8;                               // K code bytes per thread per token
+  static constexpr int KB = K8 ? D / 4 : D / 8;                  // K code bytes per thread per token
+  static constexpr int KS = D / 16;                              // k-steps of S (16 dims each)
   static constexpr int VB = D / 16;
   static constexpr int MT = D / 16;                              // m-tiles of PV
-  static constexpr int CS = kTT * RB;                            // K (or V) code bytes of a tile
-  static constexpr int STC = 2 * CS;                             // code stage: K box, then V box
-  static constexpr int STS = 2 * kTT * SB;                       // scale stage: K rows, then V rows
+  static constexpr int CSK = kTT * KRB;                          // K code bytes of a tile
+  static constexpr int CS = kTT * RB;                            // V code bytes of a tile
+  static constexpr int STC = CSK + CS;                           // code stage: K box, then V box
+  static constexpr int STS = K8 ? kTT * 4 : 2 * kTT * SB;        // scale stage: (K rows), V rows
+  static constexpr int VS = K8 ? 0 : kTT * SB;                   // V scales inside the scale stage
   static constexpr int OFF_C = 0;
-  static constexpr int OFF_S = OFF_C + kNW * kNS * STC;
-  static constexpr int OFF_Q = (OFF_S + kNW * kNS * STS + 15) / 16 * 16;
-  static constexpr int QF = KB * 128;                            // query fragments (KB/4 x 32 lanes x 16 B)
+  static constexpr int OFF_S = OFF_C + kNW * NS * STC;
+  static constexpr int OFF_Q = (OFF_S + kNW * NS * STS + 15) / 16 * 16;
+  // query fragments: 16 bytes per lane for every k-step (k8v4: q_rot hi + lo)
+  // or for every two (one f16 query)
+  static constexpr int QF = K8 ? KS * 512 : KB * 128;
   static constexpr int AS = MT * 4 + 4;                          // merge row per lane (floats)
   static constexpr int OFF_ACC = OFF_Q + QF;
   static constexpr int OFF_META = OFF_ACC + 32 * AS * 4;
   static constexpr int OFF_SEG = (OFF_META + kNW * 8 * 3 * 4 + 15) / 16 * 16;
   static constexpr int OFF_RED = OFF_SEG + kMaxSeg * 24;
   static constexpr int OFF_BAR = OFF_RED + kNW * 8;
-  static constexpr int SMEM = OFF_BAR + kNW * kNS * 8 + 1024;
+  static constexpr int SMEM = OFF_BAR + kNW * NS * 8 + 1024;
+  // k8v4 rotates the unit's queries in the merge buffer (8 heads x D FP32)
+  static_assert(!K8 || 32 * AS * 4 >= 8 * D * 4, "query scratch");
+  static_assert(VS >= 0 && KH * KHB == KRB, "stage layout");
 };
 
 struct Seg {          // one piece: tiles [t0, t0 + n) of unit u, inside split `split`
@@ -195,20 +220,20 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
 
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - smem_u32(smem_raw));
-  const uint32_t cring = base + Gm::OFF_C + warp * kNS * Gm::STC;      // this warp's code stages
-  const uint32_t sring = base + Gm::OFF_S + warp * kNS * Gm::STS;      // and scale stages
+  const uint32_t cring = base + Gm::OFF_C + warp * Gm::NS * Gm::STC;  // this warp's code stages
+  const uint32_t sring = base + Gm::OFF_S + warp * Gm::NS * Gm::STS;  // and scale stages
   const uint32_t qsm = base + Gm::OFF_Q + lane * 16;                   // query fragment group j at + 512 j
   float* sAcc = reinterpret_cast<float*>(gbase + Gm::OFF_ACC);
   float* sMeta = reinterpret_cast<float*>(gbase + Gm::OFF_META);
   Seg* sSeg = reinterpret_cast<Seg*>(gbase + Gm::OFF_SEG);
   int64_t* sRed = reinterpret_cast<int64_t*>(gbase + Gm::OFF_RED);
-  const uint32_t bars = base + Gm::OFF_BAR + warp * kNS * 8;
+  const uint32_t bars = base + Gm::OFF_BAR + warp * Gm::NS * 8;
   __shared__ int s_nseg;
   __shared__ float s_qpre;
   __shared__ long long s_cursor, s_cum, s_b;
 
   if (lane == 0) {
-    for (int s2 = 0; s2 < kNS; ++s2) mbar_init(bars + 8 * s2, 1);
+    for (int s2 = 0; s2 < Gm::NS; ++s2) mbar_init(bars + 8 * s2, 1);
     fence_mbar_init();
   }
   if (tid == 0) {
@@ -257,8 +282,18 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
   const uint32_t vp_off1 = Gm::CS + swz<RB>(2 * tig + D0 / RB, D0 % RB + 16);
   const uint32_t vps_off = kTT * SB + tig * (D / 8) + 2 * (D0 / 16);
   // INT4 V (token rows): VB bytes at VB grp of rows 2tig, 2tig+1 (+8).
-  const uint32_t v_offa = Gm::CS + swz<RB>(2 * tig, VB * grp);
-  const uint32_t v_offb = Gm::CS + swz<RB>(2 * tig + 1, VB * grp);
+  const uint32_t v_offa = Gm::CSK + swz<RB>(2 * tig, VB * grp);
+  const uint32_t v_offb = Gm::CSK + swz<RB>(2 * tig + 1, VB * grp);
+  // k8v4 K (FP8, KH lines of KHB bytes a token): the 16-byte units of bytes
+  // [KB tig, KB (tig + 1)) of token grp; token grp + 8 is 8 KRB bytes on (the
+  // swizzle pattern repeats every 8 lines).
+  constexpr int KU = Gm::K8 ? Gm::KB / 16 : 1;
+  uint32_t k8_off[KU];
+#pragma unroll
+  for (int u = 0; u < KU; ++u) {
+    const int byte = Gm::KB * tig + 16 * u;
+    k8_off[u] = swz<Gm::KHB>(grp * Gm::KH + byte / Gm::KHB, byte % Gm::KHB);
+  }
 
   const uint64_t pol = policy_evict_first();
   int issued = 0, consumed = 0;     // warp-local tile counters
@@ -335,8 +370,9 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
     int p_first = 0, p_last = -1, win = 0, pg_cur = 0, pg_nxt = 0;
     int pi = 0, po = 0;               // page index and offset of the next tile's first token
     int c_pi = -1;                    // page whose TMA bases are cached below
-    uint32_t c_row = 0;               // code-row index of that page-head chunk
+    uint32_t c_row = 0;               // code-row index of that page-head chunk (k8v4: the chunk index)
     uint32_t c_srow = 0;              // scale-row index (16 SB bytes a row) of its K scales
+    const uint8_t* c_vs = nullptr;    // k8v4: the chunk's V scales
     const int32_t* bt = a.block_table;
 
     auto issue = [&]() {      // warp-uniform; issues the next tile of this pass
@@ -376,20 +412,34 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
           if (lane == 0) set_error(a.err, KV4_EBOUNDS);
           page = 0;
         }
-        const int64_t chunk = (static_cast<int64_t>(page) * a.Hkv + is_h) * a.chunk_bytes;
-        c_row = static_cast<uint32_t>(chunk / RB);
-        c_srow = static_cast<uint32_t>((chunk + static_cast<int64_t>(a.P) * 2 * RB) / (kTT * SB));
+        const int64_t ci = static_cast<int64_t>(page) * a.Hkv + is_h;
+        const int64_t chunk = ci * a.chunk_bytes;
+        if constexpr (Gm::K8) {
+          c_row = static_cast<uint32_t>(ci);
+          c_vs = a.pool + chunk + static_cast<int64_t>(a.P) * (Gm::KRB + RB);
+        } else {
+          c_row = static_cast<uint32_t>(chunk / RB);
+          c_srow = static_cast<uint32_t>((chunk + static_cast<int64_t>(a.P) * 2 * RB) / (kTT * SB));
+        }
         c_pi = pi;
       }
       if (lane == 0) {
         const uint32_t cst = cring + islot * Gm::STC, sst = sring + islot * Gm::STS;
         const uint32_t bar = bars + 8 * islot;
-        mbar_arrive_expect_tx(bar, kTT * (2 * RB + 2 * SB));
-        // the tile's K and V code rows (one 3-D box), then its K and V scale rows
-        tma_load_3d(cst, &cmap, 0, static_cast<int>(c_row) + po, 0, bar, pol);
-        tma_load_3d(sst, &smap, 0, static_cast<int>(c_srow) + po / kTT, 0, bar, pol);
+        mbar_arrive_expect_tx(bar, Gm::STC + Gm::STS);
+        if constexpr (Gm::K8) {
+          // the tile's K lines (4-D box: line, half, token, chunk), its V rows
+          // (3-D: row, token, chunk) and its 16 V scales (a 64-byte bulk copy)
+          tma_load_4d(cst, &cmap, 0, 0, po, static_cast<int>(c_row), bar, pol);
+          tma_load_3d(cst + Gm::CSK, &smap, 0, po, static_cast<int>(c_row), bar, pol);
+          bulk_load(sst, c_vs + 4 * po, Gm::STS, bar, pol);
+        } else {
+          // the tile's K and V code rows (one 3-D box), then its K and V scale rows
+          tma_load_3d(cst, &cmap, 0, static_cast<int>(c_row) + po, 0, bar, pol);
+          tma_load_3d(sst, &smap, 0, static_cast<int>(c_srow) + po / kTT, 0, bar, pol);
+        }
       }
-      islot = (islot + 1 == kNS) ? 0 : islot + 1;
+      islot = (islot + 1 == Gm::NS) ? 0 : islot + 1;
       po += kTT;                       // a tile never straddles a page: 16 divides P
       if (po == a.P) { po = 0; ++pi; }
       ++io;
@@ -397,7 +447,7 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
       ++i_pass;
     };
 
-    for (int k0 = 0; k0 < kNS && i_pass < i_total && !timed_out; ++k0) issue();
+    for (int k0 = 0; k0 < Gm::NS && i_pass < i_total && !timed_out; ++k0) issue();
 
     for (int k = 0; k < nseg; ++k) {
       const Seg sg = sSeg[k];
@@ -414,7 +464,56 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
       // Thread (grp, tig) of any warp uses query row g0 + grp, dims
       // [2 KB tig, 2 KB (tig + 1)); warp 0 converts them (bf16 -> f16, |q|
       // pre-scaled by an exact power of two into f16 range) into shared memory.
-      if (warp == 0) {
+      if constexpr (Gm::K8) {
+        // q_rot = S_D q (the Walsh-Hadamard butterflies in FP32; the 1/sqrt(D)
+        // goes into qk_scale), built for the unit's heads in the merge buffer
+        float* qs = sAcc;
+        for (int e = tid; e < 8 * D; e += kNW * 32) {
+          const int g = e / D;
+          qs[e] = (g < ng) ? __bfloat162float(a.q[(static_cast<int64_t>(b) * a.Hq + hq0 + g) * D + e % D]) : 0.f;
+        }
+        for (int len = 1; len < D; len <<= 1) {
+          __syncthreads();
+          for (int p2 = tid; p2 < 8 * (D / 2); p2 += kNW * 32) {
+            const int vec = p2 / (D / 2), r = p2 % (D / 2);
+            float* v = qs + vec * D + (r / len) * 2 * len + (r % len);
+            const float x0 = v[0], x1 = v[len];
+            v[0] = __fadd_rn(x0, x1);
+            v[len] = __fsub_rn(x0, x1);
+          }
+        }
+        __syncthreads();
+        // |q_rot| pre-scaled into f16 range by an exact power of two
+        float qmax = 0.f;
+        for (int e = tid; e < 8 * D; e += kNW * 32) qmax = fmaxf(qmax, fabsf(qs[e]));
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(kFull, qmax, o2));
+        if (lane == 0) sMeta[warp] = qmax;
+        __syncthreads();
+        qmax = fmaxf(fmaxf(sMeta[0], sMeta[1]), fmaxf(sMeta[2], sMeta[3]));
+        float qpre = 1.f;
+        if (qmax > 16384.f) {
+          int e;
+          frexpf(qmax / 16384.f, &e);
+          qpre = ldexpf(1.f, -e);
+        }
+        // B fragments of k-step j: head grp, dims KB tig + 4j .. + 3 (the dims
+        // of the lane's K word j), q_rot as f16 hi + lo
+        for (int j = warp; j < Gm::KS; j += kNW) {
+          const float* qq = qs + grp * D + KB * tig + 4 * j;
+          uint32_t hi[2], lo[2];
+#pragma unroll
+          for (int e2 = 0; e2 < 2; ++e2) {
+            const float v0 = qq[2 * e2] * qpre, v1 = qq[2 * e2 + 1] * qpre;
+            hi[e2] = pack_f16x2(v0, v1);
+            const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi[e2]));
+            lo[e2] = pack_f16x2(v0 - hf.x, v1 - hf.y);
+          }
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};"
+                       :: "r"(qsm + j * 512), "r"(hi[0]), "r"(hi[1]), "r"(lo[0]), "r"(lo[1]) : "memory");
+        }
+        if (tid == 0) s_qpre = qpre;
+      } else if (warp == 0) {
         constexpr int NG = KB / 4;
         uint4 raw[NG];
         const bool row_ok = grp < ng;
@@ -466,7 +565,9 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
         if (lane == 0) s_qpre = qpre;
       }
       __syncthreads();
-      const float qk_scale = a.sm_scale * ((FMT == KV4_NVFP4) ? __ldg(a.gscale) : 1.f) * 1.4426950408889634f / s_qpre;
+      // NVFP4: g_K; k8v4: s_K and the rotation's 1/sqrt(D); INT4: per token below
+      const float qk_scale = a.sm_scale * ((FMT != KV4_INT4_PTH) ? __ldg(a.gscale) : 1.f) *
+                             (Gm::K8 ? rsqrtf(static_cast<float>(D)) : 1.f) * 1.4426950408889634f / s_qpre;
 
       // ---- running softmax state, heads g0 + 2tig + c, c = 0, 1 -------------------
       float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
@@ -480,7 +581,7 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
         const uint32_t st = cring + cslot * Gm::STC, sst = sring + cslot * Gm::STS;
         if (!mbar_wait_bounded(bars + 8 * cslot, cphase)) {
           // give the copies still in flight a bounded chance to land, then stop
-          for (int j = consumed + 1; j < issued; ++j) mbar_wait_bounded(bars + 8 * (j % kNS), (j / kNS) & 1);
+          for (int j = consumed + 1; j < issued; ++j) mbar_wait_bounded(bars + 8 * (j % Gm::NS), (j / Gm::NS) & 1);
           timed_out = true;
           break;
         }
@@ -493,9 +594,27 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
         sacc[0][0] = sacc[0][1] = sacc[0][2] = sacc[0][3] = 0.f;
         sacc[1][0] = sacc[1][1] = sacc[1][2] = sacc[1][3] = 0.f;
         {
+          if constexpr (Gm::K8) {
+            // FP8 keys are exact in f16: one word (4 dims) of each row per
+            // k-step, against q_rot hi (chain 0) and lo (chain 1)
+#pragma unroll
+            for (int u = 0; u < KU; ++u) {
+              const uint4 x0 = lds128(st + k8_off[u]), x1 = lds128(st + k8_off[u] + 8 * Gm::KRB);
+              const uint32_t w0[4] = {x0.x, x0.y, x0.z, x0.w}, w1[4] = {x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+              for (int jj = 0; jj < 4; ++jj) {
+                uint32_t a0, a1, a2, a3;
+                e4m3x4_to_f16x2x2(w0[jj], a0, a2);
+                e4m3x4_to_f16x2x2(w1[jj], a1, a3);
+                const uint4 qv = lds128(qsm + (4 * u + jj) * 512);
+                mma_f16_16816(sacc[0], a0, a1, a2, a3, qv.x, qv.y);
+                mma_f16_16816(sacc[1], a0, a1, a2, a3, qv.z, qv.w);
+              }
+            }
+          }
           // KCW code words of each row at a time (word c of the thread's KB bytes
           // sits at byte 4 (c % 4) of 16-byte unit c / 4)
-          constexpr int W = KB / 4, CW = KCW < W ? KCW : W;
+          constexpr int W = Gm::K8 ? 0 : KB / 4, CW = KCW < W ? KCW : (W > 0 ? W : 1);
           uint32_t hs[2][4];         // NVFP4: f16x2 broadcasts of the row's blocks
           if constexpr (FMT == KV4_NVFP4) {
 #pragma unroll
@@ -556,21 +675,21 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
         // l rescaled.
         float sv[2];
         float smax = 0.f;
-        if constexpr (FMT == KV4_INT4_PTH) {
+        if constexpr (Gm::PTV) {
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
             const int t = grp + 8 * r;
-            const float v = __uint_as_float(lds32(sst + kTT * SB + 4 * t));
+            const float v = __uint_as_float(lds32(sst + Gm::VS + 4 * t));
             sv[r] = (t < valid && v > 0.f) ? v : 0.f;     // NaN, <= 0 and past the end: no weight
             smax = fmaxf(smax, sv[r]);
           }
         }
         float tmx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
         bool raise = tmx[0] > m_run[0] + kLazy || tmx[1] > m_run[1] + kLazy;
-        if constexpr (FMT == KV4_INT4_PTH) raise = raise || smax > sref;
+        if constexpr (Gm::PTV) raise = raise || smax > sref;
         if (__any_sync(kFull, raise)) {
           float corr_o[2] = {1.f, 1.f};
-          if constexpr (FMT == KV4_INT4_PTH) {
+          if constexpr (Gm::PTV) {
 #pragma unroll
             for (int o2 = 4; o2 < 32; o2 <<= 1) smax = fmaxf(smax, __shfl_xor_sync(kFull, smax, o2));
             if (smax > sref) {
@@ -609,7 +728,7 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
             const float p = fast_exp2(x[2 * r + c] - m_run[c]);
             l_run[c] += p;
             w[c] = p;
-            if constexpr (FMT == KV4_INT4_PTH) w[c] = p * (sv[r] * inv_sref);
+            if constexpr (Gm::PTV) w[c] = p * (sv[r] * inv_sref);
           }
           const uint32_t hi = pack_f16x2(w[0], w[1]);
           const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi));
@@ -687,7 +806,7 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
         }
         __syncwarp();
         ++consumed;
-        cslot = (cslot + 1 == kNS) ? 0 : cslot + 1;
+        cslot = (cslot + 1 == Gm::NS) ? 0 : cslot + 1;
         if (cslot == 0) cphase ^= 1u;
         if (i_pass < i_total) issue();     // refill the stage just freed
       }
@@ -712,7 +831,7 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
           float* mt = sMeta + (warp * 8 + 2 * tig + c) * 3;
           const bool some = l_run[c] > 0.f;
           float my = m_run[c];
-          if constexpr (FMT == KV4_INT4_PTH) my = (sref > 0.f) ? m_run[c] + fast_log2(sref) : -INFINITY;
+          if constexpr (Gm::PTV) my = (sref > 0.f) ? m_run[c] + fast_log2(sref) : -INFINITY;
           mt[0] = some ? m_run[c] : -INFINITY;
           mt[1] = some ? my : -INFINITY;
           mt[2] = l_run[c];
@@ -746,7 +865,8 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
         }
         __syncthreads();
       }
-      const bool direct = a.unit_ctas || (S == 1 && sg.t0 == 0 && sg.n == (L + kTT - 1) / kTT);
+      // k8v4 rotates the merged output back in the combine: always pieces
+      const bool direct = !Gm::K8 && (a.unit_ctas || (S == 1 && sg.t0 == 0 && sg.n == (L + kTT - 1) / kTT));
       const int64_t slot = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(sg.u) * S + sg.split;
       for (int e = tid * 4; e < ng * D; e += kNW * 32 * 4) {
         const int g = e / D, d = e % D;
@@ -816,6 +936,13 @@ int decode4_ctas_per_sm() { return kCtas; }
 
 cudaError_t launch_decode4(const DecodeArgs& a, const CUtensorMap& cmap, const CUtensorMap& smap,
                            cudaStream_t st) {
+  if (a.fmt == KV4_K8V4) {
+    switch (a.D) {
+      case 64: return launch4<64, KV4_K8V4>(a, cmap, smap, st);
+      case 128: return launch4<128, KV4_K8V4>(a, cmap, smap, st);
+      default: return launch4<256, KV4_K8V4>(a, cmap, smap, st);
+    }
+  }
   if (a.fmt == KV4_NVFP4) {
     switch (a.D) {
       case 64: return launch4<64, KV4_NVFP4>(a, cmap, smap, st);

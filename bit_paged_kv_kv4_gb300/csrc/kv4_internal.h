@@ -140,25 +140,7 @@ struct K8V4WriteArgs {
   const float* s_k;             // [1] FP8 key scale
   int* err;
 };
-struct K8V4DecodeArgs {
-  const __nv_bfloat16* q;       // [B][Hq][D]
-  const uint8_t* pool;
-  int64_t chunk_bytes;
-  int P, Hkv, num_pages, D;
-  const float* s_k;
-  const int32_t* block_table;   // [B][max_pages]
-  int max_pages;
-  const int32_t* seq_lens;      // [B]
-  int B, Hq, G, nchunks;
-  float sm_scale;
-  float* part_o;                // [B*Hkv*nchunks][8][D]
-  float* part_ml;               // [B*Hkv*nchunks][8][2]
-  void* out;
-  int out_f32;
-  int* err;
-};
 cudaError_t launch_k8v4_write(const K8V4WriteArgs& a, cudaStream_t st);
-cudaError_t launch_k8v4_decode(const K8V4DecodeArgs& a, cudaStream_t st);
 int decode_tile_tokens(int fmt);
 // Sets the message kv4_last_error_message() returns on this thread.
 void set_error_message(const char* msg);

@@ -334,12 +334,16 @@ kv4_status kv4_decode_attention_static_ws(const void* q, const kv4_pool* pool,
  * kv4_k8v4_decode_attention -- one decode step: q_rot = H q (bf16 q
  *   [B][Hq][D]), softmax(sm_scale * q_rot . K_hat_rot) over the request's
  *   tokens (block_table / seq_lens / max_pages as kv4_decode_attention),
- *   o = H (sum_t p_t V_hat_rot_t), out [B][Hq][D] bf16 or FP32.  Each
- *   request's tokens are cut into num_chunks ranges handled by separate CTAs
- *   and merged by a second kernel; workspace (256-byte aligned) of at least
- *   kv4_k8v4_workspace_bytes(B, Hkv, D, num_chunks) bytes.  At most 8 query
- *   heads per kv head (else KV4_EUNSUPPORTED).  An empty request gives a zero
- *   row.  Asynchronous on `stream`; allocates nothing.
+ *   o = H (sum_t p_t V_hat_rot_t), out [B][Hq][D] bf16 or FP32.  The
+ *   tiles of all (request, kv head) units are spread over one wave of
+ *   persistent CTAs as in kv4_decode_attention, num_chunks (>= 1) being the
+ *   number of split ranges per unit (num_splits there); the partial results
+ *   always go through the workspace, and a second kernel merges them and
+ *   applies H.  Workspace (256-byte aligned) of at least
+ *   kv4_k8v4_workspace_bytes(B, Hkv, D, num_chunks) bytes (it depends on the
+ *   device's SM count).  At most 8 query heads per kv head (else
+ *   KV4_EUNSUPPORTED).  An empty request gives a zero row.  Asynchronous on
+ *   `stream`; allocates nothing.
  */
 kv4_status kv4_k8v4_write(const void* k, const void* v, const int64_t* slot_mapping,
                           int64_t num_tokens, const kv4_pool* pool, const float* key_scale,

@@ -34,10 +34,25 @@ def test_fp8_kv_codes_saturate_and_repeat():
     assert not np.any((c.numpy() & 0x7F) == 0x7F)
 
 
+def _a256(x):
+    return (x + 255) // 256 * 256
+
+
 def test_k8v4_workspace_sizing():
+    """The k8v4 decode workspace has the layout of kv4_decode_attention's:
+    tile offsets [B+1] int64, then per slot 8 piece states of 16 bytes and 8
+    piece rows of D floats; slots = R + B*Hkv*S, R the device's resident CTAs
+    (a wave of persistent CTAs, one piece each at most per unit)."""
     import bit_paged_kv_kv4_gb300 as K
-    n = K.kv4_k8v4_workspace_bytes(16, 4, 256, 19)
-    slots = 16 * 4 * 19
-    o_bytes = slots * 8 * 256 * 4
-    assert n == ((o_bytes + 255) // 256) * 256 + slots * 8 * 2 * 4
-    assert K.kv4_k8v4_workspace_bytes(2, 2, 64, 0) == 0     # no chunks: nothing to size
+    B, Hkv, D = 16, 4, 256
+
+    def size(R, S):
+        slots = R + B * Hkv * S
+        return _a256((B + 1) * 8) + _a256(slots * 8 * 16) + slots * 8 * D * 4
+
+    n19 = K.kv4_k8v4_workspace_bytes(B, Hkv, D, 19)
+    R = next(r for r in range(1, 100000) if size(r, 19) >= n19)
+    assert size(R, 19) == n19
+    assert K.kv4_k8v4_workspace_bytes(B, Hkv, D, 20) == size(R, 20)
+    assert K.kv4_k8v4_workspace_bytes(B, Hkv, 64, 1) == _a256((B + 1) * 8) + _a256((R + B * Hkv) * 128) + (R + B * Hkv) * 8 * 64 * 4
+    assert K.kv4_k8v4_workspace_bytes(2, 2, 64, 0) == 0     # no split count: nothing to size
