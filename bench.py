@@ -83,12 +83,16 @@ def read_tensor_peak():
         return FALLBACK_BF16_TFLOPS, "fallback"
 
 
+DECODE_SOURCES = ("kv4_decode4.cu", "kv4_decode.cu", "kv4_device.cuh")
+
+
 def decode_source_hash():
-    """Hash of the decode kernel's code with comments and blank space removed,
-    so a recorded ncu traffic figure survives comment edits but not code
-    changes."""
+    """Hash of the decode kernels' code (the NVFP4 / INT4 / k8v4 kernel, the
+    FP8 split kernel and combine, their device helpers) with comments and
+    blank space removed, so a recorded ncu traffic figure survives comment
+    edits but not code changes."""
     h = hashlib.sha256()
-    for f in ("kv4_decode.cu", "kv4_device.cuh"):
+    for f in DECODE_SOURCES:
         with open(os.path.join(ROOT, "bit_paged_kv_kv4_gb300", "csrc", f)) as fh:
             src = fh.read()
         src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
@@ -536,7 +540,7 @@ def kv4_arm(args):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": recorded_traffic(w.name),
-                     "kernel": "kv4_decode_attention (split kernel + combine)",
+                     "kernel": "decode4_kernel<256, NVFP4> + combine_kernel (kv4_decode_attention)",
                      "peak_source": f"{peak_src} hbm_gbs", "decode_us": dec_avg * 1e6,
                      "decode_timing": f"mean of {args.steps} back-to-back decode calls between two CUDA "
                                       "events on the launching stream, after the timed steps",
@@ -561,7 +565,7 @@ def kv4_arm(args):
             bx = algorithmic_decode_bytes(wx, sx.lens)
             med = statistics.median(ts)
             extra[name] = {"decode_us": med * 1e6, "gbs": bx / med / 1e9, "frac": bx / med / 1e9 / peak,
-                           "num_splits": sx.splits, "kv_bytes": bx,
+                           "num_splits": sx.splits, "kv_bytes": bx, "traffic": recorded_traffic(name),
                            "tokens_per_s_16_layers": wx.batch / (16 * med)}
             if name == "fp8_32k":
                 # the comparison the pages draw: same shapes and lengths as the
@@ -579,6 +583,7 @@ def kv4_arm(args):
         extra["write_prefill_8k_int4"] = time_write_int4(device, peak)
         # the k8v4 variant on the headline shapes: FP8 keys, 4-bit values, rotated
         extra["k8v4_32k"] = time_k8v4(device, W.ALL["nvfp4_32k"], peak)
+        extra["k8v4_32k"]["traffic"] = recorded_traffic("k8v4_32k")
         torch.cuda.empty_cache()
         line["workloads"] = extra
 

@@ -1,15 +1,11 @@
-// Paged decode attention over the 4-bit pool, split over the sequence, and
-// the log-sum-exp combine of the pieces.
-//
-// "SGLang's 4-bit KV cache", Figure 2: decode consumes the 4-bit pool as it
-// is stored, block scales included; per the page's kernel section, its kernel
-// brings in the packed code tiles and their E4M3 scales, unpacks E2M1 with a
-// hardware conversion instruction and multiplies by the scales.  INT4 per-token-head follows "KV cache in 4 bits"
-// (section "What we changed"): one scale per token and head for K and for V.
+// Paged decode attention over the FP8 E4M3 per-tensor pool (the comparison
+// format the 4-bit cache is measured against), split over the sequence, and
+// the log-sum-exp combine of the pieces, which every format's decode uses
+// (the NVFP4, INT4 and k8v4 decode kernel is in kv4_decode4.cu).
 //
 // Work decomposition (GB300: 152 SMs, two CTAs of 4 warps resident on each):
 //  * A unit is (request b, kv head h, slice of <= 8 query heads of h's group);
-//    its work is ceil(seq_len / 32) tiles of 32 tokens.  All units' tiles are
+//    its work is ceil(seq_len / 16) tiles of 16 tokens.  All units' tiles are
 //    laid end to end in (b, h, slice, tile) order.
 //  * Balanced mode (num_splits != 1): one wave of persistent CTAs; CTA c takes
 //    the tiles [c*T/n, (c+1)*T/n) of the whole list, so every CTA streams the
@@ -22,24 +18,22 @@
 //  * Unit mode (num_splits == 1): one CTA per unit, output written directly,
 //    no workspace.
 //  * Inside a CTA, each segment (one piece) is divided among the 4 warps in
-//    contiguous runs of tiles; the warps' (m_x, l, m_y, o) states merge in
-//    shared memory in warp order (deterministic) at the end of the segment.
+//    contiguous runs of tiles; the warps' (m, l, o) states merge in shared
+//    memory in warp order (deterministic) at the end of the segment.
 //
 // Per warp (GB300 data path):
-//  * A private 2-stage ring in shared memory filled by TMA: the packed code
-//    rows of K and V arrive through 2-D tiled loads (16-row boxes, 32/64/128-
-//    byte swizzle, so the fragment reads are bank-conflict free), the scale
-//    rows through 1-D bulk copies; one mbarrier per stage, bounded waits.
-//    Block-table entries are prefetched one per lane, 32 pages ahead.
-//  * Dequantisation in registers straight into tensor-core fragments:
-//    E2M1 bytes -> f16x2 by the hardware conversion, times the E4M3 block
-//    scale (e2m1 * e4m3 is exact in f16); INT4 nibbles -> f16x2 by exponent
-//    bias arithmetic, with the per-token scales applied to the FP32 scores (K)
-//    and carried in the exponent of the PV weights (V).
-//  * S^T = K q^T with A = dequantised K (16 tokens per MMA) and B = the query
-//    slice; movmatrix turns the score tile into the P^T operand of
-//    O^T += V^T P^T (A = dequantised V^T, 16 head-dim rows per MMA).
-//    m16n8k16 f16 MMA, FP32 accumulate; PV weights as f16 hi + lo pairs.
+//  * A private 2-stage ring in shared memory filled by TMA: a token's D code
+//    bytes are two code rows of D/2, and the K and V rows arrive through 2-D
+//    tiled loads (boxes of 16 or 32 rows, 32/64/128-byte swizzle, so the
+//    fragment reads are bank-conflict free); one mbarrier per stage, bounded
+//    waits.  Block-table entries are prefetched one per lane, 32 pages ahead.
+//  * E4M3 -> f16x2 by the hardware conversion straight into tensor-core
+//    fragments (exact); the layer's K and V scales act on the scores and on
+//    the output.
+//  * S^T = K q^T with A = K (16 tokens per MMA) and B = the query slice;
+//    movmatrix turns the score tile into the P^T operand of O^T += V^T P^T
+//    (A = V^T, 16 head-dim rows per MMA).  m16n8k16 f16 MMA, FP32
+//    accumulate; PV weights as f16 hi + lo pairs.
 #include <cstdint>
 #include <utility>
 
@@ -61,18 +55,17 @@ constexpr uint32_t kFull = 0xffffffffu;
 
 template <int D, int FMT>
 struct Geo {
-  static constexpr int TT = (FMT == KV4_FP8) ? 16 : 32;        // tokens per tile
-  static constexpr int RPT = (FMT == KV4_FP8) ? 2 : 1;         // code rows per token
+  static_assert(FMT == KV4_FP8, "the split kernel decodes the FP8 pool");
+  static constexpr int TT = 16;                                // tokens per tile
+  static constexpr int RPT = 2;                                // code rows per token
   static constexpr int RB = D / 2;                             // code bytes per code row
-  static constexpr int SB = (FMT == KV4_NVFP4) ? D / 16 : (FMT == KV4_FP8) ? 0 : 4;  // scale bytes per token
+  static constexpr int SB = 0;                                 // scale bytes per token
   static constexpr int KB = D / 8;                             // K code bytes per thread per token
   static constexpr int VB = D / 16;                            // V code bytes per thread per token
   static constexpr int MT = D / 16;                            // m-tiles of PV
   static constexpr int STAGE_USED = TT * (2 * RPT * RB + 2 * SB);
   static constexpr int STAGE = (STAGE_USED + 1023) / 1024 * 1024;
   static constexpr int OFF_VC = TT * RPT * RB;
-  static constexpr int OFF_KS = 2 * TT * RPT * RB;
-  static constexpr int OFF_VS = 2 * TT * RPT * RB + TT * SB;
   static constexpr int RING = kNW * kNS * STAGE;
   static constexpr int AS = MT * 4 + 4;                        // merge row per lane (floats)
   static constexpr int ACC = 32 * AS * 4;                      // merged O of one segment
@@ -106,25 +99,6 @@ __device__ __forceinline__ void load_bytes(uint32_t a0, uint32_t a1, uint32_t* w
   } else {
     w[0] = lds32(a0);
   }
-}
-
-// Load `N` scale bytes (N in {1, 2, 4}) at shared address `addr`.
-template <int N>
-__device__ __forceinline__ uint32_t load_scale_bytes(uint32_t addr) {
-  if constexpr (N == 4) return lds32(addr);
-  else if constexpr (N == 2) return lds16(addr);
-  else return lds8(addr);
-}
-
-// INT4 two's-complement nibbles at bits 0-3 and 16-19 of `x` -> f16x2 codes.
-__device__ __forceinline__ uint32_t int4_lo_pair(uint32_t x) {
-  const uint32_t h = (x & 0x000F000Fu) ^ 0x64086408u;    // 1024 + (n ^ 8)
-  return hfma2(h, 0x3C003C00u, 0xE408E408u);              // * 1 - 1032
-}
-// INT4 nibbles at bits 4-7 and 20-23 of `x` -> f16x2 codes.
-__device__ __forceinline__ uint32_t int4_hi_pair(uint32_t x) {
-  const uint32_t h = ((x & 0x00F000F0u) ^ 0x00800080u) | 0x64006400u;  // 1024 + 16 (n ^ 8)
-  return hfma2(h, 0x2C002C00u, 0xD480D480u);              // / 16 - 72
 }
 
 __device__ __forceinline__ void store_out4(void* out, int out_f32, int64_t idx, float4 r) {
@@ -246,25 +220,7 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
   __syncthreads();
 
   // ---- per-thread shared-memory offsets inside a stage ----------------------
-  // K rows 16m + grp (+8): swizzled units of row grp; V rows 16kg + 2tig (+1, +8,
-  // +9): units of rows 2tig and 2tig+1; shifting by 8 rows keeps the pattern.
-  const uint32_t k_off0 = swz<RB>(grp, KB * tig);
-  const uint32_t k_off1 = swz<RB>(grp, KB * tig + 16);
-  const uint32_t v_offa = Gm::OFF_VC + swz<RB>(2 * tig, VB * grp);
-  const uint32_t v_offb = Gm::OFF_VC + swz<RB>(2 * tig + 1, VB * grp);
-  const uint32_t ks_off = Gm::OFF_KS + grp * SB + (D / 64) * tig;
-  const uint32_t vs_off = Gm::OFF_VS + 2 * tig * SB + (VB * grp) / 8;
-  // NVFP4 V in token-pair rows (2 code rows of RB bytes per pair, D/8 scale
-  // bytes per pair): thread (grp, tig) reads head dims [D0, D0 + D/8) of the
-  // pairs holding tokens (16kg + 2tig, +1) and (16kg + 2tig + 8, +9).
-  // Threads take the D/8-dim chunks in the order pi(grp) = 4 (grp & 1) + grp / 2,
-  // so the two groups sharing a quarter-warp read pair-row halves of opposite
-  // parity: their swizzled 16-byte units then fall in distinct banks.
-  constexpr int D0S = D / 8;                          // dims (= bytes) per thread
-  const int D0 = D0S * (4 * (grp & 1) + (grp >> 1));
-  const uint32_t vp_off0 = Gm::OFF_VC + swz<RB>(2 * tig + D0 / RB, D0 % RB);
-  const uint32_t vp_off1 = Gm::OFF_VC + swz<RB>(2 * tig + D0 / RB, D0 % RB + 16);
-  const uint32_t vps_off = Gm::OFF_VS + tig * (D / 8) + 2 * (D0 / 16);
+  constexpr int D0S = D / 8;                          // V dims (= bytes) per thread
   // FP8: token rows of D bytes (two code rows).  K: thread reads its D/4 bytes
   // of token rows grp (+8); V: its D/8 bytes (dims [D0f, D0f + D/8)) of token
   // rows 2tig, 2tig+1 (+8, +9).  Shifts by multiples of 8 code rows keep the
@@ -419,12 +375,6 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
             const int row = static_cast<int>(chunk / RB) + off * RPT;
             tma_load_2d(st + u * box * RB, &tmap, 0, row, bar, pol);
             tma_load_2d(st + Gm::OFF_VC + u * box * RB, &tmap, 0, row + a.P * RPT, bar, pol);
-            if constexpr (SB > 0) {
-              const uint8_t* sc = a.pool + chunk + static_cast<int64_t>(a.P) * 2 * RB;
-              bulk_load(st + Gm::OFF_KS + u * boxt * SB, sc + off * SB, boxt * SB, bar, pol);
-              bulk_load(st + Gm::OFF_VS + u * boxt * SB, sc + static_cast<int64_t>(a.P) * SB + off * SB,
-                        boxt * SB, bar, pol);
-            }
           }
         }
       }
@@ -478,32 +428,18 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
           frexpf(qmax / 16384.f, &e);
           qpre = ldexpf(1.f, -e);
         }
-        if constexpr (FMT != KV4_INT4_PTH) {
-          // k-step kk: k (2tig, 2tig+1) <-> d = base + 4kk + {0,1}; (2tig+8, +9) <-> + {2,3}
+        // k-step kk: k (2tig, 2tig+1) <-> d = base + 4kk + {0,1}; (2tig+8, +9) <-> + {2,3}
 #pragma unroll
-          for (int i = 0; i < QN / 2; ++i) qb[i] = pack_f16x2(qf[2 * i] * qpre, qf[2 * i + 1] * qpre);
-        } else {
-          // per 8 elements e: kk even: (e0,e4), (e1,e5); kk odd: (e2,e6), (e3,e7)
-#pragma unroll
-          for (int j = 0; j < QN / 8; ++j) {
-            const float* e = qf + 8 * j;
-            qb[4 * j + 0] = pack_f16x2(e[0] * qpre, e[4] * qpre);
-            qb[4 * j + 1] = pack_f16x2(e[1] * qpre, e[5] * qpre);
-            qb[4 * j + 2] = pack_f16x2(e[2] * qpre, e[6] * qpre);
-            qb[4 * j + 3] = pack_f16x2(e[3] * qpre, e[7] * qpre);
-          }
-        }
-        const float gk = (FMT != KV4_INT4_PTH) ? __ldg(a.gscale) : 1.f;
-        gv = (FMT != KV4_INT4_PTH) ? __ldg(a.gscale + 1) : 1.f;
+        for (int i = 0; i < QN / 2; ++i) qb[i] = pack_f16x2(qf[2 * i] * qpre, qf[2 * i + 1] * qpre);
+        const float gk = __ldg(a.gscale);
+        gv = __ldg(a.gscale + 1);
         qk_scale = a.sm_scale * gk * 1.4426950408889634f / qpre;   // base-2 logits
       }
 
       // ---- running softmax state (base 2), heads g0 + 2tig + c, c = 0, 1 ------
       // m_x: running max of the logits x_t, l_run = sum 2^(x_t - m_x) (partial
-      // over this thread's tokens).  The PV weights are w_t = 2^(y_t - m_y) with
-      // y_t = x_t (NVFP4) or x_t + log2 s_V(t) (INT4: the per-token V scale rides
-      // in the exponent, so every f16 operand stays in [0, 1]);
-      // out = 2^(m_y - m_x) * sum_t w_t code_t / l.
+      // over this thread's tokens); the PV weights are w_t = 2^(x_t - m_x) and
+      // out = s_V * sum_t w_t code_t / l (m_y = m_x for this format).
       m_x[0] = m_x[1] = m_y[0] = m_y[1] = -INFINITY;
       l_run[0] = l_run[1] = 0.f;
 #pragma unroll
@@ -526,61 +462,9 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
         // sacc[m]: c0 = (16m+grp, head 2tig), c1 = (16m+grp, 2tig+1),
         //          c2 = (16m+grp+8, 2tig),    c3 = (16m+grp+8, 2tig+1)
         float sacc[NM][4];
-        uint32_t kw[NM][2][KB / 4];
 #pragma unroll
-        for (int m = 0; m < NM; ++m) {
-          sacc[m][0] = sacc[m][1] = sacc[m][2] = sacc[m][3] = 0.f;
-          if constexpr (FMT != KV4_FP8) {
-            load_bytes<KB>(st + k_off0 + 16 * m * RB, st + k_off1 + 16 * m * RB, kw[m][0]);
-            load_bytes<KB>(st + k_off0 + (16 * m + 8) * RB, st + k_off1 + (16 * m + 8) * RB, kw[m][1]);
-          }
-        }
-        if constexpr (FMT == KV4_NVFP4) {
-          constexpr int NB = D / 64;              // block scales per token this thread needs
-          // hs[m][r][j]: f16x2 broadcast of block scale j of token 16m+grp+8r
-          uint32_t hs[NM][2][NB < 2 ? 2 : NB];
-#pragma unroll
-          for (int m = 0; m < NM; ++m) {
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              const uint32_t sc = load_scale_bytes<NB>(st + ks_off + (16 * m + 8 * r) * SB);
-#pragma unroll
-              for (int j = 0; j < NB; j += 2)   // bytes [s_j s_j s_j+1 s_j+1] -> two broadcasts
-                e4m3x4_to_f16x2x2(prmt(sc, 0u, (j == 0) ? 0x1100u : 0x3322u), hs[m][r][j],
-                                  hs[m][r][j + 1]);
-            }
-          }
-#pragma unroll
-          for (int j = 0; j < KB / 4; ++j) {      // word j: k-steps 2j (bytes 0, 1), 2j+1 (bytes 2, 3)
-#pragma unroll
-            for (int m = 0; m < NM; ++m) {
-              uint32_t c0[4], c1[4];
-              e2m1x8_to_f16x2x4(kw[m][0][j], c0);
-              e2m1x8_to_f16x2x4(kw[m][1][j], c1);
-              const uint32_t s0 = hs[m][0][j >> 1], s1 = hs[m][1][j >> 1];
-              mma_f16_16816(sacc[m], hmul2(c0[0], s0), hmul2(c1[0], s1), hmul2(c0[1], s0),
-                            hmul2(c1[1], s1), qb[4 * j], qb[4 * j + 1]);
-              mma_f16_16816(sacc[m], hmul2(c0[2], s0), hmul2(c1[2], s1), hmul2(c0[3], s0),
-                            hmul2(c1[3], s1), qb[4 * j + 2], qb[4 * j + 3]);
-            }
-          }
-        } else if constexpr (FMT == KV4_INT4_PTH) {
-#pragma unroll
-          for (int j = 0; j < KB / 4; ++j) {
-#pragma unroll
-            for (int m = 0; m < NM; ++m) {
-              const uint32_t w0 = kw[m][0][j], w1 = kw[m][1][j];
-              mma_f16_16816(sacc[m], int4_lo_pair(w0), int4_lo_pair(w1), int4_hi_pair(w0),
-                            int4_hi_pair(w1), qb[4 * j + 0], qb[4 * j + 1]);
-            }
-#pragma unroll
-            for (int m = 0; m < NM; ++m) {
-              const uint32_t w0 = kw[m][0][j] >> 8, w1 = kw[m][1][j] >> 8;
-              mma_f16_16816(sacc[m], int4_lo_pair(w0), int4_lo_pair(w1), int4_hi_pair(w0),
-                            int4_hi_pair(w1), qb[4 * j + 2], qb[4 * j + 3]);
-            }
-          }
-                } else {
+        for (int m = 0; m < NM; ++m) sacc[m][0] = sacc[m][1] = sacc[m][2] = sacc[m][3] = 0.f;
+        {
           // FP8: one E4M3 byte per element; the per-tensor scale is in qk_scale.
           // Word j of a row holds dims 4j..4j+3 of the thread's range = k-step j.
           constexpr int KW8 = D / 16;             // words per row (D/4 bytes)
@@ -605,39 +489,26 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
               mma_f16_16816(sacc[m], a0, a1, a2, a3, qb[2 * j], qb[2 * j + 1]);
             }
           }
-}
+        }
 
         // -------- online softmax (base 2) over this tile ----------------------
         // token of sacc[m][2r + c]: 16m + grp + 8r; head 2tig + c
-        float yv[NM][4];                 // INT4: exponent of the PV weight
-        float tmx[2] = {-INFINITY, -INFINITY}, tmy[2] = {-INFINITY, -INFINITY};
+        float tmx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
         for (int m = 0; m < NM; ++m) {
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
             const int t = 16 * m + grp + 8 * r;
-            float sk = 1.f, lsv = 0.f;
-            bool vok = true;
-            if constexpr (FMT == KV4_INT4_PTH) {
-              sk = __uint_as_float(lds32(st + Gm::OFF_KS + 4 * grp + 4 * (16 * m + 8 * r)));
-              const float sv = __uint_as_float(lds32(st + Gm::OFF_VS + 4 * grp + 4 * (16 * m + 8 * r)));
-              lsv = fast_log2(sv);                // sv == 0: no V weight
-              vok = sv > 0.f;
-            }
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-              float x = sacc[m][2 * r + c] * qk_scale * sk;
+              float x = sacc[m][2 * r + c] * qk_scale;
               x = (t < valid) ? x : -INFINITY;
               sacc[m][2 * r + c] = x;
               tmx[c] = fmaxf(tmx[c], x);
-              if constexpr (FMT == KV4_INT4_PTH) {
-                yv[m][2 * r + c] = (t < valid && vok) ? x + lsv : -INFINITY;
-                tmy[c] = fmaxf(tmy[c], yv[m][2 * r + c]);
-              }
             }
           }
         }
-        float corr_x[2], corr_y[2], mx_new[2], my_new[2];
+        float corr_x[2], mx_new[2];
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
 #pragma unroll
@@ -645,15 +516,7 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
           mx_new[c] = fmaxf(m_x[c], tmx[c]);            // finite: valid >= 1
           corr_x[c] = fast_exp2(m_x[c] - mx_new[c]);     // 0 when m_x == -inf
           m_x[c] = mx_new[c];
-          corr_y[c] = corr_x[c];
-          my_new[c] = mx_new[c];
-          if constexpr (FMT == KV4_INT4_PTH) {
-#pragma unroll
-            for (int o2 = 4; o2 < 32; o2 <<= 1) tmy[c] = fmaxf(tmy[c], __shfl_xor_sync(kFull, tmy[c], o2));
-            my_new[c] = fmaxf(m_y[c], tmy[c]);
-            corr_y[c] = (my_new[c] == -INFINITY) ? 1.f : fast_exp2(m_y[c] - my_new[c]);
-          }
-          m_y[c] = my_new[c];
+          m_y[c] = mx_new[c];
         }
         // P^T operand of PV per 16-token group m: b0 <- tokens (2tig, 2tig+1) of head grp,
         // b1 <- tokens (8+2tig, 8+2tig+1); transposed from the score layout with movmatrix.
@@ -669,8 +532,6 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
               const float p = fast_exp2(sacc[m][2 * r + c] - mx_new[c]);
               psum[c] += p;
               w[c] = p;
-              if constexpr (FMT == KV4_INT4_PTH)
-                w[c] = (my_new[c] == -INFINITY) ? 0.f : fast_exp2(yv[m][2 * r + c] - my_new[c]);
             }
             const uint32_t hi = pack_f16x2(w[0], w[1]);
             const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hi));
@@ -681,10 +542,10 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
         }
 #pragma unroll
         for (int c = 0; c < 2; ++c) l_run[c] = l_run[c] * corr_x[c] + psum[c];
-        if (__any_sync(kFull, corr_y[0] != 1.f || corr_y[1] != 1.f)) {
+        if (__any_sync(kFull, corr_x[0] != 1.f || corr_x[1] != 1.f)) {
 #pragma unroll
           for (int mi = 0; mi < MT; ++mi) {
-            o[mi][0] *= corr_y[0]; o[mi][1] *= corr_y[1]; o[mi][2] *= corr_y[0]; o[mi][3] *= corr_y[1];
+            o[mi][0] *= corr_x[0]; o[mi][1] *= corr_x[1]; o[mi][2] *= corr_x[0]; o[mi][3] *= corr_x[1];
           }
         }
 
@@ -692,42 +553,7 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
 #pragma unroll
         for (int kg = 0; kg < NM; ++kg) {
           const int ta = kg * 16 + 2 * tig;       // tokens ta, ta+1 (k 2tig..) and ta+8, ta+9
-          if constexpr (FMT == KV4_NVFP4) {
-            // byte d of a pair row -> f16x2 (element d of the even token, of the
-            // odd token): exactly an A-fragment register of V^T, no regrouping
-            uint32_t wab[D0S / 4], wcd[D0S / 4];
-            load_bytes<D0S>(st + vp_off0 + 16 * kg * RB, st + vp_off1 + 16 * kg * RB, wab);
-            load_bytes<D0S>(st + vp_off0 + (16 * kg + 8) * RB, st + vp_off1 + (16 * kg + 8) * RB, wcd);
-            // the pairs' block scales: bytes (s_even, s_odd) per block
-            constexpr int NSB = (D0S >= 32) ? 4 : 2;
-            const uint32_t xab = load_scale_bytes<NSB>(st + vps_off + kg * D);
-            const uint32_t xcd = load_scale_bytes<NSB>(st + vps_off + kg * D + D / 2);
-            // mask tokens past the end: a zero scale zeroes the (finite) codes
-            const uint32_t mab = ((ta < valid) ? 0xFFFFu : 0u) | ((ta + 1 < valid) ? 0xFFFF0000u : 0u);
-            const uint32_t mcd = ((ta + 8 < valid) ? 0xFFFFu : 0u) | ((ta + 9 < valid) ? 0xFFFF0000u : 0u);
-            uint32_t sab[2], scd[2];
-            e4m3x4_to_f16x2x2(xab, sab[0], sab[1]);
-            e4m3x4_to_f16x2x2(xcd, scd[0], scd[1]);
-            sab[0] &= mab; sab[1] &= mab;
-            scd[0] &= mcd; scd[1] &= mcd;
-#pragma unroll
-            for (int j = 0; j < D0S / 4; ++j) {
-              uint32_t f[4], h[4];
-              e2m1x8_to_f16x2x4(wab[j], f);
-              e2m1x8_to_f16x2x4(wcd[j], h);
-#pragma unroll
-              for (int hh = 0; hh < 2; ++hh) {
-                const int mi = 2 * j + hh;                 // dims D0 + 2mi, D0 + 2mi + 1
-                const int bj = (VB >= 8) ? mi / 8 : 0;     // block of this m-tile among the thread's
-                const uint32_t a0 = hmul2(f[2 * hh], sab[bj]);
-                const uint32_t a1 = hmul2(f[2 * hh + 1], sab[bj]);
-                const uint32_t a2 = hmul2(h[2 * hh], scd[bj]);
-                const uint32_t a3 = hmul2(h[2 * hh + 1], scd[bj]);
-                mma_f16_16816(o[mi], a0, a1, a2, a3, pb[kg][0], pb[kg][1]);
-                mma_f16_16816(o[mi], a0, a1, a2, a3, pl[kg][0], pl[kg][1]);
-              }
-            }
-          } else if constexpr (FMT == KV4_FP8) {
+          {
             // token rows: word j of each row holds dims D0f + 4j .. +3 of one
             // token; byte-interleave two tokens, then E4M3x2 -> f16x2 gives
             // the (token a, token b) operand registers of two m-tiles
@@ -758,26 +584,6 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
               mma_f16_16816(o[2 * j], ab0, ab1, cd0, cd1, pl[kg][0], pl[kg][1]);
               mma_f16_16816(o[2 * j + 1], ab2, ab3, cd2, cd3, pb[kg][0], pb[kg][1]);
               mma_f16_16816(o[2 * j + 1], ab2, ab3, cd2, cd3, pl[kg][0], pl[kg][1]);
-            }
-          } else {
-            uint32_t wa[VB / 4], wb[VB / 4], wc[VB / 4], wd[VB / 4];
-            load_bytes<VB>(st + v_offa + 16 * kg * RB, 0, wa);
-            load_bytes<VB>(st + v_offb + 16 * kg * RB, 0, wb);
-            load_bytes<VB>(st + v_offa + (16 * kg + 8) * RB, 0, wc);
-            load_bytes<VB>(st + v_offb + (16 * kg + 8) * RB, 0, wd);
-#pragma unroll
-            for (int j = 0; j < VB / 4; ++j) {
-#pragma unroll
-              for (int mm = 0; mm < 4; ++mm) {
-                const int mi = 4 * j + mm;
-                const uint32_t sel = mm | (mm << 4) | ((4 + mm) << 8) | ((4 + mm) << 12);
-                const uint32_t xab = prmt(wa[j], wb[j], sel);
-                const uint32_t xcd = prmt(wc[j], wd[j], sel);
-                const uint32_t a0 = int4_lo_pair(xab), a1 = int4_hi_pair(xab);
-                const uint32_t a2 = int4_lo_pair(xcd), a3 = int4_hi_pair(xcd);
-                mma_f16_16816(o[mi], a0, a1, a2, a3, pb[kg][0], pb[kg][1]);
-                mma_f16_16816(o[mi], a0, a1, a2, a3, pl[kg][0], pl[kg][1]);
-              }
             }
           }
         }
@@ -852,12 +658,11 @@ decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap
           const float mw = sMeta[(w * 8 + g) * 3 + 0];
           l += (mw == -INFINITY) ? 0.f : sMeta[(w * 8 + g) * 3 + 2] * fast_exp2(mw - Mx);
         }
-        // (d, g) lives in lane (grp, tig) with tig = g/2 and grp the group that
-        // holds dim chunk q = (d/2) / VB (q itself for INT4, pi^-1(q) for
-        // NVFP4), in o[mi][g%2] with mi = (d/2) % VB; d+1 in o[mi][g%2 + 2];
-        // d+2, d+3 in o[mi+1][...].
+        // (d, g) lives in lane (grp, tig) with tig = g/2 and grp = the dim chunk
+        // q = (d/2) / VB, in o[mi][g%2] with mi = (d/2) % VB; d+1 in
+        // o[mi][g%2 + 2]; d+2, d+3 in o[mi+1][...].
         const int hd = d >> 1, mi = hd % VB, c = g & 1;
-        const int q = hd / VB, gq = (FMT == KV4_NVFP4) ? 2 * (q & 3) + (q >> 2) : q;
+        const int gq = hd / VB;
         const float* row = sAcc + (gq * 4 + (g >> 1)) * Gm::AS + 4 * mi + c;
         const float4 acc = make_float4(row[0], row[2], row[4], row[6]);
         if (direct) {

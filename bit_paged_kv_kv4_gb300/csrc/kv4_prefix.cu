@@ -25,7 +25,8 @@
 // One thread converts 64 consecutive elements of one (token, head, K|V) row:
 // 32 code bytes (64 for the token-pair rows of NVFP4 V, of which this token's
 // nibbles are kept), one scale word, 64 bytes stored.  One wave of resident
-// CTAs strides over the rows, so the tables are built once per CTA.
+// CTAs strides over the rows, so the tables are built once per CTA, and each
+// thread loads its next item while it converts the current one.
 #include <cstdint>
 
 #include "kv4_device.cuh"
@@ -145,7 +146,7 @@ __device__ __forceinline__ uint2 int4_word(uint2 tp, uint2 tn, uint32_t w) {
 // CTA (gx, kind = blockIdx.y, request b = blockIdx.z); item i of request b =
 // (row = (t, h), part): elements [64 part, 64 part + 64) of that row.
 template <int D, int FMT>
-__global__ void __launch_bounds__(kPrefixThreads)
+__global__ void __launch_bounds__(kPrefixThreads, 4)
 prefix_kernel(const PrefixArgs a) {
   constexpr int TPR = D / 64;                   // threads per row
   constexpr int RB = D / 2, SB = D / 16;
@@ -169,7 +170,17 @@ prefix_kernel(const PrefixArgs a) {
   uint8_t* out = kind == 0 ? a.out_k : a.out_v;
   const float r8 = __frcp_rn(s8);
 
-  for (uint32_t i = blockIdx.x * kPrefixThreads + threadIdx.x; i < items; i += gridDim.x * kPrefixThreads) {
+  // Two-deep software pipeline: the next item's block-table entry and code
+  // loads are in flight while this item is converted and stored.
+  struct Item {
+    uint4 c[4];          // codes: K (and INT4) in c[0..1]; NVFP4 V pair rows in c[0..3]
+    uint2 sw;            // scale bytes (NVFP4) or the row scale's bits (INT4, in .x)
+    int sh;              // NVFP4 V: this token's nibble within the pair byte
+    uint4* dst;          // null: nothing to do
+  };
+  auto load = [&](uint32_t i, Item& it) {
+    it.dst = nullptr;
+    if (i >= items) return;
     const uint32_t row = i / TPR;
     const int part = static_cast<int>(i % TPR);
     const uint32_t t = fdiv(row, a.hkv_div);
@@ -178,69 +189,90 @@ prefix_kernel(const PrefixArgs a) {
     const int page = __ldg(table + pidx);
     if (page < 0 || page >= a.num_pages) {
       if (part == 0) set_error(a.err, KV4_EBOUNDS);
-      continue;
+      return;
     }
     const int off = static_cast<int>(t - pidx * static_cast<uint32_t>(a.P));
     const uint8_t* chunk = a.pool + (static_cast<int64_t>(page) * a.Hkv + h) * a.chunk_bytes;
-    uint4* dst = reinterpret_cast<uint4*>(out + ((obase + t) * a.Hkv + h) * D + part * 64);
-    uint4 o[4];
-    if constexpr (FMT == KV4_NVFP4) {
-      if (kind == 0) {
-        const uint4* src = reinterpret_cast<const uint4*>(chunk + static_cast<int64_t>(off) * RB + part * 32);
-        const uint4 c0 = src[0], c1 = src[1];
-        // the four blocks' scale bytes, in order
-        const uint32_t sw = *reinterpret_cast<const uint32_t*>(chunk + static_cast<int64_t>(a.P) * D +
-                                                               static_cast<int64_t>(off) * SB + part * 4);
-        const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    it.dst = reinterpret_cast<uint4*>(out + ((obase + t) * a.Hkv + h) * D + part * 64);
+    if (FMT == KV4_NVFP4 && kind == 1) {
+      // V is stored in token pairs: byte d of pair row off/2 holds element d
+      // of this token in nibble off%2; scale byte 2 blk + off%2 of the pair
+      const uint4* src = reinterpret_cast<const uint4*>(
+          chunk + static_cast<int64_t>(a.P) * RB + static_cast<int64_t>(off >> 1) * D + part * 64);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint2 tab = s_tab[(sw >> (8 * j)) & 0xFFu];
-          const uint2 lo = nvfp4_word(tab, cw[2 * j]), hi = nvfp4_word(tab, cw[2 * j + 1]);
-          o[j] = make_uint4(lo.x, lo.y, hi.x, hi.y);
-        }
-      } else {
-        // V is stored in token pairs: byte d of pair row off/2 holds element d
-        // of this token in nibble off%2; scale byte 2 blk + off%2 of the pair
-        const uint4* src = reinterpret_cast<const uint4*>(
-            chunk + static_cast<int64_t>(a.P) * RB + static_cast<int64_t>(off >> 1) * D + part * 64);
-        const uint2 sw = *reinterpret_cast<const uint2*>(chunk + static_cast<int64_t>(a.P) * D +
-                                                         static_cast<int64_t>(a.P) * SB +
-                                                         static_cast<int64_t>(off >> 1) * 2 * SB + part * 8);
-        const int sh = 4 * (off & 1);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t sbw = j < 2 ? sw.x : sw.y;
-          const uint2 tab = s_tab[(sbw >> (16 * (j & 1) + 8 * (off & 1))) & 0xFFu];
-          const uint4 x = src[j];
-          o[j] = make_uint4(nvfp4_pair_word(tab, x.x, sh), nvfp4_pair_word(tab, x.y, sh),
-                            nvfp4_pair_word(tab, x.z, sh), nvfp4_pair_word(tab, x.w, sh));
-        }
-      }
+      for (int j = 0; j < 4; ++j) it.c[j] = src[j];
+      it.sw = *reinterpret_cast<const uint2*>(chunk + static_cast<int64_t>(a.P) * D + static_cast<int64_t>(a.P) * SB +
+                                              static_cast<int64_t>(off >> 1) * 2 * SB + part * 8);
+      it.sh = off & 1;
     } else {
       const uint4* src = reinterpret_cast<const uint4*>(chunk + static_cast<int64_t>(kind) * a.P * RB +
                                                         static_cast<int64_t>(off) * RB + part * 32);
-      const uint4 c0 = src[0], c1 = src[1];
-      const float s = *reinterpret_cast<const float*>(chunk + static_cast<int64_t>(a.P) * D +
-                                                      (static_cast<int64_t>(kind) * a.P + off) * 4);
-      // the row's tables: codes 0..7 and 8..15 (values -8..-1), x = RN(code * s)
-      const bool in_range = div_rn_in_range(r8, 16.f * fabsf(s));
-      const uint64_t ss = f2(s, s);
-      float xp[8], xn[8];
-#pragma unroll
-      for (int k = 0; k < 8; k += 2) {
-        f2_split(mul_f2(f2(static_cast<float>(k), static_cast<float>(k + 1)), ss), xp[k], xp[k + 1]);
-        f2_split(mul_f2(f2(static_cast<float>(k - 8), static_cast<float>(k - 7)), ss), xn[k], xn[k + 1]);
-      }
-      const uint2 tp = e4m3_table(xp, s8, r8, in_range), tn = e4m3_table(xn, s8, r8, in_range);
-      const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint2 lo = int4_word(tp, tn, cw[2 * j]), hi = int4_word(tp, tn, cw[2 * j + 1]);
-        o[j] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+      it.c[0] = src[0];
+      it.c[1] = src[1];
+      if constexpr (FMT == KV4_NVFP4) {
+        // the four blocks' scale bytes, in order
+        it.sw.x = *reinterpret_cast<const uint32_t*>(chunk + static_cast<int64_t>(a.P) * D +
+                                                     static_cast<int64_t>(off) * SB + part * 4);
+      } else {
+        it.sw.x = *reinterpret_cast<const uint32_t*>(chunk + static_cast<int64_t>(a.P) * D +
+                                                     (static_cast<int64_t>(kind) * a.P + off) * 4);
       }
     }
+  };
+
+  const uint32_t stride = gridDim.x * kPrefixThreads;
+  Item cur, nxt;
+  uint32_t i = blockIdx.x * kPrefixThreads + threadIdx.x;
+  load(i, cur);
+  for (; i < items; i += stride) {
+    load(i + stride, nxt);
+    if (cur.dst != nullptr) {
+      uint4 o[4];
+      if constexpr (FMT == KV4_NVFP4) {
+        if (kind == 0) {
+          const uint32_t cw[8] = {cur.c[0].x, cur.c[0].y, cur.c[0].z, cur.c[0].w,
+                                  cur.c[1].x, cur.c[1].y, cur.c[1].z, cur.c[1].w};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) dst[j] = o[j];
+          for (int j = 0; j < 4; ++j) {
+            const uint2 tab = s_tab[(cur.sw.x >> (8 * j)) & 0xFFu];
+            const uint2 lo = nvfp4_word(tab, cw[2 * j]), hi = nvfp4_word(tab, cw[2 * j + 1]);
+            o[j] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+          }
+        } else {
+          const int sh = 4 * cur.sh;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t sbw = j < 2 ? cur.sw.x : cur.sw.y;
+            const uint2 tab = s_tab[(sbw >> (16 * (j & 1) + 8 * cur.sh)) & 0xFFu];
+            const uint4 x = cur.c[j];
+            o[j] = make_uint4(nvfp4_pair_word(tab, x.x, sh), nvfp4_pair_word(tab, x.y, sh),
+                              nvfp4_pair_word(tab, x.z, sh), nvfp4_pair_word(tab, x.w, sh));
+          }
+        }
+      } else {
+        const float s = __uint_as_float(cur.sw.x);
+        // the row's tables: codes 0..7 and 8..15 (values -8..-1), x = RN(code * s)
+        const bool in_range = div_rn_in_range(r8, 16.f * fabsf(s));
+        const uint64_t ss = f2(s, s);
+        float xp[8], xn[8];
+#pragma unroll
+        for (int k = 0; k < 8; k += 2) {
+          f2_split(mul_f2(f2(static_cast<float>(k), static_cast<float>(k + 1)), ss), xp[k], xp[k + 1]);
+          f2_split(mul_f2(f2(static_cast<float>(k - 8), static_cast<float>(k - 7)), ss), xn[k], xn[k + 1]);
+        }
+        const uint2 tp = e4m3_table(xp, s8, r8, in_range), tn = e4m3_table(xn, s8, r8, in_range);
+        const uint32_t cw[8] = {cur.c[0].x, cur.c[0].y, cur.c[0].z, cur.c[0].w,
+                                cur.c[1].x, cur.c[1].y, cur.c[1].z, cur.c[1].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint2 lo = int4_word(tp, tn, cw[2 * j]), hi = int4_word(tp, tn, cw[2 * j + 1]);
+          o[j] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) cur.dst[j] = o[j];
+    }
+    cur = nxt;
   }
 }
 

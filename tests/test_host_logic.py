@@ -11,13 +11,17 @@ def test_decode_hash_ignores_comments_and_blank_space(tmp_path, monkeypatch):
     src = tmp_path / "bit_paged_kv_kv4_gb300" / "csrc"
     src.mkdir(parents=True)
     (src / "kv4_decode.cu").write_text("int f(int x) { return x + 1; }  // one\n/* block */\n")
+    (src / "kv4_decode4.cu").write_text("int g(int x) { return x; }\n")
     (src / "kv4_device.cuh").write_text("#pragma once\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     h0 = bench.decode_source_hash()
     (src / "kv4_decode.cu").write_text("int f(int x) {\n  return x + 1;  // two\n}\n")
     assert bench.decode_source_hash() == h0                 # comments and layout only
     (src / "kv4_decode.cu").write_text("int f(int x) { return x + 2; }\n")
-    assert bench.decode_source_hash() != h0                 # code changed
+    h1 = bench.decode_source_hash()
+    assert h1 != h0                                         # code changed
+    (src / "kv4_decode4.cu").write_text("int g(int x) { return -x; }\n")
+    assert bench.decode_source_hash() != h1                 # either kernel file counts
 
 
 def test_fp8_kv_codes_saturate_and_repeat():
