@@ -577,10 +577,12 @@ def kv4_arm(args):
                 extra["extend_160k"] = time_extend(device, wx, ws, read_tensor_peak()[0])
                 del ws
                 extra["write_prefill_8k"] = time_write_prefill(sx, wx, peak)
+                extra["write_prefill_128k"] = time_write_prefill(sx, wx, peak, T=131072)
             del sx
             torch.cuda.empty_cache()
         extra["calibrate_64k"] = time_calibrate(device, peak)
         extra["write_prefill_8k_int4"] = time_write_int4(device, peak)
+        extra["write_prefill_256k_int4"] = time_write_int4(device, peak, T=262144)
         # the k8v4 variant on the headline shapes: FP8 keys, 4-bit values, rotated
         extra["k8v4_32k"] = time_k8v4(device, W.ALL["nvfp4_32k"], peak)
         extra["k8v4_32k"]["traffic"] = recorded_traffic("k8v4_32k")
@@ -768,8 +770,11 @@ def time_write_int4(device, peak, T=8192):
         ts.append(a.elapsed_time(b) * 1e-3)
     med = statistics.median(ts)
     byts = algorithmic_write_bytes(w, T)
+    in_mb = T * w.num_kv_heads * w.head_dim * 2 * 2 / 1e6
+    out_mb = (byts - T * w.num_kv_heads * w.head_dim * 2 * 2) / 1e6
+    l2 = "smaller than L2, so this is an L2-warm figure" if in_mb + out_mb < 129 else "larger than L2"
     return {"tokens": T, "us": med * 1e6, "gbs": byts / med / 1e9, "frac": byts / med / 1e9 / peak,
-            "note": "8 MB in, 4.3 MB out: smaller than L2, so this is an L2-warm figure"}
+            "note": f"{in_mb:.0f} MB in, {out_mb:.1f} MB out: {l2}"}
 
 
 def time_calibrate(device, peak, T=65536, Hkv=4, D=256):
@@ -797,10 +802,13 @@ def time_calibrate(device, peak, T=65536, Hkv=4, D=256):
     return {"tokens": T, "us": med * 1e6, "gbs": byts / med / 1e9, "frac": byts / med / 1e9 / peak}
 
 
-def time_write_prefill(s, w, peak):
+def time_write_prefill(s, w, peak, T=None):
+    """Prefill write of T tokens (default: the workload's 8K chunk) of bf16
+    K/V into a scratch pool of the workload's geometry, then the same from
+    FP8 K/V: CUDA-event medians of 10 calls after 3 warm-up calls."""
     import torch
     K = s.K
-    T = w.prefix_chunk
+    T = T or w.prefix_chunk
     gen = torch.Generator(device=s.device).manual_seed(7)
     k = torch.randn((T, w.num_kv_heads, w.head_dim), generator=gen, device=s.device).to(torch.bfloat16)
     v = torch.randn((T, w.num_kv_heads, w.head_dim), generator=gen, device=s.device).to(torch.bfloat16)
@@ -838,10 +846,12 @@ def time_write_prefill(s, w, peak):
         t8.append(a.elapsed_time(b) * 1e-3)
     m8 = statistics.median(t8)
     b8 = algorithmic_write_bytes(w, T, in_bytes=1)
+    in_mb = T * w.num_kv_heads * w.head_dim * 2 * 2 / 1e6
+    out_mb = (byts - T * w.num_kv_heads * w.head_dim * 2 * 2) / 1e6
+    l2 = "smaller than L2, so these are L2-warm figures" if in_mb + out_mb < 129 else "larger than L2"
     return {"tokens": T, "us": med * 1e6, "gbs": byts / med / 1e9, "frac": byts / med / 1e9 / peak,
-            "fp8_input_us": m8 * 1e6, "fp8_input_gbs": b8 / m8 / 1e9,
-            "note": "16 MB in (8 MB with FP8 input), 9.4 MB out: smaller than L2, so these are "
-                    "L2-warm figures"}
+            "fp8_input_us": m8 * 1e6, "fp8_input_gbs": b8 / m8 / 1e9, "fp8_input_frac": b8 / m8 / 1e9 / peak,
+            "note": f"{in_mb:.0f} MB in ({in_mb / 2:.0f} MB with FP8 input), {out_mb:.1f} MB out: {l2}"}
 
 
 def main():
@@ -888,7 +898,9 @@ def only_arm(args):
         lite = types.SimpleNamespace(device=device, K=K,
                                      g=torch.tensor([1.0 / (6 * 448)] * 2, dtype=torch.float32, device=device))
         r = time_write_prefill(lite, w, peak)
+        r["128k"] = time_write_prefill(lite, w, peak, T=131072)
         r["int4"] = time_write_int4(device, peak)
+        r["int4_256k"] = time_write_int4(device, peak, T=262144)
     if K.kv4_device_error() != 0:
         raise SystemExit(f"device error {K.kv4_device_error()}")
     print(json.dumps({"only": args.only, "workload": w.name, **r}))
