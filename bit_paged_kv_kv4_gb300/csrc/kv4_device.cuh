@@ -336,6 +336,55 @@ __device__ __forceinline__ float div_rn_inrange(float a, float b, float yb) {
   return copysignf(__fmaf_rn(r, yb, q0), a);
 }
 
+// Packed FP32 pairs: each lane of mul.rn / fma.rn .f32x2 is the IEEE
+// round-to-nearest result of the scalar operation, so pairs give the same
+// bits as two scalar instructions at half the issue cost.
+__device__ __forceinline__ uint64_t f2(float x, float y) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& x, float& y) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(v));
+}
+__device__ __forceinline__ uint64_t mul_f2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma_f2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// RN(a / b) for a pair (div_rn_inrange on each lane, Markstein's correction
+// step): q0 = a yb, r = a - b q0 (exact under fma), q = q0 + r yb; the sign of
+// a zero quotient follows a.  nb = (-b, -b), yb2 = (yb, yb) with yb = RN(1/b).
+__device__ __forceinline__ void div_rn_pair(float a0, float a1, uint64_t nb, uint64_t yb2, float& q0o,
+                                            float& q1o) {
+  const uint64_t a = f2(a0, a1);
+  const uint64_t q0 = mul_f2(a, yb2);
+  const uint64_t r = fma_f2(nb, q0, a);
+  f2_split(fma_f2(r, yb2, q0), q0o, q1o);
+  q0o = __uint_as_float((__float_as_uint(q0o) & 0x7FFFFFFFu) | (__float_as_uint(a0) & 0x80000000u));
+  q1o = __uint_as_float((__float_as_uint(q1o) & 0x7FFFFFFFu) | (__float_as_uint(a1) & 0x80000000u));
+}
+
+// Eight FP32 values -> eight E2M1 codes, element i in nibble i.
+__device__ __forceinline__ uint32_t f32x8_to_e2m1x8(const float* q) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(q[0]), "f"(q[1]), "f"(q[2]), "f"(q[3]), "f"(q[4]), "f"(q[5]), "f"(q[6]), "f"(q[7]));
+  return r;
+}
+
 // ------------------------------------------------------------ misc
 __device__ __forceinline__ float fast_log2(float x) {
   float r;

@@ -36,41 +36,6 @@ namespace kv4 {
 
 constexpr int kPrefixThreads = 256;
 
-// Packed FP32 pairs: each lane of mul.rn / fma.rn .f32x2 is the IEEE
-// round-to-nearest result of the scalar operation, so pairs give the same
-// bits as two scalar instructions at half the issue cost.
-__device__ __forceinline__ uint64_t f2(float x, float y) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
-  return r;
-}
-__device__ __forceinline__ void f2_split(uint64_t v, float& x, float& y) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(v));
-}
-__device__ __forceinline__ uint64_t mul_f2(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t fma_f2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-
-// RN(a / b) for a pair (div_rn_inrange on each lane, Markstein's correction
-// step): q0 = a yb, r = a - b q0 (exact under fma), q = q0 + r yb; the sign of
-// a zero quotient follows a.  nb = (-b, -b), yb2 = (yb, yb) with yb = RN(1/b).
-__device__ __forceinline__ void div_rn_pair(float a0, float a1, uint64_t nb, uint64_t yb2, float& q0o,
-                                            float& q1o) {
-  const uint64_t a = f2(a0, a1);
-  const uint64_t q0 = mul_f2(a, yb2);
-  const uint64_t r = fma_f2(nb, q0, a);
-  f2_split(fma_f2(r, yb2, q0), q0o, q1o);
-  q0o = __uint_as_float((__float_as_uint(q0o) & 0x7FFFFFFFu) | (__float_as_uint(a0) & 0x80000000u));
-  q1o = __uint_as_float((__float_as_uint(q1o) & 0x7FFFFFFFu) | (__float_as_uint(a1) & 0x80000000u));
-}
-
 __device__ __forceinline__ uint2 pack_e4m3x8(const float (&q)[8]) {
   return make_uint2(f32x2_to_e4m3x2(q[0], q[1]) | (f32x2_to_e4m3x2(q[2], q[3]) << 16),
                     f32x2_to_e4m3x2(q[4], q[5]) | (f32x2_to_e4m3x2(q[6], q[7]) << 16));

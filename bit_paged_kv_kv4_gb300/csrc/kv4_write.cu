@@ -33,10 +33,21 @@ namespace kv4 {
 
 // E2M1 codes of 16 quotients, element 2j in the low nibble of byte j.
 __device__ __forceinline__ uint2 e2m1x16(const float (&q)[16]) {
-  uint32_t w[2] = {0u, 0u};
+  return make_uint2(f32x8_to_e2m1x8(q), f32x8_to_e2m1x8(q + 8));
+}
+
+// q_j = RN(x_j / b) for 16 values, b > 0 with yb = RN(1/b): div_rn on FP32
+// pairs where div_rn_in_range(yb, amax) holds (amax >= every |x_j|), else
+// the IEEE division.
+__device__ __forceinline__ void div16(const float (&x)[16], float b, float yb, float amax, float (&q)[16]) {
+  if (div_rn_in_range(yb, amax)) {
+    const uint64_t nb = f2(-b, -b), yb2 = f2(yb, yb);
 #pragma unroll
-  for (int j = 0; j < 8; ++j) w[j >> 2] |= f32x2_to_e2m1x2(q[2 * j], q[2 * j + 1]) << (8 * (j & 3));
-  return make_uint2(w[0], w[1]);
+    for (int j = 0; j < 16; j += 2) div_rn_pair(x[j], x[j + 1], nb, yb2, q[j], q[j + 1]);
+  } else {                                      // operands near the FP32 range limits
+#pragma unroll
+    for (int j = 0; j < 16; ++j) q[j] = __fdiv_rn(x[j], b);
+  }
 }
 
 // Eight packed nibbles (element i in nibble i) -> eight bytes, nibble i in
@@ -109,7 +120,7 @@ __device__ __forceinline__ Dest dest_of(const WriteArgs& a, int64_t t, int h, bo
 
 // Thread (token pair p, head h, 16-element block b; K|V = blockIdx.y).
 template <int D, int FMT>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 4)
 write_kernel(const WriteArgs a) {
   grid_dep_launch();   // a following decode launch may be scheduled early
   constexpr int NB = D / 16;                      // threads per row
@@ -157,13 +168,7 @@ write_kernel(const WriteArgs a) {
       word[k] = make_uint2(0u, 0u);
       if (S[k] != 0u && dr.x != 0.f) {
         float q[16];
-        if (div_rn_in_range(dr.y, amax)) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) q[j] = div_rn_inrange(x[j], dr.x, dr.y);
-        } else {                                // operands near the FP32 range limits
-#pragma unroll
-          for (int j = 0; j < 16; ++j) q[j] = __fdiv_rn(x[j], dr.x);
-        }
+        div16(x, dr.x, dr.y, amax, q);
         word[k] = e2m1x16(q);
       }
     }
@@ -219,13 +224,7 @@ write_kernel(const WriteArgs a) {
 #pragma unroll
       for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(x[j]));
       float q[16];
-      if (div_rn_in_range(rs, amax)) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) q[j] = div_rn_inrange(x[j], s, rs);
-      } else {                                  // operands near the FP32 range limits
-#pragma unroll
-        for (int j = 0; j < 16; ++j) q[j] = __fdiv_rn(x[j], s);
-      }
+      div16(x, s, rs, amax, q);
       uint32_t w[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i)
@@ -250,13 +249,7 @@ write_kernel(const WriteArgs a) {
       if (s != 0.f) {
         const float rs = __frcp_rn(s);
         float q[16];
-        if (div_rn_in_range(rs, amax)) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) q[j] = div_rn_inrange(x[j], s, rs);
-        } else {                                // operands near the FP32 range limits
-#pragma unroll
-          for (int j = 0; j < 16; ++j) q[j] = __fdiv_rn(x[j], s);
-        }
+        div16(x, s, rs, amax, q);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           int c = __float2int_rn(q[j]);
