@@ -676,8 +676,10 @@ def time_extend(device, w, ws, tpeak, reps=5):
     i64 = lambda x: torch.tensor(x, dtype=torch.int64, device=device)
     pl, cp, cl, cc = i32([Lp]), i64([0, Lp]), i32([C]), i64([0, C])
 
+    ws_ext = K.alloc_extend_workspace(1, C, Hq, D, device=device)
+
     def run():
-        K.kv4_extend_attention(q, ck, cv, wk, wv, s8, pl, cp, cl, cc, C, w.sm_scale(), out)
+        K.kv4_extend_attention(q, ck, cv, wk, wv, s8, pl, cp, cl, cc, C, w.sm_scale(), out, workspace=ws_ext)
 
     for _ in range(3):
         run()

@@ -67,8 +67,9 @@ def _load(build_if_missing=False):
                                        i32, vp]),
         "kv4_dequant_prefix": (i32, [P, vp, vp, i32, vp, vp, i32, i32, vp, vp, vp, vp]),
         "kv4_calibrate_global_scale": (i32, [vp, vp, i64, i32, i32, vp, vp]),
+        "kv4_extend_workspace_bytes": (i64, [i32, i32, i32, i32]),
         "kv4_extend_attention": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
-                                       i32, i32, f32, vp, i32, vp]),
+                                       i32, i32, f32, vp, i64, vp, i32, vp]),
         "kv4_decode_attention_static_ws": (i32, [vp, P, vp, vp, i32, vp, i32, i32, f32, i32, vp,
                                                  i32, vp]),
         "kv4_k8v4_write": (i32, [vp, vp, vp, i64, P, vp, vp]),
@@ -209,17 +210,28 @@ def kv4_dequant_prefix(pool, layer_global_scale, block_table, prefix_lens, cu_pr
     _check(st, "kv4_dequant_prefix")
 
 
+def kv4_extend_workspace_bytes(batch, max_chunk_len, num_q_heads, head_dim):
+    return _load().kv4_extend_workspace_bytes(batch, max_chunk_len, num_q_heads, head_dim)
+
+
+def alloc_extend_workspace(batch, max_chunk_len, num_q_heads, head_dim, device="cuda"):
+    n = kv4_extend_workspace_bytes(batch, max_chunk_len, num_q_heads, head_dim)
+    return None if n == 0 else torch.empty(n, dtype=torch.uint8, device=device)
+
+
 def kv4_extend_attention(q, chunk_k, chunk_v, prefix_k, prefix_v, fp8_scale, prefix_lens,
                          cu_prefix, chunk_lens, cu_chunk, max_chunk_len, sm_scale, out,
-                         stream=None):
+                         workspace=None, stream=None):
     """Extend attention of the chunk's queries q (bf16 [sum C, Hq, D]) over
     the FP8 prefix workspace plus the FP8 chunk K/V; out is bf16 or float32
-    [sum C, Hq, D]."""
+    [sum C, Hq, D].  ``workspace`` (alloc_extend_workspace) lets the last
+    partial wave of work be split over the SMs."""
     Hq, D = q.shape[1], q.shape[2]
     st = _load().kv4_extend_attention(
         _ptr(q), _ptr(chunk_k), _ptr(chunk_v), _ptr(prefix_k), _ptr(prefix_v), _ptr(fp8_scale),
         _ptr(prefix_lens), _ptr(cu_prefix), _ptr(chunk_lens), _ptr(cu_chunk),
         chunk_lens.shape[0], int(max_chunk_len), Hq, chunk_k.shape[1], D, float(sm_scale),
+        _ptr(workspace), workspace.numel() if workspace is not None else 0,
         _ptr(out), 1 if out.dtype == torch.float32 else 0, _stream(stream))
     _check(st, "kv4_extend_attention")
 

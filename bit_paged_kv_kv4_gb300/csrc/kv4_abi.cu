@@ -535,13 +535,25 @@ kv4_status kv4_dequant_prefix(const kv4_pool* pool, const float* layer_global_sc
   return e == cudaSuccess ? KV4_OK : cuda_fail(e, "kv4_dequant_prefix launch");
 }
 
+int64_t kv4_extend_workspace_bytes(int32_t batch, int32_t max_chunk_len, int32_t num_q_heads,
+                                   int32_t head_dim) {
+  if (batch <= 0 || max_chunk_len <= 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
+  const int64_t items = static_cast<int64_t>(batch) * ((static_cast<int64_t>(max_chunk_len) + 127) / 128) * num_q_heads;
+  if (items >= (int64_t{1} << 31)) return 0;
+  int split = 0, ways = 1;
+  kv4::extend_split(static_cast<int>(items), sm_count(), split, ways);
+  const int64_t pieces = static_cast<int64_t>(split) * ways;
+  return align256(pieces * 128 * head_dim * 4) + pieces * 128 * 8;
+}
+
 kv4_status kv4_extend_attention(const void* q, const void* chunk_k, const void* chunk_v,
                                 const void* prefix_k, const void* prefix_v,
                                 const float* fp8_scale, const int32_t* prefix_lens,
                                 const int64_t* cu_prefix, const int32_t* chunk_lens,
                                 const int64_t* cu_chunk, int32_t batch, int32_t max_chunk_len,
                                 int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                                float sm_scale, void* out, int32_t out_is_fp32, void* stream) {
+                                float sm_scale, void* workspace, int64_t workspace_bytes, void* out,
+                                int32_t out_is_fp32, void* stream) {
   kv4::NvtxRange nvtx_range("kv4_extend_attention");
   g_msg.clear();
   if (batch < 0 || max_chunk_len < 0) return fail(KV4_EINVAL, "batch and max_chunk_len must be >= 0");
@@ -554,6 +566,8 @@ kv4_status kv4_extend_attention(const void* q, const void* chunk_k, const void* 
   if ((static_cast<int64_t>(max_chunk_len) + 127) / 128 > 65535)
     return fail(KV4_EINVAL, "max_chunk_len exceeds the launch grid");
   if (batch == 0 || max_chunk_len == 0) return KV4_OK;
+  const int64_t items = static_cast<int64_t>(batch) * ((static_cast<int64_t>(max_chunk_len) + 127) / 128) * num_q_heads;
+  if (items >= (int64_t{1} << 31)) return fail(KV4_EINVAL, "too many (request, query tile, head) items");
   if (q == nullptr || chunk_k == nullptr || chunk_v == nullptr || prefix_k == nullptr ||
       prefix_v == nullptr || fp8_scale == nullptr || prefix_lens == nullptr ||
       cu_prefix == nullptr || chunk_lens == nullptr || cu_chunk == nullptr || out == nullptr)
@@ -583,6 +597,22 @@ kv4_status kv4_extend_attention(const void* q, const void* chunk_k, const void* 
   a.sm_scale = sm_scale;
   a.out = out;
   a.out_f32 = out_is_fp32 ? 1 : 0;
+  a.qtiles = (max_chunk_len + 127) / 128;
+  a.items = static_cast<int>(items);
+  a.split = 0;
+  a.ways = 1;
+  if (workspace != nullptr) {
+    // the remainder of the last wave split into key-range pieces
+    const int64_t need = kv4_extend_workspace_bytes(batch, max_chunk_len, num_q_heads, head_dim);
+    if (workspace_bytes < need)
+      return fail(KV4_EINVAL, "workspace of %lld bytes is smaller than the %lld needed",
+                  static_cast<long long>(workspace_bytes), static_cast<long long>(need));
+    if (!aligned(workspace, 256)) return fail(KV4_EINVAL, "workspace must be 256-byte aligned");
+    kv4::extend_split(a.items, sm_count(), a.split, a.ways);
+    const int64_t pieces = static_cast<int64_t>(a.split) * a.ways;
+    a.part_o = static_cast<float*>(workspace);
+    a.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align256(pieces * 128 * head_dim * 4));
+  }
   a.err = error_word();
   if (a.err == nullptr) return fail(KV4_ECUDA, "no CUDA device / error word unavailable");
   cudaError_t e = kv4::launch_extend(a, static_cast<cudaStream_t>(stream));

@@ -197,9 +197,18 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const ExtendArgs a)
   __shared__ volatile int conv_tile;                 // tiles the converters have stored
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.x, qt = blockIdx.y, b = blockIdx.z;
+  // this CTA's item (request b, query tile qt, head h) and key-range piece
+  int item = blockIdx.x, piece = -1;                  // piece -1: the whole key range
+  const int whole = a.items - a.split;
+  if (item >= whole) {
+    piece = (item - whole) % a.ways;
+    item = whole + (item - whole) / a.ways;
+  }
+  const int h = item % a.Hq;
+  const int qt = a.qtiles - 1 - (item / a.Hq) % a.qtiles;   // later query tiles (more keys) first
+  const int b = item / (a.Hq * a.qtiles);
   const int C = a.chunk_lens[b], Lp = a.prefix_lens[b];
-  if (qt == 0 && h == 0 && tid == 0 && (C < 0 || Lp < 0 || C > a.max_chunk_len))
+  if (qt == 0 && h == 0 && piece <= 0 && tid == 0 && (C < 0 || Lp < 0 || C > a.max_chunk_len))
     set_error(a.err, KV4_EBOUNDS);
   if (Lp < 0 || qt * kQT >= C) return;               // uniform over the CTA
   if (static_cast<int64_t>(Lp) + C >= (int64_t{1} << 31)) {
@@ -209,7 +218,22 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const ExtendArgs a)
   const int64_t c0 = a.cu_chunk[b], p0 = a.cu_prefix[b];
   const int rows = min(kQT, C - qt * kQT);
   const int kend = Lp + qt * kQT + rows;             // keys [0, kend) are visible to some row
-  const int nT = (kend + kKT - 1) / kKT;
+  // Key tiles [jt0, jt0 + nT): all of them, or piece p of the full-prefix
+  // tiles (every row sees all of those), the last piece taking the rest, so
+  // no row's first tile in its piece is fully masked.
+  int jt0 = 0, nT = (kend + kKT - 1) / kKT;
+  if (piece >= 0) {
+    const int np = Lp / kKT;
+    const int j1 = (piece == a.ways - 1) ? nT : (piece + 1) * np / a.ways;
+    jt0 = piece * np / a.ways;
+    nT = j1 - jt0;
+  }
+  const int64_t pslot = static_cast<int64_t>(item - whole) * a.ways + piece;   // partial slot
+  if (nT == 0) {
+    // an empty piece: an empty state for the merge
+    if (tid < kQT) reinterpret_cast<float2*>(a.part_ml)[pslot * kQT + tid] = make_float2(-INFINITY, 0.f);
+    return;
+  }
   const int hk = h / a.G;
 
   uint8_t* sm = align1024(ext_raw);
@@ -310,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const ExtendArgs a)
     if (lane == 0) {
       const int64_t rs = static_cast<int64_t>(a.Hkv) * D;
       auto prefetch = [&](int j) {
-        const int k0 = j * kKT, k1 = min(k0 + kKT, kend);
+        const int k0 = (jt0 + j) * kKT, k1 = min(k0 + kKT, kend);
         const int e = min(k1, Lp), s0 = max(k0, Lp);
         if (k0 < e) {
           prefetch_l2(a.pk + (p0 + k0) * rs, static_cast<uint32_t>((e - k0) * rs));
@@ -348,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const ExtendArgs a)
 #pragma unroll
       for (int m = 0; m < NI; ++m) {
         const int it = m * kConv + t, r = it / U16, u = it % U16;
-        const int key = j * kKT + r;
+        const int key = (jt0 + j) * kKT + r;
         w[m] = make_uint4(0u, 0u, 0u, 0u);
         if (key < Lp) w[m] = __ldg(reinterpret_cast<const uint4*>(pre + key * rs) + u);
         else if (key < kend) w[m] = __ldg(reinterpret_cast<const uint4*>(chk + (key - Lp) * rs) + u);
@@ -463,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const ExtendArgs a)
         tmem_ld16(tS + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&sr[c * 16]));
       tmem_wait_ld();
       float s[kKT];
-      const int kb = j * kKT;
+      const int kb = (jt0 + j) * kKT;
 #pragma unroll
       for (int c = 0; c < kKT; ++c) s[c] = __uint_as_float(sr[c]);
       if (kb + kKT - 1 > lim) {
@@ -534,10 +558,27 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const ExtendArgs a)
     } else {
       tc_fence_after();
       const bool valid = r < rows;
+      if (piece >= 0) {
+        // a piece: its unnormalised O and (base, row sum) for the merge
+        if (valid) reinterpret_cast<float2*>(a.part_ml)[pslot * kQT + r] = make_float2(m_use, l);
+        float* po = a.part_o + (pslot * kQT + r) * static_cast<int64_t>(D);
+#pragma unroll 1
+        for (int c = 0; c < D / 16; ++c) {
+          uint32_t o[16];
+          tmem_ld16(tO + lane_base + c * 16, o);
+          tmem_wait_ld();
+          if (!valid) continue;
+          float4* dst = reinterpret_cast<float4*>(po + c * 16);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
+                                 __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
+        }
+      }
       const float inv = sv / l;
       const int64_t orow = ((c0 + qt * kQT + r) * a.Hq + h) * static_cast<int64_t>(D);
 #pragma unroll 1
-      for (int c = 0; c < D / 16; ++c) {
+      for (int c = 0; c < D / 16 && piece < 0; ++c) {
         uint32_t o[16];
         tmem_ld16(tO + lane_base + c * 16, o);
         tmem_wait_ld();
@@ -573,6 +614,60 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(const ExtendArgs a)
                  :: "r"(tmem), "r"(Gm::TM_COLS) : "memory");
 }
 
+// Merge of the pieces of the split items: one warp per query row, the
+// pieces' states in piece order (deterministic), O = sum_p 2^(m_p - M) O_p,
+// l = sum_p 2^(m_p - M) l_p, out = O * s_V / l.
+template <int D>
+__global__ void __launch_bounds__(256) extend_merge_kernel(const ExtendArgs a) {
+  const int k = blockIdx.x;
+  const int item = a.items - a.split + k;
+  const int h = item % a.Hq;
+  const int qt = a.qtiles - 1 - (item / a.Hq) % a.qtiles;
+  const int b = item / (a.Hq * a.qtiles);
+  const int C = a.chunk_lens[b], Lp = a.prefix_lens[b];
+  const int r = blockIdx.y * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (Lp < 0 || C < 0 || qt * kQT + r >= C || static_cast<int64_t>(Lp) + C >= (int64_t{1} << 31)) return;
+  const float2* ml = reinterpret_cast<const float2*>(a.part_ml);
+  float M = -INFINITY;
+  for (int p = 0; p < a.ways; ++p) M = fmaxf(M, ml[(static_cast<int64_t>(k) * a.ways + p) * kQT + r].x);
+  float l = 0.f;
+  constexpr int NC = D / 128 > 0 ? D / 128 : 1;      // float4 columns per lane
+  float4 acc[NC];
+#pragma unroll
+  for (int c = 0; c < NC; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int p = 0; p < a.ways; ++p) {
+    const int64_t slot = static_cast<int64_t>(k) * a.ways + p;
+    const float2 st = ml[slot * kQT + r];
+    if (st.x == -INFINITY) continue;                 // an empty piece
+    const float w = fast_exp2(st.x - M);
+    l += w * st.y;
+    const float4* po = reinterpret_cast<const float4*>(a.part_o + (slot * kQT + r) * D);
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      const int col = lane + 32 * c;
+      if (col < D / 4) {
+        const float4 v = __ldg(po + col);
+        acc[c].x += w * v.x; acc[c].y += w * v.y; acc[c].z += w * v.z; acc[c].w += w * v.w;
+      }
+    }
+  }
+  const float inv = __ldg(a.fp8_scale + 1) / l;
+  const int64_t orow = ((a.cu_chunk[b] + qt * kQT + r) * a.Hq + h) * static_cast<int64_t>(D);
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    const int col = lane + 32 * c;
+    if (col >= D / 4) continue;
+    const float4 v = make_float4(acc[c].x * inv, acc[c].y * inv, acc[c].z * inv, acc[c].w * inv);
+    if (a.out_f32) {
+      reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow)[col] = v;
+    } else {
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+      reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + orow)[col] =
+          make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+    }
+  }
+}
+
 template <int D>
 cudaError_t launch_d(const ExtendArgs& a, cudaStream_t st) {
   using Gm = ExtGeo<D>;
@@ -586,12 +681,32 @@ cudaError_t launch_d(const ExtendArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  const dim3 grid(a.Hq, (a.max_chunk_len + kQT - 1) / kQT, a.B);
-  extend_kernel<D><<<grid, kThreads, Gm::SMEM, st>>>(a);
+  // one CTA per work-list entry: whole items, then the pieces of the split ones
+  const int64_t ctas = static_cast<int64_t>(a.items - a.split) + static_cast<int64_t>(a.split) * a.ways;
+  extend_kernel<D><<<static_cast<unsigned>(ctas), kThreads, Gm::SMEM, st>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || a.split == 0) return e;
+  extend_merge_kernel<D><<<dim3(a.split, kQT / 8), 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 
 }  // namespace
+
+void extend_split(int items, int sms, int& split, int& ways) {
+  // one CTA per SM (the kernel's shared memory): the items fill
+  // floor(items / sms) waves and the remainder X a partial one; cutting the
+  // remainder's key ranges into floor(sms / X) pieces spreads it over the SMs
+  constexpr int kMaxWays = 16;
+  split = 0;
+  ways = 1;
+  if (items <= 0 || sms <= 0) return;
+  const int x = items >= sms ? items % sms : items;
+  if (x == 0) return;
+  const int w = sms / x < kMaxWays ? sms / x : kMaxWays;
+  if (w < 2) return;
+  split = x;
+  ways = w;
+}
 
 cudaError_t launch_extend(const ExtendArgs& a, cudaStream_t st) {
   switch (a.D) {

@@ -126,8 +126,19 @@ struct ExtendArgs {
   void* out;                    // [sum C][Hq][D] bf16 or f32
   int out_f32;
   int* err;
+  // Work list: items (request, 128-row query tile, query head), longest
+  // first; the last `split` items are cut into `ways` key ranges whose
+  // partial states go to part_o / part_ml and are merged by a second kernel.
+  int qtiles;                   // query tiles per request: ceil(max_chunk_len / 128)
+  int items;                    // B * qtiles * Hq
+  int split, ways;
+  float* part_o;                // [split * ways][128][D] unnormalised O
+  float* part_ml;               // [split * ways][128][2] (base m in log2 units, l)
 };
 cudaError_t launch_extend(const ExtendArgs& a, cudaStream_t st);
+// Split of the extend work list for `sms` SMs: the remainder items of the
+// last partial wave are cut into ways pieces so they fill one wave.
+void extend_split(int items, int sms, int& split, int& ways);
 
 struct K8V4WriteArgs {
   const __nv_bfloat16* k;       // [T][Hkv][D]

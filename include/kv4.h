@@ -244,17 +244,28 @@ kv4_status kv4_dequant_prefix(const kv4_pool* pool,
  *                larger device values leave rows uncomputed and are flagged
  *                (KV4_EBOUNDS in the error word).
  *   sm_scale     > 0.   out  device [sum C][Hq][D], bf16 or FP32.
+ *   workspace    NULL, or device scratch (256-byte aligned) of at least
+ *                kv4_extend_workspace_bytes(B, max_chunk_len, Hq, D) bytes:
+ *                the work is one CTA per (request, 128-row query tile,
+ *                query head), one CTA per SM; with a workspace the items
+ *                past the last full wave have their key ranges cut into
+ *                pieces that fill one wave, and a second kernel merges the
+ *                pieces' softmax states in a fixed order.  The result is the
+ *                same function either way (up to FP32 summation order).
  * All device buffers 16-byte aligned (the int64 arrays 8-byte); Hq a
  * multiple of Hkv; head_dim 64, 128 or 256.  Asynchronous on `stream`;
  * allocates nothing.
  */
+int64_t kv4_extend_workspace_bytes(int32_t batch, int32_t max_chunk_len, int32_t num_q_heads,
+                                   int32_t head_dim);
 kv4_status kv4_extend_attention(const void* q, const void* chunk_k, const void* chunk_v,
                                 const void* prefix_k, const void* prefix_v,
                                 const float* fp8_scale, const int32_t* prefix_lens,
                                 const int64_t* cu_prefix, const int32_t* chunk_lens,
                                 const int64_t* cu_chunk, int32_t batch, int32_t max_chunk_len,
                                 int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                                float sm_scale, void* out, int32_t out_is_fp32, void* stream);
+                                float sm_scale, void* workspace, int64_t workspace_bytes, void* out,
+                                int32_t out_is_fp32, void* stream);
 
 /*
  * kv4_calibrate_global_scale -- the NVFP4 global scales of one layer from its

@@ -134,7 +134,8 @@ def test_extend_validation_without_gpu(lib):
         a.update(kw)
         return lib.kv4_extend_attention(a["q"], a["ck"], a["cv"], a["pk"], a["pv"], a["s"], a["pl"],
                                         a["cp"], a["cl"], a["cc"], a["B"], a["mc"], a["Hq"], a["Hkv"],
-                                        a["D"], a["sm"], a["out"], a["f32"], None)
+                                        a["D"], a["sm"], a.get("ws"), a.get("wsb", 0), a["out"], a["f32"],
+                                        None)
     assert ext(Hq=25) == 1                      # heads not a multiple of kv heads
     assert ext(D=96) == 2                       # head_dim not built
     assert ext(sm=0.0) == 1 and ext(sm=float("nan")) == 1
@@ -186,3 +187,22 @@ def test_every_declared_function_has_a_binding_signature():
     src = inspect.getsource(K._load)
     for name in declared_functions():
         assert f'"{name}"' in src, name
+
+
+def test_extend_workspace_sizing_and_checks(lib):
+    """The extend workspace holds one partial state (128 rows of D floats and
+    two floats) per piece of the split items: at most one piece per SM, and
+    nothing when the items fill whole waves."""
+    sms = 152   # no device here: the library assumes 152 SMs
+    n = lib.kv4_extend_workspace_bytes(1, 8192, 24, 256)      # 1536 items = 10 x 152 + 16
+    pieces = 16 * (152 // 16)
+    assert n == (pieces * 128 * 256 * 4 + 255) // 256 * 256 + pieces * 128 * 8
+    assert lib.kv4_extend_workspace_bytes(1, 128 * 152, 1, 64) == 0     # whole waves: no split
+    assert lib.kv4_extend_workspace_bytes(1, 128, 100, 64) == 0         # 100 items: 152 // 100 < 2
+    assert lib.kv4_extend_workspace_bytes(1, 128, 24, 256) > 0          # 24 items in 6 pieces each
+    assert lib.kv4_extend_workspace_bytes(0, 128, 24, 256) == 0
+    assert n <= sms * 128 * (256 * 4 + 8) + 256
+    fake = ctypes.c_void_p(1 << 20)
+    st = lib.kv4_extend_attention(fake, fake, fake, fake, fake, fake, fake, fake, fake, fake, 1, 8192, 24,
+                                  4, 256, 0.0625, fake, n - 1, fake, 0, None)
+    assert st == 1                               # workspace too small

@@ -38,12 +38,15 @@ def make(lp, lc, Hq, Hkv, D, seed=0, outliers=4, oscale=10.0, device="cuda"):
                 sm=np.float32(1.0 / np.sqrt(D)))
 
 
-def run(x, out_dtype=torch.float32, max_chunk_len=None):
+def run(x, out_dtype=torch.float32, max_chunk_len=None, split=True):
+    """With split, a workspace lets the items past the last full wave of CTAs
+    be cut into key-range pieces merged by the second kernel."""
     TC = max(int(sum(x["lc"])), 1)
     out = torch.zeros((TC, x["Hq"], x["D"]), dtype=out_dtype, device="cuda")
     mc = max(x["lc"]) if max_chunk_len is None else max_chunk_len
+    ws = K.alloc_extend_workspace(len(x["lc"]), mc, x["Hq"], x["D"]) if split else None
     K.kv4_extend_attention(x["q"], x["ck"], x["cv"], x["pk"], x["pv"], x["s"], x["pl"], x["cp"],
-                           x["cl"], x["cc"], mc, x["sm"], out)
+                           x["cl"], x["cc"], mc, x["sm"], out, workspace=ws)
     torch.cuda.synchronize()
     return out
 
@@ -70,9 +73,10 @@ def check(got, want, x, what):
     (128, 4, 4, [100, 0], [257, 3]),
     (256, 24, 4, [300, 0, 1000], [200, 129, 64]),
 ])
-def test_ragged_batch_matches_oracle(D, Hq, Hkv, lp, lc):
+@pytest.mark.parametrize("split", [False, True])
+def test_ragged_batch_matches_oracle(D, Hq, Hkv, lp, lc, split):
     x = make(lp, lc, Hq, Hkv, D, seed=D)
-    got = run(x).cpu().numpy()
+    got = run(x, split=split).cpu().numpy()
     assert K.kv4_device_error() == 0
     want = oracle(x)
     TC = int(sum(lc))
@@ -91,6 +95,24 @@ def test_bf16_output_and_determinism():
     assert np.all(np.abs(got - f) <= ulp)
     want = oracle(x)
     check(f, want, x, "fp32 beside bf16")
+
+
+@pytest.mark.parametrize("lp", [[0, 1000], [100, 70], [3000, 5]])
+def test_split_pieces_match_oracle_and_whole(lp):
+    # few items (B 2 x 3 query tiles x 4 heads = 24 < the SM count), so every
+    # item is cut into key-range pieces: prefixes shorter than the pieces
+    # (empty pieces), none, and long; rows past a chunk's end; both outputs
+    x = make(lp, [257, 190], 4, 2, 128, seed=21)
+    assert K.kv4_extend_workspace_bytes(2, 257, 4, 128) > 0
+    got = run(x).cpu().numpy()
+    assert K.kv4_device_error() == 0
+    whole = run(x, split=False).cpu().numpy()
+    want = oracle(x)
+    TC = 257 + 190
+    check(got[:TC], want[:TC], x, "pieces")
+    assert np.abs(got[:TC] - whole[:TC]).max() <= 1e-5 * max(1.0, np.abs(whole).max())
+    b = run(x, torch.bfloat16).float().cpu().numpy()
+    assert np.all(np.abs(b[:TC] - got[:TC]) <= np.maximum(np.abs(got[:TC]), 1e-30) * 2.0 ** -8)
 
 
 def test_large_prefix_many_tiles_and_rescales():
