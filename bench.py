@@ -490,24 +490,29 @@ def kv4_arm(args):
     achieved = dec_bytes / dec_avg / 1e9
 
     # ---- end to end through the public API, host buffers ----------------
-    h_q = torch.empty_like(s.q, device="cpu").pin_memory()
-    h_q.copy_(s.q.cpu())
-    h_k = s.k_new.cpu().pin_memory()
-    h_v = s.v_new.cpu().pin_memory()
-    h_slot = s.slot_new.cpu().pin_memory()
-    h_lens = s.d_lens.cpu().pin_memory()
+    # The step's inputs (q, the new K/V, their slots, the lengths) sit in one
+    # pinned host staging buffer and go over in one copy per step into one
+    # device buffer, of which the library's arguments are views (each part
+    # 256-byte aligned).
+    parts = [s.q, s.k_new, s.v_new, s.slot_new, s.d_lens]
+    offs, at = [], 0
+    for t in parts:
+        offs.append(at)
+        at += (t.numel() * t.element_size() + 255) // 256 * 256
+    h_in = torch.empty(at, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(at, dtype=torch.uint8, device=device)
+    views = []
+    for t, o in zip(parts, offs):
+        n = t.numel() * t.element_size()
+        h_in[o:o + n].copy_(t.contiguous().view(torch.uint8).reshape(-1).cpu())
+        views.append(d_in[o:o + n].view(t.dtype).view(t.shape))
+    d_q, d_k, d_v, d_slot, d_lens = views
     h_out = torch.empty((B, Hq, D), dtype=torch.float32).pin_memory()
-    d_q, d_k, d_v = torch.empty_like(s.q), torch.empty_like(s.k_new), torch.empty_like(s.v_new)
-    d_slot, d_lens = torch.empty_like(s.slot_new), torch.empty_like(s.d_lens)
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_slot, h_lens))
+    h2d = h_in.numel()                       # the staging buffer, alignment padding included
     d2h = h_out.numel() * h_out.element_size()
 
     def e2e_step():
-        d_q.copy_(h_q, non_blocking=True)
-        d_k.copy_(h_k, non_blocking=True)
-        d_v.copy_(h_v, non_blocking=True)
-        d_slot.copy_(h_slot, non_blocking=True)
-        d_lens.copy_(h_lens, non_blocking=True)
+        d_in.copy_(h_in, non_blocking=True)
         K.kv4_write(d_k, d_v, d_slot, s.pool, s.g)
         K.kv4_decode_attention(d_q, s.pool, s.g, s.d_table, d_lens, s.sm, s.out,
                                num_splits=s.splits, workspace=s.ws)

@@ -137,3 +137,48 @@ def test_write_fp8_input_bit_exact(fmt, D):
     diff = np.nonzero(got != ref)[0]
     assert diff.size == 0, f"{diff.size} bytes differ, first at {diff[:8]}"
     assert_guard_intact(pool.guard, "pool")
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "int4"])
+@pytest.mark.parametrize("D", [64, 256])
+def test_write_pair_rows_every_slot_pattern(fmt, D):
+    """A thread writes tokens 2p and 2p+1 of the call; NVFP4 V stores both
+    halves of a pair row with plain stores only when they land in one, and
+    otherwise sets each token's nibbles atomically, keeping its partner's.
+    One call mixes: an aligned run (plain stores), a run starting at an odd
+    offset, pair rows whose halves come from non-adjacent tokens, a reversed
+    pair, a skipped token beside a written partner, and an odd token count
+    (the last token alone) -- over a pool of random bytes, whose untouched
+    nibbles and rows must survive."""
+    P, H = 16, 2
+    slots = np.array([32, 33, 34, 35, 36, 37,      # aligned: pair rows 16..18
+                      5, 6, 7, 8,                  # odd start: halves of rows 2..4
+                      10, 13, 11, 12,              # rows 5 and 6 from non-adjacent tokens
+                      21, 20,                      # reversed pair
+                      44, -1,                      # a written even half, a skipped partner
+                      50, 51, 52], np.int64)       # odd count: 52 is alone
+    T = slots.size
+    rng = np.random.default_rng(D)
+    x = (rng.standard_normal((2, T, H, D)) * np.exp(rng.uniform(-3, 3, (2, T, H, 1)))).astype(np.float32)
+    x[:, :, :, 5] *= 9.0
+    k, v = f32_to_bf16_bits(x[0]), f32_to_bf16_bits(x[1])
+    g = np.array([np.abs(x[0]).max() / 2688.0, np.abs(x[1]).max() / 2688.0], np.float32)
+    pages = 4
+    spec = OP.PoolSpec(fmt, pages, P, H, D)
+    fill = rng.integers(0, 256, spec.pool_bytes, dtype=np.uint8)
+    if fmt == "int4":
+        # keep the untouched scale words finite
+        for page in range(pages):
+            for h in range(H):
+                off = int(spec.chunk_offset(page, h)) + spec.region("ks")
+                fill[off:off + 2 * P * 4] = np.full(2 * P, 0.5, np.float32).view(np.uint8)
+    ref = OP.write(fill.copy(), spec, k, v, slots, g)
+    pool = guarded_pool(fmt, pages, P, H, D)
+    pool.buffer.copy_(torch.from_numpy(fill))
+    K.kv4_write(dev_bf16(k), dev_bf16(v), torch.from_numpy(slots).cuda(), pool, torch.from_numpy(g).cuda())
+    torch.cuda.synchronize()
+    assert K.kv4_device_error() == 0
+    assert_guard_intact(pool.guard, "pool")
+    got = pool.buffer.cpu().numpy()
+    diff = np.nonzero(got != ref)[0]
+    assert diff.size == 0, f"{fmt} D{D}: {diff.size} bytes differ, first at {diff[:8]}"
