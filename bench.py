@@ -101,19 +101,34 @@ def decode_source_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload):
-    """ncu DRAM bytes per decode launch recorded in profiles/, if it was taken
-    on the current decode source; else None."""
+def recorded_ncu(workload):
+    """The ncu capture of one decode launch recorded in profiles/ (DRAM bytes,
+    duration under ncu), if it was taken on the current decode source; else
+    None."""
     p = os.path.join(ROOT, "profiles", "decode_traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
         e = d.get(workload)
         if e and e.get("source_hash") == decode_source_hash():
-            return float(e["dram_bytes_per_launch"])
+            return e
     except Exception:
         pass
     return None
+
+
+def recorded_traffic(workload):
+    """ncu DRAM bytes per decode launch (read + write), or None."""
+    e = recorded_ncu(workload)
+    return float(e["dram_bytes_per_launch"]) if e else None
+
+
+def recorded_ncu_gbs(workload):
+    """ncu DRAM bytes / ncu kernel duration of the recorded launch, GB/s."""
+    e = recorded_ncu(workload)
+    if not e or not e.get("gpu_time_duration_ns_under_ncu"):
+        return None
+    return float(e["dram_bytes_per_launch"]) / float(e["gpu_time_duration_ns_under_ncu"])
 
 
 class ClockSampler:
@@ -545,6 +560,7 @@ def kv4_arm(args):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": recorded_traffic(w.name),
+                     "ncu_dram_gbs": recorded_ncu_gbs(w.name),
                      "kernel": "decode4_kernel<256, NVFP4> + combine_kernel (kv4_decode_attention)",
                      "peak_source": f"{peak_src} hbm_gbs", "decode_us": dec_avg * 1e6,
                      "decode_timing": f"mean of {args.steps} back-to-back decode calls between two CUDA "
@@ -571,6 +587,7 @@ def kv4_arm(args):
             med = statistics.median(ts)
             extra[name] = {"decode_us": med * 1e6, "gbs": bx / med / 1e9, "frac": bx / med / 1e9 / peak,
                            "num_splits": sx.splits, "kv_bytes": bx, "traffic": recorded_traffic(name),
+                           "ncu_dram_gbs": recorded_ncu_gbs(name),
                            "tokens_per_s_16_layers": wx.batch / (16 * med)}
             if name == "fp8_32k":
                 # the comparison the pages draw: same shapes and lengths as the
@@ -591,6 +608,7 @@ def kv4_arm(args):
         # the k8v4 variant on the headline shapes: FP8 keys, 4-bit values, rotated
         extra["k8v4_32k"] = time_k8v4(device, W.ALL["nvfp4_32k"], peak)
         extra["k8v4_32k"]["traffic"] = recorded_traffic("k8v4_32k")
+        extra["k8v4_32k"]["ncu_dram_gbs"] = recorded_ncu_gbs("k8v4_32k")
         torch.cuda.empty_cache()
         line["workloads"] = extra
 
