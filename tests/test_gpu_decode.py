@@ -77,14 +77,23 @@ def test_deterministic_and_split_consistent():
     assert np.abs(a - d).max() < 1e-4
 
 
-def test_large_magnitudes_and_constant_keys():
-    # |q| far beyond f16 range is pre-scaled; constant keys give the mean of V
-    c = Case("nvfp4", 1, 4, 128, [200], 32, seed=7, kv_scale=300.0)
+def test_large_query_prescaled():
+    # |q| far beyond the f16 range is pre-scaled by a power of two in the
+    # kernel; unit-scale K/V, so the gate applies as it stands
+    c = Case("nvfp4", 1, 4, 128, [200], 32, seed=7)
     from workloads import f32_to_bf16_bits, bf16_bits_to_f32
     c.q = f32_to_bf16_bits(bf16_bits_to_f32(c.q) * np.float32(1e5))
     c.sm = np.float32(1e-9)
     want = c.oracle_out()
-    check_close(run(c, 2).cpu().numpy(), want, atol=2e-3 * 300, what="large |q|")
+    check_close(run(c, 2).cpu().numpy(), want, what="large |q|")
+
+
+def test_large_kv_magnitudes():
+    # K and V 300 times larger (global scales follow); the output inherits
+    # V's scale, so the gate applies to out / 300 (the unit-scale output)
+    c = Case("nvfp4", 1, 4, 128, [200], 32, seed=7, kv_scale=300.0)
+    want = c.oracle_out()
+    check_close(run(c, 2).cpu().numpy() / 300.0, want / 300.0, what="K, V x300")
 
 
 def test_bad_block_table_entry_is_flagged_not_faulted():
