@@ -340,6 +340,7 @@ static kv4_status write_common(const void* k, const void* v, const float* in_sca
   a.D = pool->head_dim;
   a.fmt = fmt;
   a.gscale = layer_global_scale;
+  a.sms = sm_count();
   a.err = error_word();
   if (a.err == nullptr) return fail(KV4_ECUDA, "no CUDA device / error word unavailable");
   cudaError_t e = kv4::launch_write(a, static_cast<cudaStream_t>(stream));

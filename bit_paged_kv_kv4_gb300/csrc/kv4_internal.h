@@ -75,6 +75,8 @@ struct WriteArgs {
   const uint8_t* k8;            // FP8-input write: E4M3 [T][Hkv][D] (else null)
   const uint8_t* v8;
   const float* in_scale;        // [2] {s_K, s_V} of the FP8 input
+  uint32_t units;               // ceil(T / 2) * Hkv * D / 16 (token pair, head, 16-element block)
+  int sms;                      // SMs of the device (sizes the grid)
 };
 
 struct PrefixArgs {

@@ -10,9 +10,15 @@
 // engine hands to the cache in Figure 2): then each element is
 // e4m3(code) * s_in, one FP32 product, and is encoded the same way.
 //
-// One thread owns one 16-element block (one NVFP4 scale block) of the same
+// A unit is one 16-element block (one NVFP4 scale block) of the same
 // head-dim range of two consecutive tokens 2p and 2p+1 of the call; D/16
-// neighbouring threads form a row (INT4 reduces its row maximum over them).
+// neighbouring units form a row (INT4 reduces its row maximum over their
+// threads).  The grid is sized to the resident CTAs and each warp walks its
+// 32 units a grid apart, staging their input bytes and slots in the warp's
+// part of a shared-memory ring with asynchronous copies (cp.async) issued
+// kWriteStages - 1 steps ahead, so the loads of later units are in flight
+// while the current ones are encoded; the lanes copy 512 contiguous input
+// bytes an instruction for one another.
 // NVFP4 V goes to the token-pair rows the decode kernel reads (element d of
 // tokens 2p and 2p+1 share a byte): when the two tokens land in the two
 // halves of one pair row (the usual prefill), the thread writes the pair's
@@ -36,17 +42,46 @@ __device__ __forceinline__ uint2 e2m1x16(const float (&q)[16]) {
   return make_uint2(f32x8_to_e2m1x8(q), f32x8_to_e2m1x8(q + 8));
 }
 
-// q_j = RN(x_j / b) for 16 values, b > 0 with yb = RN(1/b): div_rn on FP32
-// pairs where div_rn_in_range(yb, amax) holds (amax >= every |x_j|), else
-// the IEEE division.
-__device__ __forceinline__ void div16(const float (&x)[16], float b, float yb, float amax, float (&q)[16]) {
-  if (div_rn_in_range(yb, amax)) {
-    const uint64_t nb = f2(-b, -b), yb2 = f2(yb, yb);
+// Byte j = E2M1(lo[j]) | E2M1(hi[j]) << 4 for j = 0..15 (round to nearest
+// even, saturating at 6, sign kept): the token-pair row bytes of NVFP4 V
+// when lo / hi are the quotients of tokens 2p / 2p+1.
+__device__ __forceinline__ uint4 e2m1_pairs16(const float (&lo)[16], const float (&hi)[16]) {
+  uint32_t w[4];
 #pragma unroll
-    for (int j = 0; j < 16; j += 2) div_rn_pair(x[j], x[j + 1], nb, yb2, q[j], q[j + 1]);
+  for (int i = 0; i < 4; ++i)
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %1, %2;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %3, %4;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %5, %6;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %7, %8;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(w[i])
+        : "f"(hi[4 * i]), "f"(lo[4 * i]), "f"(hi[4 * i + 1]), "f"(lo[4 * i + 1]), "f"(hi[4 * i + 2]),
+          "f"(lo[4 * i + 2]), "f"(hi[4 * i + 3]), "f"(lo[4 * i + 3]));
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// q_j = RN(x_j / b) for 16 values given their negations nx_j = -x_j, b > 0
+// with yb = RN(1/b): Markstein's correction step on FP32 pairs where
+// div_rn_in_range(yb, amax) holds (amax >= every |x_j|), else the IEEE
+// division.  With ny = -yb the step reads q0 = RN(nx ny) = RN(x yb),
+// e = b q0 + nx = -(x - b q0) (exact under fma), q = RN(e ny + q0)
+// = RN(q0 + (x - b q0) yb): the same bits as the usual order, and for x = -0
+// (nx = +0) it gives q = -0, the IEEE sign of a zero quotient, with no
+// fix-up.
+__device__ __forceinline__ void div16(const float (&nx)[16], float b, float yb, float amax, float (&q)[16]) {
+  if (div_rn_in_range(yb, amax)) {
+    const uint64_t b2 = f2(b, b), ny2 = f2(-yb, -yb);
+#pragma unroll
+    for (int j = 0; j < 16; j += 2) {
+      const uint64_t x = f2(nx[j], nx[j + 1]);
+      const uint64_t q0 = mul_f2(x, ny2);
+      const uint64_t e = fma_f2(b2, q0, x);
+      f2_split(fma_f2(e, ny2, q0), q[j], q[j + 1]);
+    }
   } else {                                      // operands near the FP32 range limits
 #pragma unroll
-    for (int j = 0; j < 16; ++j) q[j] = __fdiv_rn(x[j], b);
+    for (int j = 0; j < 16; ++j) q[j] = -__fdiv_rn(nx[j], b);
   }
 }
 
@@ -57,35 +92,112 @@ __device__ __forceinline__ uint2 spread_nibbles(uint32_t w) {
   return make_uint2(prmt(lo4, hi4, 0x5140u), prmt(lo4, hi4, 0x7362u));
 }
 
-// 16 consecutive elements of row `row` of K or V -> FP32 (bf16, or E4M3
-// times the input scale as one FP32 product).
-__device__ __forceinline__ void load16(const WriteArgs& a, int kind, int64_t row, int D, int b, float (&x)[16]) {
-  const int64_t base = row * D + 16 * b;
+constexpr int kWriteThreads = 256;
+constexpr int kWriteWarps = kWriteThreads / 32;
+constexpr int kWriteStages = 3;          // units staged per thread (two in flight while one is encoded)
+constexpr int kWriteCtasPerSm = 3;       // 3 x 61.4 KB of staging per SM
+// A warp's stage: 128 16-byte data slots (its 32 units x 2 tokens x 32 bf16
+// bytes; FP8 input uses the first 64), then 32 slot pairs (16 bytes a unit).
+constexpr uint32_t kWarpData = 128 * 16;
+constexpr uint32_t kWarpStage = kWarpData + 32 * 16;
+constexpr int kWriteSmem = kWriteStages * kWriteWarps * kWarpStage;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// bf16 data slot m = 64 j + 2 l + c (token j, unit lane l, 16-byte half c)
+// sits at slot m ^ bit 3 of m: the copies (32 consecutive m an instruction)
+// and the reads (m = 2l + c over the lanes) are both free of bank conflicts.
+__device__ __forceinline__ uint32_t slot_pos(uint32_t m) { return m ^ ((m >> 3) & 1u); }
+
+// Unit u -> (first token t0 = 2p, head h, block b).
+struct Unit {
+  int64_t t0;
+  int h, b;
+};
+template <int D>
+__device__ __forceinline__ Unit unit_of(const WriteArgs& a, uint32_t u) {
+  constexpr int NB = D / 16;
+  const uint32_t ph = u / NB;                     // (pair, head)
+  const uint32_t pair = fdiv(ph, a.hkv_div);
+  return Unit{2 * static_cast<int64_t>(pair), static_cast<int>(ph - pair * static_cast<uint32_t>(a.Hkv)),
+              static_cast<int>(u % NB)};
+}
+
+// Stage the input and slots of the warp's units ub + 0..31 at `wst` (the
+// warp's stage).  bf16: copy instruction k moves data slots m = 32 k + lane,
+// i.e. half (lane & 1) of unit 16 (k & 1) + lane / 2's block of token k / 2,
+// so each instruction reads 512 contiguous bytes of a row run; FP8: slot
+// 32 j + lane is token j of the lane's own unit.  Slots: the even lane of a
+// pair copies token t0's slot, the odd lane t0 + 1's.  Nothing is copied for
+// a unit past the end or a token past T (those bytes are never stored).
+template <int D>
+__device__ __forceinline__ void stage_warp(const WriteArgs& a, int kind, uint32_t ub, uint32_t lane,
+                                           uint32_t wst) {
   if (a.k8 != nullptr) {
-    const uint4 raw = __ldg(reinterpret_cast<const uint4*>((kind == 0 ? a.k8 : a.v8) + base));
-    const float s_in = __ldg(a.in_scale + kind);
+    const uint32_t u = ub + lane;
+    if (u >= a.units) return;
+    const Unit n = unit_of<D>(a, u);
+    const uint8_t* src = (kind == 0 ? a.k8 : a.v8) + 16 * n.b;
+    const int64_t row0 = n.t0 * a.Hkv + n.h;
+    cp_async16(wst + 16 * lane, src + row0 * D);
+    if (n.t0 + 1 < a.T) cp_async16(wst + 16 * (32 + lane), src + (row0 + a.Hkv) * D);
+    cp_async8(wst + kWarpData + 16 * lane, a.slot_mapping + n.t0);
+    if (n.t0 + 1 < a.T) cp_async8(wst + kWarpData + 16 * lane + 8, a.slot_mapping + n.t0 + 1);
+    return;
+  }
+  const __nv_bfloat16* src = kind == 0 ? a.k : a.v;
+  const uint32_t c = lane & 1u;
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {                   // unit lane l = 16 q + lane / 2
+    const uint32_t l = 16 * q + (lane >> 1), u = ub + l;
+    if (u >= a.units) continue;
+    const Unit n = unit_of<D>(a, u);
+    const __nv_bfloat16* p = src + (n.t0 * a.Hkv + n.h) * D + 16 * n.b + 8 * c;
+    const bool live1 = n.t0 + 1 < a.T;
+    cp_async16(wst + 16 * slot_pos(2 * l + c), p);
+    if (live1) cp_async16(wst + 16 * slot_pos(64 + 2 * l + c), p + static_cast<int64_t>(a.Hkv) * D);
+    if (c == 0 || live1) cp_async8(wst + kWarpData + 16 * l + 8 * c, a.slot_mapping + n.t0 + c);
+  }
+}
+
+// The negated 16 elements of token j (0: t0, 1: t0 + 1) of unit lane `lane`
+// staged at `wst` -> FP32: -bf16 (exact), or E4M3 times -s_in as one FP32
+// product (the negation of RN(e4m3 * s_in)).
+__device__ __forceinline__ void staged16_neg(const WriteArgs& a, int kind, uint32_t wst, uint32_t lane, int j,
+                                             float (&nx)[16]) {
+  if (a.k8 != nullptr) {
+    const uint4 raw = lds128(wst + 16 * (32 * j + lane));
+    const float ns_in = -__ldg(a.in_scale + kind);
     const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       uint32_t hh[2];
       e4m3x4_to_f16x2x2(w[i], hh[0], hh[1]);
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hh[j]));
-        x[4 * i + 2 * j] = __fmul_rn(f.x, s_in);
-        x[4 * i + 2 * j + 1] = __fmul_rn(f.y, s_in);
+      for (int k = 0; k < 2; ++k) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hh[k]));
+        nx[4 * i + 2 * k] = __fmul_rn(f.x, ns_in);
+        nx[4 * i + 2 * k + 1] = __fmul_rn(f.y, ns_in);
       }
     }
   } else {
-    const uint4* src = reinterpret_cast<const uint4*>((kind == 0 ? a.k : a.v) + base);
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
-      const uint4 raw = __ldg(src + u);
+      const uint4 raw = lds128(wst + 16 * slot_pos(64 * j + 2 * lane + u));
       const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        x[8 * u + 2 * j] = __uint_as_float(w[j] << 16);           // bf16 -> FP32 is exact
-        x[8 * u + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+      for (int k = 0; k < 4; ++k) {
+        // bf16 -> FP32 is exact; adding 2^31 flips the sign bit
+        nx[8 * u + 2 * k] = __uint_as_float(w[k] * 65536u + 0x80000000u);
+        nx[8 * u + 2 * k + 1] = __uint_as_float((w[k] & 0xFFFF0000u) ^ 0x80000000u);
       }
     }
   }
@@ -99,11 +211,9 @@ struct Dest {
   int64_t slot;
   bool ok;
 };
-__device__ __forceinline__ Dest dest_of(const WriteArgs& a, int64_t t, int h, bool flag) {
+__device__ __forceinline__ Dest dest_of(const WriteArgs& a, int64_t t, int64_t slot, int h, bool flag) {
   Dest d{nullptr, 0, -1, false};
-  if (t >= a.T) return d;
-  const int64_t slot = a.slot_mapping[t];
-  if (slot < 0) return d;
+  if (t >= a.T || slot < 0) return d;
   if (slot >= static_cast<int64_t>(a.num_pages) * a.P) {
     if (flag) set_error(a.err, KV4_EBOUNDS);
     return d;
@@ -118,76 +228,58 @@ __device__ __forceinline__ Dest dest_of(const WriteArgs& a, int64_t t, int h, bo
   return d;
 }
 
-// Thread (token pair p, head h, 16-element block b; K|V = blockIdx.y).
-template <int D, int FMT>
-__global__ void __launch_bounds__(256, 4)
-write_kernel(const WriteArgs a) {
-  grid_dep_launch();   // a following decode launch may be scheduled early
+// Encode unit u (K|V = kind) from the warp's stage `wst`; `live` false for a
+// thread past the last unit (it computes on whatever the stage holds and
+// stores nothing, so that whole rows of threads share the INT4 shuffles).
+template <int D, int FMT, int kind>
+__device__ __forceinline__ void write_unit(const WriteArgs& a, uint32_t u, bool live, uint32_t wst, uint32_t lane,
+                                           const float2* s_den, float g6, float r6) {
   constexpr int NB = D / 16;                      // threads per row
   constexpr int RB = D / 2, SB = D / 16;
-  const int kind = blockIdx.y;                    // 0: K, 1: V
-  // NVFP4: (denominator, its reciprocal) of every E4M3 block-scale byte S:
-  // denom = RN(e4m3(S) * g), 1/denom correctly rounded
-  __shared__ float2 s_den[FMT == KV4_NVFP4 ? 256 : 1];
-  float g = 1.f, g6 = 1.f, r6 = 1.f;
-  if constexpr (FMT == KV4_NVFP4) {
-    g = __ldg(a.gscale + kind);
-    g6 = __fmul_rn(kE2M1Max, g);
-    r6 = __frcp_rn(g6);
-    const float den = __fmul_rn(e4m3_to_f32(threadIdx.x), g);
-    s_den[threadIdx.x] = make_float2(den, __frcp_rn(den));
-    __syncthreads();
-  }
-  const uint32_t gtid = blockIdx.x * 256u + threadIdx.x;
-  const uint32_t ph = gtid / NB;                  // (pair, head)
-  const int b = static_cast<int>(gtid % NB);
-  const uint32_t pair = fdiv(ph, a.hkv_div);
-  const int h = static_cast<int>(ph - pair * static_cast<uint32_t>(a.Hkv));
-  const int64_t t0 = 2 * static_cast<int64_t>(pair);
-  // rows past the end compute on row 0 and store nothing (whole rows of
-  // threads share the shuffles below)
-  const bool live0 = t0 < a.T, live1 = t0 + 1 < a.T;
-  const Dest d0 = dest_of(a, t0, h, b == 0), d1 = dest_of(a, t0 + 1, h, b == 0);
+  const Unit n = unit_of<D>(a, u);
+  const int b = n.b, h = n.h;
+  const int64_t t0 = live ? n.t0 : a.T;           // past the end: no destination
+  const uint4 sl = lds128(wst + kWarpData + 16 * lane);
+  const int64_t slot0 = static_cast<int64_t>((static_cast<uint64_t>(sl.y) << 32) | sl.x);
+  const int64_t slot1 = static_cast<int64_t>((static_cast<uint64_t>(sl.w) << 32) | sl.z);
+  const Dest d0 = dest_of(a, t0, slot0, h, b == 0), d1 = dest_of(a, t0 + 1, slot1, h, b == 0);
 
-  float x0[16], x1[16];
-  load16(a, kind, live0 ? t0 * a.Hkv + h : 0, D, b, x0);
-  load16(a, kind, live1 ? (t0 + 1) * a.Hkv + h : 0, D, b, x1);
-
+  // each token's elements are read from the stage as their negations
   if constexpr (FMT == KV4_NVFP4) {
-    uint2 word[2];
+    float q[2][16];
     uint32_t S[2];
+    uint2 kw[2];                      // K: token k's codes
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-      const float(&x)[16] = k == 0 ? x0 : x1;
+      float x[16];
+      staged16_neg(a, kind, wst, lane, k, x);
       float amax = 0.f;
 #pragma unroll
       for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(x[j]));
       const float sf = div_rn(amax, g6, r6);
       S[k] = f32_to_e4m3(sf);
       const float2 dr = s_den[S[k]];
-      word[k] = make_uint2(0u, 0u);
       if (S[k] != 0u && dr.x != 0.f) {
-        float q[16];
-        div16(x, dr.x, dr.y, amax, q);
-        word[k] = e2m1x16(q);
+        div16(x, dr.x, dr.y, amax, q[k]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) q[k][j] = 0.f;     // codes 0
       }
+      if constexpr (kind == 0) kw[k] = e2m1x16(q[k]);
     }
-    if (kind == 0) {
+    if constexpr (kind == 0) {
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const Dest& d = k == 0 ? d0 : d1;
         if (!d.ok) continue;
-        *reinterpret_cast<uint2*>(d.chunk + static_cast<int64_t>(d.off) * RB + 8 * b) = word[k];
+        *reinterpret_cast<uint2*>(d.chunk + static_cast<int64_t>(d.off) * RB + 8 * b) = kw[k];
         d.chunk[static_cast<int64_t>(a.P) * D + static_cast<int64_t>(d.off) * SB + b] = static_cast<uint8_t>(S[k]);
       }
     } else if (d0.ok && d1.ok && (d0.slot & 1) == 0 && d1.slot == d0.slot + 1) {
       // both halves of one pair row: byte d = element d of token 2p (low
       // nibble) and of token 2p+1 (high nibble); scale bytes (s_even, s_odd)
-      const uint2 a0 = spread_nibbles(word[0].x), a1 = spread_nibbles(word[0].y);
-      const uint2 b0 = spread_nibbles(word[1].x), b1 = spread_nibbles(word[1].y);
       *reinterpret_cast<uint4*>(d0.chunk + static_cast<int64_t>(a.P) * RB + static_cast<int64_t>(d0.off >> 1) * D +
-                                16 * b) =
-          make_uint4(a0.x | (b0.x << 4), a0.y | (b0.y << 4), a1.x | (b1.x << 4), a1.y | (b1.y << 4));
+                                16 * b) = e2m1_pairs16(q[0], q[1]);
       *reinterpret_cast<uint16_t*>(d0.chunk + static_cast<int64_t>(a.P) * D + static_cast<int64_t>(a.P) * SB +
                                    static_cast<int64_t>(d0.off >> 1) * 2 * SB + 2 * b) =
           static_cast<uint16_t>(S[0] | (S[1] << 8));
@@ -201,9 +293,10 @@ write_kernel(const WriteArgs a) {
         const int sh = 4 * (d.off & 1);
         unsigned long long* dst = reinterpret_cast<unsigned long long*>(
             d.chunk + static_cast<int64_t>(a.P) * RB + static_cast<int64_t>(d.off >> 1) * D + 16 * b);
+        const uint2 word = e2m1x16(q[k]);
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          const uint2 sp = spread_nibbles(u == 0 ? word[k].x : word[k].y);
+          const uint2 sp = spread_nibbles(u == 0 ? word.x : word.y);
           const uint64_t v = (static_cast<uint64_t>(sp.y) << 32) | sp.x;
           atomicAnd(dst + u, ~(0x0F0F0F0F0F0F0F0Full << sh));
           atomicOr(dst + u, static_cast<unsigned long long>(v << sh));
@@ -218,7 +311,8 @@ write_kernel(const WriteArgs a) {
     const float rs = __frcp_rn(s);
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-      const float(&x)[16] = k == 0 ? x0 : x1;
+      float x[16];
+      staged16_neg(a, kind, wst, lane, k, x);
       const Dest& d = k == 0 ? d0 : d1;
       float amax = 0.f;
 #pragma unroll
@@ -236,7 +330,8 @@ write_kernel(const WriteArgs a) {
   } else {
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-      const float(&x)[16] = k == 0 ? x0 : x1;
+      float x[16];
+      staged16_neg(a, kind, wst, lane, k, x);
       const Dest& d = k == 0 ? d0 : d1;
       // row amax over the D/16 threads of the row (aligned groups of a warp)
       float amax = 0.f;
@@ -267,11 +362,78 @@ write_kernel(const WriteArgs a) {
   }
 }
 
+// Each warp walks units a grid apart (K|V = kind), staging kWriteStages - 1
+// steps ahead of the one it encodes; a lane may copy bytes another lane
+// reads, so the warp syncs after its copies land and before a stage is
+// refilled.
+template <int D, int FMT, int kind>
+__device__ __forceinline__ void write_walk(const WriteArgs& a, uint8_t* s_stage, const float2* s_den, float g6,
+                                           float r6) {
+  const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+  const uint32_t total = a.units, stride = gridDim.x * kWriteThreads;
+  const uint32_t w0 = smem_u32(s_stage) + warp * kWarpStage;
+  constexpr uint32_t kStageBytes = kWriteWarps * kWarpStage;
+  uint32_t ub = blockIdx.x * kWriteThreads + warp * 32;      // the warp's units are ub + lane
+#pragma unroll
+  for (int s = 0; s < kWriteStages - 1; ++s) {
+    if (ub + s * stride < total) stage_warp<D>(a, kind, ub + s * stride, lane, w0 + s * kStageBytes);
+    cp_async_commit();
+  }
+  int cur = 0;
+  for (; ub < total; ub += stride) {
+    const uint32_t ahead = ub + (kWriteStages - 1) * stride;
+    const int nxt = cur == 0 ? kWriteStages - 1 : cur - 1;     // the stage encoded last
+    __syncwarp();                                 // every lane is done reading it
+    if (ahead < total) stage_warp<D>(a, kind, ahead, lane, w0 + nxt * kStageBytes);
+    cp_async_commit();
+    cp_async_wait<kWriteStages - 1>();            // this lane's copies for step ub
+    __syncwarp();                                 // and every other lane's
+    const uint32_t u = ub + lane;
+    write_unit<D, FMT, kind>(a, u < total ? u : 0u, u < total, w0 + cur * kStageBytes, lane, s_den, g6, r6);
+    cur = cur + 1 == kWriteStages ? 0 : cur + 1;
+  }
+  cp_async_wait<0>();                             // no copy outlives the CTA
+}
+
+// Persistent CTAs of kWriteThreads threads, kWriteCtasPerSm per SM, half on
+// K (blockIdx.y = 0) and half on V; each thread walks units a grid apart.
+template <int D, int FMT>
+__global__ void __launch_bounds__(kWriteThreads, kWriteCtasPerSm)
+write_kernel(const WriteArgs a) {
+  grid_dep_launch();   // a following decode launch may be scheduled early
+  const int kind = blockIdx.y;                    // 0: K, 1: V
+  extern __shared__ __align__(16) uint8_t s_stage[];
+  // NVFP4: (denominator, its reciprocal) of every E4M3 block-scale byte S:
+  // denom = RN(e4m3(S) * g), 1/denom correctly rounded
+  __shared__ float2 s_den[FMT == KV4_NVFP4 ? 256 : 1];
+  float g6 = 1.f, r6 = 1.f;
+  if constexpr (FMT == KV4_NVFP4) {
+    const float g = __ldg(a.gscale + kind);
+    g6 = __fmul_rn(kE2M1Max, g);
+    r6 = __frcp_rn(g6);
+    const float den = __fmul_rn(e4m3_to_f32(threadIdx.x), g);
+    s_den[threadIdx.x] = make_float2(den, __frcp_rn(den));
+    __syncthreads();
+  }
+  if (kind == 0) write_walk<D, FMT, 0>(a, s_stage, s_den, g6, r6);
+  else write_walk<D, FMT, 1>(a, s_stage, s_den, g6, r6);
+}
+
 template <int D, int FMT>
 static cudaError_t launch_write_t(const WriteArgs& a, cudaStream_t st) {
-  const int64_t threads = (a.T + 1) / 2 * a.Hkv * (D / 16);
-  const int64_t blocks = (threads + 255) / 256;
-  write_kernel<D, FMT><<<dim3(static_cast<unsigned>(blocks), 2), 256, 0, st>>>(a);
+  auto* k = write_kernel<D, FMT>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kWriteSmem);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const int64_t need = (static_cast<int64_t>(a.units) + kWriteThreads - 1) / kWriteThreads;
+  const int64_t resident = static_cast<int64_t>(a.sms) * kWriteCtasPerSm / 2;   // per K|V
+  const int64_t blocks = need < resident ? need : (resident > 0 ? resident : 1);
+  k<<<dim3(static_cast<unsigned>(blocks), 2), kWriteThreads, kWriteSmem, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -279,6 +441,7 @@ cudaError_t launch_write(const WriteArgs& a_in, cudaStream_t st) {
   if (a_in.T == 0) return cudaSuccess;
   WriteArgs a = a_in;
   a.rows = static_cast<int>(a.T * a.Hkv);
+  a.units = static_cast<uint32_t>((a.T + 1) / 2 * a.Hkv * (a.D / 16));
   a.hkv_div = make_fastdiv(static_cast<uint32_t>(a.Hkv));
   a.p_div = make_fastdiv(static_cast<uint32_t>(a.P));
   if (a.fmt == KV4_NVFP4) {

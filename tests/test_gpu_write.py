@@ -182,3 +182,65 @@ def test_write_pair_rows_every_slot_pattern(fmt, D):
     got = pool.buffer.cpu().numpy()
     diff = np.nonzero(got != ref)[0]
     assert diff.size == 0, f"{fmt} D{D}: {diff.size} bytes differ, first at {diff[:8]}"
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "int4", "fp8"])
+def test_write_many_units_per_thread(fmt):
+    """A prefill-sized call: each thread of the resident grid walks several
+    units through its staging ring (12,289 tokens x 4 heads x 16 blocks per
+    K|V, about seven units a thread).  An aligned run, a shuffled run with
+    skipped tokens and the odd last token, over a pool of random bytes."""
+    T, H, D, P = 12289, 4, 256, 64
+    pages = (T + P - 1) // P + 8
+    rng = np.random.default_rng(12289)
+    x = (rng.standard_normal((2, T, H, D)) * np.exp(rng.uniform(-3, 3, (2, T, H, 1)))).astype(np.float32)
+    x[:, :, :, 9] *= 11.0
+    k, v = f32_to_bf16_bits(x[0]), f32_to_bf16_bits(x[1])
+    g = np.array([np.abs(x[0]).max() / 2688.0, np.abs(x[1]).max() / 2688.0], np.float32)
+    half = 6000
+    slots = np.concatenate([np.arange(half) + 2 * P,
+                            rng.permutation(np.arange(half + 2 * P + 1, pages * P))[:T - half]]).astype(np.int64)
+    slots[half::13] = -1
+    spec = OP.PoolSpec(fmt, pages, P, H, D)
+    fill = rng.integers(0, 256, spec.pool_bytes, dtype=np.uint8)
+    if fmt == "int4":
+        for page in range(pages):
+            for h in range(H):
+                off = int(spec.chunk_offset(page, h)) + spec.region("ks")
+                fill[off:off + 2 * P * 4] = np.full(2 * P, 0.5, np.float32).view(np.uint8)
+    ref = OP.write(fill.copy(), spec, k, v, slots, g)
+    pool = guarded_pool(fmt, pages, P, H, D)
+    pool.buffer.copy_(torch.from_numpy(fill))
+    K.kv4_write(dev_bf16(k), dev_bf16(v), torch.from_numpy(slots).cuda(), pool, torch.from_numpy(g).cuda())
+    torch.cuda.synchronize()
+    assert K.kv4_device_error() == 0
+    assert_guard_intact(pool.guard, "pool")
+    got = pool.buffer.cpu().numpy()
+    diff = np.nonzero(got != ref)[0]
+    assert diff.size == 0, f"{fmt}: {diff.size} bytes differ, first at {diff[:8]}"
+
+
+def test_write_fp8_input_many_units_per_thread():
+    """The FP8-input write (16 staged bytes a token) at prefill size: several
+    units per thread through the staging ring, byte for byte."""
+    from workloads import fp8_kv_codes
+    T, H, D, P = 12289, 4, 256, 64
+    pages = (T + P - 1) // P + 4
+    codes, s_in = fp8_kv_codes(77, T, H, D, "cuda", [[2, 40]] * H, 12.0)
+    s_in = (s_in * np.float32(0.73)).astype(np.float32)
+    rng = np.random.default_rng(77)
+    slots = rng.permutation(pages * P)[:T].astype(np.int64)
+    slots[::29] = -1
+    g = np.array([0.017, 0.009], np.float32)
+    pool = guarded_pool("nvfp4", pages, P, H, D, fill=0x3C)
+    K.kv4_write_fp8(codes[0].contiguous(), codes[1].contiguous(), torch.from_numpy(s_in).cuda(),
+                    torch.from_numpy(slots).cuda(), pool, torch.from_numpy(g).cuda())
+    torch.cuda.synchronize()
+    assert K.kv4_device_error() == 0
+    spec = OP.PoolSpec("nvfp4", pages, P, H, D)
+    ref = OP.write_fp8(OP.new_pool(spec, 0x3C), spec, codes[0].cpu().numpy(), codes[1].cpu().numpy(),
+                       s_in, slots, g)
+    got = pool.buffer.cpu().numpy()
+    diff = np.nonzero(got != ref)[0]
+    assert diff.size == 0, f"{diff.size} bytes differ, first at {diff[:8]}"
+    assert_guard_intact(pool.guard, "pool")
