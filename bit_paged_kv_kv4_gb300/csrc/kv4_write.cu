@@ -42,23 +42,16 @@ __device__ __forceinline__ uint2 e2m1x16(const float (&q)[16]) {
   return make_uint2(f32x8_to_e2m1x8(q), f32x8_to_e2m1x8(q + 8));
 }
 
-// Byte j = E2M1(lo[j]) | E2M1(hi[j]) << 4 for j = 0..15 (round to nearest
-// even, saturating at 6, sign kept): the token-pair row bytes of NVFP4 V
-// when lo / hi are the quotients of tokens 2p / 2p+1.
-__device__ __forceinline__ uint4 e2m1_pairs16(const float (&lo)[16], const float (&hi)[16]) {
-  uint32_t w[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 b0, %1, %2;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 b1, %3, %4;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 b2, %5, %6;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 b3, %7, %8;\n\t"
-        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
-        : "=r"(w[i])
-        : "f"(hi[4 * i]), "f"(lo[4 * i]), "f"(hi[4 * i + 1]), "f"(lo[4 * i + 1]), "f"(hi[4 * i + 2]),
-          "f"(lo[4 * i + 2]), "f"(hi[4 * i + 3]), "f"(lo[4 * i + 3]));
-  return make_uint4(w[0], w[1], w[2], w[3]);
+// Eight codes of token 2p (nibble i of a) and of token 2p+1 (nibble i of b)
+// -> the pair row's eight bytes a_i | b_i << 4 (element i in byte i).
+__device__ __forceinline__ uint2 zip_nibbles(uint32_t a, uint32_t b) {
+  const uint32_t ev = (a & 0x0F0F0F0Fu) | ((b << 4) & 0xF0F0F0F0u);     // elements 0, 2, 4, 6
+  const uint32_t od = ((a >> 4) & 0x0F0F0F0Fu) | (b & 0xF0F0F0F0u);     // elements 1, 3, 5, 7
+  return make_uint2(prmt(ev, od, 0x5140u), prmt(ev, od, 0x7362u));
+}
+__device__ __forceinline__ uint4 zip16(uint2 a, uint2 b) {
+  const uint2 lo = zip_nibbles(a.x, b.x), hi = zip_nibbles(a.y, b.y);
+  return make_uint4(lo.x, lo.y, hi.x, hi.y);
 }
 
 // q_j = RN(x_j / b) for 16 values given their negations nx_j = -x_j, b > 0
@@ -94,8 +87,8 @@ __device__ __forceinline__ uint2 spread_nibbles(uint32_t w) {
 
 constexpr int kWriteThreads = 256;
 constexpr int kWriteWarps = kWriteThreads / 32;
-constexpr int kWriteStages = 3;          // units staged per thread (two in flight while one is encoded)
-constexpr int kWriteCtasPerSm = 3;       // 3 x 61.4 KB of staging per SM
+constexpr int kWriteStages = 2;          // steps staged per warp (one in flight while one is encoded)
+constexpr int kWriteCtasPerSm = 3;       // 3 x 41 KB of staging per SM
 // A warp's stage: 128 16-byte data slots (its 32 units x 2 tokens x 32 bf16
 // bytes; FP8 input uses the first 64), then 32 slot pairs (16 bytes a unit).
 constexpr uint32_t kWarpData = 128 * 16;
@@ -168,6 +161,18 @@ __device__ __forceinline__ void stage_warp(const WriteArgs& a, int kind, uint32_
   }
 }
 
+// -x as FP32 for the two bf16 values x of w (exact): (w << 16) + 2^31 and
+// (w & 0xFFFF0000) ^ 2^31, one integer instruction each (written as PTX so
+// that they are not turned into float negations, which the packed FP32
+// operations that consume them cannot fold).
+__device__ __forceinline__ void neg_bf16x2(uint32_t w, float& lo, float& hi) {
+  uint32_t l, h;
+  asm("mad.lo.u32 %0, %1, 65536, 0x80000000;" : "=r"(l) : "r"(w));
+  asm("lop3.b32 %0, %1, 0xFFFF0000, 0x80000000, 0x6a;" : "=r"(h) : "r"(w));
+  lo = __uint_as_float(l);
+  hi = __uint_as_float(h);
+}
+
 // The negated 16 elements of token j (0: t0, 1: t0 + 1) of unit lane `lane`
 // staged at `wst` -> FP32: -bf16 (exact), or E4M3 times -s_in as one FP32
 // product (the negation of RN(e4m3 * s_in)).
@@ -194,11 +199,7 @@ __device__ __forceinline__ void staged16_neg(const WriteArgs& a, int kind, uint3
       const uint4 raw = lds128(wst + 16 * slot_pos(64 * j + 2 * lane + u));
       const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        // bf16 -> FP32 is exact; adding 2^31 flips the sign bit
-        nx[8 * u + 2 * k] = __uint_as_float(w[k] * 65536u + 0x80000000u);
-        nx[8 * u + 2 * k + 1] = __uint_as_float((w[k] & 0xFFFF0000u) ^ 0x80000000u);
-      }
+      for (int k = 0; k < 4; ++k) neg_bf16x2(w[k], nx[8 * u + 2 * k], nx[8 * u + 2 * k + 1]);
     }
   }
 }
@@ -239,16 +240,18 @@ __device__ __forceinline__ void write_unit(const WriteArgs& a, uint32_t u, bool 
   const Unit n = unit_of<D>(a, u);
   const int b = n.b, h = n.h;
   const int64_t t0 = live ? n.t0 : a.T;           // past the end: no destination
-  const uint4 sl = lds128(wst + kWarpData + 16 * lane);
-  const int64_t slot0 = static_cast<int64_t>((static_cast<uint64_t>(sl.y) << 32) | sl.x);
-  const int64_t slot1 = static_cast<int64_t>((static_cast<uint64_t>(sl.w) << 32) | sl.z);
-  const Dest d0 = dest_of(a, t0, slot0, h, b == 0), d1 = dest_of(a, t0 + 1, slot1, h, b == 0);
+  // token k's destination (taken after the arithmetic where that keeps
+  // fewer registers live across it)
+  auto dest = [&](int k) {
+    const uint2 sl = lds64(wst + kWarpData + 16 * lane + 8 * k);
+    const int64_t slot = static_cast<int64_t>((static_cast<uint64_t>(sl.y) << 32) | sl.x);
+    return dest_of(a, t0 + k, slot, h, b == 0);
+  };
 
   // each token's elements are read from the stage as their negations
   if constexpr (FMT == KV4_NVFP4) {
-    float q[2][16];
     uint32_t S[2];
-    uint2 kw[2];                      // K: token k's codes
+    uint2 kw[2];                      // token k's codes, element i in nibble i
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
       float x[16];
@@ -259,14 +262,14 @@ __device__ __forceinline__ void write_unit(const WriteArgs& a, uint32_t u, bool 
       const float sf = div_rn(amax, g6, r6);
       S[k] = f32_to_e4m3(sf);
       const float2 dr = s_den[S[k]];
+      kw[k] = make_uint2(0u, 0u);
       if (S[k] != 0u && dr.x != 0.f) {
-        div16(x, dr.x, dr.y, amax, q[k]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) q[k][j] = 0.f;     // codes 0
+        float q[16];
+        div16(x, dr.x, dr.y, amax, q);
+        kw[k] = e2m1x16(q);
       }
-      if constexpr (kind == 0) kw[k] = e2m1x16(q[k]);
     }
+    const Dest d0 = dest(0), d1 = dest(1);
     if constexpr (kind == 0) {
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
@@ -279,7 +282,7 @@ __device__ __forceinline__ void write_unit(const WriteArgs& a, uint32_t u, bool 
       // both halves of one pair row: byte d = element d of token 2p (low
       // nibble) and of token 2p+1 (high nibble); scale bytes (s_even, s_odd)
       *reinterpret_cast<uint4*>(d0.chunk + static_cast<int64_t>(a.P) * RB + static_cast<int64_t>(d0.off >> 1) * D +
-                                16 * b) = e2m1_pairs16(q[0], q[1]);
+                                16 * b) = zip16(kw[0], kw[1]);
       *reinterpret_cast<uint16_t*>(d0.chunk + static_cast<int64_t>(a.P) * D + static_cast<int64_t>(a.P) * SB +
                                    static_cast<int64_t>(d0.off >> 1) * 2 * SB + 2 * b) =
           static_cast<uint16_t>(S[0] | (S[1] << 8));
@@ -293,10 +296,9 @@ __device__ __forceinline__ void write_unit(const WriteArgs& a, uint32_t u, bool 
         const int sh = 4 * (d.off & 1);
         unsigned long long* dst = reinterpret_cast<unsigned long long*>(
             d.chunk + static_cast<int64_t>(a.P) * RB + static_cast<int64_t>(d.off >> 1) * D + 16 * b);
-        const uint2 word = e2m1x16(q[k]);
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          const uint2 sp = spread_nibbles(u == 0 ? word.x : word.y);
+          const uint2 sp = spread_nibbles(u == 0 ? kw[k].x : kw[k].y);
           const uint64_t v = (static_cast<uint64_t>(sp.y) << 32) | sp.x;
           atomicAnd(dst + u, ~(0x0F0F0F0F0F0F0F0Full << sh));
           atomicOr(dst + u, static_cast<unsigned long long>(v << sh));
@@ -313,7 +315,7 @@ __device__ __forceinline__ void write_unit(const WriteArgs& a, uint32_t u, bool 
     for (int k = 0; k < 2; ++k) {
       float x[16];
       staged16_neg(a, kind, wst, lane, k, x);
-      const Dest& d = k == 0 ? d0 : d1;
+      const Dest d = dest(k);
       float amax = 0.f;
 #pragma unroll
       for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(x[j]));
@@ -332,7 +334,7 @@ __device__ __forceinline__ void write_unit(const WriteArgs& a, uint32_t u, bool 
     for (int k = 0; k < 2; ++k) {
       float x[16];
       staged16_neg(a, kind, wst, lane, k, x);
-      const Dest& d = k == 0 ? d0 : d1;
+      const Dest d = dest(k);
       // row amax over the D/16 threads of the row (aligned groups of a warp)
       float amax = 0.f;
 #pragma unroll
