@@ -213,6 +213,7 @@ __device__ __forceinline__ void staged16_neg(const WriteArgs& a, int kind, uint3
   if (a.k8 != nullptr) {
     const uint4 raw = lds128(wst + 16 * (32 * j + lane));
     const float ns_in = -__ldg(a.in_scale + kind);
+    const uint64_t ns2 = f2(ns_in, ns_in);
     const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -220,9 +221,8 @@ __device__ __forceinline__ void staged16_neg(const WriteArgs& a, int kind, uint3
       e4m3x4_to_f16x2x2(w[i], hh[0], hh[1]);
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hh[k]));
-        nx[4 * i + 2 * k] = __fmul_rn(f.x, ns_in);
-        nx[4 * i + 2 * k + 1] = __fmul_rn(f.y, ns_in);
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hh[k]));   // exact
+        f2_split(mul_f2(f2(f.x, f.y), ns2), nx[4 * i + 2 * k], nx[4 * i + 2 * k + 1]);
       }
     }
   } else {
