@@ -24,9 +24,11 @@
 //
 // One thread converts 64 consecutive elements of one (token, head, K|V) row:
 // 32 code bytes (64 for the token-pair rows of NVFP4 V, of which this token's
-// nibbles are kept), one scale word, 64 bytes stored.  One wave of resident
-// CTAs strides over the rows, so the tables are built once per CTA, and each
-// thread loads its next item while it converts the current one.
+// nibbles are kept), one scale word, 64 bytes out.  One wave of resident
+// CTAs strides over the rows, so the tables are built once per CTA; each
+// thread loads its next item while it converts the current one, and a warp's
+// 32 outputs (2 KB in a row of `out`) go out through shared memory as 512
+// contiguous bytes a store instruction.
 #include <cstdint>
 
 #include "kv4_device.cuh"
@@ -108,43 +110,53 @@ __device__ __forceinline__ uint2 int4_word(uint2 tp, uint2 tn, uint32_t w) {
   return make_uint2(int4_bytes(tp, tn, m, w), int4_bytes(tp, tn, m >> 16, w >> 16));
 }
 
-// CTA (gx, kind = blockIdx.y, request b = blockIdx.z); item i of request b =
-// (row = (t, h), part): elements [64 part, 64 part + 64) of that row.
-template <int D, int FMT>
-__global__ void __launch_bounds__(kPrefixThreads, 4)
-prefix_kernel(const PrefixArgs a) {
+// A warp's 32 items are 32 consecutive 64-byte pieces of the output.  Each
+// lane puts its 64 bytes (chunks L = 4 lane + j of 16 bytes) in the warp's
+// 2 KB of shared memory, chunk L at row L / 8, column (L % 8) ^ (row % 8),
+// which keeps both these writes and the reads below free of bank conflicts;
+// then lane l stores linear chunks 32 m + l (m = 0..3), so each store
+// instruction writes 512 contiguous bytes.  `valid` holds bit k for each
+// item k of the 32 that is to be written.
+__device__ __forceinline__ uint32_t tchunk(uint32_t L) { return L ^ ((L >> 3) & 7u); }
+
+__device__ __forceinline__ void store_warp(uint4* gdst, uint32_t sbuf, uint32_t lane, const uint4 (&o)[4],
+                                           uint32_t valid) {
+  if (valid >> lane & 1u) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t addr = sbuf + 16 * tchunk(4 * lane + j);
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(o[j].x), "r"(o[j].y), "r"(o[j].z),
+                   "r"(o[j].w)
+                   : "memory");
+    }
+  }
+  __syncwarp();
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const uint32_t L = 32 * m + lane;
+    if (valid >> (L >> 2) & 1u) gdst[L] = lds128(sbuf + 16 * tchunk(L));
+  }
+  __syncwarp();                                   // the buffer is free for the next step
+}
+
+// The walk of one (kind, request) CTA over its items (kind K|V = 0|1).
+template <int D, int FMT, int kind>
+__device__ __forceinline__ void prefix_walk(const PrefixArgs& a, uint32_t items, int64_t obase, const int32_t* table,
+                                            uint8_t* out, float s8, const uint2* s_tab, uint8_t* s_out) {
   constexpr int TPR = D / 64;                   // threads per row
   constexpr int RB = D / 2, SB = D / 16;
-  __shared__ uint2 s_tab[FMT == KV4_NVFP4 ? 256 : 1];
-  const int b = blockIdx.z;
-  const int kind = blockIdx.y;
-  const float s8 = __ldg(a.fp8_scale + kind);
-  if constexpr (FMT == KV4_NVFP4) {
-    s_tab[threadIdx.x] = nvfp4_scale_table(threadIdx.x, __ldg(a.gscale + kind), s8);
-    __syncthreads();
-  }
-  int n = a.prefix_lens[b];
-  const int cap = min(a.max_prefix_len, a.max_pages * a.P);
-  if (n < 0 || n > cap) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) set_error(a.err, KV4_EBOUNDS);
-    n = n < 0 ? 0 : cap;
-  }
-  const uint32_t items = static_cast<uint32_t>(n) * static_cast<uint32_t>(a.Hkv) * TPR;
-  const int64_t obase = a.cu_prefix[b];
-  const int32_t* table = a.block_table + static_cast<int64_t>(b) * a.max_pages;
-  uint8_t* out = kind == 0 ? a.out_k : a.out_v;
+  constexpr bool VP = FMT == KV4_NVFP4 && kind == 1;   // NVFP4 V: token-pair rows
   const float r8 = __frcp_rn(s8);
-
   // Two-deep software pipeline: the next item's block-table entry and code
   // loads are in flight while this item is converted and stored.
   struct Item {
-    uint4 c[4];          // codes: K (and INT4) in c[0..1]; NVFP4 V pair rows in c[0..3]
+    uint4 c[VP ? 4 : 2]; // codes: 32 bytes, or the 64 of an NVFP4 V pair row
     uint2 sw;            // scale bytes (NVFP4) or the row scale's bits (INT4, in .x)
     int sh;              // NVFP4 V: this token's nibble within the pair byte
-    uint4* dst;          // null: nothing to do
+    bool ok;             // false: nothing to do
   };
   auto load = [&](uint32_t i, Item& it) {
-    it.dst = nullptr;
+    it.ok = false;
     if (i >= items) return;
     const uint32_t row = i / TPR;
     const int part = static_cast<int>(i % TPR);
@@ -158,8 +170,8 @@ prefix_kernel(const PrefixArgs a) {
     }
     const int off = static_cast<int>(t - pidx * static_cast<uint32_t>(a.P));
     const uint8_t* chunk = a.pool + (static_cast<int64_t>(page) * a.Hkv + h) * a.chunk_bytes;
-    it.dst = reinterpret_cast<uint4*>(out + ((obase + t) * a.Hkv + h) * D + part * 64);
-    if (FMT == KV4_NVFP4 && kind == 1) {
+    it.ok = true;
+    if constexpr (VP) {
       // V is stored in token pairs: byte d of pair row off/2 holds element d
       // of this token in nibble off%2; scale byte 2 blk + off%2 of the pair
       const uint4* src = reinterpret_cast<const uint4*>(
@@ -186,15 +198,19 @@ prefix_kernel(const PrefixArgs a) {
   };
 
   const uint32_t stride = gridDim.x * kPrefixThreads;
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t sbuf = smem_u32(s_out) + (threadIdx.x >> 5) * 2048u;
+  uint4* gout = reinterpret_cast<uint4*>(out + obase * a.Hkv * D);
   Item cur, nxt;
-  uint32_t i = blockIdx.x * kPrefixThreads + threadIdx.x;
-  load(i, cur);
-  for (; i < items; i += stride) {
-    load(i + stride, nxt);
-    if (cur.dst != nullptr) {
-      uint4 o[4];
+  // warp-uniform walk: the warp's items are ib + lane
+  uint32_t ib = blockIdx.x * kPrefixThreads + (threadIdx.x & ~31u);
+  load(ib + lane, cur);
+  for (; ib < items; ib += stride) {
+    load(ib + stride + lane, nxt);
+    uint4 o[4];
+    if (cur.ok) {
       if constexpr (FMT == KV4_NVFP4) {
-        if (kind == 0) {
+        if constexpr (!VP) {
           const uint32_t cw[8] = {cur.c[0].x, cur.c[0].y, cur.c[0].z, cur.c[0].w,
                                   cur.c[1].x, cur.c[1].y, cur.c[1].z, cur.c[1].w};
 #pragma unroll
@@ -234,11 +250,40 @@ prefix_kernel(const PrefixArgs a) {
           o[j] = make_uint4(lo.x, lo.y, hi.x, hi.y);
         }
       }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) cur.dst[j] = o[j];
     }
+    store_warp(gout + 4 * static_cast<int64_t>(ib), sbuf, lane, o, __ballot_sync(0xFFFFFFFFu, cur.ok));
     cur = nxt;
   }
+}
+
+// CTA (gx, kind = blockIdx.y, request b = blockIdx.z); item i of request b =
+// (row = (t, h), part): elements [64 part, 64 part + 64) of that row.
+template <int D, int FMT>
+__global__ void __launch_bounds__(kPrefixThreads, 4)
+prefix_kernel(const PrefixArgs a) {
+  constexpr int TPR = D / 64;                   // threads per row
+  constexpr int RB = D / 2, SB = D / 16;
+  __shared__ uint2 s_tab[FMT == KV4_NVFP4 ? 256 : 1];
+  __shared__ __align__(16) uint8_t s_out[(kPrefixThreads / 32) * 2048];   // per warp: 32 items' output
+  const int b = blockIdx.z;
+  const int kind = blockIdx.y;
+  const float s8 = __ldg(a.fp8_scale + kind);
+  if constexpr (FMT == KV4_NVFP4) {
+    s_tab[threadIdx.x] = nvfp4_scale_table(threadIdx.x, __ldg(a.gscale + kind), s8);
+    __syncthreads();
+  }
+  int n = a.prefix_lens[b];
+  const int cap = min(a.max_prefix_len, a.max_pages * a.P);
+  if (n < 0 || n > cap) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_error(a.err, KV4_EBOUNDS);
+    n = n < 0 ? 0 : cap;
+  }
+  const uint32_t items = static_cast<uint32_t>(n) * static_cast<uint32_t>(a.Hkv) * TPR;
+  const int64_t obase = a.cu_prefix[b];
+  const int32_t* table = a.block_table + static_cast<int64_t>(b) * a.max_pages;
+  uint8_t* out = kind == 0 ? a.out_k : a.out_v;
+  if (kind == 0) prefix_walk<D, FMT, 0>(a, items, obase, table, out, s8, s_tab, s_out);
+  else prefix_walk<D, FMT, 1>(a, items, obase, table, out, s8, s_tab, s_out);
 }
 
 template <int D, int FMT>
