@@ -236,6 +236,33 @@ __device__ __forceinline__ void staged16_neg(const WriteArgs& a, int kind, uint3
   }
 }
 
+// The 16 elements of one token already loaded (bf16: raw[0..1]; FP8: raw[0])
+// -> their negations in FP32, as staged16_neg computes them.
+__device__ __forceinline__ void raw16_neg(const WriteArgs& a, int kind, const uint4 (&raw)[2], float (&nx)[16]) {
+  if (a.k8 != nullptr) {
+    const float ns_in = -__ldg(a.in_scale + kind);
+    const uint64_t ns2 = f2(ns_in, ns_in);
+    const uint32_t w[4] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t hh[2];
+      e4m3x4_to_f16x2x2(w[i], hh[0], hh[1]);
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hh[k]));   // exact
+        f2_split(mul_f2(f2(f.x, f.y), ns2), nx[4 * i + 2 * k], nx[4 * i + 2 * k + 1]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) neg_bf16x2(w[k], nx[8 * u + 2 * k], nx[8 * u + 2 * k + 1]);
+    }
+  }
+}
+
 // Where token t goes: its chunk and offset, or nothing (slot < 0, or past
 // the pool, which is recorded).
 struct Dest {
@@ -264,7 +291,7 @@ __device__ __forceinline__ Dest dest_of(const WriteArgs& a, int64_t t, int64_t s
 // Encode unit u (K|V = kind) from the warp's stage `wst`; `live` false for a
 // thread past the last unit (it computes on whatever the stage holds and
 // stores nothing, so that whole rows of threads share the INT4 shuffles).
-template <int D, int FMT, int kind>
+template <int D, int FMT, int kind, bool direct = false>
 __device__ __forceinline__ void write_unit(const WriteArgs& a, uint32_t u, bool live, uint32_t wst, uint32_t lane,
                                            const float2* s_den, float g6, float r6) {
   constexpr int NB = D / 16;                      // threads per row
@@ -274,10 +301,42 @@ __device__ __forceinline__ void write_unit(const WriteArgs& a, uint32_t u, bool 
   const int64_t t0 = live ? n.t0 : a.T;           // past the end: no destination
   // token k's destination (taken after the arithmetic where that keeps
   // fewer registers live across it)
+  // direct: both tokens' input words and slots are loaded here, before any
+  // arithmetic, so that a small call pays one memory round trip
+  uint4 raw[2][2];
+  int64_t dslot[2] = {-1, -1};
+  if constexpr (direct) {
+    const int64_t row0 = n.t0 * a.Hkv + h;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int64_t e = ((n.t0 + k < a.T) ? row0 + k * a.Hkv : row0) * D + 16 * b;
+      if (a.k8 != nullptr) {
+        raw[k][0] = __ldg(reinterpret_cast<const uint4*>((kind == 0 ? a.k8 : a.v8) + e));
+      } else {
+        const uint4* src = reinterpret_cast<const uint4*>((kind == 0 ? a.k : a.v) + e);
+        raw[k][0] = __ldg(src);
+        raw[k][1] = __ldg(src + 1);
+      }
+      if (t0 + k < a.T) dslot[k] = __ldg(a.slot_mapping + t0 + k);
+    }
+  }
   auto dest = [&](int k) {
-    const uint2 sl = lds64(wst + kWarpData + 16 * lane + 8 * k);
-    const int64_t slot = static_cast<int64_t>((static_cast<uint64_t>(sl.y) << 32) | sl.x);
+    int64_t slot = -1;
+    if constexpr (direct) {
+      slot = dslot[k];
+    } else {
+      const uint2 sl = lds64(wst + kWarpData + 16 * lane + 8 * k);
+      slot = static_cast<int64_t>((static_cast<uint64_t>(sl.y) << 32) | sl.x);
+    }
     return dest_of(a, t0 + k, slot, h, b == 0);
+  };
+  // token k's 16 elements, negated, from the stage or (direct) from global memory
+  auto elems = [&](int k, float (&x)[16]) {
+    if constexpr (direct) {
+      raw16_neg(a, kind, raw[k], x);
+    } else {
+      staged16_neg(a, kind, wst, lane, k, x);
+    }
   };
 
   // each token's elements are read from the stage as their negations
@@ -287,7 +346,7 @@ __device__ __forceinline__ void write_unit(const WriteArgs& a, uint32_t u, bool 
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
       float x[16];
-      staged16_neg(a, kind, wst, lane, k, x);
+      elems(k, x);
       float amax = 0.f;
 #pragma unroll
       for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(x[j]));
@@ -346,7 +405,7 @@ __device__ __forceinline__ void write_unit(const WriteArgs& a, uint32_t u, bool 
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
       float x[16];
-      staged16_neg(a, kind, wst, lane, k, x);
+      elems(k, x);
       const Dest d = dest(k);
       float amax = 0.f;
 #pragma unroll
@@ -365,7 +424,7 @@ __device__ __forceinline__ void write_unit(const WriteArgs& a, uint32_t u, bool 
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
       float x[16];
-      staged16_neg(a, kind, wst, lane, k, x);
+      elems(k, x);
       const Dest d = dest(k);
       // row amax over the D/16 threads of the row (aligned groups of a warp)
       float amax = 0.f;
@@ -425,8 +484,11 @@ __device__ __forceinline__ void write_walk(const WriteArgs& a, uint8_t* s_stage,
 }
 
 // Persistent CTAs of kWriteThreads threads, kWriteCtasPerSm per SM, half on
-// K (blockIdx.y = 0) and half on V; each thread walks units a grid apart.
-template <int D, int FMT>
+// K (blockIdx.y = 0) and half on V; each warp walks units a grid apart.  A
+// call whose units fit one thread each (a decode step's new tokens) takes
+// the direct form instead: one unit a thread, loaded straight from global
+// memory, no staging (and no dynamic shared memory).
+template <int D, int FMT, bool direct>
 __global__ void __launch_bounds__(kWriteThreads, kWriteCtasPerSm)
 write_kernel(const WriteArgs a) {
   grid_dep_launch();   // a following decode launch may be scheduled early
@@ -444,13 +506,26 @@ write_kernel(const WriteArgs a) {
     s_den[threadIdx.x] = make_float2(den, __frcp_rn(den));
     __syncthreads();
   }
-  if (kind == 0) write_walk<D, FMT, 0>(a, s_stage, s_den, g6, r6);
-  else write_walk<D, FMT, 1>(a, s_stage, s_den, g6, r6);
+  if constexpr (direct) {
+    const uint32_t u = blockIdx.x * kWriteThreads + threadIdx.x;
+    const bool live = u < a.units;
+    if (kind == 0) write_unit<D, FMT, 0, true>(a, live ? u : 0u, live, 0u, 0u, s_den, g6, r6);
+    else write_unit<D, FMT, 1, true>(a, live ? u : 0u, live, 0u, 0u, s_den, g6, r6);
+  } else {
+    if (kind == 0) write_walk<D, FMT, 0>(a, s_stage, s_den, g6, r6);
+    else write_walk<D, FMT, 1>(a, s_stage, s_den, g6, r6);
+  }
 }
 
 template <int D, int FMT>
 static cudaError_t launch_write_t(const WriteArgs& a, cudaStream_t st) {
-  auto* k = write_kernel<D, FMT>;
+  const int64_t need = (static_cast<int64_t>(a.units) + kWriteThreads - 1) / kWriteThreads;
+  const int64_t resident = static_cast<int64_t>(a.sms) * kWriteCtasPerSm / 2;   // per K|V
+  if (need <= resident) {                       // one unit a thread
+    write_kernel<D, FMT, true><<<dim3(static_cast<unsigned>(need), 2), kWriteThreads, 0, st>>>(a);
+    return cudaGetLastError();
+  }
+  auto* k = write_kernel<D, FMT, false>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -459,10 +534,7 @@ static cudaError_t launch_write_t(const WriteArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  const int64_t need = (static_cast<int64_t>(a.units) + kWriteThreads - 1) / kWriteThreads;
-  const int64_t resident = static_cast<int64_t>(a.sms) * kWriteCtasPerSm / 2;   // per K|V
-  const int64_t blocks = need < resident ? need : (resident > 0 ? resident : 1);
-  k<<<dim3(static_cast<unsigned>(blocks), 2), kWriteThreads, kWriteSmem, st>>>(a);
+  k<<<dim3(static_cast<unsigned>(resident > 0 ? resident : 1), 2), kWriteThreads, kWriteSmem, st>>>(a);
   return cudaGetLastError();
 }
 
