@@ -139,3 +139,20 @@ def test_fp8_input_every_e4m3_code(fmt, s_in):
     got = pool.buffer.cpu().numpy()
     diff = np.nonzero(got != ref)[0]
     assert diff.size == 0, f"{fmt} s_in={s_in}: {diff.size} bytes differ, first at {diff[:8]}"
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "int4", "fp8"])
+def test_every_finite_bf16_through_the_streamed_write(bf16_rows, fmt):
+    """The same sweep three times over (12,240 tokens, 97,920 units of K and
+    of V): more units than one pass of the resident grid has threads, so the
+    write streams them through its shared-memory stages instead of taking
+    its one-unit-a-thread form (the smaller sweeps above)."""
+    k, v = bf16_rows
+    k3 = np.concatenate([k, v, k])
+    v3 = np.concatenate([v, k, v])
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert k3.shape[0] // 2 * (D // 16) > sms * 3 // 2 * 256      # units beyond one pass of the grid
+    g = {"nvfp4": np.array([scales(k3, "calibrated")] * 2, np.float32),
+         "int4": np.array([1.0, 1.0], np.float32),
+         "fp8": np.array([0.0173, 0.0291], np.float32)}[fmt]
+    run_write(fmt, k3, v3, g)
