@@ -11,8 +11,9 @@ than L2, so every step streams it from HBM.
 
 Printed: one JSON line on rank 0 with the metric (achieved HBM GB/s of the
 step's algorithmic bytes), the roofline of the decode kernel, an end-to-end
-figure through the public API with host buffers, the oracle timed on the
-host cores, clock samples, and per-workload lines for 160K, 1M, the INT4
+figure through the public API with host buffers (every step's inputs
+copied in and its output copied back, on copy streams that overlap the
+kernels of the neighbouring steps), the oracle timed on the host cores, clock samples, and per-workload lines for 160K, 1M, the INT4
 lane and the prefix dequant under "workloads".
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kv4|reference]
@@ -506,44 +507,77 @@ def kv4_arm(args):
 
     # ---- end to end through the public API, host buffers ----------------
     # The step's inputs (q, the new K/V, their slots, the lengths) sit in one
-    # pinned host staging buffer and go over in one copy per step into one
+    # pinned host staging buffer and go over in one copy per step into a
     # device buffer, of which the library's arguments are views (each part
-    # 256-byte aligned).
+    # 256-byte aligned); the step's output comes back into pinned host memory.
+    # The copies run on their own streams, as a serving loop would run them:
+    # step k+1's inputs go over while step k computes, step k's output comes
+    # back while step k+1 computes (two device input buffers and two outputs,
+    # each reused only after the copy or the kernels that used it are done).
     parts = [s.q, s.k_new, s.v_new, s.slot_new, s.d_lens]
     offs, at = [], 0
     for t in parts:
         offs.append(at)
         at += (t.numel() * t.element_size() + 255) // 256 * 256
     h_in = torch.empty(at, dtype=torch.uint8).pin_memory()
-    d_in = torch.empty(at, dtype=torch.uint8, device=device)
-    views = []
+    d_in = [torch.empty(at, dtype=torch.uint8, device=device) for _ in range(2)]
+    views = [[], []]
     for t, o in zip(parts, offs):
         n = t.numel() * t.element_size()
         h_in[o:o + n].copy_(t.contiguous().view(torch.uint8).reshape(-1).cpu())
-        views.append(d_in[o:o + n].view(t.dtype).view(t.shape))
-    d_q, d_k, d_v, d_slot, d_lens = views
-    h_out = torch.empty((B, Hq, D), dtype=torch.float32).pin_memory()
+        for j in range(2):
+            views[j].append(d_in[j][o:o + n].view(t.dtype).view(t.shape))
+    d_out = [torch.empty_like(s.out) for _ in range(2)]
+    h_out = [torch.empty((B, Hq, D), dtype=torch.float32).pin_memory() for _ in range(2)]
     h2d = h_in.numel()                       # the staging buffer, alignment padding included
-    d2h = h_out.numel() * h_out.element_size()
+    d2h = h_out[0].numel() * h_out[0].element_size()
+    main = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        d_in.copy_(h_in, non_blocking=True)
-        K.kv4_write(d_k, d_v, d_slot, s.pool, s.g)
-        K.kv4_decode_attention(d_q, s.pool, s.g, s.d_table, d_lens, s.sm, s.out,
-                               num_splits=s.splits, workspace=s.ws)
-        h_out.copy_(s.out, non_blocking=True)
+    def e2e_step(k):
+        j = k % 2
+        d_q, d_k, d_v, d_slot, d_lens = views[j]
+        if k >= 2:
+            s_in.wait_event(ev_done[j])          # step k-2's kernels are done with d_in[j]
+        with torch.cuda.stream(s_in):
+            d_in[j].copy_(h_in, non_blocking=True)
+        ev_in[j].record(s_in)
+        main.wait_event(ev_in[j])
+        if k >= 2:
+            main.wait_event(ev_out[j])           # step k-2's output has left d_out[j]
+        K.kv4_write(d_k, d_v, d_slot, s.pool, s.g, stream=main)
+        K.kv4_decode_attention(d_q, s.pool, s.g, s.d_table, d_lens, s.sm, d_out[j],
+                               num_splits=s.splits, workspace=s.ws, stream=main)
+        ev_done[j].record(main)
+        s_out.wait_event(ev_done[j])
+        with torch.cuda.stream(s_out):
+            h_out[j].copy_(d_out[j], non_blocking=True)
+        ev_out[j].record(s_out)
 
-    for _ in range(args.warmup):
-        e2e_step()
+    def e2e_run(n):
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(main)
+        s_in.wait_event(start)
+        s_out.wait_event(start)
+        for k in range(n):
+            e2e_step(k)
+        main.wait_stream(s_in)
+        main.wait_stream(s_out)                  # the last output is back
+        end.record(main)
+        return start, end
+
+    e2e_run(args.warmup)
     torch.cuda.synchronize()
     barrier(pg, device)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record()
+    e0, e1 = e2e_run(args.steps)
     torch.cuda.synchronize()
+    # the output read back is the decode of the same inputs over the same pool
+    if not torch.equal(h_out[(args.steps - 1) % 2], s.out.cpu()):
+        raise SystemExit("the end-to-end output differs from the device-timed decode of the same inputs")
     e2e_total = max_over_ranks(pg, e0.elapsed_time(e1) * 1e-3, device)
     e2e_value = step_bytes * world / (e2e_total / args.steps) / 1e9
 
