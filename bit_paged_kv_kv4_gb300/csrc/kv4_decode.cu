@@ -761,9 +761,13 @@ combine_kernel(const DecodeArgs a) {
   const int n_u = (L + a.tile - 1) / a.tile;
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
+  // column block z of gridDim.z: float4 columns [c_lo, c_lo + cols) of the row
+  // (k8v4 rotates the whole row, so it runs one block)
+  const int cols = D / 4 / static_cast<int>(gridDim.z);
+  const int c_lo = static_cast<int>(blockIdx.z) * cols;
   if (n_u == 0) {
-    for (int d = tid * 4; d < D; d += kCombineThreads * 4)
-      store_out4(a.out, a.out_f32, row * D + d, make_float4(0.f, 0.f, 0.f, 0.f));
+    for (int c = tid; c < cols; c += kCombineThreads)
+      store_out4(a.out, a.out_f32, row * D + 4 * (c_lo + c), make_float4(0.f, 0.f, 0.f, 0.f));
     return;
   }
   const int64_t T = a.cum[a.B];
@@ -849,14 +853,25 @@ combine_kernel(const DecodeArgs a) {
   const float l = block_sum(lp, s_f);      // its barriers also publish s_w
 
   // ---- weighted sum of the pieces' o: thread = (piece group, 4 columns) --------
-  const int cols = D / 4;                        // float4 columns
+  // pieces grp, grp + groups, ... in that order, four loads in flight at a time
   const int groups = kCombineThreads / cols;     // pieces handled side by side
   const int col = tid % cols, grp = tid / cols;
+  const float4* po = reinterpret_cast<const float4*>(a.part_o) + c_lo + col;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int p = grp; p < P; p += groups) {
-    const int64_t slot = slot_of(p);
+  int p = grp;
+  for (; p + 3 * groups < P; p += 4 * groups) {
+    float4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) v[k] = __ldg(po + (slot_of(p + k * groups) * 8 + g) * (D / 4));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float w = s_w[p + k * groups];
+      acc.x += w * v[k].x; acc.y += w * v[k].y; acc.z += w * v[k].z; acc.w += w * v[k].w;
+    }
+  }
+  for (; p < P; p += groups) {
     const float w = s_w[p];
-    const float4 v = __ldg(reinterpret_cast<const float4*>(a.part_o + (slot * 8 + g) * D) + col);
+    const float4 v = __ldg(po + (slot_of(p) * 8 + g) * (D / 4));
     acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
   }
   s_o[tid] = acc;
@@ -874,7 +889,7 @@ combine_kernel(const DecodeArgs a) {
     res = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
   }
   if (a.fmt != KV4_K8V4) {
-    if (grp == 0) store_out4(a.out, a.out_f32, row * D + 4 * col, res);
+    if (grp == 0) store_out4(a.out, a.out_f32, row * D + 4 * (c_lo + col), res);
     return;
   }
   // k8v4: the pieces hold sum p V_rot; o = H o_rot with H = S_D / sqrt(D), the
@@ -953,7 +968,21 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& map, const CUt
     e = launch_decode4(a, map, smap, st);
   }
   if (e != cudaSuccess || a.unit_ctas) return e;
-  return launch_pdl(combine_kernel, dim3(a.Hq, a.B), dim3(kCombineThreads), 0, st, a);
+  // Few output rows (a small batch at long context, each row merging many
+  // pieces): split the rows into column blocks of 64 floats, up to about two
+  // CTAs per SM; many rows: one CTA a row.  (k8v4 rotates whole rows.)
+  static int sms[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 64) dev = 63;
+  if (sms[dev] == 0 && cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms[dev] = 152;
+  const int64_t rows = static_cast<int64_t>(a.Hq) * a.B;
+  const int64_t want = (2 * static_cast<int64_t>(sms[dev]) + rows - 1) / rows;
+  int64_t cz = 1;                               // a power of two that divides D / 64
+  while (2 * cz <= want && 2 * cz <= a.D / 64) cz *= 2;
+  if (a.fmt == KV4_K8V4) cz = 1;
+  return launch_pdl(combine_kernel, dim3(a.Hq, a.B, static_cast<unsigned>(cz)), dim3(kCombineThreads), 0, st, a);
 }
 
 }  // namespace kv4
