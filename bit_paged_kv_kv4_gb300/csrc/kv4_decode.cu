@@ -822,6 +822,18 @@ combine_kernel(const DecodeArgs a) {
   if (!contiguous && npieces > kMaxPieces && tid == 0) set_error(a.err, KV4_EUNSUPPORTED);
   auto slot_of = [&](int p) -> int64_t { return contiguous ? c0 + p + u : s_slot[p]; };
 
+  // the thread's first four partial outputs (pieces grp, grp + groups, ...)
+  // do not depend on the weights: their loads go out before the reductions
+  const int groups = kCombineThreads / cols;     // pieces handled side by side
+  const int col = tid % cols, grp = tid / cols;
+  const float4* po = reinterpret_cast<const float4*>(a.part_o) + c_lo + col;
+  float4 first[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int p = grp + k * groups;
+    first[k] = p < P ? __ldg(po + (slot_of(p) * 8 + g) * (D / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+
   // ---- the piece states, read once: maxima, normaliser l, weights ------------
   // Thread t holds pieces t, t + kCombineThreads, ... (at most kPPT of them);
   // each piece's O weight 2^(m_y,p - My) goes to shared memory for the sum.
@@ -854,11 +866,16 @@ combine_kernel(const DecodeArgs a) {
 
   // ---- weighted sum of the pieces' o: thread = (piece group, 4 columns) --------
   // pieces grp, grp + groups, ... in that order, four loads in flight at a time
-  const int groups = kCombineThreads / cols;     // pieces handled side by side
-  const int col = tid % cols, grp = tid / cols;
-  const float4* po = reinterpret_cast<const float4*>(a.part_o) + c_lo + col;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  int p = grp;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int p = grp + k * groups;
+    if (p < P) {
+      const float w = s_w[p];
+      acc.x += w * first[k].x; acc.y += w * first[k].y; acc.z += w * first[k].z; acc.w += w * first[k].w;
+    }
+  }
+  int p = grp + 4 * groups;
   for (; p + 3 * groups < P; p += 4 * groups) {
     float4 v[4];
 #pragma unroll
