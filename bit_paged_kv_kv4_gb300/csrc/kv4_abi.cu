@@ -532,7 +532,24 @@ kv4_status kv4_dequant_prefix(const kv4_pool* pool, const float* layer_global_sc
   a.err = error_word();
   if (a.err == nullptr) return fail(KV4_ECUDA, "no CUDA device / error word unavailable");
   a.sms = sm_count();
-  cudaError_t e = kv4::launch_prefix(a, static_cast<cudaStream_t>(stream));
+  // the workspaces as 2-D byte tensors of 128-byte rows for the kernel's
+  // tensor stores; the extent is not the buffers' (the offsets come from the
+  // device array cu_prefix): the kernel stores only the rows of its items
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return fail(KV4_ECUDA, "cuTensorMapEncodeTiled is not available");
+  CUtensorMap maps[2];
+  for (int i = 0; i < 2; ++i) {
+    cuuint64_t dims[2] = {128, cuuint64_t{1} << 31};
+    cuuint64_t strides[1] = {128};
+    cuuint32_t box[2] = {128, 16};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(&maps[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, i == 0 ? fp8_k : fp8_v, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+      return fail(KV4_ECUDA, "cuTensorMapEncodeTiled (prefix workspace) failed (%d)", static_cast<int>(r));
+  }
+  cudaError_t e = kv4::launch_prefix(a, maps[0], maps[1], static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KV4_OK : cuda_fail(e, "kv4_dequant_prefix launch");
 }
 

@@ -102,7 +102,9 @@ struct PrefixArgs {
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& map, const CUtensorMap& smap,
                           cudaStream_t st);
 cudaError_t launch_write(const WriteArgs& a, cudaStream_t st);
-cudaError_t launch_prefix(const PrefixArgs& a, cudaStream_t st);
+// mk / mv: the K / V workspaces as 2-D byte tensors of 128-byte rows (boxes of
+// 128 bytes x 16 rows, 128-byte swizzle) for the kernel's tensor stores.
+cudaError_t launch_prefix(const PrefixArgs& a, const CUtensorMap& mk, const CUtensorMap& mv, cudaStream_t st);
 
 struct CalibArgs {
   const __nv_bfloat16* k;       // [n] elements (T * Hkv * D)

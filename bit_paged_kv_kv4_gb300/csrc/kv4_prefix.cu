@@ -111,16 +111,22 @@ __device__ __forceinline__ uint2 int4_word(uint2 tp, uint2 tn, uint32_t w) {
 }
 
 // A warp's 32 items are 32 consecutive 64-byte pieces of the output.  Each
-// lane puts its 64 bytes (chunks L = 4 lane + j of 16 bytes) in the warp's
-// 2 KB of shared memory, chunk L at row L / 8, column (L % 8) ^ (row % 8),
-// which keeps both these writes and the reads below free of bank conflicts;
-// then lane l stores linear chunks 32 m + l (m = 0..3), so each store
-// instruction writes 512 contiguous bytes.  `valid` holds bit k for each
-// item k of the 32 that is to be written.
+// lane puts its 64 bytes (chunks L = 4 lane + j of 16 bytes) in one of the
+// warp's two 2 KB buffers, chunk L at row L / 8, column (L % 8) ^ (row % 8)
+// of 128-byte rows: the 128-byte swizzle of the tensor copy unit, and free of
+// bank conflicts both ways.  Then one lane stores the 2 KB with a tensor copy
+// through `tmap` (the output viewed as 128-byte rows, row `y`), or, for a step
+// with items to skip or a start off a 128-byte boundary, lane l stores
+// linear chunks 32 m + l (m = 0..3) itself, 512 contiguous bytes an
+// instruction.  `valid` holds bit k for each item k of the 32 to be written.
+// Every step commits one bulk group; a buffer is refilled only after the
+// group that read it two steps before has finished reading.
 __device__ __forceinline__ uint32_t tchunk(uint32_t L) { return L ^ ((L >> 3) & 7u); }
 
 __device__ __forceinline__ void store_warp(uint4* gdst, uint32_t sbuf, uint32_t lane, const uint4 (&o)[4],
-                                           uint32_t valid) {
+                                           uint32_t valid, const CUtensorMap* tmap, int64_t y) {
+  if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+  __syncwarp();
   if (valid >> lane & 1u) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -130,19 +136,28 @@ __device__ __forceinline__ void store_warp(uint4* gdst, uint32_t sbuf, uint32_t 
                    : "memory");
     }
   }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // visible to the tensor copy
   __syncwarp();
+  if (valid == 0xFFFFFFFFu && y >= 0) {
+    if (lane == 0)
+      asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+                   ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(0), "r"(static_cast<int>(y)), "r"(sbuf)
+                   : "memory");
+  } else {
 #pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    const uint32_t L = 32 * m + lane;
-    if (valid >> (L >> 2) & 1u) gdst[L] = lds128(sbuf + 16 * tchunk(L));
+    for (int m = 0; m < 4; ++m) {
+      const uint32_t L = 32 * m + lane;
+      if (valid >> (L >> 2) & 1u) gdst[L] = lds128(sbuf + 16 * tchunk(L));
+    }
   }
-  __syncwarp();                                   // the buffer is free for the next step
+  if (lane == 0) asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
 // The walk of one (kind, request) CTA over its items (kind K|V = 0|1).
 template <int D, int FMT, int kind>
 __device__ __forceinline__ void prefix_walk(const PrefixArgs& a, uint32_t items, int64_t obase, const int32_t* table,
-                                            uint8_t* out, float s8, const uint2* s_tab, uint8_t* s_out) {
+                                            uint8_t* out, float s8, const uint2* s_tab, uint8_t* s_out,
+                                            const CUtensorMap* tmap) {
   constexpr int TPR = D / 64;                   // threads per row
   constexpr int RB = D / 2, SB = D / 16;
   constexpr bool VP = FMT == KV4_NVFP4 && kind == 1;   // NVFP4 V: token-pair rows
@@ -199,8 +214,13 @@ __device__ __forceinline__ void prefix_walk(const PrefixArgs& a, uint32_t items,
 
   const uint32_t stride = gridDim.x * kPrefixThreads;
   const uint32_t lane = threadIdx.x & 31u;
-  const uint32_t sbuf = smem_u32(s_out) + (threadIdx.x >> 5) * 2048u;
+  const uint32_t sbuf0 = smem_u32(s_out) + (threadIdx.x >> 5) * 4096u;   // the warp's two buffers
   uint4* gout = reinterpret_cast<uint4*>(out + obase * a.Hkv * D);
+  // the request's first output byte in 128-byte rows of the tensor view, or
+  // -1 when it is off a row boundary (then every step stores from the lanes)
+  const int64_t obyte = obase * a.Hkv * D;
+  const int64_t yrow = (obyte % 128 == 0) ? obyte / 128 : -1;
+  uint32_t buf = 0;
   Item cur, nxt;
   // warp-uniform walk: the warp's items are ib + lane
   uint32_t ib = blockIdx.x * kPrefixThreads + (threadIdx.x & ~31u);
@@ -251,20 +271,24 @@ __device__ __forceinline__ void prefix_walk(const PrefixArgs& a, uint32_t items,
         }
       }
     }
-    store_warp(gout + 4 * static_cast<int64_t>(ib), sbuf, lane, o, __ballot_sync(0xFFFFFFFFu, cur.ok));
+    const int64_t y = yrow < 0 ? -1 : yrow + static_cast<int64_t>(ib) / 2;     // 64 ib bytes = ib / 2 rows
+    store_warp(gout + 4 * static_cast<int64_t>(ib), sbuf0 + 2048u * buf, lane, o, __ballot_sync(0xFFFFFFFFu, cur.ok),
+               tmap, y < (int64_t{1} << 31) - 16 ? y : -1);
+    buf ^= 1u;
     cur = nxt;
   }
+  if ((threadIdx.x & 31u) == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // CTA (gx, kind = blockIdx.y, request b = blockIdx.z); item i of request b =
 // (row = (t, h), part): elements [64 part, 64 part + 64) of that row.
 template <int D, int FMT>
-__global__ void __launch_bounds__(kPrefixThreads, 4)
-prefix_kernel(const PrefixArgs a) {
+__global__ void __launch_bounds__(kPrefixThreads, 3)
+prefix_kernel(const PrefixArgs a, const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v) {
   constexpr int TPR = D / 64;                   // threads per row
   constexpr int RB = D / 2, SB = D / 16;
   __shared__ uint2 s_tab[FMT == KV4_NVFP4 ? 256 : 1];
-  __shared__ __align__(16) uint8_t s_out[(kPrefixThreads / 32) * 2048];   // per warp: 32 items' output
+  __shared__ __align__(1024) uint8_t s_out[(kPrefixThreads / 32) * 4096];   // per warp: two 2 KB buffers
   const int b = blockIdx.z;
   const int kind = blockIdx.y;
   const float s8 = __ldg(a.fp8_scale + kind);
@@ -282,12 +306,12 @@ prefix_kernel(const PrefixArgs a) {
   const int64_t obase = a.cu_prefix[b];
   const int32_t* table = a.block_table + static_cast<int64_t>(b) * a.max_pages;
   uint8_t* out = kind == 0 ? a.out_k : a.out_v;
-  if (kind == 0) prefix_walk<D, FMT, 0>(a, items, obase, table, out, s8, s_tab, s_out);
-  else prefix_walk<D, FMT, 1>(a, items, obase, table, out, s8, s_tab, s_out);
+  if (kind == 0) prefix_walk<D, FMT, 0>(a, items, obase, table, out, s8, s_tab, s_out, &map_k);
+  else prefix_walk<D, FMT, 1>(a, items, obase, table, out, s8, s_tab, s_out, &map_v);
 }
 
 template <int D, int FMT>
-static cudaError_t launch_prefix_t(const PrefixArgs& a, cudaStream_t st) {
+static cudaError_t launch_prefix_t(const PrefixArgs& a, const CUtensorMap& mk, const CUtensorMap& mv, cudaStream_t st) {
   const int64_t items = static_cast<int64_t>(a.max_prefix_len) * a.Hkv * (D / 64);
   const int64_t need = (items + kPrefixThreads - 1) / kPrefixThreads;
   // one wave of resident CTAs over all (kind, request) pairs; each strides
@@ -302,26 +326,26 @@ static cudaError_t launch_prefix_t(const PrefixArgs& a, cudaStream_t st) {
   }
   const int64_t target = (static_cast<int64_t>(a.sms) * per_sm + 2 * a.B - 1) / (2 * a.B);
   const int64_t gx = need < target ? need : (target > 0 ? target : 1);
-  prefix_kernel<D, FMT><<<dim3(static_cast<unsigned>(gx), 2, a.B), kPrefixThreads, 0, st>>>(a);
+  prefix_kernel<D, FMT><<<dim3(static_cast<unsigned>(gx), 2, a.B), kPrefixThreads, 0, st>>>(a, mk, mv);
   return cudaGetLastError();
 }
 
-cudaError_t launch_prefix(const PrefixArgs& a_in, cudaStream_t st) {
+cudaError_t launch_prefix(const PrefixArgs& a_in, const CUtensorMap& mk, const CUtensorMap& mv, cudaStream_t st) {
   if (a_in.max_prefix_len == 0 || a_in.B == 0) return cudaSuccess;
   PrefixArgs a = a_in;
   a.hkv_div = make_fastdiv(static_cast<uint32_t>(a.Hkv));
   a.p_div = make_fastdiv(static_cast<uint32_t>(a.P));
   if (a.fmt == KV4_NVFP4) {
     switch (a.D) {
-      case 64: return launch_prefix_t<64, KV4_NVFP4>(a, st);
-      case 128: return launch_prefix_t<128, KV4_NVFP4>(a, st);
-      default: return launch_prefix_t<256, KV4_NVFP4>(a, st);
+      case 64: return launch_prefix_t<64, KV4_NVFP4>(a, mk, mv, st);
+      case 128: return launch_prefix_t<128, KV4_NVFP4>(a, mk, mv, st);
+      default: return launch_prefix_t<256, KV4_NVFP4>(a, mk, mv, st);
     }
   }
   switch (a.D) {
-    case 64: return launch_prefix_t<64, KV4_INT4_PTH>(a, st);
-    case 128: return launch_prefix_t<128, KV4_INT4_PTH>(a, st);
-    default: return launch_prefix_t<256, KV4_INT4_PTH>(a, st);
+    case 64: return launch_prefix_t<64, KV4_INT4_PTH>(a, mk, mv, st);
+    case 128: return launch_prefix_t<128, KV4_INT4_PTH>(a, mk, mv, st);
+    default: return launch_prefix_t<256, KV4_INT4_PTH>(a, mk, mv, st);
   }
 }
 
