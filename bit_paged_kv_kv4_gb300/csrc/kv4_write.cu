@@ -492,6 +492,7 @@ template <int D, int FMT, bool direct>
 __global__ void __launch_bounds__(kWriteThreads, kWriteCtasPerSm)
 write_kernel(const WriteArgs a) {
   grid_dep_launch();   // a following decode launch may be scheduled early
+  grid_dep_wait();     // launched early itself: inputs of the previous kernel are visible from here
   const int kind = blockIdx.y;                    // 0: K, 1: V
   extern __shared__ __align__(16) uint8_t s_stage[];
   // NVFP4: (denominator, its reciprocal) of every E4M3 block-scale byte S:
@@ -517,14 +518,30 @@ write_kernel(const WriteArgs a) {
   }
 }
 
+// Launched with programmatic stream serialisation: the kernel may be
+// scheduled while the previous kernel on the stream drains, and reads
+// nothing before its grid_dep_wait().
+template <typename K>
+static cudaError_t launch_pdl_write(K* k, dim3 grid, size_t smem, cudaStream_t st, const WriteArgs& a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kWriteThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, a);
+}
+
 template <int D, int FMT>
 static cudaError_t launch_write_t(const WriteArgs& a, cudaStream_t st) {
   const int64_t need = (static_cast<int64_t>(a.units) + kWriteThreads - 1) / kWriteThreads;
   const int64_t resident = static_cast<int64_t>(a.sms) * kWriteCtasPerSm / 2;   // per K|V
-  if (need <= resident) {                       // one unit a thread
-    write_kernel<D, FMT, true><<<dim3(static_cast<unsigned>(need), 2), kWriteThreads, 0, st>>>(a);
-    return cudaGetLastError();
-  }
+  if (need <= resident)                         // one unit a thread
+    return launch_pdl_write(write_kernel<D, FMT, true>, dim3(static_cast<unsigned>(need), 2), 0, st, a);
   auto* k = write_kernel<D, FMT, false>;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -534,8 +551,7 @@ static cudaError_t launch_write_t(const WriteArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  k<<<dim3(static_cast<unsigned>(resident > 0 ? resident : 1), 2), kWriteThreads, kWriteSmem, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl_write(k, dim3(static_cast<unsigned>(resident > 0 ? resident : 1), 2), kWriteSmem, st, a);
 }
 
 cudaError_t launch_write(const WriteArgs& a_in, cudaStream_t st) {
