@@ -986,8 +986,9 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& map, const CUt
   }
   if (e != cudaSuccess || a.unit_ctas) return e;
   // Few output rows (a small batch at long context, each row merging many
-  // pieces): split the rows into column blocks of 64 floats, up to about two
-  // CTAs per SM; many rows: one CTA a row.  (k8v4 rotates whole rows.)
+  // pieces): split the rows into column blocks of 32 floats or more, up to
+  // about two CTAs per SM; many rows: one CTA a row.  (k8v4 rotates whole
+  // rows.)
   static int sms[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -996,8 +997,8 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& map, const CUt
     sms[dev] = 152;
   const int64_t rows = static_cast<int64_t>(a.Hq) * a.B;
   const int64_t want = (2 * static_cast<int64_t>(sms[dev]) + rows - 1) / rows;
-  int64_t cz = 1;                               // a power of two that divides D / 64
-  while (2 * cz <= want && 2 * cz <= a.D / 64) cz *= 2;
+  int64_t cz = 1;                               // a power of two that divides D / 32
+  while (2 * cz <= want && 2 * cz <= a.D / 32) cz *= 2;
   if (a.fmt == KV4_K8V4) cz = 1;
   return launch_pdl(combine_kernel, dim3(a.Hq, a.B, static_cast<unsigned>(cz)), dim3(kCombineThreads), 0, st, a);
 }
