@@ -643,6 +643,7 @@ def kv4_arm(args):
         extra["k8v4_32k"] = time_k8v4(device, W.ALL["nvfp4_32k"], peak)
         extra["k8v4_32k"]["traffic"] = recorded_traffic("k8v4_32k")
         extra["k8v4_32k"]["ncu_dram_gbs"] = recorded_ncu_gbs("k8v4_32k")
+        extra["k8v4_write_128k"] = time_k8v4_write(device, peak)
         torch.cuda.empty_cache()
         line["workloads"] = extra
 
@@ -804,6 +805,37 @@ def time_k8v4(device, w, peak, reps=20):
             "num_chunks": chunks, "kv_bytes": byts, "tokens_per_s_16_layers": B / (16 * med)}
 
 
+def time_k8v4_write(device, peak, T=131072, Hkv=4, D=256, P=64):
+    """Prefill write of T bf16 tokens into a k8v4 pool (Hadamard rotation,
+    FP8 keys, INT4 values): CUDA-event median of 10 calls after 3 warm-up
+    calls; bytes = bf16 K and V in + the pool rows out + the slots."""
+    import torch
+    import bit_paged_kv_kv4_gb300 as K
+    gen = torch.Generator(device=device).manual_seed(11)
+    k = torch.randn((T, Hkv, D), generator=gen, device=device).to(torch.bfloat16)
+    v = torch.randn((T, Hkv, D), generator=gen, device=device).to(torch.bfloat16)
+    pool = K.Pool("k8v4", (T + P - 1) // P, P, Hkv, D, device=device)
+    slots = torch.arange(T, dtype=torch.int64, device=device)
+    s_k = torch.tensor([W.fp8_scale_from_amax(float(k.abs().amax().float()))], dtype=torch.float32, device=device)
+    for _ in range(3):
+        K.kv4_k8v4_write(k, v, slots, pool, s_k)
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(10):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        K.kv4_k8v4_write(k, v, slots, pool, s_k)
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b) * 1e-3)
+    if K.kv4_device_error() != 0:
+        raise RuntimeError("k8v4 write flagged a device error")
+    med = statistics.median(ts)
+    byts = T * Hkv * (2 * D * 2 + D + D // 2 + 4) + T * 8
+    return {"tokens": T, "us": med * 1e6, "gbs": byts / med / 1e9, "frac": byts / med / 1e9 / peak,
+            "note": f"{T * Hkv * D * 4 / 1e6:.0f} MB in, {T * Hkv * (D + D // 2 + 4) / 1e6:.1f} MB out: larger than L2"}
+
+
 def time_write_int4(device, peak, T=8192):
     """Prefill write of T bf16 tokens into an INT4 per-token-head pool with the
     shapes of the 220K INT4 workload (Hkv 2, D 256, 1600-token pages)."""
@@ -947,6 +979,7 @@ def only_arm(args):
         r = time_prefix(Setup(w, device), w, peak)
     elif args.only == "k8v4":
         r = time_k8v4(device, W.ALL["nvfp4_32k"], peak)
+        r["write_128k"] = time_k8v4_write(device, peak)
     elif args.only == "extend":
         r, ws = time_prefix(Setup(w, device), w, peak, keep=True)
         r = time_extend(device, w, ws, read_tensor_peak()[0], reps=args.steps)

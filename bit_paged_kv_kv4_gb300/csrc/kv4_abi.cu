@@ -652,7 +652,7 @@ kv4_status kv4_k8v4_write(const void* k, const void* v, const int64_t* slot_mapp
     return fail(KV4_EINVAL, "k, v, slot_mapping and key_scale must be non-NULL");
   if (!aligned(k, 16) || !aligned(v, 16) || !aligned(slot_mapping, 8) || !aligned(key_scale, 4))
     return fail(KV4_EINVAL, "k and v must be 16-byte aligned, slot_mapping 8-byte aligned");
-  if (num_tokens * pool->num_kv_heads >= (int64_t{1} << 34))
+  if (num_tokens * pool->num_kv_heads >= (int64_t{1} << 31))   // 32-bit row indices
     return fail(KV4_EINVAL, "num_tokens too large");
   kv4::K8V4WriteArgs a{};
   a.k = static_cast<const __nv_bfloat16*>(k);

@@ -154,6 +154,7 @@ struct K8V4WriteArgs {
   int P, Hkv, num_pages, D;
   const float* s_k;             // [1] FP8 key scale
   int* err;
+  FastDiv hkv_div, p_div;       // by Hkv, by P (set by the launch)
 };
 cudaError_t launch_k8v4_write(const K8V4WriteArgs& a, cudaStream_t st);
 int decode_tile_tokens(int fmt);

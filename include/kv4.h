@@ -341,6 +341,7 @@ kv4_status kv4_decode_attention_static_ws(const void* q, const kv4_pool* pool,
  * kv4_k8v4_write -- rotate and quantise T tokens of bf16 K/V
  *   ([T][Hkv][D], 16-byte aligned) into the pool at slot_mapping (int64
  *   [T], 8-byte aligned; < 0 skipped; beyond the pool flagged KV4_EBOUNDS).
+ *   T * Hkv must be below 2^31 (else KV4_EINVAL).
  *
  * kv4_k8v4_decode_attention -- one decode step: q_rot = H q (bf16 q
  *   [B][Hq][D]), softmax(sm_scale * q_rot . K_hat_rot) over the request's
