@@ -4,12 +4,12 @@
 // rotation of size D).  H = S_D / sqrt(D) (Sylvester), symmetric and
 // orthogonal.
 //
-// Write (k8v4_write_kernel): one warp per (token, head) row of K or V.  The
-// row is rotated in FP32 by the fast Walsh-Hadamard transform, stages
+// Write (k8v4_write_kernel): D/32 lanes per (token, head) row of K or V.
+// The row is rotated in FP32 by the fast Walsh-Hadamard transform, stages
 // len = 1, 2, ..., D/2 replacing (x_i, x_{i+len}) by (x_i + x_{i+len},
 // x_i - x_{i+len}) (i with bit len clear), then scaled by float32(1/sqrt D);
-// a lane holds D/32 consecutive elements, so stages below D/32 stay in the
-// lane and the others pair lanes by shuffle.  Keys: E4M3(k_rot / s_K) (one
+// a lane holds 32 consecutive elements, so stages below 32 stay in the lane
+// and the others pair the row's lanes by shuffle.  Keys: E4M3(k_rot / s_K) (one
 // per-tensor FP32 scale); values: INT4 per row, s = amax / 7,
 // code = clamp(rne(v_rot / s), -8, 7).  IEEE FP32 throughout, so the bytes
 // match the test oracle's; the divisions take Markstein's correction step
@@ -37,28 +37,42 @@ __device__ __forceinline__ float inv_sqrt_d() {
 }
 
 // ---------------------------------------------------------------- write
+// A row of D elements is held by LPR = D / 32 consecutive lanes, 32
+// consecutive elements a lane (a warp holds 32 / LPR rows), so stages
+// len = 1 .. 16 of the transform stay in the lane and len = 32 .. D/2 pair
+// lanes of the row by shuffle.
 template <int D>
 __global__ void __launch_bounds__(256) k8v4_write_kernel(const K8V4WriteArgs a) {
-  constexpr int E = D / 32;                               // elements per lane
-  const int lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  constexpr int E = 32;                                   // elements per lane
+  constexpr int LPR = D / E;                              // lanes per row
+  constexpr int RPW = 32 / LPR;                           // rows per warp
+  const int lane = threadIdx.x & 31, rl = lane % LPR;     // the lane's place in its row
+  const int64_t row = (static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * RPW + lane / LPR;
   const int kind = blockIdx.y;                            // 0: K, 1: V
-  if (row >= a.rows) return;                              // whole warp
+  // rows past the end compute on row 0 and store nothing (lanes of a row
+  // share the shuffles below, and rows of a warp share the warp)
+  const bool live = row < a.rows;
+  const int64_t r0 = live ? row : 0;
   // rows < 2^31 (host check): 32-bit multiply-high division by Hkv
-  const uint32_t t32 = fdiv(static_cast<uint32_t>(row), a.hkv_div);
+  const uint32_t t32 = fdiv(static_cast<uint32_t>(r0), a.hkv_div);
   const int64_t t = t32;
-  const int h = static_cast<int>(static_cast<uint32_t>(row) - t32 * static_cast<uint32_t>(a.Hkv));
+  const int h = static_cast<int>(static_cast<uint32_t>(r0) - t32 * static_cast<uint32_t>(a.Hkv));
+  const int64_t slot = live ? a.slot_mapping[t] : -1;     // issued early; used at the store
 
   // E consecutive bf16 -> FP32
-  const __nv_bfloat16* src = (kind == 0 ? a.k : a.v) + row * D + lane * E;
+  const uint4* src = reinterpret_cast<const uint4*>((kind == 0 ? a.k : a.v) + r0 * D + rl * E);
   float x[E];
 #pragma unroll
-  for (int i = 0; i < E; i += 2) {
-    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(src + i));
-    x[i] = f.x;
-    x[i + 1] = f.y;
+  for (int u = 0; u < E / 8; ++u) {
+    const uint4 w = __ldg(src + u);
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x[8 * u + 2 * j] = __uint_as_float(ww[j] << 16);        // bf16 -> FP32 is exact
+      x[8 * u + 2 * j + 1] = __uint_as_float(ww[j] & 0xFFFF0000u);
+    }
   }
-  // FWHT, stages len = 1 .. D/2
+  // FWHT, stages len = 1 .. D/2 in order
 #pragma unroll
   for (int len = 1; len < E; len <<= 1) {
 #pragma unroll
@@ -71,28 +85,18 @@ __global__ void __launch_bounds__(256) k8v4_write_kernel(const K8V4WriteArgs a) 
     }
   }
 #pragma unroll
-  for (int ll = 1; ll < 32; ll <<= 1) {                   // len = ll * E
-    const bool upper = (lane & ll) != 0;
+  for (int ll = 1; ll < LPR; ll <<= 1) {                  // len = ll * E
+    // the lower partner keeps x + o, the upper o - x: RN(sgn * x + o) in one
+    // fma, sgn = +-1 (sgn * x is exact), the same bits as the add or subtract
+    const float sgn = (rl & ll) ? -1.f : 1.f;
 #pragma unroll
     for (int i = 0; i < E; ++i) {
       const float o = __shfl_xor_sync(0xffffffffu, x[i], ll);
-      x[i] = upper ? __fsub_rn(o, x[i]) : __fadd_rn(x[i], o);
+      x[i] = __fmaf_rn(sgn, x[i], o);
     }
   }
 #pragma unroll
   for (int i = 0; i < E; ++i) x[i] = __fmul_rn(x[i], inv_sqrt_d<D>());
-
-  const int64_t slot = a.slot_mapping[t];
-  const int64_t cap = static_cast<int64_t>(a.num_pages) * a.P;
-  if (slot < 0) return;
-  if (slot >= cap) {
-    if (lane == 0 && kind == 0) set_error(a.err, KV4_EBOUNDS);
-    return;
-  }
-  // slots are below num_pages * P < 2^31 (the pool check), so 32-bit math
-  const uint32_t page = fdiv(static_cast<uint32_t>(slot), a.p_div);
-  const int off = static_cast<int>(static_cast<uint32_t>(slot) - page * static_cast<uint32_t>(a.P));
-  uint8_t* chunk = a.pool + (static_cast<int64_t>(page) * a.Hkv + h) * a.chunk_bytes;
 
   // quotients x / s of the lane's elements as the IEEE division gives them:
   // Markstein's correction step on FP32 pairs where the operands allow it
@@ -100,58 +104,66 @@ __global__ void __launch_bounds__(256) k8v4_write_kernel(const K8V4WriteArgs a) 
   float lam = 0.f;                                        // the lane's largest |x|
 #pragma unroll
   for (int i = 0; i < E; ++i) lam = fmaxf(lam, fabsf(x[i]));
-  auto quotients = [&](float s, float (&q)[E]) {
-    const float r = __frcp_rn(s);
-    if (div_rn_in_range(r, lam)) {
+  auto quotients8 = [&](float s, float r, bool in_range, int i0, float (&q)[8]) {
+    if (in_range) {
       const uint64_t nb = f2(-s, -s), r2 = f2(r, r);
 #pragma unroll
-      for (int i = 0; i < E; i += 2) div_rn_pair(x[i], x[i + 1], nb, r2, q[i], q[i + 1]);
+      for (int i = 0; i < 8; i += 2) div_rn_pair(x[i0 + i], x[i0 + i + 1], nb, r2, q[i], q[i + 1]);
     } else {
 #pragma unroll
-      for (int i = 0; i < E; ++i) q[i] = __fdiv_rn(x[i], s);
+      for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(x[i0 + i], s);
     }
   };
 
-  if (kind == 0) {
-    float q[E];
-    quotients(__ldg(a.s_k), q);
-    uint8_t* dst = chunk + static_cast<int64_t>(off) * D + lane * E;
-    if constexpr (E == 2) {
-      const uint32_t w2 = f32x2_to_e4m3x2(q[0], q[1]);
-      *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(w2);
-    } else {
-      uint32_t w[E / 4];
+  // V: the row's amax over its LPR lanes (before any lane leaves)
+  float amax = lam;
 #pragma unroll
-      for (int i = 0; i < E; i += 4)
-        w[i / 4] = f32x2_to_e4m3x2(q[i], q[i + 1]) | (f32x2_to_e4m3x2(q[i + 2], q[i + 3]) << 16);
-      if constexpr (E == 8) *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
-      else *reinterpret_cast<uint32_t*>(dst) = w[0];
+  for (int o = 1; o < LPR; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+
+  if (!live || slot < 0) return;
+  const int64_t cap = static_cast<int64_t>(a.num_pages) * a.P;
+  if (slot >= cap) {
+    if (rl == 0 && kind == 0) set_error(a.err, KV4_EBOUNDS);
+    return;
+  }
+  // slots are below num_pages * P < 2^31 (the pool check), so 32-bit math
+  const uint32_t page = fdiv(static_cast<uint32_t>(slot), a.p_div);
+  const int off = static_cast<int>(static_cast<uint32_t>(slot) - page * static_cast<uint32_t>(a.P));
+  uint8_t* chunk = a.pool + (static_cast<int64_t>(page) * a.Hkv + h) * a.chunk_bytes;
+
+  if (kind == 0) {
+    const float s = __ldg(a.s_k), r = __frcp_rn(s);
+    const bool in_range = div_rn_in_range(r, lam);
+    uint4* dst = reinterpret_cast<uint4*>(chunk + static_cast<int64_t>(off) * D + rl * E);
+#pragma unroll
+    for (int c = 0; c < E / 16; ++c) {
+      uint32_t w[4];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float q[8];
+        quotients8(s, r, in_range, 16 * c + 8 * hh, q);
+        w[2 * hh] = f32x2_to_e4m3x2(q[0], q[1]) | (f32x2_to_e4m3x2(q[2], q[3]) << 16);
+        w[2 * hh + 1] = f32x2_to_e4m3x2(q[4], q[5]) | (f32x2_to_e4m3x2(q[6], q[7]) << 16);
+      }
+      dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
     }
   } else {
-    float amax = lam;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const float s = div7(amax);                           // RN(amax / 7)
-    uint32_t nib = 0;                                     // E nibbles, element 2j low in byte j
+    uint32_t nib[E / 8] = {};                             // element 2j low in byte j
     if (s != 0.f) {
       // |x / s| <= 7.0000005: rint by the magic addition, no clamp needed
-      float q[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      float qe[E];
-      quotients(s, qe);
+      const float r = __frcp_rn(s);
+      const bool in_range = div_rn_in_range(r, lam);
 #pragma unroll
-      for (int i = 0; i < E; ++i) q[i] = qe[i];
-      nib = int4x8(q);
-      if constexpr (E < 8) nib &= (1u << (4 * E)) - 1u;
+      for (int c = 0; c < E / 8; ++c) {
+        float q[8];
+        quotients8(s, r, in_range, 8 * c, q);
+        nib[c] = int4x8(q);
+      }
     }
-    uint8_t* codes = chunk + static_cast<int64_t>(a.P) * D + static_cast<int64_t>(off) * (D / 2) + lane * (E / 2);
-    if constexpr (E == 8) {
-      *reinterpret_cast<uint32_t*>(codes) = nib;
-    } else if constexpr (E == 4) {
-      *reinterpret_cast<uint16_t*>(codes) = static_cast<uint16_t>(nib);
-    } else {
-      *codes = static_cast<uint8_t>(nib);
-    }
-    if (lane == 0)
+    uint8_t* codes = chunk + static_cast<int64_t>(a.P) * D + static_cast<int64_t>(off) * (D / 2) + rl * (E / 2);
+    *reinterpret_cast<uint4*>(codes) = make_uint4(nib[0], nib[1], nib[2], nib[3]);
+    if (rl == 0)
       *reinterpret_cast<float*>(chunk + static_cast<int64_t>(a.P) * D + static_cast<int64_t>(a.P) * (D / 2) +
                                 4 * off) = s;
   }
@@ -164,7 +176,8 @@ cudaError_t launch_k8v4_write(const K8V4WriteArgs& a_in, cudaStream_t st) {
   K8V4WriteArgs a = a_in;
   a.hkv_div = make_fastdiv(static_cast<uint32_t>(a.Hkv));
   a.p_div = make_fastdiv(static_cast<uint32_t>(a.P));
-  const dim3 grid(static_cast<unsigned>((a.rows + 7) / 8), 2);
+  const int64_t rows_per_cta = 8 * (32 / (a.D / 32));   // 8 warps of 32 / (D / 32) rows
+  const dim3 grid(static_cast<unsigned>((a.rows + rows_per_cta - 1) / rows_per_cta), 2);
   switch (a.D) {
     case 64: k8v4_write_kernel<64><<<grid, 256, 0, st>>>(a); break;
     case 128: k8v4_write_kernel<128><<<grid, 256, 0, st>>>(a); break;
