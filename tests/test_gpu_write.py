@@ -185,18 +185,22 @@ def test_write_pair_rows_every_slot_pattern(fmt, D):
 
 
 @pytest.mark.parametrize("fmt", ["nvfp4", "int4", "fp8"])
-def test_write_many_units_per_thread(fmt):
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_write_many_units_per_thread(fmt, D):
     """A prefill-sized call: each thread of the resident grid walks several
-    units through its staging ring (12,289 tokens x 4 heads x 16 blocks per
-    K|V, about seven units a thread).  An aligned run, a shuffled run with
-    skipped tokens and the odd last token, over a pool of random bytes."""
-    T, H, D, P = 12289, 4, 256, 64
+    units through its staging ring (12,289 tokens x 4 heads x D/16 blocks per
+    K|V: up to about seven units a thread at D = 256, and more units than one
+    pass of the grid at every D).  An aligned run, a shuffled run with skipped
+    tokens and the odd last token, over a pool of random bytes."""
+    T, H, P = 12289, 4, 64
     pages = (T + P - 1) // P + 8
     rng = np.random.default_rng(12289)
     x = (rng.standard_normal((2, T, H, D)) * np.exp(rng.uniform(-3, 3, (2, T, H, 1)))).astype(np.float32)
     x[:, :, :, 9] *= 11.0
     k, v = f32_to_bf16_bits(x[0]), f32_to_bf16_bits(x[1])
     g = np.array([np.abs(x[0]).max() / 2688.0, np.abs(x[1]).max() / 2688.0], np.float32)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert (T + 1) // 2 * H * (D // 16) > sms * 3 // 2 * 256      # the streamed form
     half = 6000
     slots = np.concatenate([np.arange(half) + 2 * P,
                             rng.permutation(np.arange(half + 2 * P + 1, pages * P))[:T - half]]).astype(np.int64)
