@@ -286,7 +286,6 @@ template <int D, int FMT>
 __global__ void __launch_bounds__(kPrefixThreads, 3)
 prefix_kernel(const PrefixArgs a, const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v) {
   constexpr int TPR = D / 64;                   // threads per row
-  constexpr int RB = D / 2, SB = D / 16;
   __shared__ uint2 s_tab[FMT == KV4_NVFP4 ? 256 : 1];
   __shared__ __align__(1024) uint8_t s_out[(kPrefixThreads / 32) * 4096];   // per warp: two 2 KB buffers
   const int b = blockIdx.z;
