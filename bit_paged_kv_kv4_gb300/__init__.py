@@ -65,6 +65,8 @@ def _load(build_if_missing=False):
         "kv4_decode_workspace_bytes": (i64, [i32, i32, i32, i32]),
         "kv4_decode_attention": (i32, [vp, P, vp, vp, i32, vp, i32, i32, f32, i32, vp, i64, vp,
                                        i32, vp]),
+        "kv4_decode_step": (i32, [vp, vp, vp, P, vp, vp, i32, vp, i32, i32, f32, i32, vp, i64, vp,
+                                  i32, vp]),
         "kv4_dequant_prefix": (i32, [P, vp, vp, i32, vp, vp, i32, i32, vp, vp, vp, vp]),
         "kv4_calibrate_global_scale": (i32, [vp, vp, i64, i32, i32, vp, vp]),
         "kv4_extend_workspace_bytes": (i64, [i32, i32, i32, i32]),
@@ -176,6 +178,20 @@ def kv4_decode_attention(q, pool, layer_global_scale, block_table, seq_lens, sm_
         _ptr(seq_lens), B, Hq, float(sm_scale), int(num_splits), _ptr(workspace), ws_bytes,
         _ptr(out), 1 if out.dtype == torch.float32 else 0, _stream(stream))
     _check(st, "kv4_decode_attention")
+
+
+def kv4_decode_step(q, k_new, v_new, pool, layer_global_scale, block_table, seq_lens, sm_scale,
+                    out, num_splits=0, workspace=None, stream=None):
+    """One decode step in one kernel: each request's new token (k_new, v_new
+    [B, Hkv, D] bf16) written into position seq_lens[b] - 1 of its pages,
+    then decode attention as kv4_decode_attention (same arguments)."""
+    B, Hq, D = q.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = _load().kv4_decode_step(
+        _ptr(q), _ptr(k_new), _ptr(v_new), pool.ref, _ptr(layer_global_scale), _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), B, Hq, float(sm_scale), int(num_splits), _ptr(workspace),
+        ws_bytes, _ptr(out), 1 if out.dtype == torch.float32 else 0, _stream(stream))
+    _check(st, "kv4_decode_step")
 
 
 def kv4_decode_attention_static_ws(q, pool, layer_global_scale, block_table, seq_lens, sm_scale,

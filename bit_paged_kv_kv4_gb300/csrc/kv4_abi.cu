@@ -374,17 +374,25 @@ int64_t kv4_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t h
   return align256((batch + 1) * 8) + align256(slots * 8 * 16) + slots * 8 * head_dim * 4;
 }
 
-kv4_status kv4_decode_attention(const void* q, const kv4_pool* pool,
+// kv4_decode_attention, and kv4_decode_step when k_new / v_new are given.
+static kv4_status decode_common(const void* q, const void* k_new, const void* v_new, const kv4_pool* pool,
                                 const float* layer_global_scale, const int32_t* block_table,
                                 int32_t max_pages, const int32_t* seq_lens, int32_t batch,
                                 int32_t num_q_heads, float sm_scale, int32_t num_splits,
                                 void* workspace, int64_t workspace_bytes, void* out,
                                 int32_t out_is_fp32, void* stream) {
-  kv4::NvtxRange nvtx_range("kv4_decode_attention");
   g_msg.clear();
   kv4_status s = kv4::check_decode_args(q, pool, layer_global_scale, block_table, max_pages,
                                         seq_lens, batch, num_q_heads, sm_scale, num_splits, out);
   if (s != KV4_OK || batch == 0) return s;
+  if (k_new != nullptr || v_new != nullptr) {
+    if (pool->fmt != KV4_NVFP4 && pool->fmt != KV4_INT4_PTH)
+      return fail(KV4_EUNSUPPORTED, "kv4_decode_step: NVFP4 and INT4 pools only (use kv4_write, then decode)");
+    if (num_q_heads / pool->num_kv_heads > 8)
+      return fail(KV4_EUNSUPPORTED, "kv4_decode_step: at most 8 query heads per kv head");
+    if (k_new == nullptr || v_new == nullptr) return fail(KV4_EINVAL, "k_new and v_new must be non-NULL");
+    if (!aligned(k_new, 16) || !aligned(v_new, 16)) return fail(KV4_EINVAL, "k_new and v_new must be 16-byte aligned");
+  }
   const int G = num_q_heads / pool->num_kv_heads;
   const int64_t need = kv4_decode_workspace_bytes(batch, num_q_heads, pool->head_dim, num_splits);
   if (need > 0) {
@@ -452,8 +460,36 @@ kv4_status kv4_decode_attention(const void* q, const kv4_pool* pool,
   } else if ((s = decode4_maps(*pool, &map, &map2)) != KV4_OK) {
     return s;
   }
+  a.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  a.v_new = static_cast<const __nv_bfloat16*>(v_new);
   cudaError_t e = kv4::launch_decode(a, map, map2, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KV4_OK : cuda_fail(e, "kv4_decode_attention launch");
+}
+
+kv4_status kv4_decode_attention(const void* q, const kv4_pool* pool,
+                                const float* layer_global_scale, const int32_t* block_table,
+                                int32_t max_pages, const int32_t* seq_lens, int32_t batch,
+                                int32_t num_q_heads, float sm_scale, int32_t num_splits,
+                                void* workspace, int64_t workspace_bytes, void* out,
+                                int32_t out_is_fp32, void* stream) {
+  kv4::NvtxRange nvtx_range("kv4_decode_attention");
+  return decode_common(q, nullptr, nullptr, pool, layer_global_scale, block_table, max_pages, seq_lens, batch,
+                       num_q_heads, sm_scale, num_splits, workspace, workspace_bytes, out, out_is_fp32, stream);
+}
+
+kv4_status kv4_decode_step(const void* q, const void* k_new, const void* v_new, const kv4_pool* pool,
+                           const float* layer_global_scale, const int32_t* block_table,
+                           int32_t max_pages, const int32_t* seq_lens, int32_t batch,
+                           int32_t num_q_heads, float sm_scale, int32_t num_splits,
+                           void* workspace, int64_t workspace_bytes, void* out,
+                           int32_t out_is_fp32, void* stream) {
+  kv4::NvtxRange nvtx_range("kv4_decode_step");
+  if (k_new == nullptr || v_new == nullptr) {
+    g_msg.clear();
+    return fail(KV4_EINVAL, "kv4_decode_step: k_new and v_new must be non-NULL");
+  }
+  return decode_common(q, k_new, v_new, pool, layer_global_scale, block_table, max_pages, seq_lens, batch,
+                       num_q_heads, sm_scale, num_splits, workspace, workspace_bytes, out, out_is_fp32, stream);
 }
 
 kv4_status kv4_calibrate_global_scale(const void* k, const void* v, int64_t num_tokens,

@@ -56,6 +56,7 @@
 #include <utility>
 
 #include "kv4_device.cuh"
+#include "kv4_encode.cuh"
 #include "kv4_internal.h"
 
 namespace kv4 {
@@ -201,6 +202,158 @@ __host__ __device__ inline int64_t part_of4(int64_t x, int64_t total, int64_t pa
 
 }  // namespace
 
+// ---------------------------------------------------------------- new tokens
+// kv4_decode_step: the new token of request b (position L - 1) for kv head h
+// and tensor `kind` (0: K, 1: V), quantised by one warp exactly as kv4_write
+// does it (the same IEEE FP32 quotients and conversions), into the pool.  A
+// lane holds E = D / 32 consecutive elements; a 16-element NVFP4 block spans
+// 16 / E lanes.  Only the CTA that decodes position L - 1 writes it, before
+// it loads that tile, so no other thread touches these bytes meanwhile (the
+// NVFP4 V pair row is updated by a plain read-modify-write).
+template <int D, int FMT>
+__device__ __noinline__ void write_new_token(const DecodeArgs& a, int b, int h, int kind) {
+  constexpr int E = D / 32, RB = D / 2;
+  const int lane = threadIdx.x & 31;
+  const int Lmax = a.max_pages * a.P;
+  int L = a.seq_lens[b];
+  L = L < 0 ? 0 : (L > Lmax ? Lmax : L);
+  if (L == 0) return;
+  const int pos = L - 1, pidx = pos / a.P, off = pos - pidx * a.P;
+  const int page = __ldg(a.block_table + static_cast<int64_t>(b) * a.max_pages + pidx);
+  if (page < 0 || page >= a.num_pages) {
+    if (lane == 0) set_error(a.err, KV4_EBOUNDS);
+    return;
+  }
+  // the pool is written only here, by the one CTA that owns this position
+  uint8_t* chunk = const_cast<uint8_t*>(a.pool) + (static_cast<int64_t>(page) * a.Hkv + h) * a.chunk_bytes;
+  const __nv_bfloat16* src = (kind == 0 ? a.k_new : a.v_new) + (static_cast<int64_t>(b) * a.Hkv + h) * D + lane * E;
+  float x[E];
+#pragma unroll
+  for (int i = 0; i < E; i += 2) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(src + i));
+    x[i] = f.x;
+    x[i + 1] = f.y;
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < E; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  // q_i = RN(x_i / b) (div_rn on pairs where in range, else IEEE), q = 0 if b = 0
+  auto quotients = [&](float bden, float bound, float (&q)[E]) {
+    const float yb = __frcp_rn(bden);
+    if (div_rn_in_range(yb, bound)) {
+      const uint64_t nb = f2(-bden, -bden), yb2 = f2(yb, yb);
+#pragma unroll
+      for (int i = 0; i < E; i += 2) div_rn_pair(x[i], x[i + 1], nb, yb2, q[i], q[i + 1]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < E; ++i) q[i] = __fdiv_rn(x[i], bden);
+    }
+  };
+  if constexpr (FMT == KV4_NVFP4) {
+    constexpr int BL = 16 / E;                            // lanes per block
+    constexpr int SB = D / 16;
+#pragma unroll
+    for (int o = 1; o < BL; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float g = __ldg(a.gscale + kind);
+    const float g6 = __fmul_rn(kE2M1Max, g);
+    const uint32_t S = f32_to_e4m3(div_rn(amax, g6, __frcp_rn(g6)));
+    const float den = __fmul_rn(e4m3_to_f32(S), g);
+    float q[E];
+#pragma unroll
+    for (int i = 0; i < E; ++i) q[i] = 0.f;
+    if (S != 0u && den != 0.f) quotients(den, amax, q);
+    uint32_t code[E];                                     // E2M1 code of element i
+#pragma unroll
+    for (int i = 0; i < E; i += 2) {
+      const uint32_t byte = f32x2_to_e2m1x2(q[i], q[i + 1]);
+      code[i] = byte & 0xFu;
+      code[i + 1] = byte >> 4;
+    }
+    const int blk = lane / BL;
+    if (kind == 0) {
+      uint8_t* dst = chunk + static_cast<int64_t>(off) * RB + lane * (E / 2);
+#pragma unroll
+      for (int i = 0; i < E; i += 2) dst[i / 2] = static_cast<uint8_t>(code[i] | (code[i + 1] << 4));
+      if (lane % BL == 0) chunk[static_cast<int64_t>(a.P) * D + static_cast<int64_t>(off) * SB + blk] = static_cast<uint8_t>(S);
+    } else {
+      // token-pair row off / 2: byte d holds element d of this token in nibble off % 2
+      const int sh = 4 * (off & 1);
+      uint8_t* row = chunk + static_cast<int64_t>(a.P) * RB + static_cast<int64_t>(off >> 1) * D + lane * E;
+#pragma unroll
+      for (int i = 0; i < E; ++i)
+        row[i] = static_cast<uint8_t>((row[i] & ~(0xFu << sh)) | (code[i] << sh));
+      if (lane % BL == 0)
+        chunk[static_cast<int64_t>(a.P) * D + static_cast<int64_t>(a.P) * SB + static_cast<int64_t>(off >> 1) * 2 * SB +
+              2 * blk + (off & 1)] = static_cast<uint8_t>(S);
+    }
+  } else {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float sc = div7(amax);                          // RN(amax / 7)
+    uint32_t nib = 0;                                     // element i in nibble i
+    if (sc != 0.f) {
+      float q[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      float qe[E];
+      quotients(sc, amax, qe);
+#pragma unroll
+      for (int i = 0; i < E; ++i) q[i] = qe[i];
+      nib = int4x8(q);
+    }
+    uint8_t* codes = chunk + static_cast<int64_t>(kind) * a.P * RB + static_cast<int64_t>(off) * RB + lane * (E / 2);
+#pragma unroll
+    for (int i = 0; i < E / 2; ++i) codes[i] = static_cast<uint8_t>(nib >> (8 * i));
+    if (lane == 0) reinterpret_cast<float*>(chunk + static_cast<int64_t>(a.P) * D)[static_cast<int64_t>(kind) * a.P + off] = sc;
+  }
+}
+
+// The new tokens this CTA must write: those of the units whose last tile is
+// in its range [c0, c1) of the global tile order (balanced mode), or of its
+// unit (unit mode).  Rounds of at most one unit per thread (requests in
+// blocks of the CTA's threads, one unit index j at a time); warp w takes the
+// round's tasks w, w + 4, ... (task = unit x K|V).
+template <int D, int FMT>
+__device__ __noinline__ void write_new_tokens(const DecodeArgs& a, int64_t c0, int64_t c1, int UPB, int64_t* red,
+                                              int* s_jobs, int* s_njobs) {
+  const int tid = threadIdx.x, warp = tid >> 5;
+  auto run_round = [&](int job) {            // job: b * UPB + j, or -1
+    if (tid == 0) *s_njobs = 0;
+    __syncthreads();
+    if (job >= 0) s_jobs[atomicAdd(s_njobs, 1)] = job;
+    __syncthreads();
+    const int nj = *s_njobs;
+    for (int t = warp; t < 2 * nj; t += kNW) {
+      const int u = s_jobs[t >> 1];
+      write_new_token<D, FMT>(a, u / UPB, u % UPB, t & 1);  // one unit per kv head (at most 8 query heads)
+    }
+    __syncthreads();
+  };
+  if (a.unit_ctas) {
+    run_round(tid == 0 ? static_cast<int>(blockIdx.x) : -1);
+  } else {
+    int64_t acc = 0;
+    for (int b0 = 0; b0 < a.B; b0 += kNW * 32) {
+      const int b = b0 + tid;
+      const int n_b = (b < a.B) ? (clamp_len(a, b, false) + kTT - 1) / kTT : 0;
+      int64_t tot;
+      const int64_t start = acc + block_scan(static_cast<int64_t>(n_b) * UPB, red, tot);
+      acc += tot;
+      // the request block's units whose last tile this CTA decodes
+      const int64_t first_last = start + n_b - 1, last_last = start + static_cast<int64_t>(UPB) * n_b - 1;
+      const bool some = n_b > 0 && last_last >= c0 && first_last < c1;
+      if (!__syncthreads_or(some)) continue;
+      for (int j = 0; j < UPB; ++j) {
+        const int64_t last = start + static_cast<int64_t>(j + 1) * n_b - 1;
+        const bool mine = n_b > 0 && last >= c0 && last < c1;
+        if (!__syncthreads_or(mine)) continue;
+        run_round(mine ? b * UPB + j : -1);
+      }
+    }
+  }
+  // the generic-proxy writes of the pool before this CTA's TMA reads of it
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  __syncthreads();
+}
+
 template <int D, int FMT>
 __global__ void __launch_bounds__(kNW * 32, kCtas)
 decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
@@ -264,6 +417,14 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
     if (tid == 0) s_cursor = part_begin4(blockIdx.x, T, a.n_cta);
   }
   __syncthreads();
+  if constexpr (FMT != KV4_K8V4) {
+    if (a.k_new != nullptr) {
+      __shared__ int s_jobs[kNW * 32];
+      __shared__ int s_njobs;
+      write_new_tokens<D, FMT>(a, a.unit_ctas ? 0 : part_begin4(blockIdx.x, T, a.n_cta), c1, UPB, sRed, s_jobs,
+                               &s_njobs);
+    }
+  }
 
   // ---- per-thread shared-memory offsets inside a stage ----------------------
   // K: bytes [KB tig, KB (tig + 1)) of token rows grp and grp + 8, in 16-byte

@@ -58,6 +58,11 @@ struct DecodeArgs {
   void* out;
   int out_f32;
   int* err;
+  // kv4_decode_step: each request's new K/V token ([B][Hkv][D] bf16), written
+  // into its position seq_lens[b] - 1 by the CTA that decodes that position;
+  // null for a plain decode
+  const __nv_bfloat16* k_new;
+  const __nv_bfloat16* v_new;
 };
 
 struct WriteArgs {

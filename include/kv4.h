@@ -195,6 +195,30 @@ kv4_status kv4_decode_attention(const void* q, const kv4_pool* pool,
                                 int32_t out_is_fp32, void* stream);
 
 /*
+ * kv4_decode_step -- one decode step with the step's new token written in
+ * the same kernel: the effect of
+ *     kv4_write(k_new, v_new, slot_mapping = the slot of position
+ *               seq_lens[b] - 1 of each request b, T = B, ...)
+ * followed by kv4_decode_attention(...) with the same arguments (Figure 2:
+ * each decode step writes its token into the 4-bit cache and attends over
+ * the request's tokens).  The new token's slot is the one the block table
+ * gives position seq_lens[b] - 1 (no slot mapping is passed); a request with
+ * seq_lens[b] == 0 writes nothing.  The CTA that decodes that position
+ * quantises the token first, so the pool bytes written and the output are
+ * bitwise those of the two calls.
+ *   k_new, v_new  device bf16 [B][Hkv][D], 16-byte aligned.
+ *   Other arguments as kv4_decode_attention.
+ * NVFP4 and INT4 pools with at most 8 query heads per kv head; anything else
+ * (FP8, k8v4, larger GQA groups) is KV4_EUNSUPPORTED: use the two calls.
+ */
+kv4_status kv4_decode_step(const void* q, const void* k_new, const void* v_new, const kv4_pool* pool,
+                           const float* layer_global_scale, const int32_t* block_table,
+                           int32_t max_pages, const int32_t* seq_lens, int32_t batch,
+                           int32_t num_q_heads, float sm_scale, int32_t num_splits,
+                           void* workspace, int64_t workspace_bytes, void* out,
+                           int32_t out_is_fp32, void* stream);
+
+/*
  * kv4_dequant_prefix -- the chunked-prefill path of Figure 2: the 4-bit
  * cached prefix is turned into FP8, in a buffer that is reused.  For each
  * request b, prefix token t < prefix_lens[b] and kv head h:

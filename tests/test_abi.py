@@ -206,3 +206,24 @@ def test_extend_workspace_sizing_and_checks(lib):
     st = lib.kv4_extend_attention(fake, fake, fake, fake, fake, fake, fake, fake, fake, fake, 1, 8192, 24,
                                   4, 256, 0.0625, fake, n - 1, fake, 0, None)
     assert st == 1                               # workspace too small
+
+
+def test_decode_step_validation_without_gpu(lib):
+    """kv4_decode_step: NVFP4 / INT4 pools with at most 8 query heads per kv
+    head, non-NULL 16-byte aligned new K/V; everything else is refused before
+    any CUDA call."""
+    fake = ctypes.c_void_p(1 << 20)
+
+    def step(d, k=fake, v=fake, Hq=8):
+        return _status(lib, lib.kv4_decode_step(fake, k, v, ctypes.byref(d), fake, fake, 8, fake, 2, Hq,
+                                                0.0625, 1, None, 0, fake, 1, None))
+    d = desc(base=1 << 20)                 # NVFP4
+    st, msg = step(desc(fmt=2, base=1 << 20))
+    assert st == 2 and "NVFP4 and INT4" in msg
+    Hkv = d.num_kv_heads
+    st, msg = step(d, Hq=16 * Hkv)
+    assert st == 2 and "8 query heads" in msg
+    st, msg = step(d, k=None)
+    assert st == 1 and "k_new" in msg
+    st, msg = step(d, v=ctypes.c_void_p((1 << 20) + 2))
+    assert st == 1 and "aligned" in msg
