@@ -1,9 +1,11 @@
 #!/usr/bin/env python
 """Decode-step benchmark of the 4-bit paged KV cache on GB300.
 
-One step is the whole decode hot path for one batch: kv4_write of each
-request's new token into the NVFP4 pool, then kv4_decode_attention (split-KV
-kernel + log-sum-exp combine) over every request's full context.  The
+One step is the whole decode hot path for one batch: each request's new
+token quantised into the NVFP4 pool and decode attention (split-KV kernel +
+log-sum-exp combine) over every request's full context, in one
+kv4_decode_step call (the decode kernel writes the new tokens itself; the
+same step as kv4_write + kv4_decode_attention, which is timed beside it).  The
 headline workload is a Qwen3.8-27B-shaped full-attention layer at 32K
 context (4 KV heads, 24 query heads, head dim 256, batch 16, lengths uniform
 in [24576, 32768], 64-token pages); the pool (about 0.53 GB) is far larger
@@ -245,8 +247,23 @@ class Setup:
         self.K.kv4_decode_attention(self.q, self.pool, self.g, self.d_table, self.d_lens, self.sm,
                                     self.out, num_splits=self.splits, workspace=self.ws)
 
+    @property
+    def fused(self):
+        """NVFP4 and INT4 have the one-call step; the FP8 comparison format not."""
+        return self.w.fmt != "fp8"
+
+    def step(self):
+        """write() + decode(), in one kv4_decode_step call where the format has
+        it (the decode kernel quantises the new tokens)."""
+        if not self.fused:
+            self.write()
+            self.decode()
+            return
+        self.K.kv4_decode_step(self.q, self.k_new, self.v_new, self.pool, self.g, self.d_table, self.d_lens,
+                               self.sm, self.out, num_splits=self.splits, workspace=self.ws)
+
     def launches_per_step(self):
-        return 1 + 1 + (0 if self.splits == 1 else 1)
+        return (0 if self.fused else 1) + 1 + (0 if self.splits == 1 else 1)
 
 
 def time_decode_only(s, iters):
@@ -465,37 +482,45 @@ def kv4_arm(args):
 
     # ---- device-resident timed region -----------------------------------
     for _ in range(args.warmup):
-        s.write()
-        s.decode()
+        s.step()
     torch.cuda.synchronize()
-    # The timed steps (write + decode); no event sits between a write and its
-    # decode, so each decode's early launch overlaps the write as in serving.
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    # The decode call's own average duration: the same decode call K times back
-    # to back between two events (the roofline's kernel time).
+    # The decode call's own average duration (the roofline's kernel time): the
+    # same kv4_decode_attention call K times back to back between two events.
     d_start = torch.cuda.Event(enable_timing=True)
     d_end = torch.cuda.Event(enable_timing=True)
+    # The timed steps: K kv4_decode_step calls back to back (the value).
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    # The same K steps as two calls each, kv4_write then kv4_decode_attention.
+    u_start = torch.cuda.Event(enable_timing=True)
+    u_end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     with clocks:
         barrier(pg, device)
         torch.cuda.synchronize()
-        t_start.record()
-        for i in range(args.steps):
-            s.write()
-            s.decode()
-        t_end.record()
-        torch.cuda.synchronize()
-        barrier(pg, device)
         d_start.record()
         for i in range(args.steps):
             s.decode()
         d_end.record()
         torch.cuda.synchronize()
         barrier(pg, device)
+        t_start.record()
+        for i in range(args.steps):
+            s.step()
+        t_end.record()
+        torch.cuda.synchronize()
+        barrier(pg, device)
+        u_start.record()
+        for i in range(args.steps):
+            s.write()
+            s.decode()
+        u_end.record()
+        torch.cuda.synchronize()
+        barrier(pg, device)
     total = t_start.elapsed_time(t_end) * 1e-3
     total = max_over_ranks(pg, total, device)
     dec_avg = max_over_ranks(pg, d_start.elapsed_time(d_end) * 1e-3 / args.steps, device)
+    split_step = max_over_ranks(pg, u_start.elapsed_time(u_end) * 1e-3 / args.steps, device)
     err = K.kv4_device_error()
     if err != 0:
         raise SystemExit(f"device error {err} during the timed region")
@@ -506,7 +531,7 @@ def kv4_arm(args):
     achieved = dec_bytes / dec_avg / 1e9
 
     # ---- end to end through the public API, host buffers ----------------
-    # The step's inputs (q, the new K/V, their slots, the lengths) sit in one
+    # The step's inputs (q, the new K/V, the lengths) sit in one
     # pinned host staging buffer and go over in one copy per step into a
     # device buffer, of which the library's arguments are views (each part
     # 256-byte aligned); the step's output comes back into pinned host memory.
@@ -514,7 +539,7 @@ def kv4_arm(args):
     # step k+1's inputs go over while step k computes, step k's output comes
     # back while step k+1 computes (two device input buffers and two outputs,
     # each reused only after the copy or the kernels that used it are done).
-    parts = [s.q, s.k_new, s.v_new, s.slot_new, s.d_lens]
+    parts = [s.q, s.k_new, s.v_new, s.d_lens] + ([] if s.fused else [s.slot_new])
     offs, at = [], 0
     for t in parts:
         offs.append(at)
@@ -539,7 +564,7 @@ def kv4_arm(args):
 
     def e2e_step(k):
         j = k % 2
-        d_q, d_k, d_v, d_slot, d_lens = views[j]
+        d_q, d_k, d_v, d_lens = views[j][:4]
         if k >= 2:
             s_in.wait_event(ev_done[j])          # step k-2's kernels are done with d_in[j]
         with torch.cuda.stream(s_in):
@@ -548,9 +573,13 @@ def kv4_arm(args):
         main.wait_event(ev_in[j])
         if k >= 2:
             main.wait_event(ev_out[j])           # step k-2's output has left d_out[j]
-        K.kv4_write(d_k, d_v, d_slot, s.pool, s.g, stream=main)
-        K.kv4_decode_attention(d_q, s.pool, s.g, s.d_table, d_lens, s.sm, d_out[j],
-                               num_splits=s.splits, workspace=s.ws, stream=main)
+        if s.fused:
+            K.kv4_decode_step(d_q, d_k, d_v, s.pool, s.g, s.d_table, d_lens, s.sm, d_out[j],
+                              num_splits=s.splits, workspace=s.ws, stream=main)
+        else:
+            K.kv4_write(d_k, d_v, views[j][4], s.pool, s.g, stream=main)
+            K.kv4_decode_attention(d_q, s.pool, s.g, s.d_table, d_lens, s.sm, d_out[j],
+                                   num_splits=s.splits, workspace=s.ws, stream=main)
         ev_done[j].record(main)
         s_out.wait_event(ev_done[j])
         with torch.cuda.stream(s_out):
@@ -583,7 +612,10 @@ def kv4_arm(args):
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": per_step * 1e3,
+        "step": ("kv4_decode_step (new-token write inside the decode kernel) + combine" if s.fused
+                 else "kv4_write + kv4_decode_attention"),
+        "ms_per_step_as_write_then_decode": split_step * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16*f16+f32 (nvfp4 cache)",
         "data": "synthetic",
         "config": {"workload": f"{w.name}: " + w.notes, "kv_heads": Hkv, "q_heads": Hq,

@@ -204,26 +204,34 @@ __host__ __device__ inline int64_t part_of4(int64_t x, int64_t total, int64_t pa
 
 // ---------------------------------------------------------------- new tokens
 // kv4_decode_step: the new token of request b (position L - 1) for kv head h
-// and tensor `kind` (0: K, 1: V), quantised by one warp exactly as kv4_write
-// does it (the same IEEE FP32 quotients and conversions), into the pool.  A
-// lane holds E = D / 32 consecutive elements; a 16-element NVFP4 block spans
+// goes into the pool before any tile is loaded.  A job is {b, h, page,
+// offset in the page} (the page looked up once, by the thread that found
+// the job); false when the request is empty or its page is out of range
+// (recorded).
+__device__ __forceinline__ bool new_token_job(const DecodeArgs& a, int b, int h, int4& job) {
+  const int L = clamp_len(a, b, false);
+  if (L == 0) return false;
+  const int pos = L - 1, pidx = pos / a.P;
+  const int page = __ldg(a.block_table + static_cast<int64_t>(b) * a.max_pages + pidx);
+  if (page < 0 || page >= a.num_pages) {
+    set_error(a.err, KV4_EBOUNDS);
+    return false;
+  }
+  job = make_int4(b, h, page, pos - pidx * a.P);
+  return true;
+}
+
+// One job's tensor `kind` (0: K, 1: V), quantised by one warp exactly as
+// kv4_write does it (the same IEEE FP32 quotients and conversions).  A lane
+// holds E = D / 32 consecutive elements; a 16-element NVFP4 block spans
 // 16 / E lanes.  Only the CTA that decodes position L - 1 writes it, before
 // it loads that tile, so no other thread touches these bytes meanwhile (the
 // NVFP4 V pair row is updated by a plain read-modify-write).
 template <int D, int FMT>
-__device__ __noinline__ void write_new_token(const DecodeArgs& a, int b, int h, int kind) {
+__device__ __forceinline__ void write_new_token(const DecodeArgs& a, const int4 job, int kind) {
   constexpr int E = D / 32, RB = D / 2;
   const int lane = threadIdx.x & 31;
-  const int Lmax = a.max_pages * a.P;
-  int L = a.seq_lens[b];
-  L = L < 0 ? 0 : (L > Lmax ? Lmax : L);
-  if (L == 0) return;
-  const int pos = L - 1, pidx = pos / a.P, off = pos - pidx * a.P;
-  const int page = __ldg(a.block_table + static_cast<int64_t>(b) * a.max_pages + pidx);
-  if (page < 0 || page >= a.num_pages) {
-    if (lane == 0) set_error(a.err, KV4_EBOUNDS);
-    return;
-  }
+  const int b = job.x, h = job.y, page = job.z, off = job.w;
   // the pool is written only here, by the one CTA that owns this position
   uint8_t* chunk = const_cast<uint8_t*>(a.pool) + (static_cast<int64_t>(page) * a.Hkv + h) * a.chunk_bytes;
   const __nv_bfloat16* src = (kind == 0 ? a.k_new : a.v_new) + (static_cast<int64_t>(b) * a.Hkv + h) * D + lane * E;
@@ -306,55 +314,49 @@ __device__ __noinline__ void write_new_token(const DecodeArgs& a, int b, int h, 
   }
 }
 
-// The new tokens this CTA must write: those of the units whose last tile is
-// in its range [c0, c1) of the global tile order (balanced mode), or of its
-// unit (unit mode).  Rounds of at most one unit per thread (requests in
-// blocks of the CTA's threads, one unit index j at a time); warp w takes the
-// round's tasks w, w + 4, ... (task = unit x K|V).
+// The CTA's jobs, two tasks each (K, V); warp w takes tasks w, w + 4, ...
 template <int D, int FMT>
-__device__ __noinline__ void write_new_tokens(const DecodeArgs& a, int64_t c0, int64_t c1, int UPB, int64_t* red,
-                                              int* s_jobs, int* s_njobs) {
-  const int tid = threadIdx.x, warp = tid >> 5;
-  auto run_round = [&](int job) {            // job: b * UPB + j, or -1
-    if (tid == 0) *s_njobs = 0;
-    __syncthreads();
-    if (job >= 0) s_jobs[atomicAdd(s_njobs, 1)] = job;
-    __syncthreads();
-    const int nj = *s_njobs;
-    for (int t = warp; t < 2 * nj; t += kNW) {
-      const int u = s_jobs[t >> 1];
-      write_new_token<D, FMT>(a, u / UPB, u % UPB, t & 1);  // one unit per kv head (at most 8 query heads)
-    }
-    __syncthreads();
-  };
-  if (a.unit_ctas) {
-    run_round(tid == 0 ? static_cast<int>(blockIdx.x) : -1);
-  } else {
-    int64_t acc = 0;
-    for (int b0 = 0; b0 < a.B; b0 += kNW * 32) {
-      const int b = b0 + tid;
-      const int n_b = (b < a.B) ? (clamp_len(a, b, false) + kTT - 1) / kTT : 0;
-      int64_t tot;
-      const int64_t start = acc + block_scan(static_cast<int64_t>(n_b) * UPB, red, tot);
-      acc += tot;
-      // the request block's units whose last tile this CTA decodes
-      const int64_t first_last = start + n_b - 1, last_last = start + static_cast<int64_t>(UPB) * n_b - 1;
-      const bool some = n_b > 0 && last_last >= c0 && first_last < c1;
-      if (!__syncthreads_or(some)) continue;
-      for (int j = 0; j < UPB; ++j) {
-        const int64_t last = start + static_cast<int64_t>(j + 1) * n_b - 1;
-        const bool mine = n_b > 0 && last >= c0 && last < c1;
-        if (!__syncthreads_or(mine)) continue;
-        run_round(mine ? b * UPB + j : -1);
-      }
-    }
-  }
-  // the generic-proxy writes of the pool before this CTA's TMA reads of it
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-  __syncthreads();
+__device__ __forceinline__ void run_new_token_jobs(const DecodeArgs& a, const int4* jobs, int nj) {
+  for (int t = threadIdx.x >> 5; t < 2 * nj; t += kNW) write_new_token<D, FMT>(a, jobs[t >> 1], t & 1);
 }
 
+// The general form of the job list: the units whose last tile is in the
+// CTA's range [c0, c1) of the global tile order, found by a scan over the
+// requests in blocks of the CTA's threads, in rounds of at most one unit per
+// thread (one unit index j at a time).  Ends with every job written.
 template <int D, int FMT>
+__device__ __forceinline__ void new_tokens_by_rounds(const DecodeArgs& a, int64_t c0, int64_t c1, int UPB,
+                                                  int64_t* red, int4* jobs, int* s_njobs) {
+  const int tid = threadIdx.x;
+  int64_t acc = 0;
+  for (int b0 = 0; b0 < a.B; b0 += kNW * 32) {
+    const int b = b0 + tid;
+    const int n_b = (b < a.B) ? (clamp_len(a, b, false) + kTT - 1) / kTT : 0;
+    int64_t tot;
+    const int64_t start = acc + block_scan(static_cast<int64_t>(n_b) * UPB, red, tot);
+    acc += tot;
+    const int64_t first_last = start + n_b - 1, last_last = start + static_cast<int64_t>(UPB) * n_b - 1;
+    const bool some = n_b > 0 && last_last >= c0 && first_last < c1;
+    if (!__syncthreads_or(some)) continue;
+    for (int j = 0; j < UPB; ++j) {
+      const int64_t last = start + static_cast<int64_t>(j + 1) * n_b - 1;
+      const bool mine = n_b > 0 && last >= c0 && last < c1;
+      if (!__syncthreads_or(mine)) continue;
+      if (tid == 0) *s_njobs = 0;
+      __syncthreads();
+      int4 job;
+      if (mine && new_token_job(a, b, j, job)) jobs[atomicAdd(s_njobs, 1)] = job;
+      __syncthreads();
+      run_new_token_jobs<D, FMT>(a, jobs, *s_njobs);
+      __syncthreads();
+    }
+  }
+}
+
+// STEP: the kv4_decode_step form (the new tokens written first; NVFP4 and
+// INT4 only); a separate instantiation, so the plain decode's code and
+// registers are untouched.
+template <int D, int FMT, bool STEP>
 __global__ void __launch_bounds__(kNW * 32, kCtas)
 decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
                const __grid_constant__ CUtensorMap smap) {
@@ -382,6 +384,7 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
   int64_t* sRed = reinterpret_cast<int64_t*>(gbase + Gm::OFF_RED);
   const uint32_t bars = base + Gm::OFF_BAR + warp * Gm::NS * 8;
   __shared__ int s_nseg;
+  __shared__ int s_njobs;           // kv4_decode_step: new-token jobs of this CTA
   __shared__ float s_qpre;
   __shared__ long long s_cursor, s_cum, s_b;
 
@@ -393,6 +396,13 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
     prefetch_tensormap(&cmap);
     prefetch_tensormap(&smap);
   }
+  // kv4_decode_step's jobs (at most kJobs listed here; sAcc is free until
+  // the first merge).  The host allows it only with G <= 8, so unit j of a
+  // request is kv head j.
+  constexpr int kJobs = kNW * 32;
+  static_assert(!STEP || 32 * Gm::AS * 4 >= kJobs * 16, "job list");
+  int4* sJobs = reinterpret_cast<int4*>(sAcc);
+  if (STEP && tid == 0) s_njobs = 0;   // before the barriers below
 
   // ---- this CTA's tile range [cursor, c1) in the global (b, unit, tile) order ------
   int64_t T = 0, c1 = 0;
@@ -402,27 +412,61 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
     if (tid == 0) {
       sSeg[0] = Seg{u, 0, n_u, 0, clamp_len(a, b, false)};
       s_nseg = 1;
+      int4 job;
+      if (STEP && new_token_job(a, b, u - b * UPB, job)) {
+        sJobs[0] = job;
+        s_njobs = 1;
+      }
     }
   } else {
+    int64_t ex0 = 0, v0 = 0;          // this thread's request when B <= kJobs
     for (int b0 = 0; b0 < a.B; b0 += kNW * 32) {
       const int b = b0 + tid;
       const int64_t v = (b < a.B) ? static_cast<int64_t>((clamp_len(a, b, blockIdx.x == 0) + kTT - 1) / kTT) * UPB : 0;
       int64_t tot;
       const int64_t ex = block_scan(v, sRed, tot);
       if (blockIdx.x == 0 && b < a.B) a.cum[b] = T + ex;        // for combine_kernel
+      if (b0 == 0) {
+        ex0 = ex;
+        v0 = v;
+      }
       T += tot;
     }
     if (blockIdx.x == 0 && tid == 0) a.cum[a.B] = T;
     c1 = part_begin4(blockIdx.x + 1, T, a.n_cta);
-    if (tid == 0) s_cursor = part_begin4(blockIdx.x, T, a.n_cta);
+    const int64_t c0 = part_begin4(blockIdx.x, T, a.n_cta);
+    if (tid == 0) s_cursor = c0;
+    if constexpr (STEP) {
+      // the units of this thread's request whose last tile is in [c0, c1)
+      if (a.B <= kJobs && v0 > 0) {
+        const int64_t n_b = v0 / UPB;
+        bool have = false;
+        int4 job;
+        for (int j = 0; j < UPB; ++j) {
+          const int64_t last = ex0 + (j + 1) * n_b - 1;
+          if (last < c0 || last >= c1) continue;
+          if (!have && !new_token_job(a, tid, 0, job)) break;
+          have = true;
+          job.y = j;
+          const int k = atomicAdd(&s_njobs, 1);
+          if (k < kJobs) sJobs[k] = job;
+        }
+      }
+    }
   }
   __syncthreads();
-  if constexpr (FMT != KV4_K8V4) {
-    if (a.k_new != nullptr) {
-      __shared__ int s_jobs[kNW * 32];
-      __shared__ int s_njobs;
-      write_new_tokens<D, FMT>(a, a.unit_ctas ? 0 : part_begin4(blockIdx.x, T, a.n_cta), c1, UPB, sRed, s_jobs,
-                               &s_njobs);
+  if constexpr (STEP) {
+    const int nj = s_njobs;
+    if ((!a.unit_ctas && a.B > kJobs) || nj > kJobs) {
+      __syncthreads();                // every thread has read s_njobs
+      new_tokens_by_rounds<D, FMT>(a, part_begin4(blockIdx.x, T, a.n_cta), c1, UPB, sRed, sJobs, &s_njobs);
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      __syncthreads();
+    } else if (nj > 0) {
+      run_new_token_jobs<D, FMT>(a, sJobs, nj);
+      // the generic-proxy writes of the pool before this CTA's TMA reads of it
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      __syncthreads();
     }
   }
 
@@ -1067,11 +1111,11 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
 }
 
 // ------------------------------------------------------------------ launch
-template <int D, int FMT>
+template <int D, int FMT, bool STEP = false>
 static cudaError_t launch4(const DecodeArgs& a, const CUtensorMap& cmap, const CUtensorMap& smap,
                            cudaStream_t st) {
   using Gm = Geo4<D, FMT>;
-  auto* k = decode4_kernel<D, FMT>;
+  auto* k = decode4_kernel<D, FMT, STEP>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1104,17 +1148,23 @@ cudaError_t launch_decode4(const DecodeArgs& a, const CUtensorMap& cmap, const C
       default: return launch4<256, KV4_K8V4>(a, cmap, smap, st);
     }
   }
+  const bool step = a.k_new != nullptr;
   if (a.fmt == KV4_NVFP4) {
     switch (a.D) {
-      case 64: return launch4<64, KV4_NVFP4>(a, cmap, smap, st);
-      case 128: return launch4<128, KV4_NVFP4>(a, cmap, smap, st);
-      default: return launch4<256, KV4_NVFP4>(a, cmap, smap, st);
+      case 64: return step ? launch4<64, KV4_NVFP4, true>(a, cmap, smap, st) : launch4<64, KV4_NVFP4>(a, cmap, smap, st);
+      case 128:
+        return step ? launch4<128, KV4_NVFP4, true>(a, cmap, smap, st) : launch4<128, KV4_NVFP4>(a, cmap, smap, st);
+      default:
+        return step ? launch4<256, KV4_NVFP4, true>(a, cmap, smap, st) : launch4<256, KV4_NVFP4>(a, cmap, smap, st);
     }
   }
   switch (a.D) {
-    case 64: return launch4<64, KV4_INT4_PTH>(a, cmap, smap, st);
-    case 128: return launch4<128, KV4_INT4_PTH>(a, cmap, smap, st);
-    default: return launch4<256, KV4_INT4_PTH>(a, cmap, smap, st);
+    case 64:
+      return step ? launch4<64, KV4_INT4_PTH, true>(a, cmap, smap, st) : launch4<64, KV4_INT4_PTH>(a, cmap, smap, st);
+    case 128:
+      return step ? launch4<128, KV4_INT4_PTH, true>(a, cmap, smap, st) : launch4<128, KV4_INT4_PTH>(a, cmap, smap, st);
+    default:
+      return step ? launch4<256, KV4_INT4_PTH, true>(a, cmap, smap, st) : launch4<256, KV4_INT4_PTH>(a, cmap, smap, st);
   }
 }
 

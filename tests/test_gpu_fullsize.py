@@ -3,9 +3,11 @@
 bench.py times.
 
 The pool is filled through kv4_write from inputs drawn on the device by the
-workload module's seeded generator.  For sampled (request, kv head) units the
-test copies those inputs to the host and the oracle re-quantises and attends
-on its own: the pages of that unit must match byte for byte and the outputs of
+workload module's seeded generator, then one kv4_decode_step writes each
+request's new token over its last position and decodes.  For sampled
+(request, kv head) units the test copies those inputs (the new token in the
+last position) to the host and the oracle re-quantises and attends on its
+own: the pages of that unit must match byte for byte and the outputs of
 its query heads must meet the attention gate.  Every other output row is
 checked against what holds at any size: finite, and inside the convex hull
 bound |out| <= max |V_hat| of its kv head.
@@ -30,7 +32,7 @@ SAMPLES = {"nvfp4_32k": [(3, 1), (11, 3)], "nvfp4_160k": [(0, 2)], "nvfp4_1m": [
 def built(request):
     w = W.ALL[request.param]
     s = bench.Setup(w, torch.device("cuda", 0), keep_kv=True, fill=0)
-    s.decode()
+    s.step()
     torch.cuda.synchronize()
     assert s.K.kv4_device_error() == 0
     yield w, s
@@ -43,6 +45,8 @@ def unit_oracle(w, s, b, h):
     L = int(s.lens[b])
     k = to_u16(s.kv[b][0][:, h])
     v = to_u16(s.kv[b][1][:, h])
+    k[L - 1] = to_u16(s.k_new[b, h])      # the step's new token
+    v[L - 1] = to_u16(s.v_new[b, h])
     P = w.page_size
     npg = (L + P - 1) // P
     spec = OP.PoolSpec(w.fmt, npg, P, 1, w.head_dim)
@@ -79,7 +83,8 @@ def test_all_outputs_finite_and_bounded(built):
     out = s.out
     assert torch.isfinite(out).all()
     for h in range(w.num_kv_heads):
-        vmax = max(float(s.kv[b][1][:, h].float().abs().max()) for b in range(w.batch))
+        vmax = max(max(float(s.kv[b][1][:, h].float().abs().max()) for b in range(w.batch)),
+                   float(s.v_new[:, h].float().abs().max()))
         # decoded V may exceed its input by at most one E2M1 step of the block
         # (NVFP4) or half an INT4 step; 1.5x is a loose, size-independent bound
         assert float(out[:, h * w.group:(h + 1) * w.group].abs().max()) <= 1.5 * vmax
