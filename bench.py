@@ -485,7 +485,10 @@ def kv4_arm(args):
         s.step()
     torch.cuda.synchronize()
     # The decode call's own average duration (the roofline's kernel time): the
-    # same kv4_decode_attention call K times back to back between two events.
+    # same kv4_decode_attention call back to back between two events, at least
+    # 200 times (a run's start-up, about one call's host time before the first
+    # launch, spread over fewer calls would read as kernel time).
+    n_roof = max(args.steps, 200)
     d_start = torch.cuda.Event(enable_timing=True)
     d_end = torch.cuda.Event(enable_timing=True)
     # The timed steps: K kv4_decode_step calls back to back (the value).
@@ -499,7 +502,7 @@ def kv4_arm(args):
         barrier(pg, device)
         torch.cuda.synchronize()
         d_start.record()
-        for i in range(args.steps):
+        for i in range(n_roof):
             s.decode()
         d_end.record()
         torch.cuda.synchronize()
@@ -519,7 +522,7 @@ def kv4_arm(args):
         barrier(pg, device)
     total = t_start.elapsed_time(t_end) * 1e-3
     total = max_over_ranks(pg, total, device)
-    dec_avg = max_over_ranks(pg, d_start.elapsed_time(d_end) * 1e-3 / args.steps, device)
+    dec_avg = max_over_ranks(pg, d_start.elapsed_time(d_end) * 1e-3 / n_roof, device)
     split_step = max_over_ranks(pg, u_start.elapsed_time(u_end) * 1e-3 / args.steps, device)
     err = K.kv4_device_error()
     if err != 0:
@@ -629,8 +632,8 @@ def kv4_arm(args):
                      "ncu_dram_gbs": recorded_ncu_gbs(w.name),
                      "kernel": "decode4_kernel<256, NVFP4> + combine_kernel (kv4_decode_attention)",
                      "peak_source": f"{peak_src} hbm_gbs", "decode_us": dec_avg * 1e6,
-                     "decode_timing": f"mean of {args.steps} back-to-back decode calls between two CUDA "
-                                      "events on the launching stream, after the timed steps",
+                     "decode_timing": f"mean of {n_roof} back-to-back kv4_decode_attention calls between "
+                                      "two CUDA events on the launching stream, before the timed steps",
                      "tokens_per_s_16_layers": B / (16 * dec_avg)},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_total / args.steps * 1e3},

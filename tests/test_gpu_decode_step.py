@@ -102,3 +102,14 @@ def test_decode_step_refuses_fp8_and_large_groups():
     with pytest.raises(K.Kv4Error):
         K.kv4_decode_step(dev_bf16(c.q), kn, kn, pool, c.d_g, torch.from_numpy(c.table).cuda(),
                           torch.from_numpy(c.lens).cuda(), c.sm, out, num_splits=1)
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "int4"])
+def test_decode_step_more_requests_than_a_cta_has_threads(fmt):
+    # 150 requests: the balanced schedule finds the new-token jobs by its
+    # general scan (rounds over request blocks); then one CTA per unit
+    rng = np.random.default_rng(5)
+    lens = [int(x) for x in rng.integers(0, 70, 150)]
+    c = Case(fmt, 2, 4, 128, lens, 16, seed=11)
+    run_both(c, 0)
+    run_both(c, 1)
