@@ -42,6 +42,65 @@ def test_k8v4_write_bit_exact(D):
     assert diff.size == 0, f"{diff.size} bytes differ, first at {diff[:8]}"
 
 
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_k8v4_write_many_groups_per_cta(D):
+    # more row groups (8 warps of 32 / (D / 32) rows) than the resident grid
+    # has CTAs: each CTA loops over several, the next group's input in
+    # flight; a ragged last group
+    H, P = 4, 16
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    group = 8 * (32 // (D // 32))
+    T = 3 * (3 * sms // 2) * group // H + 7
+    pages = (T + P - 1) // P + 3
+    k, v = draws(T, H, D, D + 5, outlier=D // 3)
+    rng = np.random.default_rng(D + 6)
+    slots = rng.permutation(pages * P)[:T].astype(np.int64)
+    slots[::29] = -1
+    s_k = np.float32(0.04)
+    pool = guarded_pool("k8v4", pages, P, H, D, fill=0x3C)
+    K.kv4_k8v4_write(dev_bf16(k), dev_bf16(v), torch.from_numpy(slots).cuda(), pool,
+                     torch.tensor([s_k], dtype=torch.float32, device="cuda"))
+    torch.cuda.synchronize()
+    assert K.kv4_device_error() == 0
+    assert_guard_intact(pool.guard, "pool")
+    ref = KV.write(KV.new_pool(pages, P, H, D, fill=0x3C), P, H, k, v, slots, s_k)
+    got = pool.buffer.cpu().numpy()
+    diff = np.nonzero(got != ref)[0]
+    assert diff.size == 0, f"{diff.size} bytes differ, first at {diff[:8]}"
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_k8v4_write_signed_zeros(D):
+    # rows of +0, -0, +x and -x: the rotation makes exact zeros of both
+    # signs (-0 + -0 = -0, x + -x = +0), so the FP8 keys' sign of zero and
+    # the quotients of zero are checked; all-(+0) and all-(-0) rows too
+    H, P, T = 2, 16, 64
+    rng = np.random.default_rng(D + 9)
+    choices = np.array([0x0000, 0x8000, 0x3FC0, 0xBFC0], np.uint16)   # +0, -0, 1.5, -1.5
+    k = choices[rng.integers(0, 4, (T, H, D))]
+    v = choices[rng.integers(0, 4, (T, H, D))]
+    k[0], v[0] = 0x0000, 0x0000
+    k[1], v[1] = 0x8000, 0x8000
+    k[2, :, ::2], v[2, :, ::2] = 0x8000, 0x8000                         # -0 and +0 alternating
+    k[2, :, 1::2], v[2, :, 1::2] = 0x0000, 0x0000
+    slots = np.arange(T, dtype=np.int64)
+    s_k = np.float32(0.01)
+    pages = (T + P - 1) // P
+    pool = guarded_pool("k8v4", pages, P, H, D, fill=0x77)
+    K.kv4_k8v4_write(dev_bf16(k), dev_bf16(v), torch.from_numpy(slots).cuda(), pool,
+                     torch.tensor([s_k], dtype=torch.float32, device="cuda"))
+    torch.cuda.synchronize()
+    assert K.kv4_device_error() == 0
+    assert_guard_intact(pool.guard, "pool")
+    ref = KV.write(KV.new_pool(pages, P, H, D, fill=0x77), P, H, k, v, slots, s_k)
+    got = pool.buffer.cpu().numpy()
+    diff = np.nonzero(got != ref)[0]
+    assert diff.size == 0, f"{diff.size} bytes differ, first at {diff[:8]}"
+    # the case holds both signs of zero among the FP8 key codes
+    kc = ref.reshape(pages, H, -1)[:, :, :P * D].reshape(-1)
+    assert (kc == 0x80).any() and (kc == 0x00).any()
+
+
 def oracle_case(Hkv, Hq, D, lens, P, seed):
     rng = np.random.default_rng(seed)
     B = len(lens)
