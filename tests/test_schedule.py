@@ -83,3 +83,47 @@ def test_piece_slots_unique_and_covering():
                         continue          # CTA with an empty range holds no piece
                     assert (u, s, c) in real
             start += n_u
+
+
+def step_jobs(tiles_per_request, UPB, n_cta):
+    """kv4_decode_step's new-token jobs, per CTA, the way the kernel lists
+    them: request b's units occupy [start_b, start_b + UPB n_b) of the line
+    (n_b tiles each, in unit order), unit j's last tile is start_b + (j + 1)
+    n_b - 1, and CTA c writes the units whose last tile is in its range."""
+    T = UPB * sum(tiles_per_request)
+    jobs = {c: [] for c in range(n_cta)}
+    start = 0
+    for b, n_b in enumerate(tiles_per_request):
+        for c in range(n_cta):
+            c0, c1 = part_begin(c, T, n_cta), part_begin(c + 1, T, n_cta)
+            for j in range(UPB):
+                last = start + (j + 1) * n_b - 1
+                if n_b > 0 and c0 <= last < c1:
+                    jobs[c].append(b * UPB + j)
+        start += UPB * n_b
+    return jobs
+
+
+def test_step_jobs_owned_by_the_cta_that_decodes_the_last_tile():
+    rng = random.Random(1)
+    for _ in range(300):
+        reqs = [rng.choice([0, 1, 2, 3, 17, 200]) for _ in range(rng.randint(1, 40))]
+        UPB = rng.choice([1, 2, 4, 8])
+        n_cta = rng.choice([1, 3, 7, 152, 456])
+        jobs = step_jobs(reqs, UPB, n_cta)
+        owner = {}
+        for c, us in jobs.items():
+            for u in us:
+                assert u not in owner, "a new token written by two CTAs"
+                owner[u] = c
+        units = [n for n in reqs for _ in range(UPB)]
+        for u, n_u in enumerate(units):
+            if n_u == 0:
+                assert u not in owner            # an empty request writes nothing
+                continue
+            assert u in owner                    # every other unit's token is written
+        # the writer is the CTA whose piece holds the unit's last tile, so no
+        # other CTA loads that tile
+        for slot, u, s, c, t, n in pieces(units, n_cta, 1):
+            if t + n == units[u]:
+                assert owner[u] == c
