@@ -439,11 +439,26 @@ def max_over_ranks(pg, x, device=None):
     return float(t.item())
 
 
+def step_config(w, lens, splits, pool_bytes, world):
+    """The bench line's `config` for workload w (both arms print the same)."""
+    dec_bytes = algorithmic_decode_bytes(w, lens)
+    return {"workload": f"{w.name}: " + w.notes, "kv_heads": w.num_kv_heads, "q_heads": w.num_q_heads,
+            "head_dim": w.head_dim, "batch": w.batch, "page_size": w.page_size,
+            "seq_lens": [int(x) for x in lens], "num_splits": splits,
+            "kv_bytes_per_step": dec_bytes, "step_bytes": dec_bytes + algorithmic_write_bytes(w, w.batch),
+            "l2": "inputs larger than L2: the pool is %.0f MB vs 129 MB L2" % (pool_bytes / 1e6),
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
 def reference_arm(args):
     rank, world, local, pg = dist_setup(args)
     if rank != 0:
         return 0
     w = W.ALL[args.workload]
+    lens = w.seq_lens()
+    num_pages, _ = w.block_table(lens)
+    # the pool's bytes: num_pages chunks of P tokens per kv head
+    pool_bytes = num_pages * w.page_size * (algorithmic_decode_bytes(w, [1]) - w.num_q_heads * w.head_dim * 6)
     r = cpu_oracle_sample(w.name, 0, max_steps=args.warmup + args.steps)
     times = r["times"][args.warmup:]
     per = statistics.mean(times)
@@ -453,11 +468,10 @@ def reference_arm(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": per * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "sample": f"request 0, kv head 0 ({w.group} query heads), "
-                   f"{r['tokens']} tokens per step"},
+        "config": step_config(w, lens, w.num_splits, pool_bytes, world),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"one request x one kv head of {w.name}, {r['tokens']} tokens, "
-                                   f"{args.steps} timed steps"},
+                         "sample": f"one request x one kv head of {w.name} (request 0, kv head 0, "
+                                   f"{w.group} query heads, {r['tokens']} tokens), {args.steps} timed steps"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -621,12 +635,7 @@ def kv4_arm(args):
         "ms_per_step_as_write_then_decode": split_step * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16*f16+f32 (nvfp4 cache)",
         "data": "synthetic",
-        "config": {"workload": f"{w.name}: " + w.notes, "kv_heads": Hkv, "q_heads": Hq,
-                   "head_dim": D, "batch": B, "page_size": w.page_size,
-                   "seq_lens": [int(x) for x in s.lens], "num_splits": s.splits,
-                   "kv_bytes_per_step": dec_bytes, "step_bytes": step_bytes,
-                   "l2": "inputs larger than L2: the pool is %.0f MB vs 129 MB L2" % (s.pool.nbytes / 1e6),
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": step_config(w, s.lens, s.splits, s.pool.nbytes, world),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": recorded_traffic(w.name),
                      "ncu_dram_gbs": recorded_ncu_gbs(w.name),
