@@ -41,7 +41,7 @@ def _pools(c, keep, fill):
     return pools
 
 
-def run_both(c, num_splits, fill=0x5A):
+def run_both(c, num_splits, fill=0x5A, out_dtype=torch.float32):
     keep, k_new, v_new, slot_new = _split(c)
     p_ref, p_step = _pools(c, keep, fill)
     B = len(c.lens)
@@ -49,7 +49,7 @@ def run_both(c, num_splits, fill=0x5A):
     lens = torch.from_numpy(c.lens).cuda()
     q = dev_bf16(c.q)
     ws = K.alloc_workspace(B, c.Hq, c.D, num_splits)
-    out_ref = torch.full((B, c.Hq, c.D), float("nan"), dtype=torch.float32, device="cuda")
+    out_ref = torch.full((B, c.Hq, c.D), float("nan"), dtype=out_dtype, device="cuda")
     out_step = torch.full_like(out_ref, float("nan"))
     # the two calls: the new tokens' write, then the decode
     K.kv4_write(dev_bf16(k_new), dev_bf16(v_new), torch.from_numpy(slot_new).cuda(), p_ref, c.d_g)
@@ -113,3 +113,12 @@ def test_decode_step_more_requests_than_a_cta_has_threads(fmt):
     c = Case(fmt, 2, 4, 128, lens, 16, seed=11)
     run_both(c, 0)
     run_both(c, 1)
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "int4"])
+def test_decode_step_bf16_output(fmt):
+    c = Case(fmt, 2, 8, 128, [200, 31, 64], 32, seed=21)
+    # bitwise equal to the two calls' bf16 output (whose rounding the decode
+    # tests hold to one bf16 ulp of the FP32 result)
+    out = run_both(c, 0, out_dtype=torch.bfloat16)
+    assert out.dtype == torch.bfloat16 and torch.isfinite(out.float()).all()
