@@ -266,6 +266,32 @@ class Setup:
         return (0 if self.fused else 1) + 1 + (0 if self.splits == 1 else 1)
 
 
+def time_calls(run, iters, rounds=3):
+    """Mean GPU time of one call: `iters` back-to-back calls between two CUDA
+    events on the launching stream, after 3 warm-up calls; the median over
+    `rounds` such runs.  A bounded GPU delay (a fixed number of clock cycles,
+    about 75 us per call) is queued before the first event, so the host has
+    issued every call before the clock starts and no host time between calls
+    is counted."""
+    import torch
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    sleep = getattr(torch.cuda, "_sleep", None)
+    means = []
+    for _ in range(rounds):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if sleep is not None:
+            sleep(int(1_000_000 + 150_000 * iters))
+        a.record()
+        for _ in range(iters):
+            run()
+        b.record()
+        torch.cuda.synchronize()
+        means.append(a.elapsed_time(b) * 1e-3 / iters)
+    return statistics.median(means)
+
+
 def time_decode_only(s, iters):
     torch = s.torch
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
@@ -737,18 +763,7 @@ def time_prefix(s, w, peak, keep=False):
     def run():
         K.kv4_dequant_prefix(s.pool, s.g, table0, d_prefix, d_cu, n, s8, wk, wv)
 
-    for _ in range(3):
-        run()
-    torch.cuda.synchronize()
-    ts = []
-    for _ in range(10):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        run()
-        b.record()
-        torch.cuda.synchronize()
-        ts.append(a.elapsed_time(b) * 1e-3)
-    med = statistics.median(ts)
+    med = time_calls(run, 10)
     D = w.head_dim
     byts = n * w.num_kv_heads * (2 * (D // 2 + D // 16) + 2 * D)
     r = {"prefix_tokens": n, "us": med * 1e6, "gbs": byts / med / 1e9, "frac": byts / med / 1e9 / peak}
@@ -783,18 +798,7 @@ def time_extend(device, w, ws, tpeak, reps=5):
     def run():
         K.kv4_extend_attention(q, ck, cv, wk, wv, s8, pl, cp, cl, cc, C, w.sm_scale(), out, workspace=ws_ext)
 
-    for _ in range(3):
-        run()
-    torch.cuda.synchronize()
-    ts = []
-    for _ in range(reps):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        run()
-        b.record()
-        torch.cuda.synchronize()
-        ts.append(a.elapsed_time(b) * 1e-3)
-    med = statistics.median(ts)
+    med = time_calls(run, reps)
     fl = extend_flops(Lp, C, Hq, D)
     return {"prefix_tokens": Lp, "chunk_tokens": C, "ms": med * 1e3, "tflops": fl / med / 1e12,
             "frac": fl / med / 1e12 / tpeak, "unit": "TFLOP/s", "bound": "tensor",
@@ -830,20 +834,9 @@ def time_k8v4(device, w, peak, reps=20):
     def run():
         K.kv4_k8v4_decode_attention(q, pool, s_k, d_table, d_lens, w.sm_scale(), out, chunks, ws)
 
-    for _ in range(3):
-        run()
-    torch.cuda.synchronize()
-    ts = []
-    for _ in range(reps):
-        a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        run()
-        b2.record()
-        torch.cuda.synchronize()
-        ts.append(a.elapsed_time(b2) * 1e-3)
+    med = time_calls(run, reps)
     if K.kv4_device_error() != 0:
         raise RuntimeError("k8v4 decode flagged a device error")
-    med = statistics.median(ts)
     byts = int(np.sum(lens)) * Hkv * (D + D // 2 + 4) + 2 * B * Hq * D * 2
     return {"decode_us": med * 1e6, "gbs": byts / med / 1e9, "frac": byts / med / 1e9 / peak,
             "num_chunks": chunks, "kv_bytes": byts, "tokens_per_s_16_layers": B / (16 * med)}
@@ -851,8 +844,8 @@ def time_k8v4(device, w, peak, reps=20):
 
 def time_k8v4_write(device, peak, T=131072, Hkv=4, D=256, P=64):
     """Prefill write of T bf16 tokens into a k8v4 pool (Hadamard rotation,
-    FP8 keys, INT4 values): CUDA-event median of 10 calls after 3 warm-up
-    calls; bytes = bf16 K and V in + the pool rows out + the slots."""
+    FP8 keys, INT4 values): time_calls over 10 back-to-back calls; bytes =
+    bf16 K and V in + the pool rows out + the slots."""
     import torch
     import bit_paged_kv_kv4_gb300 as K
     gen = torch.Generator(device=device).manual_seed(11)
@@ -861,20 +854,9 @@ def time_k8v4_write(device, peak, T=131072, Hkv=4, D=256, P=64):
     pool = K.Pool("k8v4", (T + P - 1) // P, P, Hkv, D, device=device)
     slots = torch.arange(T, dtype=torch.int64, device=device)
     s_k = torch.tensor([W.fp8_scale_from_amax(float(k.abs().amax().float()))], dtype=torch.float32, device=device)
-    for _ in range(3):
-        K.kv4_k8v4_write(k, v, slots, pool, s_k)
-    torch.cuda.synchronize()
-    ts = []
-    for _ in range(10):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        K.kv4_k8v4_write(k, v, slots, pool, s_k)
-        b.record()
-        torch.cuda.synchronize()
-        ts.append(a.elapsed_time(b) * 1e-3)
+    med = time_calls(lambda: K.kv4_k8v4_write(k, v, slots, pool, s_k), 10)
     if K.kv4_device_error() != 0:
         raise RuntimeError("k8v4 write flagged a device error")
-    med = statistics.median(ts)
     byts = T * Hkv * (2 * D * 2 + D + D // 2 + 4) + T * 8
     return {"tokens": T, "us": med * 1e6, "gbs": byts / med / 1e9, "frac": byts / med / 1e9 / peak,
             "note": f"{T * Hkv * D * 4 / 1e6:.0f} MB in, {T * Hkv * (D + D // 2 + 4) / 1e6:.1f} MB out: larger than L2"}
@@ -892,18 +874,7 @@ def time_write_int4(device, peak, T=8192):
     pool = K.Pool("int4", (T + w.page_size - 1) // w.page_size, w.page_size, w.num_kv_heads, w.head_dim,
                   device=device)
     slots = torch.arange(T, dtype=torch.int64, device=device)
-    for _ in range(3):
-        K.kv4_write(k, v, slots, pool, None)
-    torch.cuda.synchronize()
-    ts = []
-    for _ in range(10):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        K.kv4_write(k, v, slots, pool, None)
-        b.record()
-        torch.cuda.synchronize()
-        ts.append(a.elapsed_time(b) * 1e-3)
-    med = statistics.median(ts)
+    med = time_calls(lambda: K.kv4_write(k, v, slots, pool, None), 10)
     byts = algorithmic_write_bytes(w, T)
     in_mb = T * w.num_kv_heads * w.head_dim * 2 * 2 / 1e6
     out_mb = (byts - T * w.num_kv_heads * w.head_dim * 2 * 2) / 1e6
@@ -921,18 +892,7 @@ def time_calibrate(device, peak, T=65536, Hkv=4, D=256):
     k = torch.randn((T, Hkv, D), generator=gen, device=device).to(torch.bfloat16)
     v = torch.randn((T, Hkv, D), generator=gen, device=device).to(torch.bfloat16)
     out = torch.empty(2, dtype=torch.float32, device=device)
-    for _ in range(3):
-        K.kv4_calibrate_global_scale(k, v, out)
-    torch.cuda.synchronize()
-    ts = []
-    for _ in range(10):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        K.kv4_calibrate_global_scale(k, v, out)
-        b.record()
-        torch.cuda.synchronize()
-        ts.append(a.elapsed_time(b) * 1e-3)
-    med = statistics.median(ts)
+    med = time_calls(lambda: K.kv4_calibrate_global_scale(k, v, out), 10)
     byts = 2 * T * Hkv * D * 2 + 8
     return {"tokens": T, "us": med * 1e6, "gbs": byts / med / 1e9, "frac": byts / med / 1e9 / peak}
 
@@ -940,7 +900,7 @@ def time_calibrate(device, peak, T=65536, Hkv=4, D=256):
 def time_write_prefill(s, w, peak, T=None):
     """Prefill write of T tokens (default: the workload's 8K chunk) of bf16
     K/V into a scratch pool of the workload's geometry, then the same from
-    FP8 K/V: CUDA-event medians of 10 calls after 3 warm-up calls."""
+    FP8 K/V: time_calls over 10 back-to-back calls each."""
     import torch
     K = s.K
     T = T or w.prefix_chunk
@@ -951,35 +911,13 @@ def time_write_prefill(s, w, peak, T=None):
     pool = K.Pool(w.fmt, (T + w.page_size - 1) // w.page_size, w.page_size, w.num_kv_heads, w.head_dim,
                   device=s.device)
     slots = torch.arange(T, dtype=torch.int64, device=s.device)
-    for _ in range(3):
-        K.kv4_write(k, v, slots, pool, s.g)
-    torch.cuda.synchronize()
-    ts = []
-    for _ in range(10):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        K.kv4_write(k, v, slots, pool, s.g)
-        b.record()
-        torch.cuda.synchronize()
-        ts.append(a.elapsed_time(b) * 1e-3)
-    med = statistics.median(ts)
+    med = time_calls(lambda: K.kv4_write(k, v, slots, pool, s.g), 10)
     byts = algorithmic_write_bytes(w, T)
     # the same write fed with FP8 K/V (the engine's form), per-tensor input scales
     codes, s_in = W.fp8_kv_codes(w.seed, T, w.num_kv_heads, w.head_dim, s.device)
     k8, v8 = codes[0].contiguous(), codes[1].contiguous()
     d_in = torch.from_numpy(s_in).to(s.device)
-    for _ in range(3):
-        K.kv4_write_fp8(k8, v8, d_in, slots, pool, s.g)
-    torch.cuda.synchronize()
-    t8 = []
-    for _ in range(10):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        K.kv4_write_fp8(k8, v8, d_in, slots, pool, s.g)
-        b.record()
-        torch.cuda.synchronize()
-        t8.append(a.elapsed_time(b) * 1e-3)
-    m8 = statistics.median(t8)
+    m8 = time_calls(lambda: K.kv4_write_fp8(k8, v8, d_in, slots, pool, s.g), 10)
     b8 = algorithmic_write_bytes(w, T, in_bytes=1)
     in_mb = T * w.num_kv_heads * w.head_dim * 2 * 2 / 1e6
     out_mb = (byts - T * w.num_kv_heads * w.head_dim * 2 * 2) / 1e6
