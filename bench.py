@@ -937,7 +937,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the 160K / 1M / INT4 lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--only", choices=("prefix", "write", "extend", "k8v4"),
+    ap.add_argument("--only", choices=("prefix", "write", "extend", "k8v4", "calibrate"),
                     help="time just the 160K prefix dequant or the 8K prefill write and print "
                          "its line (for profiling one kernel)")
     args = ap.parse_args()
@@ -962,6 +962,8 @@ def only_arm(args):
     elif args.only == "k8v4":
         r = time_k8v4(device, W.ALL["nvfp4_32k"], peak)
         r["write_128k"] = time_k8v4_write(device, peak)
+    elif args.only == "calibrate":
+        r = time_calibrate(device, peak)
     elif args.only == "extend":
         r, ws = time_prefix(Setup(w, device), w, peak, keep=True)
         r = time_extend(device, w, ws, read_tensor_peak()[0], reps=args.steps)
