@@ -307,9 +307,21 @@ __device__ __forceinline__ void write_new_token(const DecodeArgs& a, const int4 
       for (int i = 0; i < E; ++i) q[i] = qe[i];
       nib = int4x8(q);
     }
-    uint8_t* codes = chunk + static_cast<int64_t>(kind) * a.P * RB + static_cast<int64_t>(off) * RB + lane * (E / 2);
+    if (kind == 0) {
+      uint8_t* codes = chunk + static_cast<int64_t>(off) * RB + lane * (E / 2);
 #pragma unroll
-    for (int i = 0; i < E / 2; ++i) codes[i] = static_cast<uint8_t>(nib >> (8 * i));
+      for (int i = 0; i < E / 2; ++i) codes[i] = static_cast<uint8_t>(nib >> (8 * i));
+    } else {
+      // V: pair row off / 2, this token's 16-bit halves (elements 4k .. 4k+3
+      // in the low half of word k for an even token, the high half for an
+      // odd one); byte i holds elements e, e + 1 with e = lane E + 2i
+      uint8_t* row = chunk + static_cast<int64_t>(a.P) * RB + static_cast<int64_t>(off >> 1) * D + 2 * (off & 1);
+#pragma unroll
+      for (int i = 0; i < E / 2; ++i) {
+        const int e = lane * E + 2 * i;
+        row[4 * (e >> 2) + ((e & 3) >> 1)] = static_cast<uint8_t>(nib >> (8 * i));
+      }
+    }
     if (lane == 0) reinterpret_cast<float*>(chunk + static_cast<int64_t>(a.P) * D)[static_cast<int64_t>(kind) * a.P + off] = sc;
   }
 }
@@ -486,7 +498,9 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
   const uint32_t vp_off0 = Gm::CS + swz<RB>(2 * tig + D0 / RB, D0 % RB);
   const uint32_t vp_off1 = Gm::CS + swz<RB>(2 * tig + D0 / RB, D0 % RB + 16);
   const uint32_t vps_off = kTT * SB + tig * (D / 8) + 2 * (D0 / 16);
-  // INT4 V (token rows): VB bytes at VB grp of rows 2tig, 2tig+1 (+8).
+  // INT4 V takes the same pair-row offsets (word j of a pair row holds dims
+  // 4j .. 4j+3 of both tokens).  k8v4 V (token rows): VB bytes at VB grp of
+  // rows 2tig, 2tig+1 (+8).
   const uint32_t v_offa = Gm::CSK + swz<RB>(2 * tig, VB * grp);
   const uint32_t v_offb = Gm::CSK + swz<RB>(2 * tig + 1, VB * grp);
   // k8v4 K (FP8, KH lines of KHB bytes a token): the 16-byte units of bytes
@@ -984,6 +998,32 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
               }
             }
           }
+        } else if constexpr (FMT == KV4_INT4_PTH) {
+          // INT4 V in token-pair rows, interleaved by 16-bit halves: word j of
+          // the thread's span holds dims D0 + 4j .. 4j+3 of both tokens, so a
+          // shift by 0 or 8 bits lines up two dims of the two tokens in the
+          // halves; the per-token V scale rides on the weight
+          constexpr int W = D0S / 4, CW = VCW < W ? VCW : W;
+#pragma unroll
+          for (int c0 = 0; c0 < W; c0 += CW) {
+            const uint32_t vo = st + ((c0 >> 2) ? vp_off1 : vp_off0) + 4 * (c0 & 3);
+            uint32_t wab[CW], wcd[CW];
+            load_bytes<4 * CW>(vo, wab);
+            load_bytes<4 * CW>(vo + 8 * RB, wcd);
+#pragma unroll
+            for (int jj = 0; jj < CW; ++jj) {
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                const int mi = 2 * (c0 + jj) + hh;         // dims D0 + 2mi, D0 + 2mi + 1
+                const uint32_t xa = hh ? wab[jj] >> 8 : wab[jj];
+                const uint32_t xc = hh ? wcd[jj] >> 8 : wcd[jj];
+                const uint32_t a0 = int4_lo_pair(xa), a1 = int4_hi_pair(xa);
+                const uint32_t a2 = int4_lo_pair(xc), a3 = int4_hi_pair(xc);
+                mma_f16_16816(o[mi], a0, a1, a2, a3, pb[0], pb[1]);
+                mma_f16_16816(o[mi], a0, a1, a2, a3, pl[0], pl[1]);
+              }
+            }
+          }
         } else {
           constexpr int W = VB / 4, CW = W < 2 ? W : 2;
 #pragma unroll
@@ -1086,10 +1126,10 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
           l += (mw == -INFINITY) ? 0.f : sMeta[(w * 8 + g) * 3 + 2] * fast_exp2(mw - Mx);
         }
         // (d, g) lives in lane (grp, tig) with tig = g/2 and grp the group that
-        // holds dim chunk q = (d/2) / VB (q for INT4, pi^-1(q) for NVFP4), in
+        // holds dim chunk q = (d/2) / VB (q for k8v4, pi^-1(q) for NVFP4 and INT4), in
         // o[mi][g%2] with mi = (d/2) % VB; d+1 in o[mi][g%2 + 2]; d+2, d+3 in o[mi+1].
         const int hd = d >> 1, mi = hd % VB, c = g & 1;
-        const int q = hd / VB, gq = (FMT == KV4_NVFP4) ? 2 * (q & 3) + (q >> 2) : q;
+        const int q = hd / VB, gq = (FMT != KV4_K8V4) ? 2 * (q & 3) + (q >> 2) : q;
         const float* row = sAcc + (gq * 4 + (g >> 1)) * Gm::AS + 4 * mi + c;
         const float4 acc = make_float4(row[0], row[2], row[4], row[6]);
         if (direct) {

@@ -161,13 +161,14 @@ __device__ __forceinline__ void prefix_walk(const PrefixArgs& a, uint32_t items,
   constexpr int TPR = D / 64;                   // threads per row
   constexpr int RB = D / 2, SB = D / 16;
   constexpr bool VP = FMT == KV4_NVFP4 && kind == 1;   // NVFP4 V: token-pair rows
+  constexpr bool VP16 = FMT == KV4_INT4_PTH && kind == 1;   // INT4 V: pair rows by 16-bit halves
   const float r8 = __frcp_rn(s8);
   // Two-deep software pipeline: the next item's block-table entry and code
   // loads are in flight while this item is converted and stored.
   struct Item {
-    uint4 c[VP ? 4 : 2]; // codes: 32 bytes, or the 64 of an NVFP4 V pair row
+    uint4 c[VP || VP16 ? 4 : 2]; // codes: 32 bytes, or the 64 of a V pair-row span
     uint2 sw;            // scale bytes (NVFP4) or the row scale's bits (INT4, in .x)
-    int sh;              // NVFP4 V: this token's nibble within the pair byte
+    int sh;              // V pair rows: this token's place in the pair (off % 2)
     bool ok;             // false: nothing to do
   };
   auto load = [&](uint32_t i, Item& it) {
@@ -195,6 +196,16 @@ __device__ __forceinline__ void prefix_walk(const PrefixArgs& a, uint32_t items,
       for (int j = 0; j < 4; ++j) it.c[j] = src[j];
       it.sw = *reinterpret_cast<const uint2*>(chunk + static_cast<int64_t>(a.P) * D + static_cast<int64_t>(a.P) * SB +
                                               static_cast<int64_t>(off >> 1) * 2 * SB + part * 8);
+      it.sh = off & 1;
+    } else if constexpr (VP16) {
+      // INT4 V in token pairs: word k of pair row off/2 holds the token's
+      // 16-bit chunk k in its half off%2; the row scale stays per token
+      const uint4* src = reinterpret_cast<const uint4*>(
+          chunk + static_cast<int64_t>(a.P) * RB + static_cast<int64_t>(off >> 1) * D + part * 64);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) it.c[j] = src[j];
+      it.sw.x = *reinterpret_cast<const uint32_t*>(chunk + static_cast<int64_t>(a.P) * D +
+                                                   (static_cast<int64_t>(a.P) + off) * 4);
       it.sh = off & 1;
     } else {
       const uint4* src = reinterpret_cast<const uint4*>(chunk + static_cast<int64_t>(kind) * a.P * RB +
@@ -262,8 +273,21 @@ __device__ __forceinline__ void prefix_walk(const PrefixArgs& a, uint32_t items,
           f2_split(mul_f2(f2(static_cast<float>(k - 8), static_cast<float>(k - 7)), ss), xn[k], xn[k + 1]);
         }
         const uint2 tp = e4m3_table(xp, s8, r8, in_range), tn = e4m3_table(xn, s8, r8, in_range);
-        const uint32_t cw[8] = {cur.c[0].x, cur.c[0].y, cur.c[0].z, cur.c[0].w,
-                                cur.c[1].x, cur.c[1].y, cur.c[1].z, cur.c[1].w};
+        uint32_t cw[8];
+        if constexpr (VP16) {
+          // the token's code words back from its halves of the pair words
+          const uint32_t sel = cur.sh ? 0x7632u : 0x5410u;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            cw[2 * j] = prmt(cur.c[j].x, cur.c[j].y, sel);
+            cw[2 * j + 1] = prmt(cur.c[j].z, cur.c[j].w, sel);
+          }
+        } else {
+          const uint32_t c8[8] = {cur.c[0].x, cur.c[0].y, cur.c[0].z, cur.c[0].w,
+                                  cur.c[1].x, cur.c[1].y, cur.c[1].z, cur.c[1].w};
+#pragma unroll
+          for (int j = 0; j < 8; ++j) cw[j] = c8[j];
+        }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const uint2 lo = int4_word(tp, tn, cw[2 * j]), hi = int4_word(tp, tn, cw[2 * j + 1]);

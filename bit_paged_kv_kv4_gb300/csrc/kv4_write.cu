@@ -390,11 +390,12 @@ __device__ __forceinline__ void write_unit(const WriteArgs& a, uint32_t u, bool 
                                   16 * b) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   } else {
+    uint2 word[2];                    // token k's codes, element i in nibble i
+    float sc[2];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
       float x[16];
       elems(k, x);
-      const Dest d = dest(k);
       // row amax over the D/16 threads of the row (aligned groups of a warp)
       float amax = 0.f;
 #pragma unroll
@@ -402,18 +403,51 @@ __device__ __forceinline__ void write_unit(const WriteArgs& a, uint32_t u, bool 
 #pragma unroll
       for (int o = 1; o < NB; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
       const float s = div7(amax);
-      uint2 word = make_uint2(0u, 0u);
+      word[k] = make_uint2(0u, 0u);
       if (s != 0.f) {
         const float rs = __frcp_rn(s);
         float q[16];
         div16(x, s, rs, amax, q);
-        word = make_uint2(int4x8(q), int4x8(q + 8));
+        word[k] = make_uint2(int4x8(q), int4x8(q + 8));
       }
-      if (d.ok) {
-        uint8_t* codes = d.chunk + static_cast<int64_t>(kind) * a.P * RB + static_cast<int64_t>(d.off) * RB;
-        *reinterpret_cast<uint2*>(codes + 8 * b) = word;
-        if (b == 0)
-          reinterpret_cast<float*>(d.chunk + static_cast<int64_t>(a.P) * D)[static_cast<int64_t>(kind) * a.P + d.off] = s;
+      sc[k] = s;
+    }
+    const Dest d0 = dest(0), d1 = dest(1);
+    auto put_scale = [&](const Dest& d, float s) {
+      if (b == 0)
+        reinterpret_cast<float*>(d.chunk + static_cast<int64_t>(a.P) * D)[static_cast<int64_t>(kind) * a.P + d.off] = s;
+    };
+    if constexpr (kind == 0) {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const Dest& d = k == 0 ? d0 : d1;
+        if (!d.ok) continue;
+        *reinterpret_cast<uint2*>(d.chunk + static_cast<int64_t>(d.off) * RB + 8 * b) = word[k];
+        put_scale(d, sc[k]);
+      }
+    } else if (d0.ok && d1.ok && (d0.slot & 1) == 0 && d1.slot == d0.slot + 1) {
+      // both tokens of one pair row: word 4b + c holds 16-bit chunk c
+      // (elements 4c .. 4c+3 of this block) of token 2p low, of 2p+1 high
+      *reinterpret_cast<uint4*>(d0.chunk + static_cast<int64_t>(a.P) * RB + static_cast<int64_t>(d0.off >> 1) * D +
+                                16 * b) =
+          make_uint4(prmt(word[0].x, word[1].x, 0x5410u), prmt(word[0].x, word[1].x, 0x7632u),
+                     prmt(word[0].y, word[1].y, 0x5410u), prmt(word[0].y, word[1].y, 0x7632u));
+      put_scale(d0, sc[0]);
+      put_scale(d1, sc[1]);
+    } else {
+      // a token alone in its pair row (in this thread): its own 16-bit
+      // halves, bytes no other token writes, one 2-byte store each
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const Dest& d = k == 0 ? d0 : d1;
+        if (!d.ok) continue;
+        uint16_t* dst = reinterpret_cast<uint16_t*>(d.chunk + static_cast<int64_t>(a.P) * RB +
+                                                    static_cast<int64_t>(d.off >> 1) * D + 16 * b + 2 * (d.off & 1));
+        dst[0] = static_cast<uint16_t>(word[k].x);
+        dst[2] = static_cast<uint16_t>(word[k].x >> 16);
+        dst[4] = static_cast<uint16_t>(word[k].y);
+        dst[6] = static_cast<uint16_t>(word[k].y >> 16);
+        put_scale(d, sc[k]);
       }
     }
   }

@@ -60,11 +60,15 @@
  *     INT4 : [K codes P*D/2][V codes P*D/2][K scale f32 * P][V scale f32 * P]
  *     FP8  : [K codes P*D]  [V codes P*D]
  *   chunk_bytes = P*(D + D/8) (NVFP4), P*(D + 8) (INT4), P*2*D (FP8).
- *   Row `off` of a region belongs to token `off` of the page, except NVFP4 V,
- *   stored in token pairs: byte d of pair row p (D bytes) holds element d of
- *   token 2p in its low nibble and of token 2p+1 in its high nibble, and the
- *   pair's scale row (D/8 bytes) holds block b's scale of token 2p+i at byte
- *   2b+i.  A slot is page * P + off.  The FP32 scales are not in the pool:
+ *   Row `off` of a region belongs to token `off` of the page, except the V
+ *   codes of NVFP4 and INT4, stored in token pairs.  NVFP4: byte d of pair
+ *   row p (D bytes) holds element d of token 2p in its low nibble and of
+ *   token 2p+1 in its high nibble, and the pair's scale row (D/8 bytes)
+ *   holds block b's scale of token 2p+i at byte 2b+i.  INT4: 32-bit word k
+ *   of pair row p (D bytes) holds elements 4k .. 4k+3 of token 2p in its low
+ *   16 bits and of token 2p+1 in its high 16 bits (element 4k+i in nibble i
+ *   of the half); INT4 V scales stay one FP32 per token.  A slot is
+ *   page * P + off.  The FP32 scales are not in the pool:
  *   callers pass them as a device float[2] = {g_K, g_V} per layer.
  *
  * Conventions for every entry point:

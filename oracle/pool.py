@@ -20,16 +20,24 @@ so chunk_bytes = P*(D + D/8) for NVFP4, P*(D + 8) for INT4, P*2*D for FP8.
 
 Row order inside a region:
 
-* K codes and scales, and every INT4 and FP8 region: token ``off`` of the
-  page owns row ``off`` (D/2 code bytes, element 2j in the low nibble of
-  byte j; D/16 scale bytes, or one FP32 scale; FP8: D code bytes, element d
-  in byte d).
+* K codes and scales, INT4 V scales and every FP8 region: token ``off`` of
+  the page owns row ``off`` (D/2 code bytes, element 2j in the low nibble
+  of byte j; D/16 scale bytes, or one FP32 scale; FP8: D code bytes,
+  element d in byte d).
 * NVFP4 V: tokens are stored in pairs (2p, 2p+1).  Code byte d of pair row p
   (D bytes) holds element d of token 2p in its low nibble and element d of
   token 2p+1 in its high nibble; scale byte 2*blk + i of pair row p (D/8
   bytes) is block blk of token 2p+i.  A decode kernel contracts V over
   tokens, so its tensor-core operands pair two tokens of one element: this
   order hands it those pairs as they are stored.  Sizes are unchanged.
+* INT4 V codes: also in token pairs, interleaved by 16-bit halves.  Pair
+  row p (D bytes) is D/8 words of 4 bytes; word k holds elements 4k .. 4k+3
+  of token 2p in its low half and of token 2p+1 in its high half (element
+  4k+i in nibble i of the half).  Bytes 2k, 2k+1 of a token's packed row
+  are bytes 4k + 2i, 4k + 2i + 1 of the pair row, i = off % 2.  A decode
+  kernel's shift by 4 or 8 bits of such a word lines up one element of both
+  tokens in the two halves of a 32-bit register, the form its INT4 -> f16
+  conversion takes.
 
 A slot is ``page * P + off``; a negative slot means "do not store".
 
@@ -98,6 +106,22 @@ def _pair_v(spec):
     return spec.fmt == NVFP4
 
 
+def _pair_v16(spec):
+    return spec.fmt == INT4
+
+
+def _v_pair16_codes_index(spec, page, off, head):
+    """INT4 V codes: [N, D/2] byte indices of the packed bytes of tokens
+    (page, off) inside their pair rows (byte 2k + j of the token's packed row
+    at 4k + 2 (off % 2) + j of the pair row)."""
+    off = np.asarray(off, np.int64)
+    D = spec.head_dim
+    j = np.arange(D // 2, dtype=np.int64)
+    col = 4 * (j // 2) + (j % 2)
+    base = spec.chunk_offset(page, head) + spec.region("vc") + (off // 2) * D + 2 * (off & 1)
+    return base[:, None] + col[None, :]
+
+
 def _v_pair_codes_index(spec, page, off, head):
     """NVFP4 V codes: [N, D] byte indices of the pair rows of tokens (page,
     off) and [N] nibble shifts (0 for even tokens, 4 for odd)."""
@@ -122,6 +146,8 @@ def get_codes(pool, spec, page, off, head, kind):
         idx, sh = _v_pair_codes_index(spec, page, off, head)
         nib = (pool[idx] >> sh[:, None].astype(np.uint8)) & 0xF
         return (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8)
+    if kind == "v" and _pair_v16(spec):
+        return pool[_v_pair16_codes_index(spec, page, off, head)]
     return pool[_row_index(spec, page, off, head, kind + "c")]
 
 
@@ -146,6 +172,10 @@ def put_rows(pool, spec, page, off, head, kind, codes, scales):
             old = pool[idx[r]]
             pool[idx[r]] = (old & np.uint8(0xF0 >> s)) | (nib[r] << np.uint8(s))
         pool[_v_pair_scales_index(spec, page, off, head)] = scales
+        return
+    if kind == "v" and _pair_v16(spec):
+        pool[_v_pair16_codes_index(spec, page, off, head)] = codes     # the token's own bytes only
+        pool[_row_index(spec, page, off, head, "vs")] = scales
         return
     pool[_row_index(spec, page, off, head, kind + "c")] = codes
     pool[_row_index(spec, page, off, head, kind + "s")] = scales

@@ -244,6 +244,43 @@ def test_nvfp4_error_within_half_step_when_unsaturated():
     assert np.all(err[~ok] <= (t[~ok] - 6) * (1 + 1e-6))
 
 
+def test_int4_bruteforce_tiny_by_hand():
+    """INT4, D = 16, 3 tokens: read every code at the position the layout
+    gives (K in token rows; V in token-pair rows by 16-bit halves) with its
+    per-token FP32 scale and expand the attention with Python loops."""
+    spec, pool, table, lens, g, q, Ks, Vs = build("int4", 1, 16, [3], 16, seed=3, Hq=2)
+    sm = np.float32(0.25)
+    got = A.decode_attention(q, pool, spec, g, table, lens, sm)
+    page = int(table[0, 0])
+    base = page * spec.chunk_bytes
+
+    def signed(n):
+        return n - 16 if n >= 8 else n
+
+    def row(kind, t):
+        s = float(pool[base + spec.region(kind + "s") + 4 * t:base + spec.region(kind + "s") + 4 * t + 4]
+                  .view(np.float32)[0])
+        vals = []
+        for d in range(16):
+            if kind == "k":
+                byte = int(pool[base + spec.region("kc") + t * 8 + d // 2])
+            else:
+                # pair row t//2 (16 bytes): word d//4 holds elements 4k..4k+3 of the
+                # even token in its low half and of the odd token in its high half
+                byte = int(pool[base + spec.region("vc") + (t // 2) * 16 + 4 * (d // 4) + 2 * (t % 2) +
+                                (d % 4) // 2])
+            vals.append(signed((byte >> (4 * (d % 2))) & 0xF) * s)
+        return vals
+
+    for j in range(2):
+        qq = [float(x) for x in F.bf16_to_f32(q[0, j])]
+        sc = [float(sm) * sum(a * b for a, b in zip(qq, row("k", t))) for t in range(3)]
+        mx = max(sc)
+        w = [math.exp(x - mx) for x in sc]
+        out = [sum(w[t] * row("v", t)[d] for t in range(3)) / sum(w) for d in range(16)]
+        assert np.allclose(got[0, j], out, rtol=1e-13, atol=1e-15)
+
+
 def test_fp8_bruteforce_tiny_by_hand():
     """FP8 pool, D = 16, 3 tokens: read every code byte at the position the
     layout gives (token rows of D bytes), decode it with torch's float8 view

@@ -217,7 +217,14 @@ def test_pool_write_places_rows_by_slot():
                             written[at, :] = True
                     else:
                         for d in range(D):
-                            at = base + reg[kind + "c"] + off * (D // 2) + d // 2
+                            if kind == "v":
+                                # INT4 V: pair row off//2 of D bytes; word d//4 holds
+                                # elements 4k..4k+3 of token 2p in its low 16 bits and
+                                # of token 2p+1 in its high 16 bits, element 4k+i in
+                                # nibble i of the half
+                                at = base + reg["vc"] + (off // 2) * D + 4 * (d // 4) + 2 * (off % 2) + (d % 4) // 2
+                            else:
+                                at = base + reg[kind + "c"] + off * (D // 2) + d // 2
                             assert (pool[at] >> (4 * (d % 2))) & 0xF == nib[d]
                             written[at, d % 2] = True
                         for i in range(W):
