@@ -389,7 +389,34 @@ __device__ __forceinline__ void write_unit(const WriteArgs& a, uint32_t u, bool 
         *reinterpret_cast<uint4*>(d.chunk + static_cast<int64_t>(kind) * a.P * D + static_cast<int64_t>(d.off) * D +
                                   16 * b) = make_uint4(w[0], w[1], w[2], w[3]);
     }
+  } else if constexpr (kind == 0) {
+    // K: token rows, each token stored as soon as it is encoded
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      float x[16];
+      elems(k, x);
+      const Dest d = dest(k);
+      // row amax over the D/16 threads of the row (aligned groups of a warp)
+      float amax = 0.f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(x[j]));
+#pragma unroll
+      for (int o = 1; o < NB; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const float s = div7(amax);
+      uint2 word = make_uint2(0u, 0u);
+      if (s != 0.f) {
+        const float rs = __frcp_rn(s);
+        float q[16];
+        div16(x, s, rs, amax, q);
+        word = make_uint2(int4x8(q), int4x8(q + 8));
+      }
+      if (d.ok) {
+        *reinterpret_cast<uint2*>(d.chunk + static_cast<int64_t>(d.off) * RB + 8 * b) = word;
+        if (b == 0) reinterpret_cast<float*>(d.chunk + static_cast<int64_t>(a.P) * D)[d.off] = s;
+      }
+    }
   } else {
+    // V: both tokens encoded, then stored into their pair rows
     uint2 word[2];                    // token k's codes, element i in nibble i
     float sc[2];
 #pragma unroll
@@ -414,18 +441,9 @@ __device__ __forceinline__ void write_unit(const WriteArgs& a, uint32_t u, bool 
     }
     const Dest d0 = dest(0), d1 = dest(1);
     auto put_scale = [&](const Dest& d, float s) {
-      if (b == 0)
-        reinterpret_cast<float*>(d.chunk + static_cast<int64_t>(a.P) * D)[static_cast<int64_t>(kind) * a.P + d.off] = s;
+      if (b == 0) reinterpret_cast<float*>(d.chunk + static_cast<int64_t>(a.P) * D)[a.P + d.off] = s;
     };
-    if constexpr (kind == 0) {
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const Dest& d = k == 0 ? d0 : d1;
-        if (!d.ok) continue;
-        *reinterpret_cast<uint2*>(d.chunk + static_cast<int64_t>(d.off) * RB + 8 * b) = word[k];
-        put_scale(d, sc[k]);
-      }
-    } else if (d0.ok && d1.ok && (d0.slot & 1) == 0 && d1.slot == d0.slot + 1) {
+    if (d0.ok && d1.ok && (d0.slot & 1) == 0 && d1.slot == d0.slot + 1) {
       // both tokens of one pair row: word 4b + c holds 16-bit chunk c
       // (elements 4c .. 4c+3 of this block) of token 2p low, of 2p+1 high
       *reinterpret_cast<uint4*>(d0.chunk + static_cast<int64_t>(a.P) * RB + static_cast<int64_t>(d0.off >> 1) * D +
