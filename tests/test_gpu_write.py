@@ -142,9 +142,10 @@ def test_write_fp8_input_bit_exact(fmt, D):
 @pytest.mark.parametrize("fmt", ["nvfp4", "int4"])
 @pytest.mark.parametrize("D", [64, 256])
 def test_write_pair_rows_every_slot_pattern(fmt, D):
-    """A thread writes tokens 2p and 2p+1 of the call; NVFP4 V stores both
-    halves of a pair row with plain stores only when they land in one, and
-    otherwise sets each token's nibbles atomically, keeping its partner's.
+    """A thread writes tokens 2p and 2p+1 of the call; NVFP4 and INT4 V
+    store both halves of a pair row at once only when they land in one, and
+    otherwise write each token's own part (NVFP4: its nibbles, set
+    atomically; INT4: its 16-bit halves), keeping its partner's.
     One call mixes: an aligned run (plain stores), a run starting at an odd
     offset, pair rows whose halves come from non-adjacent tokens, a reversed
     pair, a skipped token beside a written partner, and an odd token count
