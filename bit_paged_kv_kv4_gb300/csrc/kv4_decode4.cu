@@ -495,14 +495,12 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
   // quarter-warp read pair-row halves of opposite parity (distinct banks).
   constexpr int D0S = D / 8;
   const int D0 = D0S * (4 * (grp & 1) + (grp >> 1));
-  const uint32_t vp_off0 = Gm::CS + swz<RB>(2 * tig + D0 / RB, D0 % RB);
-  const uint32_t vp_off1 = Gm::CS + swz<RB>(2 * tig + D0 / RB, D0 % RB + 16);
+  const uint32_t vp_off0 = Gm::CSK + swz<RB>(2 * tig + D0 / RB, D0 % RB);
+  const uint32_t vp_off1 = Gm::CSK + swz<RB>(2 * tig + D0 / RB, D0 % RB + 16);
   const uint32_t vps_off = kTT * SB + tig * (D / 8) + 2 * (D0 / 16);
-  // INT4 V takes the same pair-row offsets (word j of a pair row holds dims
-  // 4j .. 4j+3 of both tokens).  k8v4 V (token rows): VB bytes at VB grp of
-  // rows 2tig, 2tig+1 (+8).
-  const uint32_t v_offa = Gm::CSK + swz<RB>(2 * tig, VB * grp);
-  const uint32_t v_offb = Gm::CSK + swz<RB>(2 * tig + 1, VB * grp);
+  // INT4 and k8v4 V take the same pair-row offsets (word j of a pair row
+  // holds dims 4j .. 4j+3 of both tokens); V starts after the tile's K
+  // bytes (CSK = CS but for k8v4, whose FP8 key rows are D bytes).
   // k8v4 K (FP8, KH lines of KHB bytes a token): the 16-byte units of bytes
   // [KB tig, KB (tig + 1)) of token grp; token grp + 8 is 8 KRB bytes on (the
   // swizzle pattern repeats every 8 lines).
@@ -998,8 +996,8 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
               }
             }
           }
-        } else if constexpr (FMT == KV4_INT4_PTH) {
-          // INT4 V in token-pair rows, interleaved by 16-bit halves: word j of
+        } else {
+          // INT4 / k8v4 V in token-pair rows, by 16-bit halves: word j of
           // the thread's span holds dims D0 + 4j .. 4j+3 of both tokens, so a
           // shift by 0 or 8 bits lines up two dims of the two tokens in the
           // halves; the per-token V scale rides on the weight
@@ -1019,30 +1017,6 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
                 const uint32_t xc = hh ? wcd[jj] >> 8 : wcd[jj];
                 const uint32_t a0 = int4_lo_pair(xa), a1 = int4_hi_pair(xa);
                 const uint32_t a2 = int4_lo_pair(xc), a3 = int4_hi_pair(xc);
-                mma_f16_16816(o[mi], a0, a1, a2, a3, pb[0], pb[1]);
-                mma_f16_16816(o[mi], a0, a1, a2, a3, pl[0], pl[1]);
-              }
-            }
-          }
-        } else {
-          constexpr int W = VB / 4, CW = W < 2 ? W : 2;
-#pragma unroll
-          for (int c0 = 0; c0 < W; c0 += CW) {
-            uint32_t wa[CW], wb[CW], wc[CW], wd[CW];
-            load_bytes<4 * CW>(st + v_offa + 4 * c0, wa);
-            load_bytes<4 * CW>(st + v_offb + 4 * c0, wb);
-            load_bytes<4 * CW>(st + v_offa + 8 * RB + 4 * c0, wc);
-            load_bytes<4 * CW>(st + v_offb + 8 * RB + 4 * c0, wd);
-#pragma unroll
-            for (int jj = 0; jj < CW; ++jj) {
-#pragma unroll
-              for (int mm = 0; mm < 4; ++mm) {
-                const int mi = 4 * (c0 + jj) + mm;
-                const uint32_t sel = mm | (mm << 4) | ((4 + mm) << 8) | ((4 + mm) << 12);
-                const uint32_t xab = prmt(wa[jj], wb[jj], sel);
-                const uint32_t xcd = prmt(wc[jj], wd[jj], sel);
-                const uint32_t a0 = int4_lo_pair(xab), a1 = int4_hi_pair(xab);
-                const uint32_t a2 = int4_lo_pair(xcd), a3 = int4_hi_pair(xcd);
                 mma_f16_16816(o[mi], a0, a1, a2, a3, pb[0], pb[1]);
                 mma_f16_16816(o[mi], a0, a1, a2, a3, pl[0], pl[1]);
               }
@@ -1126,10 +1100,10 @@ decode4_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap cmap,
           l += (mw == -INFINITY) ? 0.f : sMeta[(w * 8 + g) * 3 + 2] * fast_exp2(mw - Mx);
         }
         // (d, g) lives in lane (grp, tig) with tig = g/2 and grp the group that
-        // holds dim chunk q = (d/2) / VB (q for k8v4, pi^-1(q) for NVFP4 and INT4), in
+        // holds dim chunk q = (d/2) / VB (pi^-1(q) for every format), in
         // o[mi][g%2] with mi = (d/2) % VB; d+1 in o[mi][g%2 + 2]; d+2, d+3 in o[mi+1].
         const int hd = d >> 1, mi = hd % VB, c = g & 1;
-        const int q = hd / VB, gq = (FMT != KV4_K8V4) ? 2 * (q & 3) + (q >> 2) : q;
+        const int q = hd / VB, gq = 2 * (q & 3) + (q >> 2);
         const float* row = sAcc + (gq * 4 + (g >> 1)) * Gm::AS + 4 * mi + c;
         const float4 acc = make_float4(row[0], row[2], row[4], row[6]);
         if (direct) {

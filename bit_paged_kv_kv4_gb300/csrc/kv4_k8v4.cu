@@ -16,7 +16,8 @@
 // match the test oracle's; the divisions take Markstein's correction step
 // (the IEEE quotient) and the INT4 codes the round-to-nearest-even magic
 // addition, as in kv4_write.cu.
-// Chunk of P tokens: [K codes P*D][V codes P*D/2][V scales FP32 * P].
+// Chunk of P tokens: [K codes P*D][V codes P*D/2][V scales FP32 * P], the V
+// codes in token-pair rows by 16-bit halves as in the INT4 pool.
 //
 // Decode runs the NVFP4 / INT4 decode kernel (kv4_decode4.cu) with FP8 keys:
 // q is rotated the same way (q_rot . k_rot = q . k), the softmax runs over
@@ -235,7 +236,9 @@ __global__ void __launch_bounds__(256) k8v4_write_kernel(const K8V4WriteArgs a) 
     }
   } else {
     const float s = div7(amax);                           // RN(amax / 7)
-    uint8_t* codes = chunk + static_cast<int64_t>(a.P) * D + static_cast<int64_t>(off) * (D / 2);
+    // V codes in token-pair rows by 16-bit halves: elements e .. e+3 (e a
+    // multiple of 4) of this token at byte e + 2 (off % 2) of pair row off / 2
+    uint8_t* codes = chunk + static_cast<int64_t>(a.P) * D + static_cast<int64_t>(off >> 1) * D + 2 * (off & 1);
     // |y / s| <= 7.0000005: rint by the magic addition, no clamp needed
     const float r = s != 0.f ? __frcp_rn(s) : 0.f;
     const bool in_range = s != 0.f && div_rn_in_range(r, lam);
@@ -247,7 +250,7 @@ __global__ void __launch_bounds__(256) k8v4_write_kernel(const K8V4WriteArgs a) 
         quotients4(s, r, in_range, 4 * i, q);
         nib = int4x4(q);
       }
-      *reinterpret_cast<uint16_t*>(codes + elem(i) / 2) = static_cast<uint16_t>(nib);
+      *reinterpret_cast<uint16_t*>(codes + elem(i)) = static_cast<uint16_t>(nib);
     }
     if (rl == 0)
       *reinterpret_cast<float*>(chunk + static_cast<int64_t>(a.P) * D + static_cast<int64_t>(a.P) * (D / 2) +

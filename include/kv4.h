@@ -356,7 +356,9 @@ kv4_status kv4_decode_attention_static_ws(const void* q, const kv4_pool* pool,
  * site already established": the other 4-bit KV cache of the month stores
  * keys in FP8 and values in 4 bits and rotates both by one fixed FP32
  * Hadamard transform of size D).  KV4_K8V4 pools; chunk of P tokens =
- * [K codes P*D][V codes P*D/2][V scales FP32 * P], rows per token.
+ * [K codes P*D][V codes P*D/2][V scales FP32 * P]: K codes and V scales
+ * in rows per token, V codes in token-pair rows by 16-bit halves as in the
+ * INT4 pool.
  * Rotation H = S_D / sqrt(D) (Sylvester; symmetric, H H = I), evaluated on
  * the write path in FP32 as the fast Walsh-Hadamard transform (stages
  * len = 1, 2, ..., D/2, pairs (x_i, x_{i+len}) with bit len of i clear ->

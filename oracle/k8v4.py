@@ -22,7 +22,10 @@ layout and no value encoder; the readings here:
 * Values: INT4 per (token, head) row, s = amax / 7, code = clamp(rne(v_rot /
   s), -8, 7) (the INT4 format of ``quant.int4_quantize``).
 * Layout, one (page, kv head) chunk of P tokens:
-  [K codes P*D][V codes P*D/2][V scales FP32 * P], rows per token.
+  [K codes P*D][V codes P*D/2][V scales FP32 * P]; K codes and V scales in
+  rows per token, V codes in token-pair rows by 16-bit halves as in the
+  INT4 pool (word k of pair row p, D bytes, holds elements 4k .. 4k+3 of
+  token 2p in its low half and of token 2p+1 in its high half).
 * Decode: q is rotated too (q_rot = H q), so q_rot . k_rot = q . k before
   quantisation; the output is o = H (sum_t p_t v_hat_rot_t).  In float64.
 
@@ -76,6 +79,13 @@ def _chunk(pool, P, Hkv, D, page, head):
     return pool[off:off + chunk_bytes(P, D)]
 
 
+def _v_code_index(P, D, off):
+    """Chunk byte indices [D/2] of token off's packed V codes (byte 2k + j of
+    its packed row at 4k + 2 (off % 2) + j of pair row off // 2)."""
+    j = np.arange(D // 2)
+    return P * D + (off // 2) * D + 2 * (off % 2) + 4 * (j // 2) + (j % 2)
+
+
 def write(pool, P, Hkv, k_bf16, v_bf16, slot_mapping, s_k):
     """Rotate and quantise T tokens of bf16 K / V ([T, Hkv, D] bit patterns)
     into the pool at slot_mapping (int64 [T]; slots < 0 skipped)."""
@@ -92,7 +102,7 @@ def write(pool, P, Hkv, k_bf16, v_bf16, slot_mapping, s_k):
         for h in range(Hkv):
             c = _chunk(pool, P, Hkv, D, page, h)
             c[off * D:(off + 1) * D] = kc[t, h]
-            c[P * D + off * (D // 2):P * D + (off + 1) * (D // 2)] = vc[t, h]
+            c[_v_code_index(P, D, off)] = vc[t, h]
             c[P * D + P * (D // 2) + 4 * off:P * D + P * (D // 2) + 4 * off + 4] = \
                 np.asarray([vs[t, h]], np.float32).view(np.uint8)
     return pool
@@ -108,7 +118,7 @@ def read_rows(pool, P, Hkv, D, s_k, block_table_row, n, head):
         off = t % P
         c = _chunk(pool, P, Hkv, D, page, head)
         K[t] = e4m3_decode(c[off * D:(off + 1) * D]) * np.float64(np.float32(s_k))
-        code = _unpack_nibbles(c[P * D + off * (D // 2):P * D + (off + 1) * (D // 2)]).astype(np.int64)
+        code = _unpack_nibbles(c[_v_code_index(P, D, off)]).astype(np.int64)
         code = np.where(code >= 8, code - 16, code)
         s = c[P * D + P * (D // 2) + 4 * off:P * D + P * (D // 2) + 4 * off + 4].view(np.float32)[0]
         V[t] = code * np.float64(s)

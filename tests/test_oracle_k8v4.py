@@ -104,6 +104,9 @@ def test_write_stores_the_rotated_codes_in_their_rows():
     assert np.array_equal(c1[D:2 * D], Q.fp8_quantize(KV.fwht_f32(F.bf16_to_f32(k[0])), np.float32(0.05))[0])
     vc, vs = Q.int4_quantize(KV.fwht_f32(F.bf16_to_f32(v[2])))
     c0 = pool[:KV.chunk_bytes(P, D)]
-    assert np.array_equal(c0[P * D + 2 * (D // 2):P * D + 3 * (D // 2)], vc[0])
+    # slot 2: pair row 1 of the V codes, the even token's low 16-bit halves
+    pair = c0[P * D + 1 * D:P * D + 2 * D]
+    assert np.array_equal(pair.reshape(-1, 4)[:, :2].reshape(-1), vc[0])
+    assert np.all(pair.reshape(-1, 4)[:, 2:] == 0xEE)             # the odd token's halves untouched
     assert c0[P * D + P * (D // 2) + 8:P * D + P * (D // 2) + 12].view(np.float32)[0] == vs[0]
     assert np.all(c0[:2 * D] == 0xEE) and np.all(c1[:D] == 0xEE)   # untouched rows
