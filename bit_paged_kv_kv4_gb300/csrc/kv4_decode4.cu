@@ -34,14 +34,16 @@
 //    weight: w = p * s_V(t) / s_ref, s_ref the largest V scale seen so far
 //    (raised only when exceeded), and the piece's m_y = m_x + log2(s_ref)
 //    carries it to the merge and to the combine kernel.
-//  * O^T += V^T P^T with dequantised V^T as the A operand: NVFP4 V is stored
-//    in token pairs, so one hardware E2M1 conversion of a stored byte is one
-//    A-fragment register (two tokens of one dim), times the pair's scales.
+//  * O^T += V^T P^T with dequantised V^T as the A operand.  V is stored in
+//    token pairs: for NVFP4 one hardware E2M1 conversion of a stored byte is
+//    one A-fragment register (two tokens of one dim), times the pair's
+//    scales; for INT4 and k8v4 (pair rows by 16-bit halves) it is one
+//    mask-and-bias conversion of a stored word shifted by 0 or 8 bits.
 //
 // k8v4 (keys FP8 E4M3 of D bytes a token under one FP32 scale, values INT4
 // with a scale per token, both rotated by H = S_D / sqrt(D)) runs the same
 // loop: its K box is a 4-D copy of the tile's key rows as lines of at most
-// 128 bytes, its V box a 3-D copy of the value rows and its 16 V scales one
+// 128 bytes, its V box a 3-D copy of the value pair rows and its 16 V scales one
 // 64-byte bulk copy, in two ring stages per warp (a stage is half as large
 // again).  The unit's queries are rotated at the segment's start (FP32
 // butterflies; the 1/sqrt(D) joins qk_scale) and kept as f16 hi + lo
